@@ -1,0 +1,155 @@
+"""Seeded synthetic inputs shaped like the pages' workloads.
+
+This module only draws random tensors and routes tokens; it holds none of the
+quantization, transform or GEMM arithmetic, so both the CUDA path's tests and
+the CPU oracle can take their inputs from it.
+
+BF16 tensors are returned as numpy ``uint16`` bit patterns (the FP32 draws are
+rounded to BF16 by round-to-nearest-even through ``torch``'s conversion).
+
+Workloads (stand-ins for the pages' models; no dataset or weight is needed
+because the bytes moved depend only on shapes and value distributions):
+
+* ``tiny``        -- activation 256x1024 ~ N(0,1) with 0.5% outliers x50, one
+                     all-zero 32-block (row 0, cols 0..31) and one
+                     subnormal-only block (row 1, cols 0..31); weight
+                     512x1024 ~ N(0, 0.02); seed 0.
+* ``dense_mlp``   -- Qwen3-8B-shaped MLP linear: X 8192x4096 Student-t(3),
+                     W 12288x4096 N(0, 0.02), dY 8192x12288 N(0, 1e-3);
+                     seeds 1, 2, 3.
+* ``moe``         -- Qwen3-30B-A3B expert layer: X 8192x2048 Student-t(3) and
+                     a uniform top-8-of-128 router (seed 4), giving 65536
+                     expert-sorted rows; a 65536x768 down-projection input;
+                     128 experts x (gate 768x2048, up 768x2048, down 2048x768)
+                     N(0, 0.02) (seed 5).
+* ``wgrad``       -- Llama-3-8B-shaped WGRAD inputs: X 32768x4096
+                     Student-t(3) (seed 6), dY 32768x14336 N(0, 1e-3) (seed 7);
+                     RHT seed 8, SR seed 9.
+* ``weight_sync`` -- per layer l (48 layers): 128 experts x {2048x768,
+                     768x2048, 768x2048} N(0, 0.02), seed 1000 + l.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+
+def to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """FP32 array -> BF16 bit patterns (round to nearest even)."""
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def normal(rng: np.random.Generator, shape, std: float) -> np.ndarray:
+    return to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(std))
+
+
+def student_t(rng: np.random.Generator, shape, nu: float = 3.0, scale: float = 1.0) -> np.ndarray:
+    return to_bf16_bits((rng.standard_t(nu, size=shape) * scale).astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# tiny
+# ---------------------------------------------------------------------------
+
+def tiny(seed: int = 0, rows: int = 256, cols: int = 1024, out_features: int = 512):
+    """Returns dict(x, w) of BF16 bits."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((rows, cols), dtype=np.float32)
+    n_out = int(round(0.005 * rows * cols))
+    idx = rng.choice(rows * cols, size=n_out, replace=False)
+    x.reshape(-1)[idx] *= np.float32(50.0)
+    xb = to_bf16_bits(x)
+    # one all-zero 32-block: row 0, cols 0..31
+    xb[0, 0:32] = 0
+    # one subnormal-only block: row 1, cols 0..31, values +-k * 2^-133, k in 1..127
+    if rows > 1:
+        k = rng.integers(1, 128, size=32).astype(np.uint16)      # BF16 subnormal mantissa
+        sign = (rng.integers(0, 2, size=32).astype(np.uint16) << 15)
+        xb[1, 0:32] = sign | k
+    w = normal(rng, (out_features, cols), 0.02)
+    return {"x": xb, "w": w}
+
+
+# ---------------------------------------------------------------------------
+# dense_mlp
+# ---------------------------------------------------------------------------
+
+def dense_mlp(tokens: int = 8192, hidden: int = 4096, ffn: int = 12288):
+    x = student_t(np.random.default_rng(1), (tokens, hidden))
+    w = normal(np.random.default_rng(2), (ffn, hidden), 0.02)
+    dy = normal(np.random.default_rng(3), (tokens, ffn), 1e-3)
+    return {"x": x, "w": w, "dy": dy}
+
+
+# ---------------------------------------------------------------------------
+# moe
+# ---------------------------------------------------------------------------
+
+def route_uniform_topk(rng: np.random.Generator, tokens: int, experts: int, topk: int):
+    """Uniform router: each token's experts are the first ``topk`` entries of
+    a seeded Fisher-Yates permutation of 0..experts-1.  Rows are then sorted
+    stably by (expert, token).  Returns (row_token [tokens*topk] int64,
+    group_offsets [experts+1] int64)."""
+    choice = np.empty((tokens, topk), dtype=np.int64)
+    for t in range(tokens):
+        perm = np.arange(experts, dtype=np.int64)
+        u = rng.random(experts - 1)
+        for i in range(experts - 1, 0, -1):       # Fisher-Yates, back to front
+            j = int(u[experts - 1 - i] * (i + 1))
+            perm[i], perm[j] = perm[j], perm[i]
+        choice[t] = perm[:topk]
+    expert_of_row = choice.reshape(-1)
+    token_of_row = np.repeat(np.arange(tokens, dtype=np.int64), topk)
+    order = np.lexsort((token_of_row, expert_of_row))   # primary: expert, then token
+    counts = np.bincount(expert_of_row, minlength=experts)
+    offsets = np.zeros(experts + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    return token_of_row[order], offsets
+
+
+def moe(tokens: int = 8192, hidden: int = 2048, ffn: int = 768, experts: int = 128, topk: int = 8,
+        with_weights: bool = True):
+    rng = np.random.default_rng(4)
+    x = student_t(rng, (tokens, hidden))
+    row_token, offsets = route_uniform_topk(rng, tokens, experts, topk)
+    down_in = student_t(rng, (tokens * topk, ffn))
+    out = {"x": x, "row_token": row_token, "group_offsets": offsets, "down_in": down_in}
+    if with_weights:
+        wr = np.random.default_rng(5)
+        out["w_gate_up"] = normal(wr, (experts, 2 * ffn, hidden), 0.02)   # gate rows then up rows
+        out["w_down"] = normal(wr, (experts, hidden, ffn), 0.02)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# wgrad
+# ---------------------------------------------------------------------------
+
+def wgrad(tokens: int = 32768, hidden: int = 4096, ffn: int = 14336):
+    x = student_t(np.random.default_rng(6), (tokens, hidden))
+    dy = normal(np.random.default_rng(7), (tokens, ffn), 1e-3)
+    return {"x": x, "dy": dy, "rht_seed": 8, "sr_seed": 9}
+
+
+# ---------------------------------------------------------------------------
+# weight_sync
+# ---------------------------------------------------------------------------
+
+def weight_sync_layer(layer: int, experts: int = 128, hidden: int = 2048, ffn: int = 768):
+    rng = np.random.default_rng(1000 + layer)
+    return {
+        "down": normal(rng, (experts, hidden, ffn), 0.02),
+        "gate": normal(rng, (experts, ffn, hidden), 0.02),
+        "up": normal(rng, (experts, ffn, hidden), 0.02),
+    }
+
+
+def random_bf16(seed: int, shape, kind: str = "normal", scale: float = 1.0) -> np.ndarray:
+    """Small helper for parity cases of arbitrary shape."""
+    rng = np.random.default_rng(seed)
+    if kind == "normal":
+        return normal(rng, shape, scale)
+    if kind == "student_t":
+        return student_t(rng, shape, 3.0, scale)
+    raise ValueError(kind)
