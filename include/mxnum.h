@@ -1,0 +1,195 @@
+/*
+ * mxnum.h -- C ABI of libmxnum.so: block-scaled microscaling numerics on GB300 (sm_103a).
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless stated otherwise; the caller owns every buffer and the
+ *     stream.  The library allocates nothing.
+ *   - Calls validate their arguments on the host and then enqueue work asynchronously on `stream`.
+ *     A non-MX_OK return means nothing was enqueued (MX_ERR_CUDA: a launch failed; the CUDA error
+ *     is left for the caller to query).  Outputs are valid once the stream reaches the call.
+ *   - BF16 tensors are row-major 16-bit words.  Codes are row-major bytes: MXFP8 one E4M3 byte per
+ *     element; NVFP4 two E2M1 codes per byte, the even-indexed element in the low nibble.
+ *   - Every quantized operand keeps its blocks contiguous along the consuming GEMM's K dimension,
+ *     so column-wise copies are stored transposed.
+ *   - Scale bytes (E8M0 for MXFP8, E4M3 for NVFP4) are written in the block-scaled GEMM's layout:
+ *     512-byte tiles of 128 rows x 4 scale columns in row-major tile order; inside a tile the scale
+ *     of (row r, scale column c) sits at (r % 32) * 16 + ((r / 32) % 4) * 4 + (c % 4).  Rows are
+ *     padded to a multiple of 128 and scale columns to a multiple of 4; the quantizers write zeros
+ *     into the padding.  mx_scale_bytes() gives the size.
+ *   - Pointers to codes, scales, BF16 tensors and workspaces must be 16-byte aligned
+ *     (MX_ERR_ALIGNMENT otherwise); leading dimensions are in elements and must keep rows 16-byte
+ *     aligned.
+ *
+ * Sources (web pages): "Miles Blackwell RL ... MXFP8 e NVFP4 Nativos" (remio.ai); "NVFP4 RL
+ * training" (socker-news); "End-to-End MXFP8 Reinforcement Learning on Blackwell"
+ * (thelatestinai.com 2610.34915); "Train models faster with JAX and MaxText using NVFP4 on NVIDIA
+ * Blackwell" (developer.nvidia.cn).  Each declaration names the passage that defines it.
+ */
+#ifndef MXNUM_H
+#define MXNUM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MX_OK = 0,
+    MX_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad enum value              */
+    MX_ERR_ALIGNMENT = 2,     /* a pointer or leading dimension breaks 16-byte alignment       */
+    MX_ERR_UNSUPPORTED = 3,   /* a size is not a multiple of the block or tile it needs        */
+    MX_ERR_CUDA = 4,          /* a CUDA launch or runtime call failed                          */
+    MX_ERR_TIMEOUT = 5        /* a device-side bounded wait gave up (see mx_check_device_status) */
+} mx_status;
+
+typedef enum { MX_FMT_MXFP8 = 0, MX_FMT_NVFP4 = 1 } mx_format;
+typedef enum { MX_ROUND_RNE = 0, MX_ROUND_SR = 1 } mx_round;
+/* Scope of an FP32 second-level scale / GEMM epilogue factor. */
+typedef enum { MX_SCOPE_NONE = 0, MX_SCOPE_TENSOR = 1, MX_SCOPE_ROW = 2 } mx_scope;
+
+/* Human-readable name of a status code (static storage). */
+const char* mx_status_string(mx_status s);
+
+/* Bytes of a scale tensor in the GEMM layout for `rows` rows whose K extent is `k` elements with
+ * one scale per `block` elements (32 for MXFP8, 16 for NVFP4): ceil(rows/128) * ceil(k/block/4) * 512. */
+int64_t mx_scale_bytes(int64_t rows, int64_t k, int block);
+
+/* MXFP8 quantize, row-wise and/or column-wise in one pass over x.
+ * Source: Miles page -- MXFP8 = blocks of 32 E4M3 values sharing one E8M0 scale; TransformerEngine
+ * makes row-wise and column-wise copies from the high-precision input, never re-quantizing FP8
+ * (section "Um Quantizador Compartilhado"); E2E page Table 10 F6 (E8M0 keeps only the exponent).
+ * Per block: e = clamp(floor(log2 amax) - 8, -127, 127) (amax = 0 -> -127), scale byte = e + 127,
+ * code = E4M3 round-to-nearest-even, saturating, of x * 2^-e.
+ *   x      [rows, ldx] BF16 (ldx >= cols)
+ *   q_row  [rows, cols] E4M3, s_row mx_scale_bytes(rows, cols, 32)   -- blocks along cols (NULL: skip)
+ *   q_col  [cols, rows] E4M3, s_col mx_scale_bytes(cols, rows, 32)   -- blocks along rows, stored
+ *          transposed (NULL: skip).  At least one of the two outputs must be given.
+ * Requires cols % 32 == 0 for row-wise, rows % 32 == 0 for column-wise, cols % 8 == 0. */
+mx_status mx_quantize_mxfp8(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                            uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                            cudaStream_t stream);
+
+/* NVFP4 1x16 quantize with a per-token FP32 second-level scale, fused in one kernel.
+ * Source: Miles page -- NVFP4 = E2M1 values, one E4M3 scale per 16, a second FP32 scale computed
+ * separately for each token, online, fused into the activation quantizer that emits packed FP4,
+ * block scales and token scales together; NVFP4 RL page, "Baseline recipe details".
+ * Per token t: S_t = amax_t / 2688; per 16-block: bs = E4M3(amax_b / 6 / S_t) (S_t = 0 -> 0);
+ * r = 1 / (bs * S_t) (0 if bs * S_t = 0, clamped to FLT_MAX); code = E2M1 RNE saturating of x * r;
+ * every operation FP32 round-to-nearest in that order.
+ *   x [T, ldx] BF16;  q [T, H/2];  s mx_scale_bytes(T, H, 16);  s_tok [T] FP32.
+ * Requires H % 16 == 0. */
+mx_status mx_nvfp4_quantize_per_token(const void* x, int64_t T, int64_t H, int64_t ldx,
+                                      uint8_t* q, uint8_t* s, float* s_tok, cudaStream_t stream);
+
+/* NVFP4 16x16 2D weight quantize, both orientations, for G stacked matrices.
+ * Source: MaxText page, "NVFP4 pretraining recipe" -- one FP8 scale per 16x16 weight block so that
+ * FPROP and its transpose DGRAD see identical values, under a per-tensor FP32 scale; Miles page --
+ * SwiGLU gate and up are quantized together (stack them into one matrix to share the scale).
+ * Per matrix g: S_w = amax / 2688; per 16x16 tile: bs as above with the tile amax; codes as above.
+ *   w      [G, O, H] BF16 (contiguous)
+ *   q_row  [G, O, H/2];  s_row G * mx_scale_bytes(O, H, 16)   (tile scale on each of its 16 rows)
+ *   q_col  [G, H, O/2];  s_col G * mx_scale_bytes(H, O, 16)   (the same codes, transposed)
+ *   s_w    [G] FP32
+ *   workspace: mx_workspace_bytes(MX_WS_WEIGHT_2D, G, 0) bytes, 16-byte aligned, caller-owned.
+ * Requires O % 16 == 0 and H % 16 == 0. */
+mx_status mx_nvfp4_quantize_weight_2d(const void* w, int64_t G, int64_t O, int64_t H,
+                                      uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                      float* s_w, void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream);
+
+/* 16-point random Hadamard transform along the token dimension.
+ * Source: MaxText page, "NVFP4 pretraining recipe" -- a random Hadamard transform on the WGRAD
+ * inputs only, to Gaussianize outliers before 4-bit quantization.
+ * For every column n and aligned 16-token chunk: v = d * x (signs d_j = bit j of word 0 of
+ * Philox4x32-10(key = seed, ctr = (0,0,1,0)), set bit = -1); Walsh-Hadamard butterflies with
+ * strides 1, 2, 4, 8 in FP32; y = BF16 RNE of v / 4.  Use the same seed for both WGRAD operands.
+ *   x, y [T, N] BF16 (may not alias).  Requires T % 16 == 0 and N % 8 == 0. */
+mx_status mx_rht16(const void* x, int64_t T, int64_t N, uint64_t seed, void* y, cudaStream_t stream);
+
+/* NVFP4 1x16 quantize with a per-tensor FP32 second-level scale; column-wise (blocks of 16 along
+ * the token dim T, output transposed) or row-wise; optional RHT first; RNE or stochastic rounding.
+ * Source: MaxText page, "NVFP4 pretraining recipe" -- 1x16 scaling for activations and gradients,
+ * per-tensor FP32 scale, RHT on WGRAD inputs, SR on gradients (RNE on weights and activations).
+ * Pass 1: A = amax of the (transformed, BF16-rounded) tensor; S = A / 2688.  Pass 2: per block as in
+ * mx_nvfp4_quantize_per_token with S.  SR: the 16 random bits of logical element i = t * N + n are
+ * bits [16*(i&1), 16*(i&1)+16) of word (i>>1)&3 of Philox4x32-10(key = sr_seed,
+ * ctr = (i>>3 low, i>>3 high, 0, 0)); with a = |x*r| < 6 between grid points lo < hi, the code
+ * rounds up iff (a - lo)/(hi - lo) > bits * 2^-16.
+ *   x [T, N] BF16
+ *   colwise = 1: q [N, T/2], s mx_scale_bytes(N, T, 16); requires T % 16 == 0, N % 8 == 0
+ *   colwise = 0: q [T, N/2], s mx_scale_bytes(T, N, 16); requires N % 16 == 0; rht must be 0
+ *   s_tensor: one FP32 (written);  workspace: mx_workspace_bytes(MX_WS_1X16, 0, 0) bytes. */
+mx_status mx_nvfp4_quantize_1x16(const void* x, int64_t T, int64_t N, int colwise, int rht,
+                                 uint64_t rht_seed, mx_round rnd, uint64_t sr_seed,
+                                 uint8_t* q, uint8_t* s, float* s_tensor,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Dequantize codes + scales to BF16 (the "dequantized backward" operand DQ(Q(w))).
+ * Source: NVFP4 RL page, "dequantized backward" -- y = x * DQ(Q(w_bf16)) rebuilds BF16 operands
+ * from the exact low-precision forward values; Miles page (high-precision vs dequantized backward).
+ *   MXFP8: y = BF16 RNE of val(q) * 2^(s - 127);  q [rows, cols]; s mx_scale_bytes(rows, cols, 32);
+ *          s2 ignored.
+ *   NVFP4: y = BF16 RNE of fp32(val(q) * val(bs)) * S; q [rows, cols/2]; s mx_scale_bytes(rows, cols,
+ *          16); S = s2[row] (MX_SCOPE_ROW) or s2[0] (MX_SCOPE_TENSOR).
+ *   y [rows, cols] BF16.  Requires cols % 32 (MXFP8) or cols % 16 (NVFP4) == 0. */
+mx_status mx_dequantize_bf16(mx_format fmt, const uint8_t* q, const uint8_t* s, const float* s2,
+                             mx_scope s2_scope, int64_t rows, int64_t cols, void* y,
+                             cudaStream_t stream);
+
+/* Block-scaled GEMM on the 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA operand
+ * staging):  D[m, n] = BF16( alpha_a[m or 0] * alpha_b[n or 0] * sum_k DQ(A)[m, k] * DQ(B)[n, k] ).
+ * Source: Miles page -- MXFP8 forward, weight-gradient and data-gradient GEMMs; MaxText page -- the
+ * FPROP, DGRAD and WGRAD GEMMs take NVFP4 inputs and emit BF16; E2E page Table 6 (GEMM time).
+ * FPROP: A = X row-wise, B = W row-wise.  DGRAD: A = dY row-wise, B = W column-wise.  WGRAD:
+ * A = dY column-wise, B = X column-wise.
+ *   fmt MX_FMT_MXFP8: a [M, K], b [N, K] E4M3; sa mx_scale_bytes(M, K, 32), sb (N, K, 32).
+ *   fmt MX_FMT_NVFP4: a [M, K/2], b [N, K/2] E2M1; sa mx_scale_bytes(M, K, 16), sb (N, K, 16).
+ *   alpha_a: NULL / MX_SCOPE_NONE (1), one FP32 (MX_SCOPE_TENSOR) or M FP32 (MX_SCOPE_ROW); alpha_b
+ *   likewise with N.  d [M, ldd] BF16.
+ * FP32 accumulation inside the tensor core; the summation order is the hardware's.  Requires
+ * K % 128 (MXFP8) or K % 256 (NVFP4) == 0; M, N >= 1; ldd % 8 == 0. */
+mx_status mx_scaled_gemm(mx_format fmt,
+                         const uint8_t* a, const uint8_t* sa, const float* alpha_a, mx_scope alpha_a_scope,
+                         const uint8_t* b, const uint8_t* sb, const float* alpha_b, mx_scope alpha_b_scope,
+                         int64_t M, int64_t N, int64_t K, void* d, int64_t ldd, cudaStream_t stream);
+
+/* Grouped block-scaled GEMM over expert-sorted rows: for every group g,
+ *   D[rows of g] = BF16( alpha_a[row] * alpha_b[g] * A[rows of g] . B_g^T ).
+ * Source: Miles page -- NVFP4 on the routed experts' weights and activations with a per-token
+ * scale; E2E page Table 2 (Qwen3-30B-A3B: 128 experts, top-8).
+ *   group_offsets: DEVICE int64 [G + 1], nondecreasing, offsets[0] = 0, offsets[G] = total_rows.
+ *   a [total_rows, K(/2)], sa mx_scale_bytes(total_rows, K, block) (rows in expert-sorted order),
+ *   alpha_a_rows [total_rows] FP32 or NULL;  b [G, N, K(/2)], sb G * mx_scale_bytes(N, K, block),
+ *   alpha_b_groups [G] FP32 or NULL;  d [total_rows, N] BF16.
+ * Same K and alignment rules as mx_scaled_gemm. */
+mx_status mx_grouped_scaled_gemm(mx_format fmt, int64_t G, const int64_t* group_offsets,
+                                 int64_t total_rows,
+                                 const uint8_t* a, const uint8_t* sa, const float* alpha_a_rows,
+                                 const uint8_t* b, const uint8_t* sb, const float* alpha_b_groups,
+                                 int64_t N, int64_t K, void* d, cudaStream_t stream);
+
+/* Count differing bytes between x and y (the offline byte comparison of synchronized weights).
+ * Source: E2E page abstract ("synchronized weights ... equal the learner's FP8 forward weights byte
+ * for byte") and Table 11 (byte comparison check).
+ * Adds the number of positions i < nbytes with x[i] != y[i] to *count (a DEVICE uint64 that the
+ * caller zeroes).  x and y 16-byte aligned. */
+mx_status mx_count_mismatch(const uint8_t* x, const uint8_t* y, int64_t nbytes,
+                            unsigned long long* count, cudaStream_t stream);
+
+/* Workspace sizes (bytes) for the ops that take one. */
+typedef enum { MX_WS_WEIGHT_2D = 0, MX_WS_1X16 = 1 } mx_workspace_op;
+size_t mx_workspace_bytes(mx_workspace_op op, int64_t groups, int64_t unused);
+
+/* Synchronizes the device, then reports and clears the device-side watchdog word that bounded
+ * waits inside the GEMM kernels set when they give up (MX_ERR_TIMEOUT), or MX_ERR_CUDA if the
+ * device reports an error.  Host-side; for tests and health checks. */
+mx_status mx_check_device_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXNUM_H */

@@ -1,0 +1,205 @@
+"""Python binding of libmxnum.so (block-scaled microscaling numerics on GB300, sm_103a).
+
+Argument marshalling only: every function passes ``tensor.data_ptr()`` values, sizes, seeds and the
+current CUDA stream to the C ABI declared in ``include/mxnum.h`` and raises ``MXError`` on a non-OK
+status.  No arithmetic happens here and there is no CPU fallback: if the CUDA library is missing or
+a tensor is not on a CUDA device, the call raises.  ``alloc_*`` helpers only create output tensors
+of the right sizes (``torch.empty`` on the input's device).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmxnum.so")
+
+MX_FMT_MXFP8, MX_FMT_NVFP4 = 0, 1
+MX_ROUND_RNE, MX_ROUND_SR = 0, 1
+MX_SCOPE_NONE, MX_SCOPE_TENSOR, MX_SCOPE_ROW = 0, 1, 2
+MX_WS_WEIGHT_2D, MX_WS_1X16 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MXError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} failed: {text} ({status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmxnum.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I64, U64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_size_t
+            sigs = {
+                "mx_status_string": (ctypes.c_char_p, [I32]),
+                "mx_scale_bytes": (I64, [I64, I64, I32]),
+                "mx_workspace_bytes": (SZ, [I32, I64, I64]),
+                "mx_quantize_mxfp8": (I32, [P, I64, I64, I64, P, P, P, P, P]),
+                "mx_nvfp4_quantize_per_token": (I32, [P, I64, I64, I64, P, P, P, P]),
+                "mx_nvfp4_quantize_weight_2d": (I32, [P, I64, I64, I64, P, P, P, P, P, P, SZ, P]),
+                "mx_rht16": (I32, [P, I64, I64, U64, P, P]),
+                "mx_nvfp4_quantize_1x16": (I32, [P, I64, I64, I32, I32, U64, I32, U64, P, P, P, P, SZ, P]),
+                "mx_dequantize_bf16": (I32, [I32, P, P, P, I32, I64, I64, P, P]),
+                "mx_scaled_gemm": (I32, [I32, P, P, P, I32, P, P, P, I32, I64, I64, I64, P, I64, P]),
+                "mx_grouped_scaled_gemm": (I32, [I32, I64, P, I64, P, P, P, P, P, P, I64, I64, P, P]),
+                "mx_count_mismatch": (I32, [P, P, I64, P, P]),
+                "mx_check_device_status": (I32, []),
+            }
+            for name, (res, args) in sigs.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise MXError(fn, status, lib().mx_status_string(status).decode())
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("mxnum operates on CUDA tensors only (no CPU path)")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _bf16_bits(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError("BF16 input expected (bfloat16 or its 16-bit bit pattern)")
+    return t
+
+
+def scale_bytes(rows: int, k: int, block: int) -> int:
+    return int(lib().mx_scale_bytes(rows, k, block))
+
+
+def workspace_bytes(op: int, groups: int = 0) -> int:
+    return int(lib().mx_workspace_bytes(op, groups, 0))
+
+
+def check_device_status() -> None:
+    _check("mx_check_device_status", lib().mx_check_device_status())
+
+
+# ------------------------------------------------------------------------------------------------
+# quantizers
+# ------------------------------------------------------------------------------------------------
+
+def mx_quantize_mxfp8(x, q_row=None, s_row=None, q_col=None, s_col=None, stream=None):
+    x = _bf16_bits(x)
+    rows, cols = x.shape
+    _check("mx_quantize_mxfp8", lib().mx_quantize_mxfp8(
+        _p(x), rows, cols, x.stride(0), _p(q_row), _p(s_row), _p(q_col), _p(s_col), _stream(stream)))
+
+
+def mx_nvfp4_quantize_per_token(x, q, s, s_tok, stream=None):
+    x = _bf16_bits(x)
+    T, H = x.shape
+    _check("mx_nvfp4_quantize_per_token", lib().mx_nvfp4_quantize_per_token(
+        _p(x), T, H, x.stride(0), _p(q), _p(s), _p(s_tok), _stream(stream)))
+
+
+def mx_nvfp4_quantize_weight_2d(w, q_row, s_row, q_col, s_col, s_w, workspace, stream=None):
+    w = _bf16_bits(w)
+    G, O, H = w.shape
+    _check("mx_nvfp4_quantize_weight_2d", lib().mx_nvfp4_quantize_weight_2d(
+        _p(w), G, O, H, _p(q_row), _p(s_row), _p(q_col), _p(s_col), _p(s_w), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mx_rht16(x, seed: int, y, stream=None):
+    x = _bf16_bits(x)
+    T, N = x.shape
+    _check("mx_rht16", lib().mx_rht16(_p(x), T, N, seed, _p(y), _stream(stream)))
+
+
+def mx_nvfp4_quantize_1x16(x, colwise: bool, rht: bool, rht_seed: int, sr: bool, sr_seed: int, q, s, s_tensor,
+                           workspace, stream=None):
+    x = _bf16_bits(x)
+    T, N = x.shape
+    _check("mx_nvfp4_quantize_1x16", lib().mx_nvfp4_quantize_1x16(
+        _p(x), T, N, int(colwise), int(rht), rht_seed, MX_ROUND_SR if sr else MX_ROUND_RNE, sr_seed,
+        _p(q), _p(s), _p(s_tensor), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mx_dequantize_bf16(fmt: int, q, s, s2, s2_scope: int, rows: int, cols: int, y, stream=None):
+    _check("mx_dequantize_bf16", lib().mx_dequantize_bf16(
+        fmt, _p(q), _p(s), _p(s2), s2_scope, rows, cols, _p(y), _stream(stream)))
+
+
+def mx_scaled_gemm(fmt: int, a, sa, alpha_a, alpha_a_scope: int, b, sb, alpha_b, alpha_b_scope: int,
+                   M: int, N: int, K: int, d, stream=None):
+    _check("mx_scaled_gemm", lib().mx_scaled_gemm(
+        fmt, _p(a), _p(sa), _p(alpha_a), alpha_a_scope, _p(b), _p(sb), _p(alpha_b), alpha_b_scope,
+        M, N, K, _p(d), d.stride(0), _stream(stream)))
+
+
+def mx_grouped_scaled_gemm(fmt: int, group_offsets, a, sa, alpha_a_rows, b, sb, alpha_b_groups, N: int, K: int, d,
+                           stream=None):
+    G = group_offsets.numel() - 1
+    _check("mx_grouped_scaled_gemm", lib().mx_grouped_scaled_gemm(
+        fmt, G, _p(group_offsets), a.shape[0], _p(a), _p(sa), _p(alpha_a_rows), _p(b), _p(sb), _p(alpha_b_groups),
+        N, K, _p(d), _stream(stream)))
+
+
+def mx_count_mismatch(x, y, count, stream=None):
+    n = x.numel() * x.element_size()
+    if y.numel() * y.element_size() != n:
+        raise ValueError("byte sizes differ")
+    _check("mx_count_mismatch", lib().mx_count_mismatch(_p(x), _p(y), n, _p(count), _stream(stream)))
+
+
+# ------------------------------------------------------------------------------------------------
+# output allocation helpers (torch.empty only)
+# ------------------------------------------------------------------------------------------------
+
+def _u8(n: int, device) -> torch.Tensor:
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def alloc_mxfp8(rows: int, cols: int, device, rowwise: bool = True, colwise: bool = True):
+    out = {}
+    if rowwise:
+        out["q_row"] = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+        out["s_row"] = _u8(scale_bytes(rows, cols, 32), device)
+    if colwise:
+        out["q_col"] = torch.empty((cols, rows), dtype=torch.uint8, device=device)
+        out["s_col"] = _u8(scale_bytes(cols, rows, 32), device)
+    return out
+
+
+def alloc_nvfp4_rows(rows: int, k: int, device):
+    """Codes [rows, k/2], GEMM-layout scales and one FP32 second-level scale per row."""
+    return {"q": torch.empty((rows, k // 2), dtype=torch.uint8, device=device),
+            "s": _u8(scale_bytes(rows, k, 16), device),
+            "s2": torch.empty(rows, dtype=torch.float32, device=device)}
+
+
+def alloc_nvfp4_weight_2d(G: int, O: int, H: int, device):
+    return {"q_row": torch.empty((G, O, H // 2), dtype=torch.uint8, device=device),
+            "s_row": _u8(G * scale_bytes(O, H, 16), device),
+            "q_col": torch.empty((G, H, O // 2), dtype=torch.uint8, device=device),
+            "s_col": _u8(G * scale_bytes(H, O, 16), device),
+            "s_w": torch.empty(G, dtype=torch.float32, device=device),
+            "ws": _u8(max(16, workspace_bytes(MX_WS_WEIGHT_2D, G)), device)}

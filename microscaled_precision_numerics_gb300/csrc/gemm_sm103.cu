@@ -1,0 +1,537 @@
+// gemm_sm103.cu -- block-scaled GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+//   D[m, n] = BF16( alpha_a[m] * alpha_b[n] * sum_k DQ(A)[m, k] * DQ(B)[n, k] )
+//
+// Miles page: MXFP8 forward, weight-gradient and data-gradient GEMMs; MaxText page: the three MLP
+// GEMMs take NVFP4 inputs and emit BF16; E2E page Table 6: GEMM time per micro-batch.  MXFP8 uses
+// tcgen05.mma kind::mxf8f6f4 with one E8M0 scale per 32 (scale_vec::1X); NVFP4 uses kind::mxf4nvf4
+// with one E4M3 scale per 16 (scale_vec::4X); the FP32 second-level scales are applied in the
+// epilogue.
+//
+// Structure (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0        TMA producer: A/B tiles (128-byte swizzle) and scale atoms into a 4-stage ring
+//   warp 1        TMEM allocator; lane 0 issues tcgen05.cp (scales -> TMEM) and tcgen05.mma
+//   warps 2..5    epilogue: tcgen05.ld the FP32 accumulator, scale, round to BF16, store
+// Scales arrive in the GEMM layout (512-byte atoms of 128 rows x 4 scale columns); one atom is
+// copied to TMEM with tcgen05.cp.32x128b.warpx4.  For the grouped GEMM the A-side atoms of a tile
+// that starts at an arbitrary row are gathered word by word by the producer warp.
+// Every mbarrier wait is bounded: on expiry the CTA records MX_ERR_TIMEOUT in a device word, stops
+// issuing work, drains what it issued and frees its TMEM.
+#include "mx_internal.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+namespace mxk {
+
+__device__ unsigned int g_mx_device_status = 0;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BKB = 128;                  // K bytes per pipeline stage
+constexpr int STAGES = 4;
+constexpr int NUM_THREADS = 192;
+constexpr int A_STAGE_BYTES = BM * BKB;   // 16 KB
+constexpr int B_STAGE_BYTES = BN * BKB;   // 32 KB
+constexpr int TMEM_COLS = 512;
+constexpr int TMEM_SF_BASE = 256;         // accumulator uses columns [0, 256)
+constexpr int MAX_GROUPS = 1024;
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
+
+template <int FMT>
+struct Cfg {
+    static constexpr int SF_ATOMS_A = FMT == 0 ? 1 : 4;   // 512-byte atoms per stage (A side)
+    static constexpr int SFA_BYTES = 512 * SF_ATOMS_A;
+    static constexpr int SFB_BYTES = 2 * SFA_BYTES;        // two 128-row halves of the 256-row B tile
+    static constexpr int SFA_COLS = 4 * SF_ATOMS_A;        // TMEM columns per stage
+    static constexpr int SFB_COLS = 2 * SFA_COLS;
+    static constexpr int SMEM_A = 0;
+    static constexpr int SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
+    static constexpr int SMEM_SFA = SMEM_B + STAGES * B_STAGE_BYTES;
+    static constexpr int SMEM_SFB = SMEM_SFA + STAGES * SFA_BYTES;
+    static constexpr int SMEM_BAR = SMEM_SFB + STAGES * SFB_BYTES;
+    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * STAGES + 4);
+    static constexpr int SMEM_PREFIX = SMEM_MISC + 16;
+    static constexpr int SMEM_TOTAL = SMEM_PREFIX + 4 * (MAX_GROUPS + 1);
+    static constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;  // slack for 1024-byte alignment
+    static_assert(TMEM_SF_BASE + STAGES * (SFA_COLS + SFB_COLS) <= TMEM_COLS, "TMEM budget");
+};
+
+struct Params {
+    const uint8_t* sa; const uint8_t* sb;
+    const float* alpha_a; int alpha_a_scope;
+    const float* alpha_b; int alpha_b_scope;
+    int64_t M, N, K;
+    uint16_t* d; int64_t ldd;
+    int64_t G; const int64_t* group_offsets;
+    int64_t m_tiles, n_tiles, k_stages;
+    int64_t nct;            // 4-column scale tiles per row band (same for A and B: same K)
+    int64_t sb_group_bytes; // grouped: scale bytes per expert matrix
+    int64_t total_tiles;    // dense
+};
+
+// ---------------------------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: false when the wait expired or another role of this CTA aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    uint32_t it = 0;
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++it & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+                atomicOr(&g_mx_device_status, 1u);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1, uint32_t bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 :: "r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+}
+
+template <int FMT>
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t acc) {
+    if (FMT == 0) {
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+                     :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
+    } else {
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+                     :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
+    }
+}
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 bytes, 8-row groups
+// 1024 bytes apart (stride byte offset), descriptor version 1 (bits 46..48), swizzle mode 2.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Descriptor of one 512-byte scale atom (32 rows x 16 bytes, contiguous, no swizzle).
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
+           ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor for the block-scaled kinds: B scale id (bits 4-5), A/B formats (7-9,
+// 10-12), K-major A and B, N >> 3 (17-22), scale type (23: 1 = UE8M0, 0 = UE4M3), M >> 4 (24-28),
+// A scale id (29-30).
+template <int FMT>
+__device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
+    const uint32_t fmt = FMT == 0 ? 0u : 1u;          // E4M3 (mxf8f6f4) / E2M1 (mxf4nvf4)
+    const uint32_t scale_type = FMT == 0 ? 1u : 0u;
+    return (sf_id << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(BN >> 3) << 17) | (scale_type << 23) |
+           ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Tile schedule (identical in every role)
+// ---------------------------------------------------------------------------------------------
+struct Tile {
+    int64_t row0, row_end;   // A rows [row0, row0 + 128) of which [row0, row_end) are real
+    int64_t n0;              // first output column
+    int64_t g;               // group (grouped GEMM) or 0
+};
+
+// Dense: bands of 16 M-tiles; inside a band N-tiles advance every 16 tiles (L2 reuse of A and B).
+__device__ __forceinline__ Tile dense_tile(const Params& p, int64_t t) {
+    constexpr int64_t GM = 16;
+    const int64_t band_tiles = GM * p.n_tiles;
+    const int64_t band = t / band_tiles, in = t % band_tiles;
+    const int64_t band_m = min64(GM, p.m_tiles - band * GM);
+    const int64_t mt = band * GM + in % band_m, nt = in / band_m;
+    Tile r;
+    r.row0 = mt * BM; r.row_end = p.M; r.n0 = nt * BN; r.g = 0;
+    return r;
+}
+
+__device__ __forceinline__ Tile grouped_tile(const Params& p, const int* prefix, int64_t t) {
+    int lo = 0, hi = (int)p.G;   // prefix[g] <= t < prefix[g + 1]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int64_t g = lo;
+    const int64_t r0 = p.group_offsets[g], r1 = p.group_offsets[g + 1];
+    const int64_t mtiles = (r1 - r0 + BM - 1) / BM;
+    const int64_t local = t - prefix[g];
+    Tile r;
+    r.row0 = r0 + (local % mtiles) * BM; r.row_end = r1; r.n0 = (local / mtiles) * BN; r.g = g;
+    return r;
+}
+
+// ---------------------------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------------------------
+template <int FMT, bool GROUPED>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    using C = Cfg<FMT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + C::SMEM_BAR;                 // STAGES barriers
+    const uint32_t bar_empty = bar_full + 8 * STAGES;              // STAGES barriers
+    const uint32_t bar_tfull = bar_empty + 8 * STAGES;
+    const uint32_t bar_tempty = bar_tfull + 8;
+    const uint32_t bar_done = bar_tempty + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
+    int* prefix = reinterpret_cast<int*>(smem + C::SMEM_PREFIX);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_tfull, 1);
+        mbar_init(bar_tempty, 4);
+        mbar_init(bar_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmB) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    int64_t total_tiles;
+    if (GROUPED) {
+        // prefix[g] = output tiles of groups < g: counts in parallel, then one scan in shared memory
+        for (int64_t g = threadIdx.x; g < p.G; g += NUM_THREADS) {
+            const int64_t rows = __ldg(p.group_offsets + g + 1) - __ldg(p.group_offsets + g);
+            prefix[g + 1] = (int)(((rows + BM - 1) / BM) * p.n_tiles);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            prefix[0] = 0;
+            for (int64_t g = 1; g <= p.G; ++g) prefix[g] += prefix[g - 1];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    total_tiles = GROUPED ? (int64_t)prefix[p.G] : p.total_tiles;
+
+    if (warp == 0) {
+        // ------------------------------- producer -------------------------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued_parity[STAGES];
+        for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            const Tile tile = GROUPED ? grouped_tile(p, prefix, t) : dense_tile(p, t);
+            const int64_t brow = (GROUPED ? tile.g * p.N : 0) + tile.n0;
+            const uint8_t* sb_g = p.sb + (GROUPED ? tile.g * p.sb_group_bytes : 0);
+            const int64_t bt0 = tile.n0 / 128;                      // first 128-row band of B
+            const bool b_hi = tile.n0 + 128 < p.N;                  // does the second band exist?
+            for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+                const uint32_t sA = sbase + C::SMEM_A + stage * A_STAGE_BYTES;
+                const uint32_t sB = sbase + C::SMEM_B + stage * B_STAGE_BYTES;
+                const uint32_t sSFA = sbase + C::SMEM_SFA + stage * C::SFA_BYTES;
+                const uint32_t sSFB = sbase + C::SMEM_SFB + stage * C::SFB_BYTES;
+                const int64_t ct0 = ks * C::SF_ATOMS_A;             // first 4-column scale tile of this stage
+                if (GROUPED) {
+                    // gather the A-side atoms: row i of the tile -> line (i % 32), word (i / 32)
+                    uint32_t* dst = reinterpret_cast<uint32_t*>(smem + C::SMEM_SFA + stage * C::SFA_BYTES);
+                    for (int idx = lane; idx < BM * C::SF_ATOMS_A; idx += 32) {
+                        const int i = idx % BM, atom = idx / BM;
+                        const int64_t r = tile.row0 + i;
+                        uint32_t w = 0;
+                        if (r < p.M)
+                            w = __ldg(reinterpret_cast<const uint32_t*>(p.sa + ((((r >> 7) * p.nct + ct0 + atom) << 9) +
+                                                                                ((r & 31) << 4) + (((r >> 5) & 3) << 2))));
+                        dst[atom * 128 + (i & 31) * 4 + (i >> 5)] = w;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    uint32_t bytes = A_STAGE_BYTES + B_STAGE_BYTES + C::SFB_BYTES / (b_hi ? 1 : 2);
+                    if (!GROUPED) bytes += C::SFA_BYTES;
+                    mbar_arrive_expect_tx(bar_full + 8 * stage, bytes);
+                    const int32_t kb = (int32_t)(ks * BKB);
+                    tma_load_2d(sA, &tmA, kb, (int32_t)tile.row0, bar_full + 8 * stage);
+                    tma_load_2d(sB, &tmB, kb, (int32_t)brow, bar_full + 8 * stage);
+                    if (!GROUPED)
+                        bulk_load(sSFA, p.sa + (((tile.row0 >> 7) * p.nct + ct0) << 9), C::SFA_BYTES, bar_full + 8 * stage);
+                    bulk_load(sSFB, sb_g + ((bt0 * p.nct + ct0) << 9), C::SFA_BYTES, bar_full + 8 * stage);
+                    if (b_hi)
+                        bulk_load(sSFB + C::SFA_BYTES, sb_g + (((bt0 + 1) * p.nct + ct0) << 9), C::SFA_BYTES,
+                                  bar_full + 8 * stage);
+                }
+                issued_parity[stage] = (int)phase;
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+        }
+        if (!ok && lane == 0) {
+            // drain: wait (bounded) for every load this warp issued to land before the CTA exits
+            for (int s = 0; s < STAGES; ++s)
+                if (issued_parity[s] >= 0) {
+                    const unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(bar_full + 8 * s, (uint32_t)issued_parity[s]) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
+                }
+        }
+    } else if (warp == 1) {
+        // ------------------------------- MMA issuer -------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true, issued_any = false;
+            for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                if (!mbar_wait(bar_tempty, acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sA = sbase + C::SMEM_A + stage * A_STAGE_BYTES;
+                    const uint32_t sB = sbase + C::SMEM_B + stage * B_STAGE_BYTES;
+                    const uint32_t sSFA = sbase + C::SMEM_SFA + stage * C::SFA_BYTES;
+                    const uint32_t sSFB = sbase + C::SMEM_SFB + stage * C::SFB_BYTES;
+                    const uint32_t tSFA = tmem + TMEM_SF_BASE + stage * (C::SFA_COLS + C::SFB_COLS);
+                    const uint32_t tSFB = tSFA + C::SFA_COLS;
+                    // scales -> TMEM: A atom j to columns 4j..4j+3; B band h, atom j to 8j + 4h
+#pragma unroll
+                    for (int j = 0; j < C::SF_ATOMS_A; ++j) {
+                        tc_cp_sf(tSFA + 4 * j, desc_sf(sSFA + 512 * j));
+                        tc_cp_sf(tSFB + 8 * j, desc_sf(sSFB + 512 * j));
+                        tc_cp_sf(tSFB + 8 * j + 4, desc_sf(sSFB + C::SFA_BYTES + 512 * j));
+                    }
+#pragma unroll
+                    for (int j = 0; j < BKB / 32; ++j) {
+                        // MXFP8: one atom covers the 4 MMAs of the stage, the scale id picks the byte;
+                        // NVFP4: each MMA (K = 64) consumes a whole atom word
+                        const uint32_t sf_id = FMT == 0 ? (uint32_t)j : 0u;
+                        const uint32_t col = FMT == 0 ? 0u : (uint32_t)j;
+                        tc_mma<FMT>(tmem, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j), make_idesc<FMT>(sf_id),
+                                    tSFA + 4 * col, tSFB + 8 * col, (ks > 0 || j > 0) ? 1u : 0u);
+                    }
+                    issued_any = true;
+                    tc_commit(bar_empty + 8 * stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc_commit(bar_tfull);
+                acc_phase ^= 1;
+            }
+            if (issued_any) {
+                // every tcgen05 op this thread issued has completed once bar_done flips
+                tc_commit(bar_done);
+                const unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(bar_done, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------- epilogue -------------------------------
+        const int q = warp & 3;                     // TMEM lane quadrant this warp may access
+        uint32_t acc_phase = 0;
+        for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+            const Tile tile = GROUPED ? grouped_tile(p, prefix, t) : dense_tile(p, t);
+            if (!mbar_wait(bar_tfull, acc_phase, abort_flag)) break;
+            tc_fence_after();
+            const int64_t row = tile.row0 + q * 32 + lane;
+            const bool row_ok = row < tile.row_end;
+            float aa = 1.0f;
+            if (p.alpha_a_scope == 1) aa = __ldg(p.alpha_a);
+            else if (p.alpha_a_scope == 2 && row_ok) aa = __ldg(p.alpha_a + row);
+            float ab_g = 1.0f;
+            if (GROUPED && p.alpha_b_scope != 0) ab_g = __ldg(p.alpha_b + tile.g);
+            else if (!GROUPED && p.alpha_b_scope == 1) ab_g = __ldg(p.alpha_b);
+            uint16_t* drow = p.d + row * p.ldd;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                float v[32];
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
+                const int64_t nb = tile.n0 + c * 32;
+                if (!row_ok || nb >= p.N) continue;
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float f0 = __fmul_rn(v[2 * i], aa), f1 = __fmul_rn(v[2 * i + 1], aa);
+                    if (!GROUPED && p.alpha_b_scope == 2) {
+                        const int64_t n = nb + 2 * i;
+                        f0 = __fmul_rn(f0, n < p.N ? __ldg(p.alpha_b + n) : 0.0f);
+                        f1 = __fmul_rn(f1, n + 1 < p.N ? __ldg(p.alpha_b + n + 1) : 0.0f);
+                    } else {
+                        f0 = __fmul_rn(f0, ab_g);
+                        f1 = __fmul_rn(f1, ab_g);
+                    }
+                    packed[i] = pack_bf16x2(f0, f1);
+                }
+                if (nb + 32 <= p.N) {
+                    uint4* dst = reinterpret_cast<uint4*>(drow + nb);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                } else {
+                    for (int i = 0; i < 32 && nb + i < p.N; ++i)
+                        drow[nb + i] = (uint16_t)((packed[i >> 1] >> (16 * (i & 1))) & 0xFFFFu);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tempty);
+            acc_phase ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap* map, const uint8_t* base, int64_t k_bytes, int64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)k_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)k_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)BKB, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int FMT, bool GROUPED>
+cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
+    using C = Cfg<FMT>;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(bs_gemm_kernel<FMT, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::SMEM_ALLOC);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    const int64_t k_bytes = FMT == 0 ? a.K : a.K / 2;
+    const int block = FMT == 0 ? 32 : 16;
+    CUtensorMap tmA, tmB;
+    if (!make_map(&tmA, a.a, k_bytes, a.M, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&tmB, a.b, k_bytes, GROUPED ? a.G * a.N : a.N, BN)) return cudaErrorInvalidValue;
+
+    Params p{};
+    p.sa = a.sa; p.sb = a.sb;
+    p.alpha_a = a.alpha_a; p.alpha_a_scope = a.alpha_a_scope;
+    p.alpha_b = a.alpha_b; p.alpha_b_scope = a.alpha_b_scope;
+    p.M = a.M; p.N = a.N; p.K = a.K; p.d = a.d; p.ldd = a.ldd;
+    p.G = a.G; p.group_offsets = a.group_offsets;
+    p.m_tiles = (a.M + BM - 1) / BM;
+    p.n_tiles = (a.N + BN - 1) / BN;
+    p.k_stages = k_bytes / BKB;
+    p.nct = (a.K / block + 3) / 4;
+    p.sb_group_bytes = host_scale_bytes(a.N, a.K, block);
+    p.total_tiles = p.m_tiles * p.n_tiles;
+    int64_t tiles_bound = GROUPED ? (p.m_tiles + a.G) * p.n_tiles : p.total_tiles;
+    const unsigned grid = (unsigned)max64(1, min64(tiles_bound, num_sms));
+    bs_gemm_kernel<FMT, GROUPED><<<grid, NUM_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream) {
+    if (args.G > MAX_GROUPS) return cudaErrorInvalidValue;
+    if (args.fmt == 0) return args.G > 0 ? launch_impl<0, true>(args, num_sms, stream) : launch_impl<0, false>(args, num_sms, stream);
+    return args.G > 0 ? launch_impl<1, true>(args, num_sms, stream) : launch_impl<1, false>(args, num_sms, stream);
+}
+
+uint32_t read_and_clear_device_status() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_mx_device_status, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+    cudaMemcpyToSymbol(g_mx_device_status, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace mxk

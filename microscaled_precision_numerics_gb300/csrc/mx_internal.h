@@ -1,0 +1,55 @@
+// mx_internal.h -- declarations shared by the mxnum translation units (not part of the C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "mx_device.cuh"
+
+namespace mxk {
+
+// Bytes of a GEMM-layout scale tensor (see include/mxnum.h).
+__host__ __device__ inline int64_t host_scale_bytes(int64_t rows, int64_t k, int block) {
+    return ((rows + 127) / 128) * ((k / block + 3) / 4) * 512;
+}
+__host__ __device__ inline int64_t host_scale_bytes_dev(int64_t rows, int64_t k, int block) {
+    return host_scale_bytes(rows, k, block);
+}
+
+// RHT sign mask computed on the host with the same Philox4x32-10 definition as the device.
+uint32_t host_rht_sign_mask(uint64_t seed);
+
+cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q_row,
+                                  uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, cudaStream_t stream);
+cudaError_t launch_nvfp4_per_token(const uint16_t* x, int64_t T, int64_t H, int64_t ldx, uint8_t* q, uint8_t* s,
+                                   float* s_tok, cudaStream_t stream);
+cudaError_t launch_nvfp4_1x16(const uint16_t* x, int64_t T, int64_t N, bool colwise, bool rht, uint64_t rht_seed,
+                              bool sr, uint64_t sr_seed, uint8_t* q, uint8_t* s, float* s_tensor, uint32_t* ws,
+                              int num_sms, cudaStream_t stream);
+cudaError_t launch_rht16(const uint16_t* x, int64_t T, int64_t N, uint64_t seed, uint16_t* y, cudaStream_t stream);
+cudaError_t launch_nvfp4_weight_2d(const uint16_t* w, int64_t G, int64_t O, int64_t H, uint8_t* q_row, uint8_t* s_row,
+                                   uint8_t* q_col, uint8_t* s_col, float* s_w, uint32_t* ws, int num_sms,
+                                   cudaStream_t stream);
+cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const float* s2, bool per_row, int64_t R,
+                           int64_t K, uint16_t* y, cudaStream_t stream);
+cudaError_t launch_mismatch(const uint8_t* x, const uint8_t* y, int64_t nbytes, unsigned long long* count,
+                            int num_sms, cudaStream_t stream);
+
+// Block-scaled tcgen05 GEMM (dense and grouped).  fmt: 0 MXFP8, 1 NVFP4.  alpha scopes: 0 none,
+// 1 tensor, 2 row (per M row for a, per N column for b; per group for grouped b).
+struct GemmArgs {
+    int fmt;
+    const uint8_t* a; const uint8_t* sa; const float* alpha_a; int alpha_a_scope;
+    const uint8_t* b; const uint8_t* sb; const float* alpha_b; int alpha_b_scope;
+    int64_t M, N, K;
+    uint16_t* d; int64_t ldd;
+    // grouped: G > 0 and group_offsets (device) describe the expert-sorted row groups of a; b holds G
+    // matrices [N, K] with per-group scale tensors; alpha_b is per group.
+    int64_t G; const int64_t* group_offsets;
+};
+cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream);
+uint32_t read_and_clear_device_status();
+
+int device_sm_count();
+
+}  // namespace mxk

@@ -1,0 +1,167 @@
+// quant_mxfp8.cu -- MXFP8 (1x32 and 32x1 E4M3 blocks with E8M0 scales) quantizer, row-wise and
+// column-wise copies from one read of the BF16 input.
+//
+// Miles page: MXFP8 = 32 E4M3 values sharing one E8M0 scale; the tensor cores want the blocks along
+// the GEMM's reduction dimension, so TransformerEngine makes row-wise and column-wise copies from
+// the high-precision input.  E2E page Table 6: the quantizer and a separate scale-rearrangement
+// kernel cost 2.2 + 2.6 ms per micro-batch; here one kernel writes both copies with their scales
+// already in the GEMM layout.
+//
+// CTA tile: 128 rows x 64 columns of BF16 (16 KB), staged in shared memory with a padded pitch.
+//   row-wise:    256 (row, 32-column block) pairs, one per thread
+//   column-wise: 64 columns x 4 row blocks of 32, one per thread
+// Scale exponent: e = max(exp_field(amax) - 8, 0) - 127 as an E8M0 byte; the multiply by 2^-e is
+// exact in FP32 for every value that can round to a nonzero E4M3 code.
+#include "mx_internal.h"
+
+namespace mxk {
+
+namespace {
+
+constexpr int QT_ROWS = 128;
+constexpr int QT_COLS = 64;
+constexpr int QT_PITCH = 144;   // bytes per staged row: 128 + 16 keeps 16-byte accesses conflict-free
+constexpr int QT_THREADS = 256;
+
+__device__ __forceinline__ uint32_t e8m0_from_amax_bits(uint32_t amax16) {
+    const int ef = (int)((amax16 >> 7) & 0xFFu);   // BF16 exponent field (0 for zero/subnormal)
+    return (uint32_t)max(ef - 8, 0);                 // clamp e = ef - 127 - 8 at -127
+}
+
+// 2^-e for scale byte s (e = s - 127): exponent field 254 - s, always a normal FP32.
+__device__ __forceinline__ float inv_scale_from_e8m0(uint32_t s) { return __uint_as_float((254u - s) << 23); }
+
+// Quantize 32 BF16 values held as 16 packed words; writes 32 code bytes into out[8] words.
+__device__ __forceinline__ uint32_t mxfp8_block32(const uint32_t w[16], uint32_t out[8]) {
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m2 = absmax_bf16x2(m2, w[i]);
+    const uint32_t s = e8m0_from_amax_bits(fold_halves(m2));
+    const float f = inv_scale_from_e8m0(s);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        out[i] = cvt_e4m3x4(__fmul_rn(bf16_lo(w[2 * i]), f), __fmul_rn(bf16_hi(w[2 * i]), f),
+                            __fmul_rn(bf16_lo(w[2 * i + 1]), f), __fmul_rn(bf16_hi(w[2 * i + 1]), f));
+    }
+    return s;
+}
+
+template <bool ROW, bool COL>
+__global__ void __launch_bounds__(QT_THREADS)
+mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
+                      uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
+                      uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
+    __shared__ __align__(16) uint8_t tile[QT_ROWS * QT_PITCH];
+    __shared__ uint8_t colsc[4][QT_COLS];
+
+    const int tid = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.y * QT_ROWS;
+    const int64_t c0 = (int64_t)blockIdx.x * QT_COLS;
+
+    // ---- stage: 128 rows x 8 chunks of 16 bytes; each warp reads 4 whole 128-byte rows ----
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int ci = tid + QT_THREADS * j;
+        const int rr = ci >> 3, ch = ci & 7;
+        const int64_t r = r0 + rr, c = c0 + ch * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < R && c < K) v = __ldcs(reinterpret_cast<const uint4*>(x + r * ldx + c));
+        *reinterpret_cast<uint4*>(tile + rr * QT_PITCH + ch * 16) = v;
+    }
+    __syncthreads();
+
+    if (ROW) {
+        // thread -> (row rr, block b); b = tid & 1 so the two blocks of a row are adjacent lanes
+        const int rr = tid >> 1, b = tid & 1;
+        const int64_t r = r0 + rr, c = c0 + b * 32;
+        const bool valid = (r < R) && (c < K);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4*>(tile + rr * QT_PITCH + b * 64 + i * 16);
+            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+        uint32_t codes[8];
+        const uint32_t s = mxfp8_block32(w, codes);
+        if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(q_row + r * K + c);
+            __stcs(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
+            __stcs(dst + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+        }
+        // the pair (b = 0, b = 1) shares one 16-bit slot of the scale layout (c0 / 32 is even)
+        const uint32_t s_other = __shfl_down_sync(0xFFFFFFFFu, s, 1);
+        const int64_t nct = sf_col_tiles(K, 32);
+        const int64_t kb = c0 / 32;
+        if (b == 0 && r < R) {
+            const bool both = (c0 + 32 < K);
+            uint8_t* p = s_row + sf_offset(r, kb, nct);
+            if (both) *reinterpret_cast<uint16_t*>(p) = (uint16_t)(s | (s_other << 8));
+            else *p = (uint8_t)s;
+        }
+    }
+
+    if (COL) {
+        // thread -> (column cc, row block rb); consecutive lanes read consecutive columns
+        const int cc = tid & 63, rb = tid >> 6;
+        const int64_t c = c0 + cc, rbase = r0 + rb * 32;
+        const bool valid = (c < K) && (rbase < R);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t lo = *reinterpret_cast<const uint16_t*>(tile + (rb * 32 + 2 * i) * QT_PITCH + cc * 2);
+            const uint32_t hi = *reinterpret_cast<const uint16_t*>(tile + (rb * 32 + 2 * i + 1) * QT_PITCH + cc * 2);
+            w[i] = lo | (hi << 16);
+        }
+        uint32_t codes[8];
+        const uint32_t s = mxfp8_block32(w, codes);
+        if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(q_col + c * R + rbase);
+            __stcs(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
+            __stcs(dst + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+        }
+        colsc[rb][cc] = (uint8_t)s;
+        __syncthreads();
+        // one 32-bit word of 4 row-block scales per column (r0 / 32 is a multiple of 4)
+        if (tid < QT_COLS) {
+            const int64_t cw = c0 + tid;
+            if (cw < K) {
+                const int64_t nct = sf_col_tiles(R, 32);
+                const int64_t rbk = r0 / 32;
+                const int nvalid = (int)min64(4, (R - r0) / 32);
+                uint8_t* p = s_col + sf_offset(cw, rbk, nct);
+                if (nvalid == 4) {
+                    *reinterpret_cast<uint32_t*>(p) = (uint32_t)colsc[0][tid] | ((uint32_t)colsc[1][tid] << 8) |
+                                                      ((uint32_t)colsc[2][tid] << 16) | ((uint32_t)colsc[3][tid] << 24);
+                } else {
+                    for (int i = 0; i < nvalid; ++i) p[i] = colsc[i][tid];
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q_row,
+                                  uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, cudaStream_t stream) {
+    const bool row = q_row != nullptr, col = q_col != nullptr;
+    // zero the scale padding (rows beyond R up to a multiple of 128, scale columns up to a multiple of 4)
+    if (row && ((R % 128) != 0 || ((K / 32) % 4) != 0)) {
+        cudaError_t e = cudaMemsetAsync(s_row, 0, (size_t)host_scale_bytes(R, K, 32), stream);
+        if (e != cudaSuccess) return e;
+    }
+    if (col && ((K % 128) != 0 || ((R / 32) % 4) != 0)) {
+        cudaError_t e = cudaMemsetAsync(s_col, 0, (size_t)host_scale_bytes(K, R, 32), stream);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid((unsigned)((K + QT_COLS - 1) / QT_COLS), (unsigned)((R + QT_ROWS - 1) / QT_ROWS));
+    if (row && col)
+        mxfp8_quantize_kernel<true, true><<<grid, QT_THREADS, 0, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col);
+    else if (row)
+        mxfp8_quantize_kernel<true, false><<<grid, QT_THREADS, 0, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col);
+    else
+        mxfp8_quantize_kernel<false, true><<<grid, QT_THREADS, 0, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col);
+    return cudaGetLastError();
+}
+
+}  // namespace mxk

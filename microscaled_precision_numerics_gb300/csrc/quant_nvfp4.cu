@@ -1,0 +1,549 @@
+// quant_nvfp4.cu -- NVFP4 quantizers (E2M1 values, one E4M3 scale per 16, FP32 second level).
+//
+//   per-token 1x16 (Miles page: per-token FP32 scale computed online and fused into the activation
+//                   quantizer; NVFP4 RL page, "Baseline recipe details")
+//   per-tensor 1x16, row-wise or column-wise along tokens, optional RHT, RNE or SR (MaxText page,
+//                   "NVFP4 pretraining recipe": 1x16 activations/gradients, RHT on WGRAD inputs,
+//                   SR on gradients)
+//   standalone RHT16 along tokens
+//   16x16 2D weights, both orientations (MaxText page: 2D weight scaling; Miles page: joint gate/up)
+//
+// All scale arithmetic is FP32 round-to-nearest in the documented order (mx_device.cuh); E2M1 and
+// E4M3 codes come from the cvt.rn.satfinite instructions, or from the ALU stochastic rounding.
+#include "mx_internal.h"
+
+namespace mxk {
+
+namespace {
+
+// ------------------------------------------------------------------------------------------------
+// Row-wise 1x16 (per token or per tensor).  One warp per row; lane l owns 8-element chunks
+// l, l + 32, ...; a 16-block is the chunk pair (2m, 2m + 1) held by adjacent lanes.
+// ------------------------------------------------------------------------------------------------
+constexpr int RW_WARPS = 8;
+
+template <bool PER_TENSOR, bool SR>
+__global__ void __launch_bounds__(RW_WARPS * 32)
+nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64_t ldx,
+                     uint8_t* __restrict__ q, uint8_t* __restrict__ s, float* __restrict__ s_tok,
+                     const uint32_t* __restrict__ tensor_amax, float* __restrict__ s_tensor, uint64_t sr_seed) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * RW_WARPS + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const uint16_t* xr = x + t * ldx;
+    const int64_t nchunk = H / 8;
+
+    float S;
+    if (PER_TENSOR) {
+        S = nvfp4_second_scale(__uint_as_float(*tensor_amax));
+        if (t == 0 && lane == 0) *s_tensor = S;
+    } else {
+        uint32_t m2 = 0;
+        for (int64_t ch = lane; ch < nchunk; ch += 32) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + ch * 8));
+            m2 = absmax_bf16x2(m2, v.x); m2 = absmax_bf16x2(m2, v.y);
+            m2 = absmax_bf16x2(m2, v.z); m2 = absmax_bf16x2(m2, v.w);
+        }
+        const uint32_t amax16 = __reduce_max_sync(0xFFFFFFFFu, fold_halves(m2));
+        S = nvfp4_second_scale(__uint_as_float(amax16 << 16));
+        if (lane == 0) s_tok[t] = S;
+    }
+
+    const int64_t nct = sf_col_tiles(H, 16);
+    const int64_t nblk = H / 16;
+    const uint32_t k0 = (uint32_t)sr_seed, k1 = (uint32_t)(sr_seed >> 32);
+    for (int64_t base = 0; base < nchunk; base += 32) {
+        const int64_t ch = base + lane;
+        const bool valid = ch < nchunk;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) v = __ldcs(reinterpret_cast<const uint4*>(xr + ch * 8));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m2 = absmax_bf16x2(m2, w[i]);
+        uint32_t a16 = fold_halves(m2);
+        a16 = max(a16, __shfl_xor_sync(0xFFFFFFFFu, a16, 1));
+        const uint32_t bs = nvfp4_block_scale(__uint_as_float(a16 << 16), S);
+        const float r = nvfp4_block_recip(bs, S);
+        float vals[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            vals[2 * i] = __fmul_rn(bf16_lo(w[i]), r);
+            vals[2 * i + 1] = __fmul_rn(bf16_hi(w[i]), r);
+        }
+        uint32_t codes;
+        if (SR) {
+            // logical element i = t * H + ch * 8 + j; the 8 elements of a chunk share one Philox block
+            const uint64_t blk = ((uint64_t)t * (uint64_t)H + (uint64_t)ch * 8) >> 3;
+            const U4 rnd = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, k0, k1);
+            const uint32_t rw[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+            codes = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t bits = (j & 1) ? (rw[j >> 1] >> 16) : (rw[j >> 1] & 0xFFFFu);
+                codes |= e2m1_sr(vals[j], bits) << (4 * j);
+            }
+        } else {
+            codes = cvt_e2m1x8(vals);
+        }
+        if (valid) __stcs(reinterpret_cast<uint32_t*>(q + t * (H / 2) + ch * 4), codes);
+        // gather 4 consecutive block scales (chunks 8m .. 8m+7 = lanes 8m' .. 8m'+7) into one word
+        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
+        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 4);
+        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 6);
+        if (valid && (ch & 7) == 0) {
+            const int64_t blk = ch >> 1;
+            uint8_t* p = s + sf_offset(t, blk, nct);
+            if (blk + 4 <= nblk) {
+                *reinterpret_cast<uint32_t*>(p) = bs | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            } else {
+                const uint32_t bb[4] = {bs, b1, b2, b3};
+                for (int i = 0; i < (int)(nblk - blk); ++i) p[i] = (uint8_t)bb[i];
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Column-wise 1x16 along tokens with a per-tensor scale.  CTA tile: 128 tokens x 256 columns; warp
+// w owns tokens [16w, 16w + 16), lane l owns columns [8l, 8l + 8).  Codes and scales are staged
+// transposed in shared memory and written as contiguous runs along the token dimension.
+// ------------------------------------------------------------------------------------------------
+constexpr int CW_TOK = 128;
+constexpr int CW_COLS = 256;
+constexpr int CW_THREADS = 256;
+
+// Load a 16 x 8 micro-tile: xr[i] holds row i's 8 BF16 values.
+__device__ __forceinline__ void load_16x8(const uint16_t* __restrict__ x, int64_t N, int64_t t0, int64_t n0,
+                                          bool valid, uint4 xr[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        xr[i] = valid ? __ldcs(reinterpret_cast<const uint4*>(x + (t0 + i) * N + n0)) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
+    return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
+}
+
+// Column j (0..7) of the micro-tile as 16 floats, optionally transformed and re-rounded to BF16.
+template <bool RHT>
+__device__ __forceinline__ void column_values(const uint4 xr[16], int j, uint32_t signmask, float v[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t w = word_of(xr[i], j >> 1);
+        v[i] = (j & 1) ? bf16_hi(w) : bf16_lo(w);
+    }
+    if (RHT) {
+        rht16_inplace(v, signmask);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const uint32_t p = pack_bf16x2(v[i], v[i + 1]);
+            v[i] = bf16_lo(p);
+            v[i + 1] = bf16_hi(p);
+        }
+    }
+}
+
+template <bool RHT>
+__global__ void __launch_bounds__(CW_THREADS)
+colwise_amax_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint32_t signmask,
+                    uint32_t* __restrict__ amax_out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t0 = (int64_t)blockIdx.y * CW_TOK + warp * 16;
+    const int64_t n0 = (int64_t)blockIdx.x * CW_COLS + lane * 8;
+    const bool valid = (t0 < T) && (n0 < N);
+    uint4 xr[16];
+    load_16x8(x, N, t0, n0, valid, xr);
+    uint32_t m = 0;
+    if (RHT) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float v[16];
+            column_values<true>(xr, j, signmask, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+        }
+    } else {
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            m2 = absmax_bf16x2(m2, xr[i].x); m2 = absmax_bf16x2(m2, xr[i].y);
+            m2 = absmax_bf16x2(m2, xr[i].z); m2 = absmax_bf16x2(m2, xr[i].w);
+        }
+        m = fold_halves(m2) << 16;
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    __shared__ uint32_t wmax[CW_THREADS / 32];
+    if (lane == 0) wmax[warp] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t b = 0;
+        for (int i = 0; i < CW_THREADS / 32; ++i) b = max(b, wmax[i]);
+        atomicMax(amax_out, b);
+    }
+}
+
+template <bool RHT, bool SR>
+__global__ void __launch_bounds__(CW_THREADS)
+colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint32_t signmask,
+                     const uint32_t* __restrict__ tensor_amax, uint64_t sr_seed,
+                     uint8_t* __restrict__ q, uint8_t* __restrict__ s, float* __restrict__ s_tensor) {
+    __shared__ __align__(16) uint8_t qs[CW_COLS][CW_TOK / 2 + 16];   // codes, transposed (+pad)
+    __shared__ uint8_t ss[CW_COLS][CW_TOK / 16];                     // block scales, transposed
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tb0 = (int64_t)blockIdx.y * CW_TOK;
+    const int64_t cb0 = (int64_t)blockIdx.x * CW_COLS;
+    const int64_t t0 = tb0 + warp * 16;
+    const int64_t n0 = cb0 + lane * 8;
+    const bool valid = (t0 < T) && (n0 < N);
+
+    const float S = nvfp4_second_scale(__uint_as_float(*tensor_amax));
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *s_tensor = S;
+
+    uint4 xr[16];
+    load_16x8(x, N, t0, n0, valid, xr);
+
+    // SR: one Philox block per row of the micro-tile (elements t * N + n0 .. + 7)
+    uint32_t rbits[16][4];
+    if (SR) {
+        const uint32_t k0 = (uint32_t)sr_seed, k1 = (uint32_t)(sr_seed >> 32);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint64_t blk = ((uint64_t)(t0 + i) * (uint64_t)N + (uint64_t)n0) >> 3;
+            const U4 r4 = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, k0, k1);
+            rbits[i][0] = r4.x; rbits[i][1] = r4.y; rbits[i][2] = r4.z; rbits[i][3] = r4.w;
+        }
+    }
+
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float v[16];
+        column_values<RHT>(xr, j, signmask, v);
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+        const uint32_t bs = nvfp4_block_scale(__uint_as_float(m), S);
+        const float r = nvfp4_block_recip(bs, S);
+        float p[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) p[i] = __fmul_rn(v[i], r);
+        uint32_t c0, c1;
+        if (SR) {
+            c0 = 0; c1 = 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                // element (t0 + i, n0 + j): word j >> 1, half j & 1
+                const uint32_t w = rbits[i][j >> 1];
+                const uint32_t bits = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
+                const uint32_t code = e2m1_sr(p[i], bits);
+                if (i < 8) c0 |= code << (4 * i); else c1 |= code << (4 * (i - 8));
+            }
+        } else {
+            c0 = cvt_e2m1x8(p);
+            c1 = cvt_e2m1x8(p + 8);
+        }
+        const int col = lane * 8 + j;
+        *reinterpret_cast<uint2*>(&qs[col][warp * 8]) = make_uint2(c0, c1);
+        ss[col][warp] = (uint8_t)bs;
+    }
+    __syncthreads();
+
+    // write out: column col gets CW_TOK/2 = 64 contiguous bytes of codes (4 x 16 B) and 8 scales
+    const int64_t ntok = min64(CW_TOK, T - tb0);      // multiple of 16
+    const int64_t nct = sf_col_tiles(T, 16);
+    if (((T / 2) & 15) == 0) {
+        for (int idx = threadIdx.x; idx < CW_COLS * 4; idx += CW_THREADS) {
+            const int col = idx >> 2, part = idx & 3;
+            const int64_t n = cb0 + col;
+            if (n < N && part * 32 < ntok) {
+                const uint4 val = *reinterpret_cast<const uint4*>(&qs[col][part * 16]);
+                __stcs(reinterpret_cast<uint4*>(q + n * (T / 2) + tb0 / 2 + part * 16), val);
+            }
+        }
+    } else {
+        // rows of q are only 8-byte aligned when T % 32 != 0
+        for (int idx = threadIdx.x; idx < CW_COLS * 8; idx += CW_THREADS) {
+            const int col = idx >> 3, part = idx & 7;
+            const int64_t n = cb0 + col;
+            if (n < N && part * 16 < ntok) {
+                const uint2 val = *reinterpret_cast<const uint2*>(&qs[col][part * 8]);
+                __stcs(reinterpret_cast<uint2*>(q + n * (T / 2) + tb0 / 2 + part * 8), val);
+            }
+        }
+    }
+    for (int idx = threadIdx.x; idx < CW_COLS * 2; idx += CW_THREADS) {
+        const int col = idx >> 1, half = idx & 1;
+        const int64_t n = cb0 + col;
+        const int64_t kb = tb0 / 16 + half * 4;
+        const int nb = (int)min64(4, ntok / 16 - half * 4);
+        if (n < N && nb > 0) {
+            uint8_t* p = s + sf_offset(n, kb, nct);
+            if (nb == 4) {
+                *reinterpret_cast<uint32_t*>(p) = (uint32_t)ss[col][half * 4] | ((uint32_t)ss[col][half * 4 + 1] << 8) |
+                                                  ((uint32_t)ss[col][half * 4 + 2] << 16) | ((uint32_t)ss[col][half * 4 + 3] << 24);
+            } else {
+                for (int i = 0; i < nb; ++i) p[i] = ss[col][half * 4 + i];
+            }
+        }
+    }
+}
+
+// Plain amax over a BF16 tensor (row-wise per-tensor pass 1).
+__global__ void __launch_bounds__(256)
+amax_kernel(const uint16_t* __restrict__ x, int64_t n_elems, uint32_t* __restrict__ amax_out) {
+    uint32_t m2 = 0;
+    const int64_t nvec = n_elems / 8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + i);
+        m2 = absmax_bf16x2(m2, v.x); m2 = absmax_bf16x2(m2, v.y);
+        m2 = absmax_bf16x2(m2, v.z); m2 = absmax_bf16x2(m2, v.w);
+    }
+    uint32_t m = __reduce_max_sync(0xFFFFFFFFu, fold_halves(m2)) << 16;
+    __shared__ uint32_t wmax[8];
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t b = 0;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) b = max(b, wmax[i]);
+        atomicMax(amax_out, b);
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Standalone RHT16 along tokens: thread = 16 tokens x 8 columns.
+// ------------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+rht16_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint32_t signmask, uint16_t* __restrict__ y) {
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t ncg = N / 8;
+    const int64_t t0 = (gid / ncg) * 16, n0 = (gid % ncg) * 8;
+    if (t0 >= T) return;
+    uint4 xr[16];
+    load_16x8(x, N, t0, n0, true, xr);
+    uint32_t out[16][4];
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+        float a[16], b[16];
+        column_values<true>(xr, j, signmask, a);
+        column_values<true>(xr, j + 1, signmask, b);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) out[i][j >> 1] = pack_bf16x2(a[i], b[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        __stcs(reinterpret_cast<uint4*>(y + (t0 + i) * N + n0), make_uint4(out[i][0], out[i][1], out[i][2], out[i][3]));
+}
+
+// ------------------------------------------------------------------------------------------------
+// 16x16 2D weights.  Pass 1: per-matrix amax.  Pass 2: CTA tile = 64 rows (4 warps x 16) x 128
+// columns; lane l reads chunk (l & 15) of rows 2i + (l >> 4); the 16x16 tile amax combines lanes
+// l, l^1, l^16 over the 8 iterations.
+// ------------------------------------------------------------------------------------------------
+constexpr int W2_ROWS = 64;
+constexpr int W2_COLS = 128;
+
+__global__ void __launch_bounds__(256)
+matrix_amax_kernel(const uint16_t* __restrict__ w, int64_t per_matrix, uint32_t* __restrict__ amax_out) {
+    const int64_t g = blockIdx.y;
+    const uint16_t* base = w + g * per_matrix;
+    uint32_t m2 = 0;
+    const int64_t nvec = per_matrix / 8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(base) + i);
+        m2 = absmax_bf16x2(m2, v.x); m2 = absmax_bf16x2(m2, v.y);
+        m2 = absmax_bf16x2(m2, v.z); m2 = absmax_bf16x2(m2, v.w);
+    }
+    uint32_t m = __reduce_max_sync(0xFFFFFFFFu, fold_halves(m2)) << 16;
+    __shared__ uint32_t wmax[8];
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t b = 0;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) b = max(b, wmax[i]);
+        atomicMax(amax_out + g, b);
+    }
+}
+
+__global__ void __launch_bounds__(128)
+weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, const uint32_t* __restrict__ amax,
+                      uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
+                      uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, float* __restrict__ s_w) {
+    __shared__ __align__(16) uint8_t qt[W2_COLS][W2_ROWS / 2 + 16];   // transposed codes (+pad)
+    __shared__ uint8_t st[W2_ROWS / 16][W2_COLS / 16];                 // tile scales
+    const int64_t g = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t o0 = (int64_t)blockIdx.y * W2_ROWS + warp * 16;
+    const int64_t h0 = (int64_t)blockIdx.x * W2_COLS;
+    const uint16_t* wg = w + g * O * H;
+    const float S = nvfp4_second_scale(__uint_as_float(amax[g]));
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) s_w[g] = S;
+
+    const int chunk = lane & 15, rpar = lane >> 4;
+    const int64_t h = h0 + chunk * 8;
+    const bool colv = h < H;
+    const bool rowv = o0 < O;
+    uint4 xr[8];
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t o = o0 + 2 * i + rpar;
+        xr[i] = (rowv && colv) ? __ldcs(reinterpret_cast<const uint4*>(wg + o * H + h)) : make_uint4(0u, 0u, 0u, 0u);
+        m2 = absmax_bf16x2(m2, xr[i].x); m2 = absmax_bf16x2(m2, xr[i].y);
+        m2 = absmax_bf16x2(m2, xr[i].z); m2 = absmax_bf16x2(m2, xr[i].w);
+    }
+    uint32_t a16 = fold_halves(m2);
+    a16 = max(a16, __shfl_xor_sync(0xFFFFFFFFu, a16, 1));
+    a16 = max(a16, __shfl_xor_sync(0xFFFFFFFFu, a16, 16));
+    const uint32_t bs = nvfp4_block_scale(__uint_as_float(a16 << 16), S);
+    const float r = nvfp4_block_recip(bs, S);
+
+    uint8_t* qrow_g = q_row + g * O * (H / 2);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int rr = 2 * i + rpar;                     // row within the warp's 16
+        float v[8];
+        v[0] = __fmul_rn(bf16_lo(xr[i].x), r); v[1] = __fmul_rn(bf16_hi(xr[i].x), r);
+        v[2] = __fmul_rn(bf16_lo(xr[i].y), r); v[3] = __fmul_rn(bf16_hi(xr[i].y), r);
+        v[4] = __fmul_rn(bf16_lo(xr[i].z), r); v[5] = __fmul_rn(bf16_hi(xr[i].z), r);
+        v[6] = __fmul_rn(bf16_lo(xr[i].w), r); v[7] = __fmul_rn(bf16_hi(xr[i].w), r);
+        const uint32_t codes = cvt_e2m1x8(v);
+        if (rowv && colv) __stcs(reinterpret_cast<uint32_t*>(qrow_g + (o0 + rr) * (H / 2) + h / 2), codes);
+        // transposed staging: column chunk*8 + j gets the nibble of row warp*16 + rr
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t nib = (codes >> (4 * j)) & 0xFu;
+            const int row = warp * 16 + rr;
+            // two rows per byte: even row in the low nibble; rows rr and rr^1 live in lanes l and l^16
+            const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, nib, 16);
+            if (rpar == 0) qt[chunk * 8 + j][row >> 1] = (uint8_t)(nib | (other << 4));
+        }
+    }
+    if (lane < 16 && (lane & 1) == 0) st[warp][lane >> 1] = (uint8_t)bs;
+    __syncthreads();
+
+    // row-wise scales: rows o0 .. o0 + 15 of this warp, 8 tile scales each (2 words per row)
+    {
+        const int64_t nct = sf_col_tiles(H, 16);
+        const int rr = lane >> 1, half = lane & 1;
+        const int64_t o = o0 + rr;
+        const int64_t kb = h0 / 16 + half * 4;
+        const int nb = (int)min64(4, H / 16 - kb);
+        if (rowv && nb > 0) {
+            uint8_t* p = s_row + g * host_scale_bytes_dev(O, H, 16) + sf_offset(o, kb, nct);
+            if (nb == 4) {
+                *reinterpret_cast<uint32_t*>(p) = (uint32_t)st[warp][half * 4] | ((uint32_t)st[warp][half * 4 + 1] << 8) |
+                                                  ((uint32_t)st[warp][half * 4 + 2] << 16) | ((uint32_t)st[warp][half * 4 + 3] << 24);
+            } else {
+                for (int i = 0; i < nb; ++i) p[i] = st[warp][half * 4 + i];
+            }
+        }
+    }
+    // column-wise codes: column h0 + c gets 32 contiguous bytes (rows o_base .. o_base + 63)
+    const int64_t ob = (int64_t)blockIdx.y * W2_ROWS;
+    const int64_t nrows = min64(W2_ROWS, O - ob);      // multiple of 16
+    uint8_t* qcol_g = q_col + g * H * (O / 2);
+    for (int idx = threadIdx.x; idx < W2_COLS * 4; idx += 128) {
+        const int c = idx >> 2, part = idx & 3;              // part: 8-byte piece (16 rows)
+        const int64_t hc = h0 + c;
+        if (hc < H && part * 16 < nrows)
+            *reinterpret_cast<uint2*>(qcol_g + hc * (O / 2) + ob / 2 + part * 8) =
+                *reinterpret_cast<const uint2*>(&qt[c][part * 8]);
+    }
+    // column-wise scales: row hc, scale columns ob/16 .. +3 (one word when all 4 row tiles exist)
+    {
+        const int64_t nct = sf_col_tiles(O, 16);
+        const int nb = (int)(nrows / 16);
+        uint8_t* sbase = s_col + g * host_scale_bytes_dev(H, O, 16);
+        for (int c = threadIdx.x; c < W2_COLS; c += 128) {
+            const int64_t hc = h0 + c;
+            if (hc >= H) continue;
+            uint8_t* p = sbase + sf_offset(hc, ob / 16, nct);
+            const int jt = c >> 4;
+            if (nb == 4) {
+                *reinterpret_cast<uint32_t*>(p) = (uint32_t)st[0][jt] | ((uint32_t)st[1][jt] << 8) |
+                                                  ((uint32_t)st[2][jt] << 16) | ((uint32_t)st[3][jt] << 24);
+            } else {
+                for (int i = 0; i < nb; ++i) p[i] = st[i][jt];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------------------------------
+// launchers
+// ------------------------------------------------------------------------------------------------
+cudaError_t launch_nvfp4_per_token(const uint16_t* x, int64_t T, int64_t H, int64_t ldx, uint8_t* q, uint8_t* s,
+                                   float* s_tok, cudaStream_t stream) {
+    if ((T % 128) != 0 || ((H / 16) % 4) != 0) {
+        cudaError_t e = cudaMemsetAsync(s, 0, (size_t)host_scale_bytes(T, H, 16), stream);
+        if (e != cudaSuccess) return e;
+    }
+    const unsigned grid = (unsigned)((T + RW_WARPS - 1) / RW_WARPS);
+    nvfp4_rowwise_kernel<false, false><<<grid, RW_WARPS * 32, 0, stream>>>(x, T, H, ldx, q, s, s_tok, nullptr, nullptr, 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_nvfp4_1x16(const uint16_t* x, int64_t T, int64_t N, bool colwise, bool rht, uint64_t rht_seed,
+                              bool sr, uint64_t sr_seed, uint8_t* q, uint8_t* s, float* s_tensor, uint32_t* ws,
+                              int num_sms, cudaStream_t stream) {
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return e;
+    const int64_t srows = colwise ? N : T, sk = colwise ? T : N;
+    if ((srows % 128) != 0 || ((sk / 16) % 4) != 0) {
+        e = cudaMemsetAsync(s, 0, (size_t)host_scale_bytes(srows, sk, 16), stream);
+        if (e != cudaSuccess) return e;
+    }
+    if (colwise) {
+        const uint32_t mask = rht ? host_rht_sign_mask(rht_seed) : 0u;
+        dim3 grid((unsigned)((N + CW_COLS - 1) / CW_COLS), (unsigned)((T + CW_TOK - 1) / CW_TOK));
+        if (rht) colwise_amax_kernel<true><<<grid, CW_THREADS, 0, stream>>>(x, T, N, mask, ws);
+        else colwise_amax_kernel<false><<<grid, CW_THREADS, 0, stream>>>(x, T, N, mask, ws);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (rht && sr) colwise_quant_kernel<true, true><<<grid, CW_THREADS, 0, stream>>>(x, T, N, mask, ws, sr_seed, q, s, s_tensor);
+        else if (rht) colwise_quant_kernel<true, false><<<grid, CW_THREADS, 0, stream>>>(x, T, N, mask, ws, sr_seed, q, s, s_tensor);
+        else if (sr) colwise_quant_kernel<false, true><<<grid, CW_THREADS, 0, stream>>>(x, T, N, mask, ws, sr_seed, q, s, s_tensor);
+        else colwise_quant_kernel<false, false><<<grid, CW_THREADS, 0, stream>>>(x, T, N, mask, ws, sr_seed, q, s, s_tensor);
+    } else {
+        amax_kernel<<<num_sms * 4, 256, 0, stream>>>(x, T * N, ws);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        const unsigned grid = (unsigned)((T + RW_WARPS - 1) / RW_WARPS);
+        if (sr) nvfp4_rowwise_kernel<true, true><<<grid, RW_WARPS * 32, 0, stream>>>(x, T, N, N, q, s, nullptr, ws, s_tensor, sr_seed);
+        else nvfp4_rowwise_kernel<true, false><<<grid, RW_WARPS * 32, 0, stream>>>(x, T, N, N, q, s, nullptr, ws, s_tensor, sr_seed);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rht16(const uint16_t* x, int64_t T, int64_t N, uint64_t seed, uint16_t* y, cudaStream_t stream) {
+    const int64_t threads = (T / 16) * (N / 8);
+    const unsigned grid = (unsigned)((threads + 255) / 256);
+    rht16_kernel<<<grid, 256, 0, stream>>>(x, T, N, host_rht_sign_mask(seed), y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_nvfp4_weight_2d(const uint16_t* w, int64_t G, int64_t O, int64_t H, uint8_t* q_row, uint8_t* s_row,
+                                   uint8_t* q_col, uint8_t* s_col, float* s_w, uint32_t* ws, int num_sms,
+                                   cudaStream_t stream) {
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t) * (size_t)G, stream);
+    if (e != cudaSuccess) return e;
+    if ((O % 128) != 0 || ((H / 16) % 4) != 0) {
+        e = cudaMemsetAsync(s_row, 0, (size_t)(host_scale_bytes(O, H, 16) * G), stream);
+        if (e != cudaSuccess) return e;
+    }
+    if ((H % 128) != 0 || ((O / 16) % 4) != 0) {
+        e = cudaMemsetAsync(s_col, 0, (size_t)(host_scale_bytes(H, O, 16) * G), stream);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t per = O * H;
+    int64_t bx = (per / 8 + 255) / 256;
+    const int64_t cap = max64(1, (int64_t)num_sms * 8 / max64(G, 1));
+    if (bx > cap) bx = cap;
+    matrix_amax_kernel<<<dim3((unsigned)bx, (unsigned)G), 256, 0, stream>>>(w, per, ws);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    dim3 grid((unsigned)((H + W2_COLS - 1) / W2_COLS), (unsigned)((O + W2_ROWS - 1) / W2_ROWS), (unsigned)G);
+    weight2d_quant_kernel<<<grid, 128, 0, stream>>>(w, O, H, ws, q_row, s_row, q_col, s_col, s_w);
+    return cudaGetLastError();
+}
+
+}  // namespace mxk

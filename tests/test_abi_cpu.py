@@ -1,0 +1,111 @@
+"""The C ABI loads and exports every symbol include/mxnum.h declares, and host-side validation
+returns the documented status codes before anything touches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxnum.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from microscaled_precision_numerics_gb300 import _build
+    import microscaled_precision_numerics_gb300 as mx
+    _build.build()
+    return mx.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mx_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["mx_quantize_mxfp8", "mx_nvfp4_quantize_per_token", "mx_nvfp4_quantize_weight_2d", "mx_rht16",
+                     "mx_nvfp4_quantize_1x16", "mx_dequantize_bf16", "mx_scaled_gemm", "mx_grouped_scaled_gemm"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, text in [(0, b"MX_OK"), (1, b"MX_ERR_INVALID_ARG"), (2, b"MX_ERR_ALIGNMENT"), (3, b"MX_ERR_UNSUPPORTED"),
+                       (4, b"MX_ERR_CUDA"), (5, b"MX_ERR_TIMEOUT")]:
+        assert lib.mx_status_string(code) == text
+
+
+def test_scale_and_workspace_sizes(lib):
+    assert lib.mx_scale_bytes(256, 1024, 32) == 2 * 8 * 512
+    assert lib.mx_scale_bytes(130, 48, 16) == 2 * 1 * 512
+    assert lib.mx_scale_bytes(1, 16, 16) == 512
+    assert lib.mx_scale_bytes(0, 16, 16) == 0
+    assert lib.mx_scale_bytes(16, 16, 8) == 0
+    assert lib.mx_workspace_bytes(0, 128, 0) == 512
+    assert lib.mx_workspace_bytes(1, 0, 0) == 16
+
+
+# Fake, never-dereferenced device addresses: validation must reject before any launch.
+A16 = ctypes.c_void_p(0x10000)
+A8 = ctypes.c_void_p(0x10008)
+NUL = None
+
+
+def test_mxfp8_validation(lib):
+    f = lib.mx_quantize_mxfp8
+    assert f(NUL, 32, 32, 32, A16, A16, NUL, NUL, NUL) == 1            # null input
+    assert f(A16, 32, 32, 32, NUL, NUL, NUL, NUL, NUL) == 1            # no output
+    assert f(A16, 32, 32, 32, A16, NUL, NUL, NUL, NUL) == 1            # codes without scales
+    assert f(A8, 32, 32, 32, A16, A16, NUL, NUL, NUL) == 2             # misaligned input
+    assert f(A16, 32, 48, 48, A16, A16, NUL, NUL, NUL) == 3            # cols % 32
+    assert f(A16, 48, 32, 32, NUL, NUL, A16, A16, NUL) == 3            # rows % 32 for column-wise
+    assert f(A16, 32, 36, 36, A16, A16, NUL, NUL, NUL) == 2            # cols % 8 (16-byte rows)
+    assert f(A16, -1, 32, 32, A16, A16, NUL, NUL, NUL) == 1
+
+
+def test_nvfp4_validation(lib):
+    assert lib.mx_nvfp4_quantize_per_token(A16, 4, 24, 24, A16, A16, A16, NUL) == 3
+    assert lib.mx_nvfp4_quantize_per_token(A16, 4, 32, 32, A16, A16, NUL, NUL) == 1
+    assert lib.mx_nvfp4_quantize_weight_2d(A16, 1, 24, 32, A16, A16, A16, A16, A16, A16, 16, NUL) == 3
+    assert lib.mx_nvfp4_quantize_weight_2d(A16, 4, 32, 32, A16, A16, A16, A16, A16, A16, 8, NUL) == 1
+    assert lib.mx_rht16(A16, 24, 8, 0, ctypes.c_void_p(0x20000), NUL) == 3
+    assert lib.mx_rht16(A16, 32, 8, 0, A16, NUL) == 1                   # in place not allowed
+    assert lib.mx_nvfp4_quantize_1x16(A16, 32, 32, 0, 1, 0, 0, 0, A16, A16, A16, A16, 16, NUL) == 3   # row-wise RHT
+    assert lib.mx_nvfp4_quantize_1x16(A16, 40, 32, 1, 0, 0, 0, 0, A16, A16, A16, A16, 16, NUL) == 3   # T % 16
+    assert lib.mx_nvfp4_quantize_1x16(A16, 32, 32, 1, 0, 0, 7, 0, A16, A16, A16, A16, 16, NUL) == 1   # bad rounding
+    assert lib.mx_nvfp4_quantize_1x16(A16, 32, 32, 1, 0, 0, 0, 0, A16, A16, A16, A16, 4, NUL) == 1    # workspace
+
+
+def test_gemm_validation(lib):
+    g = lib.mx_scaled_gemm
+    assert g(0, A16, A16, NUL, 0, A16, A16, NUL, 0, 128, 128, 96, A16, 128, NUL) == 3   # K % 128 (MXFP8)
+    assert g(1, A16, A16, NUL, 0, A16, A16, NUL, 0, 128, 128, 128, A16, 128, NUL) == 3  # K % 256 (NVFP4)
+    assert g(2, A16, A16, NUL, 0, A16, A16, NUL, 0, 128, 128, 128, A16, 128, NUL) == 1  # bad format
+    assert g(0, A16, A16, NUL, 2, A16, A16, NUL, 0, 128, 128, 128, A16, 128, NUL) == 1  # scope without pointer
+    assert g(0, A8, A16, NUL, 0, A16, A16, NUL, 0, 128, 128, 128, A16, 128, NUL) == 2
+    assert g(0, A16, A16, NUL, 0, A16, A16, NUL, 0, 128, 128, 128, A16, 100, NUL) == 1  # ldd < N
+    gg = lib.mx_grouped_scaled_gemm
+    assert gg(1, 0, A16, 16, A16, A16, NUL, A16, A16, NUL, 256, 256, A16, NUL) == 1      # G = 0
+    assert gg(1, 5000, A16, 16, A16, A16, NUL, A16, A16, NUL, 256, 256, A16, NUL) == 1   # too many groups
+    assert gg(1, 4, A16, 16, A16, A16, NUL, A16, A16, NUL, 256, 200, A16, NUL) == 3      # K % 256
+
+
+def test_mismatch_validation(lib):
+    assert lib.mx_count_mismatch(A16, A16, -1, A16, NUL) == 1
+    assert lib.mx_count_mismatch(A8, A16, 16, A16, NUL) == 2
+    assert lib.mx_count_mismatch(A16, A16, 0, A16, NUL) == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import microscaled_precision_numerics_gb300 as mx
+    x = torch.zeros((32, 32), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mx.mx_quantize_mxfp8(x, q_row=torch.zeros((32, 32), dtype=torch.uint8), s_row=torch.zeros(512, dtype=torch.uint8))

@@ -1,0 +1,257 @@
+"""GPU parity: quantizers, RHT, dequantize and the byte comparator against the CPU oracle.
+
+Bit-exact for every code, scale byte (including the zero padding of the GEMM layout) and FP32
+second-level scale, SR included.  Shapes span several CTA tiles and ragged tails; inputs include
+zero blocks, subnormals, the largest finite BF16 values and negative zeros (the pages' quantizer
+contract: random values, boundary cases, zero tensors and max-representable values).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from gpu_util import DEV, bf16_dev, first_mismatch, to_np, to_np_u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import microscaled_precision_numerics_gb300 as m
+    m.lib()
+    return m
+
+
+def edge_tensor(seed, shape):
+    """Random values with planted boundary cases."""
+    rng = np.random.default_rng(seed)
+    x = synthetic.random_bf16(seed, shape, "student_t")
+    flat = x.reshape(-1)
+    n = flat.size
+    idx = rng.choice(n, size=min(n, 64), replace=False)
+    specials = np.array([0x7F7F, 0xFF7F, 0x0001, 0x8001, 0x007F, 0x8000, 0x0000, 0x0080, 0x3F80, 0x4380,
+                         0x43E0, 0x43E1, 0xC3E0], dtype=np.uint16)   # max, -max, subnormals, -0, 0, 1, 256, 448
+    flat[idx] = specials[np.arange(idx.size) % specials.size]
+    return x
+
+
+# ------------------------------------------------------------------------------------------------
+# MXFP8
+# ------------------------------------------------------------------------------------------------
+MXFP8_SHAPES = [(256, 1024), (512, 1024), (96, 160), (32, 32), (160, 64), (384, 416), (992, 96)]
+
+
+@pytest.mark.parametrize("shape", MXFP8_SHAPES)
+def test_mxfp8_row_and_col(mx, orc, shape):
+    R, K = shape
+    x = synthetic.tiny(rows=R, cols=K, out_features=32)["x"] if shape == (256, 1024) else edge_tensor(R * 7 + K, shape)
+    if R % 32:
+        pytest.skip("column-wise needs rows % 32 == 0")
+    out = mx.alloc_mxfp8(R, K, DEV)
+    for v in out.values():
+        v.fill_(0xAB)          # the quantizer must overwrite every byte, padding included
+    mx.mx_quantize_mxfp8(bf16_dev(x), **out)
+    torch.cuda.synchronize()
+    qr, sr = orc.mxfp8_quantize_rowwise(x)
+    qc, sc = orc.mxfp8_quantize_colwise(x)
+    assert np.array_equal(to_np(out["q_row"]), qr), first_mismatch(to_np(out["q_row"]), qr)
+    assert np.array_equal(to_np(out["s_row"]), orc.scales_to_gemm_layout(sr))
+    assert np.array_equal(to_np(out["q_col"]), qc), first_mismatch(to_np(out["q_col"]), qc)
+    assert np.array_equal(to_np(out["s_col"]), orc.scales_to_gemm_layout(sc))
+
+
+def test_mxfp8_rowwise_only_ragged_rows(mx, orc):
+    x = edge_tensor(5, (37, 96))
+    out = mx.alloc_mxfp8(37, 96, DEV, colwise=False)
+    out["s_row"].fill_(0xCD)
+    mx.mx_quantize_mxfp8(bf16_dev(x), **out)
+    qr, sr = orc.mxfp8_quantize_rowwise(x)
+    assert np.array_equal(to_np(out["q_row"]), qr)
+    assert np.array_equal(to_np(out["s_row"]), orc.scales_to_gemm_layout(sr))
+
+
+def test_mxfp8_strided_input(mx, orc):
+    base = edge_tensor(6, (64, 192))
+    xt = bf16_dev(base)[:, :128]          # ldx = 192
+    out = mx.alloc_mxfp8(64, 128, DEV)
+    mx.mx_quantize_mxfp8(xt, **out)
+    sub = np.ascontiguousarray(base[:, :128])
+    qr, sr = orc.mxfp8_quantize_rowwise(sub)
+    qc, sc = orc.mxfp8_quantize_colwise(sub)
+    assert np.array_equal(to_np(out["q_row"]), qr)
+    assert np.array_equal(to_np(out["q_col"]), qc)
+
+
+def test_mxfp8_zero_tensor(mx, orc):
+    x = np.zeros((64, 64), dtype=np.uint16)
+    out = mx.alloc_mxfp8(64, 64, DEV)
+    mx.mx_quantize_mxfp8(bf16_dev(x), **out)
+    assert int(out["q_row"].sum()) == 0 and int(out["s_row"].sum()) == 0 and int(out["q_col"].sum()) == 0
+
+
+def test_mxfp8_negative_zero_and_tiny_negatives(mx, orc):
+    row = np.full(32, 0x8000, dtype=np.uint16)      # -0
+    row[0] = 0x4300                                   # 128 (sets the block scale)
+    row[1:8] = 0x8001                                 # tiny negative subnormals -> round to -0
+    x = np.tile(row, (32, 1))
+    out = mx.alloc_mxfp8(32, 32, DEV)
+    mx.mx_quantize_mxfp8(bf16_dev(x), **out)
+    qr, _ = orc.mxfp8_quantize_rowwise(x)
+    assert np.array_equal(to_np(out["q_row"]), qr), first_mismatch(to_np(out["q_row"]), qr)
+
+
+# ------------------------------------------------------------------------------------------------
+# NVFP4 per-token
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(256, 1024), (100, 48), (65, 768), (8, 2048), (300, 4160)])
+def test_nvfp4_per_token(mx, orc, shape):
+    T, H = shape
+    x = edge_tensor(T + 3 * H, shape)
+    x[min(2, T - 1)] = 0                              # a zero token
+    out = mx.alloc_nvfp4_rows(T, H, DEV)
+    out["s"].fill_(0xEE)
+    mx.mx_nvfp4_quantize_per_token(bf16_dev(x), out["q"], out["s"], out["s2"])
+    q, s, st = orc.nvfp4_quantize_per_token(x)
+    assert np.array_equal(to_np(out["q"]), q), first_mismatch(to_np(out["q"]), q)
+    assert np.array_equal(to_np(out["s"]), orc.scales_to_gemm_layout(s))
+    assert np.array_equal(to_np(out["s2"]).view(np.uint32), st.view(np.uint32))
+
+
+def test_nvfp4_per_token_moe_gather_commutes(mx, orc):
+    """quantize(gather(X)) == gather(quantize(X)) on the device (per-token scaling)."""
+    d = synthetic.moe(tokens=256, hidden=512, ffn=128, experts=16, topk=4, with_weights=False)
+    x = d["x"]
+    xg = np.ascontiguousarray(x[d["row_token"]])
+    out = mx.alloc_nvfp4_rows(xg.shape[0], 512, DEV)
+    mx.mx_nvfp4_quantize_per_token(bf16_dev(xg), out["q"], out["s"], out["s2"])
+    q, s, st = orc.nvfp4_quantize_per_token(x)
+    assert np.array_equal(to_np(out["q"]), q[d["row_token"]])
+    assert np.array_equal(to_np(out["s2"]), st[d["row_token"]])
+
+
+# ------------------------------------------------------------------------------------------------
+# NVFP4 per-tensor 1x16 (column-wise with RHT / SR, row-wise)
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(256, 512), (48, 40), (1040, 264), (4096, 64)])
+@pytest.mark.parametrize("rht,sr", [(False, False), (True, False), (False, True), (True, True)])
+def test_nvfp4_colwise(mx, orc, shape, rht, sr):
+    T, N = shape
+    x = edge_tensor(T * 13 + N + rht * 2 + sr, shape) if not rht else synthetic.random_bf16(T + N, shape, "student_t")
+    q = torch.empty((N, T // 2), dtype=torch.uint8, device=DEV)
+    s = torch.full((mx.scale_bytes(N, T, 16),), 0x5A, dtype=torch.uint8, device=DEV)
+    S = torch.empty(1, dtype=torch.float32, device=DEV)
+    ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+    mx.mx_nvfp4_quantize_1x16(bf16_dev(x), True, rht, 8, sr, 9, q, s, S, ws)
+    qo, so, So = orc.nvfp4_quantize_1x16(x, colwise=True, rht=rht, rht_seed=8, sr=sr, sr_seed=9)
+    assert to_np(S).view(np.uint32)[0] == np.float32(So).view(np.uint32)
+    assert np.array_equal(to_np(q), qo), first_mismatch(to_np(q), qo)
+    assert np.array_equal(to_np(s), orc.scales_to_gemm_layout(so))
+
+
+@pytest.mark.parametrize("sr", [False, True])
+def test_nvfp4_rowwise_per_tensor(mx, orc, sr):
+    x = edge_tensor(77, (130, 96))
+    q = torch.empty((130, 48), dtype=torch.uint8, device=DEV)
+    s = torch.empty(mx.scale_bytes(130, 96, 16), dtype=torch.uint8, device=DEV)
+    S = torch.empty(1, dtype=torch.float32, device=DEV)
+    ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+    mx.mx_nvfp4_quantize_1x16(bf16_dev(x), False, False, 0, sr, 1234, q, s, S, ws)
+    qo, so, So = orc.nvfp4_quantize_1x16(x, colwise=False, sr=sr, sr_seed=1234)
+    assert to_np(S)[0] == So
+    assert np.array_equal(to_np(q), qo), first_mismatch(to_np(q), qo)
+    assert np.array_equal(to_np(s), orc.scales_to_gemm_layout(so))
+
+
+@pytest.mark.parametrize("shape", [(64, 48), (256, 1024), (32, 8)])
+def test_rht16(mx, orc, shape):
+    x = synthetic.random_bf16(sum(shape), shape, "student_t")
+    y = torch.empty(shape, dtype=torch.bfloat16, device=DEV)
+    mx.mx_rht16(bf16_dev(x), 8, y)
+    assert np.array_equal(to_np_u16(y), orc.rht16(x, 8))
+
+
+# ------------------------------------------------------------------------------------------------
+# NVFP4 2D weights
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("G,O,H", [(3, 48, 80), (2, 256, 512), (1, 1536, 2048), (2, 2048, 768), (1, 16, 16)])
+def test_nvfp4_weight_2d(mx, orc, G, O, H):
+    w = synthetic.random_bf16(G * O + H, (G, O, H), "normal", 0.02)
+    w[0, 0, :16] = 0x7F7F if O * H < 10000 else w[0, 0, :16]
+    out = mx.alloc_nvfp4_weight_2d(G, O, H, DEV)
+    out["s_row"].fill_(0x33)
+    out["s_col"].fill_(0x44)
+    mx.mx_nvfp4_quantize_weight_2d(bf16_dev(w), out["q_row"], out["s_row"], out["q_col"], out["s_col"], out["s_w"],
+                                   out["ws"])
+    srb = orc.scale_layout_bytes(O, (H // 16))
+    scb = orc.scale_layout_bytes(H, (O // 16))
+    for g in range(G):
+        qr, qc, st, sw = orc.nvfp4_quantize_weight_2d(np.ascontiguousarray(w[g]))
+        assert np.array_equal(to_np(out["q_row"][g]), qr), first_mismatch(to_np(out["q_row"][g]), qr)
+        assert np.array_equal(to_np(out["q_col"][g]), qc), first_mismatch(to_np(out["q_col"][g]), qc)
+        assert np.array_equal(to_np(out["s_row"][g * srb:(g + 1) * srb]),
+                              orc.scales_to_gemm_layout(orc.weight_2d_operand_scales(st, "row")))
+        assert np.array_equal(to_np(out["s_col"][g * scb:(g + 1) * scb]),
+                              orc.scales_to_gemm_layout(orc.weight_2d_operand_scales(st, "col")))
+        assert to_np(out["s_w"])[g] == sw
+
+
+# ------------------------------------------------------------------------------------------------
+# Dequantize (fed the oracle's codes, so it is checked independently of the GPU quantizers)
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(256, 1024), (130, 96)])
+def test_dequant_mxfp8(mx, orc, shape):
+    R, K = shape
+    x = edge_tensor(R + K, shape)
+    q, s = orc.mxfp8_quantize_rowwise(x)
+    y = torch.empty(shape, dtype=torch.bfloat16, device=DEV)
+    mx.mx_dequantize_bf16(mx.MX_FMT_MXFP8, torch.from_numpy(q).to(DEV),
+                          torch.from_numpy(orc.scales_to_gemm_layout(s)).to(DEV), None, 0, R, K, y)
+    ref = orc.dequant_mxfp8(q, s)
+    assert np.array_equal(to_np_u16(y), ref), first_mismatch(to_np_u16(y), ref)
+
+
+@pytest.mark.parametrize("per_row", [True, False])
+def test_dequant_nvfp4(mx, orc, per_row):
+    x = edge_tensor(99, (200, 320))
+    if per_row:
+        q, s, s2 = orc.nvfp4_quantize_per_token(x)
+    else:
+        q, s, s2 = orc.nvfp4_quantize_1x16(x, colwise=False)
+        s2 = np.array([s2], dtype=np.float32)
+    y = torch.empty((200, 320), dtype=torch.bfloat16, device=DEV)
+    mx.mx_dequantize_bf16(mx.MX_FMT_NVFP4, torch.from_numpy(q).to(DEV),
+                          torch.from_numpy(orc.scales_to_gemm_layout(s)).to(DEV), torch.from_numpy(s2).to(DEV),
+                          mx.MX_SCOPE_ROW if per_row else mx.MX_SCOPE_TENSOR, 200, 320, y)
+    ref = orc.dequant_nvfp4(q, s, s2, per_row=per_row)
+    assert np.array_equal(to_np_u16(y), ref), first_mismatch(to_np_u16(y), ref)
+
+
+def test_weight_sync_round_trip_on_device(mx, orc):
+    """Q -> DQ -> Q on the device reproduces the bytes (the weight-sync invariant) and the byte
+    comparator counts exactly the planted differences."""
+    w = synthetic.random_bf16(123, (512, 768), "normal", 0.02)
+    wd = bf16_dev(w)
+    a = mx.alloc_mxfp8(512, 768, DEV, colwise=False)
+    mx.mx_quantize_mxfp8(wd, **a)
+    y = torch.empty((512, 768), dtype=torch.bfloat16, device=DEV)
+    mx.mx_dequantize_bf16(mx.MX_FMT_MXFP8, a["q_row"], a["s_row"], None, 0, 512, 768, y)
+    b = mx.alloc_mxfp8(512, 768, DEV, colwise=False)
+    mx.mx_quantize_mxfp8(y, **b)
+    cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
+    mx.mx_count_mismatch(a["q_row"], b["q_row"], cnt)
+    mx.mx_count_mismatch(a["s_row"], b["s_row"], cnt)
+    assert int(cnt.item()) == 0
+    c = b["q_row"].clone()
+    c.view(-1)[torch.tensor([0, 5, 777, 512 * 768 - 1], device=DEV)] ^= 1
+    cnt.zero_()
+    mx.mx_count_mismatch(a["q_row"], c, cnt)
+    assert int(cnt.item()) == 4
+    # odd byte counts use the scalar tail
+    cnt.zero_()
+    mx.mx_count_mismatch(a["q_row"].view(-1)[:1001], c.view(-1)[:1001], cnt)
+    assert int(cnt.item()) == 3
+
+
+def test_device_status_clean(mx):
+    torch.cuda.synchronize()
+    mx.check_device_status()
