@@ -1,0 +1,422 @@
+#!/usr/bin/env python
+"""Benchmark of the block-scaled microscaling hot path on GB300.
+
+Default step (workload ``dense_mlp``, the Qwen3-8B-shaped MLP linear): MXFP8 row-wise + column-wise
+quantization of X [8192, 4096], W [12288, 4096] and dY [8192, 12288], then the three MXFP8
+block-scaled GEMMs FPROP (Y = X W^T), DGRAD (dX = dY W) and WGRAD (dW = dY^T X) with BF16 output.
+The metric is the step's GEMM throughput with its quantization included: 2.474 TFLOP per step /
+step time.  Other workloads (``--workload moe|wgrad|weight_sync``) time the NVFP4 paths.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxnum|reference] [--workload ...]
+
+Under torchrun (N > 1) every rank runs an independent replica of the step (the path has no
+exchange step); the reported value is all ranks' work over the slowest rank's time.  ``--impl
+reference`` times the CPU oracle on a bounded sample of the same workload on this host's cores.
+One JSON line is printed by rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quantize GB/s vs ~8 TB/s HBM; MXFP8/NVFP4 scaled-GEMM TFLOP/s vs dense peak"
+FP8_OVER_BF16 = 2.0      # nominal dense ratio: 4.5 / 2.25 PFLOP/s
+FP4_OVER_BF16 = 6.0      # nominal dense ratio: 13.5 / 2.25 PFLOP/s
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks sampling during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mxnum_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu_index), "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for r in csv.reader(f):
+                if len(r) >= 9:
+                    rows.append([c.strip() for c in r])
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        # samples under load: power above the midpoint of the observed range
+        if power:
+            thr = (max(power) + min(power)) / 2
+            loaded = [float(r[1]) for r in rows if r[3].replace(".", "").isdigit() and float(r[3]) >= thr
+                      and r[1].replace(".", "").isdigit()]
+        else:
+            loaded = sm
+        return {"sm_mhz": statistics.median(loaded or sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------------------------------------
+# workloads on the device
+# ------------------------------------------------------------------------------------------------
+class DenseMLP:
+    """MXFP8 quantize X, W, dY (row + column) + FPROP, DGRAD, WGRAD (Qwen3-8B MLP shapes)."""
+    name = "dense_mlp"
+
+    def __init__(self, mx, torch, dev, tokens=8192, hidden=4096, ffn=12288, host_inputs=None):
+        import synthetic
+        self.mx, self.torch, self.dev = mx, torch, dev
+        self.T, self.H, self.F = tokens, hidden, ffn
+        data = host_inputs or synthetic.dense_mlp(tokens, hidden, ffn)
+        self.host = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) for k, v in data.items()}
+        self.x = self.host["x"].to(dev)
+        self.w = self.host["w"].to(dev)
+        self.dy = self.host["dy"].to(dev)
+        self.qx = mx.alloc_mxfp8(tokens, hidden, dev)
+        self.qw = mx.alloc_mxfp8(ffn, hidden, dev)
+        self.qdy = mx.alloc_mxfp8(tokens, ffn, dev)
+        self.y = torch.empty((tokens, ffn), dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty((tokens, hidden), dtype=torch.bfloat16, device=dev)
+        self.dw = torch.empty((ffn, hidden), dtype=torch.bfloat16, device=dev)
+        T, H, F = tokens, hidden, ffn
+        self.gemm_flops = [2.0 * T * F * H, 2.0 * T * H * F, 2.0 * F * H * T]
+        self.quant_elems = [T * H, F * H, T * F]
+        self.launches_per_step = 6
+
+    def ops(self):
+        """The step as a list of (kind, label, callable); kinds: quant / gemm."""
+        mx = self.mx
+        F8 = mx.MX_FMT_MXFP8
+        T, H, F = self.T, self.H, self.F
+        return [
+            ("quant", "mxfp8_quantize X", lambda: mx.mx_quantize_mxfp8(self.x, **self.qx)),
+            ("quant", "mxfp8_quantize W", lambda: mx.mx_quantize_mxfp8(self.w, **self.qw)),
+            ("quant", "mxfp8_quantize dY", lambda: mx.mx_quantize_mxfp8(self.dy, **self.qdy)),
+            ("gemm", "FPROP", lambda: mx.mx_scaled_gemm(F8, self.qx["q_row"], self.qx["s_row"], None, 0,
+                                                         self.qw["q_row"], self.qw["s_row"], None, 0, T, F, H, self.y)),
+            ("gemm", "DGRAD", lambda: mx.mx_scaled_gemm(F8, self.qdy["q_row"], self.qdy["s_row"], None, 0,
+                                                         self.qw["q_col"], self.qw["s_col"], None, 0, T, H, F, self.dx)),
+            ("gemm", "WGRAD", lambda: mx.mx_scaled_gemm(F8, self.qdy["q_col"], self.qdy["s_col"], None, 0,
+                                                         self.qx["q_col"], self.qx["s_col"], None, 0, F, H, T, self.dw)),
+        ]
+
+    def units_per_step(self):
+        return sum(self.gemm_flops) / 1e12      # TFLOP
+
+    def quant_bytes(self):
+        # row + column copies: 2 B read + 2 x 1 B codes + 2 x 1/32 B scales per element
+        return [e * (2 + 2 + 2 / 32) for e in self.quant_elems]
+
+    # end-to-end: inputs from pinned host memory, results back to pinned host memory
+    def e2e_setup(self):
+        t = self.torch
+        self.hx = self.host["x"].pin_memory()
+        self.hw = self.host["w"].pin_memory()
+        self.hdy = self.host["dy"].pin_memory()
+        self.hy = t.empty(self.y.shape, dtype=t.bfloat16).pin_memory()
+        self.hdx = t.empty(self.dx.shape, dtype=t.bfloat16).pin_memory()
+        self.hdw = t.empty(self.dw.shape, dtype=t.bfloat16).pin_memory()
+        self.h2d = sum(a.numel() * 2 for a in (self.hx, self.hw, self.hdy))
+        self.d2h = sum(a.numel() * 2 for a in (self.hy, self.hdx, self.hdw))
+
+    def e2e_step(self):
+        self.x.copy_(self.hx, non_blocking=True)
+        self.w.copy_(self.hw, non_blocking=True)
+        self.dy.copy_(self.hdy, non_blocking=True)
+        for _, _, f in self.ops():
+            f()
+        self.hy.copy_(self.y, non_blocking=True)
+        self.hdx.copy_(self.dx, non_blocking=True)
+        self.hdw.copy_(self.dw, non_blocking=True)
+
+
+def time_device(work, torch, steps, warmup, dist=None):
+    """Warm up, then time `steps` steps with CUDA events on the current stream; per-op events too."""
+    ops = work.ops()
+    for _ in range(warmup):
+        for _, _, f in ops:
+            f()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n = len(ops)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for s in range(steps):
+        e = evs[s]
+        e[0].record()
+        for i, (_, _, f) in enumerate(ops):
+            f()
+            e[i + 1].record()
+    end.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    per_op = [statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)) for i in range(n)]
+    return total_ms, per_op
+
+
+def run_device(args):
+    import torch
+    import microscaled_precision_numerics_gb300 as mx
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as td
+        td.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+        dist = td
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    mx.lib()
+
+    # the CPU baseline runs before any GPU work (oracle threads, no forked pool after CUDA init)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload)
+
+    work = DenseMLP(mx, torch, dev)
+    peaks = load_peaks()
+    sampler = ClockSampler(local)
+    sampler.start()
+    total_ms, per_op = time_device(work, torch, args.steps, args.warmup, dist)
+    clocks = sampler.stop()
+    mx.check_device_status()
+
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * work.units_per_step() / (ms_per_step / 1e3)
+
+    ops = work.ops()
+    gemm_ms = sum(per_op[i] for i, (k, _, _) in enumerate(ops) if k == "gemm")
+    quant_ms = sum(per_op[i] for i, (k, _, _) in enumerate(ops) if k == "quant")
+    gemm_tflops = sum(work.gemm_flops) / (gemm_ms / 1e3) / 1e12
+    quant_gbs = sum(work.quant_bytes()) / (quant_ms / 1e3) / 1e9
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    dominant = "gemm" if gemm_ms >= quant_ms else "quant"
+    if dominant == "gemm":
+        roofline = {"kernel": "bs_gemm_kernel<MXFP8> (FPROP+DGRAD+WGRAD)", "bound": "tensor",
+                    "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                    "frac": round(gemm_tflops / fp8_peak, 4), "traffic": None,
+                    "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16:g} (nominal FP8/BF16)"}
+    else:
+        roofline = {"kernel": "mxfp8_quantize_kernel", "bound": "hbm", "achieved": round(quant_gbs, 1),
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
+                    "traffic": None, "peak_source": f"{peaks['source']} copy bandwidth"}
+
+    e2e = None
+    if not args.no_e2e:
+        work.e2e_setup()
+        e2e_steps = max(1, min(args.steps, 20))
+        for _ in range(2):
+            work.e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(e2e_steps):
+            work.e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b) / e2e_steps
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(world * work.units_per_step() / (e_ms / 1e3), 2), "unit": "TFLOP/s",
+               "ms_per_step": round(e_ms, 3), "steps": e2e_steps,
+               "h2d_bytes_per_step": work.h2d, "d2h_bytes_per_step": work.d2h}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (f32 accumulate, bf16 out)",
+            "data": "synthetic (seeded numpy draws; no dataset or trained weights needed)",
+            "config": {"workload": "dense_mlp: Qwen3-8B MLP linear, MXFP8 quantize X/W/dY row+col + FPROP/DGRAD/WGRAD",
+                       "tokens": work.T, "hidden": work.H, "ffn": work.F, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (369 MB BF16 read per step, 129 MB L2)"},
+            "components": {
+                "quantize_ms": round(quant_ms, 4), "quantize_GBps": round(quant_gbs, 1),
+                "quantize_frac_hbm": round(quant_gbs / peaks["hbm_gbs"], 4),
+                "gemm_ms": round(gemm_ms, 4), "gemm_TFLOPs": round(gemm_tflops, 1),
+                "per_op_ms": {lbl: round(per_op[i], 4) for i, (_, lbl, _) in enumerate(ops)},
+                "per_gemm_TFLOPs": {lbl: round(work.gemm_flops[j] / (per_op[i] / 1e3) / 1e12, 1)
+                                    for j, (i, (_, lbl, _)) in enumerate([(i, o) for i, o in enumerate(ops) if o[0] == "gemm"])},
+            },
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": work.launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle (reported baseline / reference arm)
+# ------------------------------------------------------------------------------------------------
+SLICE = 8     # the oracle sample is 1/8 of the tokens and 1/8 of the output features
+
+
+def oracle_sample_step(orc, data):
+    """A proportional slice of the dense_mlp step: S = T/8 tokens and Fs = F/8 output features.
+    MXFP8 row+col quantization of X[:S], W[:Fs] and dY[:S, :Fs]; FP64 reference FPROP
+    (Y[:S, :Fs]), DGRAD (dX[:S] over K = Fs) and WGRAD (dW[:Fs] over K = S)."""
+    T, F = data["x"].shape[0], data["w"].shape[0]
+    S, Fs = T // SLICE, F // SLICE
+    x = np.ascontiguousarray(data["x"][:S])
+    w = np.ascontiguousarray(data["w"][:Fs])
+    dy = np.ascontiguousarray(data["dy"][:S, :Fs])
+    qx, sx = orc.mxfp8_quantize_rowwise(x)
+    qxc, sxc = orc.mxfp8_quantize_colwise(x)
+    qw, sw = orc.mxfp8_quantize_rowwise(w)
+    qwc, swc = orc.mxfp8_quantize_colwise(w)
+    qd, sd = orc.mxfp8_quantize_rowwise(dy)
+    qdc, sdc = orc.mxfp8_quantize_colwise(dy)
+    orc.gemm_ref_mxfp8(qx, sx, qw, sw)          # FPROP
+    orc.gemm_ref_mxfp8(qd, sd, qwc, swc)        # DGRAD
+    orc.gemm_ref_mxfp8(qdc, sdc, qxc, sxc)      # WGRAD
+    return 3 * 2.0 * S * Fs * x.shape[1]
+
+
+def sample_text(data):
+    T, H = data["x"].shape
+    F = data["w"].shape[0]
+    S, Fs = T // SLICE, F // SLICE
+    return (f"1/{SLICE} slice of the dense_mlp step: tokens [0, {S}) and output features [0, {Fs}); MXFP8 row+col "
+            f"quantize of X[:{S}], W[:{Fs}], dY[:{S}, :{Fs}] (C oracle, OpenMP) and FP64 FPROP/DGRAD/WGRAD "
+            f"references (numpy), {3 * 2.0 * S * Fs * H / 1e9:.1f} GFLOP")
+
+
+def cpu_baseline(workload: str, data=None):
+    import oracle as orc
+    import synthetic
+    orc.build()
+    cores = os.cpu_count() or 1
+    orc.set_threads(cores)
+    if data is None:
+        data = synthetic.dense_mlp()
+    t0 = time.perf_counter()
+    flops = oracle_sample_step(orc, data)
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "seconds": round(dt, 2), "sample": sample_text(data)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle as orc
+    import synthetic
+    orc.build()
+    cores = os.cpu_count() or 1
+    orc.set_threads(cores)
+    data = synthetic.dense_mlp()
+    for _ in range(args.warmup):
+        oracle_sample_step(orc, data)
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        flops = oracle_sample_step(orc, data)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms / 1e3) / 1e12
+    T, H = data["x"].shape
+    F = data["w"].shape[0]
+    line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64 (oracle)", "data": "synthetic",
+            "config": {"workload": "dense_mlp: Qwen3-8B MLP linear, MXFP8 quantize X/W/dY row+col + FPROP/DGRAD/WGRAD",
+                       "tokens": T, "hidden": H, "ffn": F, "parallelism": "cpu"},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample_text(data)},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mxnum", "reference"], default="mxnum")
+    ap.add_argument("--workload", choices=["dense_mlp"], default="dense_mlp")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_device(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -150,7 +150,8 @@ mx_status mx_dequantize_bf16(mx_format fmt, const uint8_t* q, const uint8_t* s, 
  *   alpha_a: NULL / MX_SCOPE_NONE (1), one FP32 (MX_SCOPE_TENSOR) or M FP32 (MX_SCOPE_ROW); alpha_b
  *   likewise with N.  d [M, ldd] BF16.
  * FP32 accumulation inside the tensor core; the summation order is the hardware's.  Requires
- * K % 128 (MXFP8) or K % 256 (NVFP4) == 0; M, N >= 1; ldd % 8 == 0. */
+ * K % 128 (MXFP8) or K % 256 (NVFP4) == 0; M, N >= 1; ldd >= N (rows of d start 16-byte aligned
+ * when ldd % 8 == 0, which takes the vector-store epilogue; any other ldd uses 2-byte stores). */
 mx_status mx_scaled_gemm(mx_format fmt,
                          const uint8_t* a, const uint8_t* sa, const float* alpha_a, mx_scope alpha_a_scope,
                          const uint8_t* b, const uint8_t* sb, const float* alpha_b, mx_scope alpha_b_scope,

@@ -431,7 +431,7 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     packed[i] = pack_bf16x2(f0, f1);
                 }
-                if (nb + 32 <= p.N) {
+                if (nb + 32 <= p.N && (p.ldd & 7) == 0) {
                     uint4* dst = reinterpret_cast<uint4*>(drow + nb);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)

@@ -161,7 +161,6 @@ mx_status mx_scaled_gemm(mx_format fmt, const uint8_t* a, const uint8_t* sa, con
     mx_status st = validate_gemm_common(fmt, a, sa, b, sb, N, K, d);
     if (st != MX_OK) return st;
     if (M <= 0 || ldd < N) return MX_ERR_INVALID_ARG;
-    if ((ldd % 8) != 0) return MX_ERR_ALIGNMENT;
     if ((alpha_a_scope != MX_SCOPE_NONE && !alpha_a) || (alpha_b_scope != MX_SCOPE_NONE && !alpha_b))
         return MX_ERR_INVALID_ARG;
     if (alpha_a_scope < MX_SCOPE_NONE || alpha_a_scope > MX_SCOPE_ROW || alpha_b_scope < MX_SCOPE_NONE ||
