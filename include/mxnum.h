@@ -100,6 +100,24 @@ mx_status mx_nvfp4_quantize_weight_2d(const void* w, int64_t G, int64_t O, int64
                                       float* s_w, void* workspace, size_t workspace_bytes,
                                       cudaStream_t stream);
 
+/* Allocation-free variant of mx_nvfp4_quantize_weight_2d (the pages have no counterpart: it exists
+ * for callers that cannot allocate device memory, e.g. a plugin inside a host framework that owns
+ * all device memory, or a loop that must not call cudaMalloc because it synchronizes the device).
+ * Same arguments, results and rules as mx_nvfp4_quantize_weight_2d, without the workspace: the
+ * per-matrix scratch is a fixed array of MX_NOALLOC_MAX_MATRICES 32-bit words (16 KiB) inside the
+ * library, which every GPU that loads the library keeps until the process exits.
+ *   - G > MX_NOALLOC_MAX_MATRICES is rejected with MX_ERR_UNSUPPORTED (nothing is enqueued).
+ *   - The first call on each device looks up the scratch address on the host (once per device);
+ *     make that first call before any stream capture.
+ *   - The call itself allocates nothing.  It clears the scratch it uses on `stream` before use.
+ *   - All calls share the one array: calls that may overlap on the GPU (different streams, or
+ *     different host threads, without ordering between them) race and must be serialized by the
+ *     caller. */
+#define MX_NOALLOC_MAX_MATRICES 4096
+mx_status mx_nvfp4_quantize_weight_2d_noalloc(const void* w, int64_t G, int64_t O, int64_t H,
+                                              uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                              float* s_w, cudaStream_t stream);
+
 /* 16-point random Hadamard transform along the token dimension.
  * Source: MaxText page, "NVFP4 pretraining recipe" -- a random Hadamard transform on the WGRAD
  * inputs only, to Gaussianize outliers before 4-bit quantization.

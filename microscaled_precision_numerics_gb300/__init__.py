@@ -21,6 +21,7 @@ MX_FMT_MXFP8, MX_FMT_NVFP4 = 0, 1
 MX_ROUND_RNE, MX_ROUND_SR = 0, 1
 MX_SCOPE_NONE, MX_SCOPE_TENSOR, MX_SCOPE_ROW = 0, 1, 2
 MX_WS_WEIGHT_2D, MX_WS_1X16 = 0, 1
+MX_NOALLOC_MAX_MATRICES = 4096
 
 _lock = threading.Lock()
 _lib = None
@@ -126,6 +127,23 @@ def mx_nvfp4_quantize_weight_2d(w, q_row, s_row, q_col, s_col, s_w, workspace, s
     _check("mx_nvfp4_quantize_weight_2d", lib().mx_nvfp4_quantize_weight_2d(
         _p(w), G, O, H, _p(q_row), _p(s_row), _p(q_col), _p(s_col), _p(s_w), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mx_nvfp4_quantize_weight_2d_noalloc(w, q_row, s_row, q_col, s_col, s_w, stream=None):
+    """Same as mx_nvfp4_quantize_weight_2d without a workspace, for callers that cannot allocate
+    device memory: the library keeps the per-matrix scratch in a fixed internal array (at most
+    MX_NOALLOC_MAX_MATRICES matrices per call).  Calls that may overlap on the GPU share that array
+    and must be serialized by the caller."""
+    w = _bf16_bits(w)
+    G, O, H = w.shape
+    f = lib().mx_nvfp4_quantize_weight_2d_noalloc
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    f.restype = ctypes.c_int
+    f.argtypes = [P, I64, I64, I64, P, P, P, P, P, P]
+    if G > MX_NOALLOC_MAX_MATRICES:
+        raise ValueError(f"{G} matrices exceed the allocation-free limit of {MX_NOALLOC_MAX_MATRICES}")
+    _check("mx_nvfp4_quantize_weight_2d_noalloc", f(
+        _p(w), G, O, H, _p(q_row), _p(s_row), _p(q_col), _p(s_col), _p(s_w), _stream(stream)))
 
 
 def mx_rht16(x, seed: int, y, stream=None):
