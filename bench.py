@@ -181,6 +181,188 @@ class DenseMLP:
         self.hdw.copy_(self.dw, non_blocking=True)
 
 
+class MoE:
+    """Qwen3-30B-A3B expert layer, NVFP4 forward with dequantized-BF16 backward operands:
+    per-token quantize of the 65536 expert-sorted rows, 16x16 2D quantize of 128 experts' gate|up
+    (1536x2048) and down (2048x768) weights, the two grouped NVFP4 GEMMs, per-token quantize of the
+    down-projection input, and DQ(Q(w)) of both weight stacks."""
+    name = "moe"
+
+    def __init__(self, mx, torch, dev):
+        import synthetic
+        self.mx, self.torch, self.dev = mx, torch, dev
+        d = synthetic.moe()
+        bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        x = bf(d["x"])
+        self.rows = int(d["group_offsets"][-1])
+        # the expert-sorted activation rows are the GEMM's input (the routing gather is setup)
+        self.a = x.index_select(0, torch.from_numpy(d["row_token"]).to(dev)).contiguous()
+        self.down_in = bf(d["down_in"])
+        self.wgu = bf(d["w_gate_up"])
+        self.wd = bf(d["w_down"])
+        self.offs = torch.from_numpy(d["group_offsets"]).to(dev)
+        G, O1, H = self.wgu.shape
+        _, O2, F = self.wd.shape
+        self.G, self.H, self.F, self.O1, self.O2 = G, H, F, O1, O2
+        self.qa = mx.alloc_nvfp4_rows(self.rows, H, dev)
+        self.qdn = mx.alloc_nvfp4_rows(self.rows, F, dev)
+        self.qgu = mx.alloc_nvfp4_weight_2d(G, O1, H, dev)
+        self.qwd = mx.alloc_nvfp4_weight_2d(G, O2, F, dev)
+        self.y1 = torch.empty((self.rows, O1), dtype=torch.bfloat16, device=dev)
+        self.y2 = torch.empty((self.rows, O2), dtype=torch.bfloat16, device=dev)
+        self.dq_gu = torch.empty((G * O1, H), dtype=torch.bfloat16, device=dev)
+        self.dq_d = torch.empty((G * O2, F), dtype=torch.bfloat16, device=dev)
+        self.launches_per_step = 10
+
+    def ops(self):
+        mx, F4 = self.mx, self.mx.MX_FMT_NVFP4
+        G, H, F, O1, O2, R = self.G, self.H, self.F, self.O1, self.O2, self.rows
+        q = self.qgu
+        w = self.qwd
+        return [
+            ("quant", "nvfp4_per_token A", 1, R * H * (2 + 0.5 + 1 / 16) + 4 * R,
+             lambda: mx.mx_nvfp4_quantize_per_token(self.a, self.qa["q"], self.qa["s"], self.qa["s2"])),
+            ("quant", "nvfp4_weight_2d gate_up", 1, G * O1 * H * (2 + 1 + 2 / 16),
+             lambda: mx.mx_nvfp4_quantize_weight_2d(self.wgu, q["q_row"], q["s_row"], q["q_col"], q["s_col"], q["s_w"], q["ws"])),
+            ("quant", "nvfp4_weight_2d down", 1, G * O2 * F * (2 + 1 + 2 / 16),
+             lambda: mx.mx_nvfp4_quantize_weight_2d(self.wd, w["q_row"], w["s_row"], w["q_col"], w["s_col"], w["s_w"], w["ws"])),
+            ("gemm4", "grouped gate_up", 0, 2.0 * R * O1 * H,
+             lambda: mx.mx_grouped_scaled_gemm(F4, self.offs, self.qa["q"], self.qa["s"], self.qa["s2"], q["q_row"],
+                                               q["s_row"], q["s_w"], O1, H, self.y1)),
+            ("quant", "nvfp4_per_token down input", 1, R * F * (2 + 0.5 + 1 / 16) + 4 * R,
+             lambda: mx.mx_nvfp4_quantize_per_token(self.down_in, self.qdn["q"], self.qdn["s"], self.qdn["s2"])),
+            ("gemm4", "grouped down", 0, 2.0 * R * O2 * F,
+             lambda: mx.mx_grouped_scaled_gemm(F4, self.offs, self.qdn["q"], self.qdn["s"], self.qdn["s2"], w["q_row"],
+                                               w["s_row"], w["s_w"], O2, F, self.y2)),
+            ("dq", "dequantize gate_up DQ(Q(w))", 1, G * O1 * H * (0.5 + 1 / 16 + 2),
+             lambda: mx.mx_dequantize_bf16(F4, q["q_row"], q["s_row"], q["s_w"], mx.MX_SCOPE_GROUP, G * O1, H, self.dq_gu,
+                                           group_rows=O1)),
+            ("dq", "dequantize down DQ(Q(w))", 1, G * O2 * F * (0.5 + 1 / 16 + 2),
+             lambda: mx.mx_dequantize_bf16(F4, w["q_row"], w["s_row"], w["s_w"], mx.MX_SCOPE_GROUP, G * O2, F, self.dq_d,
+                                           group_rows=O2)),
+        ]
+
+    def config(self):
+        return {"workload": "moe: Qwen3-30B-A3B expert layer, NVFP4 per-token + 2D weights + grouped GEMMs + DQ(Q(w))",
+                "tokens": 8192, "routed_rows": self.rows, "experts": self.G, "hidden": self.H, "ffn": self.F}
+
+
+class WGrad:
+    """Llama-3-8B MLP WGRAD in NVFP4: RHT16 along tokens + 1x16 column-wise quantize with a
+    per-tensor scale (SR on dY, RNE on X), then dW = dY^T X over K = 32768 tokens."""
+    name = "wgrad"
+
+    def __init__(self, mx, torch, dev):
+        import synthetic
+        self.mx, self.torch, self.dev = mx, torch, dev
+        d = synthetic.wgrad()
+        bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.x, self.dy = bf(d["x"]), bf(d["dy"])
+        self.rht_seed, self.sr_seed = d["rht_seed"], d["sr_seed"]
+        T, H = self.x.shape
+        F = self.dy.shape[1]
+        self.T, self.H, self.F = T, H, F
+        u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
+        self.qdy, self.sdy = torch.empty((F, T // 2), dtype=torch.uint8, device=dev), u8(mx.scale_bytes(F, T, 16))
+        self.qx, self.sx = torch.empty((H, T // 2), dtype=torch.uint8, device=dev), u8(mx.scale_bytes(H, T, 16))
+        self.Sdy = torch.empty(1, dtype=torch.float32, device=dev)
+        self.Sx = torch.empty(1, dtype=torch.float32, device=dev)
+        self.ws1, self.ws2 = u8(16), u8(16)
+        self.dw = torch.empty((F, H), dtype=torch.bfloat16, device=dev)
+        self.rht_out = torch.empty((T, F), dtype=torch.bfloat16, device=dev)
+        self.launches_per_step = 5
+
+    def ops(self):
+        mx, F4 = self.mx, self.mx.MX_FMT_NVFP4
+        T, H, F = self.T, self.H, self.F
+        per = 2 * 2 + 0.5 + 1 / 16          # two reads (amax pass, quantize pass) + codes + scales
+        return [
+            ("quant", "rht16+nvfp4_1x16 colwise SR dY", 1, T * F * per,
+             lambda: mx.mx_nvfp4_quantize_1x16(self.dy, True, True, self.rht_seed, True, self.sr_seed, self.qdy, self.sdy,
+                                               self.Sdy, self.ws1)),
+            ("quant", "rht16+nvfp4_1x16 colwise RNE X", 1, T * H * per,
+             lambda: mx.mx_nvfp4_quantize_1x16(self.x, True, True, self.rht_seed, False, 0, self.qx, self.sx, self.Sx,
+                                               self.ws2)),
+            ("gemm4", "WGRAD", 0, 2.0 * F * H * T,
+             lambda: mx.mx_scaled_gemm(F4, self.qdy, self.sdy, self.Sdy, mx.MX_SCOPE_TENSOR, self.qx, self.sx, self.Sx,
+                                       mx.MX_SCOPE_TENSOR, F, H, T, self.dw)),
+        ]
+
+    def aux_ops(self):
+        """Standalone RHT16 (the unfused transform), timed apart from the step."""
+        return [("rht", "rht16 dY standalone", 1, self.T * self.F * 4.0,
+                 lambda: self.mx.mx_rht16(self.dy, self.rht_seed, self.rht_out))]
+
+    def config(self):
+        return {"workload": "wgrad: Llama-3-8B MLP WGRAD, RHT16 + NVFP4 1x16 colwise (SR dY, RNE X) + NVFP4 GEMM",
+                "tokens": self.T, "hidden": self.H, "ffn": self.F}
+
+
+class WeightSync:
+    """Weight-sync sweep: 48 layers of 128 experts x {2048x768, 768x2048, 768x2048}; per matrix
+    stack MXFP8 row+col quantize, dequantize, re-quantize and byte compare; NVFP4 2D quantize,
+    dequantize, re-quantize and byte compare.  One layer's weights are drawn on the device per step
+    (torch generator seeded 1000 + layer) outside the timed kernels."""
+    name = "weight_sync"
+
+    def __init__(self, mx, torch, dev, layers=48):
+        self.mx, self.torch, self.dev = mx, torch, dev
+        self.layers = layers
+        self.shapes = [(128, 2048, 768), (128, 768, 2048), (128, 768, 2048)]
+        self.layer = 0
+        self.bufs = []
+        for (G, O, H) in self.shapes:
+            b = {"w": torch.empty((G, O, H), dtype=torch.bfloat16, device=dev),
+                 "m8": mx.alloc_mxfp8(G * O, H, dev), "m8b": mx.alloc_mxfp8(G * O, H, dev, colwise=False),
+                 "n4": mx.alloc_nvfp4_weight_2d(G, O, H, dev), "n4b": mx.alloc_nvfp4_weight_2d(G, O, H, dev),
+                 "y": torch.empty((G * O, H), dtype=torch.bfloat16, device=dev)}
+            self.bufs.append(b)
+        self.count = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.launches_per_step = 3 * (2 + 1 + 1 + 2 + 1 + 2 + 2 + 3)
+
+    def draw(self, layer):
+        gen = self.torch.Generator(device=self.dev)
+        gen.manual_seed(1000 + layer)
+        for b in self.bufs:
+            b["w"].normal_(0.0, 0.02, generator=gen)
+
+    def ops(self):
+        mx = self.mx
+        out = []
+        for (G, O, H), b in zip(self.shapes, self.bufs):
+            n = G * O * H
+            R = G * O
+            m8, m8b, n4, n4b = b["m8"], b["m8b"], b["n4"], b["n4b"]
+            w2 = b["w"].view(R, H)
+            out += [
+                ("quant", f"mxfp8 Q {O}x{H}", 1, n * (2 + 2 + 2 / 32), lambda w2=w2, m8=m8: mx.mx_quantize_mxfp8(w2, **m8)),
+                ("dq", f"mxfp8 DQ {O}x{H}", 1, n * (1 + 1 / 32 + 2),
+                 lambda m8=m8, b=b, R=R, H=H: mx.mx_dequantize_bf16(mx.MX_FMT_MXFP8, m8["q_row"], m8["s_row"], None, 0, R, H, b["y"])),
+                ("quant", f"mxfp8 re-Q {O}x{H}", 1, n * (2 + 1 + 1 / 32), lambda b=b, m8b=m8b: mx.mx_quantize_mxfp8(b["y"], **m8b)),
+                ("cmp", f"mxfp8 compare {O}x{H}", 1, 2 * n * (1 + 1 / 32),
+                 lambda m8=m8, m8b=m8b: (mx.mx_count_mismatch(m8["q_row"], m8b["q_row"], self.count),
+                                         mx.mx_count_mismatch(m8["s_row"], m8b["s_row"], self.count))),
+                ("quant", f"nvfp4 2D Q {O}x{H}", 1, n * (2 + 1 + 2 / 16),
+                 lambda b=b, n4=n4: mx.mx_nvfp4_quantize_weight_2d(b["w"], n4["q_row"], n4["s_row"], n4["q_col"], n4["s_col"],
+                                                                    n4["s_w"], n4["ws"])),
+                ("dq", f"nvfp4 DQ {O}x{H}", 1, n * (0.5 + 1 / 16 + 2),
+                 lambda n4=n4, b=b, R=R, H=H, O=O: mx.mx_dequantize_bf16(mx.MX_FMT_NVFP4, n4["q_row"], n4["s_row"], n4["s_w"],
+                                                                       mx.MX_SCOPE_GROUP, R, H, b["y"], group_rows=O)),
+                ("quant", f"nvfp4 2D re-Q {O}x{H}", 1, n * (2 + 1 + 2 / 16),
+                 lambda b=b, n4b=n4b, G=G, O=O, H=H: mx.mx_nvfp4_quantize_weight_2d(b["y"].view(G, O, H), n4b["q_row"], n4b["s_row"],
+                                                                                   n4b["q_col"], n4b["s_col"], n4b["s_w"], n4b["ws"])),
+                ("cmp", f"nvfp4 compare {O}x{H}", 1, 2 * n * (0.5 + 0.5 + 2 / 16),
+                 lambda n4=n4, n4b=n4b: (mx.mx_count_mismatch(n4["q_row"], n4b["q_row"], self.count),
+                                         mx.mx_count_mismatch(n4["q_col"], n4b["q_col"], self.count),
+                                         mx.mx_count_mismatch(n4["s_row"], n4b["s_row"], self.count))),
+            ]
+        return out
+
+    def config(self):
+        return {"workload": "weight_sync: 48 layers x 128 experts x {2048x768, 768x2048, 768x2048}, MXFP8 + NVFP4-2D "
+                            "quantize, dequantize, re-quantize, byte compare", "layers": self.layers}
+
+
 def time_device(work, torch, steps, warmup, dist=None):
     """Warm up, then time `steps` steps with CUDA events on the current stream; per-op events too."""
     ops = work.ops()
@@ -209,6 +391,113 @@ def time_device(work, torch, steps, warmup, dist=None):
     total_ms = start.elapsed_time(end)
     per_op = [statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)) for i in range(n)]
     return total_ms, per_op
+
+
+def time_ops(ops, torch, steps, warmup):
+    """Per-op CUDA-event times (ms, averaged over `steps`) for a list of 5-tuples."""
+    for _ in range(warmup):
+        for op in ops:
+            op[4]()
+    torch.cuda.synchronize()
+    n = len(ops)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for st in range(steps):
+        evs[st][0].record()
+        for i, op in enumerate(ops):
+            op[4]()
+            evs[st][i + 1].record()
+    end.record()
+    torch.cuda.synchronize()
+    per_op = [statistics.mean(evs[st][i].elapsed_time(evs[st][i + 1]) for st in range(steps)) for i in range(n)]
+    return start.elapsed_time(end), per_op
+
+
+def op_report(ops, per_op, peaks):
+    """Achieved rate and roofline fraction per op (bytes ops vs HBM, FP4 GEMMs vs the FP4 peak)."""
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    rep, by_kind = {}, {}
+    for (kind, label, is_bytes, units, _), ms in zip(ops, per_op):
+        if is_bytes:
+            ach = units / (ms / 1e3) / 1e9
+            rep[label] = {"ms": round(ms, 4), "GBps": round(ach, 1), "frac_hbm": round(ach / peaks["hbm_gbs"], 4)}
+        else:
+            ach = units / (ms / 1e3) / 1e12
+            rep[label] = {"ms": round(ms, 4), "TFLOPs": round(ach, 1), "frac_fp4_peak": round(ach / fp4_peak, 4)}
+        k = by_kind.setdefault(kind, [0.0, 0.0, is_bytes])
+        k[0] += ms
+        k[1] += units
+    return rep, by_kind
+
+
+def run_workload(args):
+    import torch
+    import microscaled_precision_numerics_gb300 as mx
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    mx.lib()
+    peaks = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    sampler = ClockSampler(0)
+    if args.workload == "weight_sync":
+        work = WeightSync(mx, torch, dev, layers=args.layers)
+        ops = work.ops()
+        acc = [0.0] * len(ops)
+        total_ms = 0.0
+        sampler.start()
+        for layer in range(work.layers):
+            work.draw(layer)
+            t_ms, per = time_ops(ops, torch, 1, args.warmup if layer == 0 else 0)
+            total_ms += sum(per)
+            acc = [a + b for a, b in zip(acc, per)]
+        clocks = sampler.stop()
+        mx.check_device_status()
+        per_op = acc
+        bytes_total = sum(op[3] for op in ops) * work.layers
+        value = bytes_total / (total_ms / 1e3) / 1e9
+        rep, by_kind = op_report(ops, [p / work.layers for p in per_op], peaks)
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": work.layers,
+                "warmup": args.warmup, "ms_per_step": round(total_ms / work.layers, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16 -> e4m3/e2m1 codes",
+                "data": "synthetic (per-layer N(0, 0.02) draws on the device, seed 1000 + layer)",
+                "config": work.config(), "frac_hbm": round(value / peaks["hbm_gbs"], 4),
+                "mismatched_bytes": int(work.count.item()), "per_op": rep, "clocks": clocks,
+                "gpu_launches": work.launches_per_step * work.layers}
+        print(json.dumps(line), flush=True)
+        return
+    work = MoE(mx, torch, dev) if args.workload == "moe" else WGrad(mx, torch, dev)
+    ops = work.ops()
+    sampler.start()
+    total_ms, per_op = time_ops(ops, torch, args.steps, args.warmup)
+    clocks = sampler.stop()
+    aux = {}
+    if hasattr(work, "aux_ops"):
+        aops = work.aux_ops()
+        _, aper = time_ops(aops, torch, args.steps, args.warmup)
+        aux, _ = op_report(aops, aper, peaks)
+    mx.check_device_status()
+    rep, by_kind = op_report(ops, per_op, peaks)
+    flops = sum(op[3] for op in ops if not op[2])
+    ms = total_ms / args.steps
+    value = flops / (ms / 1e3) / 1e12
+    dominant = max(by_kind.items(), key=lambda kv: kv[1][0])
+    kind, (kms, kunits, is_bytes) = dominant
+    if is_bytes:
+        ach = kunits / (kms / 1e3) / 1e9
+        roof = {"kernel": kind, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None}
+    else:
+        ach = kunits / (kms / 1e3) / 1e12
+        roof = {"kernel": kind, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp4_peak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / fp4_peak, 4), "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4/BF16)"}
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e2m1 (f32 accumulate, bf16 out)", "data": "synthetic (seeded numpy draws)",
+            "config": work.config(), "per_op": rep, "aux": aux, "roofline": roof, "clocks": clocks,
+            "gpu_launches": work.launches_per_step * args.steps}
+    print(json.dumps(line), flush=True)
 
 
 def run_device(args):
@@ -406,7 +695,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mxnum", "reference"], default="mxnum")
-    ap.add_argument("--workload", choices=["dense_mlp"], default="dense_mlp")
+    ap.add_argument("--workload", choices=["dense_mlp", "moe", "wgrad", "weight_sync"], default="dense_mlp")
+    ap.add_argument("--layers", type=int, default=48, help="weight_sync: layers swept")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -414,6 +704,9 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload != "dense_mlp":
+        run_workload(args)
         return
     run_device(args)
 

@@ -48,7 +48,7 @@ typedef enum {
 typedef enum { MX_FMT_MXFP8 = 0, MX_FMT_NVFP4 = 1 } mx_format;
 typedef enum { MX_ROUND_RNE = 0, MX_ROUND_SR = 1 } mx_round;
 /* Scope of an FP32 second-level scale / GEMM epilogue factor. */
-typedef enum { MX_SCOPE_NONE = 0, MX_SCOPE_TENSOR = 1, MX_SCOPE_ROW = 2 } mx_scope;
+typedef enum { MX_SCOPE_NONE = 0, MX_SCOPE_TENSOR = 1, MX_SCOPE_ROW = 2, MX_SCOPE_GROUP = 3 } mx_scope;
 
 /* Human-readable name of a status code (static storage). */
 const char* mx_status_string(mx_status s);
@@ -151,10 +151,12 @@ mx_status mx_nvfp4_quantize_1x16(const void* x, int64_t T, int64_t N, int colwis
  *   MXFP8: y = BF16 RNE of val(q) * 2^(s - 127);  q [rows, cols]; s mx_scale_bytes(rows, cols, 32);
  *          s2 ignored.
  *   NVFP4: y = BF16 RNE of fp32(val(q) * val(bs)) * S; q [rows, cols/2]; s mx_scale_bytes(rows, cols,
- *          16); S = s2[row] (MX_SCOPE_ROW) or s2[0] (MX_SCOPE_TENSOR).
+ *          16); S = s2[row] (MX_SCOPE_ROW), s2[row / group_rows] (MX_SCOPE_GROUP: stacked matrices of
+ *          group_rows rows each, e.g. per-expert 2D weights; group_rows % 128 == 0 so the stacked scale
+ *          tensors form one layout) or s2[0] (MX_SCOPE_TENSOR).
  *   y [rows, cols] BF16.  Requires cols % 32 (MXFP8) or cols % 16 (NVFP4) == 0. */
 mx_status mx_dequantize_bf16(mx_format fmt, const uint8_t* q, const uint8_t* s, const float* s2,
-                             mx_scope s2_scope, int64_t rows, int64_t cols, void* y,
+                             mx_scope s2_scope, int64_t group_rows, int64_t rows, int64_t cols, void* y,
                              cudaStream_t stream);
 
 /* Block-scaled GEMM on the 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA operand
@@ -168,8 +170,8 @@ mx_status mx_dequantize_bf16(mx_format fmt, const uint8_t* q, const uint8_t* s, 
  *   alpha_a: NULL / MX_SCOPE_NONE (1), one FP32 (MX_SCOPE_TENSOR) or M FP32 (MX_SCOPE_ROW); alpha_b
  *   likewise with N.  d [M, ldd] BF16.
  * FP32 accumulation inside the tensor core; the summation order is the hardware's.  Requires
- * K % 128 (MXFP8) or K % 256 (NVFP4) == 0; M, N >= 1; ldd >= N (rows of d start 16-byte aligned
- * when ldd % 8 == 0, which takes the vector-store epilogue; any other ldd uses 2-byte stores). */
+ * K % 128 (MXFP8) or K % 256 (NVFP4) == 0; M, N >= 1; N % 8 == 0 and ldd % 8 == 0 (rows of d are
+ * written in 16-byte groups), ldd >= N. */
 mx_status mx_scaled_gemm(mx_format fmt,
                          const uint8_t* a, const uint8_t* sa, const float* alpha_a, mx_scope alpha_a_scope,
                          const uint8_t* b, const uint8_t* sb, const float* alpha_b, mx_scope alpha_b_scope,

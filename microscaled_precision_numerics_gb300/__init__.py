@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libmxnum.so")
 
 MX_FMT_MXFP8, MX_FMT_NVFP4 = 0, 1
 MX_ROUND_RNE, MX_ROUND_SR = 0, 1
-MX_SCOPE_NONE, MX_SCOPE_TENSOR, MX_SCOPE_ROW = 0, 1, 2
+MX_SCOPE_NONE, MX_SCOPE_TENSOR, MX_SCOPE_ROW, MX_SCOPE_GROUP = 0, 1, 2, 3
 MX_WS_WEIGHT_2D, MX_WS_1X16 = 0, 1
 MX_NOALLOC_MAX_MATRICES = 4096
 
@@ -51,7 +51,7 @@ def lib() -> ctypes.CDLL:
                 "mx_nvfp4_quantize_weight_2d": (I32, [P, I64, I64, I64, P, P, P, P, P, P, SZ, P]),
                 "mx_rht16": (I32, [P, I64, I64, U64, P, P]),
                 "mx_nvfp4_quantize_1x16": (I32, [P, I64, I64, I32, I32, U64, I32, U64, P, P, P, P, SZ, P]),
-                "mx_dequantize_bf16": (I32, [I32, P, P, P, I32, I64, I64, P, P]),
+                "mx_dequantize_bf16": (I32, [I32, P, P, P, I32, I64, I64, I64, P, P]),
                 "mx_scaled_gemm": (I32, [I32, P, P, P, I32, P, P, P, I32, I64, I64, I64, P, I64, P]),
                 "mx_grouped_scaled_gemm": (I32, [I32, I64, P, I64, P, P, P, P, P, P, I64, I64, P, P]),
                 "mx_count_mismatch": (I32, [P, P, I64, P, P]),
@@ -161,9 +161,9 @@ def mx_nvfp4_quantize_1x16(x, colwise: bool, rht: bool, rht_seed: int, sr: bool,
         _p(q), _p(s), _p(s_tensor), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def mx_dequantize_bf16(fmt: int, q, s, s2, s2_scope: int, rows: int, cols: int, y, stream=None):
+def mx_dequantize_bf16(fmt: int, q, s, s2, s2_scope: int, rows: int, cols: int, y, stream=None, group_rows: int = 0):
     _check("mx_dequantize_bf16", lib().mx_dequantize_bf16(
-        fmt, _p(q), _p(s), _p(s2), s2_scope, rows, cols, _p(y), _stream(stream)))
+        fmt, _p(q), _p(s), _p(s2), s2_scope, group_rows, rows, cols, _p(y), _stream(stream)))
 
 
 def mx_scaled_gemm(fmt: int, a, sa, alpha_a, alpha_a_scope: int, b, sb, alpha_b, alpha_b_scope: int,

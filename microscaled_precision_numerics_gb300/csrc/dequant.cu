@@ -43,12 +43,12 @@ dequant_mxfp8_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ 
 // NVFP4: thread = one 16-block (8 code bytes) -> 16 BF16.
 __global__ void __launch_bounds__(256)
 dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, const float* __restrict__ s2,
-                     bool per_row, int64_t R, int64_t K, uint16_t* __restrict__ y) {
+                     int64_t rows_per_scale, int64_t R, int64_t K, uint16_t* __restrict__ y) {
     const int64_t per_row_blk = K / 16;
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (gid >= R * per_row_blk) return;
     const int64_t r = gid / per_row_blk, b = gid % per_row_blk;
-    const float S = per_row ? __ldg(s2 + r) : __ldg(s2);
+    const float S = rows_per_scale > 0 ? __ldg(s2 + r / rows_per_scale) : __ldg(s2);
     const float bs = e4m3_to_f32(__ldg(s + sf_offset(r, b, sf_col_tiles(K, 16))));
     const uint2 c = __ldcs(reinterpret_cast<const uint2*>(q + r * (K / 2) + b * 8));
     const uint32_t cw[2] = {c.x, c.y};
@@ -97,14 +97,14 @@ mismatch_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ y, in
 
 }  // namespace
 
-cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const float* s2, bool per_row, int64_t R,
-                           int64_t K, uint16_t* y, cudaStream_t stream) {
+cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const float* s2, int64_t rows_per_scale,
+                           int64_t R, int64_t K, uint16_t* y, cudaStream_t stream) {
     if (fmt == 0) {
         const int64_t threads = R * (K / 16);
         dequant_mxfp8_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(q, s, R, K, y);
     } else {
         const int64_t threads = R * (K / 16);
-        dequant_nvfp4_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(q, s, s2, per_row, R, K, y);
+        dequant_nvfp4_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(q, s, s2, rows_per_scale, R, K, y);
     }
     return cudaGetLastError();
 }

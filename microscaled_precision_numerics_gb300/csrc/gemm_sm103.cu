@@ -227,7 +227,7 @@ __device__ __forceinline__ Tile grouped_tile(const Params& p, const int* prefix,
 // ---------------------------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------------------------
-template <int FMT, bool GROUPED>
+template <int FMT, bool GROUPED, bool COL_ALPHA>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
     using C = Cfg<FMT>;
@@ -411,39 +411,39 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (GROUPED && p.alpha_b_scope != 0) ab_g = __ldg(p.alpha_b + tile.g);
             else if (!GROUPED && p.alpha_b_scope == 1) ab_g = __ldg(p.alpha_b);
             uint16_t* drow = p.d + row * p.ldd;
-#pragma unroll 1
+            // drain the accumulator slice (this thread's row, 256 columns) into packed BF16 registers,
+            // then hand TMEM back to the MMA warp before the global stores
+            uint32_t packed[BN / 2];
+#pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
                 float v[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
-                const int64_t nb = tile.n0 + c * 32;
-                if (!row_ok || nb >= p.N) continue;
-                uint32_t packed[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     float f0 = __fmul_rn(v[2 * i], aa), f1 = __fmul_rn(v[2 * i + 1], aa);
-                    if (!GROUPED && p.alpha_b_scope == 2) {
-                        const int64_t n = nb + 2 * i;
+                    if (COL_ALPHA) {
+                        const int64_t n = tile.n0 + c * 32 + 2 * i;
                         f0 = __fmul_rn(f0, n < p.N ? __ldg(p.alpha_b + n) : 0.0f);
                         f1 = __fmul_rn(f1, n + 1 < p.N ? __ldg(p.alpha_b + n + 1) : 0.0f);
                     } else {
                         f0 = __fmul_rn(f0, ab_g);
                         f1 = __fmul_rn(f1, ab_g);
                     }
-                    packed[i] = pack_bf16x2(f0, f1);
-                }
-                if (nb + 32 <= p.N && (p.ldd & 7) == 0) {
-                    uint4* dst = reinterpret_cast<uint4*>(drow + nb);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-                } else {
-                    for (int i = 0; i < 32 && nb + i < p.N; ++i)
-                        drow[nb + i] = (uint16_t)((packed[i >> 1] >> (16 * (i & 1))) & 0xFFFFu);
+                    packed[c * 16 + i] = pack_bf16x2(f0, f1);
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_tempty);
+            if (row_ok) {
+                // N and ldd are multiples of 8: every 8-column group is one aligned 16-byte store
+#pragma unroll
+                for (int g8 = 0; g8 < BN / 8; ++g8) {
+                    if (tile.n0 + g8 * 8 < p.N)
+                        *reinterpret_cast<uint4*>(drow + tile.n0 + g8 * 8) =
+                            make_uint4(packed[4 * g8], packed[4 * g8 + 1], packed[4 * g8 + 2], packed[4 * g8 + 3]);
+                }
+            }
             acc_phase ^= 1;
         }
     }
@@ -484,13 +484,13 @@ bool make_map(CUtensorMap* map, const uint8_t* base, int64_t k_bytes, int64_t ro
     return r == CUDA_SUCCESS;
 }
 
-template <int FMT, bool GROUPED>
+template <int FMT, bool GROUPED, bool COL_ALPHA>
 cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
     using C = Cfg<FMT>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(bs_gemm_kernel<FMT, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(bs_gemm_kernel<FMT, GROUPED, COL_ALPHA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::SMEM_ALLOC);
     });
     if (attr_err != cudaSuccess) return attr_err;
@@ -515,7 +515,7 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
     p.total_tiles = p.m_tiles * p.n_tiles;
     int64_t tiles_bound = GROUPED ? (p.m_tiles + a.G) * p.n_tiles : p.total_tiles;
     const unsigned grid = (unsigned)max64(1, min64(tiles_bound, num_sms));
-    bs_gemm_kernel<FMT, GROUPED><<<grid, NUM_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmB, p);
+    bs_gemm_kernel<FMT, GROUPED, COL_ALPHA><<<grid, NUM_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmB, p);
     return cudaGetLastError();
 }
 
@@ -523,8 +523,13 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
 
 cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream) {
     if (args.G > MAX_GROUPS) return cudaErrorInvalidValue;
-    if (args.fmt == 0) return args.G > 0 ? launch_impl<0, true>(args, num_sms, stream) : launch_impl<0, false>(args, num_sms, stream);
-    return args.G > 0 ? launch_impl<1, true>(args, num_sms, stream) : launch_impl<1, false>(args, num_sms, stream);
+    const bool col_alpha = args.G == 0 && args.alpha_b_scope == 2;   // per-output-column factor (dense only)
+    if (args.fmt == 0) {
+        if (args.G > 0) return launch_impl<0, true, false>(args, num_sms, stream);
+        return col_alpha ? launch_impl<0, false, true>(args, num_sms, stream) : launch_impl<0, false, false>(args, num_sms, stream);
+    }
+    if (args.G > 0) return launch_impl<1, true, false>(args, num_sms, stream);
+    return col_alpha ? launch_impl<1, false, true>(args, num_sms, stream) : launch_impl<1, false, false>(args, num_sms, stream);
 }
 
 uint32_t read_and_clear_device_status() {

@@ -130,17 +130,24 @@ mx_status mx_nvfp4_quantize_1x16(const void* x, int64_t T, int64_t N, int colwis
 }
 
 mx_status mx_dequantize_bf16(mx_format fmt, const uint8_t* q, const uint8_t* s, const float* s2, mx_scope s2_scope,
-                             int64_t rows, int64_t cols, void* y, cudaStream_t stream) {
+                             int64_t group_rows, int64_t rows, int64_t cols, void* y, cudaStream_t stream) {
     if (!q || !s || !y || rows <= 0 || cols <= 0) return MX_ERR_INVALID_ARG;
     if (fmt != MX_FMT_MXFP8 && fmt != MX_FMT_NVFP4) return MX_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(y)) return MX_ERR_ALIGNMENT;
+    int64_t per = 0;   // rows sharing one second-level scale (0: one for the whole tensor)
     if (fmt == MX_FMT_MXFP8) {
         if ((cols % 32) != 0) return MX_ERR_UNSUPPORTED;
     } else {
-        if (!s2 || (s2_scope != MX_SCOPE_TENSOR && s2_scope != MX_SCOPE_ROW)) return MX_ERR_INVALID_ARG;
+        if (!s2) return MX_ERR_INVALID_ARG;
+        if (s2_scope == MX_SCOPE_ROW) per = 1;
+        else if (s2_scope == MX_SCOPE_GROUP) {
+            if (group_rows <= 0) return MX_ERR_INVALID_ARG;
+            if ((group_rows % 128) != 0) return MX_ERR_UNSUPPORTED;
+            per = group_rows;
+        } else if (s2_scope != MX_SCOPE_TENSOR) return MX_ERR_INVALID_ARG;
         if ((cols % 16) != 0) return MX_ERR_UNSUPPORTED;
     }
-    return from_cuda(mxk::launch_dequant(fmt == MX_FMT_MXFP8 ? 0 : 1, q, s, s2, s2_scope == MX_SCOPE_ROW, rows, cols,
+    return from_cuda(mxk::launch_dequant(fmt == MX_FMT_MXFP8 ? 0 : 1, q, s, s2, per, rows, cols,
                                          static_cast<uint16_t*>(y), stream));
 }
 
@@ -161,6 +168,7 @@ mx_status mx_scaled_gemm(mx_format fmt, const uint8_t* a, const uint8_t* sa, con
     mx_status st = validate_gemm_common(fmt, a, sa, b, sb, N, K, d);
     if (st != MX_OK) return st;
     if (M <= 0 || ldd < N) return MX_ERR_INVALID_ARG;
+    if ((N % 8) != 0 || (ldd % 8) != 0) return MX_ERR_ALIGNMENT;
     if ((alpha_a_scope != MX_SCOPE_NONE && !alpha_a) || (alpha_b_scope != MX_SCOPE_NONE && !alpha_b))
         return MX_ERR_INVALID_ARG;
     if (alpha_a_scope < MX_SCOPE_NONE || alpha_a_scope > MX_SCOPE_ROW || alpha_b_scope < MX_SCOPE_NONE ||

@@ -7,9 +7,8 @@
 // kernel cost 2.2 + 2.6 ms per micro-batch; here one kernel writes both copies with their scales
 // already in the GEMM layout.
 //
-// CTA tile: 128 rows x 64 columns of BF16 (16 KB), staged in shared memory with a padded pitch.
-//   row-wise:    256 (row, 32-column block) pairs, one per thread
-//   column-wise: 64 columns x 4 row blocks of 32, one per thread
+// CTA tile: 128 rows x 128 columns of BF16 (32 KB), staged in shared memory with a padded pitch; both
+// passes read it with 16-byte loads and keep the values in registers between amax and conversion.
 // Scale exponent: e = max(exp_field(amax) - 8, 0) - 127 as an E8M0 byte; the multiply by 2^-e is
 // exact in FP32 for every value that can round to a nonzero E4M3 code.
 #include "mx_internal.h"
@@ -19,8 +18,8 @@ namespace mxk {
 namespace {
 
 constexpr int QT_ROWS = 128;
-constexpr int QT_COLS = 64;
-constexpr int QT_PITCH = 144;   // bytes per staged row: 128 + 16 keeps 16-byte accesses conflict-free
+constexpr int QT_COLS = 128;
+constexpr int QT_PITCH = 272;   // bytes per staged row: 256 + 16 keeps 16-byte accesses conflict-free
 constexpr int QT_THREADS = 256;
 
 __device__ __forceinline__ uint32_t e8m0_from_amax_bits(uint32_t amax16) {
@@ -46,6 +45,16 @@ __device__ __forceinline__ uint32_t mxfp8_block32(const uint32_t w[16], uint32_t
     return s;
 }
 
+// Element j (0..7) of a 16-byte chunk of 8 BF16 values.
+__device__ __forceinline__ float chunk_elem(const uint4& v, int j) {
+    const uint32_t w = (j >> 1) == 0 ? v.x : ((j >> 1) == 1 ? v.y : ((j >> 1) == 2 ? v.z : v.w));
+    return (j & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+
+// CTA tile: 128 rows x 128 columns of BF16 staged in shared memory (pitch 272 B).
+//   row pass:    thread -> (row, pair of 32-column blocks); 8 x 16-byte shared loads
+//   column pass: thread -> (8-column chunk, 32-row block, quarter of 8 rows); 8 x 16-byte shared
+//                loads; the 32-row amax combines the 4 quarters (lanes l, l^8, l^16, l^24)
 template <bool ROW, bool COL>
 __global__ void __launch_bounds__(QT_THREADS)
 mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
@@ -54,15 +63,15 @@ mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int6
     __shared__ __align__(16) uint8_t tile[QT_ROWS * QT_PITCH];
     __shared__ uint8_t colsc[4][QT_COLS];
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t r0 = (int64_t)blockIdx.y * QT_ROWS;
     const int64_t c0 = (int64_t)blockIdx.x * QT_COLS;
 
-    // ---- stage: 128 rows x 8 chunks of 16 bytes; each warp reads 4 whole 128-byte rows ----
+    // ---- stage: 128 rows x 16 chunks of 16 bytes; each warp reads two whole 256-byte rows ----
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j) {
         const int ci = tid + QT_THREADS * j;
-        const int rr = ci >> 3, ch = ci & 7;
+        const int rr = ci >> 4, ch = ci & 15;
         const int64_t r = r0 + rr, c = c0 + ch * 8;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (r < R && c < K) v = __ldcs(reinterpret_cast<const uint4*>(x + r * ldx + c));
@@ -71,55 +80,78 @@ mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int6
     __syncthreads();
 
     if (ROW) {
-        // thread -> (row rr, block b); b = tid & 1 so the two blocks of a row are adjacent lanes
-        const int rr = tid >> 1, b = tid & 1;
-        const int64_t r = r0 + rr, c = c0 + b * 32;
-        const bool valid = (r < R) && (c < K);
-        uint32_t w[16];
+        // lanes 0..7 take 8 different rows of the same 64-column half: conflict-free 16-byte loads
+        const int half = (tid >> 3) & 1;
+        const int rr = (tid & 7) + 8 * (tid >> 4);
+        const int64_t r = r0 + rr;
+        uint32_t s2[2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 v = *reinterpret_cast<const uint4*>(tile + rr * QT_PITCH + b * 64 + i * 16);
-            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        for (int b = 0; b < 2; ++b) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = *reinterpret_cast<const uint4*>(tile + rr * QT_PITCH + half * 128 + b * 64 + i * 16);
+                w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+            }
+            uint32_t codes[8];
+            s2[b] = mxfp8_block32(w, codes);
+            const int64_t c = c0 + half * 64 + b * 32;
+            if (r < R && c < K) {
+                uint4* dst = reinterpret_cast<uint4*>(q_row + r * K + c);
+                __stcs(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
+                __stcs(dst + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+            }
         }
-        uint32_t codes[8];
-        const uint32_t s = mxfp8_block32(w, codes);
-        if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(q_row + r * K + c);
-            __stcs(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-            __stcs(dst + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
-        }
-        // the pair (b = 0, b = 1) shares one 16-bit slot of the scale layout (c0 / 32 is even)
-        const uint32_t s_other = __shfl_down_sync(0xFFFFFFFFu, s, 1);
-        const int64_t nct = sf_col_tiles(K, 32);
-        const int64_t kb = c0 / 32;
-        if (b == 0 && r < R) {
-            const bool both = (c0 + 32 < K);
+        // the row's 4 scales: this thread's two and those of lane + 8 (the other half)
+        const uint32_t mine = s2[0] | (s2[1] << 8);
+        const uint32_t other = __shfl_down_sync(0xFFFFFFFFu, mine, 8);
+        if (half == 0 && r < R) {
+            const int64_t nct = sf_col_tiles(K, 32);
+            const int64_t kb = c0 / 32;
+            const int nvalid = (int)min64(4, (K - c0) / 32);
             uint8_t* p = s_row + sf_offset(r, kb, nct);
-            if (both) *reinterpret_cast<uint16_t*>(p) = (uint16_t)(s | (s_other << 8));
-            else *p = (uint8_t)s;
+            const uint32_t word = mine | (other << 16);
+            if (nvalid == 4) *reinterpret_cast<uint32_t*>(p) = word;
+            else for (int i = 0; i < nvalid; ++i) p[i] = (uint8_t)(word >> (8 * i));
         }
     }
 
     if (COL) {
-        // thread -> (column cc, row block rb); consecutive lanes read consecutive columns
-        const int cc = tid & 63, rb = tid >> 6;
-        const int64_t c = c0 + cc, rbase = r0 + rb * 32;
-        const bool valid = (c < K) && (rbase < R);
-        uint32_t w[16];
+        const int rb = warp >> 1;                        // 32-row block
+        const int chunk = (warp & 1) * 8 + (lane & 7);   // 8-column chunk
+        const int q = lane >> 3;                         // quarter: rows q*8 .. q*8+7 of the block
+        uint4 v[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t lo = *reinterpret_cast<const uint16_t*>(tile + (rb * 32 + 2 * i) * QT_PITCH + cc * 2);
-            const uint32_t hi = *reinterpret_cast<const uint16_t*>(tile + (rb * 32 + 2 * i + 1) * QT_PITCH + cc * 2);
-            w[i] = lo | (hi << 16);
+        for (int i = 0; i < 8; ++i)
+            v[i] = *reinterpret_cast<const uint4*>(tile + (rb * 32 + q * 8 + i) * QT_PITCH + chunk * 16);
+        // per-column |max| as packed 16-bit pairs, then across the four quarters
+        uint32_t m[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            m[0] = absmax_bf16x2(m[0], v[i].x); m[1] = absmax_bf16x2(m[1], v[i].y);
+            m[2] = absmax_bf16x2(m[2], v[i].z); m[3] = absmax_bf16x2(m[3], v[i].w);
         }
-        uint32_t codes[8];
-        const uint32_t s = mxfp8_block32(w, codes);
-        if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(q_col + c * R + rbase);
-            __stcs(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-            __stcs(dst + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            m[k] = __vmaxu2(m[k], __shfl_xor_sync(0xFFFFFFFFu, m[k], 8));
+            m[k] = __vmaxu2(m[k], __shfl_xor_sync(0xFFFFFFFFu, m[k], 16));
         }
-        colsc[rb][cc] = (uint8_t)s;
+        const int64_t rbase = r0 + rb * 32;
+        const bool rows_ok = rbase < R;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t a16 = (j & 1) ? (m[j >> 1] >> 16) : (m[j >> 1] & 0xFFFFu);
+            const uint32_t s = e8m0_from_amax_bits(a16);
+            const float f = inv_scale_from_e8m0(s);
+            const uint32_t lo = cvt_e4m3x4(__fmul_rn(chunk_elem(v[0], j), f), __fmul_rn(chunk_elem(v[1], j), f),
+                                           __fmul_rn(chunk_elem(v[2], j), f), __fmul_rn(chunk_elem(v[3], j), f));
+            const uint32_t hi = cvt_e4m3x4(__fmul_rn(chunk_elem(v[4], j), f), __fmul_rn(chunk_elem(v[5], j), f),
+                                           __fmul_rn(chunk_elem(v[6], j), f), __fmul_rn(chunk_elem(v[7], j), f));
+            const int64_t c = c0 + chunk * 8 + j;
+            if (rows_ok && c < K)
+                __stcs(reinterpret_cast<uint2*>(q_col + c * R + rbase + q * 8), make_uint2(lo, hi));
+            if (q == 0) colsc[rb][chunk * 8 + j] = (uint8_t)s;
+        }
         __syncthreads();
         // one 32-bit word of 4 row-block scales per column (r0 / 32 is a multiple of 4)
         if (tid < QT_COLS) {

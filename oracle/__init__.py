@@ -79,6 +79,9 @@ def _load():
                 "orc_rht16": (None, [P, I64, I64, U64, P]),
                 "orc_nvfp4_quantize_1x16": (None, [P, I64, I64, ctypes.c_int, ctypes.c_int, U64,
                                                    ctypes.c_int, U64, P, P, P]),
+                "orc_nvfp4_1x16_amax": (ctypes.c_float, [P, I64, I64, ctypes.c_int, U64]),
+                "orc_nvfp4_1x16_pass2": (None, [P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_int, U64, ctypes.c_int, U64,
+                                                ctypes.c_float, P, P]),
                 "orc_dequant_mxfp8": (None, [P, P, I64, I64, P]),
                 "orc_dequant_nvfp4": (None, [P, P, P, ctypes.c_int, I64, I64, P]),
                 "orc_decode_mxfp8_f64": (None, [P, P, I64, I64, P]),
@@ -301,6 +304,35 @@ def nvfp4_quantize_1x16(x: np.ndarray, colwise: bool, rht: bool = False, rht_see
     _load().orc_nvfp4_quantize_1x16(_p(x), T, N, int(colwise), int(rht), rht_seed, int(sr), sr_seed,
                                     _p(q), _p(s), _p(st))
     return q, s, np.float32(st[0])
+
+
+def nvfp4_1x16_amax(x: np.ndarray, rht: bool = False, rht_seed: int = 0) -> np.float32:
+    """Pass 1 of the per-tensor 1x16 quantizer on a [T, N] tensor or column slab (MaxText recipe:
+    per-tensor FP32 scale; RHT on WGRAD inputs)."""
+    x = _bf16(x)
+    T, N = x.shape
+    return np.float32(_load().orc_nvfp4_1x16_amax(_p(x), T, N, int(rht), rht_seed))
+
+
+def nvfp4_1x16_pass2(x_slab: np.ndarray, n_offset: int, N_total: int, S, colwise: bool, rht: bool = False,
+                     rht_seed: int = 0, sr: bool = False, sr_seed: int = 0):
+    """Pass 2 on columns [n_offset, n_offset + N) of a [T, N_total] tensor with a given per-tensor
+    scale S; SR indices use the global element index t * N_total + n."""
+    x = _bf16(x_slab)
+    T, N = x.shape
+    if colwise:
+        q = np.zeros((N, T // 2), dtype=np.uint8)
+        s = np.zeros((N, T // 16), dtype=np.uint8)
+    else:
+        q = np.zeros((T, N // 2), dtype=np.uint8)
+        s = np.zeros((T, N // 16), dtype=np.uint8)
+    _load().orc_nvfp4_1x16_pass2(_p(x), T, N, n_offset, N_total, int(colwise), int(rht), rht_seed, int(sr), sr_seed,
+                                 float(np.float32(S)), _p(q), _p(s))
+    return q, s
+
+
+def nvfp4_second_scale(amax) -> np.float32:
+    return np.float32(_load().orc_nvfp4_second_scale(float(np.float32(amax))))
 
 
 # ---------------------------------------------------------------------------

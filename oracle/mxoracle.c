@@ -435,16 +435,15 @@ ORC_API void orc_rht16(const uint16_t* x, int64_t T, int64_t N, uint64_t seed, u
     }
 }
 
-/* 1x16 quantization with a per-tensor FP32 second-level scale ([MaxText]).
- * x [T, N] BF16.  colwise = 1: blocks of 16 along T, optional RHT first,
- * output transposed q [N, T/2], s compact [N, T/16].  colwise = 0: blocks
- * along N, q [T, N/2], s compact [T, N/16] (rht must be 0).
- * Pass 1: A = amax over the (BF16-rounded, transformed) tensor, S = A/2688.
- * Pass 2: per block as in the per-token case, RNE, or SR with the 16 bits of
- * logical element i = t * N + n. */
-ORC_API void orc_nvfp4_quantize_1x16(const uint16_t* x, int64_t T, int64_t N, int colwise, int rht,
-                                     uint64_t rht_seed, int sr, uint64_t sr_seed,
-                                     uint8_t* q, uint8_t* s, float* s_tensor) {
+/* 1x16 quantization with a per-tensor FP32 second-level scale ([MaxText]), in its two passes.
+ * Pass 1 (orc_nvfp4_1x16_amax): A = amax over the (BF16-rounded, transformed) tensor.  The RHT acts
+ * on each column separately, so the amax of a tensor is the max over any split into column slabs.
+ * Pass 2 (orc_nvfp4_1x16_pass2): with S = A / 2688, per block as in the per-token case, RNE, or SR
+ * with the 16 bits of logical element i = t * N_total + n_global.  The slab holds columns
+ * [n_offset, n_offset + N) of a [T, N_total] tensor.
+ * colwise = 1: blocks of 16 along T, output transposed q [N, T/2], s compact [N, T/16].
+ * colwise = 0: blocks along N, q [T, N/2], s compact [T, N/16] (rht must be 0). */
+ORC_API float orc_nvfp4_1x16_amax(const uint16_t* x, int64_t T, int64_t N, int rht, uint64_t rht_seed) {
     uint16_t* y = NULL;
     const uint16_t* src = x;
     if (rht) {
@@ -454,8 +453,20 @@ ORC_API void orc_nvfp4_quantize_1x16(const uint16_t* x, int64_t T, int64_t N, in
     }
     float amax = 0.0f;
     for (int64_t i = 0; i < T * N; ++i) amax = fmaxf(amax, fabsf(bf16_to_float(src[i])));
-    float S = orc_nvfp4_second_scale(amax);
-    *s_tensor = S;
+    free(y);
+    return amax;
+}
+
+ORC_API void orc_nvfp4_1x16_pass2(const uint16_t* x, int64_t T, int64_t N, int64_t n_offset, int64_t N_total,
+                                  int colwise, int rht, uint64_t rht_seed, int sr, uint64_t sr_seed, float S,
+                                  uint8_t* q, uint8_t* s) {
+    uint16_t* y = NULL;
+    const uint16_t* src = x;
+    if (rht) {
+        y = (uint16_t*)malloc((size_t)(T * N) * sizeof(uint16_t));
+        orc_rht16(x, T, N, rht_seed, y);
+        src = y;
+    }
     if (colwise) {
         int64_t nb = T / 16;
 #pragma omp parallel for schedule(static)
@@ -469,8 +480,8 @@ ORC_API void orc_nvfp4_quantize_1x16(const uint16_t* x, int64_t T, int64_t N, in
                 for (int i = 0; i < 16; ++i) {
                     int64_t t = b * 16 + i;
                     float v = bf16_to_float(src[t * N + n]) * r;
-                    uint8_t c = sr ? orc_e2m1_encode_sr(v, orc_sr_bits16(sr_seed, (uint64_t)(t * N + n)))
-                                   : orc_e2m1_encode((double)v);
+                    uint64_t gi = (uint64_t)(t * N_total + n_offset + n);
+                    uint8_t c = sr ? orc_e2m1_encode_sr(v, orc_sr_bits16(sr_seed, gi)) : orc_e2m1_encode((double)v);
                     put_nibble(q + n * (T / 2), t, c);
                 }
             }
@@ -488,14 +499,23 @@ ORC_API void orc_nvfp4_quantize_1x16(const uint16_t* x, int64_t T, int64_t N, in
                 for (int i = 0; i < 16; ++i) {
                     int64_t n = b * 16 + i;
                     float v = bf16_to_float(src[t * N + n]) * r;
-                    uint8_t c = sr ? orc_e2m1_encode_sr(v, orc_sr_bits16(sr_seed, (uint64_t)(t * N + n)))
-                                   : orc_e2m1_encode((double)v);
+                    uint64_t gi = (uint64_t)(t * N_total + n_offset + n);
+                    uint8_t c = sr ? orc_e2m1_encode_sr(v, orc_sr_bits16(sr_seed, gi)) : orc_e2m1_encode((double)v);
                     put_nibble(q + t * (N / 2), n, c);
                 }
             }
         }
     }
     free(y);
+}
+
+/* Both passes on a whole [T, N] tensor. */
+ORC_API void orc_nvfp4_quantize_1x16(const uint16_t* x, int64_t T, int64_t N, int colwise, int rht,
+                                     uint64_t rht_seed, int sr, uint64_t sr_seed,
+                                     uint8_t* q, uint8_t* s, float* s_tensor) {
+    float S = orc_nvfp4_second_scale(orc_nvfp4_1x16_amax(x, T, N, rht, rht_seed));
+    *s_tensor = S;
+    orc_nvfp4_1x16_pass2(x, T, N, 0, N, colwise, rht, rht_seed, sr, sr_seed, S, q, s);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -91,6 +91,7 @@ def test_gemm_validation(lib):
     assert g(0, A16, A16, NUL, 2, A16, A16, NUL, 0, 128, 128, 128, A16, 128, NUL) == 1  # scope without pointer
     assert g(0, A8, A16, NUL, 0, A16, A16, NUL, 0, 128, 128, 128, A16, 128, NUL) == 2
     assert g(0, A16, A16, NUL, 0, A16, A16, NUL, 0, 128, 128, 128, A16, 100, NUL) == 1  # ldd < N
+    assert g(0, A16, A16, NUL, 0, A16, A16, NUL, 0, 128, 100, 128, A16, 100, NUL) == 2  # N % 8
     gg = lib.mx_grouped_scaled_gemm
     assert gg(1, 0, A16, 16, A16, A16, NUL, A16, A16, NUL, 256, 256, A16, NUL) == 1      # G = 0
     assert gg(1, 5000, A16, 16, A16, A16, NUL, A16, A16, NUL, 256, 256, A16, NUL) == 1   # too many groups

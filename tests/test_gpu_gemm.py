@@ -54,7 +54,7 @@ def run_mxfp8(mx, orc, a, b, M, N, K):
     return d, A @ B.T, np.abs(A) @ np.abs(B).T
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (128, 256, 512), (256, 512, 1024), (200, 300, 384),
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (128, 256, 512), (256, 512, 1024), (200, 296, 384),
                                    (1, 8, 128), (640, 1280, 2048)])
 def test_mxfp8_gemm(mx, orc, M, N, K):
     a = synthetic.random_bf16(M + K, (M, K), "student_t")
@@ -107,7 +107,7 @@ def test_mxfp8_gemm_rejects_wrong_scale_layout(mx, orc):
 # ------------------------------------------------------------------------------------------------
 # NVFP4
 # ------------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 1024), (200, 300, 512), (640, 768, 2048)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 1024), (200, 296, 512), (640, 768, 2048)])
 def test_nvfp4_gemm_per_token_times_per_tensor(mx, orc, M, N, K):
     a = synthetic.random_bf16(M * 3 + K, (M, K), "student_t")
     b = synthetic.random_bf16(N * 3 + K, (N, K), "normal", 0.02)
@@ -213,3 +213,18 @@ def test_grouped_gemm_ragged(mx, orc, fmt):
         B = decode(qbs[g], sb_c) * np.float64(sws[g])
         ref = A[r0:r1] @ B.T
         check_close(orc, d[r0:r1], ref, np.abs(A[r0:r1]) @ np.abs(B).T)
+
+
+def test_nvfp4_gemm_per_column_alpha(mx, orc):
+    """Both operands per-token quantized: the B side's FP32 scales are per output column."""
+    M, N, K = 384, 520, 512
+    a = synthetic.random_bf16(21, (M, K), "student_t")
+    b = synthetic.random_bf16(22, (N, K), "student_t")
+    qa, sa, sta = orc.nvfp4_quantize_per_token(a)
+    qb, sb, stb = orc.nvfp4_quantize_per_token(b)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    mx.mx_scaled_gemm(mx.MX_FMT_NVFP4, dev_u8(qa), dev_u8(orc.scales_to_gemm_layout(sa)), dev_f32(sta), mx.MX_SCOPE_ROW,
+                      dev_u8(qb), dev_u8(orc.scales_to_gemm_layout(sb)), dev_f32(stb), mx.MX_SCOPE_ROW, M, N, K, d)
+    A = orc.decode_nvfp4_f64(qa, sa) * sta.astype(np.float64)[:, None]
+    B = orc.decode_nvfp4_f64(qb, sb) * stb.astype(np.float64)[:, None]
+    check_close(orc, d, A @ B.T, np.abs(A) @ np.abs(B).T)

@@ -255,3 +255,21 @@ def test_weight_sync_round_trip_on_device(mx, orc):
 def test_device_status_clean(mx):
     torch.cuda.synchronize()
     mx.check_device_status()
+
+
+def test_dequant_nvfp4_stacked_2d_weights_group_scope(mx, orc):
+    """Per-expert 2D weights stacked as one [G*O, H] operand dequantize in one launch with one FP32
+    scale per expert (the dequantized backward's DQ(Q(w)) for all experts)."""
+    G, O, H = 3, 256, 96
+    w = synthetic.random_bf16(31, (G, O, H), "normal", 0.02)
+    out = mx.alloc_nvfp4_weight_2d(G, O, H, DEV)
+    mx.mx_nvfp4_quantize_weight_2d(bf16_dev(w), out["q_row"], out["s_row"], out["q_col"], out["s_col"], out["s_w"],
+                                   out["ws"])
+    y = torch.empty((G * O, H), dtype=torch.bfloat16, device=DEV)
+    mx.mx_dequantize_bf16(mx.MX_FMT_NVFP4, out["q_row"], out["s_row"], out["s_w"], mx.MX_SCOPE_GROUP, G * O, H, y,
+                          group_rows=O)
+    got = to_np_u16(y).reshape(G, O, H)
+    for g in range(G):
+        qr, qc, st, sw = orc.nvfp4_quantize_weight_2d(np.ascontiguousarray(w[g]))
+        ref = orc.dequant_nvfp4(qr, orc.weight_2d_operand_scales(st, "row"), sw, per_row=False)
+        assert np.array_equal(got[g], ref), first_mismatch(got[g], ref)

@@ -35,7 +35,7 @@ MUTATIONS = {
  'w2d_tile_idx': ('s_tile[bo * th + bh] = bs;', 's_tile[bh * to + bo] = bs;'),
  'w2d_qcol': ('put_nibble(q_col + h * (O / 2), o, c);', 'put_nibble(q_col + o * (H / 2), h, c);'),
  'pt_amax_block': ('for (int64_t k = 0; k < H; ++k) amax = fmaxf', 'for (int64_t k = 0; k < 16; ++k) amax = fmaxf'),
- 'sr_index': ('orc_sr_bits16(sr_seed, (uint64_t)(t * N + n)))\n                                   : orc_e2m1_encode((double)v);\n                    put_nibble(q + n', 'orc_sr_bits16(sr_seed, (uint64_t)(n * T + t)))\n                                   : orc_e2m1_encode((double)v);\n                    put_nibble(q + n'),
+ 'sr_index': ('uint64_t gi = (uint64_t)(t * N_total + n_offset + n);', 'uint64_t gi = (uint64_t)(n * T + t);'),
  'sat448': ('uint8_t c = enumerate_nearest(fabs(v), orc_e4m3_value, 127, 448.0);', 'uint8_t c = enumerate_nearest(fabs(v), orc_e4m3_value, 126, 448.0);'),
  'second_scale': ('static const float NVFP4_S_DIV = 2688.0f;', 'static const float NVFP4_S_DIV = 448.0f;'),
  'dq_mx_scale': ('* orc_e8m0_value(s[r * (K / 32) + k / 32]);\n            y[r', '* orc_e8m0_value(s[r * (K / 32) + k / 32] + 1);\n            y[r'),

@@ -160,3 +160,18 @@ def test_sr_bits_follow_the_logical_element(orc):
         out[:, 1::2] = q >> 4
         return out
     np.testing.assert_array_equal(nib(qc).T, nib(qr))
+
+
+def test_two_pass_split_over_column_slabs_matches_whole_tensor(orc):
+    """Pass 1 max-combined over column slabs and pass 2 per slab (with global SR indices) give the
+    whole-tensor result: the transform, the blocks and the random bits are all column-local."""
+    x = synthetic.random_bf16(47, (64, 48), "student_t")
+    q, s, S = orc.nvfp4_quantize_1x16(x, colwise=True, rht=True, rht_seed=8, sr=True, sr_seed=9)
+    slabs = [(0, 16), (16, 40), (40, 48)]
+    A = max(orc.nvfp4_1x16_amax(np.ascontiguousarray(x[:, a:b]), rht=True, rht_seed=8) for a, b in slabs)
+    assert orc.nvfp4_second_scale(A) == S
+    for a, b in slabs:
+        qs, ss = orc.nvfp4_1x16_pass2(np.ascontiguousarray(x[:, a:b]), a, 48, S, colwise=True, rht=True, rht_seed=8,
+                                      sr=True, sr_seed=9)
+        np.testing.assert_array_equal(qs, q[a:b])
+        np.testing.assert_array_equal(ss, s[a:b])
