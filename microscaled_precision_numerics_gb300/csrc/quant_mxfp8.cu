@@ -51,7 +51,28 @@ __device__ __forceinline__ float chunk_elem(const uint4& v, int j) {
     return (j & 1) ? bf16_hi(w) : bf16_lo(w);
 }
 
-// CTA tile: 128 rows x 128 columns of BF16 staged in shared memory (pitch 272 B).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Issue the 16-byte loads of one 128 x 128 tile into a staging buffer (zero fill outside the tensor).
+__device__ __forceinline__ void stage_tile(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
+                                           int64_t r0, int64_t c0, uint32_t buf) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int ci = (int)threadIdx.x + QT_THREADS * j;
+        const int rr = ci >> 4, ch = ci & 15;
+        const int64_t r = r0 + rr, c = c0 + ch * 8;
+        const bool valid = r < R && c < K;
+        cp_async_16(buf + rr * QT_PITCH + ch * 16, valid ? (const void*)(x + r * ldx + c) : (const void*)x, valid);
+    }
+}
+
+// CTA tile: 128 rows x 128 columns of BF16 staged in shared memory (pitch 272 B).  Persistent CTAs
+// walk the tiles with two staging buffers: the next tile's loads are in flight while this one is
+// quantized.
 //   row pass:    thread -> (row, pair of 32-column blocks); 8 x 16-byte shared loads
 //   column pass: thread -> (8-column chunk, 32-row block, quarter of 8 rows); 8 x 16-byte shared
 //                loads; the 32-row amax combines the 4 quarters (lanes l, l^8, l^16, l^24)
@@ -59,116 +80,116 @@ template <bool ROW, bool COL>
 __global__ void __launch_bounds__(QT_THREADS)
 mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
                       uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
-                      uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
-    __shared__ __align__(16) uint8_t tile[QT_ROWS * QT_PITCH];
-    __shared__ uint8_t colsc[4][QT_COLS];
+                      uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, int64_t tiles_c, int64_t tiles) {
+    extern __shared__ __align__(16) uint8_t qsm[];
+    uint8_t (*colsc)[QT_COLS] = reinterpret_cast<uint8_t (*)[QT_COLS]>(qsm + 2 * QT_ROWS * QT_PITCH);
+    const uint32_t buf_base = (uint32_t)__cvta_generic_to_shared(qsm);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t r0 = (int64_t)blockIdx.y * QT_ROWS;
-    const int64_t c0 = (int64_t)blockIdx.x * QT_COLS;
-
-    // ---- stage: 128 rows x 16 chunks of 16 bytes; each warp reads two whole 256-byte rows ----
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int ci = tid + QT_THREADS * j;
-        const int rr = ci >> 4, ch = ci & 15;
-        const int64_t r = r0 + rr, c = c0 + ch * 8;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < R && c < K) v = __ldcs(reinterpret_cast<const uint4*>(x + r * ldx + c));
-        *reinterpret_cast<uint4*>(tile + rr * QT_PITCH + ch * 16) = v;
-    }
-    __syncthreads();
-
-    if (ROW) {
-        // lanes 0..7 take 8 different rows of the same 64-column half: conflict-free 16-byte loads
-        const int half = (tid >> 3) & 1;
-        const int rr = (tid & 7) + 8 * (tid >> 4);
-        const int64_t r = r0 + rr;
-        uint32_t s2[2];
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            uint32_t w[16];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 v = *reinterpret_cast<const uint4*>(tile + rr * QT_PITCH + half * 128 + b * 64 + i * 16);
-                w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-            }
-            uint32_t codes[8];
-            s2[b] = mxfp8_block32(w, codes);
-            const int64_t c = c0 + half * 64 + b * 32;
-            if (r < R && c < K) {
-                uint4* dst = reinterpret_cast<uint4*>(q_row + r * K + c);
-                __stcs(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-                __stcs(dst + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
-            }
-        }
-        // the row's 4 scales: this thread's two and those of lane + 8 (the other half)
-        const uint32_t mine = s2[0] | (s2[1] << 8);
-        const uint32_t other = __shfl_down_sync(0xFFFFFFFFu, mine, 8);
-        if (half == 0 && r < R) {
-            const int64_t nct = sf_col_tiles(K, 32);
-            const int64_t kb = c0 / 32;
-            const int nvalid = (int)min64(4, (K - c0) / 32);
-            uint8_t* p = s_row + sf_offset(r, kb, nct);
-            const uint32_t word = mine | (other << 16);
-            if (nvalid == 4) *reinterpret_cast<uint32_t*>(p) = word;
-            else for (int i = 0; i < nvalid; ++i) p[i] = (uint8_t)(word >> (8 * i));
-        }
-    }
-
-    if (COL) {
-        const int rb = warp >> 1;                        // 32-row block
-        const int chunk = (warp & 1) * 8 + (lane & 7);   // 8-column chunk
-        const int q = lane >> 3;                         // quarter: rows q*8 .. q*8+7 of the block
-        uint4 v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            v[i] = *reinterpret_cast<const uint4*>(tile + (rb * 32 + q * 8 + i) * QT_PITCH + chunk * 16);
-        // per-column |max| as packed 16-bit pairs, then across the four quarters
-        uint32_t m[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            m[0] = absmax_bf16x2(m[0], v[i].x); m[1] = absmax_bf16x2(m[1], v[i].y);
-            m[2] = absmax_bf16x2(m[2], v[i].z); m[3] = absmax_bf16x2(m[3], v[i].w);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            m[k] = __vmaxu2(m[k], __shfl_xor_sync(0xFFFFFFFFu, m[k], 8));
-            m[k] = __vmaxu2(m[k], __shfl_xor_sync(0xFFFFFFFFu, m[k], 16));
-        }
-        const int64_t rbase = r0 + rb * 32;
-        const bool rows_ok = rbase < R;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t a16 = (j & 1) ? (m[j >> 1] >> 16) : (m[j >> 1] & 0xFFFFu);
-            const uint32_t s = e8m0_from_amax_bits(a16);
-            const float f = inv_scale_from_e8m0(s);
-            const uint32_t lo = cvt_e4m3x4(__fmul_rn(chunk_elem(v[0], j), f), __fmul_rn(chunk_elem(v[1], j), f),
-                                           __fmul_rn(chunk_elem(v[2], j), f), __fmul_rn(chunk_elem(v[3], j), f));
-            const uint32_t hi = cvt_e4m3x4(__fmul_rn(chunk_elem(v[4], j), f), __fmul_rn(chunk_elem(v[5], j), f),
-                                           __fmul_rn(chunk_elem(v[6], j), f), __fmul_rn(chunk_elem(v[7], j), f));
-            const int64_t c = c0 + chunk * 8 + j;
-            if (rows_ok && c < K)
-                __stcs(reinterpret_cast<uint2*>(q_col + c * R + rbase + q * 8), make_uint2(lo, hi));
-            if (q == 0) colsc[rb][chunk * 8 + j] = (uint8_t)s;
-        }
+    int64_t t = blockIdx.x;
+    if (t < tiles) stage_tile(x, R, K, ldx, (t / tiles_c) * QT_ROWS, (t % tiles_c) * QT_COLS, buf_base);
+    cp_async_commit();
+    for (int it = 0; t < tiles; ++it, t += gridDim.x) {
+        const int64_t tn = t + gridDim.x;
+        if (tn < tiles)
+            stage_tile(x, R, K, ldx, (tn / tiles_c) * QT_ROWS, (tn % tiles_c) * QT_COLS,
+                       buf_base + ((it + 1) & 1) * QT_ROWS * QT_PITCH);
+        cp_async_commit();
+        cp_async_wait_1();
         __syncthreads();
-        // one 32-bit word of 4 row-block scales per column (r0 / 32 is a multiple of 4)
-        if (tid < QT_COLS) {
-            const int64_t cw = c0 + tid;
-            if (cw < K) {
-                const int64_t nct = sf_col_tiles(R, 32);
-                const int64_t rbk = r0 / 32;
-                const int nvalid = (int)min64(4, (R - r0) / 32);
-                uint8_t* p = s_col + sf_offset(cw, rbk, nct);
-                if (nvalid == 4) {
-                    *reinterpret_cast<uint32_t*>(p) = (uint32_t)colsc[0][tid] | ((uint32_t)colsc[1][tid] << 8) |
-                                                      ((uint32_t)colsc[2][tid] << 16) | ((uint32_t)colsc[3][tid] << 24);
-                } else {
-                    for (int i = 0; i < nvalid; ++i) p[i] = colsc[i][tid];
+        const uint8_t* tile = qsm + (it & 1) * QT_ROWS * QT_PITCH;
+        const int64_t r0 = (t / tiles_c) * QT_ROWS;
+        const int64_t c0 = (t % tiles_c) * QT_COLS;
+
+        if (ROW) {
+            // lanes 0..7 take 8 different rows of the same 64-column half: conflict-free 16-byte loads
+            const int half = (tid >> 3) & 1;
+            const int rr = (tid & 7) + 8 * (tid >> 4);
+            const int64_t r = r0 + rr;
+            uint32_t s2[2];
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(tile + rr * QT_PITCH + half * 128 + b * 64 + i * 16);
+                    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+                }
+                uint32_t codes[8];
+                s2[b] = mxfp8_block32(w, codes);
+                const int64_t c = c0 + half * 64 + b * 32;
+                if (r < R && c < K) {
+                    uint4* dst = reinterpret_cast<uint4*>(q_row + r * K + c);
+                    __stcs(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
+                    __stcs(dst + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+                }
+            }
+            // the row's 4 scales: this thread's two and those of lane + 8 (the other half)
+            const uint32_t mine = s2[0] | (s2[1] << 8);
+            const uint32_t other = __shfl_down_sync(0xFFFFFFFFu, mine, 8);
+            if (half == 0 && r < R) {
+                const int64_t nct = sf_col_tiles(K, 32);
+                const int nvalid = (int)min64(4, (K - c0) / 32);
+                uint8_t* p = s_row + sf_offset(r, c0 / 32, nct);
+                const uint32_t word = mine | (other << 16);
+                if (nvalid == 4) *reinterpret_cast<uint32_t*>(p) = word;
+                else for (int i = 0; i < nvalid; ++i) p[i] = (uint8_t)(word >> (8 * i));
+            }
+        }
+
+        if (COL) {
+            const int rb = warp >> 1;                        // 32-row block
+            const int chunk = (warp & 1) * 8 + (lane & 7);   // 8-column chunk
+            const int q = lane >> 3;                         // quarter: rows q*8 .. q*8+7 of the block
+            uint4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[i] = *reinterpret_cast<const uint4*>(tile + (rb * 32 + q * 8 + i) * QT_PITCH + chunk * 16);
+            uint32_t m[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                m[0] = absmax_bf16x2(m[0], v[i].x); m[1] = absmax_bf16x2(m[1], v[i].y);
+                m[2] = absmax_bf16x2(m[2], v[i].z); m[3] = absmax_bf16x2(m[3], v[i].w);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                m[k] = __vmaxu2(m[k], __shfl_xor_sync(0xFFFFFFFFu, m[k], 8));
+                m[k] = __vmaxu2(m[k], __shfl_xor_sync(0xFFFFFFFFu, m[k], 16));
+            }
+            const int64_t rbase = r0 + rb * 32;
+            const bool rows_ok = rbase < R;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t a16 = (j & 1) ? (m[j >> 1] >> 16) : (m[j >> 1] & 0xFFFFu);
+                const uint32_t sc = e8m0_from_amax_bits(a16);
+                const float f = inv_scale_from_e8m0(sc);
+                const uint32_t lo = cvt_e4m3x4(__fmul_rn(chunk_elem(v[0], j), f), __fmul_rn(chunk_elem(v[1], j), f),
+                                               __fmul_rn(chunk_elem(v[2], j), f), __fmul_rn(chunk_elem(v[3], j), f));
+                const uint32_t hi = cvt_e4m3x4(__fmul_rn(chunk_elem(v[4], j), f), __fmul_rn(chunk_elem(v[5], j), f),
+                                               __fmul_rn(chunk_elem(v[6], j), f), __fmul_rn(chunk_elem(v[7], j), f));
+                const int64_t c = c0 + chunk * 8 + j;
+                if (rows_ok && c < K)
+                    __stcs(reinterpret_cast<uint2*>(q_col + c * R + rbase + q * 8), make_uint2(lo, hi));
+                if (q == 0) colsc[rb][chunk * 8 + j] = (uint8_t)sc;
+            }
+            __syncthreads();
+            // one 32-bit word of 4 row-block scales per column (r0 / 32 is a multiple of 4)
+            if (tid < QT_COLS) {
+                const int64_t cw = c0 + tid;
+                if (cw < K) {
+                    const int64_t nct = sf_col_tiles(R, 32);
+                    const int nvalid = (int)min64(4, (R - r0) / 32);
+                    uint8_t* p = s_col + sf_offset(cw, r0 / 32, nct);
+                    if (nvalid == 4) {
+                        *reinterpret_cast<uint32_t*>(p) = (uint32_t)colsc[0][tid] | ((uint32_t)colsc[1][tid] << 8) |
+                                                          ((uint32_t)colsc[2][tid] << 16) | ((uint32_t)colsc[3][tid] << 24);
+                    } else {
+                        for (int i = 0; i < nvalid; ++i) p[i] = colsc[i][tid];
+                    }
                 }
             }
         }
+        __syncthreads();   // this buffer (and colsc) is refilled two iterations later
     }
 }
 
@@ -186,13 +207,22 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64
         cudaError_t e = cudaMemsetAsync(s_col, 0, (size_t)host_scale_bytes(K, R, 32), stream);
         if (e != cudaSuccess) return e;
     }
-    dim3 grid((unsigned)((K + QT_COLS - 1) / QT_COLS), (unsigned)((R + QT_ROWS - 1) / QT_ROWS));
+    const int64_t tiles_c = (K + QT_COLS - 1) / QT_COLS, tiles = tiles_c * ((R + QT_ROWS - 1) / QT_ROWS);
+    const size_t smem = 2 * QT_ROWS * QT_PITCH + 4 * QT_COLS;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaFuncSetAttribute(mxfp8_quantize_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(mxfp8_quantize_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(mxfp8_quantize_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attr_done = true;
+    }
+    const unsigned grid = (unsigned)min64(tiles, (int64_t)device_sm_count() * 3);
     if (row && col)
-        mxfp8_quantize_kernel<true, true><<<grid, QT_THREADS, 0, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col);
+        mxfp8_quantize_kernel<true, true><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col, tiles_c, tiles);
     else if (row)
-        mxfp8_quantize_kernel<true, false><<<grid, QT_THREADS, 0, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col);
+        mxfp8_quantize_kernel<true, false><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col, tiles_c, tiles);
     else
-        mxfp8_quantize_kernel<false, true><<<grid, QT_THREADS, 0, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col);
+        mxfp8_quantize_kernel<false, true><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col, tiles_c, tiles);
     return cudaGetLastError();
 }
 
