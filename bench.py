@@ -188,10 +188,10 @@ class MoE:
     down-projection input, and DQ(Q(w)) of both weight stacks."""
     name = "moe"
 
-    def __init__(self, mx, torch, dev):
+    def __init__(self, mx, torch, dev, experts=128):
         import synthetic
         self.mx, self.torch, self.dev = mx, torch, dev
-        d = synthetic.moe()
+        d = synthetic.moe(experts=experts)
         bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
         x = bf(d["x"])
         self.rows = int(d["group_offsets"][-1])
@@ -204,8 +204,8 @@ class MoE:
         G, O1, H = self.wgu.shape
         _, O2, F = self.wd.shape
         self.G, self.H, self.F, self.O1, self.O2 = G, H, F, O1, O2
-        self.qa = mx.alloc_nvfp4_rows(self.rows, H, dev)
-        self.qdn = mx.alloc_nvfp4_rows(self.rows, F, dev)
+        self.qa = mx.alloc_nvfp4_rows_grouped(self.rows, G, H, dev)
+        self.qdn = mx.alloc_nvfp4_rows_grouped(self.rows, G, F, dev)
         self.qgu = mx.alloc_nvfp4_weight_2d(G, O1, H, dev)
         self.qwd = mx.alloc_nvfp4_weight_2d(G, O2, F, dev)
         self.y1 = torch.empty((self.rows, O1), dtype=torch.bfloat16, device=dev)
@@ -221,7 +221,7 @@ class MoE:
         w = self.qwd
         return [
             ("quant", "nvfp4_per_token A", 1, R * H * (2 + 0.5 + 1 / 16) + 4 * R,
-             lambda: mx.mx_nvfp4_quantize_per_token(self.a, self.qa["q"], self.qa["s"], self.qa["s2"])),
+             lambda: mx.mx_nvfp4_quantize_per_token_grouped(self.a, self.offs, self.qa["q"], self.qa["s"], self.qa["s2"])),
             ("quant", "nvfp4_weight_2d gate_up", 1, G * O1 * H * (2 + 1 + 2 / 16),
              lambda: mx.mx_nvfp4_quantize_weight_2d(self.wgu, q["q_row"], q["s_row"], q["q_col"], q["s_col"], q["s_w"], q["ws"])),
             ("quant", "nvfp4_weight_2d down", 1, G * O2 * F * (2 + 1 + 2 / 16),
@@ -230,7 +230,8 @@ class MoE:
              lambda: mx.mx_grouped_scaled_gemm(F4, self.offs, self.qa["q"], self.qa["s"], self.qa["s2"], q["q_row"],
                                                q["s_row"], q["s_w"], O1, H, self.y1)),
             ("quant", "nvfp4_per_token down input", 1, R * F * (2 + 0.5 + 1 / 16) + 4 * R,
-             lambda: mx.mx_nvfp4_quantize_per_token(self.down_in, self.qdn["q"], self.qdn["s"], self.qdn["s2"])),
+             lambda: mx.mx_nvfp4_quantize_per_token_grouped(self.down_in, self.offs, self.qdn["q"], self.qdn["s"],
+                                                            self.qdn["s2"])),
             ("gemm4", "grouped down", 0, 2.0 * R * O2 * F,
              lambda: mx.mx_grouped_scaled_gemm(F4, self.offs, self.qdn["q"], self.qdn["s"], self.qdn["s2"], w["q_row"],
                                                w["s_row"], w["s_w"], O2, F, self.y2)),
@@ -305,10 +306,10 @@ class WeightSync:
     (torch generator seeded 1000 + layer) outside the timed kernels."""
     name = "weight_sync"
 
-    def __init__(self, mx, torch, dev, layers=48):
+    def __init__(self, mx, torch, dev, layers=48, experts=128):
         self.mx, self.torch, self.dev = mx, torch, dev
         self.layers = layers
-        self.shapes = [(128, 2048, 768), (128, 768, 2048), (128, 768, 2048)]
+        self.shapes = [(experts, 2048, 768), (experts, 768, 2048), (experts, 768, 2048)]
         self.layer = 0
         self.bufs = []
         for (G, O, H) in self.shapes:
@@ -441,7 +442,7 @@ def run_workload(args):
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     sampler = ClockSampler(0)
     if args.workload == "weight_sync":
-        work = WeightSync(mx, torch, dev, layers=args.layers)
+        work = WeightSync(mx, torch, dev, layers=args.layers, experts=args.experts)
         ops = work.ops()
         acc = [0.0] * len(ops)
         total_ms = 0.0
@@ -466,7 +467,7 @@ def run_workload(args):
                 "gpu_launches": work.launches_per_step * work.layers}
         print(json.dumps(line), flush=True)
         return
-    work = MoE(mx, torch, dev) if args.workload == "moe" else WGrad(mx, torch, dev)
+    work = MoE(mx, torch, dev, experts=args.experts) if args.workload == "moe" else WGrad(mx, torch, dev)
     ops = work.ops()
     sampler.start()
     total_ms, per_op = time_ops(ops, torch, args.steps, args.warmup)
@@ -697,6 +698,7 @@ def main():
     ap.add_argument("--impl", choices=["mxnum", "reference"], default="mxnum")
     ap.add_argument("--workload", choices=["dense_mlp", "moe", "wgrad", "weight_sync"], default="dense_mlp")
     ap.add_argument("--layers", type=int, default=48, help="weight_sync: layers swept")
+    ap.add_argument("--experts", type=int, default=128, help="moe / weight_sync: experts (fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

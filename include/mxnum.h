@@ -46,6 +46,9 @@ typedef enum {
 } mx_status;
 
 typedef enum { MX_FMT_MXFP8 = 0, MX_FMT_NVFP4 = 1 } mx_format;
+
+/* Largest number of expert groups the grouped entry points accept. */
+#define MX_MAX_GROUPS 1024
 typedef enum { MX_ROUND_RNE = 0, MX_ROUND_SR = 1 } mx_round;
 /* Scope of an FP32 second-level scale / GEMM epilogue factor. */
 typedef enum { MX_SCOPE_NONE = 0, MX_SCOPE_TENSOR = 1, MX_SCOPE_ROW = 2, MX_SCOPE_GROUP = 3 } mx_scope;
@@ -83,6 +86,28 @@ mx_status mx_quantize_mxfp8(const void* x, int64_t rows, int64_t cols, int64_t l
  * Requires H % 16 == 0. */
 mx_status mx_nvfp4_quantize_per_token(const void* x, int64_t T, int64_t H, int64_t ldx,
                                       uint8_t* q, uint8_t* s, float* s_tok, cudaStream_t stream);
+
+/* Grouped scale layout for expert-sorted rows (the A operand of mx_grouped_scaled_gemm): the
+ * scales of group g's rows [off[g], off[g+1]) start on a 128-row tile of the GEMM layout, at padded
+ * row P_g = sum over j < g of ceil(m_j / 128) * 128; row r of group g sits at padded row
+ * P_g + (r - off[g]).  The rows between groups are zero.  Codes stay in plain row order.
+ * Source: Miles page -- NVFP4 on the routed experts; E2E page Table 6 and Table 10 F3 (a separate
+ * scale rearrangement costs time and can go stale, so the quantizer writes the GEMM's layout).
+ * mx_grouped_scale_bytes(rows, G, k, block) = mx_scale_bytes(rows + 127 * G, k, block) bounds it. */
+int64_t mx_grouped_scale_bytes(int64_t rows, int64_t G, int64_t k, int block);
+
+/* mx_nvfp4_quantize_per_token for expert-sorted rows: identical codes and token scales, block
+ * scales in the grouped scale layout.  group_offsets: DEVICE int64 [G + 1] (as for
+ * mx_grouped_scaled_gemm); s: mx_grouped_scale_bytes(T, G, H, 16) bytes.  1 <= G <= MX_MAX_GROUPS. */
+mx_status mx_nvfp4_quantize_per_token_grouped(const void* x, int64_t T, int64_t H, int64_t ldx, int64_t G,
+                                              const int64_t* group_offsets, uint8_t* q, uint8_t* s,
+                                              float* s_tok, cudaStream_t stream);
+
+/* mx_quantize_mxfp8 row-wise for expert-sorted rows: identical codes, scales in the grouped scale
+ * layout.  s_row: mx_grouped_scale_bytes(rows, G, cols, 32) bytes.  1 <= G <= MX_MAX_GROUPS. */
+mx_status mx_quantize_mxfp8_grouped(const void* x, int64_t rows, int64_t cols, int64_t ldx, int64_t G,
+                                    const int64_t* group_offsets, uint8_t* q_row, uint8_t* s_row,
+                                    cudaStream_t stream);
 
 /* NVFP4 16x16 2D weight quantize, both orientations, for G stacked matrices.
  * Source: MaxText page, "NVFP4 pretraining recipe" -- one FP8 scale per 16x16 weight block so that
@@ -181,11 +206,13 @@ mx_status mx_scaled_gemm(mx_format fmt,
  *   D[rows of g] = BF16( alpha_a[row] * alpha_b[g] * A[rows of g] . B_g^T ).
  * Source: Miles page -- NVFP4 on the routed experts' weights and activations with a per-token
  * scale; E2E page Table 2 (Qwen3-30B-A3B: 128 experts, top-8).
- *   group_offsets: DEVICE int64 [G + 1], nondecreasing, offsets[0] = 0, offsets[G] = total_rows.
- *   a [total_rows, K(/2)], sa mx_scale_bytes(total_rows, K, block) (rows in expert-sorted order),
+ *   group_offsets: DEVICE int64 [G + 1], nondecreasing, offsets[0] = 0, offsets[G] = total_rows;
+ *   1 <= G <= MX_MAX_GROUPS.
+ *   a [total_rows, K(/2)] codes in plain row order; sa in the grouped scale layout
+ *   (mx_grouped_scale_bytes(total_rows, G, K, block), as written by the *_grouped quantizers);
  *   alpha_a_rows [total_rows] FP32 or NULL;  b [G, N, K(/2)], sb G * mx_scale_bytes(N, K, block),
  *   alpha_b_groups [G] FP32 or NULL;  d [total_rows, N] BF16.
- * Same K and alignment rules as mx_scaled_gemm. */
+ * Same K rules as mx_scaled_gemm; N % 8 == 0. */
 mx_status mx_grouped_scaled_gemm(mx_format fmt, int64_t G, const int64_t* group_offsets,
                                  int64_t total_rows,
                                  const uint8_t* a, const uint8_t* sa, const float* alpha_a_rows,

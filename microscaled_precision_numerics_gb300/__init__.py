@@ -48,6 +48,9 @@ def lib() -> ctypes.CDLL:
                 "mx_workspace_bytes": (SZ, [I32, I64, I64]),
                 "mx_quantize_mxfp8": (I32, [P, I64, I64, I64, P, P, P, P, P]),
                 "mx_nvfp4_quantize_per_token": (I32, [P, I64, I64, I64, P, P, P, P]),
+                "mx_nvfp4_quantize_per_token_grouped": (I32, [P, I64, I64, I64, I64, P, P, P, P, P]),
+                "mx_quantize_mxfp8_grouped": (I32, [P, I64, I64, I64, I64, P, P, P, P]),
+                "mx_grouped_scale_bytes": (I64, [I64, I64, I64, I32]),
                 "mx_nvfp4_quantize_weight_2d": (I32, [P, I64, I64, I64, P, P, P, P, P, P, SZ, P]),
                 "mx_rht16": (I32, [P, I64, I64, U64, P, P]),
                 "mx_nvfp4_quantize_1x16": (I32, [P, I64, I64, I32, I32, U64, I32, U64, P, P, P, P, SZ, P]),
@@ -119,6 +122,26 @@ def mx_nvfp4_quantize_per_token(x, q, s, s_tok, stream=None):
     T, H = x.shape
     _check("mx_nvfp4_quantize_per_token", lib().mx_nvfp4_quantize_per_token(
         _p(x), T, H, x.stride(0), _p(q), _p(s), _p(s_tok), _stream(stream)))
+
+
+def mx_nvfp4_quantize_per_token_grouped(x, group_offsets, q, s, s_tok, stream=None):
+    x = _bf16_bits(x)
+    T, H = x.shape
+    _check("mx_nvfp4_quantize_per_token_grouped", lib().mx_nvfp4_quantize_per_token_grouped(
+        _p(x), T, H, x.stride(0), group_offsets.numel() - 1, _p(group_offsets), _p(q), _p(s), _p(s_tok),
+        _stream(stream)))
+
+
+def mx_quantize_mxfp8_grouped(x, group_offsets, q_row, s_row, stream=None):
+    x = _bf16_bits(x)
+    rows, cols = x.shape
+    _check("mx_quantize_mxfp8_grouped", lib().mx_quantize_mxfp8_grouped(
+        _p(x), rows, cols, x.stride(0), group_offsets.numel() - 1, _p(group_offsets), _p(q_row), _p(s_row),
+        _stream(stream)))
+
+
+def grouped_scale_bytes(rows: int, G: int, k: int, block: int) -> int:
+    return int(lib().mx_grouped_scale_bytes(rows, G, k, block))
 
 
 def mx_nvfp4_quantize_weight_2d(w, q_row, s_row, q_col, s_col, s_w, workspace, stream=None):
@@ -211,6 +234,13 @@ def alloc_nvfp4_rows(rows: int, k: int, device):
     """Codes [rows, k/2], GEMM-layout scales and one FP32 second-level scale per row."""
     return {"q": torch.empty((rows, k // 2), dtype=torch.uint8, device=device),
             "s": _u8(scale_bytes(rows, k, 16), device),
+            "s2": torch.empty(rows, dtype=torch.float32, device=device)}
+
+
+def alloc_nvfp4_rows_grouped(rows: int, G: int, k: int, device):
+    """Like alloc_nvfp4_rows with the scales sized for the grouped scale layout."""
+    return {"q": torch.empty((rows, k // 2), dtype=torch.uint8, device=device),
+            "s": _u8(grouped_scale_bytes(rows, G, k, 16), device),
             "s2": torch.empty(rows, dtype=torch.float32, device=device)}
 
 

@@ -12,11 +12,13 @@
 //   warp 0        TMA producer: A/B tiles (128-byte swizzle) and scale atoms into a 4-stage ring
 //   warp 1        TMEM allocator; lane 0 issues tcgen05.cp (scales -> TMEM) and tcgen05.mma
 //   warps 2..5    epilogue: tcgen05.ld the FP32 accumulator, scale, round to BF16, store
-// Scales arrive in the GEMM layout (512-byte atoms of 128 rows x 4 scale columns); one atom is
-// copied to TMEM with tcgen05.cp.32x128b.warpx4.  For the grouped GEMM the A-side atoms of a tile
-// that starts at an arbitrary row are gathered word by word by the producer warp.
+// Scales arrive in the GEMM layout (512-byte atoms of 128 rows x 4 scale columns) and each stage's
+// atoms are bulk-copied to shared memory, then to TMEM with tcgen05.cp.32x128b.warpx4.  For the
+// grouped GEMM the A scales are in the grouped layout, where every expert group starts on a
+// 128-row band, so a tile at an arbitrary row offset still reads whole atoms.
 // Every mbarrier wait is bounded: on expiry the CTA records MX_ERR_TIMEOUT in a device word, stops
 // issuing work, drains what it issued and frees its TMEM.
+#include "../../include/mxnum.h"
 #include "mx_internal.h"
 
 #include <cuda.h>
@@ -38,7 +40,7 @@ constexpr int A_STAGE_BYTES = BM * BKB;   // 16 KB
 constexpr int B_STAGE_BYTES = BN * BKB;   // 32 KB
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_SF_BASE = 256;         // accumulator uses columns [0, 256)
-constexpr int MAX_GROUPS = 1024;
+constexpr int MAX_GROUPS = MX_MAX_GROUPS;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
 
 template <int FMT>
@@ -55,7 +57,8 @@ struct Cfg {
     static constexpr int SMEM_BAR = SMEM_SFB + STAGES * SFB_BYTES;
     static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * STAGES + 4);
     static constexpr int SMEM_PREFIX = SMEM_MISC + 16;
-    static constexpr int SMEM_TOTAL = SMEM_PREFIX + 4 * (MAX_GROUPS + 1);
+    static constexpr int SMEM_WARP = SMEM_PREFIX + 4 * (MAX_GROUPS + 1);
+    static constexpr int SMEM_TOTAL = SMEM_WARP + 4 * 32;
     static constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;  // slack for 1024-byte alignment
     static_assert(TMEM_SF_BASE + STAGES * (SFA_COLS + SFB_COLS) <= TMEM_COLS, "TMEM budget");
 };
@@ -195,6 +198,7 @@ struct Tile {
     int64_t row0, row_end;   // A rows [row0, row0 + 128) of which [row0, row_end) are real
     int64_t n0;              // first output column
     int64_t g;               // group (grouped GEMM) or 0
+    int64_t sf_tile;         // 128-row band of A's scale layout holding this tile's scales
 };
 
 // Dense: bands of 16 M-tiles; inside a band N-tiles advance every 16 tiles (L2 reuse of A and B).
@@ -205,22 +209,27 @@ __device__ __forceinline__ Tile dense_tile(const Params& p, int64_t t) {
     const int64_t band_m = min64(GM, p.m_tiles - band * GM);
     const int64_t mt = band * GM + in % band_m, nt = in / band_m;
     Tile r;
-    r.row0 = mt * BM; r.row_end = p.M; r.n0 = nt * BN; r.g = 0;
+    r.row0 = mt * BM; r.row_end = p.M; r.n0 = nt * BN; r.g = 0; r.sf_tile = mt;
     return r;
 }
 
-__device__ __forceinline__ Tile grouped_tile(const Params& p, const int* prefix, int64_t t) {
-    int lo = 0, hi = (int)p.G;   // prefix[g] <= t < prefix[g + 1]
+// Grouped: ptile[g] = M-tiles of groups < g (also group g's first 128-row band in the grouped scale
+// layout); output tiles of group g are [ptile[g] * n_tiles, ptile[g + 1] * n_tiles).
+__device__ __forceinline__ Tile grouped_tile(const Params& p, const int* ptile, int64_t t) {
+    const int64_t mt_global = t / p.n_tiles;      // tiles are ordered group by group, M-tile major
+    int lo = 0, hi = (int)p.G;                    // ptile[g] <= mt_global < ptile[g + 1]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= t) lo = mid; else hi = mid;
+        if (ptile[mid] <= mt_global) lo = mid; else hi = mid;
     }
     const int64_t g = lo;
-    const int64_t r0 = p.group_offsets[g], r1 = p.group_offsets[g + 1];
-    const int64_t mtiles = (r1 - r0 + BM - 1) / BM;
-    const int64_t local = t - prefix[g];
+    const int64_t mt = mt_global - ptile[g];
     Tile r;
-    r.row0 = r0 + (local % mtiles) * BM; r.row_end = r1; r.n0 = (local / mtiles) * BN; r.g = g;
+    r.row0 = __ldg(p.group_offsets + g) + mt * BM;
+    r.row_end = __ldg(p.group_offsets + g + 1);
+    r.n0 = (t % p.n_tiles) * BN;
+    r.g = g;
+    r.sf_tile = mt_global;
     return r;
 }
 
@@ -241,7 +250,8 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t bar_done = bar_tempty + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
-    int* prefix = reinterpret_cast<int*>(smem + C::SMEM_PREFIX);
+    int* ptile = reinterpret_cast<int*>(smem + C::SMEM_PREFIX);
+    int* s_warp = reinterpret_cast<int*>(smem + C::SMEM_WARP);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -265,23 +275,12 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     int64_t total_tiles;
-    if (GROUPED) {
-        // prefix[g] = output tiles of groups < g: counts in parallel, then one scan in shared memory
-        for (int64_t g = threadIdx.x; g < p.G; g += NUM_THREADS) {
-            const int64_t rows = __ldg(p.group_offsets + g + 1) - __ldg(p.group_offsets + g);
-            prefix[g + 1] = (int)(((rows + BM - 1) / BM) * p.n_tiles);
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            prefix[0] = 0;
-            for (int64_t g = 1; g <= p.G; ++g) prefix[g] += prefix[g - 1];
-        }
-    }
+    if (GROUPED) scan_group_tiles(p.group_offsets, (int)p.G, ptile, s_warp);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    total_tiles = GROUPED ? (int64_t)prefix[p.G] : p.total_tiles;
+    total_tiles = GROUPED ? (int64_t)ptile[p.G] * p.n_tiles : p.total_tiles;
 
     if (warp == 0) {
         // ------------------------------- producer -------------------------------
@@ -291,7 +290,7 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-            const Tile tile = GROUPED ? grouped_tile(p, prefix, t) : dense_tile(p, t);
+            const Tile tile = GROUPED ? grouped_tile(p, ptile, t) : dense_tile(p, t);
             const int64_t brow = (GROUPED ? tile.g * p.N : 0) + tile.n0;
             const uint8_t* sb_g = p.sb + (GROUPED ? tile.g * p.sb_group_bytes : 0);
             const int64_t bt0 = tile.n0 / 128;                      // first 128-row band of B
@@ -303,30 +302,13 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const uint32_t sSFA = sbase + C::SMEM_SFA + stage * C::SFA_BYTES;
                 const uint32_t sSFB = sbase + C::SMEM_SFB + stage * C::SFB_BYTES;
                 const int64_t ct0 = ks * C::SF_ATOMS_A;             // first 4-column scale tile of this stage
-                if (GROUPED) {
-                    // gather the A-side atoms: row i of the tile -> line (i % 32), word (i / 32)
-                    uint32_t* dst = reinterpret_cast<uint32_t*>(smem + C::SMEM_SFA + stage * C::SFA_BYTES);
-                    for (int idx = lane; idx < BM * C::SF_ATOMS_A; idx += 32) {
-                        const int i = idx % BM, atom = idx / BM;
-                        const int64_t r = tile.row0 + i;
-                        uint32_t w = 0;
-                        if (r < p.M)
-                            w = __ldg(reinterpret_cast<const uint32_t*>(p.sa + ((((r >> 7) * p.nct + ct0 + atom) << 9) +
-                                                                                ((r & 31) << 4) + (((r >> 5) & 3) << 2))));
-                        dst[atom * 128 + (i & 31) * 4 + (i >> 5)] = w;
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
                 if (lane == 0) {
-                    uint32_t bytes = A_STAGE_BYTES + B_STAGE_BYTES + C::SFB_BYTES / (b_hi ? 1 : 2);
-                    if (!GROUPED) bytes += C::SFA_BYTES;
+                    const uint32_t bytes = A_STAGE_BYTES + B_STAGE_BYTES + C::SFA_BYTES + C::SFB_BYTES / (b_hi ? 1 : 2);
                     mbar_arrive_expect_tx(bar_full + 8 * stage, bytes);
                     const int32_t kb = (int32_t)(ks * BKB);
                     tma_load_2d(sA, &tmA, kb, (int32_t)tile.row0, bar_full + 8 * stage);
                     tma_load_2d(sB, &tmB, kb, (int32_t)brow, bar_full + 8 * stage);
-                    if (!GROUPED)
-                        bulk_load(sSFA, p.sa + (((tile.row0 >> 7) * p.nct + ct0) << 9), C::SFA_BYTES, bar_full + 8 * stage);
+                    bulk_load(sSFA, p.sa + ((tile.sf_tile * p.nct + ct0) << 9), C::SFA_BYTES, bar_full + 8 * stage);
                     bulk_load(sSFB, sb_g + ((bt0 * p.nct + ct0) << 9), C::SFA_BYTES, bar_full + 8 * stage);
                     if (b_hi)
                         bulk_load(sSFB + C::SFA_BYTES, sb_g + (((bt0 + 1) * p.nct + ct0) << 9), C::SFA_BYTES,
@@ -399,7 +381,7 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int q = warp & 3;                     // TMEM lane quadrant this warp may access
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-            const Tile tile = GROUPED ? grouped_tile(p, prefix, t) : dense_tile(p, t);
+            const Tile tile = GROUPED ? grouped_tile(p, ptile, t) : dense_tile(p, t);
             if (!mbar_wait(bar_tfull, acc_phase, abort_flag)) break;
             tc_fence_after();
             const int64_t row = tile.row0 + q * 32 + lane;

@@ -79,21 +79,24 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
 // Stochastic rounding onto the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6} with 16 random bits.
 // a = |v|; a >= 6 -> 6; else lo/hi are the neighbouring grid points, f = (a - lo) / (hi - lo)
 // (exact), and the result rounds up iff f > bits * 2^-16.  Returns the 4-bit code (sign kept).
+// Evaluated on the FP32 bit fields (same decisions as the quotient form).
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t bits16) {
-    const float a = fabsf(v);
-    uint32_t code;
-    if (a >= 6.0f) {
-        code = 7u;
-    } else {
-        // index of the largest grid point <= a
-        uint32_t lo = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) + (a >= 4.0f);
-        const float lov = lo < 4 ? 0.5f * (float)lo : (lo == 4 ? 2.0f : (lo == 5 ? 3.0f : 4.0f));
-        const float step = lo < 4 ? 0.5f : (lo < 6 ? 1.0f : 2.0f);
-        const float f = __fdiv_rn(__fsub_rn(a, lov), step);
-        const float u = __fmul_rn((float)bits16, 1.0f / 65536.0f);
-        code = lo + (f > u ? 1u : 0u);
-    }
+    // For a in [1, 6) the two grid points of each binade [2^e, 2^(e+1)) are 2^e and 1.5 * 2^e, so the
+    // lower grid point is picked by the top mantissa bit and f is exactly the remaining 22 mantissa
+    // bits over 2^22; f > bits16 * 2^-16 is then the integer compare below.  In [0.5, 1) the only grid
+    // point is 0.5 and f is the whole 23-bit mantissa over 2^23.  Below 0.5 the quotient 2a is formed.
+    // All four cases are evaluated and selected without branches.
+    const uint32_t u = __float_as_uint(v) & 0x7FFFFFFFu;
+    const float a = __uint_as_float(u);
+    const int e = (int)(u >> 23) - 127;
+    const uint32_t m = u & 0x7FFFFFu;
+    const uint32_t c_small = __fmul_rn(a, 2.0f) > __fmul_rn((float)bits16, 1.0f / 65536.0f) ? 1u : 0u;
+    const uint32_t c_half = 1u + ((m > (bits16 << 7)) ? 1u : 0u);
+    const uint32_t c_norm = 2u + 2u * (uint32_t)max(e, 0) + (m >> 22) + (((m & 0x3FFFFFu) > (bits16 << 6)) ? 1u : 0u);
+    uint32_t code = e < 0 ? c_half : c_norm;
+    code = a < 0.5f ? c_small : code;
+    code = a >= 6.0f ? 7u : code;
     return code | ((__float_as_uint(v) >> 28) & 8u);
 }
 
@@ -174,4 +177,74 @@ __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
 }
 __device__ __forceinline__ uint32_t fold_halves(uint32_t m2) { return max(m2 & 0xFFFFu, m2 >> 16); }
 
+// ---------------------------------------------------------------------------------------------
+// Expert-group tables for the grouped scale layout: group g's rows [off[g], off[g+1]) start at
+// padded 128-row tile ptile[g] = sum over j < g of ceil(m_j / 128).  Built by a whole block:
+// offsets copied to shared memory, tile counts scanned in parallel (warp shuffles + one pass over
+// the warp totals).  s_off needs G + 1 entries, s_ptile G + 1 entries, s_warp 32 entries.
+// ---------------------------------------------------------------------------------------------
+// Tile prefix only, reading the offsets through `off` (shared or global memory).
+__device__ __forceinline__ void scan_group_tiles(const int64_t* off, int G, int* s_ptile, int* s_warp) {
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, wid = tid >> 5, nwarps = nthr >> 5;
+    // thread tid owns groups [tid * per, tid * per + per)
+    const int per = (G + nthr - 1) / nthr;
+    int local = 0;
+    for (int k = 0; k < per; ++k) {
+        const int g = tid * per + k;
+        if (g < G) local += (int)((off[g + 1] - off[g] + 127) / 128);
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_warp[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int w = lane < nwarps ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, w, o);
+            if (lane >= o) w += v;
+        }
+        if (lane < nwarps) s_warp[lane] = w;   // inclusive warp totals
+    }
+    __syncthreads();
+    int run = incl - local + (wid > 0 ? s_warp[wid - 1] : 0);   // exclusive prefix of this thread's first group
+    for (int k = 0; k < per; ++k) {
+        const int g = tid * per + k;
+        if (g < G) {
+            s_ptile[g] = run;
+            run += (int)((off[g + 1] - off[g] + 127) / 128);
+        }
+        if (g == G - 1) s_ptile[G] = run;
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ void load_group_tables(const int64_t* __restrict__ offsets, int G, int64_t* s_off,
+                                                  int* s_ptile, int* s_warp) {
+    for (int i = threadIdx.x; i <= G; i += blockDim.x) s_off[i] = __ldg(offsets + i);
+    __syncthreads();
+    scan_group_tiles(s_off, G, s_ptile, s_warp);
+}
+
+// Group of row r: the g with s_off[g] <= r < s_off[g + 1] (empty groups are skipped).
+__device__ __forceinline__ int find_group(const int64_t* s_off, int G, int64_t r) {
+    int lo = 0, hi = G;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= r) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// Row of r in the grouped scale layout.
+__device__ __forceinline__ int64_t grouped_scale_row(const int64_t* s_off, const int* s_ptile, int G, int64_t r) {
+    const int g = find_group(s_off, G, r);
+    return (int64_t)s_ptile[g] * 128 + (r - s_off[g]);
+}
+
 }  // namespace mxk
+

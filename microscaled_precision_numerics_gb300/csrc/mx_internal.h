@@ -20,9 +20,10 @@ __host__ __device__ inline int64_t host_scale_bytes_dev(int64_t rows, int64_t k,
 uint32_t host_rht_sign_mask(uint64_t seed);
 
 cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q_row,
-                                  uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, cudaStream_t stream);
+                                  uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int G, const int64_t* group_offsets,
+                                  cudaStream_t stream);
 cudaError_t launch_nvfp4_per_token(const uint16_t* x, int64_t T, int64_t H, int64_t ldx, uint8_t* q, uint8_t* s,
-                                   float* s_tok, cudaStream_t stream);
+                                   float* s_tok, int G, const int64_t* group_offsets, int num_sms, cudaStream_t stream);
 cudaError_t launch_nvfp4_1x16(const uint16_t* x, int64_t T, int64_t N, bool colwise, bool rht, uint64_t rht_seed,
                               bool sr, uint64_t sr_seed, uint8_t* q, uint8_t* s, float* s_tensor, uint32_t* ws,
                               int num_sms, cudaStream_t stream);

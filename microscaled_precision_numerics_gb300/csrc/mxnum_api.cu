@@ -75,7 +75,24 @@ mx_status mx_quantize_mxfp8(const void* x, int64_t rows, int64_t cols, int64_t l
     if (q_row && (cols % 32) != 0) return MX_ERR_UNSUPPORTED;
     if (q_col && (rows % 32) != 0) return MX_ERR_UNSUPPORTED;
     return from_cuda(mxk::launch_mxfp8_quantize(static_cast<const uint16_t*>(x), rows, cols, ldx, q_row, s_row,
-                                                 q_col, s_col, stream));
+                                                 q_col, s_col, 0, nullptr, stream));
+}
+
+mx_status mx_quantize_mxfp8_grouped(const void* x, int64_t rows, int64_t cols, int64_t ldx, int64_t G,
+                                    const int64_t* group_offsets, uint8_t* q_row, uint8_t* s_row, cudaStream_t stream) {
+    if (!x || !q_row || !s_row || !group_offsets || rows <= 0 || cols <= 0 || ldx < cols) return MX_ERR_INVALID_ARG;
+    if (G <= 0 || G > MX_MAX_GROUPS) return MX_ERR_INVALID_ARG;
+    if ((cols % 8) != 0 || (ldx % 8) != 0 || !aligned16(x) || !aligned16(q_row) || !aligned16(s_row) ||
+        !aligned16(group_offsets))
+        return MX_ERR_ALIGNMENT;
+    if ((cols % 32) != 0) return MX_ERR_UNSUPPORTED;
+    return from_cuda(mxk::launch_mxfp8_quantize(static_cast<const uint16_t*>(x), rows, cols, ldx, q_row, s_row,
+                                                 nullptr, nullptr, (int)G, group_offsets, stream));
+}
+
+int64_t mx_grouped_scale_bytes(int64_t rows, int64_t G, int64_t k, int block) {
+    if (rows <= 0 || G <= 0 || k <= 0 || (block != 16 && block != 32)) return 0;
+    return mxk::host_scale_bytes(rows + 127 * G, k, block);
 }
 
 mx_status mx_nvfp4_quantize_per_token(const void* x, int64_t T, int64_t H, int64_t ldx, uint8_t* q, uint8_t* s,
@@ -83,8 +100,21 @@ mx_status mx_nvfp4_quantize_per_token(const void* x, int64_t T, int64_t H, int64
     if (!x || !q || !s || !s_tok || T <= 0 || H <= 0 || ldx < H) return MX_ERR_INVALID_ARG;
     if ((ldx % 8) != 0 || !aligned16(x) || !aligned16(q) || !aligned16(s) || !aligned16(s_tok)) return MX_ERR_ALIGNMENT;
     if ((H % 16) != 0) return MX_ERR_UNSUPPORTED;
-    if (((H / 2) % 4) != 0) return MX_ERR_ALIGNMENT;
-    return from_cuda(mxk::launch_nvfp4_per_token(static_cast<const uint16_t*>(x), T, H, ldx, q, s, s_tok, stream));
+    return from_cuda(mxk::launch_nvfp4_per_token(static_cast<const uint16_t*>(x), T, H, ldx, q, s, s_tok, 0, nullptr,
+                                                  mxk::device_sm_count(), stream));
+}
+
+mx_status mx_nvfp4_quantize_per_token_grouped(const void* x, int64_t T, int64_t H, int64_t ldx, int64_t G,
+                                              const int64_t* group_offsets, uint8_t* q, uint8_t* s, float* s_tok,
+                                              cudaStream_t stream) {
+    if (!x || !q || !s || !s_tok || !group_offsets || T <= 0 || H <= 0 || ldx < H) return MX_ERR_INVALID_ARG;
+    if (G <= 0 || G > MX_MAX_GROUPS) return MX_ERR_INVALID_ARG;
+    if ((ldx % 8) != 0 || !aligned16(x) || !aligned16(q) || !aligned16(s) || !aligned16(s_tok) ||
+        !aligned16(group_offsets))
+        return MX_ERR_ALIGNMENT;
+    if ((H % 16) != 0) return MX_ERR_UNSUPPORTED;
+    return from_cuda(mxk::launch_nvfp4_per_token(static_cast<const uint16_t*>(x), T, H, ldx, q, s, s_tok, (int)G,
+                                                  group_offsets, mxk::device_sm_count(), stream));
 }
 
 mx_status mx_nvfp4_quantize_weight_2d(const void* w, int64_t G, int64_t O, int64_t H, uint8_t* q_row, uint8_t* s_row,
@@ -122,7 +152,6 @@ mx_status mx_nvfp4_quantize_1x16(const void* x, int64_t T, int64_t N, int colwis
     } else {
         if (rht) return MX_ERR_UNSUPPORTED;
         if ((N % 16) != 0) return MX_ERR_UNSUPPORTED;
-        if (((N / 2) % 4) != 0) return MX_ERR_ALIGNMENT;
     }
     return from_cuda(mxk::launch_nvfp4_1x16(static_cast<const uint16_t*>(x), T, N, colwise != 0, rht != 0, rht_seed,
                                              rnd == MX_ROUND_SR, sr_seed, q, s, s_tensor,
@@ -189,7 +218,7 @@ mx_status mx_grouped_scaled_gemm(mx_format fmt, int64_t G, const int64_t* group_
                                  cudaStream_t stream) {
     mx_status st = validate_gemm_common(fmt, a, sa, b, sb, N, K, d);
     if (st != MX_OK) return st;
-    if (G <= 0 || G > 4096 || !group_offsets || total_rows <= 0) return MX_ERR_INVALID_ARG;
+    if (G <= 0 || G > MX_MAX_GROUPS || !group_offsets || total_rows <= 0) return MX_ERR_INVALID_ARG;
     if (!aligned16(group_offsets)) return MX_ERR_ALIGNMENT;
     if ((N % 8) != 0) return MX_ERR_ALIGNMENT;
     mxk::GemmArgs g{};

@@ -76,14 +76,20 @@ __device__ __forceinline__ void stage_tile(const uint16_t* __restrict__ x, int64
 //   row pass:    thread -> (row, pair of 32-column blocks); 8 x 16-byte shared loads
 //   column pass: thread -> (8-column chunk, 32-row block, quarter of 8 rows); 8 x 16-byte shared
 //                loads; the 32-row amax combines the 4 quarters (lanes l, l^8, l^16, l^24)
-template <bool ROW, bool COL>
+template <bool ROW, bool COL, bool GROUPED>
 __global__ void __launch_bounds__(QT_THREADS)
 mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
                       uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
-                      uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, int64_t tiles_c, int64_t tiles) {
+                      uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, int64_t tiles_c, int64_t tiles,
+                      int G, const int64_t* __restrict__ group_offsets) {
     extern __shared__ __align__(16) uint8_t qsm[];
     uint8_t (*colsc)[QT_COLS] = reinterpret_cast<uint8_t (*)[QT_COLS]>(qsm + 2 * QT_ROWS * QT_PITCH);
     const uint32_t buf_base = (uint32_t)__cvta_generic_to_shared(qsm);
+    // expert-group tables (grouped row-wise scale layout) after the staging buffers
+    int64_t* s_off = reinterpret_cast<int64_t*>(qsm + 2 * QT_ROWS * QT_PITCH + 4 * QT_COLS);
+    int* s_ptile = reinterpret_cast<int*>(s_off + (G + 1));
+    int* s_warp = s_ptile + (G + 1);
+    if (GROUPED) load_group_tables(group_offsets, G, s_off, s_ptile, s_warp);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int64_t t = blockIdx.x;
@@ -130,7 +136,8 @@ mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int6
             if (half == 0 && r < R) {
                 const int64_t nct = sf_col_tiles(K, 32);
                 const int nvalid = (int)min64(4, (K - c0) / 32);
-                uint8_t* p = s_row + sf_offset(r, c0 / 32, nct);
+                const int64_t srow = GROUPED ? grouped_scale_row(s_off, s_ptile, G, r) : r;
+                uint8_t* p = s_row + sf_offset(srow, c0 / 32, nct);
                 const uint32_t word = mine | (other << 16);
                 if (nvalid == 4) *reinterpret_cast<uint32_t*>(p) = word;
                 else for (int i = 0; i < nvalid; ++i) p[i] = (uint8_t)(word >> (8 * i));
@@ -196,11 +203,13 @@ mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int6
 }  // namespace
 
 cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q_row,
-                                  uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, cudaStream_t stream) {
+                                  uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int G, const int64_t* group_offsets,
+                                  cudaStream_t stream) {
     const bool row = q_row != nullptr, col = q_col != nullptr;
-    // zero the scale padding (rows beyond R up to a multiple of 128, scale columns up to a multiple of 4)
-    if (row && ((R % 128) != 0 || ((K / 32) % 4) != 0)) {
-        cudaError_t e = cudaMemsetAsync(s_row, 0, (size_t)host_scale_bytes(R, K, 32), stream);
+    // zero the scale padding (rows beyond R up to a multiple of 128, scale columns up to a multiple of 4;
+    // in the grouped layout also the rows between groups)
+    if (row && (G > 0 || (R % 128) != 0 || ((K / 32) % 4) != 0)) {
+        cudaError_t e = cudaMemsetAsync(s_row, 0, (size_t)host_scale_bytes(R + 127 * (int64_t)G, K, 32), stream);
         if (e != cudaSuccess) return e;
     }
     if (col && ((K % 128) != 0 || ((R / 32) % 4) != 0)) {
@@ -208,21 +217,29 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64
         if (e != cudaSuccess) return e;
     }
     const int64_t tiles_c = (K + QT_COLS - 1) / QT_COLS, tiles = tiles_c * ((R + QT_ROWS - 1) / QT_ROWS);
-    const size_t smem = 2 * QT_ROWS * QT_PITCH + 4 * QT_COLS;
+    const size_t smem = 2 * QT_ROWS * QT_PITCH + 4 * QT_COLS + (G > 0 ? (size_t)12 * (G + 1) + 128 : 0);
     static bool attr_done = false;
     if (!attr_done) {
-        cudaFuncSetAttribute(mxfp8_quantize_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(mxfp8_quantize_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(mxfp8_quantize_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        const int max_smem = 2 * QT_ROWS * QT_PITCH + 4 * QT_COLS + 12 * 4097 + 128;
+        cudaFuncSetAttribute(mxfp8_quantize_kernel<true, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        cudaFuncSetAttribute(mxfp8_quantize_kernel<true, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        cudaFuncSetAttribute(mxfp8_quantize_kernel<false, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        cudaFuncSetAttribute(mxfp8_quantize_kernel<true, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         attr_done = true;
     }
     const unsigned grid = (unsigned)min64(tiles, (int64_t)device_sm_count() * 3);
-    if (row && col)
-        mxfp8_quantize_kernel<true, true><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col, tiles_c, tiles);
+    if (G > 0)
+        mxfp8_quantize_kernel<true, false, true><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, nullptr, nullptr,
+                                                                                      tiles_c, tiles, G, group_offsets);
+    else if (row && col)
+        mxfp8_quantize_kernel<true, true, false><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col,
+                                                                                      tiles_c, tiles, 0, nullptr);
     else if (row)
-        mxfp8_quantize_kernel<true, false><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col, tiles_c, tiles);
+        mxfp8_quantize_kernel<true, false, false><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col,
+                                                                                       tiles_c, tiles, 0, nullptr);
     else
-        mxfp8_quantize_kernel<false, true><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col, tiles_c, tiles);
+        mxfp8_quantize_kernel<false, true, false><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col,
+                                                                                       tiles_c, tiles, 0, nullptr);
     return cudaGetLastError();
 }
 

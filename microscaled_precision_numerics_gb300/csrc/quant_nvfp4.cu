@@ -17,97 +17,161 @@ namespace mxk {
 namespace {
 
 // ------------------------------------------------------------------------------------------------
-// Row-wise 1x16 (per token or per tensor).  One warp per row; lane l owns 8-element chunks
-// l, l + 32, ...; a 16-block is the chunk pair (2m, 2m + 1) held by adjacent lanes.
+// Row-wise 1x16 (per token or per tensor).  One warp per row (grid-stride over rows); lane l owns
+// the 16-element blocks l, l + 32, ..., so the block-scale arithmetic runs once per 16 elements.
+// Rows of up to 32 * RW_MAXB blocks stay in registers between the amax and the quantize pass;
+// longer rows are read twice (the second read hits L1/L2).
 // ------------------------------------------------------------------------------------------------
 constexpr int RW_WARPS = 8;
+constexpr int RW_MAXB = 4;     // blocks per lane kept in registers (H <= 2048)
 
-template <bool PER_TENSOR, bool SR>
-__global__ void __launch_bounds__(RW_WARPS * 32)
-nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64_t ldx,
-                     uint8_t* __restrict__ q, uint8_t* __restrict__ s, float* __restrict__ s_tok,
-                     const uint32_t* __restrict__ tensor_amax, float* __restrict__ s_tensor, uint64_t sr_seed) {
-    const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * RW_WARPS + (threadIdx.x >> 5);
-    if (t >= T) return;
-    const uint16_t* xr = x + t * ldx;
-    const int64_t nchunk = H / 8;
-
-    float S;
-    if (PER_TENSOR) {
-        S = nvfp4_second_scale(__uint_as_float(*tensor_amax));
-        if (t == 0 && lane == 0) *s_tensor = S;
-    } else {
-        uint32_t m2 = 0;
-        for (int64_t ch = lane; ch < nchunk; ch += 32) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + ch * 8));
-            m2 = absmax_bf16x2(m2, v.x); m2 = absmax_bf16x2(m2, v.y);
-            m2 = absmax_bf16x2(m2, v.z); m2 = absmax_bf16x2(m2, v.w);
-        }
-        const uint32_t amax16 = __reduce_max_sync(0xFFFFFFFFu, fold_halves(m2));
-        S = nvfp4_second_scale(__uint_as_float(amax16 << 16));
-        if (lane == 0) s_tok[t] = S;
+// Quantize one 16-element block held in two 16-byte words; returns the 8 code bytes.
+template <bool SR>
+__device__ __forceinline__ uint2 quant_block16(const uint4& a, const uint4& b, float r, uint64_t elem0,
+                                               uint32_t k0, uint32_t k1) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = __fmul_rn(bf16_lo(w[i]), r);
+        v[2 * i + 1] = __fmul_rn(bf16_hi(w[i]), r);
     }
-
-    const int64_t nct = sf_col_tiles(H, 16);
-    const int64_t nblk = H / 16;
-    const uint32_t k0 = (uint32_t)sr_seed, k1 = (uint32_t)(sr_seed >> 32);
-    for (int64_t base = 0; base < nchunk; base += 32) {
-        const int64_t ch = base + lane;
-        const bool valid = ch < nchunk;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) v = __ldcs(reinterpret_cast<const uint4*>(xr + ch * 8));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t m2 = 0;
+    if (SR) {
+        // elements elem0 .. elem0 + 15 (elem0 % 16 == 0): two Philox blocks of 8
+        uint32_t c[2] = {0u, 0u};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) m2 = absmax_bf16x2(m2, w[i]);
-        uint32_t a16 = fold_halves(m2);
-        a16 = max(a16, __shfl_xor_sync(0xFFFFFFFFu, a16, 1));
-        const uint32_t bs = nvfp4_block_scale(__uint_as_float(a16 << 16), S);
-        const float r = nvfp4_block_recip(bs, S);
-        float vals[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            vals[2 * i] = __fmul_rn(bf16_lo(w[i]), r);
-            vals[2 * i + 1] = __fmul_rn(bf16_hi(w[i]), r);
-        }
-        uint32_t codes;
-        if (SR) {
-            // logical element i = t * H + ch * 8 + j; the 8 elements of a chunk share one Philox block
-            const uint64_t blk = ((uint64_t)t * (uint64_t)H + (uint64_t)ch * 8) >> 3;
+        for (int h = 0; h < 2; ++h) {
+            const uint64_t blk = (elem0 >> 3) + h;
             const U4 rnd = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, k0, k1);
             const uint32_t rw[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
-            codes = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t bits = (j & 1) ? (rw[j >> 1] >> 16) : (rw[j >> 1] & 0xFFFFu);
-                codes |= e2m1_sr(vals[j], bits) << (4 * j);
+                c[h] |= e2m1_sr(v[8 * h + j], bits) << (4 * j);
             }
-        } else {
-            codes = cvt_e2m1x8(vals);
         }
-        if (valid) __stcs(reinterpret_cast<uint32_t*>(q + t * (H / 2) + ch * 4), codes);
-        // gather 4 consecutive block scales (chunks 8m .. 8m+7 = lanes 8m' .. 8m'+7) into one word
-        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
-        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 4);
-        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 6);
-        if (valid && (ch & 7) == 0) {
-            const int64_t blk = ch >> 1;
-            uint8_t* p = s + sf_offset(t, blk, nct);
-            if (blk + 4 <= nblk) {
-                *reinterpret_cast<uint32_t*>(p) = bs | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        return make_uint2(c[0], c[1]);
+    }
+    return make_uint2(cvt_e2m1x8(v), cvt_e2m1x8(v + 8));
+}
+
+template <bool PER_TENSOR, bool SR, bool GROUPED, int LPR>
+__global__ void __launch_bounds__(RW_WARPS * 32)
+nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64_t ldx,
+                     uint8_t* __restrict__ q, uint8_t* __restrict__ s, float* __restrict__ s_tok,
+                     const uint32_t* __restrict__ tensor_amax, float* __restrict__ s_tensor, uint64_t sr_seed,
+                     int G, const int64_t* __restrict__ group_offsets) {
+    // LPR lanes per row (32 or 16): a warp works on 32 / LPR rows at once
+    constexpr int RPW = 32 / LPR;
+    extern __shared__ __align__(16) uint8_t rw_sm[];
+    int64_t* s_off = reinterpret_cast<int64_t*>(rw_sm);
+    int* s_ptile = reinterpret_cast<int*>(rw_sm + 8 * (G + 1));
+    int* s_warp = s_ptile + (G + 1);
+    if (GROUPED) load_group_tables(group_offsets, G, s_off, s_ptile, s_warp);
+
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % LPR;                      // lane within the row group
+    const int half = lane / LPR;                     // which of the warp's rows
+    const uint32_t gmask = LPR == 32 ? 0xFFFFFFFFu : (0xFFFFu << (16 * half));
+    const int64_t nblk = H / 16;
+    const int64_t nct = sf_col_tiles(H, 16);
+    const bool cached = nblk <= LPR * RW_MAXB;
+    const uint32_t k0 = (uint32_t)sr_seed, k1 = (uint32_t)(sr_seed >> 32);
+    for (int64_t tw = ((int64_t)blockIdx.x * RW_WARPS + (threadIdx.x >> 5)) * RPW; tw < T;
+         tw += (int64_t)gridDim.x * RW_WARPS * RPW) {
+        const int64_t t = tw + half;
+        const bool row_ok = t < T;                   // the warp stays converged for the shuffles below
+        const uint4* xr = reinterpret_cast<const uint4*>(x + (row_ok ? t : tw) * ldx);
+        uint4 ra[RW_MAXB], rb[RW_MAXB];
+        float S;
+        if (PER_TENSOR) {
+            S = nvfp4_second_scale(__uint_as_float(*tensor_amax));
+            if (t == 0 && sub == 0) *s_tensor = S;
+        } else {
+            uint32_t m2 = 0;
+            if (cached) {
+#pragma unroll
+                for (int i = 0; i < RW_MAXB; ++i) {
+                    const int64_t b = sub + LPR * i;
+                    ra[i] = rb[i] = make_uint4(0u, 0u, 0u, 0u);
+                    if (row_ok && b < nblk) { ra[i] = __ldcs(xr + 2 * b); rb[i] = __ldcs(xr + 2 * b + 1); }
+                    m2 = absmax_bf16x2(m2, ra[i].x); m2 = absmax_bf16x2(m2, ra[i].y);
+                    m2 = absmax_bf16x2(m2, ra[i].z); m2 = absmax_bf16x2(m2, ra[i].w);
+                    m2 = absmax_bf16x2(m2, rb[i].x); m2 = absmax_bf16x2(m2, rb[i].y);
+                    m2 = absmax_bf16x2(m2, rb[i].z); m2 = absmax_bf16x2(m2, rb[i].w);
+                }
+            } else if (row_ok) {
+                for (int64_t b = sub; b < nblk; b += LPR) {
+                    const uint4 a = __ldg(xr + 2 * b), c = __ldg(xr + 2 * b + 1);
+                    m2 = absmax_bf16x2(m2, a.x); m2 = absmax_bf16x2(m2, a.y);
+                    m2 = absmax_bf16x2(m2, a.z); m2 = absmax_bf16x2(m2, a.w);
+                    m2 = absmax_bf16x2(m2, c.x); m2 = absmax_bf16x2(m2, c.y);
+                    m2 = absmax_bf16x2(m2, c.z); m2 = absmax_bf16x2(m2, c.w);
+                }
+            }
+            const uint32_t amax16 = __reduce_max_sync(gmask, fold_halves(m2));
+            S = nvfp4_second_scale(__uint_as_float(amax16 << 16));
+            if (row_ok && sub == 0) s_tok[t] = S;
+        }
+        const int64_t srow = (GROUPED && row_ok) ? grouped_scale_row(s_off, s_ptile, G, t) : t;
+        const int64_t nrounds = (nblk + LPR - 1) / LPR;
+        for (int64_t i = 0; i < nrounds; ++i) {
+            const int64_t b = sub + LPR * i;
+            const bool valid = row_ok && b < nblk;
+            uint4 a, c;
+            if (!PER_TENSOR && cached && i < RW_MAXB) {
+                // static register index: unrolled selection keeps ra/rb in registers
+                a = ra[0]; c = rb[0];
+#pragma unroll
+                for (int k = 1; k < RW_MAXB; ++k) if (i == k) { a = ra[k]; c = rb[k]; }
             } else {
-                const uint32_t bb[4] = {bs, b1, b2, b3};
-                for (int i = 0; i < (int)(nblk - blk); ++i) p[i] = (uint8_t)bb[i];
+                a = c = make_uint4(0u, 0u, 0u, 0u);
+                if (valid) { a = __ldcs(xr + 2 * b); c = __ldcs(xr + 2 * b + 1); }
+            }
+            uint32_t m2 = 0;
+            m2 = absmax_bf16x2(m2, a.x); m2 = absmax_bf16x2(m2, a.y); m2 = absmax_bf16x2(m2, a.z); m2 = absmax_bf16x2(m2, a.w);
+            m2 = absmax_bf16x2(m2, c.x); m2 = absmax_bf16x2(m2, c.y); m2 = absmax_bf16x2(m2, c.z); m2 = absmax_bf16x2(m2, c.w);
+            const uint32_t bs = nvfp4_block_scale(__uint_as_float(fold_halves(m2) << 16), S);
+            const float r = nvfp4_block_recip(bs, S);
+            const uint2 codes = quant_block16<SR>(a, c, r, (uint64_t)t * (uint64_t)H + (uint64_t)b * 16, k0, k1);
+            if (valid) __stcs(reinterpret_cast<uint2*>(q + t * (H / 2) + b * 8), codes);
+            // four consecutive block scales (lanes 4m .. 4m+3 of the row group) form one word
+            const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 1);
+            const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
+            const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 3);
+            if (valid && (b & 3) == 0) {
+                uint8_t* p = s + sf_offset(srow, b, nct);
+                if (b + 4 <= nblk) {
+                    *reinterpret_cast<uint32_t*>(p) = bs | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                } else {
+                    const uint32_t bb[4] = {bs, b1, b2, b3};
+                    for (int k = 0; k < (int)(nblk - b); ++k) p[k] = (uint8_t)bb[k];
+                }
             }
         }
     }
 }
 
+template <bool PER_TENSOR, bool SR, bool GROUPED>
+void launch_rowwise(int64_t T, int64_t H, unsigned grid_cap, size_t smem, cudaStream_t stream, const uint16_t* x,
+                    int64_t ldx, uint8_t* q, uint8_t* s, float* s_tok, const uint32_t* amax, float* s_tensor,
+                    uint64_t sr_seed, int G, const int64_t* offs) {
+    if (H / 16 <= 64) {
+        const int64_t blocks = (T + RW_WARPS * 2 - 1) / (RW_WARPS * 2);
+        nvfp4_rowwise_kernel<PER_TENSOR, SR, GROUPED, 16><<<(unsigned)min64(blocks, grid_cap), RW_WARPS * 32, smem, stream>>>(
+            x, T, H, ldx, q, s, s_tok, amax, s_tensor, sr_seed, G, offs);
+    } else {
+        const int64_t blocks = (T + RW_WARPS - 1) / RW_WARPS;
+        nvfp4_rowwise_kernel<PER_TENSOR, SR, GROUPED, 32><<<(unsigned)min64(blocks, grid_cap), RW_WARPS * 32, smem, stream>>>(
+            x, T, H, ldx, q, s, s_tok, amax, s_tensor, sr_seed, G, offs);
+    }
+}
+
 // ------------------------------------------------------------------------------------------------
 // Column-wise 1x16 along tokens with a per-tensor scale.  CTA tile: 128 tokens x 256 columns; warp
-// w owns tokens [16w, 16w + 16), lane l owns columns [8l, 8l + 8).  Codes and scales are staged
-// transposed in shared memory and written as contiguous runs along the token dimension.
+// w owns tokens [16w, 16w + 16), lane l owns columns [8l, 8l + 8).  Each column's 16 codes (8 bytes)
+// are stored straight from registers into the transposed output (the 8 warps fill 64 contiguous
+// bytes per column, merged in L2); block scales are staged in shared memory and written as words.
 // ------------------------------------------------------------------------------------------------
 constexpr int CW_TOK = 128;
 constexpr int CW_COLS = 256;
@@ -184,12 +248,11 @@ colwise_amax_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint32
 }
 
 template <bool RHT, bool SR>
-__global__ void __launch_bounds__(CW_THREADS)
+__global__ void __launch_bounds__(CW_THREADS, 2)
 colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint32_t signmask,
                      const uint32_t* __restrict__ tensor_amax, uint64_t sr_seed,
                      uint8_t* __restrict__ q, uint8_t* __restrict__ s, float* __restrict__ s_tensor) {
-    __shared__ __align__(16) uint8_t qs[CW_COLS][CW_TOK / 2 + 16];   // codes, transposed (+pad)
-    __shared__ uint8_t ss[CW_COLS][CW_TOK / 16];                     // block scales, transposed
+    __shared__ uint8_t ss[CW_TOK / 16][CW_COLS];                     // block scales: [token block][column]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tb0 = (int64_t)blockIdx.y * CW_TOK;
     const int64_t cb0 = (int64_t)blockIdx.x * CW_COLS;
@@ -203,74 +266,66 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
     uint4 xr[16];
     load_16x8(x, N, t0, n0, valid, xr);
 
-    // SR: one Philox block per row of the micro-tile (elements t * N + n0 .. + 7)
-    uint32_t rbits[16][4];
-    if (SR) {
-        const uint32_t k0 = (uint32_t)sr_seed, k1 = (uint32_t)(sr_seed >> 32);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint64_t blk = ((uint64_t)(t0 + i) * (uint64_t)N + (uint64_t)n0) >> 3;
-            const U4 r4 = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, k0, k1);
-            rbits[i][0] = r4.x; rbits[i][1] = r4.y; rbits[i][2] = r4.z; rbits[i][3] = r4.w;
-        }
-    }
-
+    // Phase A, per column j: (transform and re-round in place,) block amax, block scale, reciprocal.
+    float rcp[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         float v[16];
         column_values<RHT>(xr, j, signmask, v);
+        if (RHT) {
+            // store the BF16-rounded transformed values back in place of the inputs
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                uint32_t* w = (j >> 1) == 0 ? &xr[i].x : ((j >> 1) == 1 ? &xr[i].y : ((j >> 1) == 2 ? &xr[i].z : &xr[i].w));
+                const uint32_t b = __float_as_uint(v[i]) >> 16;
+                *w = (j & 1) ? ((*w & 0x0000FFFFu) | (b << 16)) : ((*w & 0xFFFF0000u) | b);
+            }
+        }
         uint32_t m = 0;
 #pragma unroll
         for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
         const uint32_t bs = nvfp4_block_scale(__uint_as_float(m), S);
-        const float r = nvfp4_block_recip(bs, S);
-        float p[16];
+        rcp[j] = nvfp4_block_recip(bs, S);
+        ss[warp][lane * 8 + j] = (uint8_t)bs;
+        if (!SR) {
+            float p[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) p[i] = __fmul_rn(v[i], r);
-        uint32_t c0, c1;
-        if (SR) {
-            c0 = 0; c1 = 0;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                // element (t0 + i, n0 + j): word j >> 1, half j & 1
-                const uint32_t w = rbits[i][j >> 1];
-                const uint32_t bits = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
-                const uint32_t code = e2m1_sr(p[i], bits);
-                if (i < 8) c0 |= code << (4 * i); else c1 |= code << (4 * (i - 8));
-            }
-        } else {
-            c0 = cvt_e2m1x8(p);
-            c1 = cvt_e2m1x8(p + 8);
+            for (int i = 0; i < 16; ++i) p[i] = __fmul_rn(v[i], rcp[j]);
+            // the 16 tokens of column n0 + j: 8 bytes, stored straight to the transposed output
+            if (valid) __stcs(reinterpret_cast<uint2*>(q + (n0 + j) * (T / 2) + t0 / 2),
+                              make_uint2(cvt_e2m1x8(p), cvt_e2m1x8(p + 8)));
         }
-        const int col = lane * 8 + j;
-        *reinterpret_cast<uint2*>(&qs[col][warp * 8]) = make_uint2(c0, c1);
-        ss[col][warp] = (uint8_t)bs;
+    }
+    if (SR) {
+        // Phase B, per row i: one Philox block covers the row's 8 columns (elements t * N + n0 .. + 7)
+        const uint32_t k0 = (uint32_t)sr_seed, k1 = (uint32_t)(sr_seed >> 32);
+        uint32_t code[8][2];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { code[j][0] = 0u; code[j][1] = 0u; }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint64_t blk = ((uint64_t)(t0 + i) * (uint64_t)N + (uint64_t)n0) >> 3;
+            const U4 r4 = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, k0, k1);
+            const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t w = word_of(xr[i], j >> 1);
+                const float v = (j & 1) ? bf16_hi(w) : bf16_lo(w);
+                const uint32_t bits = (j & 1) ? (rw[j >> 1] >> 16) : (rw[j >> 1] & 0xFFFFu);
+                code[j][i >> 3] |= e2m1_sr(__fmul_rn(v, rcp[j]), bits) << (4 * (i & 7));
+            }
+        }
+        if (valid) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                __stcs(reinterpret_cast<uint2*>(q + (n0 + j) * (T / 2) + t0 / 2), make_uint2(code[j][0], code[j][1]));
+        }
     }
     __syncthreads();
 
-    // write out: column col gets CW_TOK/2 = 64 contiguous bytes of codes (4 x 16 B) and 8 scales
+    // scales: column col gets the 8 block scales of this CTA's 128 tokens (two words of the layout)
     const int64_t ntok = min64(CW_TOK, T - tb0);      // multiple of 16
     const int64_t nct = sf_col_tiles(T, 16);
-    if (((T / 2) & 15) == 0) {
-        for (int idx = threadIdx.x; idx < CW_COLS * 4; idx += CW_THREADS) {
-            const int col = idx >> 2, part = idx & 3;
-            const int64_t n = cb0 + col;
-            if (n < N && part * 32 < ntok) {
-                const uint4 val = *reinterpret_cast<const uint4*>(&qs[col][part * 16]);
-                __stcs(reinterpret_cast<uint4*>(q + n * (T / 2) + tb0 / 2 + part * 16), val);
-            }
-        }
-    } else {
-        // rows of q are only 8-byte aligned when T % 32 != 0
-        for (int idx = threadIdx.x; idx < CW_COLS * 8; idx += CW_THREADS) {
-            const int col = idx >> 3, part = idx & 7;
-            const int64_t n = cb0 + col;
-            if (n < N && part * 16 < ntok) {
-                const uint2 val = *reinterpret_cast<const uint2*>(&qs[col][part * 8]);
-                __stcs(reinterpret_cast<uint2*>(q + n * (T / 2) + tb0 / 2 + part * 8), val);
-            }
-        }
-    }
     for (int idx = threadIdx.x; idx < CW_COLS * 2; idx += CW_THREADS) {
         const int col = idx >> 1, half = idx & 1;
         const int64_t n = cb0 + col;
@@ -279,10 +334,10 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
         if (n < N && nb > 0) {
             uint8_t* p = s + sf_offset(n, kb, nct);
             if (nb == 4) {
-                *reinterpret_cast<uint32_t*>(p) = (uint32_t)ss[col][half * 4] | ((uint32_t)ss[col][half * 4 + 1] << 8) |
-                                                  ((uint32_t)ss[col][half * 4 + 2] << 16) | ((uint32_t)ss[col][half * 4 + 3] << 24);
+                *reinterpret_cast<uint32_t*>(p) = (uint32_t)ss[half * 4][col] | ((uint32_t)ss[half * 4 + 1][col] << 8) |
+                                                  ((uint32_t)ss[half * 4 + 2][col] << 16) | ((uint32_t)ss[half * 4 + 3][col] << 24);
             } else {
-                for (int i = 0; i < nb; ++i) p[i] = ss[col][half * 4 + i];
+                for (int i = 0; i < nb; ++i) p[i] = ss[half * 4 + i][col];
             }
         }
     }
@@ -368,7 +423,6 @@ __global__ void __launch_bounds__(128)
 weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, const uint32_t* __restrict__ amax,
                       uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
                       uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, float* __restrict__ s_w) {
-    __shared__ __align__(16) uint8_t qt[W2_COLS][W2_ROWS / 2 + 16];   // transposed codes (+pad)
     __shared__ uint8_t st[W2_ROWS / 16][W2_COLS / 16];                 // tile scales
     const int64_t g = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -398,6 +452,7 @@ weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, cons
     const float r = nvfp4_block_recip(bs, S);
 
     uint8_t* qrow_g = q_row + g * O * (H / 2);
+    uint32_t codes[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int rr = 2 * i + rpar;                     // row within the warp's 16
@@ -406,17 +461,29 @@ weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, cons
         v[2] = __fmul_rn(bf16_lo(xr[i].y), r); v[3] = __fmul_rn(bf16_hi(xr[i].y), r);
         v[4] = __fmul_rn(bf16_lo(xr[i].z), r); v[5] = __fmul_rn(bf16_hi(xr[i].z), r);
         v[6] = __fmul_rn(bf16_lo(xr[i].w), r); v[7] = __fmul_rn(bf16_hi(xr[i].w), r);
-        const uint32_t codes = cvt_e2m1x8(v);
-        if (rowv && colv) __stcs(reinterpret_cast<uint32_t*>(qrow_g + (o0 + rr) * (H / 2) + h / 2), codes);
-        // transposed staging: column chunk*8 + j gets the nibble of row warp*16 + rr
+        codes[i] = cvt_e2m1x8(v);
+        if (rowv && colv) __stcs(reinterpret_cast<uint32_t*>(qrow_g + (o0 + rr) * (H / 2) + h / 2), codes[i]);
+    }
+    // transposed copy: lanes l (even rows) and l ^ 16 (odd rows) swap code words; the even-row lane
+    // then emits columns 0..3 of its chunk and the odd-row lane columns 4..7, each as the 8 bytes
+    // (16 rows, two per byte, even row in the low nibble) of that column's slice
+    uint32_t other[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t nib = (codes >> (4 * j)) & 0xFu;
-            const int row = warp * 16 + rr;
-            // two rows per byte: even row in the low nibble; rows rr and rr^1 live in lanes l and l^16
-            const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, nib, 16);
-            if (rpar == 0) qt[chunk * 8 + j][row >> 1] = (uint8_t)(nib | (other << 4));
+    for (int i = 0; i < 8; ++i) other[i] = __shfl_xor_sync(0xFFFFFFFFu, codes[i], 16);
+    uint8_t* qcol_g = q_col + g * H * (O / 2);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        const int j = jj + 4 * rpar;
+        uint32_t lo = 0u, hi = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t even = ((rpar ? other[i] : codes[i]) >> (4 * j)) & 0xFu;
+            const uint32_t odd = ((rpar ? codes[i] : other[i]) >> (4 * j)) & 0xFu;
+            const uint32_t byte = even | (odd << 4);
+            if (i < 4) lo |= byte << (8 * i); else hi |= byte << (8 * (i - 4));
         }
+        const int64_t hc = h + j;
+        if (rowv && colv) __stcs(reinterpret_cast<uint2*>(qcol_g + hc * (O / 2) + o0 / 2), make_uint2(lo, hi));
     }
     if (lane < 16 && (lane & 1) == 0) st[warp][lane >> 1] = (uint8_t)bs;
     __syncthreads();
@@ -438,17 +505,8 @@ weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, cons
             }
         }
     }
-    // column-wise codes: column h0 + c gets 32 contiguous bytes (rows o_base .. o_base + 63)
     const int64_t ob = (int64_t)blockIdx.y * W2_ROWS;
     const int64_t nrows = min64(W2_ROWS, O - ob);      // multiple of 16
-    uint8_t* qcol_g = q_col + g * H * (O / 2);
-    for (int idx = threadIdx.x; idx < W2_COLS * 4; idx += 128) {
-        const int c = idx >> 2, part = idx & 3;              // part: 8-byte piece (16 rows)
-        const int64_t hc = h0 + c;
-        if (hc < H && part * 16 < nrows)
-            *reinterpret_cast<uint2*>(qcol_g + hc * (O / 2) + ob / 2 + part * 8) =
-                *reinterpret_cast<const uint2*>(&qt[c][part * 8]);
-    }
     // column-wise scales: row hc, scale columns ob/16 .. +3 (one word when all 4 row tiles exist)
     {
         const int64_t nct = sf_col_tiles(O, 16);
@@ -475,13 +533,21 @@ weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, cons
 // launchers
 // ------------------------------------------------------------------------------------------------
 cudaError_t launch_nvfp4_per_token(const uint16_t* x, int64_t T, int64_t H, int64_t ldx, uint8_t* q, uint8_t* s,
-                                   float* s_tok, cudaStream_t stream) {
-    if ((T % 128) != 0 || ((H / 16) % 4) != 0) {
+                                   float* s_tok, int G, const int64_t* group_offsets, int num_sms, cudaStream_t stream) {
+    if (G > 0) {
+        // grouped layout: the padding between groups is zero
+        cudaError_t e = cudaMemsetAsync(s, 0, (size_t)host_scale_bytes(T + 127 * (int64_t)G, H, 16), stream);
+        if (e != cudaSuccess) return e;
+    } else if ((T % 128) != 0 || ((H / 16) % 4) != 0) {
         cudaError_t e = cudaMemsetAsync(s, 0, (size_t)host_scale_bytes(T, H, 16), stream);
         if (e != cudaSuccess) return e;
     }
-    const unsigned grid = (unsigned)((T + RW_WARPS - 1) / RW_WARPS);
-    nvfp4_rowwise_kernel<false, false><<<grid, RW_WARPS * 32, 0, stream>>>(x, T, H, ldx, q, s, s_tok, nullptr, nullptr, 0);
+    const unsigned cap = (unsigned)num_sms * 16;
+    if (G > 0)
+        launch_rowwise<false, false, true>(T, H, cap, (size_t)12 * (G + 1) + 128, stream, x, ldx, q, s, s_tok, nullptr,
+                                           nullptr, 0, G, group_offsets);
+    else
+        launch_rowwise<false, false, false>(T, H, cap, 0, stream, x, ldx, q, s, s_tok, nullptr, nullptr, 0, 0, nullptr);
     return cudaGetLastError();
 }
 
@@ -508,9 +574,9 @@ cudaError_t launch_nvfp4_1x16(const uint16_t* x, int64_t T, int64_t N, bool colw
     } else {
         amax_kernel<<<num_sms * 4, 256, 0, stream>>>(x, T * N, ws);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        const unsigned grid = (unsigned)((T + RW_WARPS - 1) / RW_WARPS);
-        if (sr) nvfp4_rowwise_kernel<true, true><<<grid, RW_WARPS * 32, 0, stream>>>(x, T, N, N, q, s, nullptr, ws, s_tensor, sr_seed);
-        else nvfp4_rowwise_kernel<true, false><<<grid, RW_WARPS * 32, 0, stream>>>(x, T, N, N, q, s, nullptr, ws, s_tensor, sr_seed);
+        const unsigned cap = (unsigned)num_sms * 16;
+        if (sr) launch_rowwise<true, true, false>(T, N, cap, 0, stream, x, N, q, s, nullptr, ws, s_tensor, sr_seed, 0, nullptr);
+        else launch_rowwise<true, false, false>(T, N, cap, 0, stream, x, N, q, s, nullptr, ws, s_tensor, sr_seed, 0, nullptr);
     }
     return cudaGetLastError();
 }

@@ -69,6 +69,8 @@ def _load():
                 "orc_scale_layout_offset": (I64, [I64, I64, I64]),
                 "orc_scales_to_gemm_layout": (None, [P, I64, I64, P]),
                 "orc_scales_from_gemm_layout": (None, [P, I64, I64, P]),
+                "orc_grouped_padded_rows": (I64, [I64, P]),
+                "orc_scales_to_grouped_layout": (None, [P, I64, I64, I64, P, P, I64]),
                 "orc_mxfp8_quantize_rowwise": (None, [P, I64, I64, I64, P, P]),
                 "orc_mxfp8_quantize_colwise": (None, [P, I64, I64, I64, P, P]),
                 "orc_nvfp4_second_scale": (ctypes.c_float, [ctypes.c_float]),
@@ -217,6 +219,24 @@ def scales_from_gemm_layout(laid: np.ndarray, rows: int, scols: int) -> np.ndarr
     laid = np.ascontiguousarray(laid, dtype=np.uint8)
     out = np.zeros((rows, scols), dtype=np.uint8)
     _load().orc_scales_from_gemm_layout(_p(laid), rows, scols, _p(out))
+    return out
+
+
+def grouped_padded_rows(group_offsets) -> int:
+    off = np.ascontiguousarray(group_offsets, dtype=np.int64)
+    return int(_load().orc_grouped_padded_rows(off.size - 1, _p(off)))
+
+
+def scales_to_grouped_layout(compact: np.ndarray, group_offsets, out_bytes: int = None) -> np.ndarray:
+    """Compact scales [rows, scols] of expert-sorted rows -> the grouped GEMM layout (each group's
+    rows start on a 128-row tile)."""
+    compact = np.ascontiguousarray(compact, dtype=np.uint8)
+    off = np.ascontiguousarray(group_offsets, dtype=np.int64)
+    rows, scols = compact.shape
+    if out_bytes is None:
+        out_bytes = scale_layout_bytes(max(1, grouped_padded_rows(off)), scols)
+    out = np.zeros(out_bytes, dtype=np.uint8)
+    _load().orc_scales_to_grouped_layout(_p(compact), rows, scols, off.size - 1, _p(off), _p(out), out_bytes)
     return out
 
 

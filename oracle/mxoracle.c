@@ -219,6 +219,29 @@ ORC_API void orc_scales_from_gemm_layout(const uint8_t* laid, int64_t rows, int6
             compact[r * scols + c] = laid[orc_scale_layout_offset(r, c, scols)];
 }
 
+/* Grouped variant for expert-sorted rows: group g's rows [off[g], off[g+1])
+ * are placed from padded row P_g = sum over j < g of ceil(m_j / 128) * 128, so
+ * every group starts on a 128-row tile; row r of group g sits at padded row
+ * P_g + (r - off[g]) of the plain layout above.  Padding is zero. */
+ORC_API int64_t orc_grouped_padded_rows(int64_t G, const int64_t* off) {
+    int64_t p = 0;
+    for (int64_t g = 0; g < G; ++g) p += (off[g + 1] - off[g] + 127) / 128 * 128;
+    return p;
+}
+
+ORC_API void orc_scales_to_grouped_layout(const uint8_t* compact, int64_t rows, int64_t scols, int64_t G,
+                                          const int64_t* off, uint8_t* out, int64_t out_bytes) {
+    memset(out, 0, (size_t)out_bytes);
+    int64_t P = 0;
+    for (int64_t g = 0; g < G; ++g) {
+        for (int64_t r = off[g]; r < off[g + 1]; ++r)
+            for (int64_t c = 0; c < scols; ++c)
+                out[orc_scale_layout_offset(P + (r - off[g]), c, scols)] = compact[r * scols + c];
+        P += (off[g + 1] - off[g] + 127) / 128 * 128;
+    }
+    (void)rows;
+}
+
 /* ------------------------------------------------------------------------ */
 /* MXFP8: one E8M0 scale per 32 consecutive elements along the GEMM's K.     */
 /* [Miles] "cada bloco de 32 valores E4M3 compartilha uma escala E8M0";      */

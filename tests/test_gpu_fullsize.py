@@ -112,12 +112,12 @@ def moe(mx):
     x = bf16_dev(d["x"])
     a = x.index_select(0, torch.from_numpy(d["row_token"]).to(DEV)).contiguous()
     G, O1, H = d["w_gate_up"].shape
-    qa = mx.alloc_nvfp4_rows(rows, H, DEV)
-    mx.mx_nvfp4_quantize_per_token(a, qa["q"], qa["s"], qa["s2"])
+    offs = torch.from_numpy(d["group_offsets"]).to(DEV)
+    qa = mx.alloc_nvfp4_rows_grouped(rows, G, H, DEV)
+    mx.mx_nvfp4_quantize_per_token_grouped(a, offs, qa["q"], qa["s"], qa["s2"])
     qw = mx.alloc_nvfp4_weight_2d(G, O1, H, DEV)
     mx.mx_nvfp4_quantize_weight_2d(bf16_dev(d["w_gate_up"]), qw["q_row"], qw["s_row"], qw["q_col"], qw["s_col"],
                                    qw["s_w"], qw["ws"])
-    offs = torch.from_numpy(d["group_offsets"]).to(DEV)
     y = torch.empty((rows, O1), dtype=torch.bfloat16, device=DEV)
     mx.mx_grouped_scaled_gemm(mx.MX_FMT_NVFP4, offs, qa["q"], qa["s"], qa["s2"], qw["q_row"], qw["s_row"], qw["s_w"],
                               O1, H, y)
@@ -134,7 +134,12 @@ def test_moe_per_token_sampled(orc, moe):
     rows = np.sort(np.random.default_rng(102).choice(R, 256, replace=False))
     q, s, st = orc.nvfp4_quantize_per_token(np.ascontiguousarray(d["x"][d["row_token"][rows]]))
     assert np.array_equal(to_np(qa["q"])[rows], q)
-    assert np.array_equal(laid_rows(orc, to_np(qa["s"]), R, H // 16, rows), s)
+    offs = d["group_offsets"]
+    laid = orc.scales_from_gemm_layout(to_np(qa["s"]), to_np(qa["s"]).size // 512 * 128 // ((H // 16 + 3) // 4), H // 16)
+    # padded row of r: its group's first 128-row tile plus the offset inside the group
+    g = np.searchsorted(offs, rows, side="right") - 1
+    ptile = np.concatenate([[0], np.cumsum((np.diff(offs) + 127) // 128)])
+    assert np.array_equal(laid[ptile[g] * 128 + (rows - offs[g])], s)
     assert np.array_equal(to_np(qa["s2"])[rows], st)
 
 

@@ -199,7 +199,8 @@ def test_grouped_gemm_ragged(mx, orc, fmt):
         alpha_a, alpha_b = None, None
         decode = lambda q, s: orc.decode_mxfp8_f64(q, s)
     d = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device=DEV)
-    mx.mx_grouped_scaled_gemm(fmt, torch.from_numpy(offs).to(DEV), dev_u8(qa), dev_u8(orc.scales_to_gemm_layout(sa)),
+    sa_grouped = orc.scales_to_grouped_layout(sa, offs, mx.grouped_scale_bytes(R, G, K, 32 if fmt == 0 else 16))
+    mx.mx_grouped_scaled_gemm(fmt, torch.from_numpy(offs).to(DEV), dev_u8(qa), dev_u8(sa_grouped),
                               alpha_a, dev_u8(np.stack(qbs)), dev_u8(np.concatenate(sbs)), alpha_b, N, K, d)
     torch.cuda.synchronize()
     mx.check_device_status()

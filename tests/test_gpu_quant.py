@@ -273,3 +273,27 @@ def test_dequant_nvfp4_stacked_2d_weights_group_scope(mx, orc):
         qr, qc, st, sw = orc.nvfp4_quantize_weight_2d(np.ascontiguousarray(w[g]))
         ref = orc.dequant_nvfp4(qr, orc.weight_2d_operand_scales(st, "row"), sw, per_row=False)
         assert np.array_equal(got[g], ref), first_mismatch(got[g], ref)
+
+
+@pytest.mark.parametrize("sizes", [[0, 130, 7, 300, 128, 1], [512] * 3, [1] * 40])
+def test_grouped_quantizers_write_grouped_layout(mx, orc, sizes):
+    """The *_grouped quantizers give the plain codes and the scales in the grouped layout."""
+    G = len(sizes)
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    R, K = int(offs[-1]), 256
+    x = edge_tensor(R + G, (R, K))
+    offs_d = torch.from_numpy(offs).to(DEV)
+    q = torch.empty((R, K // 2), dtype=torch.uint8, device=DEV)
+    s = torch.full((mx.grouped_scale_bytes(R, G, K, 16),), 0x77, dtype=torch.uint8, device=DEV)
+    st = torch.empty(R, dtype=torch.float32, device=DEV)
+    mx.mx_nvfp4_quantize_per_token_grouped(bf16_dev(x), offs_d, q, s, st)
+    qo, so, sto = orc.nvfp4_quantize_per_token(x)
+    assert np.array_equal(to_np(q), qo)
+    assert np.array_equal(to_np(st), sto)
+    assert np.array_equal(to_np(s), orc.scales_to_grouped_layout(so, offs, s.numel()))
+    q8 = torch.empty((R, K), dtype=torch.uint8, device=DEV)
+    s8 = torch.full((mx.grouped_scale_bytes(R, G, K, 32),), 0x77, dtype=torch.uint8, device=DEV)
+    mx.mx_quantize_mxfp8_grouped(bf16_dev(x), offs_d, q8, s8)
+    q8o, s8o = orc.mxfp8_quantize_rowwise(x)
+    assert np.array_equal(to_np(q8), q8o)
+    assert np.array_equal(to_np(s8), orc.scales_to_grouped_layout(s8o, offs, s8.numel()))

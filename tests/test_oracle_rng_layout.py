@@ -56,3 +56,21 @@ def test_scale_layout_round_trip_and_padding(orc):
         np.testing.assert_array_equal(orc.scales_from_gemm_layout(laid, rows, scols), comp)
         # every real scale lands on a distinct byte; the rest is zero padding
         assert int((laid != 0).sum()) == rows * scols
+
+
+def test_grouped_layout_places_each_group_on_a_tile(orc):
+    """Groups of 3, 0, 130 and 1 rows: padded starts 0, 128, 128, 384 (the empty group takes no
+    tile); within a group the plain layout applies from the group's first tile."""
+    sizes = [3, 0, 130, 1]
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    rows, scols = int(off[-1]), 8
+    comp = (np.arange(rows * scols, dtype=np.int64) % 251 + 1).astype(np.uint8).reshape(rows, scols)
+    assert orc.grouped_padded_rows(off) == 128 + 256 + 128
+    laid = orc.scales_to_grouped_layout(comp, off)
+    plain = orc.scales_from_gemm_layout(laid, 512, scols)
+    np.testing.assert_array_equal(plain[0:3], comp[0:3])
+    assert not plain[3:128].any()
+    np.testing.assert_array_equal(plain[128:258], comp[3:133])
+    assert not plain[258:384].any()
+    np.testing.assert_array_equal(plain[384], comp[133])
+    assert int((laid != 0).sum()) == rows * scols
