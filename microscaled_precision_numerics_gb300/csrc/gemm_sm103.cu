@@ -10,8 +10,9 @@
 //
 // Structure (one CTA per SM, persistent over 128 x 256 output tiles):
 //   warp 0        TMA producer: A/B tiles (128-byte swizzle) and scale atoms into a 4-stage ring
-//   warp 1        TMEM allocator; lane 0 issues tcgen05.cp (scales -> TMEM) and tcgen05.mma
-//   warps 2..5    epilogue: tcgen05.ld the FP32 accumulator, scale, round to BF16, store
+//   warp 1        TMEM allocator; lane 0 issues tcgen05.mma
+//   warp 2        lane 0 issues tcgen05.cp (scale atoms -> TMEM), one stage at a time
+//   warps 3..6    epilogue: tcgen05.ld the FP32 accumulator, scale, round to BF16, store
 // Scales arrive in the GEMM layout (512-byte atoms of 128 rows x 4 scale columns) and each stage's
 // atoms are bulk-copied to shared memory, then to TMEM with tcgen05.cp.32x128b.warpx4.  For the
 // grouped GEMM the A scales are in the grouped layout, where every expert group starts on a
@@ -34,8 +35,11 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BKB = 128;                  // K bytes per pipeline stage
-constexpr int STAGES = 4;
-constexpr int NUM_THREADS = 192;
+#ifndef MXK_GEMM_STAGES
+#define MXK_GEMM_STAGES 4
+#endif
+constexpr int STAGES = MXK_GEMM_STAGES;     // depth of the shared-memory operand ring
+constexpr int NUM_THREADS = 224;         // producer, MMA, scale-copy, 4 epilogue warps
 constexpr int A_STAGE_BYTES = BM * BKB;   // 16 KB
 constexpr int B_STAGE_BYTES = BN * BKB;   // 32 KB
 constexpr int TMEM_COLS = 512;
@@ -55,7 +59,7 @@ struct Cfg {
     static constexpr int SMEM_SFA = SMEM_B + STAGES * B_STAGE_BYTES;
     static constexpr int SMEM_SFB = SMEM_SFA + STAGES * SFA_BYTES;
     static constexpr int SMEM_BAR = SMEM_SFB + STAGES * SFB_BYTES;
-    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * STAGES + 4);
+    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (3 * STAGES + 5);
     static constexpr int SMEM_PREFIX = SMEM_MISC + 16;
     static constexpr int SMEM_WARP = SMEM_PREFIX + 4 * (MAX_GROUPS + 1);
     static constexpr int SMEM_TOTAL = SMEM_WARP + 4 * 32;
@@ -248,6 +252,8 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t bar_tfull = bar_empty + 8 * STAGES;
     const uint32_t bar_tempty = bar_tfull + 8;
     const uint32_t bar_done = bar_tempty + 8;
+    const uint32_t bar_sfready = bar_done + 8;                     // STAGES barriers
+    const uint32_t bar_sfdone = bar_sfready + 8 * STAGES;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
     int* ptile = reinterpret_cast<int*>(smem + C::SMEM_PREFIX);
@@ -263,6 +269,8 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         mbar_init(bar_tfull, 1);
         mbar_init(bar_tempty, 4);
         mbar_init(bar_done, 1);
+        for (int st = 0; st < STAGES; ++st) mbar_init(bar_sfready + 8 * st, 1);
+        mbar_init(bar_sfdone, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -328,6 +336,8 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
     } else if (warp == 1) {
         // ------------------------------- MMA issuer -------------------------------
+        // Only waits and MMAs on this thread: the scale copies for each stage are issued by the
+        // scale-copy warp, which signals sf_ready[stage] once they have landed in TMEM.
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
@@ -336,21 +346,13 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (!mbar_wait(bar_tempty, acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 for (int64_t ks = 0; ks < p.k_stages; ++ks) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag) ||
+                        !mbar_wait(bar_sfready + 8 * stage, phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sA = sbase + C::SMEM_A + stage * A_STAGE_BYTES;
                     const uint32_t sB = sbase + C::SMEM_B + stage * B_STAGE_BYTES;
-                    const uint32_t sSFA = sbase + C::SMEM_SFA + stage * C::SFA_BYTES;
-                    const uint32_t sSFB = sbase + C::SMEM_SFB + stage * C::SFB_BYTES;
                     const uint32_t tSFA = tmem + TMEM_SF_BASE + stage * (C::SFA_COLS + C::SFB_COLS);
                     const uint32_t tSFB = tSFA + C::SFA_COLS;
-                    // scales -> TMEM: A atom j to columns 4j..4j+3; B band h, atom j to 8j + 4h
-#pragma unroll
-                    for (int j = 0; j < C::SF_ATOMS_A; ++j) {
-                        tc_cp_sf(tSFA + 4 * j, desc_sf(sSFA + 512 * j));
-                        tc_cp_sf(tSFB + 8 * j, desc_sf(sSFB + 512 * j));
-                        tc_cp_sf(tSFB + 8 * j + 4, desc_sf(sSFB + C::SFA_BYTES + 512 * j));
-                    }
 #pragma unroll
                     for (int j = 0; j < BKB / 32; ++j) {
                         // MXFP8: one atom covers the 4 MMAs of the stage, the scale id picks the byte;
@@ -373,6 +375,42 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 tc_commit(bar_done);
                 const unsigned long long t0 = globaltimer();
                 while (!mbar_try_wait(bar_done, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------- scale copies -------------------------------
+        // Per stage: wait for the loads, copy the A and B scale atoms into that stage's TMEM scale
+        // slot, and signal sf_ready[stage] when the copies complete.  The slot is rewritten only
+        // after the producer re-arms the stage, i.e. after the MMAs that read it have completed.
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true, issued_any = false;
+            for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sSFA = sbase + C::SMEM_SFA + stage * C::SFA_BYTES;
+                    const uint32_t sSFB = sbase + C::SMEM_SFB + stage * C::SFB_BYTES;
+                    const uint32_t tSFA = tmem + TMEM_SF_BASE + stage * (C::SFA_COLS + C::SFB_COLS);
+                    const uint32_t tSFB = tSFA + C::SFA_COLS;
+                    // A atom j to columns 4j..4j+3; B band h, atom j to 8j + 4h
+#pragma unroll
+                    for (int j = 0; j < C::SF_ATOMS_A; ++j) {
+                        tc_cp_sf(tSFA + 4 * j, desc_sf(sSFA + 512 * j));
+                        tc_cp_sf(tSFB + 8 * j, desc_sf(sSFB + 512 * j));
+                        tc_cp_sf(tSFB + 8 * j + 4, desc_sf(sSFB + C::SFA_BYTES + 512 * j));
+                    }
+                    tc_commit(bar_sfready + 8 * stage);
+                    issued_any = true;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (issued_any) {
+                tc_commit(bar_sfdone);
+                const unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(bar_sfdone, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
             }
         }
         __syncwarp();
