@@ -37,6 +37,21 @@ FP8_OVER_BF16 = 2.0      # nominal dense ratio: 4.5 / 2.25 PFLOP/s
 FP4_OVER_BF16 = 6.0      # nominal dense ratio: 13.5 / 2.25 PFLOP/s
 
 
+def recorded_traffic(kernel: str):
+    """Per-launch DRAM bytes (read + write) of `kernel` from the committed ncu capture, or None when
+    the kernel's source has changed since the counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic_dense_mlp.json")) as f:
+            rec = json.load(f)["kernels"][kernel]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
+                return None
+        return int(rec["mean_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -547,12 +562,14 @@ def run_device(args):
     if dominant == "gemm":
         roofline = {"kernel": "bs_gemm_kernel<MXFP8> (FPROP+DGRAD+WGRAD)", "bound": "tensor",
                     "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                    "frac": round(gemm_tflops / fp8_peak, 4), "traffic": None,
+                    "frac": round(gemm_tflops / fp8_peak, 4), "traffic": recorded_traffic("bs_gemm_kernel<MXFP8>"),
+                    "traffic_unit": "DRAM bytes per launch (mean of FPROP, DGRAD, WGRAD; ncu)",
                     "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16:g} (nominal FP8/BF16)"}
     else:
         roofline = {"kernel": "mxfp8_quantize_kernel", "bound": "hbm", "achieved": round(quant_gbs, 1),
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
-                    "traffic": None, "peak_source": f"{peaks['source']} copy bandwidth"}
+                    "traffic": recorded_traffic("mxfp8_quantize_kernel<row,col>"),
+                    "peak_source": f"{peaks['source']} copy bandwidth"}
 
     e2e = None
     if not args.no_e2e:
