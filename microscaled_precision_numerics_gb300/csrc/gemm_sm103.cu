@@ -10,9 +10,14 @@
 //
 // Structure (one CTA per SM, persistent over 128 x 256 output tiles):
 //   warp 0        TMA producer: A/B tiles (128-byte swizzle) and scale atoms into a 4-stage ring
-//   warp 1        TMEM allocator; lane 0 issues tcgen05.mma
-//   warp 2        lane 0 issues tcgen05.cp (scale atoms -> TMEM), one stage at a time
-//   warps 3..6    epilogue: tcgen05.ld the FP32 accumulator, scale, round to BF16, store
+//   warp 1        TMEM allocator; per stage one elected lane copies the stage's scale atoms to TMEM
+//                 (tcgen05.cp) and issues the stage's tcgen05.mma, which the tensor pipe runs in order
+//   warps 2..5    epilogue: tcgen05.ld the FP32 accumulator, scale, round to BF16, hand TMEM back,
+//                 then stage 32-row x (32 | 16)-column BF16 chunks in swizzled shared memory and
+//                 write them with TMA tensor stores (coalesced lines; the map clips ragged edges)
+// The producer and MMA warps run their loops warp-wide and issue through elect.sync: issuing the
+// asynchronous tensor ops from a converged warp is several times cheaper per op than from a single
+// diverged lane.
 // Scales arrive in the GEMM layout (512-byte atoms of 128 rows x 4 scale columns) and each stage's
 // atoms are bulk-copied to shared memory, then to TMEM with tcgen05.cp.32x128b.warpx4.  For the
 // grouped GEMM the A scales are in the grouped layout, where every expert group starts on a
@@ -39,7 +44,7 @@ constexpr int BKB = 128;                  // K bytes per pipeline stage
 #define MXK_GEMM_STAGES 4
 #endif
 constexpr int STAGES = MXK_GEMM_STAGES;     // depth of the shared-memory operand ring
-constexpr int NUM_THREADS = 224;         // producer, MMA, scale-copy, 4 epilogue warps
+constexpr int NUM_THREADS = 192;         // producer, MMA, 4 epilogue warps
 constexpr int A_STAGE_BYTES = BM * BKB;   // 16 KB
 constexpr int B_STAGE_BYTES = BN * BKB;   // 32 KB
 constexpr int TMEM_COLS = 512;
@@ -47,24 +52,33 @@ constexpr int TMEM_SF_BASE = 256;         // accumulator uses columns [0, 256)
 constexpr int MAX_GROUPS = MX_MAX_GROUPS;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
 
-template <int FMT>
+template <int FMT, bool GROUPED>
 struct Cfg {
+    // NVFP4 grouped keeps one stage fewer: its group table and the epilogue staging must fit too
+    static constexpr int NST = (FMT == 1 && GROUPED) ? STAGES - 1 : STAGES;
     static constexpr int SF_ATOMS_A = FMT == 0 ? 1 : 4;   // 512-byte atoms per stage (A side)
     static constexpr int SFA_BYTES = 512 * SF_ATOMS_A;
     static constexpr int SFB_BYTES = 2 * SFA_BYTES;        // two 128-row halves of the 256-row B tile
     static constexpr int SFA_COLS = 4 * SF_ATOMS_A;        // TMEM columns per stage
     static constexpr int SFB_COLS = 2 * SFA_COLS;
+    // epilogue chunk: 32 rows x EPI_COLS BF16 columns per warp, double-buffered, swizzled rows of
+    // 64 bytes (MXFP8) or 32 bytes (NVFP4, whose larger scale stages leave less shared memory)
+    static constexpr int EPI_COLS = FMT == 0 ? 32 : 16;
+    static constexpr int EPI_ROW_BYTES = 2 * EPI_COLS;
+    static constexpr int EPI_BUF_BYTES = 32 * EPI_ROW_BYTES;
     static constexpr int SMEM_A = 0;
-    static constexpr int SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
-    static constexpr int SMEM_SFA = SMEM_B + STAGES * B_STAGE_BYTES;
-    static constexpr int SMEM_SFB = SMEM_SFA + STAGES * SFA_BYTES;
-    static constexpr int SMEM_BAR = SMEM_SFB + STAGES * SFB_BYTES;
-    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (3 * STAGES + 5);
+    static constexpr int SMEM_B = SMEM_A + NST * A_STAGE_BYTES;
+    static constexpr int SMEM_SFA = SMEM_B + NST * B_STAGE_BYTES;
+    static constexpr int SMEM_SFB = SMEM_SFA + NST * SFA_BYTES;
+    static constexpr int SMEM_EPI = SMEM_SFB + NST * SFB_BYTES;      // 1024-aligned (all above are)
+    static constexpr int SMEM_BAR = SMEM_EPI + 4 * 2 * EPI_BUF_BYTES;
+    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 3);
     static constexpr int SMEM_PREFIX = SMEM_MISC + 16;
-    static constexpr int SMEM_WARP = SMEM_PREFIX + 4 * (MAX_GROUPS + 1);
-    static constexpr int SMEM_TOTAL = SMEM_WARP + 4 * 32;
+    static constexpr int SMEM_WARP = SMEM_PREFIX + (GROUPED ? 4 * (MAX_GROUPS + 1) : 0);
+    static constexpr int SMEM_TOTAL = SMEM_WARP + (GROUPED ? 4 * 32 : 0);
     static constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;  // slack for 1024-byte alignment
-    static_assert(TMEM_SF_BASE + STAGES * (SFA_COLS + SFB_COLS) <= TMEM_COLS, "TMEM budget");
+    static_assert(TMEM_SF_BASE + NST * (SFA_COLS + SFB_COLS) <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
 struct Params {
@@ -124,10 +138,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// All lanes of the warp wait; the result is made warp-uniform (any lane's failure fails all).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag)) != 0;
+}
+// One lane of a converged warp (always the lowest active lane, so the same lane every time).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p;
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+    return p != 0;
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1, uint32_t bar) {
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
                  :: "r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar) : "memory");
 }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0, int32_t c1, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 :: "l"(map), "r"(c0), "r"(c1), "r"(src) : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
@@ -242,18 +277,18 @@ __device__ __forceinline__ Tile grouped_tile(const Params& p, const int* ptile, 
 // ---------------------------------------------------------------------------------------------
 template <int FMT, bool GROUPED, bool COL_ALPHA>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
-    using C = Cfg<FMT>;
+bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmD, const Params p) {
+    using C = Cfg<FMT, GROUPED>;
+    constexpr int NST = C::NST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase + C::SMEM_BAR;                 // STAGES barriers
-    const uint32_t bar_empty = bar_full + 8 * STAGES;              // STAGES barriers
-    const uint32_t bar_tfull = bar_empty + 8 * STAGES;
+    const uint32_t bar_full = sbase + C::SMEM_BAR;                 // NST barriers
+    const uint32_t bar_empty = bar_full + 8 * NST;              // NST barriers
+    const uint32_t bar_tfull = bar_empty + 8 * NST;
     const uint32_t bar_tempty = bar_tfull + 8;
     const uint32_t bar_done = bar_tempty + 8;
-    const uint32_t bar_sfready = bar_done + 8;                     // STAGES barriers
-    const uint32_t bar_sfdone = bar_sfready + 8 * STAGES;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
     int* ptile = reinterpret_cast<int*>(smem + C::SMEM_PREFIX);
@@ -262,21 +297,20 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_tfull, 1);
         mbar_init(bar_tempty, 4);
         mbar_init(bar_done, 1);
-        for (int st = 0; st < STAGES; ++st) mbar_init(bar_sfready + 8 * st, 1);
-        mbar_init(bar_sfdone, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0 && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" :: "l"(&tmA) : "memory");
         asm volatile("prefetch.tensormap [%0];" :: "l"(&tmB) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmD) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
@@ -294,8 +328,8 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ------------------------------- producer -------------------------------
         int stage = 0;
         uint32_t phase = 0;
-        int issued_parity[STAGES];
-        for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+        int issued_parity[NST];
+        for (int s = 0; s < NST; ++s) issued_parity[s] = -1;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
             const Tile tile = GROUPED ? grouped_tile(p, ptile, t) : dense_tile(p, t);
@@ -304,13 +338,13 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int64_t bt0 = tile.n0 / 128;                      // first 128-row band of B
             const bool b_hi = tile.n0 + 128 < p.N;                  // does the second band exist?
             for (int64_t ks = 0; ks < p.k_stages; ++ks) {
-                if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+                if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
                 const uint32_t sA = sbase + C::SMEM_A + stage * A_STAGE_BYTES;
                 const uint32_t sB = sbase + C::SMEM_B + stage * B_STAGE_BYTES;
                 const uint32_t sSFA = sbase + C::SMEM_SFA + stage * C::SFA_BYTES;
                 const uint32_t sSFB = sbase + C::SMEM_SFB + stage * C::SFB_BYTES;
                 const int64_t ct0 = ks * C::SF_ATOMS_A;             // first 4-column scale tile of this stage
-                if (lane == 0) {
+                if (elect_one()) {
                     const uint32_t bytes = A_STAGE_BYTES + B_STAGE_BYTES + C::SFA_BYTES + C::SFB_BYTES / (b_hi ? 1 : 2);
                     mbar_arrive_expect_tx(bar_full + 8 * stage, bytes);
                     const int32_t kb = (int32_t)(ks * BKB);
@@ -322,75 +356,36 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         bulk_load(sSFB + C::SFA_BYTES, sb_g + (((bt0 + 1) * p.nct + ct0) << 9), C::SFA_BYTES,
                                   bar_full + 8 * stage);
                 }
+                __syncwarp();
                 issued_parity[stage] = (int)phase;
-                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                if (++stage == NST) { stage = 0; phase ^= 1; }
             }
         }
         if (!ok && lane == 0) {
             // drain: wait (bounded) for every load this warp issued to land before the CTA exits
-            for (int s = 0; s < STAGES; ++s)
+            for (int s = 0; s < NST; ++s)
                 if (issued_parity[s] >= 0) {
                     const unsigned long long t0 = globaltimer();
                     while (!mbar_try_wait(bar_full + 8 * s, (uint32_t)issued_parity[s]) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
                 }
         }
     } else if (warp == 1) {
-        // ------------------------------- MMA issuer -------------------------------
-        // Only waits and MMAs on this thread: the scale copies for each stage are issued by the
-        // scale-copy warp, which signals sf_ready[stage] once they have landed in TMEM.
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
-            bool ok = true, issued_any = false;
-            for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                if (!mbar_wait(bar_tempty, acc_phase ^ 1, abort_flag)) { ok = false; break; }
+        // ------------------------------- scale copies + MMA issuer -------------------------------
+        // Per stage: copy the A and B scale atoms into the stage's TMEM scale slot, then the MMAs that
+        // read them; the tensor pipe executes one thread's tcgen05.cp and tcgen05.mma in issue order,
+        // and a slot is rewritten only after the MMAs of its previous use were issued.
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        bool ok = true, issued_any = false;
+        for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            if (!warp_wait(bar_tempty, acc_phase ^ 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                if (!warp_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                for (int64_t ks = 0; ks < p.k_stages; ++ks) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag) ||
-                        !mbar_wait(bar_sfready + 8 * stage, phase, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
+                if (elect_one()) {
                     const uint32_t sA = sbase + C::SMEM_A + stage * A_STAGE_BYTES;
                     const uint32_t sB = sbase + C::SMEM_B + stage * B_STAGE_BYTES;
-                    const uint32_t tSFA = tmem + TMEM_SF_BASE + stage * (C::SFA_COLS + C::SFB_COLS);
-                    const uint32_t tSFB = tSFA + C::SFA_COLS;
-#pragma unroll
-                    for (int j = 0; j < BKB / 32; ++j) {
-                        // MXFP8: one atom covers the 4 MMAs of the stage, the scale id picks the byte;
-                        // NVFP4: each MMA (K = 64) consumes a whole atom word
-                        const uint32_t sf_id = FMT == 0 ? (uint32_t)j : 0u;
-                        const uint32_t col = FMT == 0 ? 0u : (uint32_t)j;
-                        tc_mma<FMT>(tmem, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j), make_idesc<FMT>(sf_id),
-                                    tSFA + 4 * col, tSFB + 8 * col, (ks > 0 || j > 0) ? 1u : 0u);
-                    }
-                    issued_any = true;
-                    tc_commit(bar_empty + 8 * stage);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
-                }
-                if (!ok) break;
-                tc_commit(bar_tfull);
-                acc_phase ^= 1;
-            }
-            if (issued_any) {
-                // every tcgen05 op this thread issued has completed once bar_done flips
-                tc_commit(bar_done);
-                const unsigned long long t0 = globaltimer();
-                while (!mbar_try_wait(bar_done, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
-            }
-        }
-        __syncwarp();
-    } else if (warp == 2) {
-        // ------------------------------- scale copies -------------------------------
-        // Per stage: wait for the loads, copy the A and B scale atoms into that stage's TMEM scale
-        // slot, and signal sf_ready[stage] when the copies complete.  The slot is rewritten only
-        // after the producer re-arms the stage, i.e. after the MMAs that read it have completed.
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true, issued_any = false;
-            for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                for (int64_t ks = 0; ks < p.k_stages; ++ks) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
                     const uint32_t sSFA = sbase + C::SMEM_SFA + stage * C::SFA_BYTES;
                     const uint32_t sSFB = sbase + C::SMEM_SFB + stage * C::SFB_BYTES;
                     const uint32_t tSFA = tmem + TMEM_SF_BASE + stage * (C::SFA_COLS + C::SFB_COLS);
@@ -402,22 +397,39 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         tc_cp_sf(tSFB + 8 * j, desc_sf(sSFB + 512 * j));
                         tc_cp_sf(tSFB + 8 * j + 4, desc_sf(sSFB + C::SFA_BYTES + 512 * j));
                     }
-                    tc_commit(bar_sfready + 8 * stage);
-                    issued_any = true;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+#pragma unroll
+                    for (int j = 0; j < BKB / 32; ++j) {
+                        // MXFP8: one atom covers the 4 MMAs of the stage, the scale id picks the byte;
+                        // NVFP4: each MMA (K = 64) consumes a whole atom word
+                        const uint32_t sf_id = FMT == 0 ? (uint32_t)j : 0u;
+                        const uint32_t col = FMT == 0 ? 0u : (uint32_t)j;
+                        tc_mma<FMT>(tmem, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j), make_idesc<FMT>(sf_id),
+                                    tSFA + 4 * col, tSFB + 8 * col, (ks > 0 || j > 0) ? 1u : 0u);
+                    }
+                    tc_commit(bar_empty + 8 * stage);
                 }
+                __syncwarp();
+                issued_any = true;
+                if (++stage == NST) { stage = 0; phase ^= 1; }
             }
-            if (issued_any) {
-                tc_commit(bar_sfdone);
-                const unsigned long long t0 = globaltimer();
-                while (!mbar_try_wait(bar_sfdone, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
-            }
+            if (!ok) break;
+            if (elect_one()) tc_commit(bar_tfull);
+            __syncwarp();
+            acc_phase ^= 1;
         }
-        __syncwarp();
+        if (issued_any) {
+            // every tcgen05 op this warp issued has completed once bar_done flips
+            if (elect_one()) {
+                tc_commit(bar_done);
+                const unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(bar_done, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
+            }
+            __syncwarp();
+        }
     } else {
         // ------------------------------- epilogue -------------------------------
         const int q = warp & 3;                     // TMEM lane quadrant this warp may access
-        uint32_t acc_phase = 0;
+        uint32_t acc_phase = 0, epi_chunk = 0;
         for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
             const Tile tile = GROUPED ? grouped_tile(p, ptile, t) : dense_tile(p, t);
             if (!mbar_wait(bar_tfull, acc_phase, abort_flag)) break;
@@ -430,9 +442,8 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             float ab_g = 1.0f;
             if (GROUPED && p.alpha_b_scope != 0) ab_g = __ldg(p.alpha_b + tile.g);
             else if (!GROUPED && p.alpha_b_scope == 1) ab_g = __ldg(p.alpha_b);
-            uint16_t* drow = p.d + row * p.ldd;
             // drain the accumulator slice (this thread's row, 256 columns) into packed BF16 registers,
-            // then hand TMEM back to the MMA warp before the global stores
+            // then hand TMEM back to the MMA warp before the stores
             uint32_t packed[BN / 2];
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
@@ -455,17 +466,55 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_tempty);
-            if (row_ok) {
-                // N and ldd are multiples of 8: every 8-column group is one aligned 16-byte store
+            const int64_t wrow0 = tile.row0 + q * 32;              // first row of this warp's slice
+            if (wrow0 < tile.row_end) {
+                if (!GROUPED || wrow0 + 32 <= tile.row_end) {
+                    // TMA stores; the tensor map clips rows >= M and columns >= N
+                    const uint32_t ebase = sbase + C::SMEM_EPI + (uint32_t)(q * 2 * C::EPI_BUF_BYTES);
+                    const uint32_t rbase_off = (uint32_t)(lane * C::EPI_ROW_BYTES);
 #pragma unroll
-                for (int g8 = 0; g8 < BN / 8; ++g8) {
-                    if (tile.n0 + g8 * 8 < p.N)
-                        *reinterpret_cast<uint4*>(drow + tile.n0 + g8 * 8) =
-                            make_uint4(packed[4 * g8], packed[4 * g8 + 1], packed[4 * g8 + 2], packed[4 * g8 + 3]);
+                    for (int c = 0; c < BN / C::EPI_COLS; ++c) {
+                        const int64_t col0 = tile.n0 + c * C::EPI_COLS;
+                        if (col0 < p.N) {
+                            const uint32_t buf = ebase + (epi_chunk & 1u) * (uint32_t)C::EPI_BUF_BYTES;
+                            ++epi_chunk;
+                            // the store issued from this buffer two chunks ago must have read it
+                            if (lane == 0) bulk_wait_group_read1();
+                            __syncwarp();
+#pragma unroll
+                            for (int j = 0; j < C::EPI_COLS / 8; ++j) {
+                                // 16-byte piece j of this row, at its 64-byte (MXFP8) / 32-byte (NVFP4)
+                                // swizzle position
+                                const uint32_t phys = FMT == 0 ? ((uint32_t)j ^ ((uint32_t)(lane >> 1) & 3u))
+                                                               : ((uint32_t)j ^ ((uint32_t)(lane >> 2) & 1u));
+                                const int pk = c * (C::EPI_COLS / 2) + 4 * j;
+                                st_shared_v4(buf + rbase_off + 16u * phys, packed[pk], packed[pk + 1], packed[pk + 2],
+                                             packed[pk + 3]);
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&tmD, (int32_t)col0, (int32_t)wrow0, buf);
+                                bulk_commit_group();
+                            }
+                        }
+                    }
+                } else if (row_ok) {
+                    // the slice straddles the end of the expert group: the next group's rows belong to
+                    // another tile, so store this group's rows only (16-byte stores, N and ldd % 8 == 0)
+                    uint16_t* drow = p.d + row * p.ldd;
+#pragma unroll
+                    for (int g8 = 0; g8 < BN / 8; ++g8) {
+                        if (tile.n0 + g8 * 8 < p.N)
+                            *reinterpret_cast<uint4*>(drow + tile.n0 + g8 * 8) =
+                                make_uint4(packed[4 * g8], packed[4 * g8 + 1], packed[4 * g8 + 2], packed[4 * g8 + 3]);
+                    }
                 }
             }
             acc_phase ^= 1;
         }
+        if (lane == 0) bulk_wait_group_all();     // staging buffers read and stores complete before exit
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -504,9 +553,24 @@ bool make_map(CUtensorMap* map, const uint8_t* base, int64_t k_bytes, int64_t ro
     return r == CUDA_SUCCESS;
 }
 
+// Output map: BF16 [rows, N] with row pitch ldd, box of `box_cols` x 32 rows, swizzled to match the
+// epilogue's staging layout.
+bool make_out_map(CUtensorMap* map, uint16_t* d, int64_t rows, int64_t N, int64_t ldd, uint32_t box_cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ldd * 2)};
+    cuuint32_t box[2] = {box_cols, 32};
+    cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw = box_cols * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, d, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int FMT, bool GROUPED, bool COL_ALPHA>
 cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
-    using C = Cfg<FMT>;
+    using C = Cfg<FMT, GROUPED>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -520,6 +584,8 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
     CUtensorMap tmA, tmB;
     if (!make_map(&tmA, a.a, k_bytes, a.M, BM)) return cudaErrorInvalidValue;
     if (!make_map(&tmB, a.b, k_bytes, GROUPED ? a.G * a.N : a.N, BN)) return cudaErrorInvalidValue;
+    CUtensorMap tmD;
+    if (!make_out_map(&tmD, a.d, a.M, a.N, a.ldd, (uint32_t)C::EPI_COLS)) return cudaErrorInvalidValue;
 
     Params p{};
     p.sa = a.sa; p.sb = a.sb;
@@ -535,7 +601,7 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
     p.total_tiles = p.m_tiles * p.n_tiles;
     int64_t tiles_bound = GROUPED ? (p.m_tiles + a.G) * p.n_tiles : p.total_tiles;
     const unsigned grid = (unsigned)max64(1, min64(tiles_bound, num_sms));
-    bs_gemm_kernel<FMT, GROUPED, COL_ALPHA><<<grid, NUM_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmB, p);
+    bs_gemm_kernel<FMT, GROUPED, COL_ALPHA><<<grid, NUM_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmB, tmD, p);
     return cudaGetLastError();
 }
 
