@@ -160,6 +160,27 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0,
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
                  :: "l"(map), "r"(c0), "r"(c1), "r"(src) : "memory");
 }
+// Load signalling an mbarrier that may sit in the peer CTA of the pair (cta_group::2 form).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1, uint32_t bar_cluster) {
+    asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 :: "r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar_cluster) : "memory");
+}
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t cta_rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(cta_rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(bar_cluster) : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -176,6 +197,29 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 }
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Pair (cta_group::2) forms: issued by the even CTA of the pair, act on both CTAs' shared memory and
+// TMEM at the same addresses; commits arrive on the barrier at the same offset in every CTA of `mask`.
+__device__ __forceinline__ void tc2_commit_mc(uint32_t bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 :: "r"(bar), "h"(mask) : "memory");
+}
+__device__ __forceinline__ void tc2_cp_sf(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+}
+template <int FMT>
+__device__ __forceinline__ void tc2_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                        uint32_t sfb, uint32_t acc) {
+    if (FMT == 0) {
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+                     :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
+    } else {
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+                     :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
+    }
 }
 
 template <int FMT>
@@ -207,12 +251,12 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
 // Instruction descriptor for the block-scaled kinds: B scale id (bits 4-5), A/B formats (7-9,
 // 10-12), K-major A and B, N >> 3 (17-22), scale type (23: 1 = UE8M0, 0 = UE4M3), M >> 4 (24-28),
 // A scale id (29-30).
-template <int FMT>
+template <int FMT, int MMA_M = BM>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
     const uint32_t fmt = FMT == 0 ? 0u : 1u;          // E4M3 (mxf8f6f4) / E2M1 (mxf4nvf4)
     const uint32_t scale_type = FMT == 0 ? 1u : 0u;
     return (sf_id << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(BN >> 3) << 17) | (scale_type << 23) |
-           ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
+           ((uint32_t)(MMA_M >> 4) << 24) | (sf_id << 29);
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
@@ -270,6 +314,96 @@ __device__ __forceinline__ Tile grouped_tile(const Params& p, const int* ptile, 
     r.g = g;
     r.sf_tile = mt_global;
     return r;
+}
+
+// One output tile slice of an epilogue warp: drain the warp's 32 TMEM lanes (256 FP32 columns) into
+// packed BF16 registers with the second-level scales applied, hand TMEM back (arrive on tempty_bar,
+// in this CTA or, for the pair kernel, in the leader CTA), then store the rows [row0 + 32 q, +32) that
+// belong to the tile: TMA stores from the warp's two staging buffers at ebase, or plain 16-byte
+// stores for a slice that straddles the end of an expert group.
+template <int FMT, bool GROUPED, bool COL_ALPHA, int EPI_COLS, int EPI_BUF_BYTES, bool REMOTE_ARRIVE>
+__device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap* tmD, uint32_t tmem, int q, int lane,
+                                              int64_t row0, int64_t row_end, int64_t n0, int64_t g, uint32_t ebase,
+                                              uint32_t& epi_chunk, uint32_t tempty_bar) {
+    constexpr int EPI_ROW_BYTES = 2 * EPI_COLS;
+    const int64_t row = row0 + q * 32 + lane;
+    const bool row_ok = row < row_end;
+    float aa = 1.0f;
+    if (p.alpha_a_scope == 1) aa = __ldg(p.alpha_a);
+    else if (p.alpha_a_scope == 2 && row_ok) aa = __ldg(p.alpha_a + row);
+    float ab_g = 1.0f;
+    if (GROUPED && p.alpha_b_scope != 0) ab_g = __ldg(p.alpha_b + g);
+    else if (!GROUPED && p.alpha_b_scope == 1) ab_g = __ldg(p.alpha_b);
+    // drain the accumulator slice (this thread's row, 256 columns) into packed BF16 registers,
+    // then hand TMEM back to the MMA warp before the stores
+    uint32_t packed[BN / 2];
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float f0 = __fmul_rn(v[2 * i], aa), f1 = __fmul_rn(v[2 * i + 1], aa);
+            if (COL_ALPHA) {
+                const int64_t n = n0 + c * 32 + 2 * i;
+                f0 = __fmul_rn(f0, n < p.N ? __ldg(p.alpha_b + n) : 0.0f);
+                f1 = __fmul_rn(f1, n + 1 < p.N ? __ldg(p.alpha_b + n + 1) : 0.0f);
+            } else {
+                f0 = __fmul_rn(f0, ab_g);
+                f1 = __fmul_rn(f1, ab_g);
+            }
+            packed[c * 16 + i] = pack_bf16x2(f0, f1);
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+        if (REMOTE_ARRIVE) mbar_arrive_cluster(tempty_bar); else mbar_arrive(tempty_bar);
+    }
+    const int64_t wrow0 = row0 + q * 32;              // first row of this warp's slice
+    if (wrow0 < row_end) {
+        if (!GROUPED || wrow0 + 32 <= row_end) {
+            // TMA stores; the tensor map clips rows >= M and columns >= N
+            const uint32_t rbase_off = (uint32_t)(lane * EPI_ROW_BYTES);
+#pragma unroll
+            for (int c = 0; c < BN / EPI_COLS; ++c) {
+                const int64_t col0 = n0 + c * EPI_COLS;
+                if (col0 < p.N) {
+                    const uint32_t buf = ebase + (epi_chunk & 1u) * (uint32_t)EPI_BUF_BYTES;
+                    ++epi_chunk;
+                    // the store issued from this buffer two chunks ago must have read it
+                    if (lane == 0) bulk_wait_group_read1();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < EPI_COLS / 8; ++j) {
+                        // 16-byte piece j of this row at its position under the 64-byte (32-column
+                        // chunk) or 32-byte (16-column chunk) swizzle of the output map
+                        const uint32_t phys = EPI_COLS == 32 ? ((uint32_t)j ^ ((uint32_t)(lane >> 1) & 3u))
+                                                             : ((uint32_t)j ^ ((uint32_t)(lane >> 2) & 1u));
+                        const int pk = c * (EPI_COLS / 2) + 4 * j;
+                        st_shared_v4(buf + rbase_off + 16u * phys, packed[pk], packed[pk + 1], packed[pk + 2],
+                                     packed[pk + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(tmD, (int32_t)col0, (int32_t)wrow0, buf);
+                        bulk_commit_group();
+                    }
+                }
+            }
+        } else if (row_ok) {
+            // the slice straddles the end of the expert group: the next group's rows belong to
+            // another tile, so store this group's rows only (16-byte stores, N and ldd % 8 == 0)
+            uint16_t* drow = p.d + row * p.ldd;
+#pragma unroll
+            for (int g8 = 0; g8 < BN / 8; ++g8) {
+                if (n0 + g8 * 8 < p.N)
+                    *reinterpret_cast<uint4*>(drow + n0 + g8 * 8) =
+                        make_uint4(packed[4 * g8], packed[4 * g8 + 1], packed[4 * g8 + 2], packed[4 * g8 + 3]);
+            }
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -434,83 +568,9 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const Tile tile = GROUPED ? grouped_tile(p, ptile, t) : dense_tile(p, t);
             if (!mbar_wait(bar_tfull, acc_phase, abort_flag)) break;
             tc_fence_after();
-            const int64_t row = tile.row0 + q * 32 + lane;
-            const bool row_ok = row < tile.row_end;
-            float aa = 1.0f;
-            if (p.alpha_a_scope == 1) aa = __ldg(p.alpha_a);
-            else if (p.alpha_a_scope == 2 && row_ok) aa = __ldg(p.alpha_a + row);
-            float ab_g = 1.0f;
-            if (GROUPED && p.alpha_b_scope != 0) ab_g = __ldg(p.alpha_b + tile.g);
-            else if (!GROUPED && p.alpha_b_scope == 1) ab_g = __ldg(p.alpha_b);
-            // drain the accumulator slice (this thread's row, 256 columns) into packed BF16 registers,
-            // then hand TMEM back to the MMA warp before the stores
-            uint32_t packed[BN / 2];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                float v[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float f0 = __fmul_rn(v[2 * i], aa), f1 = __fmul_rn(v[2 * i + 1], aa);
-                    if (COL_ALPHA) {
-                        const int64_t n = tile.n0 + c * 32 + 2 * i;
-                        f0 = __fmul_rn(f0, n < p.N ? __ldg(p.alpha_b + n) : 0.0f);
-                        f1 = __fmul_rn(f1, n + 1 < p.N ? __ldg(p.alpha_b + n + 1) : 0.0f);
-                    } else {
-                        f0 = __fmul_rn(f0, ab_g);
-                        f1 = __fmul_rn(f1, ab_g);
-                    }
-                    packed[c * 16 + i] = pack_bf16x2(f0, f1);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tempty);
-            const int64_t wrow0 = tile.row0 + q * 32;              // first row of this warp's slice
-            if (wrow0 < tile.row_end) {
-                if (!GROUPED || wrow0 + 32 <= tile.row_end) {
-                    // TMA stores; the tensor map clips rows >= M and columns >= N
-                    const uint32_t ebase = sbase + C::SMEM_EPI + (uint32_t)(q * 2 * C::EPI_BUF_BYTES);
-                    const uint32_t rbase_off = (uint32_t)(lane * C::EPI_ROW_BYTES);
-#pragma unroll
-                    for (int c = 0; c < BN / C::EPI_COLS; ++c) {
-                        const int64_t col0 = tile.n0 + c * C::EPI_COLS;
-                        if (col0 < p.N) {
-                            const uint32_t buf = ebase + (epi_chunk & 1u) * (uint32_t)C::EPI_BUF_BYTES;
-                            ++epi_chunk;
-                            // the store issued from this buffer two chunks ago must have read it
-                            if (lane == 0) bulk_wait_group_read1();
-                            __syncwarp();
-#pragma unroll
-                            for (int j = 0; j < C::EPI_COLS / 8; ++j) {
-                                // 16-byte piece j of this row, at its 64-byte (MXFP8) / 32-byte (NVFP4)
-                                // swizzle position
-                                const uint32_t phys = FMT == 0 ? ((uint32_t)j ^ ((uint32_t)(lane >> 1) & 3u))
-                                                               : ((uint32_t)j ^ ((uint32_t)(lane >> 2) & 1u));
-                                const int pk = c * (C::EPI_COLS / 2) + 4 * j;
-                                st_shared_v4(buf + rbase_off + 16u * phys, packed[pk], packed[pk + 1], packed[pk + 2],
-                                             packed[pk + 3]);
-                            }
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) {
-                                tma_store_2d(&tmD, (int32_t)col0, (int32_t)wrow0, buf);
-                                bulk_commit_group();
-                            }
-                        }
-                    }
-                } else if (row_ok) {
-                    // the slice straddles the end of the expert group: the next group's rows belong to
-                    // another tile, so store this group's rows only (16-byte stores, N and ldd % 8 == 0)
-                    uint16_t* drow = p.d + row * p.ldd;
-#pragma unroll
-                    for (int g8 = 0; g8 < BN / 8; ++g8) {
-                        if (tile.n0 + g8 * 8 < p.N)
-                            *reinterpret_cast<uint4*>(drow + tile.n0 + g8 * 8) =
-                                make_uint4(packed[4 * g8], packed[4 * g8 + 1], packed[4 * g8 + 2], packed[4 * g8 + 3]);
-                    }
-                }
-            }
+            epilogue_tile<FMT, GROUPED, COL_ALPHA, C::EPI_COLS, C::EPI_BUF_BYTES, false>(
+                p, &tmD, tmem, q, lane, tile.row0, tile.row_end, tile.n0, tile.g,
+                sbase + C::SMEM_EPI + (uint32_t)(q * 2 * C::EPI_BUF_BYTES), epi_chunk, bar_tempty);
             acc_phase ^= 1;
         }
         if (lane == 0) bulk_wait_group_all();     // staging buffers read and stores complete before exit
@@ -522,6 +582,269 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc_fence_after();
     if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
+}
+
+
+// ---------------------------------------------------------------------------------------------
+// CTA-pair kernel: 256 x 256 output tiles, each computed by the two CTAs of a cluster with the
+// cta_group::2 MMA (M = 256, 128 rows in each CTA's TMEM; B split by N halves between the two CTAs'
+// shared memory).  Each SM loads half of the B tile, so a stage carries 2/3 of the single-CTA bytes
+// for the same MMA work, and the ring holds more stages.
+//   both CTAs  warp 0: TMA loads of this CTA's A rows, B half and scale atoms (the B scales of all
+//              256 columns, which each CTA's tensor core reads from its own TMEM); every load
+//              signals the stage barrier in the even (leader) CTA
+//   leader     warp 1: tcgen05.cp (each CTA's atoms into its own TMEM) and tcgen05.mma for the pair;
+//              commits arrive on the barriers of both CTAs
+//   both CTAs  warps 2..5: epilogue of this CTA's 128 rows; TMEM release arrives in the leader
+// ---------------------------------------------------------------------------------------------
+template <int FMT, bool GROUPED>
+struct PairCfg {
+    static constexpr int NST = FMT == 0 ? 6 : 5;
+    static constexpr int SF_ATOMS_A = FMT == 0 ? 1 : 4;
+    static constexpr int SFA_BYTES = 512 * SF_ATOMS_A;     // this CTA's 128 rows
+    static constexpr int SFB_BYTES = 2 * SFA_BYTES;        // all 256 columns
+    static constexpr int SFA_COLS = 4 * SF_ATOMS_A;
+    static constexpr int SFB_COLS = 2 * SFA_COLS;
+    static constexpr int A_BYTES = 128 * BKB;
+    static constexpr int B_BYTES = 128 * BKB;
+    static constexpr uint32_t STAGE_TX = 2u * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES);   // both CTAs
+    static constexpr int EPI_COLS = FMT == 0 ? 32 : 16;
+    static constexpr int EPI_BUF_BYTES = 32 * 2 * EPI_COLS;
+    static constexpr int SMEM_A = 0;
+    static constexpr int SMEM_B = SMEM_A + NST * A_BYTES;
+    static constexpr int SMEM_SFA = SMEM_B + NST * B_BYTES;
+    static constexpr int SMEM_SFB = SMEM_SFA + NST * SFA_BYTES;
+    static constexpr int SMEM_EPI = SMEM_SFB + NST * SFB_BYTES;
+    static constexpr int SMEM_BAR = SMEM_EPI + 4 * 2 * EPI_BUF_BYTES;
+    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 3);
+    static constexpr int SMEM_TABLES = SMEM_MISC + 16;     // grouped: pair-tile and band prefixes
+    static constexpr int SMEM_TOTAL = SMEM_TABLES + (GROUPED ? 4 * (2 * (MAX_GROUPS + 1) + 32) : 0);
+    static constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;
+    static_assert(SMEM_EPI % 1024 == 0, "staging alignment");
+    static_assert(TMEM_SF_BASE + NST * (SFA_COLS + SFB_COLS) <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+struct PairTile {
+    int64_t row0, row_end;   // this CTA's rows [row0, row0 + 128), real below row_end
+    int64_t n0;              // first output column of the pair tile
+    int64_t g;               // group (grouped GEMM) or 0
+    int64_t band_a;          // 128-row band of A's scale layout holding this CTA's rows
+};
+
+// Dense: bands of 8 pair rows (16 M-tiles); inside a band N-tiles advance every 8 pair tiles.
+__device__ __forceinline__ PairTile pair_dense_tile(const Params& p, int64_t t, uint32_t rank) {
+    constexpr int64_t GM = 8;
+    const int64_t band_tiles = GM * p.n_tiles;
+    const int64_t band = t / band_tiles, in = t % band_tiles;
+    const int64_t band_m = min64(GM, p.m_tiles - band * GM);
+    const int64_t mp = band * GM + in % band_m, nt = in / band_m;
+    PairTile r;
+    r.row0 = mp * 256 + 128 * (int64_t)rank; r.row_end = p.M; r.n0 = nt * BN; r.g = 0;
+    r.band_a = mp * 2 + rank;
+    return r;
+}
+
+// Grouped: ptile2[g] = pair tiles (256 rows) of groups < g, pband[g] = 128-row bands of groups < g
+// (group g's first band in the grouped scale layout).
+__device__ __forceinline__ PairTile pair_grouped_tile(const Params& p, const int* ptile2, const int* pband, int64_t t,
+                                                      uint32_t rank) {
+    const int64_t mt_global = t / p.n_tiles;
+    int lo = 0, hi = (int)p.G;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (ptile2[mid] <= mt_global) lo = mid; else hi = mid;
+    }
+    const int64_t g = lo;
+    const int64_t pm = mt_global - ptile2[g];
+    PairTile r;
+    r.row0 = __ldg(p.group_offsets + g) + pm * 256 + 128 * (int64_t)rank;
+    r.row_end = __ldg(p.group_offsets + g + 1);
+    r.n0 = (t % p.n_tiles) * BN;
+    r.g = g;
+    r.band_a = pband[g] + 2 * pm + rank;
+    return r;
+}
+
+template <int FMT, bool GROUPED, bool COL_ALPHA>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                    const __grid_constant__ CUtensorMap tmD, const Params p) {
+    using C = PairCfg<FMT, GROUPED>;
+    constexpr int NST = C::NST;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + C::SMEM_BAR;                 // NST barriers (used in the leader)
+    const uint32_t bar_empty = bar_full + 8 * NST;                 // NST barriers
+    const uint32_t bar_tfull = bar_empty + 8 * NST;
+    const uint32_t bar_tempty = bar_tfull + 8;                     // used in the leader
+    const uint32_t bar_done = bar_tempty + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
+    int* ptile2 = reinterpret_cast<int*>(smem + C::SMEM_TABLES);
+    int* pband = ptile2 + (MAX_GROUPS + 1);
+    int* s_warp = pband + (MAX_GROUPS + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_tfull, 1);
+        mbar_init(bar_tempty, 8);            // 4 epilogue warps in each CTA
+        mbar_init(bar_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmB) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmSA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmSB) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmD) : "memory");
+    }
+    if (warp == 1) {
+        // one allocation for the pair, made by a warp of each CTA together
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    if (GROUPED) {
+        scan_group_tiles<256>(p.group_offsets, (int)p.G, ptile2, s_warp);
+        scan_group_tiles<128>(p.group_offsets, (int)p.G, pband, s_warp);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();                       // barriers of both CTAs initialised before any signal
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int64_t total_tiles = GROUPED ? (int64_t)ptile2[p.G] * p.n_tiles : p.total_tiles;
+    const int64_t pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+
+    if (warp == 0) {
+        // ------------------------------- producer (both CTAs) -------------------------------
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
+            const PairTile tile = GROUPED ? pair_grouped_tile(p, ptile2, pband, t, rank) : pair_dense_tile(p, t, rank);
+            const int64_t brow = (GROUPED ? tile.g * p.N : 0) + tile.n0 + 128 * (int64_t)rank;
+            const int64_t sfb_y0 = GROUPED ? tile.g * (p.sb_group_bytes >> 8) : 0;   // 256-byte rows
+            const int64_t bt0 = tile.n0 / 128;
+            for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+                if (elect_one()) {
+                    const uint32_t fb = map_to_cta(bar_full + 8 * stage, 0);
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::STAGE_TX);
+                    const uint32_t sA = sbase + C::SMEM_A + stage * C::A_BYTES;
+                    const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES;
+                    const uint32_t sSFA = sbase + C::SMEM_SFA + stage * C::SFA_BYTES;
+                    const uint32_t sSFB = sbase + C::SMEM_SFB + stage * C::SFB_BYTES;
+                    const int64_t ct0 = ks * C::SF_ATOMS_A;
+                    const int32_t kb = (int32_t)(ks * BKB);
+                    tma_load_2d_pair(sA, &tmA, kb, (int32_t)tile.row0, fb);
+                    tma_load_2d_pair(sB, &tmB, kb, (int32_t)brow, fb);
+                    // scale atoms: 512 bytes = two 256-byte rows of the scale maps; bands past the
+                    // end of a tensor read as zeros
+                    tma_load_2d_pair(sSFA, &tmSA, 0, (int32_t)((tile.band_a * p.nct + ct0) * 2), fb);
+                    tma_load_2d_pair(sSFB, &tmSB, 0, (int32_t)(sfb_y0 + (bt0 * p.nct + ct0) * 2), fb);
+                    tma_load_2d_pair(sSFB + C::SFA_BYTES, &tmSB, 0, (int32_t)(sfb_y0 + ((bt0 + 1) * p.nct + ct0) * 2), fb);
+                }
+                __syncwarp();
+                if (++stage == NST) { stage = 0; phase ^= 1; }
+            }
+        }
+        if (!ok && lane == 0) *abort_flag = 1;
+    } else if (warp == 1) {
+        // ------------------------------- scale copies + MMA (leader) -------------------------------
+        if (leader) {
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true, issued_any = false;
+            for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
+                if (!warp_wait(bar_tempty, acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                    if (!warp_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    if (elect_one()) {
+                        const uint32_t sA = sbase + C::SMEM_A + stage * C::A_BYTES;
+                        const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES;
+                        const uint32_t sSFA = sbase + C::SMEM_SFA + stage * C::SFA_BYTES;
+                        const uint32_t sSFB = sbase + C::SMEM_SFB + stage * C::SFB_BYTES;
+                        const uint32_t tSFA = tmem + TMEM_SF_BASE + stage * (C::SFA_COLS + C::SFB_COLS);
+                        const uint32_t tSFB = tSFA + C::SFA_COLS;
+#pragma unroll
+                        for (int j = 0; j < C::SF_ATOMS_A; ++j) {
+                            tc2_cp_sf(tSFA + 4 * j, desc_sf(sSFA + 512 * j));
+                            tc2_cp_sf(tSFB + 8 * j, desc_sf(sSFB + 512 * j));
+                            tc2_cp_sf(tSFB + 8 * j + 4, desc_sf(sSFB + C::SFA_BYTES + 512 * j));
+                        }
+#pragma unroll
+                        for (int j = 0; j < BKB / 32; ++j) {
+                            const uint32_t sf_id = FMT == 0 ? (uint32_t)j : 0u;
+                            const uint32_t col = FMT == 0 ? 0u : (uint32_t)j;
+                            tc2_mma<FMT>(tmem, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j),
+                                         make_idesc<FMT, 2 * BM>(sf_id), tSFA + 4 * col, tSFB + 8 * col,
+                                         (ks > 0 || j > 0) ? 1u : 0u);
+                        }
+                        tc2_commit_mc(bar_empty + 8 * stage, (uint16_t)3);
+                    }
+                    __syncwarp();
+                    issued_any = true;
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                if (elect_one()) tc2_commit_mc(bar_tfull, (uint16_t)3);
+                __syncwarp();
+                acc_phase ^= 1;
+            }
+            if (issued_any) {
+                // the pair's MMAs read the peer's shared memory: all of them complete before either
+                // CTA leaves the final cluster barrier
+                if (elect_one()) {
+                    tc2_commit_mc(bar_done, (uint16_t)1);
+                    const unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(bar_done, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
+                }
+                __syncwarp();
+            }
+        }
+    } else {
+        // ------------------------------- epilogue (both CTAs) -------------------------------
+        const int q = warp & 3;
+        const uint32_t tempty_leader = map_to_cta(bar_tempty, 0);
+        uint32_t acc_phase = 0, epi_chunk = 0;
+        for (int64_t t = pair_id; t < total_tiles; t += n_pairs) {
+            const PairTile tile = GROUPED ? pair_grouped_tile(p, ptile2, pband, t, rank) : pair_dense_tile(p, t, rank);
+            if (!mbar_wait(bar_tfull, acc_phase, abort_flag)) break;
+            tc_fence_after();
+            epilogue_tile<FMT, GROUPED, COL_ALPHA, C::EPI_COLS, C::EPI_BUF_BYTES, true>(
+                p, &tmD, tmem, q, lane, tile.row0, tile.row_end, tile.n0, tile.g,
+                sbase + C::SMEM_EPI + (uint32_t)(q * 2 * C::EPI_BUF_BYTES), epi_chunk, tempty_leader);
+            acc_phase ^= 1;
+        }
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        // after an expired wait: give loads already issued by this CTA time to land before exit
+        const unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {}
+    }
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -605,17 +928,105 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+
+// Scale tensor viewed as rows of 256 bytes (two rows per 512-byte atom), box of `atoms` atoms.
+bool make_sf_map(CUtensorMap* map, const uint8_t* base, int64_t bytes, uint32_t atoms) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {256, (cuuint64_t)(bytes / 256)};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {256, 2 * atoms};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int FMT, bool GROUPED, bool COL_ALPHA>
+cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
+    using C = PairCfg<FMT, GROUPED>;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    static int resident_pairs = 0;          // CTA pairs that fit on the GPU at once
+    std::call_once(attr_once, [num_sms] {
+        auto kern = bs_gemm_pair_kernel<FMT, GROUPED, COL_ALPHA>;
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        if (attr_err != cudaSuccess) return;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(num_sms & ~1));
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2; attr[0].val.clusterDim.y = 1; attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr; cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = num_sms / 2;
+        }
+        resident_pairs = n;
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    const int64_t k_bytes = FMT == 0 ? a.K : a.K / 2;
+    const int block = FMT == 0 ? 32 : 16;
+    // scale tensor sizes as the API defines them (grouped A: every group padded to 128-row bands)
+    const int64_t sa_bytes = GROUPED ? host_scale_bytes(a.M + 127 * a.G, a.K, block) : host_scale_bytes(a.M, a.K, block);
+    const int64_t sb_group_bytes = host_scale_bytes(a.N, a.K, block);
+    const int64_t sb_bytes = (GROUPED ? a.G : 1) * sb_group_bytes;
+    CUtensorMap tmA, tmB, tmSA, tmSB, tmD;
+    if (!make_map(&tmA, a.a, k_bytes, a.M, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&tmB, a.b, k_bytes, GROUPED ? a.G * a.N : a.N, 128)) return cudaErrorInvalidValue;
+    if (!make_sf_map(&tmSA, a.sa, sa_bytes, (uint32_t)C::SF_ATOMS_A)) return cudaErrorInvalidValue;
+    if (!make_sf_map(&tmSB, a.sb, sb_bytes, (uint32_t)C::SF_ATOMS_A)) return cudaErrorInvalidValue;
+    if (!make_out_map(&tmD, a.d, a.M, a.N, a.ldd, (uint32_t)C::EPI_COLS)) return cudaErrorInvalidValue;
+
+    Params p{};
+    p.sa = a.sa; p.sb = a.sb;
+    p.alpha_a = a.alpha_a; p.alpha_a_scope = a.alpha_a_scope;
+    p.alpha_b = a.alpha_b; p.alpha_b_scope = a.alpha_b_scope;
+    p.M = a.M; p.N = a.N; p.K = a.K; p.d = a.d; p.ldd = a.ldd;
+    p.G = a.G; p.group_offsets = a.group_offsets;
+    p.m_tiles = (a.M + 2 * BM - 1) / (2 * BM);        // pair rows (256)
+    p.n_tiles = (a.N + BN - 1) / BN;
+    p.k_stages = k_bytes / BKB;
+    p.nct = (a.K / block + 3) / 4;
+    p.sb_group_bytes = sb_group_bytes;
+    p.total_tiles = p.m_tiles * p.n_tiles;
+    const int64_t tiles_bound = GROUPED ? (p.m_tiles + a.G) * p.n_tiles : p.total_tiles;
+    // a persistent grid: only as many pairs as can be resident together (an odd SM left in a GPC
+    // cannot host half a cluster)
+    const int64_t pairs = max64(1, min64(tiles_bound, (int64_t)min(resident_pairs, num_sms / 2)));
+    bs_gemm_pair_kernel<FMT, GROUPED, COL_ALPHA><<<(unsigned)(2 * pairs), NUM_THREADS, C::SMEM_ALLOC, stream>>>(
+        tmA, tmB, tmSA, tmSB, tmD, p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
+#ifndef MXK_GEMM_PAIR
+#define MXK_GEMM_PAIR 1
+#endif
 cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream) {
     if (args.G > MAX_GROUPS) return cudaErrorInvalidValue;
     const bool col_alpha = args.G == 0 && args.alpha_b_scope == 2;   // per-output-column factor (dense only)
+#if MXK_GEMM_PAIR
+    if (args.fmt == 0) {
+        if (args.G > 0) return launch_pair_impl<0, true, false>(args, num_sms, stream);
+        return col_alpha ? launch_pair_impl<0, false, true>(args, num_sms, stream) : launch_pair_impl<0, false, false>(args, num_sms, stream);
+    }
+    if (args.G > 0) return launch_pair_impl<1, true, false>(args, num_sms, stream);
+    return col_alpha ? launch_pair_impl<1, false, true>(args, num_sms, stream) : launch_pair_impl<1, false, false>(args, num_sms, stream);
+#else
     if (args.fmt == 0) {
         if (args.G > 0) return launch_impl<0, true, false>(args, num_sms, stream);
         return col_alpha ? launch_impl<0, false, true>(args, num_sms, stream) : launch_impl<0, false, false>(args, num_sms, stream);
     }
     if (args.G > 0) return launch_impl<1, true, false>(args, num_sms, stream);
     return col_alpha ? launch_impl<1, false, true>(args, num_sms, stream) : launch_impl<1, false, false>(args, num_sms, stream);
+#endif
 }
 
 uint32_t read_and_clear_device_status() {

@@ -184,6 +184,7 @@ __device__ __forceinline__ uint32_t fold_halves(uint32_t m2) { return max(m2 & 0
 // the warp totals).  s_off needs G + 1 entries, s_ptile G + 1 entries, s_warp 32 entries.
 // ---------------------------------------------------------------------------------------------
 // Tile prefix only, reading the offsets through `off` (shared or global memory).
+template <int ROWS = 128>
 __device__ __forceinline__ void scan_group_tiles(const int64_t* off, int G, int* s_ptile, int* s_warp) {
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, wid = tid >> 5, nwarps = nthr >> 5;
     // thread tid owns groups [tid * per, tid * per + per)
@@ -191,7 +192,7 @@ __device__ __forceinline__ void scan_group_tiles(const int64_t* off, int G, int*
     int local = 0;
     for (int k = 0; k < per; ++k) {
         const int g = tid * per + k;
-        if (g < G) local += (int)((off[g + 1] - off[g] + 127) / 128);
+        if (g < G) local += (int)((off[g + 1] - off[g] + ROWS - 1) / ROWS);
     }
     int incl = local;
 #pragma unroll
@@ -216,7 +217,7 @@ __device__ __forceinline__ void scan_group_tiles(const int64_t* off, int G, int*
         const int g = tid * per + k;
         if (g < G) {
             s_ptile[g] = run;
-            run += (int)((off[g + 1] - off[g] + 127) / 128);
+            run += (int)((off[g + 1] - off[g] + ROWS - 1) / ROWS);
         }
         if (g == G - 1) s_ptile[G] = run;
     }
