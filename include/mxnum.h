@@ -195,8 +195,9 @@ mx_status mx_dequantize_bf16(mx_format fmt, const uint8_t* q, const uint8_t* s, 
  *   alpha_a: NULL / MX_SCOPE_NONE (1), one FP32 (MX_SCOPE_TENSOR) or M FP32 (MX_SCOPE_ROW); alpha_b
  *   likewise with N.  d [M, ldd] BF16.
  * FP32 accumulation inside the tensor core; the summation order is the hardware's.  Requires
- * K % 128 (MXFP8) or K % 256 (NVFP4) == 0; M, N >= 1; N % 8 == 0 and ldd % 8 == 0 (rows of d are
- * written in 16-byte groups), ldd >= N. */
+ * K % 128 (MXFP8) or K % 256 (NVFP4) == 0; M, N >= 1; N % 8 == 0 and ldd % 8 == 0 (d is written by
+ * TMA tensor stores, whose row pitch is a multiple of 16 bytes), ldd >= N; a, b, sa, sb, d 16-byte
+ * aligned.  Runs as persistent clusters of two CTAs (one per SM) on 256 x 256 output tiles. */
 mx_status mx_scaled_gemm(mx_format fmt,
                          const uint8_t* a, const uint8_t* sa, const float* alpha_a, mx_scope alpha_a_scope,
                          const uint8_t* b, const uint8_t* sb, const float* alpha_b, mx_scope alpha_b_scope,

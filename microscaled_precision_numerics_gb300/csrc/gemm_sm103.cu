@@ -8,22 +8,32 @@
 // with one E4M3 scale per 16 (scale_vec::4X); the FP32 second-level scales are applied in the
 // epilogue.
 //
-// Structure (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0        TMA producer: A/B tiles (128-byte swizzle) and scale atoms into a 4-stage ring
-//   warp 1        TMEM allocator; per stage one elected lane copies the stage's scale atoms to TMEM
-//                 (tcgen05.cp) and issues the stage's tcgen05.mma, which the tensor pipe runs in order
-//   warps 2..5    epilogue: tcgen05.ld the FP32 accumulator, scale, round to BF16, hand TMEM back,
-//                 then stage 32-row x (32 | 16)-column BF16 chunks in swizzled shared memory and
-//                 write them with TMA tensor stores (coalesced lines; the map clips ragged edges)
+// Structure: persistent clusters of two CTAs (one per SM) over 256 x 256 output tiles.  The even
+// CTA issues the pair MMA (tcgen05.mma.cta_group::2, M = 256): each CTA holds 128 rows of A and 128
+// of the 256 B rows in its shared memory and 128 accumulator rows in its TMEM, so each SM loads half
+// of the B tile.
+//   warp 0        (both CTAs) TMA producer: A rows, B half and scale atoms (128-byte swizzle for the
+//                 operands) into a 6-stage (MXFP8) / 5-stage (NVFP4) ring; the loads of both CTAs
+//                 signal the stage barrier in the even CTA
+//   warp 1        TMEM allocation for the pair; in the even CTA one elected lane copies each stage's
+//                 scale atoms into the TMEM of both CTAs (tcgen05.cp.cta_group::2: each CTA's own
+//                 atoms into its own TMEM) and issues the stage's MMAs, which the tensor pipe runs in
+//                 issue order; its commits arrive on the barriers of both CTAs
+//   warps 2..5    (both CTAs) epilogue: tcgen05.ld the FP32 accumulator, scale, round to BF16, hand
+//                 TMEM back (arriving in the even CTA), then stage 32-row x (32 | 16)-column BF16
+//                 chunks in swizzled shared memory and write them with TMA tensor stores (coalesced
+//                 lines; the map clips ragged edges)
 // The producer and MMA warps run their loops warp-wide and issue through elect.sync: issuing the
 // asynchronous tensor ops from a converged warp is several times cheaper per op than from a single
 // diverged lane.
-// Scales arrive in the GEMM layout (512-byte atoms of 128 rows x 4 scale columns) and each stage's
-// atoms are bulk-copied to shared memory, then to TMEM with tcgen05.cp.32x128b.warpx4.  For the
-// grouped GEMM the A scales are in the grouped layout, where every expert group starts on a
-// 128-row band, so a tile at an arbitrary row offset still reads whole atoms.
+// Scales arrive in the GEMM layout (512-byte atoms of 128 rows x 4 scale columns).  Every CTA loads
+// the atoms of its own 128 A rows and of all 256 B rows, because each CTA's tensor core reads the A
+// scales of its rows and the B scales of every column from its own TMEM.  The scale tensors are
+// read through TMA maps, so atoms past the end of a tensor (the upper half of a pair tile past M)
+// arrive as zeros.  For the grouped GEMM the A scales are in the grouped layout, where every expert
+// group starts on a 128-row band, so a tile at an arbitrary row offset still reads whole atoms.
 // Every mbarrier wait is bounded: on expiry the CTA records MX_ERR_TIMEOUT in a device word, stops
-// issuing work, drains what it issued and frees its TMEM.
+// issuing work and lets its in-flight copies land before the pair leaves and frees its TMEM.
 #include "../../include/mxnum.h"
 #include "mx_internal.h"
 
@@ -37,49 +47,14 @@ __device__ unsigned int g_mx_device_status = 0;
 
 namespace {
 
-constexpr int BM = 128;
+constexpr int BM = 128;                   // rows per CTA (256 per pair)
 constexpr int BN = 256;
 constexpr int BKB = 128;                  // K bytes per pipeline stage
-#ifndef MXK_GEMM_STAGES
-#define MXK_GEMM_STAGES 4
-#endif
-constexpr int STAGES = MXK_GEMM_STAGES;     // depth of the shared-memory operand ring
 constexpr int NUM_THREADS = 192;         // producer, MMA, 4 epilogue warps
-constexpr int A_STAGE_BYTES = BM * BKB;   // 16 KB
-constexpr int B_STAGE_BYTES = BN * BKB;   // 32 KB
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_SF_BASE = 256;         // accumulator uses columns [0, 256)
 constexpr int MAX_GROUPS = MX_MAX_GROUPS;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
-
-template <int FMT, bool GROUPED>
-struct Cfg {
-    // NVFP4 grouped keeps one stage fewer: its group table and the epilogue staging must fit too
-    static constexpr int NST = (FMT == 1 && GROUPED) ? STAGES - 1 : STAGES;
-    static constexpr int SF_ATOMS_A = FMT == 0 ? 1 : 4;   // 512-byte atoms per stage (A side)
-    static constexpr int SFA_BYTES = 512 * SF_ATOMS_A;
-    static constexpr int SFB_BYTES = 2 * SFA_BYTES;        // two 128-row halves of the 256-row B tile
-    static constexpr int SFA_COLS = 4 * SF_ATOMS_A;        // TMEM columns per stage
-    static constexpr int SFB_COLS = 2 * SFA_COLS;
-    // epilogue chunk: 32 rows x EPI_COLS BF16 columns per warp, double-buffered, swizzled rows of
-    // 64 bytes (MXFP8) or 32 bytes (NVFP4, whose larger scale stages leave less shared memory)
-    static constexpr int EPI_COLS = FMT == 0 ? 32 : 16;
-    static constexpr int EPI_ROW_BYTES = 2 * EPI_COLS;
-    static constexpr int EPI_BUF_BYTES = 32 * EPI_ROW_BYTES;
-    static constexpr int SMEM_A = 0;
-    static constexpr int SMEM_B = SMEM_A + NST * A_STAGE_BYTES;
-    static constexpr int SMEM_SFA = SMEM_B + NST * B_STAGE_BYTES;
-    static constexpr int SMEM_SFB = SMEM_SFA + NST * SFA_BYTES;
-    static constexpr int SMEM_EPI = SMEM_SFB + NST * SFB_BYTES;      // 1024-aligned (all above are)
-    static constexpr int SMEM_BAR = SMEM_EPI + 4 * 2 * EPI_BUF_BYTES;
-    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 3);
-    static constexpr int SMEM_PREFIX = SMEM_MISC + 16;
-    static constexpr int SMEM_WARP = SMEM_PREFIX + (GROUPED ? 4 * (MAX_GROUPS + 1) : 0);
-    static constexpr int SMEM_TOTAL = SMEM_WARP + (GROUPED ? 4 * 32 : 0);
-    static constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;  // slack for 1024-byte alignment
-    static_assert(TMEM_SF_BASE + NST * (SFA_COLS + SFB_COLS) <= TMEM_COLS, "TMEM budget");
-    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
-};
 
 struct Params {
     const uint8_t* sa; const uint8_t* sb;
@@ -149,10 +124,6 @@ __device__ __forceinline__ bool elect_one() {
     return p != 0;
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1, uint32_t bar) {
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-                 :: "r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar) : "memory");
-}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -184,20 +155,10 @@ __device__ __forceinline__ void cluster_sync_all() {
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
-}
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
-}
 
 // Pair (cta_group::2) forms: issued by the even CTA of the pair, act on both CTAs' shared memory and
 // TMEM at the same addresses; commits arrive on the barrier at the same offset in every CTA of `mask`.
@@ -222,19 +183,6 @@ __device__ __forceinline__ void tc2_mma(uint32_t d, uint64_t adesc, uint64_t bde
     }
 }
 
-template <int FMT>
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
-                                       uint32_t sfb, uint32_t acc) {
-    if (FMT == 0) {
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-                     :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
-    } else {
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-                     :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
-    }
-}
 
 // Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 bytes, 8-row groups
 // 1024 bytes apart (stride byte offset), descriptor version 1 (bits 46..48), swizzle mode 2.
@@ -277,45 +225,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
 // ---------------------------------------------------------------------------------------------
 // Tile schedule (identical in every role)
 // ---------------------------------------------------------------------------------------------
-struct Tile {
-    int64_t row0, row_end;   // A rows [row0, row0 + 128) of which [row0, row_end) are real
-    int64_t n0;              // first output column
-    int64_t g;               // group (grouped GEMM) or 0
-    int64_t sf_tile;         // 128-row band of A's scale layout holding this tile's scales
-};
-
-// Dense: bands of 16 M-tiles; inside a band N-tiles advance every 16 tiles (L2 reuse of A and B).
-__device__ __forceinline__ Tile dense_tile(const Params& p, int64_t t) {
-    constexpr int64_t GM = 16;
-    const int64_t band_tiles = GM * p.n_tiles;
-    const int64_t band = t / band_tiles, in = t % band_tiles;
-    const int64_t band_m = min64(GM, p.m_tiles - band * GM);
-    const int64_t mt = band * GM + in % band_m, nt = in / band_m;
-    Tile r;
-    r.row0 = mt * BM; r.row_end = p.M; r.n0 = nt * BN; r.g = 0; r.sf_tile = mt;
-    return r;
-}
-
-// Grouped: ptile[g] = M-tiles of groups < g (also group g's first 128-row band in the grouped scale
-// layout); output tiles of group g are [ptile[g] * n_tiles, ptile[g + 1] * n_tiles).
-__device__ __forceinline__ Tile grouped_tile(const Params& p, const int* ptile, int64_t t) {
-    const int64_t mt_global = t / p.n_tiles;      // tiles are ordered group by group, M-tile major
-    int lo = 0, hi = (int)p.G;                    // ptile[g] <= mt_global < ptile[g + 1]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (ptile[mid] <= mt_global) lo = mid; else hi = mid;
-    }
-    const int64_t g = lo;
-    const int64_t mt = mt_global - ptile[g];
-    Tile r;
-    r.row0 = __ldg(p.group_offsets + g) + mt * BM;
-    r.row_end = __ldg(p.group_offsets + g + 1);
-    r.n0 = (t % p.n_tiles) * BN;
-    r.g = g;
-    r.sf_tile = mt_global;
-    return r;
-}
-
 // One output tile slice of an epilogue warp: drain the warp's 32 TMEM lanes (256 FP32 columns) into
 // packed BF16 registers with the second-level scales applied, hand TMEM back (arrive on tempty_bar,
 // in this CTA or, for the pair kernel, in the leader CTA), then store the rows [row0 + 32 q, +32) that
@@ -405,185 +314,6 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
         }
     }
 }
-
-// ---------------------------------------------------------------------------------------------
-// The kernel
-// ---------------------------------------------------------------------------------------------
-template <int FMT, bool GROUPED, bool COL_ALPHA>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmD, const Params p) {
-    using C = Cfg<FMT, GROUPED>;
-    constexpr int NST = C::NST;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase + C::SMEM_BAR;                 // NST barriers
-    const uint32_t bar_empty = bar_full + 8 * NST;              // NST barriers
-    const uint32_t bar_tfull = bar_empty + 8 * NST;
-    const uint32_t bar_tempty = bar_tfull + 8;
-    const uint32_t bar_done = bar_tempty + 8;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
-    int* ptile = reinterpret_cast<int*>(smem + C::SMEM_PREFIX);
-    int* s_warp = reinterpret_cast<int*>(smem + C::SMEM_WARP);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NST; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
-        }
-        mbar_init(bar_tfull, 1);
-        mbar_init(bar_tempty, 4);
-        mbar_init(bar_done, 1);
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 0 && lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmA) : "memory");
-        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmB) : "memory");
-        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmD) : "memory");
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    int64_t total_tiles;
-    if (GROUPED) scan_group_tiles(p.group_offsets, (int)p.G, ptile, s_warp);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    total_tiles = GROUPED ? (int64_t)ptile[p.G] * p.n_tiles : p.total_tiles;
-
-    if (warp == 0) {
-        // ------------------------------- producer -------------------------------
-        int stage = 0;
-        uint32_t phase = 0;
-        int issued_parity[NST];
-        for (int s = 0; s < NST; ++s) issued_parity[s] = -1;
-        bool ok = true;
-        for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-            const Tile tile = GROUPED ? grouped_tile(p, ptile, t) : dense_tile(p, t);
-            const int64_t brow = (GROUPED ? tile.g * p.N : 0) + tile.n0;
-            const uint8_t* sb_g = p.sb + (GROUPED ? tile.g * p.sb_group_bytes : 0);
-            const int64_t bt0 = tile.n0 / 128;                      // first 128-row band of B
-            const bool b_hi = tile.n0 + 128 < p.N;                  // does the second band exist?
-            for (int64_t ks = 0; ks < p.k_stages; ++ks) {
-                if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
-                const uint32_t sA = sbase + C::SMEM_A + stage * A_STAGE_BYTES;
-                const uint32_t sB = sbase + C::SMEM_B + stage * B_STAGE_BYTES;
-                const uint32_t sSFA = sbase + C::SMEM_SFA + stage * C::SFA_BYTES;
-                const uint32_t sSFB = sbase + C::SMEM_SFB + stage * C::SFB_BYTES;
-                const int64_t ct0 = ks * C::SF_ATOMS_A;             // first 4-column scale tile of this stage
-                if (elect_one()) {
-                    const uint32_t bytes = A_STAGE_BYTES + B_STAGE_BYTES + C::SFA_BYTES + C::SFB_BYTES / (b_hi ? 1 : 2);
-                    mbar_arrive_expect_tx(bar_full + 8 * stage, bytes);
-                    const int32_t kb = (int32_t)(ks * BKB);
-                    tma_load_2d(sA, &tmA, kb, (int32_t)tile.row0, bar_full + 8 * stage);
-                    tma_load_2d(sB, &tmB, kb, (int32_t)brow, bar_full + 8 * stage);
-                    bulk_load(sSFA, p.sa + ((tile.sf_tile * p.nct + ct0) << 9), C::SFA_BYTES, bar_full + 8 * stage);
-                    bulk_load(sSFB, sb_g + ((bt0 * p.nct + ct0) << 9), C::SFA_BYTES, bar_full + 8 * stage);
-                    if (b_hi)
-                        bulk_load(sSFB + C::SFA_BYTES, sb_g + (((bt0 + 1) * p.nct + ct0) << 9), C::SFA_BYTES,
-                                  bar_full + 8 * stage);
-                }
-                __syncwarp();
-                issued_parity[stage] = (int)phase;
-                if (++stage == NST) { stage = 0; phase ^= 1; }
-            }
-        }
-        if (!ok && lane == 0) {
-            // drain: wait (bounded) for every load this warp issued to land before the CTA exits
-            for (int s = 0; s < NST; ++s)
-                if (issued_parity[s] >= 0) {
-                    const unsigned long long t0 = globaltimer();
-                    while (!mbar_try_wait(bar_full + 8 * s, (uint32_t)issued_parity[s]) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
-                }
-        }
-    } else if (warp == 1) {
-        // ------------------------------- scale copies + MMA issuer -------------------------------
-        // Per stage: copy the A and B scale atoms into the stage's TMEM scale slot, then the MMAs that
-        // read them; the tensor pipe executes one thread's tcgen05.cp and tcgen05.mma in issue order,
-        // and a slot is rewritten only after the MMAs of its previous use were issued.
-        int stage = 0;
-        uint32_t phase = 0, acc_phase = 0;
-        bool ok = true, issued_any = false;
-        for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-            if (!warp_wait(bar_tempty, acc_phase ^ 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            for (int64_t ks = 0; ks < p.k_stages; ++ks) {
-                if (!warp_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                if (elect_one()) {
-                    const uint32_t sA = sbase + C::SMEM_A + stage * A_STAGE_BYTES;
-                    const uint32_t sB = sbase + C::SMEM_B + stage * B_STAGE_BYTES;
-                    const uint32_t sSFA = sbase + C::SMEM_SFA + stage * C::SFA_BYTES;
-                    const uint32_t sSFB = sbase + C::SMEM_SFB + stage * C::SFB_BYTES;
-                    const uint32_t tSFA = tmem + TMEM_SF_BASE + stage * (C::SFA_COLS + C::SFB_COLS);
-                    const uint32_t tSFB = tSFA + C::SFA_COLS;
-                    // A atom j to columns 4j..4j+3; B band h, atom j to 8j + 4h
-#pragma unroll
-                    for (int j = 0; j < C::SF_ATOMS_A; ++j) {
-                        tc_cp_sf(tSFA + 4 * j, desc_sf(sSFA + 512 * j));
-                        tc_cp_sf(tSFB + 8 * j, desc_sf(sSFB + 512 * j));
-                        tc_cp_sf(tSFB + 8 * j + 4, desc_sf(sSFB + C::SFA_BYTES + 512 * j));
-                    }
-#pragma unroll
-                    for (int j = 0; j < BKB / 32; ++j) {
-                        // MXFP8: one atom covers the 4 MMAs of the stage, the scale id picks the byte;
-                        // NVFP4: each MMA (K = 64) consumes a whole atom word
-                        const uint32_t sf_id = FMT == 0 ? (uint32_t)j : 0u;
-                        const uint32_t col = FMT == 0 ? 0u : (uint32_t)j;
-                        tc_mma<FMT>(tmem, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j), make_idesc<FMT>(sf_id),
-                                    tSFA + 4 * col, tSFB + 8 * col, (ks > 0 || j > 0) ? 1u : 0u);
-                    }
-                    tc_commit(bar_empty + 8 * stage);
-                }
-                __syncwarp();
-                issued_any = true;
-                if (++stage == NST) { stage = 0; phase ^= 1; }
-            }
-            if (!ok) break;
-            if (elect_one()) tc_commit(bar_tfull);
-            __syncwarp();
-            acc_phase ^= 1;
-        }
-        if (issued_any) {
-            // every tcgen05 op this warp issued has completed once bar_done flips
-            if (elect_one()) {
-                tc_commit(bar_done);
-                const unsigned long long t0 = globaltimer();
-                while (!mbar_try_wait(bar_done, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
-            }
-            __syncwarp();
-        }
-    } else {
-        // ------------------------------- epilogue -------------------------------
-        const int q = warp & 3;                     // TMEM lane quadrant this warp may access
-        uint32_t acc_phase = 0, epi_chunk = 0;
-        for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-            const Tile tile = GROUPED ? grouped_tile(p, ptile, t) : dense_tile(p, t);
-            if (!mbar_wait(bar_tfull, acc_phase, abort_flag)) break;
-            tc_fence_after();
-            epilogue_tile<FMT, GROUPED, COL_ALPHA, C::EPI_COLS, C::EPI_BUF_BYTES, false>(
-                p, &tmD, tmem, q, lane, tile.row0, tile.row_end, tile.n0, tile.g,
-                sbase + C::SMEM_EPI + (uint32_t)(q * 2 * C::EPI_BUF_BYTES), epi_chunk, bar_tempty);
-            acc_phase ^= 1;
-        }
-        if (lane == 0) bulk_wait_group_all();     // staging buffers read and stores complete before exit
-        __syncwarp();
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
-}
-
 
 // ---------------------------------------------------------------------------------------------
 // CTA-pair kernel: 256 x 256 output tiles, each computed by the two CTAs of a cluster with the
@@ -891,44 +621,6 @@ bool make_out_map(CUtensorMap* map, uint16_t* d, int64_t rows, int64_t N, int64_
     return r == CUDA_SUCCESS;
 }
 
-template <int FMT, bool GROUPED, bool COL_ALPHA>
-cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
-    using C = Cfg<FMT, GROUPED>;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(bs_gemm_kernel<FMT, GROUPED, COL_ALPHA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        C::SMEM_ALLOC);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
-
-    const int64_t k_bytes = FMT == 0 ? a.K : a.K / 2;
-    const int block = FMT == 0 ? 32 : 16;
-    CUtensorMap tmA, tmB;
-    if (!make_map(&tmA, a.a, k_bytes, a.M, BM)) return cudaErrorInvalidValue;
-    if (!make_map(&tmB, a.b, k_bytes, GROUPED ? a.G * a.N : a.N, BN)) return cudaErrorInvalidValue;
-    CUtensorMap tmD;
-    if (!make_out_map(&tmD, a.d, a.M, a.N, a.ldd, (uint32_t)C::EPI_COLS)) return cudaErrorInvalidValue;
-
-    Params p{};
-    p.sa = a.sa; p.sb = a.sb;
-    p.alpha_a = a.alpha_a; p.alpha_a_scope = a.alpha_a_scope;
-    p.alpha_b = a.alpha_b; p.alpha_b_scope = a.alpha_b_scope;
-    p.M = a.M; p.N = a.N; p.K = a.K; p.d = a.d; p.ldd = a.ldd;
-    p.G = a.G; p.group_offsets = a.group_offsets;
-    p.m_tiles = (a.M + BM - 1) / BM;
-    p.n_tiles = (a.N + BN - 1) / BN;
-    p.k_stages = k_bytes / BKB;
-    p.nct = (a.K / block + 3) / 4;
-    p.sb_group_bytes = host_scale_bytes(a.N, a.K, block);
-    p.total_tiles = p.m_tiles * p.n_tiles;
-    int64_t tiles_bound = GROUPED ? (p.m_tiles + a.G) * p.n_tiles : p.total_tiles;
-    const unsigned grid = (unsigned)max64(1, min64(tiles_bound, num_sms));
-    bs_gemm_kernel<FMT, GROUPED, COL_ALPHA><<<grid, NUM_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmB, tmD, p);
-    return cudaGetLastError();
-}
-
-
 // Scale tensor viewed as rows of 256 bytes (two rows per 512-byte atom), box of `atoms` atoms.
 bool make_sf_map(CUtensorMap* map, const uint8_t* base, int64_t bytes, uint32_t atoms) {
     auto fn = encode_fn();
@@ -1006,27 +698,15 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
 
 }  // namespace
 
-#ifndef MXK_GEMM_PAIR
-#define MXK_GEMM_PAIR 1
-#endif
 cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream) {
     if (args.G > MAX_GROUPS) return cudaErrorInvalidValue;
     const bool col_alpha = args.G == 0 && args.alpha_b_scope == 2;   // per-output-column factor (dense only)
-#if MXK_GEMM_PAIR
     if (args.fmt == 0) {
         if (args.G > 0) return launch_pair_impl<0, true, false>(args, num_sms, stream);
         return col_alpha ? launch_pair_impl<0, false, true>(args, num_sms, stream) : launch_pair_impl<0, false, false>(args, num_sms, stream);
     }
     if (args.G > 0) return launch_pair_impl<1, true, false>(args, num_sms, stream);
     return col_alpha ? launch_pair_impl<1, false, true>(args, num_sms, stream) : launch_pair_impl<1, false, false>(args, num_sms, stream);
-#else
-    if (args.fmt == 0) {
-        if (args.G > 0) return launch_impl<0, true, false>(args, num_sms, stream);
-        return col_alpha ? launch_impl<0, false, true>(args, num_sms, stream) : launch_impl<0, false, false>(args, num_sms, stream);
-    }
-    if (args.G > 0) return launch_impl<1, true, false>(args, num_sms, stream);
-    return col_alpha ? launch_impl<1, false, true>(args, num_sms, stream) : launch_impl<1, false, false>(args, num_sms, stream);
-#endif
 }
 
 uint32_t read_and_clear_device_status() {
