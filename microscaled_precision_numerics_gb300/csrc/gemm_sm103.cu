@@ -19,10 +19,11 @@
 //                 scale atoms into the TMEM of both CTAs (tcgen05.cp.cta_group::2: each CTA's own
 //                 atoms into its own TMEM) and issues the stage's MMAs, which the tensor pipe runs in
 //                 issue order; its commits arrive on the barriers of both CTAs
-//   warps 2..5    (both CTAs) epilogue: tcgen05.ld the FP32 accumulator, scale, round to BF16, hand
-//                 TMEM back (arriving in the even CTA), then stage 32-row x (32 | 16)-column BF16
-//                 chunks in swizzled shared memory and write them with TMA tensor stores (coalesced
-//                 lines; the map clips ragged edges)
+//   warps 2..9    (both CTAs) epilogue, two warps per TMEM lane quadrant (one per column half):
+//                 load the row's FP32 scales before the accumulator is ready, tcgen05.ld the
+//                 accumulator, scale, round to BF16, hand TMEM back (arriving in the even CTA), then
+//                 stage 32-row x 16-column BF16 chunks in swizzled shared memory and write them with
+//                 TMA tensor stores (the map clips ragged edges)
 // The producer and MMA warps run their loops warp-wide and issue through elect.sync: issuing the
 // asynchronous tensor ops from a converged warp is several times cheaper per op than from a single
 // diverged lane.
@@ -48,11 +49,9 @@ __device__ unsigned int g_mx_device_status = 0;
 namespace {
 
 constexpr int BM = 128;                   // rows per CTA (256 per pair)
-constexpr int BN = 256;
 constexpr int BKB = 128;                  // K bytes per pipeline stage
-constexpr int NUM_THREADS = 192;         // producer, MMA, 4 epilogue warps
+constexpr int NUM_THREADS = 320;         // producer, MMA, 8 epilogue warps
 constexpr int TMEM_COLS = 512;
-constexpr int TMEM_SF_BASE = 256;         // accumulator uses columns [0, 256)
 constexpr int MAX_GROUPS = MX_MAX_GROUPS;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
 
@@ -79,9 +78,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -199,11 +195,11 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
 // Instruction descriptor for the block-scaled kinds: B scale id (bits 4-5), A/B formats (7-9,
 // 10-12), K-major A and B, N >> 3 (17-22), scale type (23: 1 = UE8M0, 0 = UE4M3), M >> 4 (24-28),
 // A scale id (29-30).
-template <int FMT, int MMA_M = BM>
+template <int FMT, int MMA_M, int MMA_N>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
     const uint32_t fmt = FMT == 0 ? 0u : 1u;          // E4M3 (mxf8f6f4) / E2M1 (mxf4nvf4)
     const uint32_t scale_type = FMT == 0 ? 1u : 0u;
-    return (sf_id << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(BN >> 3) << 17) | (scale_type << 23) |
+    return (sf_id << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(MMA_N >> 3) << 17) | (scale_type << 23) |
            ((uint32_t)(MMA_M >> 4) << 24) | (sf_id << 29);
 }
 
@@ -225,36 +221,42 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
 // ---------------------------------------------------------------------------------------------
 // Tile schedule (identical in every role)
 // ---------------------------------------------------------------------------------------------
-// One output tile slice of an epilogue warp: drain the warp's 32 TMEM lanes (256 FP32 columns) into
-// packed BF16 registers with the second-level scales applied, hand TMEM back (arrive on tempty_bar,
-// in this CTA or, for the pair kernel, in the leader CTA), then store the rows [row0 + 32 q, +32) that
-// belong to the tile: TMA stores from the warp's two staging buffers at ebase, or plain 16-byte
-// stores for a slice that straddles the end of an expert group.
-template <int FMT, bool GROUPED, bool COL_ALPHA, int EPI_COLS, int EPI_BUF_BYTES, bool REMOTE_ARRIVE>
-__device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap* tmD, uint32_t tmem, int q, int lane,
-                                              int64_t row0, int64_t row_end, int64_t n0, int64_t g, uint32_t ebase,
-                                              uint32_t& epi_chunk, uint32_t tempty_bar) {
-    constexpr int EPI_ROW_BYTES = 2 * EPI_COLS;
-    const int64_t row = row0 + q * 32 + lane;
-    const bool row_ok = row < row_end;
-    float aa = 1.0f;
+// Epilogue geometry: 8 warps, two per TMEM lane quadrant; warp (q, h) owns rows [32 q, 32 q + 32) of
+// the CTA's 128 and columns [TN/2 h, TN/2 (h + 1)) of the tile.  Stores go out in 32-row x 16-column
+// chunks (32-byte rows, 32-byte swizzle) through two 1 KB staging buffers per warp.
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_COLS = 16;
+constexpr int EPI_BUF_BYTES = 32 * 2 * EPI_COLS;
+
+// Second-level scales of this thread's row (loaded before the accumulator is ready).
+template <bool GROUPED>
+__device__ __forceinline__ void epilogue_alphas(const Params& p, int64_t row, bool row_ok, int64_t g, float& aa,
+                                                float& ab_g) {
+    aa = 1.0f;
     if (p.alpha_a_scope == 1) aa = __ldg(p.alpha_a);
     else if (p.alpha_a_scope == 2 && row_ok) aa = __ldg(p.alpha_a + row);
-    float ab_g = 1.0f;
+    ab_g = 1.0f;
     if (GROUPED && p.alpha_b_scope != 0) ab_g = __ldg(p.alpha_b + g);
     else if (!GROUPED && p.alpha_b_scope == 1) ab_g = __ldg(p.alpha_b);
-    // drain the accumulator slice (this thread's row, 256 columns) into packed BF16 registers,
-    // then hand TMEM back to the MMA warp before the stores
-    uint32_t packed[BN / 2];
+}
+
+// Drain of one tile by an epilogue warp: its 32 TMEM lanes x TN/2 FP32 columns (accumulator at tacc)
+// into packed BF16 registers with the second-level scales applied; then TMEM is handed back
+// (arrive on tempty_bar, in the leader CTA).
+template <int TN, bool COL_ALPHA>
+__device__ __forceinline__ void epilogue_drain(const Params& p, uint32_t tacc, int q, int h, int lane, int64_t n0,
+                                               float aa, float ab_g, uint32_t tempty_bar, uint32_t (&packed)[TN / 4]) {
+    constexpr int EPI_HALF = TN / 2;                // columns per epilogue warp
+    const int64_t nh = n0 + h * EPI_HALF;           // first column of this warp's half
 #pragma unroll
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = 0; c < EPI_HALF / 32; ++c) {
         float v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
+        tmem_ld32(tacc + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * EPI_HALF + c * 32), v);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             float f0 = __fmul_rn(v[2 * i], aa), f1 = __fmul_rn(v[2 * i + 1], aa);
             if (COL_ALPHA) {
-                const int64_t n = n0 + c * 32 + 2 * i;
+                const int64_t n = nh + c * 32 + 2 * i;
                 f0 = __fmul_rn(f0, n < p.N ? __ldg(p.alpha_b + n) : 0.0f);
                 f1 = __fmul_rn(f1, n + 1 < p.N ? __ldg(p.alpha_b + n + 1) : 0.0f);
             } else {
@@ -266,92 +268,107 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) {
-        if (REMOTE_ARRIVE) mbar_arrive_cluster(tempty_bar); else mbar_arrive(tempty_bar);
-    }
+    if (lane == 0) mbar_arrive_cluster(tempty_bar);
+}
+
+// Stores of one drained tile slice: rows [row0 + 32 q, +32) that belong to the tile, columns of the
+// warp's half.  TMA stores from the warp's two staging buffers at ebase, or plain 16-byte stores for
+// a slice that straddles the end of an expert group.
+template <int TN, bool GROUPED>
+__device__ __forceinline__ void epilogue_store(const Params& p, const CUtensorMap* tmD, int q, int h, int lane,
+                                               int64_t row0, int64_t row_end, int64_t n0, uint32_t ebase,
+                                               uint32_t& epi_chunk, const uint32_t (&packed)[TN / 4]) {
+    constexpr int EPI_HALF = TN / 2;
+    const int64_t row = row0 + q * 32 + lane;
+    const bool row_ok = row < row_end;
+    const int64_t nh = n0 + h * EPI_HALF;
     const int64_t wrow0 = row0 + q * 32;              // first row of this warp's slice
-    if (wrow0 < row_end) {
-        if (!GROUPED || wrow0 + 32 <= row_end) {
-            // TMA stores; the tensor map clips rows >= M and columns >= N
-            const uint32_t rbase_off = (uint32_t)(lane * EPI_ROW_BYTES);
+    if (wrow0 >= row_end) return;
+    if (!GROUPED || wrow0 + 32 <= row_end) {
+        // TMA stores; the tensor map clips rows >= M and columns >= N
+        const uint32_t rbase_off = (uint32_t)(lane * 2 * EPI_COLS);
 #pragma unroll
-            for (int c = 0; c < BN / EPI_COLS; ++c) {
-                const int64_t col0 = n0 + c * EPI_COLS;
-                if (col0 < p.N) {
-                    const uint32_t buf = ebase + (epi_chunk & 1u) * (uint32_t)EPI_BUF_BYTES;
-                    ++epi_chunk;
-                    // the store issued from this buffer two chunks ago must have read it
-                    if (lane == 0) bulk_wait_group_read1();
-                    __syncwarp();
+        for (int c = 0; c < EPI_HALF / EPI_COLS; ++c) {
+            const int64_t col0 = nh + c * EPI_COLS;
+            if (col0 < p.N) {
+                const uint32_t buf = ebase + (epi_chunk & 1u) * (uint32_t)EPI_BUF_BYTES;
+                ++epi_chunk;
+                // the store issued from this buffer two chunks ago must have read it
+                if (lane == 0) bulk_wait_group_read1();
+                __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < EPI_COLS / 8; ++j) {
-                        // 16-byte piece j of this row at its position under the 64-byte (32-column
-                        // chunk) or 32-byte (16-column chunk) swizzle of the output map
-                        const uint32_t phys = EPI_COLS == 32 ? ((uint32_t)j ^ ((uint32_t)(lane >> 1) & 3u))
-                                                             : ((uint32_t)j ^ ((uint32_t)(lane >> 2) & 1u));
-                        const int pk = c * (EPI_COLS / 2) + 4 * j;
-                        st_shared_v4(buf + rbase_off + 16u * phys, packed[pk], packed[pk + 1], packed[pk + 2],
-                                     packed[pk + 3]);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(tmD, (int32_t)col0, (int32_t)wrow0, buf);
-                        bulk_commit_group();
-                    }
+                for (int j = 0; j < 2; ++j) {
+                    // 16-byte piece j of this row at its position under the 32-byte swizzle
+                    const uint32_t phys = (uint32_t)j ^ ((uint32_t)(lane >> 2) & 1u);
+                    const int pk = c * (EPI_COLS / 2) + 4 * j;
+                    st_shared_v4(buf + rbase_off + 16u * phys, packed[pk], packed[pk + 1], packed[pk + 2], packed[pk + 3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tmD, (int32_t)col0, (int32_t)wrow0, buf);
+                    bulk_commit_group();
                 }
             }
-        } else if (row_ok) {
-            // the slice straddles the end of the expert group: the next group's rows belong to
-            // another tile, so store this group's rows only (16-byte stores, N and ldd % 8 == 0)
-            uint16_t* drow = p.d + row * p.ldd;
+        }
+    } else if (row_ok) {
+        // the slice straddles the end of the expert group: the next group's rows belong to another
+        // tile, so store this group's rows only (16-byte stores, N and ldd % 8 == 0)
+        uint16_t* drow = p.d + row * p.ldd;
 #pragma unroll
-            for (int g8 = 0; g8 < BN / 8; ++g8) {
-                if (n0 + g8 * 8 < p.N)
-                    *reinterpret_cast<uint4*>(drow + n0 + g8 * 8) =
-                        make_uint4(packed[4 * g8], packed[4 * g8 + 1], packed[4 * g8 + 2], packed[4 * g8 + 3]);
-            }
+        for (int g8 = 0; g8 < EPI_HALF / 8; ++g8) {
+            if (nh + g8 * 8 < p.N)
+                *reinterpret_cast<uint4*>(drow + nh + g8 * 8) =
+                    make_uint4(packed[4 * g8], packed[4 * g8 + 1], packed[4 * g8 + 2], packed[4 * g8 + 3]);
         }
     }
 }
 
 // ---------------------------------------------------------------------------------------------
-// CTA-pair kernel: 256 x 256 output tiles, each computed by the two CTAs of a cluster with the
+// CTA-pair kernel: 256 x TN output tiles, each computed by the two CTAs of a cluster with the
 // cta_group::2 MMA (M = 256, 128 rows in each CTA's TMEM; B split by N halves between the two CTAs'
-// shared memory).  Each SM loads half of the B tile, so a stage carries 2/3 of the single-CTA bytes
+// shared memory).  Each SM loads half of the B tile, so a stage carries less than a single-CTA tile
 // for the same MMA work, and the ring holds more stages.
+//   TN = 256: one accumulator (256 TMEM columns); long-K dense GEMMs, where the tile-boundary
+//             drain is a small share of a tile
+//   TN = 128: two accumulators (2 x 128 columns): the epilogue of tile i overlaps the MMAs of tile
+//             i + 1; short-K grouped GEMMs, where a tile is only a few stages long
 //   both CTAs  warp 0: TMA loads of this CTA's A rows, B half and scale atoms (the B scales of all
-//              256 columns, which each CTA's tensor core reads from its own TMEM); every load
+//              TN columns, which each CTA's tensor core reads from its own TMEM); every load
 //              signals the stage barrier in the even (leader) CTA
 //   leader     warp 1: tcgen05.cp (each CTA's atoms into its own TMEM) and tcgen05.mma for the pair;
 //              commits arrive on the barriers of both CTAs
-//   both CTAs  warps 2..5: epilogue of this CTA's 128 rows; TMEM release arrives in the leader
+//   both CTAs  warps 2..9: epilogue of this CTA's 128 rows; TMEM release arrives in the leader
 // ---------------------------------------------------------------------------------------------
-template <int FMT, bool GROUPED>
+template <int FMT, bool GROUPED, int TN>
 struct PairCfg {
-    static constexpr int NST = FMT == 0 ? 6 : 5;
+    static_assert(TN == 128 || TN == 256, "tile width");
+    static constexpr int ACC = TN == 128 ? 2 : 1;          // accumulator buffers
+    // ring depth within the shared-memory budget (the grouped tables take 16.5 KB)
+    static constexpr int NST = FMT == 0 ? (TN == 256 ? (GROUPED ? 5 : 6) : (GROUPED ? 6 : 8))
+                                        : (TN == 256 ? 5 : (GROUPED ? 6 : 7));
     static constexpr int SF_ATOMS_A = FMT == 0 ? 1 : 4;
+    static constexpr int SFB_BANDS = TN / 128;
     static constexpr int SFA_BYTES = 512 * SF_ATOMS_A;     // this CTA's 128 rows
-    static constexpr int SFB_BYTES = 2 * SFA_BYTES;        // all 256 columns
+    static constexpr int SFB_BYTES = SFB_BANDS * SFA_BYTES; // all TN columns
     static constexpr int SFA_COLS = 4 * SF_ATOMS_A;
-    static constexpr int SFB_COLS = 2 * SFA_COLS;
+    static constexpr int SFB_COLS = SFB_BANDS * SFA_COLS;
+    static constexpr int TMEM_SF = ACC * TN;                // scale slots after the accumulators
     static constexpr int A_BYTES = 128 * BKB;
-    static constexpr int B_BYTES = 128 * BKB;
+    static constexpr int B_BYTES = (TN / 2) * BKB;
     static constexpr uint32_t STAGE_TX = 2u * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES);   // both CTAs
-    static constexpr int EPI_COLS = FMT == 0 ? 32 : 16;
-    static constexpr int EPI_BUF_BYTES = 32 * 2 * EPI_COLS;
     static constexpr int SMEM_A = 0;
     static constexpr int SMEM_B = SMEM_A + NST * A_BYTES;
     static constexpr int SMEM_SFA = SMEM_B + NST * B_BYTES;
     static constexpr int SMEM_SFB = SMEM_SFA + NST * SFA_BYTES;
-    static constexpr int SMEM_EPI = SMEM_SFB + NST * SFB_BYTES;
-    static constexpr int SMEM_BAR = SMEM_EPI + 4 * 2 * EPI_BUF_BYTES;
-    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 3);
-    static constexpr int SMEM_TABLES = SMEM_MISC + 16;     // grouped: pair-tile and band prefixes
-    static constexpr int SMEM_TOTAL = SMEM_TABLES + (GROUPED ? 4 * (2 * (MAX_GROUPS + 1) + 32) : 0);
+    static constexpr int SMEM_EPI = (SMEM_SFB + NST * SFB_BYTES + 1023) / 1024 * 1024;
+    static constexpr int SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
+    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 5);
+    static constexpr int SMEM_TABLES = SMEM_MISC + 16;     // grouped: row offsets, pair-tile and band prefixes
+    static constexpr int SMEM_TOTAL = SMEM_TABLES + (GROUPED ? 8 * (MAX_GROUPS + 1) + 4 * (2 * (MAX_GROUPS + 1) + 32) : 0);
     static constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;
-    static_assert(SMEM_EPI % 1024 == 0, "staging alignment");
-    static_assert(TMEM_SF_BASE + NST * (SFA_COLS + SFB_COLS) <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM_B % 1024 == 0 && SMEM_EPI % 1024 == 0, "operand and staging alignment");
+    static_assert(TMEM_SF + NST * (SFA_COLS + SFB_COLS) <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -363,6 +380,7 @@ struct PairTile {
 };
 
 // Dense: bands of 8 pair rows (16 M-tiles); inside a band N-tiles advance every 8 pair tiles.
+template <int TN>
 __device__ __forceinline__ PairTile pair_dense_tile(const Params& p, int64_t t, uint32_t rank) {
     constexpr int64_t GM = 8;
     const int64_t band_tiles = GM * p.n_tiles;
@@ -370,15 +388,16 @@ __device__ __forceinline__ PairTile pair_dense_tile(const Params& p, int64_t t, 
     const int64_t band_m = min64(GM, p.m_tiles - band * GM);
     const int64_t mp = band * GM + in % band_m, nt = in / band_m;
     PairTile r;
-    r.row0 = mp * 256 + 128 * (int64_t)rank; r.row_end = p.M; r.n0 = nt * BN; r.g = 0;
+    r.row0 = mp * 256 + 128 * (int64_t)rank; r.row_end = p.M; r.n0 = nt * TN; r.g = 0;
     r.band_a = mp * 2 + rank;
     return r;
 }
 
-// Grouped: ptile2[g] = pair tiles (256 rows) of groups < g, pband[g] = 128-row bands of groups < g
-// (group g's first band in the grouped scale layout).
-__device__ __forceinline__ PairTile pair_grouped_tile(const Params& p, const int* ptile2, const int* pband, int64_t t,
-                                                      uint32_t rank) {
+// Grouped: s_off = the group row offsets, ptile2[g] = pair tiles (256 rows) of groups < g, pband[g] =
+// 128-row bands of groups < g (group g's first band in the grouped scale layout); all in shared memory.
+template <int TN>
+__device__ __forceinline__ PairTile pair_grouped_tile(const Params& p, const int64_t* s_off, const int* ptile2,
+                                                      const int* pband, int64_t t, uint32_t rank) {
     const int64_t mt_global = t / p.n_tiles;
     int lo = 0, hi = (int)p.G;
     while (hi - lo > 1) {
@@ -388,32 +407,33 @@ __device__ __forceinline__ PairTile pair_grouped_tile(const Params& p, const int
     const int64_t g = lo;
     const int64_t pm = mt_global - ptile2[g];
     PairTile r;
-    r.row0 = __ldg(p.group_offsets + g) + pm * 256 + 128 * (int64_t)rank;
-    r.row_end = __ldg(p.group_offsets + g + 1);
-    r.n0 = (t % p.n_tiles) * BN;
+    r.row0 = s_off[g] + pm * 256 + 128 * (int64_t)rank;
+    r.row_end = s_off[g + 1];
+    r.n0 = (t % p.n_tiles) * TN;
     r.g = g;
     r.band_a = pband[g] + 2 * pm + rank;
     return r;
 }
 
-template <int FMT, bool GROUPED, bool COL_ALPHA>
+template <int FMT, bool GROUPED, bool COL_ALPHA, int TN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                     const __grid_constant__ CUtensorMap tmD, const Params p) {
-    using C = PairCfg<FMT, GROUPED>;
+    using C = PairCfg<FMT, GROUPED, TN>;
     constexpr int NST = C::NST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase + C::SMEM_BAR;                 // NST barriers (used in the leader)
     const uint32_t bar_empty = bar_full + 8 * NST;                 // NST barriers
-    const uint32_t bar_tfull = bar_empty + 8 * NST;
-    const uint32_t bar_tempty = bar_tfull + 8;                     // used in the leader
-    const uint32_t bar_done = bar_tempty + 8;
+    const uint32_t bar_tfull = bar_empty + 8 * NST;                // 2 barriers (one per accumulator)
+    const uint32_t bar_tempty = bar_tfull + 16;                    // 2 barriers (used in the leader)
+    const uint32_t bar_done = bar_tempty + 16;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
-    int* ptile2 = reinterpret_cast<int*>(smem + C::SMEM_TABLES);
+    int64_t* s_off = reinterpret_cast<int64_t*>(smem + C::SMEM_TABLES);
+    int* ptile2 = reinterpret_cast<int*>(s_off + (MAX_GROUPS + 1));
     int* pband = ptile2 + (MAX_GROUPS + 1);
     int* s_warp = pband + (MAX_GROUPS + 1);
 
@@ -426,8 +446,10 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
-        mbar_init(bar_tfull, 1);
-        mbar_init(bar_tempty, 8);            // 4 epilogue warps in each CTA
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_tfull + 8 * b, 1);
+            mbar_init(bar_tempty + 8 * b, 2 * EPI_WARPS);   // the epilogue warps of both CTAs
+        }
         mbar_init(bar_done, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -445,8 +467,10 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     if (GROUPED) {
-        scan_group_tiles<256>(p.group_offsets, (int)p.G, ptile2, s_warp);
-        scan_group_tiles<128>(p.group_offsets, (int)p.G, pband, s_warp);
+        for (int i = threadIdx.x; i <= (int)p.G; i += blockDim.x) s_off[i] = __ldg(p.group_offsets + i);
+        __syncthreads();
+        scan_group_tiles<256>(s_off, (int)p.G, ptile2, s_warp);
+        scan_group_tiles<128>(s_off, (int)p.G, pband, s_warp);
     }
     tc_fence_before();
     __syncthreads();
@@ -462,8 +486,8 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint32_t phase = 0;
         bool ok = true;
         for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
-            const PairTile tile = GROUPED ? pair_grouped_tile(p, ptile2, pband, t, rank) : pair_dense_tile(p, t, rank);
-            const int64_t brow = (GROUPED ? tile.g * p.N : 0) + tile.n0 + 128 * (int64_t)rank;
+            const PairTile tile = GROUPED ? pair_grouped_tile<TN>(p, s_off, ptile2, pband, t, rank) : pair_dense_tile<TN>(p, t, rank);
+            const int64_t brow = (GROUPED ? tile.g * p.N : 0) + tile.n0 + (TN / 2) * (int64_t)rank;
             const int64_t sfb_y0 = GROUPED ? tile.g * (p.sb_group_bytes >> 8) : 0;   // 256-byte rows
             const int64_t bt0 = tile.n0 / 128;
             for (int64_t ks = 0; ks < p.k_stages; ++ks) {
@@ -482,8 +506,10 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     // scale atoms: 512 bytes = two 256-byte rows of the scale maps; bands past the
                     // end of a tensor read as zeros
                     tma_load_2d_pair(sSFA, &tmSA, 0, (int32_t)((tile.band_a * p.nct + ct0) * 2), fb);
-                    tma_load_2d_pair(sSFB, &tmSB, 0, (int32_t)(sfb_y0 + (bt0 * p.nct + ct0) * 2), fb);
-                    tma_load_2d_pair(sSFB + C::SFA_BYTES, &tmSB, 0, (int32_t)(sfb_y0 + ((bt0 + 1) * p.nct + ct0) * 2), fb);
+#pragma unroll
+                    for (int hb = 0; hb < C::SFB_BANDS; ++hb)
+                        tma_load_2d_pair(sSFB + hb * C::SFA_BYTES, &tmSB, 0,
+                                         (int32_t)(sfb_y0 + ((bt0 + hb) * p.nct + ct0) * 2), fb);
                 }
                 __syncwarp();
                 if (++stage == NST) { stage = 0; phase ^= 1; }
@@ -494,11 +520,15 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // ------------------------------- scale copies + MMA (leader) -------------------------------
         if (leader) {
             int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            uint32_t phase = 0;
             bool ok = true, issued_any = false;
-            for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
-                if (!warp_wait(bar_tempty, acc_phase ^ 1, abort_flag)) { ok = false; break; }
+            int64_t ti = 0;                           // this pair's tile count: accumulator ti % ACC
+            for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs, ++ti) {
+                const uint32_t ab = (uint32_t)(ti % C::ACC);
+                const uint32_t use = (uint32_t)(ti / C::ACC);        // uses of this accumulator so far
+                if (!warp_wait(bar_tempty + 8 * ab, (use & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
+                const uint32_t tacc = tmem + ab * TN;
                 for (int64_t ks = 0; ks < p.k_stages; ++ks) {
                     if (!warp_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
@@ -507,21 +537,25 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES;
                         const uint32_t sSFA = sbase + C::SMEM_SFA + stage * C::SFA_BYTES;
                         const uint32_t sSFB = sbase + C::SMEM_SFB + stage * C::SFB_BYTES;
-                        const uint32_t tSFA = tmem + TMEM_SF_BASE + stage * (C::SFA_COLS + C::SFB_COLS);
+                        const uint32_t tSFA = tmem + C::TMEM_SF + stage * (C::SFA_COLS + C::SFB_COLS);
                         const uint32_t tSFB = tSFA + C::SFA_COLS;
+                        // A atom j to columns 4j..4j+3; B band h, atom j to SFB_BANDS * 4j + 4h
 #pragma unroll
                         for (int j = 0; j < C::SF_ATOMS_A; ++j) {
                             tc2_cp_sf(tSFA + 4 * j, desc_sf(sSFA + 512 * j));
-                            tc2_cp_sf(tSFB + 8 * j, desc_sf(sSFB + 512 * j));
-                            tc2_cp_sf(tSFB + 8 * j + 4, desc_sf(sSFB + C::SFA_BYTES + 512 * j));
+#pragma unroll
+                            for (int hb = 0; hb < C::SFB_BANDS; ++hb)
+                                tc2_cp_sf(tSFB + C::SFB_BANDS * 4 * j + 4 * hb, desc_sf(sSFB + hb * C::SFA_BYTES + 512 * j));
                         }
 #pragma unroll
                         for (int j = 0; j < BKB / 32; ++j) {
+                            // MXFP8: one atom covers the 4 MMAs of the stage, the scale id picks the byte;
+                            // NVFP4: each MMA (K = 64) consumes a whole atom word
                             const uint32_t sf_id = FMT == 0 ? (uint32_t)j : 0u;
                             const uint32_t col = FMT == 0 ? 0u : (uint32_t)j;
-                            tc2_mma<FMT>(tmem, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j),
-                                         make_idesc<FMT, 2 * BM>(sf_id), tSFA + 4 * col, tSFB + 8 * col,
-                                         (ks > 0 || j > 0) ? 1u : 0u);
+                            tc2_mma<FMT>(tacc, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j),
+                                         make_idesc<FMT, 2 * BM, TN>(sf_id), tSFA + 4 * col,
+                                         tSFB + C::SFB_BANDS * 4 * col, (ks > 0 || j > 0) ? 1u : 0u);
                         }
                         tc2_commit_mc(bar_empty + 8 * stage, (uint16_t)3);
                     }
@@ -530,9 +564,8 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (++stage == NST) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                if (elect_one()) tc2_commit_mc(bar_tfull, (uint16_t)3);
+                if (elect_one()) tc2_commit_mc(bar_tfull + 8 * ab, (uint16_t)3);
                 __syncwarp();
-                acc_phase ^= 1;
             }
             if (issued_any) {
                 // the pair's MMAs read the peer's shared memory: all of them complete before either
@@ -547,17 +580,35 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     } else {
         // ------------------------------- epilogue (both CTAs) -------------------------------
-        const int q = warp & 3;
+        const int q = warp & 3;                     // TMEM lane quadrant this warp may access
+        const int h = (warp - 2) >> 2;              // column half
         const uint32_t tempty_leader = map_to_cta(bar_tempty, 0);
-        uint32_t acc_phase = 0, epi_chunk = 0;
-        for (int64_t t = pair_id; t < total_tiles; t += n_pairs) {
-            const PairTile tile = GROUPED ? pair_grouped_tile(p, ptile2, pband, t, rank) : pair_dense_tile(p, t, rank);
-            if (!mbar_wait(bar_tfull, acc_phase, abort_flag)) break;
+        const uint32_t ebase = sbase + C::SMEM_EPI + (uint32_t)((warp - 2) * 2 * EPI_BUF_BYTES);
+        uint32_t epi_chunk = 0;
+        // tile coordinates and row scales of the next tile are fetched while this tile's stores run
+        PairTile tile{};
+        float aa = 1.0f, ab_g = 1.0f;
+        if (pair_id < total_tiles) {
+            tile = GROUPED ? pair_grouped_tile<TN>(p, s_off, ptile2, pband, pair_id, rank) : pair_dense_tile<TN>(p, pair_id, rank);
+            const int64_t row = tile.row0 + q * 32 + lane;
+            epilogue_alphas<GROUPED>(p, row, row < tile.row_end, tile.g, aa, ab_g);
+        }
+        int64_t ti = 0;
+        for (int64_t t = pair_id; t < total_tiles; t += n_pairs, ++ti) {
+            const uint32_t ab = (uint32_t)(ti % C::ACC);
+            const uint32_t use = (uint32_t)(ti / C::ACC);
+            if (!mbar_wait(bar_tfull + 8 * ab, use & 1u, abort_flag)) break;
             tc_fence_after();
-            epilogue_tile<FMT, GROUPED, COL_ALPHA, C::EPI_COLS, C::EPI_BUF_BYTES, true>(
-                p, &tmD, tmem, q, lane, tile.row0, tile.row_end, tile.n0, tile.g,
-                sbase + C::SMEM_EPI + (uint32_t)(q * 2 * C::EPI_BUF_BYTES), epi_chunk, tempty_leader);
-            acc_phase ^= 1;
+            uint32_t packed[TN / 4];
+            epilogue_drain<TN, COL_ALPHA>(p, tmem + ab * TN, q, h, lane, tile.n0, aa, ab_g, tempty_leader + 8 * ab, packed);
+            const PairTile cur = tile;
+            const int64_t tn = t + n_pairs;
+            if (tn < total_tiles) {
+                tile = GROUPED ? pair_grouped_tile<TN>(p, s_off, ptile2, pband, tn, rank) : pair_dense_tile<TN>(p, tn, rank);
+                const int64_t row = tile.row0 + q * 32 + lane;
+                epilogue_alphas<GROUPED>(p, row, row < tile.row_end, tile.g, aa, ab_g);
+            }
+            epilogue_store<TN, GROUPED>(p, &tmD, q, h, lane, cur.row0, cur.row_end, cur.n0, ebase, epi_chunk, packed);
         }
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
@@ -635,14 +686,14 @@ bool make_sf_map(CUtensorMap* map, const uint8_t* base, int64_t bytes, uint32_t 
     return r == CUDA_SUCCESS;
 }
 
-template <int FMT, bool GROUPED, bool COL_ALPHA>
+template <int FMT, bool GROUPED, bool COL_ALPHA, int TN>
 cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
-    using C = PairCfg<FMT, GROUPED>;
+    using C = PairCfg<FMT, GROUPED, TN>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     static int resident_pairs = 0;          // CTA pairs that fit on the GPU at once
     std::call_once(attr_once, [num_sms] {
-        auto kern = bs_gemm_pair_kernel<FMT, GROUPED, COL_ALPHA>;
+        auto kern = bs_gemm_pair_kernel<FMT, GROUPED, COL_ALPHA, TN>;
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
         if (attr_err != cudaSuccess) return;
         cudaLaunchConfig_t cfg = {};
@@ -670,10 +721,10 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
     const int64_t sb_bytes = (GROUPED ? a.G : 1) * sb_group_bytes;
     CUtensorMap tmA, tmB, tmSA, tmSB, tmD;
     if (!make_map(&tmA, a.a, k_bytes, a.M, 128)) return cudaErrorInvalidValue;
-    if (!make_map(&tmB, a.b, k_bytes, GROUPED ? a.G * a.N : a.N, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&tmB, a.b, k_bytes, GROUPED ? a.G * a.N : a.N, TN / 2)) return cudaErrorInvalidValue;
     if (!make_sf_map(&tmSA, a.sa, sa_bytes, (uint32_t)C::SF_ATOMS_A)) return cudaErrorInvalidValue;
-    if (!make_sf_map(&tmSB, a.sb, sb_bytes, (uint32_t)C::SF_ATOMS_A)) return cudaErrorInvalidValue;
-    if (!make_out_map(&tmD, a.d, a.M, a.N, a.ldd, (uint32_t)C::EPI_COLS)) return cudaErrorInvalidValue;
+    if (!make_sf_map(&tmSB, a.sb, sb_bytes, (uint32_t)C::SF_ATOMS_A)) return cudaErrorInvalidValue;   // one band per load
+    if (!make_out_map(&tmD, a.d, a.M, a.N, a.ldd, (uint32_t)EPI_COLS)) return cudaErrorInvalidValue;
 
     Params p{};
     p.sa = a.sa; p.sb = a.sb;
@@ -682,7 +733,7 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
     p.M = a.M; p.N = a.N; p.K = a.K; p.d = a.d; p.ldd = a.ldd;
     p.G = a.G; p.group_offsets = a.group_offsets;
     p.m_tiles = (a.M + 2 * BM - 1) / (2 * BM);        // pair rows (256)
-    p.n_tiles = (a.N + BN - 1) / BN;
+    p.n_tiles = (a.N + TN - 1) / TN;
     p.k_stages = k_bytes / BKB;
     p.nct = (a.K / block + 3) / 4;
     p.sb_group_bytes = sb_group_bytes;
@@ -691,7 +742,7 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
     // a persistent grid: only as many pairs as can be resident together (an odd SM left in a GPC
     // cannot host half a cluster)
     const int64_t pairs = max64(1, min64(tiles_bound, (int64_t)min(resident_pairs, num_sms / 2)));
-    bs_gemm_pair_kernel<FMT, GROUPED, COL_ALPHA><<<(unsigned)(2 * pairs), NUM_THREADS, C::SMEM_ALLOC, stream>>>(
+    bs_gemm_pair_kernel<FMT, GROUPED, COL_ALPHA, TN><<<(unsigned)(2 * pairs), NUM_THREADS, C::SMEM_ALLOC, stream>>>(
         tmA, tmB, tmSA, tmSB, tmD, p);
     return cudaGetLastError();
 }
@@ -701,12 +752,16 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
 cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream) {
     if (args.G > MAX_GROUPS) return cudaErrorInvalidValue;
     const bool col_alpha = args.G == 0 && args.alpha_b_scope == 2;   // per-output-column factor (dense only)
+    // dense: 256-column tiles, one accumulator; grouped (a few K stages per tile): 128-column tiles
+    // with two accumulators so that each tile's epilogue overlaps the next tile's MMAs
     if (args.fmt == 0) {
-        if (args.G > 0) return launch_pair_impl<0, true, false>(args, num_sms, stream);
-        return col_alpha ? launch_pair_impl<0, false, true>(args, num_sms, stream) : launch_pair_impl<0, false, false>(args, num_sms, stream);
+        if (args.G > 0) return launch_pair_impl<0, true, false, 256>(args, num_sms, stream);
+        return col_alpha ? launch_pair_impl<0, false, true, 256>(args, num_sms, stream)
+                         : launch_pair_impl<0, false, false, 256>(args, num_sms, stream);
     }
-    if (args.G > 0) return launch_pair_impl<1, true, false>(args, num_sms, stream);
-    return col_alpha ? launch_pair_impl<1, false, true>(args, num_sms, stream) : launch_pair_impl<1, false, false>(args, num_sms, stream);
+    if (args.G > 0) return launch_pair_impl<1, true, false, 256>(args, num_sms, stream);
+    return col_alpha ? launch_pair_impl<1, false, true, 256>(args, num_sms, stream)
+                     : launch_pair_impl<1, false, false, 256>(args, num_sms, stream);
 }
 
 uint32_t read_and_clear_device_status() {
