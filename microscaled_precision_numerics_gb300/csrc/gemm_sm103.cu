@@ -37,6 +37,7 @@
 // issuing work and lets its in-flight copies land before the pair leaves and frees its TMEM.
 #include "../../include/mxnum.h"
 #include "mx_internal.h"
+#include "mx_async.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -53,7 +54,6 @@ constexpr int BKB = 128;                  // K bytes per pipeline stage
 constexpr int NUM_THREADS = 320;         // producer, MMA, 8 epilogue warps
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_GROUPS = MX_MAX_GROUPS;
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
 
 struct Params {
     const uint8_t* sa; const uint8_t* sb;
@@ -71,54 +71,7 @@ struct Params {
 // ---------------------------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded wait: false when the wait expired or another role of this CTA aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    uint32_t it = 0;
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((++it & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-                atomicOr(&g_mx_device_status, 1u);
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    }
-}
-
-// All lanes of the warp wait; the result is made warp-uniform (any lane's failure fails all).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag)) != 0;
-}
-// One lane of a converged warp (always the lowest active lane, so the same lane every time).
-__device__ __forceinline__ bool elect_one() {
-    uint32_t p;
-    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
-    return p != 0;
-}
+using namespace async;
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -491,7 +444,7 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int64_t sfb_y0 = GROUPED ? tile.g * (p.sb_group_bytes >> 8) : 0;   // 256-byte rows
             const int64_t bt0 = tile.n0 / 128;
             for (int64_t ks = 0; ks < p.k_stages; ++ks) {
-                if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+                if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
                 if (elect_one()) {
                     const uint32_t fb = map_to_cta(bar_full + 8 * stage, 0);
                     if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::STAGE_TX);
@@ -526,11 +479,11 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs, ++ti) {
                 const uint32_t ab = (uint32_t)(ti % C::ACC);
                 const uint32_t use = (uint32_t)(ti / C::ACC);        // uses of this accumulator so far
-                if (!warp_wait(bar_tempty + 8 * ab, (use & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+                if (!warp_wait(bar_tempty + 8 * ab, (use & 1u) ^ 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t tacc = tmem + ab * TN;
                 for (int64_t ks = 0; ks < p.k_stages; ++ks) {
-                    if (!warp_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                    if (!warp_wait(bar_full + 8 * stage, phase, abort_flag, &g_mx_device_status)) { ok = false; break; }
                     tc_fence_after();
                     if (elect_one()) {
                         const uint32_t sA = sbase + C::SMEM_A + stage * C::A_BYTES;
@@ -597,7 +550,7 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (int64_t t = pair_id; t < total_tiles; t += n_pairs, ++ti) {
             const uint32_t ab = (uint32_t)(ti % C::ACC);
             const uint32_t use = (uint32_t)(ti / C::ACC);
-            if (!mbar_wait(bar_tfull + 8 * ab, use & 1u, abort_flag)) break;
+            if (!mbar_wait(bar_tfull + 8 * ab, use & 1u, abort_flag, &g_mx_device_status)) break;
             tc_fence_after();
             uint32_t packed[TN / 4];
             epilogue_drain<TN, COL_ALPHA>(p, tmem + ab * TN, q, h, lane, tile.n0, aa, ab_g, tempty_leader + 8 * ab, packed);
@@ -631,59 +584,24 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // ---------------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
 bool make_map(CUtensorMap* map, const uint8_t* base, int64_t k_bytes, int64_t rows, uint32_t box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)k_bytes, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)k_bytes};
-    cuuint32_t box[2] = {(cuuint32_t)BKB, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_tensor_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, (uint64_t)k_bytes, (uint64_t)rows,
+                                (uint64_t)k_bytes, (uint32_t)BKB, box_rows, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 // Output map: BF16 [rows, N] with row pitch ldd, box of `box_cols` x 32 rows, swizzled to match the
 // epilogue's staging layout.
 bool make_out_map(CUtensorMap* map, uint16_t* d, int64_t rows, int64_t N, int64_t ldd, uint32_t box_cols) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(ldd * 2)};
-    cuuint32_t box[2] = {box_cols, 32};
-    cuuint32_t estr[2] = {1, 1};
     const CUtensorMapSwizzle sw = box_cols * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, d, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_tensor_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, d, (uint64_t)N, (uint64_t)rows, (uint64_t)(ldd * 2),
+                                box_cols, 32, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 // Scale tensor viewed as rows of 256 bytes (two rows per 512-byte atom), box of `atoms` atoms.
 bool make_sf_map(CUtensorMap* map, const uint8_t* base, int64_t bytes, uint32_t atoms) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {256, (cuuint64_t)(bytes / 256)};
-    cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {256, 2 * atoms};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_tensor_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 256, (uint64_t)(bytes / 256), 256, 256,
+                                2 * atoms, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 template <int FMT, bool GROUPED, bool COL_ALPHA, int TN>
@@ -748,6 +666,35 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
 }
 
 }  // namespace
+
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+}  // namespace
+
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t outer,
+                          uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle,
+                          CUtensorMapL2promotion promo) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream) {
     if (args.G > MAX_GROUPS) return cudaErrorInvalidValue;

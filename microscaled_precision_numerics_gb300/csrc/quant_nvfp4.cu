@@ -424,7 +424,9 @@ weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, cons
                       uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
                       uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, float* __restrict__ s_w) {
     __shared__ uint8_t st[W2_ROWS / 16][W2_COLS / 16];                 // tile scales
-    const int64_t g = blockIdx.z;
+    // matrices in the reverse of the amax pass's order: the first CTAs find the matrices that pass
+    // read last still in L2
+    const int64_t g = gridDim.z - 1 - blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t o0 = (int64_t)blockIdx.y * W2_ROWS + warp * 16;
     const int64_t h0 = (int64_t)blockIdx.x * W2_COLS;
