@@ -50,6 +50,7 @@ struct GemmArgs {
 };
 cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream);
 uint32_t read_and_clear_device_status();
+uint32_t read_and_clear_mxfp8_status();
 
 int device_sm_count();
 

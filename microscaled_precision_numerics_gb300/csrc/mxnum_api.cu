@@ -240,7 +240,7 @@ mx_status mx_count_mismatch(const uint8_t* x, const uint8_t* y, int64_t nbytes, 
 
 mx_status mx_check_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return MX_ERR_CUDA;
-    const uint32_t w = mxk::read_and_clear_device_status();
+    const uint32_t w = mxk::read_and_clear_device_status() | mxk::read_and_clear_mxfp8_status();
     return w ? MX_ERR_TIMEOUT : MX_OK;
 }
 

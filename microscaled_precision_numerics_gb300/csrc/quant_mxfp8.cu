@@ -7,11 +7,16 @@
 // kernel cost 2.2 + 2.6 ms per micro-batch; here one kernel writes both copies with their scales
 // already in the GEMM layout.
 //
-// CTA tile: 128 rows x 128 columns of BF16 (32 KB), staged in shared memory with a padded pitch; both
-// passes read it with 16-byte loads and keep the values in registers between amax and conversion.
+// CTA tile: 128 rows x 128 columns of BF16 (32 KB), brought into shared memory by TMA (128-byte
+// swizzle); both passes read it with 16-byte loads and keep the values in registers between amax and
+// conversion.
 // Scale exponent: e = max(exp_field(amax) - 8, 0) - 127 as an E8M0 byte; the multiply by 2^-e is
 // exact in FP32 for every value that can round to a nonzero E4M3 code.
+#include "../../include/mxnum.h"
 #include "mx_internal.h"
+#include "mx_async.cuh"
+
+#include <mutex>
 
 namespace mxk {
 
@@ -19,7 +24,6 @@ namespace {
 
 constexpr int QT_ROWS = 128;
 constexpr int QT_COLS = 128;
-constexpr int QT_PITCH = 272;   // bytes per staged row: 256 + 16 keeps 16-byte accesses conflict-free
 constexpr int QT_THREADS = 256;
 
 __device__ __forceinline__ uint32_t e8m0_from_amax_bits(uint32_t amax16) {
@@ -51,64 +55,88 @@ __device__ __forceinline__ float chunk_elem(const uint4& v, int j) {
     return (j & 1) ? bf16_hi(w) : bf16_lo(w);
 }
 
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ unsigned int g_mx8_status = 0;
 
-// Issue the 16-byte loads of one 128 x 128 tile into a staging buffer (zero fill outside the tensor).
-__device__ __forceinline__ void stage_tile(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
-                                           int64_t r0, int64_t c0, uint32_t buf) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int ci = (int)threadIdx.x + QT_THREADS * j;
-        const int rr = ci >> 4, ch = ci & 15;
-        const int64_t r = r0 + rr, c = c0 + ch * 8;
-        const bool valid = r < R && c < K;
-        cp_async_16(buf + rr * QT_PITCH + ch * 16, valid ? (const void*)(x + r * ldx + c) : (const void*)x, valid);
-    }
+constexpr int QT_CONSUMERS = QT_THREADS;               // 8 consumer warps
+constexpr int QT_BLOCK = QT_CONSUMERS + 32;            // + 1 producer warp
+constexpr int QT_NST = 2;                              // ring stages of one 32 KB tile
+constexpr int QT_CTAS_PER_SM = 3;                      // occupancy hides the passes' dependent chains
+constexpr int QT_TILE_BYTES = QT_ROWS * QT_COLS * 2;
+constexpr int QT_BOX_BYTES = QT_TILE_BYTES / 2;        // 128 rows x 64 columns (128 bytes)
+
+// Byte offset of 16-byte chunk c (0..15 along the 128 columns) of tile row r in a staged tile: two TMA
+// boxes of 128 rows x 128 bytes (columns 0..63, 64..127), each with the 128-byte swizzle (chunk index
+// XOR row & 7), which keeps both passes' 16-byte shared loads free of bank conflicts.
+__device__ __forceinline__ uint32_t qt_off(int r, int c) {
+    return (uint32_t)((c >> 3) * QT_BOX_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// CTA tile: 128 rows x 128 columns of BF16 staged in shared memory (pitch 272 B).  Persistent CTAs
-// walk the tiles with two staging buffers: the next tile's loads are in flight while this one is
-// quantized.
+__device__ __forceinline__ void named_sync_consumers() { asm volatile("bar.sync 1, %0;" :: "r"(QT_CONSUMERS) : "memory"); }
+
+// Persistent CTAs (three per SM) walk the 128 x 128 tiles; warp 0 streams them through a 2-stage ring
+// by TMA, warps 1..8 quantize:
 //   row pass:    thread -> (row, pair of 32-column blocks); 8 x 16-byte shared loads
 //   column pass: thread -> (8-column chunk, 32-row block, quarter of 8 rows); 8 x 16-byte shared
 //                loads; the 32-row amax combines the 4 quarters (lanes l, l^8, l^16, l^24)
 template <bool ROW, bool COL, bool GROUPED>
-__global__ void __launch_bounds__(QT_THREADS)
-mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
+__global__ void __launch_bounds__(QT_BLOCK, QT_CTAS_PER_SM)
+mxfp8_quantize_kernel(const __grid_constant__ CUtensorMap tmX, int64_t R, int64_t K,
                       uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
                       uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, int64_t tiles_c, int64_t tiles,
                       int G, const int64_t* __restrict__ group_offsets) {
-    extern __shared__ __align__(16) uint8_t qsm[];
-    uint8_t (*colsc)[QT_COLS] = reinterpret_cast<uint8_t (*)[QT_COLS]>(qsm + 2 * QT_ROWS * QT_PITCH);
-    const uint32_t buf_base = (uint32_t)__cvta_generic_to_shared(qsm);
-    // expert-group tables (grouped row-wise scale layout) after the staging buffers
-    int64_t* s_off = reinterpret_cast<int64_t*>(qsm + 2 * QT_ROWS * QT_PITCH + 4 * QT_COLS);
+    using namespace async;
+    extern __shared__ uint8_t qsm_raw[];
+    uint8_t* qsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t (*colsc)[QT_COLS] = reinterpret_cast<uint8_t (*)[QT_COLS]>(qsm + QT_NST * QT_TILE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(qsm + QT_NST * QT_TILE_BYTES + 4 * QT_COLS);   // full[3], empty[3]
+    int* abort_flag = reinterpret_cast<int*>(bars + 2 * QT_NST);
+    // expert-group tables (grouped row-wise scale layout)
+    int64_t* s_off = reinterpret_cast<int64_t*>(qsm + QT_NST * QT_TILE_BYTES + 4 * QT_COLS + 64);
     int* s_ptile = reinterpret_cast<int*>(s_off + (G + 1));
     int* s_warp = s_ptile + (G + 1);
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * QT_NST;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < QT_NST; ++st) {
+            mbar_init(full0 + 8 * st, 1);
+            mbar_init(empty0 + 8 * st, 1);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
     if (GROUPED) load_group_tables(group_offsets, G, s_off, s_ptile, s_warp);
+    __syncthreads();
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int64_t t = blockIdx.x;
-    if (t < tiles) stage_tile(x, R, K, ldx, (t / tiles_c) * QT_ROWS, (t % tiles_c) * QT_COLS, buf_base);
-    cp_async_commit();
-    for (int it = 0; t < tiles; ++it, t += gridDim.x) {
-        const int64_t tn = t + gridDim.x;
-        if (tn < tiles)
-            stage_tile(x, R, K, ldx, (tn / tiles_c) * QT_ROWS, (tn % tiles_c) * QT_COLS,
-                       buf_base + ((it + 1) & 1) * QT_ROWS * QT_PITCH);
-        cp_async_commit();
-        cp_async_wait_1();
-        __syncthreads();
-        const uint8_t* tile = qsm + (it & 1) * QT_ROWS * QT_PITCH;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) {
+        // ------------------------------- producer -------------------------------
+        if (lane == 0) asm volatile("prefetch.tensormap [%0];" :: "l"(&tmX) : "memory");
+        uint32_t k = 0;
+        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++k) {
+            const uint32_t stage = k % QT_NST, phase = (k / QT_NST) & 1u;
+            if (!warp_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, &g_mx8_status)) break;
+            if (elect_one()) {
+                const int32_t r0 = (int32_t)((t / tiles_c) * QT_ROWS), c0 = (int32_t)((t % tiles_c) * QT_COLS);
+                const uint32_t dst = smem_u32(qsm + stage * QT_TILE_BYTES);
+                mbar_arrive_expect_tx(full0 + 8 * stage, QT_TILE_BYTES);
+                tma_load_2d(dst, &tmX, c0, r0, full0 + 8 * stage);
+                tma_load_2d(dst + QT_BOX_BYTES, &tmX, c0 + 64, r0, full0 + 8 * stage);
+            }
+            __syncwarp();
+        }
+        return;
+    }
+    const int tid = threadIdx.x - 32, cw = tid >> 5;         // consumer thread / warp
+    uint32_t k = 0;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++k) {
+        const uint32_t stage = k % QT_NST, phase = (k / QT_NST) & 1u;
+        // warp-uniform: the passes below use full-warp shuffles
+        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * stage, phase, abort_flag, &g_mx8_status)) != 0;
+        const uint8_t* tile = qsm + stage * QT_TILE_BYTES;
         const int64_t r0 = (t / tiles_c) * QT_ROWS;
         const int64_t c0 = (t % tiles_c) * QT_COLS;
 
-        if (ROW) {
-            // lanes 0..7 take 8 different rows of the same 64-column half: conflict-free 16-byte loads
+        if (ROW && ok) {
+            // lanes 0..7 take 8 different rows of the same 64-column half
             const int half = (tid >> 3) & 1;
             const int rr = (tid & 7) + 8 * (tid >> 4);
             const int64_t r = r0 + rr;
@@ -118,7 +146,7 @@ mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int6
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(tile + rr * QT_PITCH + half * 128 + b * 64 + i * 16);
+                    const uint4 v = *reinterpret_cast<const uint4*>(tile + qt_off(rr, half * 8 + b * 4 + i));
                     w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
                 }
                 uint32_t codes[8];
@@ -144,14 +172,13 @@ mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int6
             }
         }
 
-        if (COL) {
-            const int rb = warp >> 1;                        // 32-row block
-            const int chunk = (warp & 1) * 8 + (lane & 7);   // 8-column chunk
+        if (COL && ok) {
+            const int rb = cw >> 1;                          // 32-row block
+            const int chunk = (cw & 1) * 8 + (lane & 7);     // 8-column chunk
             const int q = lane >> 3;                         // quarter: rows q*8 .. q*8+7 of the block
             uint4 v[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                v[i] = *reinterpret_cast<const uint4*>(tile + (rb * 32 + q * 8 + i) * QT_PITCH + chunk * 16);
+            for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint4*>(tile + qt_off(rb * 32 + q * 8 + i, chunk));
             uint32_t m[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -159,9 +186,9 @@ mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int6
                 m[2] = absmax_bf16x2(m[2], v[i].z); m[3] = absmax_bf16x2(m[3], v[i].w);
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                m[k] = __vmaxu2(m[k], __shfl_xor_sync(0xFFFFFFFFu, m[k], 8));
-                m[k] = __vmaxu2(m[k], __shfl_xor_sync(0xFFFFFFFFu, m[k], 16));
+            for (int kk = 0; kk < 4; ++kk) {
+                m[kk] = __vmaxu2(m[kk], __shfl_xor_sync(0xFFFFFFFFu, m[kk], 8));
+                m[kk] = __vmaxu2(m[kk], __shfl_xor_sync(0xFFFFFFFFu, m[kk], 16));
             }
             const int64_t rbase = r0 + rb * 32;
             const bool rows_ok = rbase < R;
@@ -179,14 +206,18 @@ mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int6
                     __stcs(reinterpret_cast<uint2*>(q_col + c * R + rbase + q * 8), make_uint2(lo, hi));
                 if (q == 0) colsc[rb][chunk * 8 + j] = (uint8_t)sc;
             }
-            __syncthreads();
+        }
+        // both passes have read the stage: hand it back to the producer
+        named_sync_consumers();
+        if (tid == 0) mbar_arrive(empty0 + 8 * stage);
+        if (COL) {
             // one 32-bit word of 4 row-block scales per column (r0 / 32 is a multiple of 4)
-            if (tid < QT_COLS) {
-                const int64_t cw = c0 + tid;
-                if (cw < K) {
+            if (ok && tid < QT_COLS) {
+                const int64_t cw_ = c0 + tid;
+                if (cw_ < K) {
                     const int64_t nct = sf_col_tiles(R, 32);
                     const int nvalid = (int)min64(4, (R - r0) / 32);
-                    uint8_t* p = s_col + sf_offset(cw, r0 / 32, nct);
+                    uint8_t* p = s_col + sf_offset(cw_, r0 / 32, nct);
                     if (nvalid == 4) {
                         *reinterpret_cast<uint32_t*>(p) = (uint32_t)colsc[0][tid] | ((uint32_t)colsc[1][tid] << 8) |
                                                           ((uint32_t)colsc[2][tid] << 16) | ((uint32_t)colsc[3][tid] << 24);
@@ -195,8 +226,13 @@ mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int6
                     }
                 }
             }
+            named_sync_consumers();   // colsc is rewritten by the next tile
         }
-        __syncthreads();   // this buffer (and colsc) is refilled two iterations later
+    }
+    if (*abort_flag && tid == 0) {
+        // after an expired wait: give loads already issued by this CTA time to land before exit
+        const unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {}
     }
 }
 
@@ -216,31 +252,44 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64
         cudaError_t e = cudaMemsetAsync(s_col, 0, (size_t)host_scale_bytes(K, R, 32), stream);
         if (e != cudaSuccess) return e;
     }
+    CUtensorMap tmX;     // [R, K] BF16 with row pitch ldx, 128 x 64 boxes, 128-byte swizzle
+    if (!encode_tensor_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, (uint64_t)K, (uint64_t)R, (uint64_t)(ldx * 2), 64,
+                              QT_ROWS, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return cudaErrorInvalidValue;
     const int64_t tiles_c = (K + QT_COLS - 1) / QT_COLS, tiles = tiles_c * ((R + QT_ROWS - 1) / QT_ROWS);
-    const size_t smem = 2 * QT_ROWS * QT_PITCH + 4 * QT_COLS + (G > 0 ? (size_t)12 * (G + 1) + 128 : 0);
-    static bool attr_done = false;
-    if (!attr_done) {
-        const int max_smem = 2 * QT_ROWS * QT_PITCH + 4 * QT_COLS + 12 * 4097 + 128;
-        cudaFuncSetAttribute(mxfp8_quantize_kernel<true, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-        cudaFuncSetAttribute(mxfp8_quantize_kernel<true, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-        cudaFuncSetAttribute(mxfp8_quantize_kernel<false, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-        cudaFuncSetAttribute(mxfp8_quantize_kernel<true, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-        attr_done = true;
-    }
-    const unsigned grid = (unsigned)min64(tiles, (int64_t)device_sm_count() * 3);
+    const size_t base = (size_t)QT_NST * QT_TILE_BYTES + 4 * QT_COLS + 64 + 1024;
+    const size_t smem = base + (G > 0 ? (size_t)12 * (G + 1) + 128 : 0);
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [base] {
+        const int max_smem = (int)(base + 12 * (MX_MAX_GROUPS + 1) + 128);
+        const void* ks[] = {(const void*)mxfp8_quantize_kernel<true, true, false>, (const void*)mxfp8_quantize_kernel<true, false, false>,
+                            (const void*)mxfp8_quantize_kernel<false, true, false>, (const void*)mxfp8_quantize_kernel<true, false, true>};
+        for (const void* kf : ks)
+            if (attr_err == cudaSuccess) attr_err = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const unsigned grid = (unsigned)min64(tiles, (int64_t)device_sm_count() * QT_CTAS_PER_SM);
     if (G > 0)
-        mxfp8_quantize_kernel<true, false, true><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, nullptr, nullptr,
-                                                                                      tiles_c, tiles, G, group_offsets);
+        mxfp8_quantize_kernel<true, false, true><<<grid, QT_BLOCK, smem, stream>>>(tmX, R, K, q_row, s_row, nullptr, nullptr,
+                                                                                    tiles_c, tiles, G, group_offsets);
     else if (row && col)
-        mxfp8_quantize_kernel<true, true, false><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col,
-                                                                                      tiles_c, tiles, 0, nullptr);
+        mxfp8_quantize_kernel<true, true, false><<<grid, QT_BLOCK, smem, stream>>>(tmX, R, K, q_row, s_row, q_col, s_col,
+                                                                                    tiles_c, tiles, 0, nullptr);
     else if (row)
-        mxfp8_quantize_kernel<true, false, false><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col,
-                                                                                       tiles_c, tiles, 0, nullptr);
+        mxfp8_quantize_kernel<true, false, false><<<grid, QT_BLOCK, smem, stream>>>(tmX, R, K, q_row, s_row, q_col, s_col,
+                                                                                     tiles_c, tiles, 0, nullptr);
     else
-        mxfp8_quantize_kernel<false, true, false><<<grid, QT_THREADS, smem, stream>>>(x, R, K, ldx, q_row, s_row, q_col, s_col,
-                                                                                       tiles_c, tiles, 0, nullptr);
+        mxfp8_quantize_kernel<false, true, false><<<grid, QT_BLOCK, smem, stream>>>(tmX, R, K, q_row, s_row, q_col, s_col,
+                                                                                     tiles_c, tiles, 0, nullptr);
     return cudaGetLastError();
+}
+
+uint32_t read_and_clear_mxfp8_status() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_mx8_status, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+    cudaMemcpyToSymbol(g_mx8_status, &zero, sizeof(zero));
+    return v;
 }
 
 }  // namespace mxk
