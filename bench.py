@@ -379,6 +379,22 @@ class WeightSync:
                             "quantize, dequantize, re-quantize, byte compare", "layers": self.layers}
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The largest value of x over all ranks (x itself on a single process)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Work per second of the whole job: every rank processes units_per_rank_step per step, and a step
+    takes the slowest rank's time."""
+    return world * units_per_rank_step / (ms_per_step / 1e3)
+
+
 def time_device(work, torch, steps, warmup, dist=None):
     """Warm up, then time `steps` steps with CUDA events on the current stream; per-op events too."""
     ops = work.ops()
@@ -545,12 +561,9 @@ def run_device(args):
     clocks = sampler.stop()
     mx.check_device_status()
 
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
-    value = world * work.units_per_step() / (ms_per_step / 1e3)
+    value = whole_job_rate(work.units_per_step(), world, ms_per_step)
 
     ops = work.ops()
     gemm_ms = sum(per_op[i] for i, (k, _, _) in enumerate(ops) if k == "gemm")
@@ -560,9 +573,9 @@ def run_device(args):
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     dominant = "gemm" if gemm_ms >= quant_ms else "quant"
     if dominant == "gemm":
-        roofline = {"kernel": "bs_gemm_kernel<MXFP8> (FPROP+DGRAD+WGRAD)", "bound": "tensor",
+        roofline = {"kernel": "bs_gemm_pair_kernel<MXFP8> (FPROP+DGRAD+WGRAD)", "bound": "tensor",
                     "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                    "frac": round(gemm_tflops / fp8_peak, 4), "traffic": recorded_traffic("bs_gemm_kernel<MXFP8>"),
+                    "frac": round(gemm_tflops / fp8_peak, 4), "traffic": recorded_traffic("bs_gemm_pair_kernel<MXFP8>"),
                     "traffic_unit": "DRAM bytes per launch (mean of FPROP, DGRAD, WGRAD; ncu)",
                     "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16:g} (nominal FP8/BF16)"}
     else:
@@ -585,11 +598,8 @@ def run_device(args):
         b.record()
         torch.cuda.synchronize()
         e_ms = a.elapsed_time(b) / e2e_steps
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": round(world * work.units_per_step() / (e_ms / 1e3), 2), "unit": "TFLOP/s",
+        e_ms = max_over_ranks(e_ms, dist, dev)
+        e2e = {"value": round(whole_job_rate(work.units_per_step(), world, e_ms), 2), "unit": "TFLOP/s",
                "ms_per_step": round(e_ms, 3), "steps": e2e_steps,
                "h2d_bytes_per_step": work.h2d, "d2h_bytes_per_step": work.d2h}
 
