@@ -168,35 +168,37 @@ void launch_rowwise(int64_t T, int64_t H, unsigned grid_cap, size_t smem, cudaSt
 }
 
 // ------------------------------------------------------------------------------------------------
-// Column-wise 1x16 along tokens with a per-tensor scale.  CTA tile: 128 tokens x 256 columns; warp
-// w owns tokens [16w, 16w + 16), lane l owns columns [8l, 8l + 8).  Each column's 16 codes (8 bytes)
-// are stored straight from registers into the transposed output (the 8 warps fill 64 contiguous
-// bytes per column, merged in L2); block scales are staged in shared memory and written as words.
+// Column-wise 1x16 along tokens with a per-tensor scale.  CTA tile: 128 tokens x (32 CPT) columns;
+// warp w owns tokens [16w, 16w + 16), lane l owns columns [CPT l, CPT l + CPT) (CPT = 8 with
+// stochastic rounding, whose Philox block spans 8 columns; 4 otherwise, which halves the registers
+// a thread holds and doubles the resident warps).  Each column's 16 codes (8 bytes) are stored
+// straight from registers into the transposed output (the 8 warps fill 64 contiguous bytes per
+// column, merged in L2); block scales are staged in shared memory and written as words.
 // ------------------------------------------------------------------------------------------------
 constexpr int CW_TOK = 128;
-constexpr int CW_COLS = 256;
 constexpr int CW_THREADS = 256;
 
-// Load a 16 x 8 micro-tile: xr[i] holds row i's 8 BF16 values.
-__device__ __forceinline__ void load_16x8(const uint16_t* __restrict__ x, int64_t N, int64_t t0, int64_t n0,
-                                          bool valid, uint4 xr[16]) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        xr[i] = valid ? __ldcs(reinterpret_cast<const uint4*>(x + (t0 + i) * N + n0)) : make_uint4(0u, 0u, 0u, 0u);
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
-    return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
-}
-
-// Column j (0..7) of the micro-tile as 16 floats, optionally transformed and re-rounded to BF16.
-template <bool RHT>
-__device__ __forceinline__ void column_values(const uint4 xr[16], int j, uint32_t signmask, float v[16]) {
+// Load a 16 x CPT micro-tile: xw[i] holds row i's CPT BF16 values as CPT / 2 words.
+template <int CPT>
+__device__ __forceinline__ void load_16(const uint16_t* __restrict__ x, int64_t N, int64_t t0, int64_t n0, bool valid,
+                                        uint32_t (&xw)[16][CPT / 2]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const uint32_t w = word_of(xr[i], j >> 1);
-        v[i] = (j & 1) ? bf16_hi(w) : bf16_lo(w);
+        if (CPT == 8) {
+            const uint4 v = valid ? __ldcs(reinterpret_cast<const uint4*>(x + (t0 + i) * N + n0)) : make_uint4(0u, 0u, 0u, 0u);
+            xw[i][0] = v.x; xw[i][1] = v.y; xw[i][CPT / 2 - 2] = v.z; xw[i][CPT / 2 - 1] = v.w;
+        } else {
+            const uint2 v = valid ? __ldcs(reinterpret_cast<const uint2*>(x + (t0 + i) * N + n0)) : make_uint2(0u, 0u);
+            xw[i][0] = v.x; xw[i][CPT / 2 - 1] = v.y;
+        }
     }
+}
+
+// Column j of the micro-tile as 16 floats, optionally transformed and re-rounded to BF16.
+template <bool RHT, int CPT>
+__device__ __forceinline__ void column_values(const uint32_t (&xw)[16][CPT / 2], int j, uint32_t signmask, float v[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = (j & 1) ? bf16_hi(xw[i][j >> 1]) : bf16_lo(xw[i][j >> 1]);
     if (RHT) {
         rht16_inplace(v, signmask);
 #pragma unroll
@@ -208,32 +210,39 @@ __device__ __forceinline__ void column_values(const uint4 xr[16], int j, uint32_
     }
 }
 
+// Tensor amax of the (transformed) input.  With the transform, the maximum is taken over the FP32
+// butterfly outputs and scaled by 1/4 and rounded to BF16 once: both steps are monotone in the
+// magnitude, so this equals the maximum of the rounded transformed values.
 template <bool RHT>
 __global__ void __launch_bounds__(CW_THREADS)
 colwise_amax_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint32_t signmask,
                     uint32_t* __restrict__ amax_out) {
+    constexpr int CPT = 4;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t0 = (int64_t)blockIdx.y * CW_TOK + warp * 16;
-    const int64_t n0 = (int64_t)blockIdx.x * CW_COLS + lane * 8;
+    const int64_t n0 = (int64_t)blockIdx.x * (32 * CPT) + lane * CPT;
     const bool valid = (t0 < T) && (n0 < N);
-    uint4 xr[16];
-    load_16x8(x, N, t0, n0, valid, xr);
+    uint32_t xw[16][CPT / 2];
+    load_16<CPT>(x, N, t0, n0, valid, xw);
     uint32_t m = 0;
     if (RHT) {
+        float mf = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < CPT; ++j) {
             float v[16];
-            column_values<true>(xr, j, signmask, v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+            for (int i = 0; i < 16; ++i) v[i] = (j & 1) ? bf16_hi(xw[i][j >> 1]) : bf16_lo(xw[i][j >> 1]);
+            rht16_unscaled(v, signmask);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mf = fmaxf(mf, fabsf(v[i]));
         }
+        m = (pack_bf16x2(__fmul_rn(mf, 0.25f), 0.0f) & 0xFFFFu) << 16;
     } else {
         uint32_t m2 = 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            m2 = absmax_bf16x2(m2, xr[i].x); m2 = absmax_bf16x2(m2, xr[i].y);
-            m2 = absmax_bf16x2(m2, xr[i].z); m2 = absmax_bf16x2(m2, xr[i].w);
-        }
+        for (int i = 0; i < 16; ++i)
+#pragma unroll
+            for (int w = 0; w < CPT / 2; ++w) m2 = absmax_bf16x2(m2, xw[i][w]);
         m = fold_halves(m2) << 16;
     }
     m = __reduce_max_sync(0xFFFFFFFFu, m);
@@ -247,38 +256,40 @@ colwise_amax_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint32
     }
 }
 
-template <bool RHT, bool SR>
-__global__ void __launch_bounds__(CW_THREADS, 2)
+template <bool RHT, bool SR, int CPT>
+__global__ void __launch_bounds__(CW_THREADS, CPT == 8 ? 2 : 3)
 colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint32_t signmask,
                      const uint32_t* __restrict__ tensor_amax, uint64_t sr_seed,
                      uint8_t* __restrict__ q, uint8_t* __restrict__ s, float* __restrict__ s_tensor) {
-    __shared__ uint8_t ss[CW_TOK / 16][CW_COLS];                     // block scales: [token block][column]
+    static_assert(!SR || CPT == 8, "one Philox block covers 8 columns");
+    constexpr int COLS = 32 * CPT;
+    __shared__ uint8_t ss[CW_TOK / 16][COLS];                         // block scales: [token block][column]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tb0 = (int64_t)blockIdx.y * CW_TOK;
-    const int64_t cb0 = (int64_t)blockIdx.x * CW_COLS;
+    const int64_t cb0 = (int64_t)blockIdx.x * COLS;
     const int64_t t0 = tb0 + warp * 16;
-    const int64_t n0 = cb0 + lane * 8;
+    const int64_t n0 = cb0 + lane * CPT;
     const bool valid = (t0 < T) && (n0 < N);
 
     const float S = nvfp4_second_scale(__uint_as_float(*tensor_amax));
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *s_tensor = S;
 
-    uint4 xr[16];
-    load_16x8(x, N, t0, n0, valid, xr);
+    uint32_t xw[16][CPT / 2];
+    load_16<CPT>(x, N, t0, n0, valid, xw);
 
     // Phase A, per column j: (transform and re-round in place,) block amax, block scale, reciprocal.
-    float rcp[8];
+    float rcp[CPT];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < CPT; ++j) {
         float v[16];
-        column_values<RHT>(xr, j, signmask, v);
+        column_values<RHT, CPT>(xw, j, signmask, v);
         if (RHT) {
             // store the BF16-rounded transformed values back in place of the inputs
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                uint32_t* w = (j >> 1) == 0 ? &xr[i].x : ((j >> 1) == 1 ? &xr[i].y : ((j >> 1) == 2 ? &xr[i].z : &xr[i].w));
+                uint32_t& w = xw[i][j >> 1];
                 const uint32_t b = __float_as_uint(v[i]) >> 16;
-                *w = (j & 1) ? ((*w & 0x0000FFFFu) | (b << 16)) : ((*w & 0xFFFF0000u) | b);
+                w = (j & 1) ? ((w & 0x0000FFFFu) | (b << 16)) : ((w & 0xFFFF0000u) | b);
             }
         }
         uint32_t m = 0;
@@ -286,7 +297,7 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
         for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
         const uint32_t bs = nvfp4_block_scale(__uint_as_float(m), S);
         rcp[j] = nvfp4_block_recip(bs, S);
-        ss[warp][lane * 8 + j] = (uint8_t)bs;
+        ss[warp][lane * CPT + j] = (uint8_t)bs;
         if (!SR) {
             float p[16];
 #pragma unroll
@@ -299,17 +310,17 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
     if (SR) {
         // Phase B, per row i: one Philox block covers the row's 8 columns (elements t * N + n0 .. + 7)
         const uint32_t k0 = (uint32_t)sr_seed, k1 = (uint32_t)(sr_seed >> 32);
-        uint32_t code[8][2];
+        uint32_t code[CPT][2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) { code[j][0] = 0u; code[j][1] = 0u; }
+        for (int j = 0; j < CPT; ++j) { code[j][0] = 0u; code[j][1] = 0u; }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const uint64_t blk = ((uint64_t)(t0 + i) * (uint64_t)N + (uint64_t)n0) >> 3;
             const U4 r4 = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, k0, k1);
             const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t w = word_of(xr[i], j >> 1);
+            for (int j = 0; j < CPT; ++j) {
+                const uint32_t w = xw[i][j >> 1];
                 const float v = (j & 1) ? bf16_hi(w) : bf16_lo(w);
                 const uint32_t bits = (j & 1) ? (rw[j >> 1] >> 16) : (rw[j >> 1] & 0xFFFFu);
                 code[j][i >> 3] |= e2m1_sr(__fmul_rn(v, rcp[j]), bits) << (4 * (i & 7));
@@ -317,7 +328,7 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
         }
         if (valid) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+            for (int j = 0; j < CPT; ++j)
                 __stcs(reinterpret_cast<uint2*>(q + (n0 + j) * (T / 2) + t0 / 2), make_uint2(code[j][0], code[j][1]));
         }
     }
@@ -326,7 +337,7 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
     // scales: column col gets the 8 block scales of this CTA's 128 tokens (two words of the layout)
     const int64_t ntok = min64(CW_TOK, T - tb0);      // multiple of 16
     const int64_t nct = sf_col_tiles(T, 16);
-    for (int idx = threadIdx.x; idx < CW_COLS * 2; idx += CW_THREADS) {
+    for (int idx = threadIdx.x; idx < COLS * 2; idx += CW_THREADS) {
         const int col = idx >> 1, half = idx & 1;
         const int64_t n = cb0 + col;
         const int64_t kb = tb0 / 16 + half * 4;
@@ -373,14 +384,14 @@ rht16_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint32_t sign
     const int64_t ncg = N / 8;
     const int64_t t0 = (gid / ncg) * 16, n0 = (gid % ncg) * 8;
     if (t0 >= T) return;
-    uint4 xr[16];
-    load_16x8(x, N, t0, n0, true, xr);
+    uint32_t xw[16][4];
+    load_16<8>(x, N, t0, n0, true, xw);
     uint32_t out[16][4];
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
         float a[16], b[16];
-        column_values<true>(xr, j, signmask, a);
-        column_values<true>(xr, j + 1, signmask, b);
+        column_values<true, 8>(xw, j, signmask, a);
+        column_values<true, 8>(xw, j + 1, signmask, b);
 #pragma unroll
         for (int i = 0; i < 16; ++i) out[i][j >> 1] = pack_bf16x2(a[i], b[i]);
     }
@@ -565,14 +576,15 @@ cudaError_t launch_nvfp4_1x16(const uint16_t* x, int64_t T, int64_t N, bool colw
     }
     if (colwise) {
         const uint32_t mask = rht ? host_rht_sign_mask(rht_seed) : 0u;
-        dim3 grid((unsigned)((N + CW_COLS - 1) / CW_COLS), (unsigned)((T + CW_TOK - 1) / CW_TOK));
-        if (rht) colwise_amax_kernel<true><<<grid, CW_THREADS, 0, stream>>>(x, T, N, mask, ws);
-        else colwise_amax_kernel<false><<<grid, CW_THREADS, 0, stream>>>(x, T, N, mask, ws);
+        const unsigned gt = (unsigned)((T + CW_TOK - 1) / CW_TOK);
+        const dim3 grid4((unsigned)((N + 127) / 128), gt), grid8((unsigned)((N + 255) / 256), gt);
+        if (rht) colwise_amax_kernel<true><<<grid4, CW_THREADS, 0, stream>>>(x, T, N, mask, ws);
+        else colwise_amax_kernel<false><<<grid4, CW_THREADS, 0, stream>>>(x, T, N, mask, ws);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if (rht && sr) colwise_quant_kernel<true, true><<<grid, CW_THREADS, 0, stream>>>(x, T, N, mask, ws, sr_seed, q, s, s_tensor);
-        else if (rht) colwise_quant_kernel<true, false><<<grid, CW_THREADS, 0, stream>>>(x, T, N, mask, ws, sr_seed, q, s, s_tensor);
-        else if (sr) colwise_quant_kernel<false, true><<<grid, CW_THREADS, 0, stream>>>(x, T, N, mask, ws, sr_seed, q, s, s_tensor);
-        else colwise_quant_kernel<false, false><<<grid, CW_THREADS, 0, stream>>>(x, T, N, mask, ws, sr_seed, q, s, s_tensor);
+        if (rht && sr) colwise_quant_kernel<true, true, 8><<<grid8, CW_THREADS, 0, stream>>>(x, T, N, mask, ws, sr_seed, q, s, s_tensor);
+        else if (rht) colwise_quant_kernel<true, false, 4><<<grid4, CW_THREADS, 0, stream>>>(x, T, N, mask, ws, sr_seed, q, s, s_tensor);
+        else if (sr) colwise_quant_kernel<false, true, 8><<<grid8, CW_THREADS, 0, stream>>>(x, T, N, mask, ws, sr_seed, q, s, s_tensor);
+        else colwise_quant_kernel<false, false, 4><<<grid4, CW_THREADS, 0, stream>>>(x, T, N, mask, ws, sr_seed, q, s, s_tensor);
     } else {
         amax_kernel<<<num_sms * 4, 256, 0, stream>>>(x, T * N, ws);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
