@@ -229,6 +229,12 @@ class MoE:
         self.dq_d = torch.empty((G * O2, F), dtype=torch.bfloat16, device=dev)
         self.launches_per_step = 10
 
+    def gemm_min_bytes(self, N, K):
+        """HBM bytes a grouped NVFP4 GEMM cannot avoid: A and B codes and block scales read once, the
+        FP32 row and group scales, the BF16 output written once."""
+        R, G = self.rows, self.G
+        return R * K * (0.5 + 1 / 16) + G * N * K * (0.5 + 1 / 16) + 4 * R + 4 * G + 2 * R * N
+
     def ops(self):
         mx, F4 = self.mx, self.mx.MX_FMT_NVFP4
         G, H, F, O1, O2, R = self.G, self.H, self.F, self.O1, self.O2, self.rows
@@ -243,13 +249,15 @@ class MoE:
              lambda: mx.mx_nvfp4_quantize_weight_2d(self.wd, w["q_row"], w["s_row"], w["q_col"], w["s_col"], w["s_w"], w["ws"])),
             ("gemm4", "grouped gate_up", 0, 2.0 * R * O1 * H,
              lambda: mx.mx_grouped_scaled_gemm(F4, self.offs, self.qa["q"], self.qa["s"], self.qa["s2"], q["q_row"],
-                                               q["s_row"], q["s_w"], O1, H, self.y1)),
+                                               q["s_row"], q["s_w"], O1, H, self.y1),
+             self.gemm_min_bytes(O1, H)),
             ("quant", "nvfp4_per_token down input", 1, R * F * (2 + 0.5 + 1 / 16) + 4 * R,
              lambda: mx.mx_nvfp4_quantize_per_token_grouped(self.down_in, self.offs, self.qdn["q"], self.qdn["s"],
                                                             self.qdn["s2"])),
             ("gemm4", "grouped down", 0, 2.0 * R * O2 * F,
              lambda: mx.mx_grouped_scaled_gemm(F4, self.offs, self.qdn["q"], self.qdn["s"], self.qdn["s2"], w["q_row"],
-                                               w["s_row"], w["s_w"], O2, F, self.y2)),
+                                               w["s_row"], w["s_w"], O2, F, self.y2),
+             self.gemm_min_bytes(O2, F)),
             ("dq", "dequantize gate_up DQ(Q(w))", 1, G * O1 * H * (0.5 + 1 / 16 + 2),
              lambda: mx.mx_dequantize_bf16(F4, q["q_row"], q["s_row"], q["s_w"], mx.MX_SCOPE_GROUP, G * O1, H, self.dq_gu,
                                            group_rows=O1)),
@@ -447,16 +455,28 @@ def time_ops(ops, torch, steps, warmup):
 
 
 def op_report(ops, per_op, peaks):
-    """Achieved rate and roofline fraction per op (bytes ops vs HBM, FP4 GEMMs vs the FP4 peak)."""
+    """Achieved rate and roofline fraction per op: byte-moving ops against the HBM copy bandwidth;
+    FP4 GEMMs against the FP4 peak and, when the op carries its minimum HBM traffic (a sixth tuple
+    element: operand codes and scales read once, output written once), against the memory roofline
+    too -- the bound is whichever of the two takes longer at peak."""
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     rep, by_kind = {}, {}
-    for (kind, label, is_bytes, units, _), ms in zip(ops, per_op):
+    for op, ms in zip(ops, per_op):
+        kind, label, is_bytes, units = op[:4]
+        mem = op[5] if len(op) > 5 else None
         if is_bytes:
             ach = units / (ms / 1e3) / 1e9
             rep[label] = {"ms": round(ms, 4), "GBps": round(ach, 1), "frac_hbm": round(ach / peaks["hbm_gbs"], 4)}
         else:
             ach = units / (ms / 1e3) / 1e12
             rep[label] = {"ms": round(ms, 4), "TFLOPs": round(ach, 1), "frac_fp4_peak": round(ach / fp4_peak, 4)}
+            if mem:
+                t_flop = units / (fp4_peak * 1e12) * 1e3
+                t_mem = mem / (peaks["hbm_gbs"] * 1e9) * 1e3
+                rep[label].update({"min_hbm_bytes": int(mem), "GBps": round(mem / (ms / 1e3) / 1e9, 1),
+                                   "frac_hbm": round(mem / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                   "bound": "hbm" if t_mem > t_flop else "tensor",
+                                   "frac_roofline": round(max(t_flop, t_mem) / ms, 4)})
         k = by_kind.setdefault(kind, [0.0, 0.0, is_bytes])
         k[0] += ms
         k[1] += units
