@@ -24,6 +24,7 @@ namespace {
 // ------------------------------------------------------------------------------------------------
 constexpr int RW_WARPS = 8;
 constexpr int RW_MAXB = 4;     // blocks per lane kept in registers (H <= 2048)
+constexpr int RW_CTAS_PER_SM = 4;   // 64 registers: resident warps hide the block-scale division chains
 
 // Quantize one 16-element block held in two 16-byte words; returns the 8 code bytes.
 template <bool SR>
@@ -56,7 +57,7 @@ __device__ __forceinline__ uint2 quant_block16(const uint4& a, const uint4& b, f
 }
 
 template <bool PER_TENSOR, bool SR, bool GROUPED, int LPR>
-__global__ void __launch_bounds__(RW_WARPS * 32)
+__global__ void __launch_bounds__(RW_WARPS * 32, RW_CTAS_PER_SM)
 nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64_t ldx,
                      uint8_t* __restrict__ q, uint8_t* __restrict__ s, float* __restrict__ s_tok,
                      const uint32_t* __restrict__ tensor_amax, float* __restrict__ s_tensor, uint64_t sr_seed,
@@ -83,24 +84,35 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
         const bool row_ok = t < T;                   // the warp stays converged for the shuffles below
         const uint4* xr = reinterpret_cast<const uint4*>(x + (row_ok ? t : tw) * ldx);
         uint4 ra[RW_MAXB], rb[RW_MAXB];
+        uint32_t bam[RW_MAXB];                       // block amax bits of the cached blocks
         float S;
         if (PER_TENSOR) {
             S = nvfp4_second_scale(__uint_as_float(*tensor_amax));
             if (t == 0 && sub == 0) *s_tensor = S;
-        } else {
-            uint32_t m2 = 0;
-            if (cached) {
+        }
+        if (cached) {
+            uint32_t m = 0;
 #pragma unroll
-                for (int i = 0; i < RW_MAXB; ++i) {
-                    const int64_t b = sub + LPR * i;
-                    ra[i] = rb[i] = make_uint4(0u, 0u, 0u, 0u);
-                    if (row_ok && b < nblk) { ra[i] = __ldcs(xr + 2 * b); rb[i] = __ldcs(xr + 2 * b + 1); }
-                    m2 = absmax_bf16x2(m2, ra[i].x); m2 = absmax_bf16x2(m2, ra[i].y);
-                    m2 = absmax_bf16x2(m2, ra[i].z); m2 = absmax_bf16x2(m2, ra[i].w);
-                    m2 = absmax_bf16x2(m2, rb[i].x); m2 = absmax_bf16x2(m2, rb[i].y);
-                    m2 = absmax_bf16x2(m2, rb[i].z); m2 = absmax_bf16x2(m2, rb[i].w);
-                }
-            } else if (row_ok) {
+            for (int i = 0; i < RW_MAXB; ++i) {
+                const int64_t b = sub + LPR * i;
+                ra[i] = rb[i] = make_uint4(0u, 0u, 0u, 0u);
+                if (row_ok && b < nblk) { ra[i] = __ldcs(xr + 2 * b); rb[i] = __ldcs(xr + 2 * b + 1); }
+                uint32_t m2 = 0;
+                m2 = absmax_bf16x2(m2, ra[i].x); m2 = absmax_bf16x2(m2, ra[i].y);
+                m2 = absmax_bf16x2(m2, ra[i].z); m2 = absmax_bf16x2(m2, ra[i].w);
+                m2 = absmax_bf16x2(m2, rb[i].x); m2 = absmax_bf16x2(m2, rb[i].y);
+                m2 = absmax_bf16x2(m2, rb[i].z); m2 = absmax_bf16x2(m2, rb[i].w);
+                bam[i] = fold_halves(m2);
+                m = max(m, bam[i]);
+            }
+            if (!PER_TENSOR) {
+                const uint32_t amax16 = __reduce_max_sync(gmask, m);
+                S = nvfp4_second_scale(__uint_as_float(amax16 << 16));
+                if (row_ok && sub == 0) s_tok[t] = S;
+            }
+        } else if (!PER_TENSOR) {
+            uint32_t m2 = 0;
+            if (row_ok) {
                 for (int64_t b = sub; b < nblk; b += LPR) {
                     const uint4 a = __ldg(xr + 2 * b), c = __ldg(xr + 2 * b + 1);
                     m2 = absmax_bf16x2(m2, a.x); m2 = absmax_bf16x2(m2, a.y);
@@ -114,28 +126,11 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
             if (row_ok && sub == 0) s_tok[t] = S;
         }
         const int64_t srow = (GROUPED && row_ok) ? grouped_scale_row(s_off, s_ptile, G, t) : t;
-        const int64_t nrounds = (nblk + LPR - 1) / LPR;
-        for (int64_t i = 0; i < nrounds; ++i) {
-            const int64_t b = sub + LPR * i;
-            const bool valid = row_ok && b < nblk;
-            uint4 a, c;
-            if (!PER_TENSOR && cached && i < RW_MAXB) {
-                // static register index: unrolled selection keeps ra/rb in registers
-                a = ra[0]; c = rb[0];
-#pragma unroll
-                for (int k = 1; k < RW_MAXB; ++k) if (i == k) { a = ra[k]; c = rb[k]; }
-            } else {
-                a = c = make_uint4(0u, 0u, 0u, 0u);
-                if (valid) { a = __ldcs(xr + 2 * b); c = __ldcs(xr + 2 * b + 1); }
-            }
-            uint32_t m2 = 0;
-            m2 = absmax_bf16x2(m2, a.x); m2 = absmax_bf16x2(m2, a.y); m2 = absmax_bf16x2(m2, a.z); m2 = absmax_bf16x2(m2, a.w);
-            m2 = absmax_bf16x2(m2, c.x); m2 = absmax_bf16x2(m2, c.y); m2 = absmax_bf16x2(m2, c.z); m2 = absmax_bf16x2(m2, c.w);
-            const uint32_t bs = nvfp4_block_scale(__uint_as_float(fold_halves(m2) << 16), S);
-            const float r = nvfp4_block_recip(bs, S);
+
+        // codes, and the four consecutive block scales of lanes 4m .. 4m+3 of the row group as one word
+        auto emit = [&](int64_t b, bool valid, const uint4& a, const uint4& c, uint32_t bs, float r) {
             const uint2 codes = quant_block16<SR>(a, c, r, (uint64_t)t * (uint64_t)H + (uint64_t)b * 16, k0, k1);
             if (valid) __stcs(reinterpret_cast<uint2*>(q + t * (H / 2) + b * 8), codes);
-            // four consecutive block scales (lanes 4m .. 4m+3 of the row group) form one word
             const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 1);
             const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
             const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 3);
@@ -147,6 +142,37 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
                     const uint32_t bb[4] = {bs, b1, b2, b3};
                     for (int k = 0; k < (int)(nblk - b); ++k) p[k] = (uint8_t)bb[k];
                 }
+            }
+        };
+        if (cached) {
+            // all block scales first: the lane's independent scale chains overlap
+            uint32_t bsv[RW_MAXB];
+            float rv[RW_MAXB];
+#pragma unroll
+            for (int i = 0; i < RW_MAXB; ++i) {
+                bsv[i] = nvfp4_block_scale(__uint_as_float(bam[i] << 16), S);
+                rv[i] = nvfp4_block_recip(bsv[i], S);
+            }
+            const int64_t nrounds = (nblk + LPR - 1) / LPR;
+#pragma unroll
+            for (int i = 0; i < RW_MAXB; ++i) {
+                if (i < nrounds) {                  // warp-uniform
+                    const int64_t b = sub + LPR * i;
+                    emit(b, row_ok && b < nblk, ra[i], rb[i], bsv[i], rv[i]);
+                }
+            }
+        } else {
+            const int64_t nrounds = (nblk + LPR - 1) / LPR;
+            for (int64_t i = 0; i < nrounds; ++i) {
+                const int64_t b = sub + LPR * i;
+                const bool valid = row_ok && b < nblk;
+                uint4 a = make_uint4(0u, 0u, 0u, 0u), c = make_uint4(0u, 0u, 0u, 0u);
+                if (valid) { a = __ldcs(xr + 2 * b); c = __ldcs(xr + 2 * b + 1); }
+                uint32_t m2 = 0;
+                m2 = absmax_bf16x2(m2, a.x); m2 = absmax_bf16x2(m2, a.y); m2 = absmax_bf16x2(m2, a.z); m2 = absmax_bf16x2(m2, a.w);
+                m2 = absmax_bf16x2(m2, c.x); m2 = absmax_bf16x2(m2, c.y); m2 = absmax_bf16x2(m2, c.z); m2 = absmax_bf16x2(m2, c.w);
+                const uint32_t bs = nvfp4_block_scale(__uint_as_float(fold_halves(m2) << 16), S);
+                emit(b, valid, a, c, bs, nvfp4_block_recip(bs, S));
             }
         }
     }
