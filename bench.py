@@ -271,6 +271,73 @@ class MoE:
                 "tokens": 8192, "routed_rows": self.rows, "experts": self.G, "hidden": self.H, "ffn": self.F}
 
 
+class MoE8(MoE):
+    """The same Qwen3-30B-A3B expert layer with MXFP8 instead of NVFP4: row-wise MXFP8 of the 65536
+    expert-sorted rows (grouped scale layout) and of the 128 experts' stacked gate|up and down weights,
+    the two grouped MXFP8 GEMMs, row-wise MXFP8 of the down-projection input."""
+    name = "moe_mxfp8"
+    dtype = "e4m3 (f32 accumulate, bf16 out)"
+
+    def __init__(self, mx, torch, dev, experts=128):
+        import synthetic
+        self.mx, self.torch, self.dev = mx, torch, dev
+        d = synthetic.moe(experts=experts)
+        bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        x = bf(d["x"])
+        self.rows = int(d["group_offsets"][-1])
+        self.a = x.index_select(0, torch.from_numpy(d["row_token"]).to(dev)).contiguous()
+        self.down_in = bf(d["down_in"])
+        G, O1, H = d["w_gate_up"].shape
+        _, O2, F = d["w_down"].shape
+        self.wgu = bf(d["w_gate_up"]).reshape(G * O1, H)
+        self.wd = bf(d["w_down"]).reshape(G * O2, F)
+        self.offs = torch.from_numpy(d["group_offsets"]).to(dev)
+        self.G, self.H, self.F, self.O1, self.O2 = G, H, F, O1, O2
+        u8 = lambda n: torch.zeros(n, dtype=torch.uint8, device=dev)
+        R = self.rows
+        self.qa, self.sa = torch.empty((R, H), dtype=torch.uint8, device=dev), u8(mx.grouped_scale_bytes(R, G, H, 32))
+        self.qdn, self.sdn = torch.empty((R, F), dtype=torch.uint8, device=dev), u8(mx.grouped_scale_bytes(R, G, F, 32))
+        self.qgu = mx.alloc_mxfp8(G * O1, H, dev, rowwise=True, colwise=False)
+        self.qwd = mx.alloc_mxfp8(G * O2, F, dev, rowwise=True, colwise=False)
+        self.y1 = torch.empty((R, O1), dtype=torch.bfloat16, device=dev)
+        self.y2 = torch.empty((R, O2), dtype=torch.bfloat16, device=dev)
+        self.launches_per_step = 6
+
+    def gemm_min_bytes(self, N, K):
+        """HBM bytes a grouped MXFP8 GEMM cannot avoid: A and B codes and scales read once, the BF16
+        output written once."""
+        R, G = self.rows, self.G
+        return R * K * (1 + 1 / 32) + G * N * K * (1 + 1 / 32) + 2 * R * N
+
+    def ops(self):
+        mx, F8 = self.mx, self.mx.MX_FMT_MXFP8
+        G, H, F, O1, O2, R = self.G, self.H, self.F, self.O1, self.O2, self.rows
+        per = 2 + 1 + 1 / 32
+        return [
+            ("quant", "mxfp8 routed rows A", 1, R * H * per,
+             lambda: mx.mx_quantize_mxfp8_grouped(self.a, self.offs, self.qa, self.sa)),
+            ("quant", "mxfp8 weights gate_up", 1, G * O1 * H * per,
+             lambda: mx.mx_quantize_mxfp8(self.wgu, self.qgu["q_row"], self.qgu["s_row"])),
+            ("quant", "mxfp8 weights down", 1, G * O2 * F * per,
+             lambda: mx.mx_quantize_mxfp8(self.wd, self.qwd["q_row"], self.qwd["s_row"])),
+            ("gemm8", "grouped gate_up", 0, 2.0 * R * O1 * H,
+             lambda: mx.mx_grouped_scaled_gemm(F8, self.offs, self.qa, self.sa, None, self.qgu["q_row"],
+                                               self.qgu["s_row"], None, O1, H, self.y1),
+             self.gemm_min_bytes(O1, H)),
+            ("quant", "mxfp8 down input", 1, R * F * per,
+             lambda: mx.mx_quantize_mxfp8_grouped(self.down_in, self.offs, self.qdn, self.sdn)),
+            ("gemm8", "grouped down", 0, 2.0 * R * O2 * F,
+             lambda: mx.mx_grouped_scaled_gemm(F8, self.offs, self.qdn, self.sdn, None, self.qwd["q_row"],
+                                               self.qwd["s_row"], None, O2, F, self.y2),
+             self.gemm_min_bytes(O2, F)),
+        ]
+
+    def config(self):
+        c = super().config()
+        c["workload"] = "moe_mxfp8: Qwen3-30B-A3B expert layer, MXFP8 routed rows + weights + grouped MXFP8 GEMMs"
+        return c
+
+
 class WGrad:
     """Llama-3-8B MLP WGRAD in NVFP4: RHT16 along tokens + 1x16 column-wise quantize with a
     per-tensor scale (SR on dY, RNE on X), then dW = dY^T X over K = 32768 tokens."""
@@ -459,7 +526,6 @@ def op_report(ops, per_op, peaks):
     FP4 GEMMs against the FP4 peak and, when the op carries its minimum HBM traffic (a sixth tuple
     element: operand codes and scales read once, output written once), against the memory roofline
     too -- the bound is whichever of the two takes longer at peak."""
-    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     rep, by_kind = {}, {}
     for op, ms in zip(ops, per_op):
         kind, label, is_bytes, units = op[:4]
@@ -468,10 +534,13 @@ def op_report(ops, per_op, peaks):
             ach = units / (ms / 1e3) / 1e9
             rep[label] = {"ms": round(ms, 4), "GBps": round(ach, 1), "frac_hbm": round(ach / peaks["hbm_gbs"], 4)}
         else:
+            fp8 = kind == "gemm8"
+            peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if fp8 else FP4_OVER_BF16)
             ach = units / (ms / 1e3) / 1e12
-            rep[label] = {"ms": round(ms, 4), "TFLOPs": round(ach, 1), "frac_fp4_peak": round(ach / fp4_peak, 4)}
+            rep[label] = {"ms": round(ms, 4), "TFLOPs": round(ach, 1),
+                          ("frac_fp8_peak" if fp8 else "frac_fp4_peak"): round(ach / peak, 4)}
             if mem:
-                t_flop = units / (fp4_peak * 1e12) * 1e3
+                t_flop = units / (peak * 1e12) * 1e3
                 t_mem = mem / (peaks["hbm_gbs"] * 1e9) * 1e3
                 rep[label].update({"min_hbm_bytes": int(mem), "GBps": round(mem / (ms / 1e3) / 1e9, 1),
                                    "frac_hbm": round(mem / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -518,7 +587,12 @@ def run_workload(args):
                 "gpu_launches": work.launches_per_step * work.layers}
         print(json.dumps(line), flush=True)
         return
-    work = MoE(mx, torch, dev, experts=args.experts) if args.workload == "moe" else WGrad(mx, torch, dev)
+    if args.workload == "moe":
+        work = MoE(mx, torch, dev, experts=args.experts)
+    elif args.workload == "moe_mxfp8":
+        work = MoE8(mx, torch, dev, experts=args.experts)
+    else:
+        work = WGrad(mx, torch, dev)
     ops = work.ops()
     sampler.start()
     total_ms, per_op = time_ops(ops, torch, args.steps, args.warmup)
@@ -540,13 +614,15 @@ def run_workload(args):
         roof = {"kernel": kind, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None}
     else:
+        ratio = FP8_OVER_BF16 if kind == "gemm8" else FP4_OVER_BF16
+        tpeak = peaks["bf16_tflops"] * ratio
         ach = kunits / (kms / 1e3) / 1e12
-        roof = {"kernel": kind, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp4_peak, 1),
-                "unit": "TFLOP/s", "frac": round(ach / fp4_peak, 4), "traffic": None,
-                "peak_source": f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4/BF16)"}
+        roof = {"kernel": kind, "bound": "tensor", "achieved": round(ach, 1), "peak": round(tpeak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / tpeak, 4), "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 burst x {ratio:g} (nominal {'FP8' if ratio == FP8_OVER_BF16 else 'FP4'}/BF16)"}
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "e2m1 (f32 accumulate, bf16 out)", "data": "synthetic (seeded numpy draws)",
+            "vs_baseline": None, "dtype": getattr(work, "dtype", "e2m1 (f32 accumulate, bf16 out)"), "data": "synthetic (seeded numpy draws)",
             "config": work.config(), "per_op": rep, "aux": aux, "roofline": roof, "clocks": clocks,
             "gpu_launches": work.launches_per_step * args.steps}
     print(json.dumps(line), flush=True)
@@ -743,7 +819,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mxnum", "reference"], default="mxnum")
-    ap.add_argument("--workload", choices=["dense_mlp", "moe", "wgrad", "weight_sync"], default="dense_mlp")
+    ap.add_argument("--workload", choices=["dense_mlp", "moe", "moe_mxfp8", "wgrad", "weight_sync"], default="dense_mlp")
     ap.add_argument("--layers", type=int, default=48, help="weight_sync: layers swept")
     ap.add_argument("--experts", type=int, default=128, help="moe / weight_sync: experts (fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -169,6 +169,50 @@ def test_moe_weights_grouped_gemm_and_dq_sampled(orc, moe):
 
 
 # ------------------------------------------------------------------------------------------------
+# moe with MXFP8: the same expert layer, routed rows and expert weights in MXFP8, grouped MXFP8 GEMM
+# ------------------------------------------------------------------------------------------------
+@pytest.fixture(scope="module")
+def moe8(mx):
+    d = synthetic.moe()
+    rows = int(d["group_offsets"][-1])
+    x = bf16_dev(d["x"])
+    a = x.index_select(0, torch.from_numpy(d["row_token"]).to(DEV)).contiguous()
+    G, O1, H = d["w_gate_up"].shape
+    offs = torch.from_numpy(d["group_offsets"]).to(DEV)
+    qa = torch.empty((rows, H), dtype=torch.uint8, device=DEV)
+    sa = torch.zeros(mx.grouped_scale_bytes(rows, G, H, 32), dtype=torch.uint8, device=DEV)
+    mx.mx_quantize_mxfp8_grouped(a, offs, qa, sa)
+    qw = mx.alloc_mxfp8(G * O1, H, DEV, rowwise=True, colwise=False)     # the G matrices stacked
+    mx.mx_quantize_mxfp8(bf16_dev(d["w_gate_up"].reshape(G * O1, H)), qw["q_row"], qw["s_row"])
+    y = torch.empty((rows, O1), dtype=torch.bfloat16, device=DEV)
+    mx.mx_grouped_scaled_gemm(mx.MX_FMT_MXFP8, offs, qa, sa, None, qw["q_row"], qw["s_row"], None, O1, H, y)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    return {"d": d, "qa": qa, "sa": sa, "qw": qw, "y": y, "G": G, "O1": O1, "H": H}
+
+
+def test_moe_mxfp8_grouped_gemm_sampled(orc, moe8):
+    d, G, O1, H = moe8["d"], moe8["G"], moe8["O1"], moe8["H"]
+    offs = d["group_offsets"]
+    y = moe8["y"].float().cpu().numpy()
+    qw, sw_laid = to_np(moe8["qw"]["q_row"]).reshape(G, O1, H), to_np(moe8["qw"]["s_row"])
+    srb = orc.scale_layout_bytes(O1, H // 32)
+    ptile = np.concatenate([[0], np.cumsum((np.diff(offs) + 127) // 128)])
+    sa_laid = orc.scales_from_gemm_layout(to_np(moe8["sa"]), int(ptile[-1]) * 128, H // 32)
+    for g in (0, 77, G - 1):
+        qb, sb = orc.mxfp8_quantize_rowwise(np.ascontiguousarray(d["w_gate_up"][g]))
+        assert np.array_equal(qw[g], qb), g
+        assert np.array_equal(sw_laid[g * srb:(g + 1) * srb], orc.scales_to_gemm_layout(sb)), g
+        r0, r1 = int(offs[g]), int(offs[g + 1])
+        qa, sa = orc.mxfp8_quantize_rowwise(np.ascontiguousarray(d["x"][d["row_token"][r0:r1]]))
+        assert np.array_equal(to_np(moe8["qa"])[r0:r1], qa), g
+        assert np.array_equal(sa_laid[ptile[g] * 128:ptile[g] * 128 + (r1 - r0)], sa), g
+        A, B = orc.decode_mxfp8_f64(qa, sa), orc.decode_mxfp8_f64(qb, sb)
+        cols = np.sort(np.random.default_rng(1000 + g).choice(O1, 128, replace=False))
+        check_block(orc, y[r0:r1][:, cols], A @ B[cols].T, np.abs(A) @ np.abs(B[cols]).T)
+
+
+# ------------------------------------------------------------------------------------------------
 # wgrad: Llama-3-8B WGRAD, RHT16 + column-wise NVFP4 (SR on dY) + NVFP4 GEMM
 # ------------------------------------------------------------------------------------------------
 def test_wgrad_fullsize_sampled(mx, orc):
