@@ -78,6 +78,8 @@ def _load():
                 "orc_nvfp4_block_recip": (ctypes.c_float, [ctypes.c_uint8, ctypes.c_float]),
                 "orc_nvfp4_quantize_per_token": (None, [P, I64, I64, I64, P, P, P]),
                 "orc_nvfp4_quantize_weight_2d": (None, [P, I64, I64, P, P, P, P]),
+                "orc_nvfp4_quantize_weight_2d_46": (None, [P, I64, I64, P, P, P, P]),
+                "orc_nvfp4_quantize_per_token_46": (None, [P, I64, I64, I64, P, P, P]),
                 "orc_rht16": (None, [P, I64, I64, U64, P]),
                 "orc_nvfp4_quantize_1x16": (None, [P, I64, I64, ctypes.c_int, ctypes.c_int, U64,
                                                    ctypes.c_int, U64, P, P, P]),
@@ -289,6 +291,31 @@ def nvfp4_quantize_weight_2d(w: np.ndarray):
     st = np.zeros((O // 16, H // 16), dtype=np.uint8)
     sw = np.zeros(1, dtype=np.float32)
     _load().orc_nvfp4_quantize_weight_2d(_p(w), O, H, _p(q_row), _p(q_col), _p(st), _p(sw))
+    return q_row, q_col, st, np.float32(sw[0])
+
+
+def nvfp4_quantize_per_token_46(x: np.ndarray):
+    """Per-token NVFP4 with Four-over-Six block scales (NVIDIA RL blog, "Four-Over-Six"): each block
+    keeps the scale mapping its maximum to 4 or to 6, whichever gives the smaller largest
+    dequantization error (ties keep 6).  Returns as nvfp4_quantize_per_token."""
+    x = _bf16(x)
+    T, H = x.shape
+    q = np.zeros((T, H // 2), dtype=np.uint8)
+    s = np.zeros((T, H // 16), dtype=np.uint8)
+    st = np.zeros(T, dtype=np.float32)
+    _load().orc_nvfp4_quantize_per_token_46(_p(x), T, H, H, _p(q), _p(s), _p(st))
+    return q, s, st
+
+
+def nvfp4_quantize_weight_2d_46(w: np.ndarray):
+    """16x16 2D weight NVFP4 with Four-over-Six tile scales.  Returns as nvfp4_quantize_weight_2d."""
+    w = _bf16(w)
+    O, H = w.shape
+    q_row = np.zeros((O, H // 2), dtype=np.uint8)
+    q_col = np.zeros((H, O // 2), dtype=np.uint8)
+    st = np.zeros((O // 16, H // 16), dtype=np.uint8)
+    sw = np.zeros(1, dtype=np.float32)
+    _load().orc_nvfp4_quantize_weight_2d_46(_p(w), O, H, _p(q_row), _p(q_col), _p(st), _p(sw))
     return q_row, q_col, st, np.float32(sw[0])
 
 

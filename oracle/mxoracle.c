@@ -418,6 +418,109 @@ ORC_API void orc_nvfp4_quantize_weight_2d(const uint16_t* w, int64_t O, int64_t 
 }
 
 /* ------------------------------------------------------------------------ */
+/* Four-over-Six ([NVIDIA RL blog] "Four-Over-Six (4/6)": instead of always  */
+/* mapping a block's maximum to the E2M1 maximum 6, map it to 4 or to 6 and  */
+/* keep the lower error; the largest error drops from 1/6 to 1/8 of the      */
+/* range).  Readings: the error is the largest absolute difference between   */
+/* a value and its FP32 dequantization fp32(fp32(value(q) * value(bs)) * S); */
+/* 4 is kept only if strictly better (ties keep the standard 6); S is        */
+/* unchanged (amax / 2688), so consumers of the codes need no change.        */
+/*   bs_m = E4M3( fp32( fp32(amax_b / m) / S ) ),  m in {6, 4}               */
+/* ------------------------------------------------------------------------ */
+
+static uint8_t nvfp4_block_scale_m(float amax_b, float S, float m) {
+    if (S == 0.0f) return 0;
+    float t = amax_b / m;
+    t = t / S;
+    return orc_e4m3_encode((double)t);
+}
+
+/* Codes of n values under block scale bs and second-level scale S, and the largest absolute
+ * dequantization error. */
+static float nvfp4_block_candidate(const float* x, int n, uint8_t bs, float S, uint8_t* codes) {
+    float r = orc_nvfp4_block_recip(bs, S);
+    float bsv = (float)orc_e4m3_value(bs);
+    float err = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float v = x[i] * r;
+        codes[i] = orc_e2m1_encode((double)v);
+        float prod = (float)orc_e2m1_value(codes[i]) * bsv;
+        float deq = prod * S;
+        err = fmaxf(err, fabsf(deq - x[i]));
+    }
+    return err;
+}
+
+/* Chooses between the two candidates for one block of n values (n = 16 or 256); returns the scale,
+ * the codes in codes[]. */
+static uint8_t nvfp4_block_four_over_six(const float* x, int n, float amax_b, float S, uint8_t* codes) {
+    uint8_t c6[256], c4[256];
+    uint8_t bs6 = nvfp4_block_scale_m(amax_b, S, 6.0f);
+    uint8_t bs4 = nvfp4_block_scale_m(amax_b, S, 4.0f);
+    float e6 = nvfp4_block_candidate(x, n, bs6, S, c6);
+    float e4 = nvfp4_block_candidate(x, n, bs4, S, c4);
+    int four = e4 < e6;
+    memcpy(codes, four ? c4 : c6, (size_t)n);
+    return four ? bs4 : bs6;
+}
+
+/* Per-token 1x16 with 4/6 block scales; arguments as orc_nvfp4_quantize_per_token. */
+ORC_API void orc_nvfp4_quantize_per_token_46(const uint16_t* x, int64_t T, int64_t H, int64_t ldx,
+                                             uint8_t* q, uint8_t* s, float* s_tok) {
+    int64_t nb = H / 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t* xr = x + t * ldx;
+        float amax = 0.0f;
+        for (int64_t k = 0; k < H; ++k) amax = fmaxf(amax, fabsf(bf16_to_float(xr[k])));
+        float S = orc_nvfp4_second_scale(amax);
+        s_tok[t] = S;
+        uint8_t* qr = q + t * (H / 2);
+        for (int64_t b = 0; b < nb; ++b) {
+            float xv[16], ab = 0.0f;
+            for (int i = 0; i < 16; ++i) {
+                xv[i] = bf16_to_float(xr[b * 16 + i]);
+                ab = fmaxf(ab, fabsf(xv[i]));
+            }
+            uint8_t codes[16];
+            s[t * nb + b] = nvfp4_block_four_over_six(xv, 16, ab, S, codes);
+            for (int i = 0; i < 16; ++i) put_nibble(qr, b * 16 + i, codes[i]);
+        }
+    }
+}
+
+/* 16x16 2D weights with 4/6 tile scales; arguments as orc_nvfp4_quantize_weight_2d.  A tile's values
+ * are taken row by row (the error is a maximum, so the order does not matter). */
+ORC_API void orc_nvfp4_quantize_weight_2d_46(const uint16_t* w, int64_t O, int64_t H,
+                                             uint8_t* q_row, uint8_t* q_col, uint8_t* s_tile, float* s_w) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < O * H; ++i) amax = fmaxf(amax, fabsf(bf16_to_float(w[i])));
+    float S = orc_nvfp4_second_scale(amax);
+    *s_w = S;
+    int64_t to = O / 16, th = H / 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t bo = 0; bo < to; ++bo) {
+        for (int64_t bh = 0; bh < th; ++bh) {
+            float xv[256], ab = 0.0f;
+            for (int i = 0; i < 16; ++i)
+                for (int j = 0; j < 16; ++j) {
+                    xv[i * 16 + j] = bf16_to_float(w[(bo * 16 + i) * H + bh * 16 + j]);
+                    ab = fmaxf(ab, fabsf(xv[i * 16 + j]));
+                }
+            uint8_t codes[256];
+            s_tile[bo * th + bh] = nvfp4_block_four_over_six(xv, 256, ab, S, codes);
+            for (int i = 0; i < 16; ++i) {
+                for (int j = 0; j < 16; ++j) {
+                    int64_t o = bo * 16 + i, h = bh * 16 + j;
+                    put_nibble(q_row + o * (H / 2), h, codes[i * 16 + j]);
+                    put_nibble(q_col + h * (O / 2), o, codes[i * 16 + j]);
+                }
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Random Hadamard transform ([MaxText]: applied only to WGRAD inputs).      */
 /* Along the token dim, per column and per aligned 16-token chunk:           */
 /*   v = d * x (exact sign flip); Walsh-Hadamard butterflies with strides    */

@@ -38,12 +38,17 @@ MUTATIONS = {
  'sr_index': ('uint64_t gi = (uint64_t)(t * N_total + n_offset + n);', 'uint64_t gi = (uint64_t)(n * T + t);'),
  'sat448': ('uint8_t c = enumerate_nearest(fabs(v), orc_e4m3_value, 127, 448.0);', 'uint8_t c = enumerate_nearest(fabs(v), orc_e4m3_value, 126, 448.0);'),
  'second_scale': ('static const float NVFP4_S_DIV = 2688.0f;', 'static const float NVFP4_S_DIV = 448.0f;'),
+ 'fos_tie': ('int four = e4 < e6;', 'int four = e4 <= e6;'),
+ 'fos_div4': ('uint8_t bs4 = nvfp4_block_scale_m(amax_b, S, 4.0f);', 'uint8_t bs4 = nvfp4_block_scale_m(amax_b, S, 6.0f);'),
+ 'fos_sum_err': ('        err = fmaxf(err, fabsf(deq - x[i]));', '        err = err + (deq - x[i]) * (deq - x[i]);'),
+ 'fos_no_S': ('        float deq = prod * S;', '        float deq = prod;'),
  'dq_mx_scale': ('* orc_e8m0_value(s[r * (K / 32) + k / 32]);\n            y[r', '* orc_e8m0_value(s[r * (K / 32) + k / 32] + 1);\n            y[r'),
 }
 
 
 PIN_FILES = ["tests/test_oracle_formats.py", "tests/test_oracle_rng_layout.py", "tests/test_oracle_mxfp8.py",
-             "tests/test_oracle_nvfp4.py", "tests/test_oracle_rht_sr.py", "tests/test_oracle_gemm_ref.py"]
+             "tests/test_oracle_nvfp4.py", "tests/test_oracle_rht_sr.py", "tests/test_oracle_gemm_ref.py",
+             "tests/test_oracle_four_over_six.py"]
 
 
 @pytest.fixture(scope="module")
