@@ -271,6 +271,23 @@ class MoE:
                 "tokens": 8192, "routed_rows": self.rows, "experts": self.G, "hidden": self.H, "ffn": self.F}
 
 
+    def aux_ops(self):
+        """Four-over-Six variants of the two NVFP4 quantizers on the same tensors (reported beside the
+        step, not part of it)."""
+        mx, G, H, O1, R = self.mx, self.G, self.H, self.O1, self.rows
+        if not hasattr(self, "q46"):
+            self.q46 = mx.alloc_nvfp4_rows(R, H, self.dev)
+            self.w46 = mx.alloc_nvfp4_weight_2d(G, O1, H, self.dev)
+        q, w = self.q46, self.w46
+        return [
+            ("quant", "nvfp4_per_token 4/6 A", 1, R * H * (2 + 0.5 + 1 / 16) + 4 * R,
+             lambda: mx.mx_nvfp4_quantize_per_token_46(self.a, q["q"], q["s"], q["s2"])),
+            ("quant", "nvfp4_weight_2d 4/6 gate_up", 1, G * O1 * H * (2 + 1 + 2 / 16),
+             lambda: mx.mx_nvfp4_quantize_weight_2d_46(self.wgu, w["q_row"], w["s_row"], w["q_col"], w["s_col"],
+                                                       w["s_w"], w["ws"])),
+        ]
+
+
 class MoE8(MoE):
     """The same Qwen3-30B-A3B expert layer with MXFP8 instead of NVFP4: row-wise MXFP8 of the 65536
     expert-sorted rows (grouped scale layout) and of the 128 experts' stacked gate|up and down weights,
@@ -331,6 +348,9 @@ class MoE8(MoE):
                                                self.qwd["s_row"], None, O2, F, self.y2),
              self.gemm_min_bytes(O2, F)),
         ]
+
+    def aux_ops(self):
+        return []
 
     def config(self):
         c = super().config()

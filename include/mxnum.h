@@ -125,6 +125,24 @@ mx_status mx_nvfp4_quantize_weight_2d(const void* w, int64_t G, int64_t O, int64
                                       float* s_w, void* workspace, size_t workspace_bytes,
                                       cudaStream_t stream);
 
+/* Four-over-Six variants of the two NVFP4 quantizers above.
+ * Source: NVIDIA RL blog, "Four-Over-Six (4/6)" for weights and activations -- instead of always mapping
+ * a block's maximum to the E2M1 maximum 6, map it to 4 or to 6, whichever errs less (the largest
+ * error drops from 1/6 to 1/8 of the range); applied to activations in pretraining and also to
+ * weights in RL.  Readings: per block (1x16 per token, 16x16 for weights) both candidates
+ *   bs_m = E4M3(fp32(fp32(amax_b / m) / S)), m in {6, 4}, codes as above with bs_m,
+ * are formed, and the one with the smaller largest |fp32(fp32(value(q) * value(bs_m)) * S) - x| is kept
+ * (a tie keeps 6).  The FP32 second-level scales are unchanged (amax / 2688), so the codes and scales
+ * are consumed exactly like those of the standard quantizers (GEMMs, dequantize).
+ * Same arguments, sizes, alignment and error rules as mx_nvfp4_quantize_per_token and
+ * mx_nvfp4_quantize_weight_2d. */
+mx_status mx_nvfp4_quantize_per_token_46(const void* x, int64_t T, int64_t H, int64_t ldx, uint8_t* q, uint8_t* s,
+                                         float* s_tok, cudaStream_t stream);
+mx_status mx_nvfp4_quantize_weight_2d_46(const void* w, int64_t G, int64_t O, int64_t H,
+                                         uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                         float* s_w, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream);
+
 /* Allocation-free variant of mx_nvfp4_quantize_weight_2d (the pages have no counterpart: it exists
  * for callers that cannot allocate device memory, e.g. a plugin inside a host framework that owns
  * all device memory, or a loop that must not call cudaMalloc because it synchronizes the device).

@@ -48,10 +48,12 @@ def lib() -> ctypes.CDLL:
                 "mx_workspace_bytes": (SZ, [I32, I64, I64]),
                 "mx_quantize_mxfp8": (I32, [P, I64, I64, I64, P, P, P, P, P]),
                 "mx_nvfp4_quantize_per_token": (I32, [P, I64, I64, I64, P, P, P, P]),
+                "mx_nvfp4_quantize_per_token_46": (I32, [P, I64, I64, I64, P, P, P, P]),
                 "mx_nvfp4_quantize_per_token_grouped": (I32, [P, I64, I64, I64, I64, P, P, P, P, P]),
                 "mx_quantize_mxfp8_grouped": (I32, [P, I64, I64, I64, I64, P, P, P, P]),
                 "mx_grouped_scale_bytes": (I64, [I64, I64, I64, I32]),
                 "mx_nvfp4_quantize_weight_2d": (I32, [P, I64, I64, I64, P, P, P, P, P, P, SZ, P]),
+                "mx_nvfp4_quantize_weight_2d_46": (I32, [P, I64, I64, I64, P, P, P, P, P, P, SZ, P]),
                 "mx_rht16": (I32, [P, I64, I64, U64, P, P]),
                 "mx_nvfp4_quantize_1x16": (I32, [P, I64, I64, I32, I32, U64, I32, U64, P, P, P, P, SZ, P]),
                 "mx_dequantize_bf16": (I32, [I32, P, P, P, I32, I64, I64, I64, P, P]),
@@ -124,6 +126,13 @@ def mx_nvfp4_quantize_per_token(x, q, s, s_tok, stream=None):
         _p(x), T, H, x.stride(0), _p(q), _p(s), _p(s_tok), _stream(stream)))
 
 
+def mx_nvfp4_quantize_per_token_46(x, q, s, s_tok, stream=None):
+    x = _bf16_bits(x)
+    T, H = x.shape
+    _check("mx_nvfp4_quantize_per_token_46", lib().mx_nvfp4_quantize_per_token_46(
+        _p(x), T, H, x.stride(0), _p(q), _p(s), _p(s_tok), _stream(stream)))
+
+
 def mx_nvfp4_quantize_per_token_grouped(x, group_offsets, q, s, s_tok, stream=None):
     x = _bf16_bits(x)
     T, H = x.shape
@@ -148,6 +157,14 @@ def mx_nvfp4_quantize_weight_2d(w, q_row, s_row, q_col, s_col, s_w, workspace, s
     w = _bf16_bits(w)
     G, O, H = w.shape
     _check("mx_nvfp4_quantize_weight_2d", lib().mx_nvfp4_quantize_weight_2d(
+        _p(w), G, O, H, _p(q_row), _p(s_row), _p(q_col), _p(s_col), _p(s_w), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mx_nvfp4_quantize_weight_2d_46(w, q_row, s_row, q_col, s_col, s_w, workspace, stream=None):
+    w = _bf16_bits(w)
+    G, O, H = w.shape
+    _check("mx_nvfp4_quantize_weight_2d_46", lib().mx_nvfp4_quantize_weight_2d_46(
         _p(w), G, O, H, _p(q_row), _p(s_row), _p(q_col), _p(s_col), _p(s_w), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 

@@ -69,6 +69,13 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float v[8]) {
 }
 
 // Two packed E2M1 codes (one byte) -> two FP16 values (exact); element 0 from the low nibble.
+// Value of a 4-bit E2M1 code (s ee m, bias 1; e = 0 subnormal m * 0.5) from its field definition.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+    const uint32_t mag = e ? (((e + 126u) << 23) | (m << 22)) : (m ? 0x3F000000u : 0u);
+    return __uint_as_float(mag | ((c & 8u) << 28));
+}
+
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
     uint32_t r;
     asm("{\n\t.reg .b8 c;\n\tcvt.u8.u32 c, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, c;\n\t}" : "=r"(r) : "r"(byte & 0xFFu));
@@ -153,10 +160,13 @@ __device__ __forceinline__ void rht16_inplace(float v[16], uint32_t signmask) {
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ float nvfp4_second_scale(float amax) { return __fdiv_rn(amax, 2688.0f); }
 
-__device__ __forceinline__ uint32_t nvfp4_block_scale(float amax_b, float S) {
+// bs = E4M3(fp32(fp32(amax_b / m) / S)) with m = 6 (the block maximum maps to the E2M1 maximum) or,
+// for the Four-over-Six alternative, m = 4.
+__device__ __forceinline__ uint32_t nvfp4_block_scale_m(float amax_b, float S, float m) {
     if (S == 0.0f) return 0u;
-    return cvt_e4m3(__fdiv_rn(__fdiv_rn(amax_b, 6.0f), S));
+    return cvt_e4m3(__fdiv_rn(__fdiv_rn(amax_b, m), S));
 }
+__device__ __forceinline__ uint32_t nvfp4_block_scale(float amax_b, float S) { return nvfp4_block_scale_m(amax_b, S, 6.0f); }
 
 __device__ __forceinline__ float nvfp4_block_recip(uint32_t bs, float S) {
     const float d = __fmul_rn(e4m3_to_f32(bs), S);

@@ -23,14 +23,15 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64
                                   uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int G, const int64_t* group_offsets,
                                   cudaStream_t stream);
 cudaError_t launch_nvfp4_per_token(const uint16_t* x, int64_t T, int64_t H, int64_t ldx, uint8_t* q, uint8_t* s,
-                                   float* s_tok, int G, const int64_t* group_offsets, int num_sms, cudaStream_t stream);
+                                   float* s_tok, int G, const int64_t* group_offsets, int num_sms, cudaStream_t stream,
+                                   bool four_six = false);
 cudaError_t launch_nvfp4_1x16(const uint16_t* x, int64_t T, int64_t N, bool colwise, bool rht, uint64_t rht_seed,
                               bool sr, uint64_t sr_seed, uint8_t* q, uint8_t* s, float* s_tensor, uint32_t* ws,
                               int num_sms, cudaStream_t stream);
 cudaError_t launch_rht16(const uint16_t* x, int64_t T, int64_t N, uint64_t seed, uint16_t* y, cudaStream_t stream);
 cudaError_t launch_nvfp4_weight_2d(const uint16_t* w, int64_t G, int64_t O, int64_t H, uint8_t* q_row, uint8_t* s_row,
                                    uint8_t* q_col, uint8_t* s_col, float* s_w, uint32_t* ws, int num_sms,
-                                   cudaStream_t stream);
+                                   cudaStream_t stream, bool four_six = false);
 cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const float* s2, int64_t rows_per_scale, int64_t R,
                            int64_t K, uint16_t* y, cudaStream_t stream);
 cudaError_t launch_mismatch(const uint8_t* x, const uint8_t* y, int64_t nbytes, unsigned long long* count,

@@ -132,6 +132,30 @@ mx_status mx_nvfp4_quantize_weight_2d(const void* w, int64_t G, int64_t O, int64
                                                   stream));
 }
 
+mx_status mx_nvfp4_quantize_per_token_46(const void* x, int64_t T, int64_t H, int64_t ldx, uint8_t* q, uint8_t* s,
+                                         float* s_tok, cudaStream_t stream) {
+    if (!x || !q || !s || !s_tok || T <= 0 || H <= 0 || ldx < H) return MX_ERR_INVALID_ARG;
+    if ((ldx % 8) != 0 || !aligned16(x) || !aligned16(q) || !aligned16(s) || !aligned16(s_tok)) return MX_ERR_ALIGNMENT;
+    if ((H % 16) != 0) return MX_ERR_UNSUPPORTED;
+    return from_cuda(mxk::launch_nvfp4_per_token(static_cast<const uint16_t*>(x), T, H, ldx, q, s, s_tok, 0, nullptr,
+                                                  mxk::device_sm_count(), stream, true));
+}
+
+mx_status mx_nvfp4_quantize_weight_2d_46(const void* w, int64_t G, int64_t O, int64_t H, uint8_t* q_row, uint8_t* s_row,
+                                         uint8_t* q_col, uint8_t* s_col, float* s_w, void* workspace,
+                                         size_t workspace_bytes, cudaStream_t stream) {
+    if (!w || !q_row || !s_row || !q_col || !s_col || !s_w || !workspace) return MX_ERR_INVALID_ARG;
+    if (G <= 0 || O <= 0 || H <= 0) return MX_ERR_INVALID_ARG;
+    if (workspace_bytes < mx_workspace_bytes(MX_WS_WEIGHT_2D, G, 0)) return MX_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q_row) || !aligned16(s_row) || !aligned16(q_col) || !aligned16(s_col) ||
+        !aligned16(s_w) || !aligned16(workspace))
+        return MX_ERR_ALIGNMENT;
+    if ((O % 16) != 0 || (H % 16) != 0) return MX_ERR_UNSUPPORTED;
+    return from_cuda(mxk::launch_nvfp4_weight_2d(static_cast<const uint16_t*>(w), G, O, H, q_row, s_row, q_col, s_col,
+                                                  s_w, static_cast<uint32_t*>(workspace), mxk::device_sm_count(),
+                                                  stream, true));
+}
+
 mx_status mx_rht16(const void* x, int64_t T, int64_t N, uint64_t seed, void* y, cudaStream_t stream) {
     if (!x || !y || T <= 0 || N <= 0 || x == y) return MX_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(y) || (N % 8) != 0) return MX_ERR_ALIGNMENT;

@@ -56,7 +56,45 @@ __device__ __forceinline__ uint2 quant_block16(const uint4& a, const uint4& b, f
     return make_uint2(cvt_e2m1x8(v), cvt_e2m1x8(v + 8));
 }
 
-template <bool PER_TENSOR, bool SR, bool GROUPED, int LPR>
+// Largest |fp32(fp32(value(q_i) * value(bs)) * S) - x_i| over n values whose codes are packed 8 per
+// word (even index in the low nibble).
+__device__ __forceinline__ float nvfp4_max_dq_error(const float* x, const uint32_t* codes, int n, uint32_t bs, float S) {
+    const float bsv = e4m3_to_f32(bs);
+    float err = 0.0f;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+        const float deq = __fmul_rn(__fmul_rn(e2m1_value((codes[i >> 3] >> (4 * (i & 7))) & 0xFu), bsv), S);
+        err = fmaxf(err, fabsf(__fsub_rn(deq, x[i])));
+    }
+    return err;
+}
+
+// Four-over-Six (NVIDIA RL blog, "Four-Over-Six (4/6)"): the block is quantized with its maximum mapped
+// to 6 and to 4, and the candidate with the smaller largest dequantization error is kept (a tie keeps
+// 6).  Returns the 8 code bytes and the chosen scale.
+__device__ __forceinline__ uint2 quant_block16_46(const uint4& a, const uint4& c, float amax_b, float S, uint32_t& bs_out) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { x[2 * i] = bf16_lo(w[i]); x[2 * i + 1] = bf16_hi(w[i]); }
+    uint32_t best[2], bs_best = 0;
+    float err_best = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint32_t bs = nvfp4_block_scale_m(amax_b, S, k == 0 ? 6.0f : 4.0f);
+        const float r = nvfp4_block_recip(bs, S);
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(x[i], r);
+        const uint32_t codes[2] = {cvt_e2m1x8(v), cvt_e2m1x8(v + 8)};
+        const float err = nvfp4_max_dq_error(x, codes, 16, bs, S);
+        if (k == 0 || err < err_best) { best[0] = codes[0]; best[1] = codes[1]; bs_best = bs; err_best = err; }
+    }
+    bs_out = bs_best;
+    return make_uint2(best[0], best[1]);
+}
+
+template <bool PER_TENSOR, bool SR, bool GROUPED, int LPR, bool FOUR_SIX = false>
 __global__ void __launch_bounds__(RW_WARPS * 32, RW_CTAS_PER_SM)
 nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64_t ldx,
                      uint8_t* __restrict__ q, uint8_t* __restrict__ s, float* __restrict__ s_tok,
@@ -128,8 +166,10 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
         const int64_t srow = (GROUPED && row_ok) ? grouped_scale_row(s_off, s_ptile, G, t) : t;
 
         // codes, and the four consecutive block scales of lanes 4m .. 4m+3 of the row group as one word
-        auto emit = [&](int64_t b, bool valid, const uint4& a, const uint4& c, uint32_t bs, float r) {
-            const uint2 codes = quant_block16<SR>(a, c, r, (uint64_t)t * (uint64_t)H + (uint64_t)b * 16, k0, k1);
+        auto emit = [&](int64_t b, bool valid, const uint4& a, const uint4& c, uint32_t bs, float r, uint32_t amax_bits) {
+            uint2 codes;
+            if (FOUR_SIX) codes = quant_block16_46(a, c, __uint_as_float(amax_bits << 16), S, bs);
+            else codes = quant_block16<SR>(a, c, r, (uint64_t)t * (uint64_t)H + (uint64_t)b * 16, k0, k1);
             if (valid) __stcs(reinterpret_cast<uint2*>(q + t * (H / 2) + b * 8), codes);
             const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 1);
             const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
@@ -150,15 +190,15 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
             float rv[RW_MAXB];
 #pragma unroll
             for (int i = 0; i < RW_MAXB; ++i) {
-                bsv[i] = nvfp4_block_scale(__uint_as_float(bam[i] << 16), S);
-                rv[i] = nvfp4_block_recip(bsv[i], S);
+                bsv[i] = FOUR_SIX ? 0u : nvfp4_block_scale(__uint_as_float(bam[i] << 16), S);
+                rv[i] = FOUR_SIX ? 0.0f : nvfp4_block_recip(bsv[i], S);
             }
             const int64_t nrounds = (nblk + LPR - 1) / LPR;
 #pragma unroll
             for (int i = 0; i < RW_MAXB; ++i) {
                 if (i < nrounds) {                  // warp-uniform
                     const int64_t b = sub + LPR * i;
-                    emit(b, row_ok && b < nblk, ra[i], rb[i], bsv[i], rv[i]);
+                    emit(b, row_ok && b < nblk, ra[i], rb[i], bsv[i], rv[i], bam[i]);
                 }
             }
         } else {
@@ -171,24 +211,25 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
                 uint32_t m2 = 0;
                 m2 = absmax_bf16x2(m2, a.x); m2 = absmax_bf16x2(m2, a.y); m2 = absmax_bf16x2(m2, a.z); m2 = absmax_bf16x2(m2, a.w);
                 m2 = absmax_bf16x2(m2, c.x); m2 = absmax_bf16x2(m2, c.y); m2 = absmax_bf16x2(m2, c.z); m2 = absmax_bf16x2(m2, c.w);
-                const uint32_t bs = nvfp4_block_scale(__uint_as_float(fold_halves(m2) << 16), S);
-                emit(b, valid, a, c, bs, nvfp4_block_recip(bs, S));
+                const uint32_t am = fold_halves(m2);
+                const uint32_t bs = FOUR_SIX ? 0u : nvfp4_block_scale(__uint_as_float(am << 16), S);
+                emit(b, valid, a, c, bs, FOUR_SIX ? 0.0f : nvfp4_block_recip(bs, S), am);
             }
         }
     }
 }
 
-template <bool PER_TENSOR, bool SR, bool GROUPED>
+template <bool PER_TENSOR, bool SR, bool GROUPED, bool FOUR_SIX = false>
 void launch_rowwise(int64_t T, int64_t H, unsigned grid_cap, size_t smem, cudaStream_t stream, const uint16_t* x,
                     int64_t ldx, uint8_t* q, uint8_t* s, float* s_tok, const uint32_t* amax, float* s_tensor,
                     uint64_t sr_seed, int G, const int64_t* offs) {
     if (H / 16 <= 64) {
         const int64_t blocks = (T + RW_WARPS * 2 - 1) / (RW_WARPS * 2);
-        nvfp4_rowwise_kernel<PER_TENSOR, SR, GROUPED, 16><<<(unsigned)min64(blocks, grid_cap), RW_WARPS * 32, smem, stream>>>(
+        nvfp4_rowwise_kernel<PER_TENSOR, SR, GROUPED, 16, FOUR_SIX><<<(unsigned)min64(blocks, grid_cap), RW_WARPS * 32, smem, stream>>>(
             x, T, H, ldx, q, s, s_tok, amax, s_tensor, sr_seed, G, offs);
     } else {
         const int64_t blocks = (T + RW_WARPS - 1) / RW_WARPS;
-        nvfp4_rowwise_kernel<PER_TENSOR, SR, GROUPED, 32><<<(unsigned)min64(blocks, grid_cap), RW_WARPS * 32, smem, stream>>>(
+        nvfp4_rowwise_kernel<PER_TENSOR, SR, GROUPED, 32, FOUR_SIX><<<(unsigned)min64(blocks, grid_cap), RW_WARPS * 32, smem, stream>>>(
             x, T, H, ldx, q, s, s_tok, amax, s_tensor, sr_seed, G, offs);
     }
 }
@@ -456,6 +497,7 @@ matrix_amax_kernel(const uint16_t* __restrict__ w, int64_t per_matrix, uint32_t*
     }
 }
 
+template <bool FOUR_SIX>
 __global__ void __launch_bounds__(128)
 weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, const uint32_t* __restrict__ amax,
                       uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
@@ -487,20 +529,50 @@ weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, cons
     uint32_t a16 = fold_halves(m2);
     a16 = max(a16, __shfl_xor_sync(0xFFFFFFFFu, a16, 1));
     a16 = max(a16, __shfl_xor_sync(0xFFFFFFFFu, a16, 16));
-    const uint32_t bs = nvfp4_block_scale(__uint_as_float(a16 << 16), S);
-    const float r = nvfp4_block_recip(bs, S);
-
     uint8_t* qrow_g = q_row + g * O * (H / 2);
+    // codes of this lane's 8 rows x 8 columns with the tile's scale; with Four-over-Six both candidates
+    // (the tile maximum mapped to 6 and to 4) and their largest dequantization errors, combined over the
+    // tile's four lanes (l, l^1, l^16, l^17), decide the scale
     uint32_t codes[8];
+    uint32_t bs = 0;
+    float err_keep = 0.0f;
+#pragma unroll
+    for (int k = 0; k < (FOUR_SIX ? 2 : 1); ++k) {
+        const uint32_t bsk = nvfp4_block_scale_m(__uint_as_float(a16 << 16), S, k == 0 ? 6.0f : 4.0f);
+        const float r = nvfp4_block_recip(bsk, S);
+        uint32_t ck[8];
+        float x[64];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            x[8 * i + 0] = bf16_lo(xr[i].x); x[8 * i + 1] = bf16_hi(xr[i].x);
+            x[8 * i + 2] = bf16_lo(xr[i].y); x[8 * i + 3] = bf16_hi(xr[i].y);
+            x[8 * i + 4] = bf16_lo(xr[i].z); x[8 * i + 5] = bf16_hi(xr[i].z);
+            x[8 * i + 6] = bf16_lo(xr[i].w); x[8 * i + 7] = bf16_hi(xr[i].w);
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(x[8 * i + j], r);
+            ck[i] = cvt_e2m1x8(v);
+        }
+        if (!FOUR_SIX) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) codes[i] = ck[i];
+            bs = bsk;
+        } else {
+            float err = nvfp4_max_dq_error(x, ck, 64, bsk, S);
+            err = fmaxf(err, __shfl_xor_sync(0xFFFFFFFFu, err, 1));
+            err = fmaxf(err, __shfl_xor_sync(0xFFFFFFFFu, err, 16));
+            // the four lanes of a tile hold the same combined error, so they agree on the choice
+            if (k == 0 || err < err_keep) {
+                err_keep = err;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) codes[i] = ck[i];
+                bs = bsk;
+            }
+        }
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int rr = 2 * i + rpar;                     // row within the warp's 16
-        float v[8];
-        v[0] = __fmul_rn(bf16_lo(xr[i].x), r); v[1] = __fmul_rn(bf16_hi(xr[i].x), r);
-        v[2] = __fmul_rn(bf16_lo(xr[i].y), r); v[3] = __fmul_rn(bf16_hi(xr[i].y), r);
-        v[4] = __fmul_rn(bf16_lo(xr[i].z), r); v[5] = __fmul_rn(bf16_hi(xr[i].z), r);
-        v[6] = __fmul_rn(bf16_lo(xr[i].w), r); v[7] = __fmul_rn(bf16_hi(xr[i].w), r);
-        codes[i] = cvt_e2m1x8(v);
         if (rowv && colv) __stcs(reinterpret_cast<uint32_t*>(qrow_g + (o0 + rr) * (H / 2) + h / 2), codes[i]);
     }
     // transposed copy: lanes l (even rows) and l ^ 16 (odd rows) swap code words; the even-row lane
@@ -572,7 +644,8 @@ weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, cons
 // launchers
 // ------------------------------------------------------------------------------------------------
 cudaError_t launch_nvfp4_per_token(const uint16_t* x, int64_t T, int64_t H, int64_t ldx, uint8_t* q, uint8_t* s,
-                                   float* s_tok, int G, const int64_t* group_offsets, int num_sms, cudaStream_t stream) {
+                                   float* s_tok, int G, const int64_t* group_offsets, int num_sms, cudaStream_t stream,
+                                   bool four_six) {
     if (G > 0) {
         // grouped layout: the padding between groups is zero
         cudaError_t e = cudaMemsetAsync(s, 0, (size_t)host_scale_bytes(T + 127 * (int64_t)G, H, 16), stream);
@@ -582,9 +655,14 @@ cudaError_t launch_nvfp4_per_token(const uint16_t* x, int64_t T, int64_t H, int6
         if (e != cudaSuccess) return e;
     }
     const unsigned cap = (unsigned)num_sms * 16;
-    if (G > 0)
+    if (G > 0 && four_six)
+        launch_rowwise<false, false, true, true>(T, H, cap, (size_t)12 * (G + 1) + 128, stream, x, ldx, q, s, s_tok, nullptr,
+                                                 nullptr, 0, G, group_offsets);
+    else if (G > 0)
         launch_rowwise<false, false, true>(T, H, cap, (size_t)12 * (G + 1) + 128, stream, x, ldx, q, s, s_tok, nullptr,
                                            nullptr, 0, G, group_offsets);
+    else if (four_six)
+        launch_rowwise<false, false, false, true>(T, H, cap, 0, stream, x, ldx, q, s, s_tok, nullptr, nullptr, 0, 0, nullptr);
     else
         launch_rowwise<false, false, false>(T, H, cap, 0, stream, x, ldx, q, s, s_tok, nullptr, nullptr, 0, 0, nullptr);
     return cudaGetLastError();
@@ -630,7 +708,7 @@ cudaError_t launch_rht16(const uint16_t* x, int64_t T, int64_t N, uint64_t seed,
 
 cudaError_t launch_nvfp4_weight_2d(const uint16_t* w, int64_t G, int64_t O, int64_t H, uint8_t* q_row, uint8_t* s_row,
                                    uint8_t* q_col, uint8_t* s_col, float* s_w, uint32_t* ws, int num_sms,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, bool four_six) {
     cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t) * (size_t)G, stream);
     if (e != cudaSuccess) return e;
     if ((O % 128) != 0 || ((H / 16) % 4) != 0) {
@@ -648,7 +726,8 @@ cudaError_t launch_nvfp4_weight_2d(const uint16_t* w, int64_t G, int64_t O, int6
     matrix_amax_kernel<<<dim3((unsigned)bx, (unsigned)G), 256, 0, stream>>>(w, per, ws);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     dim3 grid((unsigned)((H + W2_COLS - 1) / W2_COLS), (unsigned)((O + W2_ROWS - 1) / W2_ROWS), (unsigned)G);
-    weight2d_quant_kernel<<<grid, 128, 0, stream>>>(w, O, H, ws, q_row, s_row, q_col, s_col, s_w);
+    if (four_six) weight2d_quant_kernel<true><<<grid, 128, 0, stream>>>(w, O, H, ws, q_row, s_row, q_col, s_col, s_w);
+    else weight2d_quant_kernel<false><<<grid, 128, 0, stream>>>(w, O, H, ws, q_row, s_row, q_col, s_col, s_w);
     return cudaGetLastError();
 }
 

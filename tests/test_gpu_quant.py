@@ -297,3 +297,43 @@ def test_grouped_quantizers_write_grouped_layout(mx, orc, sizes):
     q8o, s8o = orc.mxfp8_quantize_rowwise(x)
     assert np.array_equal(to_np(q8), q8o)
     assert np.array_equal(to_np(s8), orc.scales_to_grouped_layout(s8o, offs, s8.numel()))
+
+
+# ------------------------------------------------------------------------------------------------
+# Four-over-Six NVFP4 (per token, 2D weights)
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(256, 512), (37, 48), (130, 2048), (64, 2560)])
+def test_nvfp4_per_token_four_over_six(mx, orc, shape):
+    T, H = shape
+    x = synthetic.random_bf16(T * 7 + H, shape, "student_t")
+    x[min(2, T - 1)] = 0                              # a zero token
+    out = mx.alloc_nvfp4_rows(T, H, DEV)
+    out["s"].fill_(0xEE)
+    mx.mx_nvfp4_quantize_per_token_46(bf16_dev(x), out["q"], out["s"], out["s2"])
+    q, s, st = orc.nvfp4_quantize_per_token_46(x)
+    assert np.array_equal(to_np(out["q"]), q), first_mismatch(to_np(out["q"]), q)
+    assert np.array_equal(to_np(out["s"]), orc.scales_to_gemm_layout(s))
+    assert np.array_equal(to_np(out["s2"]).view(np.uint32), st.view(np.uint32))
+    _, s6, _ = orc.nvfp4_quantize_per_token(x)
+    assert (s != s6).any()                            # some blocks took the scale-to-4
+
+
+@pytest.mark.parametrize("G,O,H", [(3, 96, 160), (2, 256, 512)])
+def test_nvfp4_weight_2d_four_over_six(mx, orc, G, O, H):
+    w = synthetic.random_bf16(G * O + H + 1, (G, O, H), "normal", 0.02)
+    out = mx.alloc_nvfp4_weight_2d(G, O, H, DEV)
+    out["s_row"].fill_(0x33)
+    out["s_col"].fill_(0x44)
+    mx.mx_nvfp4_quantize_weight_2d_46(bf16_dev(w), out["q_row"], out["s_row"], out["q_col"], out["s_col"], out["s_w"],
+                                      out["ws"])
+    srb = orc.scale_layout_bytes(O, (H // 16))
+    scb = orc.scale_layout_bytes(H, (O // 16))
+    for g in range(G):
+        qr, qc, st, sw = orc.nvfp4_quantize_weight_2d_46(np.ascontiguousarray(w[g]))
+        assert np.array_equal(to_np(out["q_row"][g]), qr), first_mismatch(to_np(out["q_row"][g]), qr)
+        assert np.array_equal(to_np(out["q_col"][g]), qc), first_mismatch(to_np(out["q_col"][g]), qc)
+        assert np.array_equal(to_np(out["s_row"][g * srb:(g + 1) * srb]),
+                              orc.scales_to_gemm_layout(orc.weight_2d_operand_scales(st, "row")))
+        assert np.array_equal(to_np(out["s_col"][g * scb:(g + 1) * scb]),
+                              orc.scales_to_gemm_layout(orc.weight_2d_operand_scales(st, "col")))
+        assert to_np(out["s_w"])[g] == sw
