@@ -80,6 +80,8 @@ def _load():
                 "orc_nvfp4_quantize_weight_2d": (None, [P, I64, I64, P, P, P, P]),
                 "orc_nvfp4_quantize_weight_2d_46": (None, [P, I64, I64, P, P, P, P]),
                 "orc_nvfp4_quantize_per_token_46": (None, [P, I64, I64, I64, P, P, P]),
+                "orc_fp8_blockwise_1x128": (None, [P, I64, I64, I64, ctypes.c_int, P, P, P]),
+                "orc_fp8_blockwise_128x128": (None, [P, I64, I64, ctypes.c_int, P, P, P, P]),
                 "orc_rht16": (None, [P, I64, I64, U64, P]),
                 "orc_nvfp4_quantize_1x16": (None, [P, I64, I64, ctypes.c_int, ctypes.c_int, U64,
                                                    ctypes.c_int, U64, P, P, P]),
@@ -317,6 +319,50 @@ def nvfp4_quantize_weight_2d_46(w: np.ndarray):
     sw = np.zeros(1, dtype=np.float32)
     _load().orc_nvfp4_quantize_weight_2d_46(_p(w), O, H, _p(q_row), _p(q_col), _p(st), _p(sw))
     return q_row, q_col, st, np.float32(sw[0])
+
+
+def fp8_blockwise_1x128(x: np.ndarray, pow2: bool):
+    """Blockwise FP8 of activations / gradients (PT page, "FP8 nas camadas lineares": E4M3 in [1, 128]
+    tiles with one FP32 scale each; optionally power-of-two scales).
+    Returns (codes uint8 [R, K], scales FP32 [R, K/128], E8M0 codes [R, K/128] (power of two only))."""
+    x = _bf16(x)
+    R, K = x.shape
+    q = np.zeros((R, K), dtype=np.uint8)
+    s = np.zeros((R, K // 128), dtype=np.float32)
+    e8 = np.zeros((R, K // 128), dtype=np.uint8)
+    _load().orc_fp8_blockwise_1x128(_p(x), R, K, K, int(pow2), _p(q), _p(s), _p(e8))
+    return q, s, e8
+
+
+def fp8_blockwise_128x128(w: np.ndarray, pow2: bool):
+    """Blockwise FP8 of weights in [128, 128] blocks, both orientations.
+    Returns (q_row [O, H], q_col [H, O], scales FP32 [ceil(O/128), ceil(H/128)], E8M0 codes of that shape)."""
+    w = _bf16(w)
+    O, H = w.shape
+    q_row = np.zeros((O, H), dtype=np.uint8)
+    q_col = np.zeros((H, O), dtype=np.uint8)
+    bo, bh = (O + 127) // 128, (H + 127) // 128
+    s = np.zeros((bo, bh), dtype=np.float32)
+    e8 = np.zeros((bo, bh), dtype=np.uint8)
+    _load().orc_fp8_blockwise_128x128(_p(w), O, H, int(pow2), _p(q_row), _p(q_col), _p(s), _p(e8))
+    return q_row, q_col, s, e8
+
+
+def fp8_blockwise_e8m0_rowwise(e8: np.ndarray, block: int = 128) -> np.ndarray:
+    """E8M0 codes of power-of-two [1, 128] tiles repeated over their four 32-element sub-blocks: the MXFP8
+    row-wise scale array [R, K/32] that decodes the same codes to the same values."""
+    return np.repeat(np.asarray(e8, dtype=np.uint8), block // 32, axis=1)
+
+
+def fp8_blockwise_e8m0_weight(e8: np.ndarray, O: int, H: int, orientation: str) -> np.ndarray:
+    """E8M0 codes of power-of-two [128, 128] weight blocks as MXFP8 scales of one operand orientation:
+    "row" gives [O, H/32] for the codes q_row [O, H]; "col" gives [H, O/32] for q_col [H, O]."""
+    e8 = np.asarray(e8, dtype=np.uint8)
+    if orientation == "row":
+        return e8[np.arange(O)[:, None] // 128, (np.arange(H // 32) * 32)[None, :] // 128]
+    if orientation == "col":
+        return e8[(np.arange(O // 32) * 32)[None, :] // 128, np.arange(H)[:, None] // 128]
+    raise ValueError(orientation)
 
 
 def weight_2d_operand_scales(s_tile: np.ndarray, orientation: str) -> np.ndarray:

@@ -300,6 +300,96 @@ ORC_API void orc_mxfp8_quantize_colwise(const uint16_t* x, int64_t rows, int64_t
 }
 
 /* ------------------------------------------------------------------------ */
+/* Blockwise FP8 ([PT page] "FP8 nas camadas lineares": E4M3, weights in     */
+/* [128, 128] blocks, input activations and output gradients in [1, 128]     */
+/* tiles, one FP32 scale per block; option: power-of-two scales).  Per block */
+/* with amax = max |x|:                                                      */
+/*   FP32 scale:    s = fp32(amax / 448), q_i = E4M3(fp32(x_i / s));         */
+/*                  amax = 0 gives s = 0 and q = 0                           */
+/*   power of two:  k = the smallest integer with 448 * 2^k >= amax,         */
+/*                  clamped to [-127, 127] (amax = 0 gives -127); s = 2^k;    */
+/*                  q_i = E4M3(x_i * 2^-k) (exact scaling, one rounding)     */
+/* The power-of-two k is an E8M0 exponent: code k + 127.                     */
+/* ------------------------------------------------------------------------ */
+
+static int fp8bw_pow2_exponent(float amax) {
+    if (amax == 0.0f) return -127;
+    int ex;
+    frexp((double)amax, &ex);                      /* amax in [2^(ex-1), 2^ex) */
+    /* 448 * 2^(ex-10) = 0.875 * 2^(ex-1) < amax, so the answer is ex - 9 or above */
+    int k = ex - 9;
+    while (ldexp(448.0, k) < (double)amax) ++k;     /* exact comparisons in double */
+    if (k < -127) k = -127;
+    if (k > 127) k = 127;
+    return k;
+}
+
+/* Codes of the n values of one block; returns its FP32 scale, and the E8M0 code in *e8 (power of two). */
+static float fp8bw_block(const float* v, int n, int pow2, uint8_t* q, uint8_t* e8) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    if (pow2) {
+        int k = fp8bw_pow2_exponent(amax);
+        for (int i = 0; i < n; ++i) q[i] = orc_e4m3_encode(ldexp((double)v[i], -k));
+        *e8 = (uint8_t)(k + 127);
+        return (float)ldexp(1.0, k);
+    }
+    *e8 = 0;
+    float sc = amax / 448.0f;
+    if (amax == 0.0f) {
+        for (int i = 0; i < n; ++i) q[i] = orc_e4m3_encode(0.0 * v[i]);
+        return 0.0f;
+    }
+    for (int i = 0; i < n; ++i) {
+        float t = v[i] / sc;
+        q[i] = orc_e4m3_encode((double)t);
+    }
+    return sc;
+}
+
+/* Activations / gradients, [1, 128] tiles along K.  x [R, ldx] BF16, K % 128 == 0; q [R, K];
+ * s [R, K/128] FP32; e8 [R, K/128] (E8M0 codes of the power-of-two scales, 0 otherwise). */
+ORC_API void orc_fp8_blockwise_1x128(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, int pow2,
+                                     uint8_t* q, float* s, uint8_t* e8) {
+    int64_t nb = K / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        float v[128];
+        for (int64_t b = 0; b < nb; ++b) {
+            for (int i = 0; i < 128; ++i) v[i] = bf16_to_float(x[r * ldx + b * 128 + i]);
+            s[r * nb + b] = fp8bw_block(v, 128, pow2, q + r * K + b * 128, e8 + r * nb + b);
+        }
+    }
+}
+
+/* Weights, [128, 128] blocks (the last block row / column may be partial).  w [O, H] BF16;
+ * q_row [O, H]; q_col [H, O] (the same codes, transposed); s [ceil(O/128), ceil(H/128)] FP32; e8 the
+ * same shape (E8M0 codes of the power-of-two scales, 0 otherwise). */
+ORC_API void orc_fp8_blockwise_128x128(const uint16_t* w, int64_t O, int64_t H, int pow2,
+                                       uint8_t* q_row, uint8_t* q_col, float* s, uint8_t* e8) {
+    int64_t bo_n = (O + 127) / 128, bh_n = (H + 127) / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t bo = 0; bo < bo_n; ++bo) {
+        float* v = (float*)malloc(sizeof(float) * 128 * 128);
+        uint8_t* c = (uint8_t*)malloc(128 * 128);
+        for (int64_t bh = 0; bh < bh_n; ++bh) {
+            int64_t ro = bo * 128, rh = bh * 128;
+            int no = (int)(O - ro < 128 ? O - ro : 128), nh = (int)(H - rh < 128 ? H - rh : 128);
+            for (int i = 0; i < no; ++i)
+                for (int j = 0; j < nh; ++j) v[i * nh + j] = bf16_to_float(w[(ro + i) * H + rh + j]);
+            s[bo * bh_n + bh] = fp8bw_block(v, no * nh, pow2, c, e8 + bo * bh_n + bh);
+            for (int i = 0; i < no; ++i)
+                for (int j = 0; j < nh; ++j) {
+                    q_row[(ro + i) * H + rh + j] = c[i * nh + j];
+                    q_col[(rh + j) * O + ro + i] = c[i * nh + j];
+                }
+        }
+        free(v);
+        free(c);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* NVFP4: E2M1 values, one E4M3 scale per 16, under an FP32 second-level     */
 /* scale S ([Miles] per token; [MaxText] per tensor).  For every block:      */
 /*   bs = E4M3( fp32( fp32(amax_b / 6) / S ) )      (S = 0 gives bs = 0)     */

@@ -42,13 +42,19 @@ MUTATIONS = {
  'fos_div4': ('uint8_t bs4 = nvfp4_block_scale_m(amax_b, S, 4.0f);', 'uint8_t bs4 = nvfp4_block_scale_m(amax_b, S, 6.0f);'),
  'fos_sum_err': ('        err = fmaxf(err, fabsf(deq - x[i]));', '        err = err + (deq - x[i]) * (deq - x[i]);'),
  'fos_no_S': ('        float deq = prod * S;', '        float deq = prod;'),
+ 'bw_pow2_ge': ('while (ldexp(448.0, k) < (double)amax) ++k;', 'while (ldexp(448.0, k) <= (double)amax) ++k;'),
+ 'bw_div': ('float t = v[i] / sc;', 'float t = v[i] * sc;'),
+ 'bw_max_448': ('float sc = amax / 448.0f;', 'float sc = amax / 480.0f;'),
+ 'bw_zero_exp': ('if (amax == 0.0f) return -127;', 'if (amax == 0.0f) return 0;'),
+ 'bw_qcol': ('q_col[(rh + j) * O + ro + i] = c[i * nh + j];', 'q_col[(rh + j) * O + ro + i] = c[j * nh + i];'),
+ 'bw_tile_amax': ('for (int i = 0; i < n; ++i) amax = fmaxf(amax, fabsf(v[i]));', 'for (int i = 1; i < n; ++i) amax = fmaxf(amax, fabsf(v[i]));'),
  'dq_mx_scale': ('* orc_e8m0_value(s[r * (K / 32) + k / 32]);\n            y[r', '* orc_e8m0_value(s[r * (K / 32) + k / 32] + 1);\n            y[r'),
 }
 
 
 PIN_FILES = ["tests/test_oracle_formats.py", "tests/test_oracle_rng_layout.py", "tests/test_oracle_mxfp8.py",
              "tests/test_oracle_nvfp4.py", "tests/test_oracle_rht_sr.py", "tests/test_oracle_gemm_ref.py",
-             "tests/test_oracle_four_over_six.py"]
+             "tests/test_oracle_four_over_six.py", "tests/test_oracle_blockwise_fp8.py"]
 
 
 @pytest.fixture(scope="module")
