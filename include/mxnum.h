@@ -161,6 +161,46 @@ mx_status mx_nvfp4_quantize_weight_2d_noalloc(const void* w, int64_t G, int64_t 
                                               uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                                               float* s_w, cudaStream_t stream);
 
+/* Blockwise FP8 quantize of activations or gradients: [1, 128] tiles, one scale per tile.
+ * Source: NVIDIA NeMo RL FP8 page, "FP8 nas camadas lineares" -- E4M3 values; input activations and
+ * output gradients in [1, 128] tiles with an FP32 scale each (the DeepSeek-V3 recipe); "Opções
+ * avançadas" -- power-of-two scales instead of FP32.  Per tile, amax = max |x|:
+ *   pow2 = 0:  s = fp32(amax / 448), code = E4M3 (RNE, saturating) of fp32(x / s); amax = 0 gives s = 0
+ *              and signed-zero codes.
+ *   pow2 = 1:  k = the smallest integer with 448 * 2^k >= amax, clamped to [-127, 127] (amax = 0 gives
+ *              -127); s = 2^k; code = E4M3 of x * 2^-k (exact scaling, one rounding).
+ * Row-wise tiles run along cols; column-wise tiles run along rows (the copy a GEMM contracting over
+ * rows consumes, e.g. the weight gradient), stored transposed.  Both copies come from one read of x.
+ *   x       [rows, ldx] BF16 (ldx >= cols)
+ *   q_row   [rows, cols] E4M3, s_row [rows, cols/128] FP32            (NULL q_row: skip row-wise)
+ *   sf_row  pow2 only (else NULL): mx_scale_bytes(rows, cols, 32) bytes, E8M0 byte k + 127 of each tile
+ *           repeated over its four 32-element sub-blocks in the MXFP8 GEMM scale layout, so q_row and
+ *           sf_row are an MXFP8 GEMM operand decoding to the same values (NULL: skip)
+ *   q_col   [cols, rows] E4M3, s_col [cols, rows/128] FP32            (NULL q_col: skip column-wise)
+ *   sf_col  pow2 only: mx_scale_bytes(cols, rows, 32) bytes, as sf_row for q_col (NULL: skip)
+ * Requires cols % 128 == 0 for row-wise, rows % 128 == 0 for column-wise, cols % 16 == 0, ldx % 8 == 0;
+ * pointers 16-byte aligned.  The rows/cols of the GEMM layout padding are not written. */
+mx_status mx_fp8_blockwise_quantize_1x128(const void* x, int64_t rows, int64_t cols, int64_t ldx, int pow2,
+                                          uint8_t* q_row, float* s_row, uint8_t* sf_row,
+                                          uint8_t* q_col, float* s_col, uint8_t* sf_col, cudaStream_t stream);
+
+/* Blockwise FP8 quantize of weights: [128, 128] blocks, one scale per block, codes in both
+ * orientations (the forward GEMM reads [O, H] with blocks along H, the data-gradient GEMM reads
+ * [H, O] with blocks along O; a square block has one scale for both).
+ * Source: NVIDIA NeMo RL FP8 page, "FP8 nas camadas lineares" -- weights in [128, 128] blocks with an
+ * FP32 scale each; "Opções avançadas" -- power-of-two scales.  Scale and code rules as in
+ * mx_fp8_blockwise_quantize_1x128 with the block's amax; the last block row / column may be partial.
+ *   w      [G, O, H] BF16, G stacked matrices (experts)
+ *   q_row  [G, O, H] E4M3;  q_col [G, H, O] E4M3 (the same codes transposed)
+ *   s      [G, ceil(O/128), ceil(H/128)] FP32
+ *   sf_row pow2 only (else NULL): G x mx_scale_bytes(O, H, 32) bytes, MXFP8 GEMM layout for q_row (NULL: skip)
+ *   sf_col pow2 only: G x mx_scale_bytes(H, O, 32) bytes, for q_col (NULL: skip)
+ * Requires O % 16 == 0 and H % 16 == 0 (O % 128 == 0 and H % 128 == 0 when sf_row / sf_col is given);
+ * pointers 16-byte aligned. */
+mx_status mx_fp8_blockwise_quantize_128x128(const void* w, int64_t G, int64_t O, int64_t H, int pow2,
+                                            uint8_t* q_row, uint8_t* q_col, float* s,
+                                            uint8_t* sf_row, uint8_t* sf_col, cudaStream_t stream);
+
 /* 16-point random Hadamard transform along the token dimension.
  * Source: MaxText page, "NVFP4 pretraining recipe" -- a random Hadamard transform on the WGRAD
  * inputs only, to Gaussianize outliers before 4-bit quantization.

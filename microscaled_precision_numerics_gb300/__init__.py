@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
                 "mx_nvfp4_quantize_weight_2d": (I32, [P, I64, I64, I64, P, P, P, P, P, P, SZ, P]),
                 "mx_nvfp4_quantize_weight_2d_46": (I32, [P, I64, I64, I64, P, P, P, P, P, P, SZ, P]),
                 "mx_rht16": (I32, [P, I64, I64, U64, P, P]),
+                "mx_fp8_blockwise_quantize_1x128": (I32, [P, I64, I64, I64, I32, P, P, P, P, P, P, P]),
+                "mx_fp8_blockwise_quantize_128x128": (I32, [P, I64, I64, I64, I32, P, P, P, P, P, P]),
                 "mx_nvfp4_quantize_1x16": (I32, [P, I64, I64, I32, I32, U64, I32, U64, P, P, P, P, SZ, P]),
                 "mx_dequantize_bf16": (I32, [I32, P, P, P, I32, I64, I64, I64, P, P]),
                 "mx_scaled_gemm": (I32, [I32, P, P, P, I32, P, P, P, I32, I64, I64, I64, P, I64, P]),
@@ -184,6 +186,27 @@ def mx_nvfp4_quantize_weight_2d_noalloc(w, q_row, s_row, q_col, s_col, s_w, stre
         raise ValueError(f"{G} matrices exceed the allocation-free limit of {MX_NOALLOC_MAX_MATRICES}")
     _check("mx_nvfp4_quantize_weight_2d_noalloc", f(
         _p(w), G, O, H, _p(q_row), _p(s_row), _p(q_col), _p(s_col), _p(s_w), _stream(stream)))
+
+
+def mx_fp8_blockwise_quantize_1x128(x, pow2: bool, q_row=None, s_row=None, sf_row=None, q_col=None, s_col=None,
+                                    sf_col=None, stream=None):
+    """Blockwise FP8 of activations / gradients in [1, 128] tiles: row-wise (q_row [R, C], s_row
+    [R, C/128]) and/or column-wise stored transposed (q_col [C, R], s_col [C, R/128]); with pow2 the
+    E8M0 scales may also be written in the MXFP8 GEMM layout (sf_row / sf_col)."""
+    x = _bf16_bits(x)
+    rows, cols = x.shape
+    _check("mx_fp8_blockwise_quantize_1x128", lib().mx_fp8_blockwise_quantize_1x128(
+        _p(x), rows, cols, x.stride(0), int(bool(pow2)), _p(q_row), _p(s_row), _p(sf_row), _p(q_col), _p(s_col),
+        _p(sf_col), _stream(stream)))
+
+
+def mx_fp8_blockwise_quantize_128x128(w, pow2: bool, q_row, q_col, s, sf_row=None, sf_col=None, stream=None):
+    """Blockwise FP8 of G stacked weights [G, O, H] in [128, 128] blocks: q_row [G, O, H], q_col
+    [G, H, O], s [G, ceil(O/128), ceil(H/128)]; with pow2 optionally the MXFP8-layout E8M0 scales."""
+    w = _bf16_bits(w)
+    G, O, H = w.shape
+    _check("mx_fp8_blockwise_quantize_128x128", lib().mx_fp8_blockwise_quantize_128x128(
+        _p(w), G, O, H, int(bool(pow2)), _p(q_row), _p(q_col), _p(s), _p(sf_row), _p(sf_col), _stream(stream)))
 
 
 def mx_rht16(x, seed: int, y, stream=None):

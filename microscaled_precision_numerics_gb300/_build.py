@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libmxnum.so")
 
-SOURCES = ["mxnum_api.cu", "quant_mxfp8.cu", "quant_nvfp4.cu", "dequant.cu", "gemm_sm103.cu", "noalloc.cu"]
+SOURCES = ["mxnum_api.cu", "quant_mxfp8.cu", "quant_nvfp4.cu", "dequant.cu", "gemm_sm103.cu", "noalloc.cu",
+           "quant_fp8_blockwise.cu"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -156,6 +156,42 @@ mx_status mx_nvfp4_quantize_weight_2d_46(const void* w, int64_t G, int64_t O, in
                                                   stream, true));
 }
 
+mx_status mx_fp8_blockwise_quantize_1x128(const void* x, int64_t rows, int64_t cols, int64_t ldx, int pow2,
+                                          uint8_t* q_row, float* s_row, uint8_t* sf_row, uint8_t* q_col, float* s_col,
+                                          uint8_t* sf_col, cudaStream_t stream) {
+    if (!x || rows <= 0 || cols <= 0 || ldx < cols || (pow2 != 0 && pow2 != 1)) return MX_ERR_INVALID_ARG;
+    if (!q_row && !q_col) return MX_ERR_INVALID_ARG;
+    if ((q_row && !s_row) || (q_col && !s_col)) return MX_ERR_INVALID_ARG;
+    if (!pow2 && (sf_row || sf_col)) return MX_ERR_INVALID_ARG;
+    if ((sf_row && !q_row) || (sf_col && !q_col)) return MX_ERR_INVALID_ARG;
+    if ((ldx % 8) != 0 || !aligned16(x) || (q_row && (!aligned16(q_row) || !aligned16(s_row))) ||
+        (q_col && (!aligned16(q_col) || !aligned16(s_col))) || (sf_row && !aligned16(sf_row)) ||
+        (sf_col && !aligned16(sf_col)))
+        return MX_ERR_ALIGNMENT;
+    if ((cols % 16) != 0) return MX_ERR_UNSUPPORTED;
+    if (q_row && (cols % 128) != 0) return MX_ERR_UNSUPPORTED;
+    if (q_col && ((rows % 128) != 0 || rows / 128 > 65535)) return MX_ERR_UNSUPPORTED;
+    return from_cuda(mxk::launch_fp8_blockwise_1x128(static_cast<const uint16_t*>(x), rows, cols, ldx, pow2 != 0, q_row,
+                                                      s_row, sf_row, q_col, s_col, sf_col, mxk::device_sm_count(),
+                                                      stream));
+}
+
+mx_status mx_fp8_blockwise_quantize_128x128(const void* w, int64_t G, int64_t O, int64_t H, int pow2, uint8_t* q_row,
+                                            uint8_t* q_col, float* s, uint8_t* sf_row, uint8_t* sf_col,
+                                            cudaStream_t stream) {
+    if (!w || !q_row || !q_col || !s || G <= 0 || O <= 0 || H <= 0 || (pow2 != 0 && pow2 != 1))
+        return MX_ERR_INVALID_ARG;
+    if (G > 65535 || (O + 127) / 128 > 65535) return MX_ERR_UNSUPPORTED;
+    if (!pow2 && (sf_row || sf_col)) return MX_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q_row) || !aligned16(q_col) || !aligned16(s) || (sf_row && !aligned16(sf_row)) ||
+        (sf_col && !aligned16(sf_col)))
+        return MX_ERR_ALIGNMENT;
+    if ((O % 16) != 0 || (H % 16) != 0) return MX_ERR_UNSUPPORTED;
+    if ((sf_row || sf_col) && ((O % 128) != 0 || (H % 128) != 0)) return MX_ERR_UNSUPPORTED;
+    return from_cuda(mxk::launch_fp8_blockwise_128x128(static_cast<const uint16_t*>(w), G, O, H, pow2 != 0, q_row,
+                                                        q_col, s, sf_row, sf_col, stream));
+}
+
 mx_status mx_rht16(const void* x, int64_t T, int64_t N, uint64_t seed, void* y, cudaStream_t stream) {
     if (!x || !y || T <= 0 || N <= 0 || x == y) return MX_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(y) || (N % 8) != 0) return MX_ERR_ALIGNMENT;

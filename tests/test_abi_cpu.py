@@ -27,7 +27,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ["mx_quantize_mxfp8", "mx_nvfp4_quantize_per_token", "mx_nvfp4_quantize_weight_2d", "mx_rht16",
-                     "mx_nvfp4_quantize_1x16", "mx_dequantize_bf16", "mx_scaled_gemm", "mx_grouped_scaled_gemm"]:
+                     "mx_nvfp4_quantize_1x16", "mx_dequantize_bf16", "mx_scaled_gemm", "mx_grouped_scaled_gemm",
+                     "mx_fp8_blockwise_quantize_1x128", "mx_fp8_blockwise_quantize_128x128"]:
         assert required in names
 
 
@@ -81,6 +82,24 @@ def test_nvfp4_validation(lib):
     assert lib.mx_nvfp4_quantize_1x16(A16, 40, 32, 1, 0, 0, 0, 0, A16, A16, A16, A16, 16, NUL) == 3   # T % 16
     assert lib.mx_nvfp4_quantize_1x16(A16, 32, 32, 1, 0, 0, 7, 0, A16, A16, A16, A16, 16, NUL) == 1   # bad rounding
     assert lib.mx_nvfp4_quantize_1x16(A16, 32, 32, 1, 0, 0, 0, 0, A16, A16, A16, A16, 4, NUL) == 1    # workspace
+
+
+def test_fp8_blockwise_validation(lib):
+    f = lib.mx_fp8_blockwise_quantize_1x128
+    assert f(A16, 128, 256, 256, 0, NUL, NUL, NUL, NUL, NUL, NUL, NUL) == 1           # no output
+    assert f(A16, 128, 256, 256, 2, A16, A16, NUL, NUL, NUL, NUL, NUL) == 1           # pow2 not 0/1
+    assert f(A16, 128, 256, 256, 0, A16, A16, A16, NUL, NUL, NUL, NUL) == 1           # E8M0 layout needs pow2
+    assert f(A16, 128, 192, 192, 1, A16, A16, NUL, NUL, NUL, NUL, NUL) == 3           # cols % 128 (row-wise)
+    assert f(A16, 96, 256, 256, 1, NUL, NUL, NUL, A16, A16, NUL, NUL) == 3            # rows % 128 (column-wise)
+    assert f(A16, 128, 200, 200, 1, NUL, NUL, NUL, A16, A16, NUL, NUL) == 3           # cols % 16
+    assert f(A8, 128, 256, 256, 1, A16, A16, NUL, NUL, NUL, NUL, NUL) == 2            # misaligned input
+    assert f(A16, 128, 256, 252, 1, A16, A16, NUL, NUL, NUL, NUL, NUL) == 1           # ldx < cols
+    w = lib.mx_fp8_blockwise_quantize_128x128
+    assert w(A16, 1, 200, 256, 0, A16, A16, NUL, NUL, NUL, NUL) == 1                  # no scale output
+    assert w(A16, 1, 200, 256, 1, A16, A16, A16, A16, NUL, NUL) == 3                  # E8M0 layout needs O % 128
+    assert w(A16, 1, 200, 250, 1, A16, A16, A16, NUL, NUL, NUL) == 3                  # H % 16
+    assert w(A16, 0, 256, 256, 1, A16, A16, A16, NUL, NUL, NUL) == 1                  # G = 0
+    assert w(A16, 1, 256, 256, 0, A16, A16, A16, NUL, A16, NUL) == 1                  # E8M0 layout needs pow2
 
 
 def test_gemm_validation(lib):
