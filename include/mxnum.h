@@ -178,8 +178,8 @@ mx_status mx_nvfp4_quantize_weight_2d_noalloc(const void* w, int64_t G, int64_t 
  *           sf_row are an MXFP8 GEMM operand decoding to the same values (NULL: skip)
  *   q_col   [cols, rows] E4M3, s_col [cols, rows/128] FP32            (NULL q_col: skip column-wise)
  *   sf_col  pow2 only: mx_scale_bytes(cols, rows, 32) bytes, as sf_row for q_col (NULL: skip)
- * Requires cols % 128 == 0 for row-wise, rows % 128 == 0 for column-wise, cols % 16 == 0, ldx % 8 == 0;
- * pointers 16-byte aligned.  The rows/cols of the GEMM layout padding are not written. */
+ * Requires cols % 128 == 0 for row-wise, rows % 128 == 0 for column-wise, cols % 16 == 0, ldx % 8 == 0,
+ * rows * cols / 128 < 2^31; pointers 16-byte aligned.  The rows/cols of the GEMM layout padding are not written. */
 mx_status mx_fp8_blockwise_quantize_1x128(const void* x, int64_t rows, int64_t cols, int64_t ldx, int pow2,
                                           uint8_t* q_row, float* s_row, uint8_t* sf_row,
                                           uint8_t* q_col, float* s_col, uint8_t* sf_col, cudaStream_t stream);

@@ -37,7 +37,7 @@ cudaError_t launch_fp8_blockwise_1x128(const uint16_t* x, int64_t R, int64_t K, 
                                        uint8_t* sf_col, int num_sms, cudaStream_t stream);
 cudaError_t launch_fp8_blockwise_128x128(const uint16_t* w, int64_t G, int64_t O, int64_t H, bool pow2,
                                          uint8_t* q_row, uint8_t* q_col, float* s, uint8_t* sf_row, uint8_t* sf_col,
-                                         cudaStream_t stream);
+                                         int num_sms, cudaStream_t stream);
 cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const float* s2, int64_t rows_per_scale, int64_t R,
                            int64_t K, uint16_t* y, cudaStream_t stream);
 cudaError_t launch_mismatch(const uint8_t* x, const uint8_t* y, int64_t nbytes, unsigned long long* count,

@@ -171,6 +171,7 @@ mx_status mx_fp8_blockwise_quantize_1x128(const void* x, int64_t rows, int64_t c
     if ((cols % 16) != 0) return MX_ERR_UNSUPPORTED;
     if (q_row && (cols % 128) != 0) return MX_ERR_UNSUPPORTED;
     if (q_col && ((rows % 128) != 0 || rows / 128 > 65535)) return MX_ERR_UNSUPPORTED;
+    if (rows * (cols / 128) >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
     return from_cuda(mxk::launch_fp8_blockwise_1x128(static_cast<const uint16_t*>(x), rows, cols, ldx, pow2 != 0, q_row,
                                                       s_row, sf_row, q_col, s_col, sf_col, mxk::device_sm_count(),
                                                       stream));
@@ -189,7 +190,7 @@ mx_status mx_fp8_blockwise_quantize_128x128(const void* w, int64_t G, int64_t O,
     if ((O % 16) != 0 || (H % 16) != 0) return MX_ERR_UNSUPPORTED;
     if ((sf_row || sf_col) && ((O % 128) != 0 || (H % 128) != 0)) return MX_ERR_UNSUPPORTED;
     return from_cuda(mxk::launch_fp8_blockwise_128x128(static_cast<const uint16_t*>(w), G, O, H, pow2 != 0, q_row,
-                                                        q_col, s, sf_row, sf_col, stream));
+                                                        q_col, s, sf_row, sf_col, mxk::device_sm_count(), stream));
 }
 
 mx_status mx_rht16(const void* x, int64_t T, int64_t N, uint64_t seed, void* y, cudaStream_t stream) {

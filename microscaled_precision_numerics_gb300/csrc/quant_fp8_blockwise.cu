@@ -13,9 +13,12 @@
 //                   the MXFP8 GEMM scale layout (one byte per 32 elements), so the MXFP8 tensor-core
 //                   GEMM consumes power-of-two blockwise operands unchanged.
 //
-// Two kernels, both bound by HBM:
-//   fp8bw_rowwise_kernel   [1, 128] tiles along a row: 16 lanes per tile, 16-byte loads, four tile
-//                          pairs in flight per warp, a grid of resident CTAs striding over tile pairs.
+// Two kernels, both meant to run at the HBM roofline; the arithmetic per element is kept small:
+// block maxima on packed BF16 pairs (max of magnitudes, one instruction per pair), each BF16 value
+// widened once, one scale per block computed once per lane group.
+//   fp8bw_rowwise_kernel   [1, 128] tiles along a row: 4 lanes per tile (32 values each, four
+//                          16-byte loads), 8 tiles per warp and pass, RW_U passes in flight; a grid
+//                          of resident CTAs strides over the tiles.
 //   fp8bw_tile_kernel      one 128 x 128 BF16 tile per CTA (256 threads, 8 rows x 8 columns each):
 //                          WEIGHT mode -- one [128, 128] block: row-major codes, the same codes
 //                          transposed, one scale; ACT mode -- [1, 128] tiles along rows and/or along
@@ -43,15 +46,12 @@ __device__ __forceinline__ int pow2_exponent(uint32_t amax_bits) {
     return k < -127 ? -127 : (k > 127 ? 127 : k);
 }
 
-// 2^-k as FP32 (k in [-127, 126]: a normal number).
-__device__ __forceinline__ float pow2_neg(int k) { return __uint_as_float((uint32_t)(127 - k) << 23); }
-
-// The scale applied per element: multiply by `mul` (power of two) or divide by `div` (FP32 scale).
+// One block's scale: `f` is what each value is multiplied by (power of two: 2^-k) or divided by
+// (FP32: s, 0 for an all-zero block); `s` the stored FP32 scale; `e8` = k + 127 (power of two).
 struct BlockScale {
-    float mul;       // power of two: 2^-k; FP32: unused
-    float div;       // FP32: s (0 for an all-zero block); power of two: unused
-    float s;         // the stored FP32 scale
-    uint32_t e8;     // power of two: k + 127
+    float f;
+    float s;
+    uint32_t e8;
 };
 
 template <bool POW2>
@@ -60,46 +60,68 @@ __device__ __forceinline__ BlockScale block_scale(uint32_t amax_bf16) {
     const uint32_t bits = amax_bf16 << 16;
     if constexpr (POW2) {
         const int k = pow2_exponent(bits);
-        b.mul = pow2_neg(k);
-        b.div = 0.0f;
-        b.s = __uint_as_float((uint32_t)(k + 127) << 23);
-        if (k == -127) b.s = __uint_as_float(0x00400000u);   // 2^-127 (FP32 subnormal)
+        b.f = __uint_as_float((uint32_t)(127 - k) << 23);            // 2^-k, k <= 126 for finite BF16
+        b.s = k == -127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(k + 127) << 23);
         b.e8 = (uint32_t)(k + 127);
     } else {
         b.s = __fdiv_rn(__uint_as_float(bits), E4M3_MAX);
-        b.div = b.s;
-        b.mul = 0.0f;
+        b.f = b.s;
         b.e8 = 0;
     }
     return b;
 }
 
 template <bool POW2>
-__device__ __forceinline__ float scaled(float x, const BlockScale& b) {
+__device__ __forceinline__ float scaled(float x, float f) {
     if constexpr (POW2) {
-        return x * b.mul;
+        return x * f;
     } else {
-        return b.div == 0.0f ? x * 0.0f : __fdiv_rn(x, b.div);
+        return f == 0.0f ? x * 0.0f : __fdiv_rn(x, f);
     }
 }
 
-// Eight BF16 (one 16-byte chunk) -> eight E4M3 codes (two words, element 0 in the low byte).
+// max(|a|, |b|) of each BF16 half of two packed pairs; the sign bits of the result are meaningless
+// (masked once at the end of a reduction).  Inputs hold no NaN.
+__device__ __forceinline__ uint32_t max_abs2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Largest magnitude of the two halves of a reduced pair (BF16 bits, low 16 bits).
+__device__ __forceinline__ uint32_t fold_abs(uint32_t m) {
+    m &= 0x7FFF7FFFu;
+    return max(m & 0xFFFFu, m >> 16);
+}
+
+__device__ __forceinline__ uint32_t chunk_max_abs2(const uint4& v) {
+    return max_abs2(max_abs2(v.x, v.y), max_abs2(v.z, v.w));
+}
+
+// Eight BF16 values (one 16-byte chunk) widened to FP32.
+__device__ __forceinline__ void widen8(const uint4& v, float f[8]) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// Eight values, one scale -> eight E4M3 codes (element 0 in the low byte).
 template <bool POW2>
-__device__ __forceinline__ uint2 quant8(const uint4& v, const BlockScale& b) {
+__device__ __forceinline__ uint2 quant8(const float f[8], float s) {
     uint2 r;
-    r.x = cvt_e4m3x4(scaled<POW2>(bf16_lo(v.x), b), scaled<POW2>(bf16_hi(v.x), b), scaled<POW2>(bf16_lo(v.y), b),
-                     scaled<POW2>(bf16_hi(v.y), b));
-    r.y = cvt_e4m3x4(scaled<POW2>(bf16_lo(v.z), b), scaled<POW2>(bf16_hi(v.z), b), scaled<POW2>(bf16_lo(v.w), b),
-                     scaled<POW2>(bf16_hi(v.w), b));
+    r.x = cvt_e4m3x4(scaled<POW2>(f[0], s), scaled<POW2>(f[1], s), scaled<POW2>(f[2], s), scaled<POW2>(f[3], s));
+    r.y = cvt_e4m3x4(scaled<POW2>(f[4], s), scaled<POW2>(f[5], s), scaled<POW2>(f[6], s), scaled<POW2>(f[7], s));
     return r;
 }
 
-__device__ __forceinline__ uint32_t chunk_absmax(const uint4& v) {
-    uint32_t m = absmax_bf16x2(0u, v.x);
-    m = absmax_bf16x2(m, v.y);
-    m = absmax_bf16x2(m, v.z);
-    m = absmax_bf16x2(m, v.w);
-    return fold_halves(m);
+// Eight values, one scale per value (eight columns).
+template <bool POW2>
+__device__ __forceinline__ uint2 quant8_cols(const float f[8], const float s[8]) {
+    uint2 r;
+    r.x = cvt_e4m3x4(scaled<POW2>(f[0], s[0]), scaled<POW2>(f[1], s[1]), scaled<POW2>(f[2], s[2]),
+                     scaled<POW2>(f[3], s[3]));
+    r.y = cvt_e4m3x4(scaled<POW2>(f[4], s[4]), scaled<POW2>(f[5], s[5]), scaled<POW2>(f[6], s[6]),
+                     scaled<POW2>(f[7], s[7]));
+    return r;
 }
 
 __device__ __forceinline__ uint4 ldg16(const uint16_t* p) {
@@ -107,46 +129,76 @@ __device__ __forceinline__ uint4 ldg16(const uint16_t* p) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// [1, 128] tiles along rows.  Tile t = r * (K / 128) + b; a warp takes pairs of consecutive tiles
-// (lanes 0..15 the even one, 16..31 the odd one), RW_U pairs per pass.
+// [1, 128] tiles along rows.  Tile t = r * (K / 128) + b.  Lane l of a warp works on tile
+// (8 * pass + l / 4) with chunks (l % 4) + 4 j, j = 0..3 (8 values each): per load instruction the
+// warp reads 64 contiguous bytes of each of 8 tiles.  The row of a tile comes from a multiply-shift
+// division by K / 128 (exact for t < 2^31).
 // ---------------------------------------------------------------------------------------------
 constexpr int RW_THREADS = 256;
-constexpr int RW_U = 4;
+constexpr int RW_U = 2;
 constexpr int RW_CTAS_PER_SM = 4;
+
+// n / d = (n * m) >> (32 + l) for 0 <= n < 2^31, with l = ceil(log2 d) and m = ceil(2^(32+l) / d):
+// the product overshoots n / d by less than n / 2^(32+l) < 2^-l <= 1 / d, which cannot reach the next
+// integer.
+struct FastDiv {
+    uint64_t m;
+    uint32_t shift;
+};
+
+FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const unsigned __int128 num = (unsigned __int128)1 << (32 + l);
+    return FastDiv{(uint64_t)((num + d - 1) / d), 32 + l};
+}
+
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+    return (uint32_t)(((uint64_t)n * f.m) >> f.shift);
+}
 
 template <bool POW2>
 __global__ void __launch_bounds__(RW_THREADS, RW_CTAS_PER_SM)
-fp8bw_rowwise_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx, uint8_t* __restrict__ q,
-                     float* __restrict__ s, uint8_t* __restrict__ sf) {
+fp8bw_rowwise_kernel(const uint16_t* __restrict__ x, uint32_t R, uint32_t nb, int64_t ldx, uint8_t* __restrict__ q,
+                     float* __restrict__ s, uint8_t* __restrict__ sf, FastDiv div_nb) {
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4, c = lane & 15;
-    const int64_t nb = K >> 7, T = R * nb, pairs = (T + 1) >> 1;
-    const int64_t nct = nb;                        // 4-column tiles of the E8M0 layout per row band
-    const int64_t warp = (int64_t)blockIdx.x * (RW_THREADS / 32) + (threadIdx.x >> 5);
-    const int64_t nwarps = (int64_t)gridDim.x * (RW_THREADS / 32);
-    for (int64_t p0 = warp * RW_U; p0 < pairs; p0 += nwarps * RW_U) {
-        uint4 v[RW_U];
-        int64_t r[RW_U], b[RW_U];
+    const int sub = lane & 3;
+    const uint32_t T = R * nb;
+    const uint32_t warp = blockIdx.x * (RW_THREADS / 32) + (threadIdx.x >> 5);
+    const uint32_t nwarps = gridDim.x * (RW_THREADS / 32);
+    for (uint32_t t0 = warp * (8 * RW_U); t0 < T; t0 += nwarps * (8 * RW_U)) {
+        uint4 v[RW_U][4];
+        uint32_t tt[RW_U], rr[RW_U];
 #pragma unroll
         for (int u = 0; u < RW_U; ++u) {
-            const int64_t t = 2 * (p0 + u) + half;
-            r[u] = t / nb;
-            b[u] = t - r[u] * nb;
-            v[u] = t < T ? ldg16(x + r[u] * ldx + b[u] * 128 + c * 8) : make_uint4(0, 0, 0, 0);
+            const uint32_t t = t0 + 8 * u + (lane >> 2);
+            tt[u] = t;
+            const uint32_t r = fast_div(t, div_nb);
+            rr[u] = r;
+            const uint16_t* src = x + (int64_t)r * ldx + (t - r * nb) * 128 + sub * 8;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[u][j] = t < T ? ldg16(src + 32 * j) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < RW_U; ++u) {
-            uint32_t m = chunk_absmax(v[u]);
+            uint32_t m = max_abs2(chunk_max_abs2(v[u][0]), chunk_max_abs2(v[u][1]));
+            m = max_abs2(m, max_abs2(chunk_max_abs2(v[u][2]), chunk_max_abs2(v[u][3])));
+            m = max_abs2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+            m = max_abs2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            const uint32_t t = tt[u];
+            if (t >= T) continue;
+            const BlockScale bs = block_scale<POW2>(fold_abs(m));
+            uint8_t* dst = q + (int64_t)t * 128 + sub * 8;
 #pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-            if (r[u] >= R) continue;
-            const BlockScale bs = block_scale<POW2>(m);
-            const uint2 codes = quant8<POW2>(v[u], bs);
-            *reinterpret_cast<uint2*>(q + r[u] * K + b[u] * 128 + c * 8) = codes;
-            if (c == 0) {
-                s[r[u] * nb + b[u]] = bs.s;
+            for (int j = 0; j < 4; ++j) {
+                float f[8];
+                widen8(v[u][j], f);
+                *reinterpret_cast<uint2*>(dst + 32 * j) = quant8<POW2>(f, bs.f);
+            }
+            if (sub == 0) {
+                s[t] = bs.s;
                 if (POW2 && sf)
-                    *reinterpret_cast<uint32_t*>(sf + sf_offset(r[u], 4 * b[u], nct)) = bs.e8 * 0x01010101u;
+                    *reinterpret_cast<uint32_t*>(sf + sf_offset(rr[u], 4 * (t - rr[u] * nb), nb)) = bs.e8 * 0x01010101u;
             }
         }
     }
@@ -154,10 +206,10 @@ fp8bw_rowwise_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64
 
 // ---------------------------------------------------------------------------------------------
 // 128 x 128 tiles.  Thread t: column chunk c = t % 16 (columns 8c..8c+7 of the tile), row group
-// g = t / 16 (rows 8g..8g+7).  The transposed staging tile holds, for tile column j, 128 code bytes
-// (one per tile row) in 16 units of 8 bytes; unit g of column j sits at unit position g ^ (j / 8 % 16),
-// so a half-warp's 8-byte stores (16 different column chunks) and a quarter-warp's 16-byte loads
-// (one column's 128 bytes) are free of bank conflicts.
+// g = t / 16 (rows 8g..8g+7); a half-warp holds 8 whole rows.  The transposed staging tile holds,
+// for tile column j, 128 code bytes (one per tile row) in 16 units of 8 bytes; unit g of column j
+// sits at unit position g ^ (j / 8 % 16), so a half-warp's 8-byte stores (16 different column
+// chunks) and a quarter-warp's 16-byte loads (one column's 128 bytes) are free of bank conflicts.
 // ---------------------------------------------------------------------------------------------
 constexpr int TL_THREADS = 256;
 constexpr int TL_CTAS_PER_SM = 3;
@@ -217,10 +269,33 @@ __device__ __forceinline__ void store_transposed(const uint8_t* st, uint8_t* out
     }
 }
 
+// Row maxima of the 8 rows a half-warp holds (a[i] = this lane's packed pair maximum of row i):
+// a butterfly that halves the rows kept at each step, so lane c of the half-warp ends with the
+// maximum of row c / 2 (8 shuffles instead of 32).
+__device__ __forceinline__ uint32_t half_warp_row_max(const uint32_t a[8], int c) {
+    uint32_t b[4], d[2];
+    const bool h8 = c & 8, h4 = c & 4, h2 = c & 2;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t send = h8 ? a[k] : a[k + 4], keep = h8 ? a[k + 4] : a[k];
+        b[k] = max_abs2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 8));
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint32_t send = h4 ? b[k] : b[k + 2], keep = h4 ? b[k + 2] : b[k];
+        d[k] = max_abs2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 4));
+    }
+    const uint32_t send = h2 ? d[0] : d[1], keep = h2 ? d[1] : d[0];
+    uint32_t e = max_abs2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 2));
+    e = max_abs2(e, __shfl_xor_sync(0xFFFFFFFFu, e, 1));
+    return fold_abs(e);
+}
+
 template <int MODE, bool POW2, bool ROW, bool COL>
-__global__ void __launch_bounds__(TL_THREADS, (ROW && COL) ? 2 : TL_CTAS_PER_SM) fp8bw_tile_kernel(const TileArgs a) {
+__global__ void __launch_bounds__(TL_THREADS, (ROW && COL && !POW2) ? 2 : TL_CTAS_PER_SM) fp8bw_tile_kernel(const TileArgs a) {
     __shared__ __align__(16) uint8_t st[128 * 128];
     __shared__ uint32_t red[8][16][4];
+    __shared__ __align__(16) float colf[128];
     __shared__ uint32_t red_all[8];
 
     const int t = threadIdx.x, c = t & 15, g = t >> 4, warp = t >> 5;
@@ -239,19 +314,23 @@ __global__ void __launch_bounds__(TL_THREADS, (ROW && COL) ? 2 : TL_CTAS_PER_SM)
 
     uint2 cw[8];
     if constexpr (MODE == MODE_WEIGHT) {
-        uint32_t m = 0;
+        uint32_t m = chunk_max_abs2(v[0]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m = max(m, chunk_absmax(v[i]));
+        for (int i = 1; i < 8; ++i) m = max_abs2(m, chunk_max_abs2(v[i]));
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if ((t & 31) == 0) red_all[warp] = m;
+        for (int o = 16; o >= 1; o >>= 1) m = max_abs2(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if ((t & 31) == 0) red_all[warp] = fold_abs(m);
         __syncthreads();
-        m = red_all[0];
+        uint32_t amax = red_all[0];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) m = max(m, red_all[w]);
-        const BlockScale bs = block_scale<POW2>(m);
+        for (int w = 1; w < 8; ++w) amax = max(amax, red_all[w]);
+        const BlockScale bs = block_scale<POW2>(amax);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cw[i] = quant8<POW2>(v[i], bs);
+        for (int i = 0; i < 8; ++i) {
+            float f[8];
+            widen8(v[i], f);
+            cw[i] = quant8<POW2>(f, bs.f);
+        }
 
         const int64_t tr = gridDim.y, tc = gridDim.x;
         uint8_t* q_row = a.q_row + bz * R * C;
@@ -278,74 +357,76 @@ __global__ void __launch_bounds__(TL_THREADS, (ROW && COL) ? 2 : TL_CTAS_PER_SM)
         __syncthreads();
         store_transposed(st, q_col, R, r0, c0, R, C);
     } else {
+        // Row scales ([1, 128] tiles along rows): lane c of each half-warp owns row 8g + c / 2.
+        float rowf[8];
         if constexpr (ROW) {
-            // [1, 128] tiles along the row: the 16 lanes of a half-warp hold one row's 128 values.
+            uint32_t rm[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint32_t m = chunk_absmax(v[i]);
-#pragma unroll
-                for (int o = 8; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-                const BlockScale bs = block_scale<POW2>(m);
-                const uint2 codes = quant8<POW2>(v[i], bs);
-                const int64_t r = r0 + 8 * g + i;
-                *reinterpret_cast<uint2*>(a.q_row + r * C + c0 + 8 * c) = codes;
-                if (c == 0) {
-                    a.s_row[r * (C >> 7) + blockIdx.x] = bs.s;
-                    if (POW2 && a.sf_row)
-                        *reinterpret_cast<uint32_t*>(a.sf_row + sf_offset(r, 4 * (int64_t)blockIdx.x, C >> 7)) =
-                            bs.e8 * 0x01010101u;
-                }
+            for (int i = 0; i < 8; ++i) rm[i] = chunk_max_abs2(v[i]);
+            const BlockScale bs = block_scale<POW2>(half_warp_row_max(rm, c));
+            const int64_t r = r0 + 8 * g + (c >> 1);
+            if ((c & 1) == 0) {
+                a.s_row[r * (C >> 7) + blockIdx.x] = bs.s;
+                if (POW2 && a.sf_row)
+                    *reinterpret_cast<uint32_t*>(a.sf_row + sf_offset(r, 4 * (int64_t)blockIdx.x, C >> 7)) =
+                        bs.e8 * 0x01010101u;
             }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rowf[i] = __shfl_sync(0xFFFFFFFFu, bs.f, (t & 16) | (2 * i));
         }
+        // Column scales ([1, 128] tiles along columns): packed maxima of the thread's 8 rows, then
+        // over the 16 row groups (lane pair, then the 8 warps); thread j < 128 finishes column j.
+        float cf[8];
         if constexpr (COL) {
-            // [1, 128] tiles along the column (128 rows of one column): per-column maxima of the
-            // thread's 8 rows, then over the 16 row groups (lane pair, then the 8 warps).
             uint32_t cm[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                uint32_t m = 0;
+                uint32_t m = j == 0 ? v[0].x : j == 1 ? v[0].y : j == 2 ? v[0].z : v[0].w;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t w = j == 0 ? v[i].x : j == 1 ? v[i].y : j == 2 ? v[i].z : v[i].w;
-                    m = absmax_bf16x2(m, w);
-                }
-                m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
-                cm[j] = m;
+                for (int i = 1; i < 8; ++i)
+                    m = max_abs2(m, j == 0 ? v[i].x : j == 1 ? v[i].y : j == 2 ? v[i].z : v[i].w);
+                cm[j] = max_abs2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
             }
             if ((t & 31) < 16) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) red[warp][c][j] = cm[j];
             }
             __syncthreads();
+            if (t < 128) {
+                const int cc = t >> 3, word = (t & 7) >> 1;
+                uint32_t m = red[0][cc][word];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t m = red[0][c][j];
-#pragma unroll
-                for (int w = 1; w < 8; ++w) m = __vmaxu2(m, red[w][c][j]);
-                cm[j] = m;
-            }
-            BlockScale bs[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) bs[j] = block_scale<POW2>(j & 1 ? cm[j >> 1] >> 16 : cm[j >> 1] & 0xFFFFu);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint4 w = v[i];
-                cw[i].x = cvt_e4m3x4(scaled<POW2>(bf16_lo(w.x), bs[0]), scaled<POW2>(bf16_hi(w.x), bs[1]),
-                                     scaled<POW2>(bf16_lo(w.y), bs[2]), scaled<POW2>(bf16_hi(w.y), bs[3]));
-                cw[i].y = cvt_e4m3x4(scaled<POW2>(bf16_lo(w.z), bs[4]), scaled<POW2>(bf16_hi(w.z), bs[5]),
-                                     scaled<POW2>(bf16_lo(w.w), bs[6]), scaled<POW2>(bf16_hi(w.w), bs[7]));
-            }
-            if (g == 0 && col_ok) {
-                const int64_t nbr = R >> 7;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int64_t col = c0 + 8 * c + j;
-                    a.s_col[col * nbr + blockIdx.y] = bs[j].s;
+                for (int w = 1; w < 8; ++w) m = max_abs2(m, red[w][cc][word]);
+                m &= 0x7FFF7FFFu;
+                const BlockScale bs = block_scale<POW2>((t & 1) ? (m >> 16) : (m & 0xFFFFu));
+                colf[t] = bs.f;
+                const int64_t col = c0 + t;
+                if (col < C) {
+                    const int64_t nbr = R >> 7;
+                    a.s_col[col * nbr + blockIdx.y] = bs.s;
                     if (POW2 && a.sf_col)
                         *reinterpret_cast<uint32_t*>(a.sf_col + sf_offset(col, 4 * (int64_t)blockIdx.y, nbr)) =
-                            bs[j].e8 * 0x01010101u;
+                            bs.e8 * 0x01010101u;
                 }
             }
+            __syncthreads();
+            const float4 f0 = *reinterpret_cast<const float4*>(colf + 8 * c);
+            const float4 f1 = *reinterpret_cast<const float4*>(colf + 8 * c + 4);
+            cf[0] = f0.x; cf[1] = f0.y; cf[2] = f0.z; cf[3] = f0.w;
+            cf[4] = f1.x; cf[5] = f1.y; cf[6] = f1.z; cf[7] = f1.w;
+        }
+        // Each value widened once, quantized with its row scale and with its column scale.
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float f[8];
+            widen8(v[i], f);
+            if constexpr (ROW) {
+                const int64_t r = r0 + 8 * g + i;
+                *reinterpret_cast<uint2*>(a.q_row + r * C + c0 + 8 * c) = quant8<POW2>(f, rowf[i]);
+            }
+            if constexpr (COL) cw[i] = quant8_cols<POW2>(f, cf);
+        }
+        if constexpr (COL) {
             stage_transposed(st, cw, c, g);
             __syncthreads();
             store_transposed(st, a.q_col, R, r0, c0, R, C);
@@ -363,12 +444,13 @@ cudaError_t launch_tile(const TileArgs& a, int64_t G, cudaStream_t stream) {
 template <bool POW2>
 cudaError_t launch_rowwise(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q, float* s, uint8_t* sf,
                            int num_sms, cudaStream_t stream) {
-    const int64_t pairs = (R * (K >> 7) + 1) >> 1;
-    const int64_t warps = (pairs + RW_U - 1) / RW_U;
+    const int64_t tiles = R * (K >> 7);
+    const int64_t warps = (tiles + 8 * RW_U - 1) / (8 * RW_U);
     const int64_t need = (warps + RW_THREADS / 32 - 1) / (RW_THREADS / 32);
     const int64_t resident = (int64_t)num_sms * RW_CTAS_PER_SM;
     const unsigned grid = (unsigned)(need < resident ? need : resident);
-    fp8bw_rowwise_kernel<POW2><<<grid, RW_THREADS, 0, stream>>>(x, R, K, ldx, q, s, sf);
+    fp8bw_rowwise_kernel<POW2><<<grid, RW_THREADS, 0, stream>>>(x, (uint32_t)R, (uint32_t)(K >> 7), ldx, q, s, sf,
+                                                                 make_fastdiv((uint32_t)(K >> 7)));
     return cudaGetLastError();
 }
 
@@ -395,7 +477,8 @@ cudaError_t launch_fp8_blockwise_1x128(const uint16_t* x, int64_t R, int64_t K, 
 
 cudaError_t launch_fp8_blockwise_128x128(const uint16_t* w, int64_t G, int64_t O, int64_t H, bool pow2,
                                          uint8_t* q_row, uint8_t* q_col, float* s, uint8_t* sf_row, uint8_t* sf_col,
-                                         cudaStream_t stream) {
+                                         int num_sms, cudaStream_t stream) {
+    (void)num_sms;
     TileArgs a{};
     a.x = w; a.R = O; a.C = H; a.ldx = H; a.x_batch = O * H;
     a.q_row = q_row; a.q_col = q_col; a.s_blk = s;
