@@ -5,7 +5,8 @@ Default step (workload ``dense_mlp``, the Qwen3-8B-shaped MLP linear): MXFP8 row
 quantization of X [8192, 4096], W [12288, 4096] and dY [8192, 12288], then the three MXFP8
 block-scaled GEMMs FPROP (Y = X W^T), DGRAD (dX = dY W) and WGRAD (dW = dY^T X) with BF16 output.
 The metric is the step's GEMM throughput with its quantization included: 2.474 TFLOP per step /
-step time.  Other workloads (``--workload moe|wgrad|weight_sync``) time the NVFP4 paths.
+step time.  Other workloads (``--workload moe|moe_mxfp8|dense_fp8_blockwise|wgrad|weight_sync``) time the
+NVFP4 paths, the grouped MXFP8 MoE layer and blockwise FP8 (power-of-two scales on the MXFP8 GEMM).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxnum|reference] [--workload ...]
 
@@ -409,6 +410,81 @@ class WGrad:
                 "tokens": self.T, "hidden": self.H, "ffn": self.F}
 
 
+class DenseBlockwise:
+    """The Qwen3-8B MLP linear of the default step with DeepSeek-V3-style blockwise FP8 and power-of-two
+    scales (the learner's form on Blackwell): [1, 128] row + column tiles of X and dY from one read each,
+    [128, 128] blocks of W in both orientations, E8M0 scale bytes written straight into the MXFP8 GEMM
+    layout, then FPROP, DGRAD and WGRAD on the MXFP8 tensor-core GEMM.  Aux: the FP32-scale quantizers
+    (the sampler's form) of X and W."""
+    name = "dense_fp8_blockwise"
+    dtype = "e4m3 (f32 accumulate, bf16 out)"
+
+    def __init__(self, mx, torch, dev, tokens=8192, hidden=4096, ffn=12288):
+        import synthetic
+        self.mx, self.torch, self.dev = mx, torch, dev
+        data = synthetic.dense_mlp(tokens, hidden, ffn)
+        bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.x, self.w, self.dy = bf(data["x"]), bf(data["w"]), bf(data["dy"])
+        T, H, F = tokens, hidden, ffn
+        self.T, self.H, self.F = T, H, F
+        u8 = lambda *shape: torch.zeros(shape, dtype=torch.uint8, device=dev)
+        f32 = lambda *shape: torch.zeros(shape, dtype=torch.float32, device=dev)
+
+        def act(R, C):
+            return {"q_row": u8(R, C), "s_row": f32(R, C // 128), "sf_row": u8(mx.scale_bytes(R, C, 32)),
+                    "q_col": u8(C, R), "s_col": f32(C, R // 128), "sf_col": u8(mx.scale_bytes(C, R, 32))}
+        self.qx, self.qdy = act(T, H), act(T, F)
+        self.qw = {"q_row": u8(1, F, H), "q_col": u8(1, H, F), "s": f32(1, F // 128, H // 128),
+                   "sf_row": u8(mx.scale_bytes(F, H, 32)), "sf_col": u8(mx.scale_bytes(H, F, 32))}
+        self.fx = {"q_row": u8(T, H), "s_row": f32(T, H // 128)}
+        self.fw = {"q_row": u8(1, F, H), "q_col": u8(1, H, F), "s": f32(1, F // 128, H // 128)}
+        self.y = torch.empty((T, F), dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.dw = torch.empty((F, H), dtype=torch.bfloat16, device=dev)
+        self.launches_per_step = 6
+
+    def ops(self):
+        mx, F8 = self.mx, self.mx.MX_FMT_MXFP8
+        T, H, F = self.T, self.H, self.F
+        act_per = 2 + 2 + 2 * (4 + 4) / 128      # BF16 read, two code copies, FP32 + E8M0 scales per copy
+        w_per = 2 + 2
+        qx, qdy, qw = self.qx, self.qdy, self.qw
+        return [
+            ("quant", "blockwise 1x128 row+col X", 1, T * H * act_per,
+             lambda: mx.mx_fp8_blockwise_quantize_1x128(self.x, True, **qx)),
+            ("quant", "blockwise 128x128 W", 1, F * H * w_per,
+             lambda: mx.mx_fp8_blockwise_quantize_128x128(self.w[None], True, qw["q_row"], qw["q_col"], qw["s"],
+                                                          sf_row=qw["sf_row"], sf_col=qw["sf_col"])),
+            ("quant", "blockwise 1x128 row+col dY", 1, T * F * act_per,
+             lambda: mx.mx_fp8_blockwise_quantize_1x128(self.dy, True, **qdy)),
+            ("gemm8", "FPROP", 0, 2.0 * T * F * H,
+             lambda: mx.mx_scaled_gemm(F8, qx["q_row"], qx["sf_row"], None, 0, qw["q_row"][0], qw["sf_row"], None, 0,
+                                       T, F, H, self.y)),
+            ("gemm8", "DGRAD", 0, 2.0 * T * H * F,
+             lambda: mx.mx_scaled_gemm(F8, qdy["q_row"], qdy["sf_row"], None, 0, qw["q_col"][0], qw["sf_col"], None, 0,
+                                       T, H, F, self.dx)),
+            ("gemm8", "WGRAD", 0, 2.0 * F * H * T,
+             lambda: mx.mx_scaled_gemm(F8, qdy["q_col"], qdy["sf_col"], None, 0, qx["q_col"], qx["sf_col"], None, 0,
+                                       F, H, T, self.dw)),
+        ]
+
+    def aux_ops(self):
+        """FP32-scale blockwise quantizers (the sampler's form): X row-wise, W both orientations."""
+        mx, T, H, F = self.mx, self.T, self.H, self.F
+        return [
+            ("quant", "blockwise 1x128 row FP32-scale X", 1, T * H * (2 + 1 + 4 / 128),
+             lambda: mx.mx_fp8_blockwise_quantize_1x128(self.x, False, q_row=self.fx["q_row"], s_row=self.fx["s_row"])),
+            ("quant", "blockwise 128x128 FP32-scale W", 1, F * H * 4,
+             lambda: mx.mx_fp8_blockwise_quantize_128x128(self.w[None], False, self.fw["q_row"], self.fw["q_col"],
+                                                          self.fw["s"])),
+        ]
+
+    def config(self):
+        return {"workload": "dense_fp8_blockwise: Qwen3-8B MLP linear, blockwise FP8 (power-of-two scales) "
+                            "X/dY 1x128 row+col, W 128x128 + FPROP/DGRAD/WGRAD on the MXFP8 GEMM",
+                "tokens": self.T, "hidden": self.H, "ffn": self.F}
+
+
 class WeightSync:
     """Weight-sync sweep: 48 layers of 128 experts x {2048x768, 768x2048, 768x2048}; per matrix
     stack MXFP8 row+col quantize, dequantize, re-quantize and byte compare; NVFP4 2D quantize,
@@ -611,6 +687,8 @@ def run_workload(args):
         work = MoE(mx, torch, dev, experts=args.experts)
     elif args.workload == "moe_mxfp8":
         work = MoE8(mx, torch, dev, experts=args.experts)
+    elif args.workload == "dense_fp8_blockwise":
+        work = DenseBlockwise(mx, torch, dev)
     else:
         work = WGrad(mx, torch, dev)
     ops = work.ops()
@@ -839,7 +917,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mxnum", "reference"], default="mxnum")
-    ap.add_argument("--workload", choices=["dense_mlp", "moe", "moe_mxfp8", "wgrad", "weight_sync"], default="dense_mlp")
+    ap.add_argument("--workload", choices=["dense_mlp", "moe", "moe_mxfp8", "dense_fp8_blockwise", "wgrad", "weight_sync"], default="dense_mlp")
     ap.add_argument("--layers", type=int, default=48, help="weight_sync: layers swept")
     ap.add_argument("--experts", type=int, default=128, help="moe / weight_sync: experts (fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
