@@ -261,6 +261,28 @@ mx_status mx_scaled_gemm(mx_format fmt,
                          const uint8_t* b, const uint8_t* sb, const float* alpha_b, mx_scope alpha_b_scope,
                          int64_t M, int64_t N, int64_t K, void* d, int64_t ldd, cudaStream_t stream);
 
+/* BF16 GEMM with a dequantized-NVFP4 B operand expanded inside the GEMM (the "dequantized backward"
+ * without a BF16 copy of B in HBM):
+ *   D[m, n] = BF16( alpha_a[m or 0] * sum_k A[m, k] * DQ(B)[n, k] ),
+ *   DQ(B)[n, k] = BF16( fp32(val(q) * val(bs)) * S ), the values mx_dequantize_bf16 writes for B.
+ * Source: 4-bitter page, "dequantized backward" -- the backward GEMMs use BF16 operands rebuilt from the
+ * forward's exact NVFP4 values (y = x * DQ(Q(w))), which cut the peak memory by 70 % (150 -> 45 MB for a
+ * 2k x 2k input and 8k output features); MaxText page (2D weight blocks give the same values in the FPROP
+ * and DGRAD orientations).  Data gradient of a linear layer: A = dY [T, O] BF16, B = the column-wise codes
+ * of the 2D-quantized weight [H, O/2] with their scales and S_w, D = dX [T, H].
+ *   a      [M, K] BF16, contiguous (row pitch K)
+ *   alpha_a NULL / MX_SCOPE_NONE, one FP32 (MX_SCOPE_TENSOR) or M FP32 (MX_SCOPE_ROW)
+ *   qb     [N, K/2] E2M1 codes (even element in the low nibble); sb mx_scale_bytes(N, K, 16) E4M3 scales
+ *          in the GEMM layout; sb2 the FP32 second-level scale: one value (MX_SCOPE_TENSOR) or one per B
+ *          row (MX_SCOPE_ROW)
+ *   d      [M, ldd] BF16
+ * FP32 accumulation in the tensor core (kind::f16), summation order the hardware's.  Requires K % 64 == 0,
+ * N % 8 == 0, ldd % 8 == 0, ldd >= N, M, N < 2^31; a, qb, sb, d 16-byte aligned.  Persistent clusters of
+ * two CTAs on 256 x 256 tiles. */
+mx_status mx_gemm_bf16_dq_nvfp4(const void* a, const float* alpha_a, mx_scope alpha_a_scope, const uint8_t* qb,
+                                const uint8_t* sb, const float* sb2, mx_scope sb2_scope, int64_t M, int64_t N,
+                                int64_t K, void* d, int64_t ldd, cudaStream_t stream);
+
 /* Grouped block-scaled GEMM over expert-sorted rows: for every group g,
  *   D[rows of g] = BF16( alpha_a[row] * alpha_b[g] * A[rows of g] . B_g^T ).
  * Source: Miles page -- NVFP4 on the routed experts' weights and activations with a per-token

@@ -62,6 +62,7 @@ def lib() -> ctypes.CDLL:
                 "mx_scaled_gemm": (I32, [I32, P, P, P, I32, P, P, P, I32, I64, I64, I64, P, I64, P]),
                 "mx_grouped_scaled_gemm": (I32, [I32, I64, P, I64, P, P, P, P, P, P, I64, I64, P, P]),
                 "mx_count_mismatch": (I32, [P, P, I64, P, P]),
+                "mx_gemm_bf16_dq_nvfp4": (I32, [P, P, I32, P, P, P, I32, I64, I64, I64, P, I64, P]),
                 "mx_check_device_status": (I32, []),
             }
             for name, (res, args) in sigs.items():
@@ -234,6 +235,18 @@ def mx_scaled_gemm(fmt: int, a, sa, alpha_a, alpha_a_scope: int, b, sb, alpha_b,
     _check("mx_scaled_gemm", lib().mx_scaled_gemm(
         fmt, _p(a), _p(sa), _p(alpha_a), alpha_a_scope, _p(b), _p(sb), _p(alpha_b), alpha_b_scope,
         M, N, K, _p(d), d.stride(0), _stream(stream)))
+
+
+def mx_gemm_bf16_dq_nvfp4(a, qb, sb, sb2, sb2_scope, M: int, N: int, K: int, d, alpha_a=None, alpha_a_scope=0,
+                          stream=None):
+    """D = BF16(alpha_a * A @ DQ(B)^T) with A BF16 [M, K] and B NVFP4 codes [N, K/2] + GEMM-layout scales + FP32
+    second-level scale(s) sb2 (MX_SCOPE_TENSOR or MX_SCOPE_ROW), B expanded to BF16 inside the GEMM."""
+    a = _bf16_bits(a)
+    if a.stride(0) != K or a.stride(1) != 1:
+        raise ValueError("A must be a contiguous [M, K] BF16 tensor")
+    _check("mx_gemm_bf16_dq_nvfp4", lib().mx_gemm_bf16_dq_nvfp4(
+        _p(a), _p(alpha_a), int(alpha_a_scope), _p(qb), _p(sb), _p(sb2), int(sb2_scope), M, N, K, _p(d), d.stride(0),
+        _stream(stream)))
 
 
 def mx_grouped_scaled_gemm(fmt: int, group_offsets, a, sa, alpha_a_rows, b, sb, alpha_b_groups, N: int, K: int, d,

@@ -582,6 +582,335 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 }
 
 // ---------------------------------------------------------------------------------------------
+// Dequantize-in-mainloop BF16 GEMM (the dequantized backward of the 4-bitter page: the backward
+// GEMMs take BF16 operands rebuilt from the forward's NVFP4 values, y = x * DQ(Q(w))):
+//   D[m, n] = BF16( alpha_a[m] * sum_k A[m, k] * DQ(B)[n, k] ),
+//   DQ(B)[n, k] = BF16( fp32(val(q) * val(bs)) * S ),  S per B tensor or per B row,
+// i.e. exactly the values mx_dequantize_bf16 would write, without that BF16 copy of B in HBM: B is
+// read as NVFP4 codes + E4M3 scales and expanded in shared memory.  Same CTA-pair structure as the
+// block-scaled kernel (256 x 256 tiles, tcgen05.mma.cta_group::2, here kind::f16 with BF16 operands
+// and FP32 accumulation), two accumulators (512 TMEM columns) so the drain of one tile overlaps the
+// next tile's MMAs, and four converter warps per CTA:
+//   warp 0        TMA: A (BF16, 128 rows x 64 values per stage) signalling the even CTA's stage
+//                 barrier; this CTA's 128 B rows of codes (32 bytes each) and their scale atom into
+//                 a local barrier
+//   warp 1        (even CTA) the pair MMAs, 4 per stage (K = 16 each)
+//   warps 2..9    epilogue (32-column chunks: tcgen05.ld, row factor, BF16, TMA store)
+//   warps 10..13  converters: thread r expands B row r of this CTA's half for the stage (64 values:
+//                 E2M1 pairs to FP16, exact product with the FP16 block scale, times S in FP32,
+//                 round to BF16) into the 128-byte-swizzled K-major tile the MMA descriptor expects,
+//                 fences the generic-proxy writes for the tensor core and arrives (one lane per warp)
+//                 on the even CTA's stage barrier
+// ---------------------------------------------------------------------------------------------
+constexpr int DQ_THREADS = 448;
+constexpr int DQ_TN = 256;
+constexpr int DQ_CONV_WARP0 = 10;
+
+struct DqCfg {
+    static constexpr int NST = 5;
+    static constexpr int A_BYTES = 128 * BKB;              // 128 rows x 64 BF16
+    static constexpr int B_BYTES = 128 * BKB;              // this CTA's 128 B rows x 64 BF16 (built here)
+    static constexpr int Q_BYTES = 128 * 32;               // their codes, 64 E2M1 values per row
+    static constexpr int SF_BYTES = 512;                   // their scale atom (4 scales per row)
+    static constexpr uint32_t A_TX = 2u * A_BYTES;         // both CTAs' A rows, on the even CTA's barrier
+    static constexpr uint32_t Q_TX = Q_BYTES + SF_BYTES;   // per CTA, on its own barrier
+    static constexpr int FULL_ARRIVALS = 1 + 2 * 4;        // producer + four converter warps per CTA
+    static constexpr int SMEM_A = 0;
+    static constexpr int SMEM_B = SMEM_A + NST * A_BYTES;
+    static constexpr int SMEM_Q = SMEM_B + NST * B_BYTES;
+    static constexpr int SMEM_SF = SMEM_Q + NST * Q_BYTES;
+    static constexpr int SMEM_EPI = (SMEM_SF + NST * SF_BYTES + 1023) / 1024 * 1024;
+    static constexpr int SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
+    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (3 * NST + 5);
+    static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024;
+    static_assert(SMEM_B % 1024 == 0 && SMEM_Q % 1024 == 0 && SMEM_EPI % 1024 == 0, "alignment");
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+// kind::f16 instruction descriptor: D FP32 (bits 4-5 = 1), A and B BF16 (7-9, 10-12 = 1), K-major
+// A and B, N >> 3 (17-22), M >> 4 (24-28).
+template <int MMA_M, int MMA_N>
+__device__ __forceinline__ uint32_t make_idesc_bf16() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(MMA_N >> 3) << 17) | ((uint32_t)(MMA_M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc2_mma_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
+}
+
+// One E4M3 scale byte -> the same FP16 value in both halves (exact).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t byte) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(r) : "r"(byte * 0x0101u));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Eight E2M1 codes (one word, element 0 in the low nibble) of one 16-block -> four BF16 pairs:
+// BF16(fp32(val(q) * val(bs)) * S).  val(q) * val(bs) has at most 6 significant bits and lies in
+// [2^-10, 2688], so the FP16 product is exact and equals the FP32 one.
+__device__ __forceinline__ uint4 dq_word(uint32_t w, uint32_t bs_h2, float S) {
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t prod = hmul2_u32(e2m1x2_to_f16x2((w >> (8 * j)) & 0xFFu), bs_h2);
+        const float f0 = __half2float(__ushort_as_half((unsigned short)(prod & 0xFFFFu)));
+        const float f1 = __half2float(__ushort_as_half((unsigned short)(prod >> 16)));
+        o[j] = pack_bf16x2(__fmul_rn(f0, S), __fmul_rn(f1, S));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+struct DqParams {
+    const float* alpha_a; int alpha_a_scope;
+    const float* sb2; int sb2_scope;        // B's FP32 second-level scale: 1 = one value, 2 = per B row
+    int64_t M, N, K;
+    uint16_t* d; int64_t ldd;
+    int64_t m_tiles, n_tiles, k_stages, nct, total_tiles;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DQ_THREADS, 1)
+dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmSB, const __grid_constant__ CUtensorMap tmD,
+                    const DqParams p) {
+    using C = DqCfg;
+    constexpr int NST = C::NST;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + C::SMEM_BAR;            // NST (even CTA): A bytes + converter arrivals
+    const uint32_t bar_qfull = bar_full + 8 * NST;            // NST (each CTA): codes + scale atom
+    const uint32_t bar_empty = bar_qfull + 8 * NST;           // NST (each CTA): the stage's MMAs are done
+    const uint32_t bar_tfull = bar_empty + 8 * NST;           // 2
+    const uint32_t bar_tempty = bar_tfull + 16;               // 2 (even CTA)
+    const uint32_t bar_done = bar_tempty + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(bar_full + 8 * s, C::FULL_ARRIVALS);
+            mbar_init(bar_qfull + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_tfull + 8 * b, 1);
+            mbar_init(bar_tempty + 8 * b, 2 * EPI_WARPS);
+        }
+        mbar_init(bar_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmQ) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmSB) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmD) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int64_t total_tiles = p.total_tiles;
+    const int64_t pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    Params tp{};                                               // the tile schedule's view
+    tp.M = p.M; tp.N = p.N; tp.m_tiles = p.m_tiles; tp.n_tiles = p.n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------- producer (both CTAs) -------------------------------
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
+            const PairTile tile = pair_dense_tile<DQ_TN>(tp, t, rank);
+            const int64_t brow = tile.n0 + 128 * (int64_t)rank;
+            const int64_t band = brow / 128;
+            for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                if (elect_one()) {
+                    const uint32_t fb = map_to_cta(bar_full + 8 * stage, 0);
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_TX);
+                    tma_load_2d_pair(sbase + C::SMEM_A + stage * C::A_BYTES, &tmA, (int32_t)(ks * BKB), (int32_t)tile.row0, fb);
+                    const uint32_t qb = bar_qfull + 8 * stage;
+                    mbar_arrive_expect_tx(qb, C::Q_TX);
+                    tma_load_2d(sbase + C::SMEM_Q + stage * C::Q_BYTES, &tmQ, (int32_t)(ks * 32), (int32_t)brow, qb);
+                    tma_load_2d(sbase + C::SMEM_SF + stage * C::SF_BYTES, &tmSB, 0, (int32_t)((band * p.nct + ks) * 2), qb);
+                }
+                __syncwarp();
+                if (++stage == NST) { stage = 0; phase ^= 1; }
+            }
+        }
+        if (!ok && lane == 0) *abort_flag = 1;
+    } else if (warp == 1) {
+        // ------------------------------- MMA (even CTA) -------------------------------
+        if (leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true, issued_any = false;
+            int64_t ti = 0;
+            for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs, ++ti) {
+                const uint32_t ab = (uint32_t)(ti & 1);
+                const uint32_t use = (uint32_t)(ti >> 1);
+                if (!warp_wait(bar_tempty + 8 * ab, (use & 1u) ^ 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t tacc = tmem + ab * DQ_TN;
+                for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                    if (!warp_wait(bar_full + 8 * stage, phase, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                    tc_fence_after();
+                    if (elect_one()) {
+                        const uint32_t sA = sbase + C::SMEM_A + stage * C::A_BYTES;
+                        const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES;
+#pragma unroll
+                        for (int j = 0; j < BKB / 32; ++j)
+                            tc2_mma_bf16(tacc, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j),
+                                         make_idesc_bf16<2 * BM, DQ_TN>(), (ks > 0 || j > 0) ? 1u : 0u);
+                        tc2_commit_mc(bar_empty + 8 * stage, (uint16_t)3);
+                    }
+                    __syncwarp();
+                    issued_any = true;
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                if (elect_one()) tc2_commit_mc(bar_tfull + 8 * ab, (uint16_t)3);
+                __syncwarp();
+            }
+            if (issued_any) {
+                if (elect_one()) {
+                    tc2_commit_mc(bar_done, (uint16_t)1);
+                    const unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(bar_done, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
+                }
+                __syncwarp();
+            }
+        }
+    } else if (warp < DQ_CONV_WARP0) {
+        // ------------------------------- epilogue (both CTAs) -------------------------------
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        const uint32_t tempty_leader = map_to_cta(bar_tempty, 0);
+        const uint32_t ebase = sbase + C::SMEM_EPI + (uint32_t)((warp - 2) * 2 * EPI_BUF_BYTES);
+        uint32_t epi_chunk = 0;
+        int64_t ti = 0;
+        for (int64_t t = pair_id; t < total_tiles; t += n_pairs, ++ti) {
+            const PairTile tile = pair_dense_tile<DQ_TN>(tp, t, rank);
+            const int64_t row = tile.row0 + q * 32 + lane;
+            float aa = 1.0f;
+            if (p.alpha_a_scope == 1) aa = __ldg(p.alpha_a);
+            else if (p.alpha_a_scope == 2 && row < p.M) aa = __ldg(p.alpha_a + row);
+            const uint32_t ab = (uint32_t)(ti & 1);
+            const uint32_t use = (uint32_t)(ti >> 1);
+            if (!mbar_wait(bar_tfull + 8 * ab, use & 1u, abort_flag, &g_mx_device_status)) break;
+            tc_fence_after();
+            const int64_t wrow0 = tile.row0 + q * 32;
+            const uint32_t rbase_off = (uint32_t)(lane * 2 * EPI_COLS);
+#pragma unroll 1
+            for (int c = 0; c < DQ_TN / 2 / 32; ++c) {
+                float v[32];
+                tmem_ld32(tmem + ab * DQ_TN + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * (DQ_TN / 2) + c * 32), v);
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(__fmul_rn(v[2 * i], aa), __fmul_rn(v[2 * i + 1], aa));
+                if (wrow0 < p.M) {
+#pragma unroll
+                    for (int s2 = 0; s2 < 2; ++s2) {
+                        const int64_t col0 = tile.n0 + h * (DQ_TN / 2) + c * 32 + s2 * EPI_COLS;
+                        if (col0 < p.N) {
+                            const uint32_t buf = ebase + (epi_chunk & 1u) * (uint32_t)EPI_BUF_BYTES;
+                            ++epi_chunk;
+                            if (lane == 0) bulk_wait_group_read1();
+                            __syncwarp();
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const uint32_t phys = (uint32_t)j ^ ((uint32_t)(lane >> 2) & 1u);
+                                const int pk = s2 * 8 + 4 * j;
+                                st_shared_v4(buf + rbase_off + 16u * phys, packed[pk], packed[pk + 1], packed[pk + 2], packed[pk + 3]);
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&tmD, (int32_t)col0, (int32_t)wrow0, buf);
+                                bulk_commit_group();
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader + 8 * ab);
+        }
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
+    } else {
+        // ------------------------------- converters (both CTAs) -------------------------------
+        const int r = threadIdx.x - 32 * DQ_CONV_WARP0;            // B row of this CTA's half
+        const uint32_t full_leader = map_to_cta(bar_full, 0);
+        const uint32_t row_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+        const uint32_t sf_off = (uint32_t)((r & 31) * 16 + ((r >> 5) & 3) * 4);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
+            const PairTile tile = pair_dense_tile<DQ_TN>(tp, t, rank);
+            const int64_t brow = tile.n0 + 128 * (int64_t)rank + r;
+            float S = 0.0f;
+            if (p.sb2_scope == 1) S = __ldg(p.sb2);
+            else if (brow < p.N) S = __ldg(p.sb2 + brow);
+            for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                if (!warp_wait(bar_qfull + 8 * stage, phase, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                const uint8_t* qrow = smem + C::SMEM_Q + stage * C::Q_BYTES + r * 32;
+                const uint4 c0 = *reinterpret_cast<const uint4*>(qrow);
+                const uint4 c1 = *reinterpret_cast<const uint4*>(qrow + 16);
+                const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + C::SMEM_SF + stage * C::SF_BYTES + sf_off);
+                const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES + row_off;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    // chunk i = values 8i..8i+7 of the stage, block i / 2 of the row's four
+                    const uint32_t bs_h2 = e4m3_to_f16x2_bcast((sc >> (8 * (i >> 1))) & 0xFFu);
+                    const uint4 o = dq_word(w[i], bs_h2, S);
+                    st_shared_v4(sB + 16u * ((uint32_t)i ^ (uint32_t)(r & 7)), o.x, o.y, o.z, o.w);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(full_leader + 8 * stage);
+                if (++stage == NST) { stage = 0; phase ^= 1; }
+            }
+        }
+        if (!ok && lane == 0) *abort_flag = 1;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        const unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {}
+    }
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------------
 bool make_map(CUtensorMap* map, const uint8_t* base, int64_t k_bytes, int64_t rows, uint32_t box_rows) {
@@ -665,6 +994,51 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
     return cudaGetLastError();
 }
 
+cudaError_t launch_dq_impl(const DqGemmArgs& a, int num_sms, cudaStream_t stream) {
+    using C = DqCfg;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    static int resident_pairs = 0;
+    std::call_once(attr_once, [num_sms] {
+        attr_err = cudaFuncSetAttribute(dq_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        if (attr_err != cudaSuccess) return;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(num_sms & ~1));
+        cfg.blockDim = dim3(DQ_THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2; attr[0].val.clusterDim.y = 1; attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr; cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, dq_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = num_sms / 2;
+        }
+        resident_pairs = n;
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    CUtensorMap tmA, tmQ, tmSB, tmD;
+    if (!make_map(&tmA, reinterpret_cast<const uint8_t*>(a.a), a.K * 2, a.M, 128)) return cudaErrorInvalidValue;
+    if (!encode_tensor_map_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qb, (uint64_t)(a.K / 2), (uint64_t)a.N,
+                              (uint64_t)(a.K / 2), 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return cudaErrorInvalidValue;
+    if (!make_sf_map(&tmSB, a.sb, host_scale_bytes(a.N, a.K, 16), 1)) return cudaErrorInvalidValue;
+    if (!make_out_map(&tmD, a.d, a.M, a.N, a.ldd, (uint32_t)EPI_COLS)) return cudaErrorInvalidValue;
+    DqParams p{};
+    p.alpha_a = a.alpha_a; p.alpha_a_scope = a.alpha_a_scope;
+    p.sb2 = a.sb2; p.sb2_scope = a.sb2_scope;
+    p.M = a.M; p.N = a.N; p.K = a.K; p.d = a.d; p.ldd = a.ldd;
+    p.m_tiles = (a.M + 2 * BM - 1) / (2 * BM);
+    p.n_tiles = (a.N + DQ_TN - 1) / DQ_TN;
+    p.k_stages = a.K / 64;
+    p.nct = (a.K / 16 + 3) / 4;
+    p.total_tiles = p.m_tiles * p.n_tiles;
+    const int64_t pairs = max64(1, min64(p.total_tiles, (int64_t)min(resident_pairs, num_sms / 2)));
+    dq_gemm_pair_kernel<<<(unsigned)(2 * pairs), DQ_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmQ, tmSB, tmD, p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 
@@ -709,6 +1083,10 @@ cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t s
     if (args.G > 0) return launch_pair_impl<1, true, false, 256>(args, num_sms, stream);
     return col_alpha ? launch_pair_impl<1, false, true, 256>(args, num_sms, stream)
                      : launch_pair_impl<1, false, false, 256>(args, num_sms, stream);
+}
+
+cudaError_t launch_dq_gemm(const DqGemmArgs& args, int num_sms, cudaStream_t stream) {
+    return launch_dq_impl(args, num_sms, stream);
 }
 
 uint32_t read_and_clear_device_status() {

@@ -56,6 +56,16 @@ struct GemmArgs {
     int64_t G; const int64_t* group_offsets;
 };
 cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream);
+
+// BF16 x dequantized-NVFP4 GEMM: A BF16 [M, K]; B NVFP4 codes [N, K/2], E4M3 scales in the GEMM layout and an
+// FP32 second-level scale (sb2_scope 1: one value, 2: per B row); alpha_a as in GemmArgs.
+struct DqGemmArgs {
+    const uint16_t* a; const float* alpha_a; int alpha_a_scope;
+    const uint8_t* qb; const uint8_t* sb; const float* sb2; int sb2_scope;
+    int64_t M, N, K;
+    uint16_t* d; int64_t ldd;
+};
+cudaError_t launch_dq_gemm(const DqGemmArgs& args, int num_sms, cudaStream_t stream);
 uint32_t read_and_clear_device_status();
 uint32_t read_and_clear_mxfp8_status();
 

@@ -273,6 +273,24 @@ mx_status mx_scaled_gemm(mx_format fmt, const uint8_t* a, const uint8_t* sa, con
     return from_cuda(mxk::launch_scaled_gemm(g, mxk::device_sm_count(), stream));
 }
 
+mx_status mx_gemm_bf16_dq_nvfp4(const void* a, const float* alpha_a, mx_scope alpha_a_scope, const uint8_t* qb,
+                                const uint8_t* sb, const float* sb2, mx_scope sb2_scope, int64_t M, int64_t N,
+                                int64_t K, void* d, int64_t ldd, cudaStream_t stream) {
+    if (!a || !qb || !sb || !sb2 || !d || M <= 0 || N <= 0 || K <= 0 || ldd < N) return MX_ERR_INVALID_ARG;
+    if (alpha_a_scope < MX_SCOPE_NONE || alpha_a_scope > MX_SCOPE_ROW || (alpha_a_scope != MX_SCOPE_NONE && !alpha_a))
+        return MX_ERR_INVALID_ARG;
+    if (sb2_scope != MX_SCOPE_TENSOR && sb2_scope != MX_SCOPE_ROW) return MX_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(qb) || !aligned16(sb) || !aligned16(d) || (N % 8) != 0 || (ldd % 8) != 0)
+        return MX_ERR_ALIGNMENT;
+    if ((K % 64) != 0 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
+    mxk::DqGemmArgs g{};
+    g.a = static_cast<const uint16_t*>(a);
+    g.alpha_a = alpha_a; g.alpha_a_scope = alpha_a ? (int)alpha_a_scope : 0;
+    g.qb = qb; g.sb = sb; g.sb2 = sb2; g.sb2_scope = sb2_scope == MX_SCOPE_TENSOR ? 1 : 2;
+    g.M = M; g.N = N; g.K = K; g.d = static_cast<uint16_t*>(d); g.ldd = ldd;
+    return from_cuda(mxk::launch_dq_gemm(g, mxk::device_sm_count(), stream));
+}
+
 mx_status mx_grouped_scaled_gemm(mx_format fmt, int64_t G, const int64_t* group_offsets, int64_t total_rows,
                                  const uint8_t* a, const uint8_t* sa, const float* alpha_a_rows, const uint8_t* b,
                                  const uint8_t* sb, const float* alpha_b_groups, int64_t N, int64_t K, void* d,

@@ -494,6 +494,19 @@ def gemm_ref_nvfp4(qa, sa, alpha_a, qb, sb, alpha_b) -> np.ndarray:
     return ref * aa * ab
 
 
+def gemm_ref_bf16_dq_nvfp4(a: np.ndarray, qb, sb, sb2, per_row: bool, alpha_a=None) -> np.ndarray:
+    """The dequantized-backward GEMM (4-bitter page, "dequantized backward": BF16 operands rebuilt from the
+    forward's NVFP4 values): ref = alpha_a * A @ DQ(B)^T with A BF16 [M, K] and DQ(B) the BF16 values of
+    dequant_nvfp4 (sb the compact [N, K/16] scales); numpy's float64 matmul is the library step."""
+    A = bf16_to_f32(_bf16(a)).astype(np.float64)
+    B = bf16_to_f32(dequant_nvfp4(qb, sb, sb2, per_row)).astype(np.float64)
+    ref = A @ B.T
+    if alpha_a is not None:
+        aa = np.asarray(alpha_a, dtype=np.float64)
+        ref = ref * (aa.reshape(-1, 1) if aa.ndim else aa)
+    return ref
+
+
 def rel_fro_error(d: np.ndarray, ref: np.ndarray) -> float:
     """||D - ref||_F / ||ref||_F."""
     d = np.asarray(d, dtype=np.float64)

@@ -86,3 +86,33 @@ def test_rel_fro_error(orc):
     ref = np.ones((4, 4))
     assert orc.rel_fro_error(ref * 1.01, ref) == np.float64(0.01).item() or \
         abs(orc.rel_fro_error(ref * 1.01, ref) - 0.01) < 1e-12
+
+
+def test_dq_backward_ref_matches_block_scaled_ref_when_dequantization_is_exact(orc):
+    """The dequantized-backward reference (BF16 A times the BF16 DQ(B)) equals the block-scaled NVFP4
+    reference on the same codes when every dequantized value is exact in BF16 (power-of-two second-level
+    scales), and a triple loop over hand-decoded values; a transposed or mis-scaled operand fails."""
+    rng = np.random.default_rng(21)
+    M, N, K = 6, 5, 64
+    qa = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    qb = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa = rng.integers(0x28, 0x48, size=(M, K // 16), dtype=np.uint8)      # E4M3 scales 2^-2 .. 2^1.9
+    sb = rng.integers(0x28, 0x48, size=(N, K // 16), dtype=np.uint8)
+    Sa, Sb = np.float32(0.125), np.float32(4.0)
+    a_bf16 = orc.dequant_nvfp4(qa, sa, Sa, False)                          # exact: <= 6 significant bits
+    ref = orc.gemm_ref_bf16_dq_nvfp4(a_bf16, qb, sb, Sb, False)
+    assert np.array_equal(ref, orc.gemm_ref_nvfp4(qa, sa, Sa, qb, sb, Sb))
+    e2m1 = [0, .5, 1, 1.5, 2, 3, 4, 6]
+
+    def val(q, s, S, r, k):
+        c = (int(q[r, k // 2]) >> (4 * (k & 1))) & 0xF
+        return (-1 if c & 8 else 1) * e2m1[c & 7] * orc.e4m3_value(int(s[r, k // 16])) * float(S)
+
+    loop = np.array([[sum(val(qa, sa, Sa, m, k) * val(qb, sb, Sb, n, k) for k in range(K)) for n in range(N)]
+                     for m in range(M)])
+    assert np.array_equal(ref, loop)
+    # per-row second-level scales of B and a per-row alpha of A
+    Sb_rows = np.float32(2.0) ** rng.integers(-3, 3, size=N).astype(np.float32)
+    aa = np.float32(2.0) ** rng.integers(-2, 2, size=M).astype(np.float32)
+    ref2 = orc.gemm_ref_bf16_dq_nvfp4(a_bf16, qb, sb, Sb_rows, True, alpha_a=aa)
+    assert np.array_equal(ref2, orc.gemm_ref_nvfp4(qa, sa, Sa * aa, qb, sb, Sb_rows))
