@@ -600,11 +600,15 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 //                 E2M1 pairs to FP16, exact product with the FP16 block scale, times S in FP32,
 //                 round to BF16) into the 128-byte-swizzled K-major tile the MMA descriptor expects,
 //                 fences the generic-proxy writes for the tensor core and arrives (one lane per warp)
-//                 on the even CTA's stage barrier
+//                 on a barrier of its own CTA: the even CTA's stage barrier directly; in the odd CTA a
+//                 local barrier that warp 1 (idle there) forwards to the even CTA's stage barrier as the
+//                 completion of a 16-byte bulk copy
 // ---------------------------------------------------------------------------------------------
-constexpr int DQ_THREADS = 448;
-constexpr int DQ_TN = 256;
+constexpr int DQ_CONV_WARPS = 8;                           // converter warps per CTA (2 per scheduler)
 constexpr int DQ_CONV_WARP0 = 10;
+constexpr int DQ_THREADS = 32 * (DQ_CONV_WARP0 + DQ_CONV_WARPS);
+constexpr int DQ_TN = 256;
+constexpr int DQ_CONV_CHUNKS = 8 * 4 / DQ_CONV_WARPS;          // 16-byte BF16 chunks per converter thread
 
 struct DqCfg {
     static constexpr int NST = 5;
@@ -614,15 +618,17 @@ struct DqCfg {
     static constexpr int SF_BYTES = 512;                   // their scale atom (4 scales per row)
     static constexpr uint32_t A_TX = 2u * A_BYTES;         // both CTAs' A rows, on the even CTA's barrier
     static constexpr uint32_t Q_TX = Q_BYTES + SF_BYTES;   // per CTA, on its own barrier
-    static constexpr int FULL_ARRIVALS = 1 + 2 * 4;        // producer + four converter warps per CTA
+    static constexpr int FULL_ARRIVALS = 1 + DQ_CONV_WARPS;      // producer and the even CTA's converter warps
+    static constexpr uint32_t SIGNAL_TX = 16;                    // the odd CTA's per-stage signal copy
     static constexpr int SMEM_A = 0;
     static constexpr int SMEM_B = SMEM_A + NST * A_BYTES;
     static constexpr int SMEM_Q = SMEM_B + NST * B_BYTES;
     static constexpr int SMEM_SF = SMEM_Q + NST * Q_BYTES;
     static constexpr int SMEM_EPI = (SMEM_SF + NST * SF_BYTES + 1023) / 1024 * 1024;
     static constexpr int SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
-    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (3 * NST + 5);
-    static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024;
+    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (4 * NST + 5);
+    static constexpr int SMEM_SIGNAL = (SMEM_MISC + 16 + 15) / 16 * 16;   // 16-byte target / source
+    static constexpr int SMEM_ALLOC = SMEM_SIGNAL + 16 + 1024;
     static_assert(SMEM_B % 1024 == 0 && SMEM_Q % 1024 == 0 && SMEM_EPI % 1024 == 0, "alignment");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
@@ -645,6 +651,13 @@ __device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t byte) {
     uint32_t r;
     asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(r) : "r"(byte * 0x0101u));
     return r;
+}
+
+// Bulk copy from this CTA's shared memory into another CTA's of the cluster, completing `bytes` on
+// the destination CTA's mbarrier.
+__device__ __forceinline__ void bulk_signal_copy(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster) : "memory");
 }
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
@@ -691,6 +704,7 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t bar_tfull = bar_empty + 8 * NST;           // 2
     const uint32_t bar_tempty = bar_tfull + 16;               // 2 (even CTA)
     const uint32_t bar_done = bar_tempty + 16;
+    const uint32_t bar_bconv = bar_done + 8;                  // NST (odd CTA): its converter warps are done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
 
@@ -703,6 +717,7 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             mbar_init(bar_full + 8 * s, C::FULL_ARRIVALS);
             mbar_init(bar_qfull + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_bconv + 8 * s, DQ_CONV_WARPS);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_tfull + 8 * b, 1);
@@ -745,7 +760,7 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
                 if (elect_one()) {
                     const uint32_t fb = map_to_cta(bar_full + 8 * stage, 0);
-                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_TX);
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_TX + C::SIGNAL_TX);
                     tma_load_2d_pair(sbase + C::SMEM_A + stage * C::A_BYTES, &tmA, (int32_t)(ks * BKB), (int32_t)tile.row0, fb);
                     const uint32_t qb = bar_qfull + 8 * stage;
                     mbar_arrive_expect_tx(qb, C::Q_TX);
@@ -798,6 +813,26 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 __syncwarp();
             }
+        } else {
+            // odd CTA: once all of this CTA's converter warps have finished a stage (they arrive on a
+            // local barrier), a 16-byte bulk copy into the even CTA completes SIGNAL_TX bytes on its
+            // stage barrier.  The copy is an asynchronous-proxy operation ordered after the converters'
+            // fenced writes, and issuing it does not block (a cluster-scope release arrival stalled the
+            // issuing thread ~1-2k cycles per stage and starved the tensor core).
+            const uint32_t full_leader = map_to_cta(bar_full, 0);
+            const uint32_t sig_dst = map_to_cta(sbase + C::SMEM_SIGNAL, 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
+                for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                    if (!warp_wait(bar_bconv + 8 * stage, phase, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                    if (lane == 0) bulk_signal_copy(sig_dst, sbase + C::SMEM_SIGNAL, C::SIGNAL_TX, full_leader + 8 * stage);
+                    __syncwarp();
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok && lane == 0) *abort_flag = 1;
         }
     } else if (warp < DQ_CONV_WARP0) {
         // ------------------------------- epilogue (both CTAs) -------------------------------
@@ -859,8 +894,9 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         __syncwarp();
     } else {
         // ------------------------------- converters (both CTAs) -------------------------------
-        const int r = threadIdx.x - 32 * DQ_CONV_WARP0;            // B row of this CTA's half
-        const uint32_t full_leader = map_to_cta(bar_full, 0);
+        // thread ct: B row r of this CTA's half, chunks [part * DQ_CONV_CHUNKS, +DQ_CONV_CHUNKS) of its 8
+        const int ct = threadIdx.x - 32 * DQ_CONV_WARP0;
+        const int r = ct / (8 / DQ_CONV_CHUNKS), part = ct % (8 / DQ_CONV_CHUNKS);
         const uint32_t row_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
         const uint32_t sf_off = (uint32_t)((r & 31) * 16 + ((r >> 5) & 3) * 4);
         int stage = 0;
@@ -875,22 +911,26 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int64_t ks = 0; ks < p.k_stages; ++ks) {
                 if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
                 if (!warp_wait(bar_qfull + 8 * stage, phase, abort_flag, &g_mx_device_status)) { ok = false; break; }
-                const uint8_t* qrow = smem + C::SMEM_Q + stage * C::Q_BYTES + r * 32;
-                const uint4 c0 = *reinterpret_cast<const uint4*>(qrow);
-                const uint4 c1 = *reinterpret_cast<const uint4*>(qrow + 16);
+                const uint8_t* qsrc = smem + C::SMEM_Q + stage * C::Q_BYTES + r * 32 + part * 4 * DQ_CONV_CHUNKS;
+                uint32_t w[DQ_CONV_CHUNKS];
+#pragma unroll
+                for (int i = 0; i < DQ_CONV_CHUNKS; i += 4) {
+                    const uint4 c4 = *reinterpret_cast<const uint4*>(qsrc + 4 * i);
+                    w[i] = c4.x; w[i + 1] = c4.y; w[i + 2] = c4.z; w[i + 3] = c4.w;
+                }
                 const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + C::SMEM_SF + stage * C::SF_BYTES + sf_off);
-                const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
                 const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES + row_off;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    // chunk i = values 8i..8i+7 of the stage, block i / 2 of the row's four
-                    const uint32_t bs_h2 = e4m3_to_f16x2_bcast((sc >> (8 * (i >> 1))) & 0xFFu);
+                for (int i = 0; i < DQ_CONV_CHUNKS; ++i) {
+                    // chunk ci = values 8 ci .. 8 ci + 7 of the stage, block ci / 2 of the row's four
+                    const int ci = part * DQ_CONV_CHUNKS + i;
+                    const uint32_t bs_h2 = e4m3_to_f16x2_bcast((sc >> (8 * (ci >> 1))) & 0xFFu);
                     const uint4 o = dq_word(w[i], bs_h2, S);
-                    st_shared_v4(sB + 16u * ((uint32_t)i ^ (uint32_t)(r & 7)), o.x, o.y, o.z, o.w);
+                    st_shared_v4(sB + 16u * ((uint32_t)ci ^ (uint32_t)(r & 7)), o.x, o.y, o.z, o.w);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(full_leader + 8 * stage);
+                if (lane == 0) mbar_arrive(leader ? bar_full + 8 * stage : bar_bconv + 8 * stage);
                 if (++stage == NST) { stage = 0; phase ^= 1; }
             }
         }
