@@ -606,13 +606,25 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // ---------------------------------------------------------------------------------------------
 constexpr int DQ_CONV_WARPS = 8;                           // converter warps per CTA (2 per scheduler)
 constexpr int DQ_CONV_WARP0 = 10;
-constexpr int DQ_THREADS = 32 * (DQ_CONV_WARP0 + DQ_CONV_WARPS);
+constexpr int DQ_QPROD_WARP = DQ_CONV_WARP0 + DQ_CONV_WARPS;   // the codes producer
+constexpr int DQ_THREADS = 32 * (DQ_QPROD_WARP + 1);
 constexpr int DQ_TN = 256;
 constexpr int DQ_CONV_CHUNKS = 8 * 4 / DQ_CONV_WARPS;          // 16-byte BF16 chunks per converter thread
+static_assert(DQ_CONV_CHUNKS == 2 || DQ_CONV_CHUNKS == 4 || DQ_CONV_CHUNKS == 8, "converter split");
+
+struct DqParams {
+    const float* alpha_a; int alpha_a_scope;
+    const float* sb2; int sb2_scope;        // B's FP32 second-level scale: 1 = one value, 2 = per B row
+    int64_t M, N, K;
+    uint16_t* d; int64_t ldd;
+    int64_t m_tiles, n_tiles, k_stages, nct, total_tiles;
+};
 
 struct DqCfg {
-    static constexpr int NST = 5;
-    static constexpr int A_BYTES = 128 * BKB;              // 128 rows x 64 BF16
+    static constexpr int NST = 4;                          // A / B (BF16) ring
+    static constexpr int NQ = 3;                           // codes ring
+    static constexpr int A_BLOCK = 128 * BKB;              // 128 rows x 64 BF16
+    static constexpr int A_BYTES = 2 * A_BLOCK;            // this CTA's rows of both 256-row halves of the tile
     static constexpr int B_BYTES = 128 * BKB;              // this CTA's 128 B rows x 64 BF16 (built here)
     static constexpr int Q_BYTES = 128 * 32;               // their codes, 64 E2M1 values per row
     static constexpr int SF_BYTES = 512;                   // their scale atom (4 scales per row)
@@ -623,15 +635,30 @@ struct DqCfg {
     static constexpr int SMEM_A = 0;
     static constexpr int SMEM_B = SMEM_A + NST * A_BYTES;
     static constexpr int SMEM_Q = SMEM_B + NST * B_BYTES;
-    static constexpr int SMEM_SF = SMEM_Q + NST * Q_BYTES;
-    static constexpr int SMEM_EPI = (SMEM_SF + NST * SF_BYTES + 1023) / 1024 * 1024;
+    static constexpr int SMEM_SF = SMEM_Q + NQ * Q_BYTES;
+    static constexpr int SMEM_EPI = (SMEM_SF + NQ * SF_BYTES + 1023) / 1024 * 1024;
     static constexpr int SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
-    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (4 * NST + 5);
+    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (3 * NST + 2 * NQ + 5);
     static constexpr int SMEM_SIGNAL = (SMEM_MISC + 16 + 15) / 16 * 16;   // 16-byte target / source
     static constexpr int SMEM_ALLOC = SMEM_SIGNAL + 16 + 1024;
     static_assert(SMEM_B % 1024 == 0 && SMEM_Q % 1024 == 0 && SMEM_EPI % 1024 == 0, "alignment");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
+
+// Output tiles of 512 rows x 256 columns: the pair runs two M = 256 MMAs per K step on the same
+// converted B tile (rows [m0, m0 + 256) and [m0 + 256, m0 + 512), CTA r holding rows 128 r + [0, 128)
+// of each half), so each expanded B value feeds twice the tensor work.  Bands of 8 row tiles; inside
+// a band N-tiles advance every 8 tiles.
+__device__ __forceinline__ PairTile dq_tile(const DqParams& p, int64_t t, uint32_t rank) {
+    constexpr int64_t GM = 8;
+    const int64_t band_tiles = GM * p.n_tiles;
+    const int64_t band = t / band_tiles, in = t % band_tiles;
+    const int64_t band_m = min64(GM, p.m_tiles - band * GM);
+    const int64_t mp = band * GM + in % band_m, nt = in / band_m;
+    PairTile r;
+    r.row0 = mp * 512 + 128 * (int64_t)rank; r.row_end = p.M; r.n0 = nt * DQ_TN; r.g = 0; r.band_a = 0;
+    return r;
+}
 
 // kind::f16 instruction descriptor: D FP32 (bits 4-5 = 1), A and B BF16 (7-9, 10-12 = 1), K-major
 // A and B, N >> 3 (17-22), M >> 4 (24-28).
@@ -681,13 +708,7 @@ __device__ __forceinline__ uint4 dq_word(uint32_t w, uint32_t bs_h2, float S) {
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-struct DqParams {
-    const float* alpha_a; int alpha_a_scope;
-    const float* sb2; int sb2_scope;        // B's FP32 second-level scale: 1 = one value, 2 = per B row
-    int64_t M, N, K;
-    uint16_t* d; int64_t ldd;
-    int64_t m_tiles, n_tiles, k_stages, nct, total_tiles;
-};
+
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DQ_THREADS, 1)
 dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmQ,
@@ -698,13 +719,14 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase + C::SMEM_BAR;            // NST (even CTA): A bytes + converter arrivals
-    const uint32_t bar_qfull = bar_full + 8 * NST;            // NST (each CTA): codes + scale atom
-    const uint32_t bar_empty = bar_qfull + 8 * NST;           // NST (each CTA): the stage's MMAs are done
-    const uint32_t bar_tfull = bar_empty + 8 * NST;           // 2
+    const uint32_t bar_full = sbase + C::SMEM_BAR;            // NST (even CTA): A bytes + converters + signal
+    const uint32_t bar_empty = bar_full + 8 * NST;            // NST (each CTA): the stage's MMAs are done
+    const uint32_t bar_bconv = bar_empty + 8 * NST;           // NST (odd CTA): its converter warps are done
+    const uint32_t bar_qfull = bar_bconv + 8 * NST;           // NQ (each CTA): codes + scale atom landed
+    const uint32_t bar_qempty = bar_qfull + 8 * C::NQ;        // NQ (each CTA): the converters have read them
+    const uint32_t bar_tfull = bar_qempty + 8 * C::NQ;        // 2
     const uint32_t bar_tempty = bar_tfull + 16;               // 2 (even CTA)
     const uint32_t bar_done = bar_tempty + 16;
-    const uint32_t bar_bconv = bar_done + 8;                  // NST (odd CTA): its converter warps are done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
 
@@ -715,9 +737,12 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(bar_full + 8 * s, C::FULL_ARRIVALS);
-            mbar_init(bar_qfull + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
             mbar_init(bar_bconv + 8 * s, DQ_CONV_WARPS);
+        }
+        for (int s = 0; s < C::NQ; ++s) {
+            mbar_init(bar_qfull + 8 * s, 1);
+            mbar_init(bar_qempty + 8 * s, DQ_CONV_WARPS);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_tfull + 8 * b, 1);
@@ -744,8 +769,6 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t tmem = *tmem_slot;
     const int64_t total_tiles = p.total_tiles;
     const int64_t pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
-    Params tp{};                                               // the tile schedule's view
-    tp.M = p.M; tp.N = p.N; tp.m_tiles = p.m_tiles; tp.n_tiles = p.n_tiles;
 
     if (warp == 0) {
         // ------------------------------- producer (both CTAs) -------------------------------
@@ -753,19 +776,15 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint32_t phase = 0;
         bool ok = true;
         for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
-            const PairTile tile = pair_dense_tile<DQ_TN>(tp, t, rank);
-            const int64_t brow = tile.n0 + 128 * (int64_t)rank;
-            const int64_t band = brow / 128;
+            const PairTile tile = dq_tile(p, t, rank);
             for (int64_t ks = 0; ks < p.k_stages; ++ks) {
                 if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
                 if (elect_one()) {
                     const uint32_t fb = map_to_cta(bar_full + 8 * stage, 0);
                     if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_TX + C::SIGNAL_TX);
-                    tma_load_2d_pair(sbase + C::SMEM_A + stage * C::A_BYTES, &tmA, (int32_t)(ks * BKB), (int32_t)tile.row0, fb);
-                    const uint32_t qb = bar_qfull + 8 * stage;
-                    mbar_arrive_expect_tx(qb, C::Q_TX);
-                    tma_load_2d(sbase + C::SMEM_Q + stage * C::Q_BYTES, &tmQ, (int32_t)(ks * 32), (int32_t)brow, qb);
-                    tma_load_2d(sbase + C::SMEM_SF + stage * C::SF_BYTES, &tmSB, 0, (int32_t)((band * p.nct + ks) * 2), qb);
+                    const uint32_t sA = sbase + C::SMEM_A + stage * C::A_BYTES;
+                    tma_load_2d_pair(sA, &tmA, (int32_t)(ks * BKB), (int32_t)tile.row0, fb);
+                    tma_load_2d_pair(sA + C::A_BLOCK, &tmA, (int32_t)(ks * BKB), (int32_t)(tile.row0 + 256), fb);
                 }
                 __syncwarp();
                 if (++stage == NST) { stage = 0; phase ^= 1; }
@@ -780,11 +799,9 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             bool ok = true, issued_any = false;
             int64_t ti = 0;
             for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs, ++ti) {
-                const uint32_t ab = (uint32_t)(ti & 1);
-                const uint32_t use = (uint32_t)(ti >> 1);
-                if (!warp_wait(bar_tempty + 8 * ab, (use & 1u) ^ 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                // both accumulators (rows m0 + [0, 256) and m0 + [256, 512)) fill all 512 TMEM columns
+                if (!warp_wait(bar_tempty, ((uint32_t)ti & 1u) ^ 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t tacc = tmem + ab * DQ_TN;
                 for (int64_t ks = 0; ks < p.k_stages; ++ks) {
                     if (!warp_wait(bar_full + 8 * stage, phase, abort_flag, &g_mx_device_status)) { ok = false; break; }
                     tc_fence_after();
@@ -792,9 +809,13 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const uint32_t sA = sbase + C::SMEM_A + stage * C::A_BYTES;
                         const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES;
 #pragma unroll
-                        for (int j = 0; j < BKB / 32; ++j)
-                            tc2_mma_bf16(tacc, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j),
-                                         make_idesc_bf16<2 * BM, DQ_TN>(), (ks > 0 || j > 0) ? 1u : 0u);
+                        for (int j = 0; j < BKB / 32; ++j) {
+                            const uint64_t bd = desc_sw128(sB + 32 * j);
+                            const uint32_t acc = (ks > 0 || j > 0) ? 1u : 0u;
+                            tc2_mma_bf16(tmem, desc_sw128(sA + 32 * j), bd, make_idesc_bf16<2 * BM, DQ_TN>(), acc);
+                            tc2_mma_bf16(tmem + DQ_TN, desc_sw128(sA + C::A_BLOCK + 32 * j), bd,
+                                         make_idesc_bf16<2 * BM, DQ_TN>(), acc);
+                        }
                         tc2_commit_mc(bar_empty + 8 * stage, (uint16_t)3);
                     }
                     __syncwarp();
@@ -802,7 +823,7 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (++stage == NST) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                if (elect_one()) tc2_commit_mc(bar_tfull + 8 * ab, (uint16_t)3);
+                if (elect_one()) tc2_commit_mc(bar_tfull, (uint16_t)3);
                 __syncwarp();
             }
             if (issued_any) {
@@ -843,44 +864,46 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint32_t epi_chunk = 0;
         int64_t ti = 0;
         for (int64_t t = pair_id; t < total_tiles; t += n_pairs, ++ti) {
-            const PairTile tile = pair_dense_tile<DQ_TN>(tp, t, rank);
-            const int64_t row = tile.row0 + q * 32 + lane;
-            float aa = 1.0f;
-            if (p.alpha_a_scope == 1) aa = __ldg(p.alpha_a);
-            else if (p.alpha_a_scope == 2 && row < p.M) aa = __ldg(p.alpha_a + row);
-            const uint32_t ab = (uint32_t)(ti & 1);
-            const uint32_t use = (uint32_t)(ti >> 1);
-            if (!mbar_wait(bar_tfull + 8 * ab, use & 1u, abort_flag, &g_mx_device_status)) break;
+            const PairTile tile = dq_tile(p, t, rank);
+            if (!mbar_wait_backoff(bar_tfull, (uint32_t)ti & 1u, abort_flag, &g_mx_device_status)) break;
             tc_fence_after();
-            const int64_t wrow0 = tile.row0 + q * 32;
-            const uint32_t rbase_off = (uint32_t)(lane * 2 * EPI_COLS);
 #pragma unroll 1
-            for (int c = 0; c < DQ_TN / 2 / 32; ++c) {
-                float v[32];
-                tmem_ld32(tmem + ab * DQ_TN + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * (DQ_TN / 2) + c * 32), v);
-                uint32_t packed[16];
+            for (int half = 0; half < 2; ++half) {
+                const int64_t wrow0 = tile.row0 + 256 * half + q * 32;
+                const int64_t row = wrow0 + lane;
+                float aa = 1.0f;
+                if (p.alpha_a_scope == 1) aa = __ldg(p.alpha_a);
+                else if (p.alpha_a_scope == 2 && row < p.M) aa = __ldg(p.alpha_a + row);
+                const uint32_t rbase_off = (uint32_t)(lane * 2 * EPI_COLS);
+#pragma unroll 1
+                for (int c = 0; c < DQ_TN / 2 / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(tmem + half * DQ_TN + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * (DQ_TN / 2) + c * 32), v);
+                    uint32_t packed[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(__fmul_rn(v[2 * i], aa), __fmul_rn(v[2 * i + 1], aa));
-                if (wrow0 < p.M) {
+                    for (int i2 = 0; i2 < 16; ++i2)
+                        packed[i2] = pack_bf16x2(__fmul_rn(v[2 * i2], aa), __fmul_rn(v[2 * i2 + 1], aa));
+                    if (wrow0 < p.M) {
 #pragma unroll
-                    for (int s2 = 0; s2 < 2; ++s2) {
-                        const int64_t col0 = tile.n0 + h * (DQ_TN / 2) + c * 32 + s2 * EPI_COLS;
-                        if (col0 < p.N) {
-                            const uint32_t buf = ebase + (epi_chunk & 1u) * (uint32_t)EPI_BUF_BYTES;
-                            ++epi_chunk;
-                            if (lane == 0) bulk_wait_group_read1();
-                            __syncwarp();
+                        for (int s2 = 0; s2 < 2; ++s2) {
+                            const int64_t col0 = tile.n0 + h * (DQ_TN / 2) + c * 32 + s2 * EPI_COLS;
+                            if (col0 < p.N) {
+                                const uint32_t buf = ebase + (epi_chunk & 1u) * (uint32_t)EPI_BUF_BYTES;
+                                ++epi_chunk;
+                                if (lane == 0) bulk_wait_group_read1();
+                                __syncwarp();
 #pragma unroll
-                            for (int j = 0; j < 2; ++j) {
-                                const uint32_t phys = (uint32_t)j ^ ((uint32_t)(lane >> 2) & 1u);
-                                const int pk = s2 * 8 + 4 * j;
-                                st_shared_v4(buf + rbase_off + 16u * phys, packed[pk], packed[pk + 1], packed[pk + 2], packed[pk + 3]);
-                            }
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) {
-                                tma_store_2d(&tmD, (int32_t)col0, (int32_t)wrow0, buf);
-                                bulk_commit_group();
+                                for (int j = 0; j < 2; ++j) {
+                                    const uint32_t phys = (uint32_t)j ^ ((uint32_t)(lane >> 2) & 1u);
+                                    const int pk = s2 * 8 + 4 * j;
+                                    st_shared_v4(buf + rbase_off + 16u * phys, packed[pk], packed[pk + 1], packed[pk + 2], packed[pk + 3]);
+                                }
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_store_2d(&tmD, (int32_t)col0, (int32_t)wrow0, buf);
+                                    bulk_commit_group();
+                                }
                             }
                         }
                     }
@@ -888,37 +911,45 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tempty_leader + 8 * ab);
+            if (lane == 0) mbar_arrive_cluster(tempty_leader);
         }
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
-    } else {
+    } else if (warp < DQ_QPROD_WARP) {
         // ------------------------------- converters (both CTAs) -------------------------------
         // thread ct: B row r of this CTA's half, chunks [part * DQ_CONV_CHUNKS, +DQ_CONV_CHUNKS) of its 8
         const int ct = threadIdx.x - 32 * DQ_CONV_WARP0;
         const int r = ct / (8 / DQ_CONV_CHUNKS), part = ct % (8 / DQ_CONV_CHUNKS);
         const uint32_t row_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
         const uint32_t sf_off = (uint32_t)((r & 31) * 16 + ((r >> 5) & 3) * 4);
-        int stage = 0;
-        uint32_t phase = 0;
+        int stage = 0, qstage = 0;
+        uint32_t phase = 0, qphase = 0;
         bool ok = true;
         for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
-            const PairTile tile = pair_dense_tile<DQ_TN>(tp, t, rank);
+            const PairTile tile = dq_tile(p, t, rank);
             const int64_t brow = tile.n0 + 128 * (int64_t)rank + r;
             float S = 0.0f;
             if (p.sb2_scope == 1) S = __ldg(p.sb2);
             else if (brow < p.N) S = __ldg(p.sb2 + brow);
             for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                if (!warp_wait(bar_qfull + 8 * qstage, qphase, abort_flag, &g_mx_device_status)) { ok = false; break; }
                 if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
-                if (!warp_wait(bar_qfull + 8 * stage, phase, abort_flag, &g_mx_device_status)) { ok = false; break; }
-                const uint8_t* qsrc = smem + C::SMEM_Q + stage * C::Q_BYTES + r * 32 + part * 4 * DQ_CONV_CHUNKS;
+                const uint8_t* qsrc = smem + C::SMEM_Q + qstage * C::Q_BYTES + r * 32 + part * 4 * DQ_CONV_CHUNKS;
                 uint32_t w[DQ_CONV_CHUNKS];
+                if constexpr (DQ_CONV_CHUNKS >= 4) {
 #pragma unroll
-                for (int i = 0; i < DQ_CONV_CHUNKS; i += 4) {
-                    const uint4 c4 = *reinterpret_cast<const uint4*>(qsrc + 4 * i);
-                    w[i] = c4.x; w[i + 1] = c4.y; w[i + 2] = c4.z; w[i + 3] = c4.w;
+                    for (int i = 0; i < DQ_CONV_CHUNKS; i += 4) {
+                        const uint4 c4 = *reinterpret_cast<const uint4*>(qsrc + 4 * i);
+                        w[i] = c4.x; w[i + 1] = c4.y; w[i + 2] = c4.z; w[i + 3] = c4.w;
+                    }
+                } else {
+                    const uint2 c2 = *reinterpret_cast<const uint2*>(qsrc);
+                    w[0] = c2.x; w[1] = c2.y;
                 }
-                const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + C::SMEM_SF + stage * C::SF_BYTES + sf_off);
+                const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + C::SMEM_SF + qstage * C::SF_BYTES + sf_off);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_qempty + 8 * qstage);            // codes slot read
+                if (++qstage == C::NQ) { qstage = 0; qphase ^= 1; }
                 const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES + row_off;
 #pragma unroll
                 for (int i = 0; i < DQ_CONV_CHUNKS; ++i) {
@@ -932,6 +963,29 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 __syncwarp();
                 if (lane == 0) mbar_arrive(leader ? bar_full + 8 * stage : bar_bconv + 8 * stage);
                 if (++stage == NST) { stage = 0; phase ^= 1; }
+            }
+        }
+        if (!ok && lane == 0) *abort_flag = 1;
+    } else {
+        // ------------------------------- codes producer (both CTAs) -------------------------------
+        // codes and scale atom of this CTA's 128 B rows, up to NQ stages ahead of the converters
+        int qstage = 0;
+        uint32_t qphase = 0;
+        bool ok = true;
+        for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
+            const PairTile tile = dq_tile(p, t, rank);
+            const int64_t brow = tile.n0 + 128 * (int64_t)rank;
+            const int64_t band = brow / 128;
+            for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                if (!warp_wait(bar_qempty + 8 * qstage, qphase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                if (elect_one()) {
+                    const uint32_t qb = bar_qfull + 8 * qstage;
+                    mbar_arrive_expect_tx(qb, C::Q_TX);
+                    tma_load_2d(sbase + C::SMEM_Q + qstage * C::Q_BYTES, &tmQ, (int32_t)(ks * 32), (int32_t)brow, qb);
+                    tma_load_2d(sbase + C::SMEM_SF + qstage * C::SF_BYTES, &tmSB, 0, (int32_t)((band * p.nct + ks) * 2), qb);
+                }
+                __syncwarp();
+                if (++qstage == C::NQ) { qstage = 0; qphase ^= 1; }
             }
         }
         if (!ok && lane == 0) *abort_flag = 1;
@@ -1069,7 +1123,7 @@ cudaError_t launch_dq_impl(const DqGemmArgs& a, int num_sms, cudaStream_t stream
     p.alpha_a = a.alpha_a; p.alpha_a_scope = a.alpha_a_scope;
     p.sb2 = a.sb2; p.sb2_scope = a.sb2_scope;
     p.M = a.M; p.N = a.N; p.K = a.K; p.d = a.d; p.ldd = a.ldd;
-    p.m_tiles = (a.M + 2 * BM - 1) / (2 * BM);
+    p.m_tiles = (a.M + 511) / 512;
     p.n_tiles = (a.N + DQ_TN - 1) / DQ_TN;
     p.k_stages = a.K / 64;
     p.nct = (a.K / 16 + 3) / 4;

@@ -53,6 +53,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// The same bounded wait for roles whose wait is long and not latency-critical (an epilogue waiting for
+// a whole tile): between polls the warp sleeps, leaving issue slots to the warps doing work.
+__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  unsigned int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        __nanosleep(256);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+            atomicOr(status, 1u);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
 // All lanes of the warp wait; the result is made warp-uniform (any lane's failure fails all).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned int* status) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status)) != 0;
