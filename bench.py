@@ -5,8 +5,9 @@ Default step (workload ``dense_mlp``, the Qwen3-8B-shaped MLP linear): MXFP8 row
 quantization of X [8192, 4096], W [12288, 4096] and dY [8192, 12288], then the three MXFP8
 block-scaled GEMMs FPROP (Y = X W^T), DGRAD (dX = dY W) and WGRAD (dW = dY^T X) with BF16 output.
 The metric is the step's GEMM throughput with its quantization included: 2.474 TFLOP per step /
-step time.  Other workloads (``--workload moe|moe_mxfp8|dense_fp8_blockwise|wgrad|weight_sync``) time the
-NVFP4 paths, the grouped MXFP8 MoE layer and blockwise FP8 (power-of-two scales on the MXFP8 GEMM).
+step time.  Other workloads (``--workload moe|moe_mxfp8|dense_fp8_blockwise|dense_nvfp4|wgrad|weight_sync``)
+time the NVFP4 paths, the grouped MXFP8 MoE layer, blockwise FP8 (power-of-two scales on the MXFP8 GEMM) and
+the NVFP4 pretraining linear layer with the dequantized-backward GEMM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxnum|reference] [--workload ...]
 
@@ -485,6 +486,90 @@ class DenseBlockwise:
                 "tokens": self.T, "hidden": self.H, "ffn": self.F}
 
 
+class DenseNVFP4:
+    """The NVFP4 pretraining linear layer (MaxText recipe) at Llama-3-8B MLP shapes: W in 16x16 2D blocks
+    (both orientations), X and dY 1x16 row-wise under per-tensor scales (RNE for X, SR for dY), FPROP and
+    DGRAD as NVFP4 GEMMs with the 2D weight, RHT16 + column-wise 1x16 of dY (SR) and X (RNE) and the NVFP4
+    WGRAD.  Aux: the dequantized-backward DGRAD (BF16 dY times DQ(W) expanded inside the GEMM, no BF16
+    weight copy) and, for comparison, the materialized DQ(W) it avoids."""
+    name = "dense_nvfp4"
+
+    def __init__(self, mx, torch, dev):
+        import synthetic
+        self.mx, self.torch, self.dev = mx, torch, dev
+        d = synthetic.dense_nvfp4()
+        bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.x, self.dy, self.w = bf(d["x"]), bf(d["dy"]), bf(d["w"])
+        self.rht_seed, self.sr_seed = d["rht_seed"], d["sr_seed"]
+        T, H = self.x.shape
+        F = self.dy.shape[1]
+        self.T, self.H, self.F = T, H, F
+        u8 = lambda *shape: torch.empty(shape, dtype=torch.uint8, device=dev)
+        z8 = lambda n: torch.zeros(n, dtype=torch.uint8, device=dev)
+        f32 = lambda n: torch.empty(n, dtype=torch.float32, device=dev)
+        self.qw = mx.alloc_nvfp4_weight_2d(1, F, H, dev)
+        self.qx, self.sx, self.Sx = u8(T, H // 2), z8(mx.scale_bytes(T, H, 16)), f32(1)
+        self.qdy, self.sdy, self.Sdy = u8(T, F // 2), z8(mx.scale_bytes(T, F, 16)), f32(1)
+        self.qdy_c, self.sdy_c, self.Sdy_c = u8(F, T // 2), z8(mx.scale_bytes(F, T, 16)), f32(1)
+        self.qx_c, self.sx_c, self.Sx_c = u8(H, T // 2), z8(mx.scale_bytes(H, T, 16)), f32(1)
+        self.ws = [z8(16) for _ in range(4)]
+        self.y = torch.empty((T, F), dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.dw = torch.empty((F, H), dtype=torch.bfloat16, device=dev)
+        self.dx_dq = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.wdq = torch.empty((H, F), dtype=torch.bfloat16, device=dev)
+        self.launches_per_step = 13
+
+    def ops(self):
+        mx, F4 = self.mx, self.mx.MX_FMT_NVFP4
+        T, H, F = self.T, self.H, self.F
+        TS = mx.MX_SCOPE_TENSOR
+        qw = self.qw
+        per_tensor_1x16 = 2 * 2 + 0.5 + 1 / 16           # amax pass + quantize pass reads, codes, scales
+        return [
+            ("quant", "nvfp4 2D W", 1, F * H * (2 + 1 + 2 / 16),
+             lambda: mx.mx_nvfp4_quantize_weight_2d(self.w[None], qw["q_row"], qw["s_row"], qw["q_col"], qw["s_col"],
+                                                    qw["s_w"], qw["ws"])),
+            ("quant", "nvfp4 1x16 X", 1, T * H * per_tensor_1x16,
+             lambda: mx.mx_nvfp4_quantize_1x16(self.x, False, False, 0, False, 0, self.qx, self.sx, self.Sx, self.ws[0])),
+            ("gemm4", "FPROP", 0, 2.0 * T * F * H,
+             lambda: mx.mx_scaled_gemm(F4, self.qx, self.sx, self.Sx, TS, qw["q_row"][0], qw["s_row"], qw["s_w"], TS,
+                                       T, F, H, self.y)),
+            ("quant", "nvfp4 1x16 SR dY", 1, T * F * per_tensor_1x16,
+             lambda: mx.mx_nvfp4_quantize_1x16(self.dy, False, False, 0, True, self.sr_seed, self.qdy, self.sdy, self.Sdy,
+                                               self.ws[1])),
+            ("gemm4", "DGRAD", 0, 2.0 * T * H * F,
+             lambda: mx.mx_scaled_gemm(F4, self.qdy, self.sdy, self.Sdy, TS, qw["q_col"][0], qw["s_col"], qw["s_w"], TS,
+                                       T, H, F, self.dx)),
+            ("quant", "rht16+nvfp4 colwise SR dY", 1, T * F * per_tensor_1x16,
+             lambda: mx.mx_nvfp4_quantize_1x16(self.dy, True, True, self.rht_seed, True, self.sr_seed, self.qdy_c,
+                                               self.sdy_c, self.Sdy_c, self.ws[2])),
+            ("quant", "rht16+nvfp4 colwise X", 1, T * H * per_tensor_1x16,
+             lambda: mx.mx_nvfp4_quantize_1x16(self.x, True, True, self.rht_seed, False, 0, self.qx_c, self.sx_c,
+                                               self.Sx_c, self.ws[3])),
+            ("gemm4", "WGRAD", 0, 2.0 * F * H * T,
+             lambda: mx.mx_scaled_gemm(F4, self.qdy_c, self.sdy_c, self.Sdy_c, TS, self.qx_c, self.sx_c, self.Sx_c, TS,
+                                       F, H, T, self.dw)),
+        ]
+
+    def aux_ops(self):
+        mx, T, H, F = self.mx, self.T, self.H, self.F
+        qw = self.qw
+        return [
+            ("gemm16", "DGRAD dequantized backward (BF16 dY x DQ(W) in the mainloop)", 0, 2.0 * T * H * F,
+             lambda: mx.mx_gemm_bf16_dq_nvfp4(self.dy, qw["q_col"][0], qw["s_col"], qw["s_w"], mx.MX_SCOPE_TENSOR,
+                                              T, H, F, self.dx_dq)),
+            ("quant", "DQ(W) materialized (the BF16 copy the fused GEMM avoids)", 1, F * H * (0.5 + 1 / 16 + 2),
+             lambda: mx.mx_dequantize_bf16(mx.MX_FMT_NVFP4, qw["q_col"][0], qw["s_col"], qw["s_w"], mx.MX_SCOPE_TENSOR,
+                                           H, F, self.wdq)),
+        ]
+
+    def config(self):
+        return {"workload": "dense_nvfp4: Llama-3-8B MLP linear in NVFP4 (MaxText recipe: 2D weights, 1x16 per-tensor "
+                            "X/dY, RHT16 + SR on WGRAD inputs) FPROP/DGRAD/WGRAD",
+                "tokens": self.T, "hidden": self.H, "ffn": self.F}
+
+
 class WeightSync:
     """Weight-sync sweep: 48 layers of 128 experts x {2048x768, 768x2048, 768x2048}; per matrix
     stack MXFP8 row+col quantize, dequantize, re-quantize and byte compare; NVFP4 2D quantize,
@@ -630,11 +715,11 @@ def op_report(ops, per_op, peaks):
             ach = units / (ms / 1e3) / 1e9
             rep[label] = {"ms": round(ms, 4), "GBps": round(ach, 1), "frac_hbm": round(ach / peaks["hbm_gbs"], 4)}
         else:
-            fp8 = kind == "gemm8"
-            peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if fp8 else FP4_OVER_BF16)
+            ratio, tag = {"gemm8": (FP8_OVER_BF16, "frac_fp8_peak"), "gemm16": (1.0, "frac_bf16_peak")}.get(
+                kind, (FP4_OVER_BF16, "frac_fp4_peak"))
+            peak = peaks["bf16_tflops"] * ratio
             ach = units / (ms / 1e3) / 1e12
-            rep[label] = {"ms": round(ms, 4), "TFLOPs": round(ach, 1),
-                          ("frac_fp8_peak" if fp8 else "frac_fp4_peak"): round(ach / peak, 4)}
+            rep[label] = {"ms": round(ms, 4), "TFLOPs": round(ach, 1), tag: round(ach / peak, 4)}
             if mem:
                 t_flop = units / (peak * 1e12) * 1e3
                 t_mem = mem / (peaks["hbm_gbs"] * 1e9) * 1e3
@@ -689,6 +774,8 @@ def run_workload(args):
         work = MoE8(mx, torch, dev, experts=args.experts)
     elif args.workload == "dense_fp8_blockwise":
         work = DenseBlockwise(mx, torch, dev)
+    elif args.workload == "dense_nvfp4":
+        work = DenseNVFP4(mx, torch, dev)
     else:
         work = WGrad(mx, torch, dev)
     ops = work.ops()
@@ -917,7 +1004,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mxnum", "reference"], default="mxnum")
-    ap.add_argument("--workload", choices=["dense_mlp", "moe", "moe_mxfp8", "dense_fp8_blockwise", "wgrad", "weight_sync"], default="dense_mlp")
+    ap.add_argument("--workload", choices=["dense_mlp", "moe", "moe_mxfp8", "dense_fp8_blockwise", "dense_nvfp4", "wgrad", "weight_sync"], default="dense_mlp")
     ap.add_argument("--layers", type=int, default=48, help="weight_sync: layers swept")
     ap.add_argument("--experts", type=int, default=128, help="moe / weight_sync: experts (fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")

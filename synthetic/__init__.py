@@ -132,6 +132,14 @@ def wgrad(tokens: int = 32768, hidden: int = 4096, ffn: int = 14336):
     return {"x": x, "dy": dy, "rht_seed": 8, "sr_seed": 9}
 
 
+def dense_nvfp4(tokens: int = 32768, hidden: int = 4096, ffn: int = 14336):
+    """The NVFP4 pretraining linear layer at the MaxText benchmark's Llama-3-8B MLP shapes: the WGRAD
+    inputs of ``wgrad`` plus the weight [ffn, hidden] N(0, 0.02) (seed 10)."""
+    d = wgrad(tokens, hidden, ffn)
+    d["w"] = normal(np.random.default_rng(10), (ffn, hidden), 0.02)
+    return d
+
+
 # ---------------------------------------------------------------------------
 # weight_sync
 # ---------------------------------------------------------------------------
