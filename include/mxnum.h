@@ -278,7 +278,7 @@ mx_status mx_scaled_gemm(mx_format fmt,
  *   d      [M, ldd] BF16
  * FP32 accumulation in the tensor core (kind::f16), summation order the hardware's.  Requires K % 64 == 0,
  * N % 8 == 0, ldd % 8 == 0, ldd >= N, M, N < 2^31; a, qb, sb, d 16-byte aligned.  Persistent clusters of
- * two CTAs on 256 x 256 tiles. */
+ * two CTAs on 512 x 256 output tiles (two M = 256 pair MMAs per K step share each expanded B tile). */
 mx_status mx_gemm_bf16_dq_nvfp4(const void* a, const float* alpha_a, mx_scope alpha_a_scope, const uint8_t* qb,
                                 const uint8_t* sb, const float* sb2, mx_scope sb2_scope, int64_t M, int64_t N,
                                 int64_t K, void* d, int64_t ldd, cudaStream_t stream);
