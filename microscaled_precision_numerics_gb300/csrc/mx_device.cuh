@@ -89,21 +89,19 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
 // Evaluated on the FP32 bit fields (same decisions as the quotient form).
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t bits16) {
-    // For a in [1, 6) the two grid points of each binade [2^e, 2^(e+1)) are 2^e and 1.5 * 2^e, so the
-    // lower grid point is picked by the top mantissa bit and f is exactly the remaining 22 mantissa
-    // bits over 2^22; f > bits16 * 2^-16 is then the integer compare below.  In [0.5, 1) the only grid
-    // point is 0.5 and f is the whole 23-bit mantissa over 2^23.  Below 0.5 the quotient 2a is formed.
-    // All four cases are evaluated and selected without branches.
+    // For a in [1, 6) the two grid points of each binade [2^e, 2^(e+1)) are 2^e and 1.5 * 2^e: the top
+    // mantissa bit picks the lower one and f is the remaining 22 mantissa bits over 2^22, so f > bits16 *
+    // 2^-16 exactly when adding 2^22 - 1 - (bits16 << 6) to the FP32 bits carries into that top bit; the
+    // code 2 + 2e + m is then read off the sum (a carry out of the binade lands on the next grid point,
+    // and anything from 6 up clamps to 7).  In [0.5, 1) the grid points are 0.5 and 1 and f is the whole
+    // 23-bit mantissa over 2^23: the same carry test one bit up.  Below 0.5 (grid 0 and 0.5) f = 2a, and
+    // 2a > bits16 * 2^-16 is compared as a * 2^17 > bits16 in FP32 (both sides exact).
     const uint32_t u = __float_as_uint(v) & 0x7FFFFFFFu;
-    const float a = __uint_as_float(u);
-    const int e = (int)(u >> 23) - 127;
-    const uint32_t m = u & 0x7FFFFFu;
-    const uint32_t c_small = __fmul_rn(a, 2.0f) > __fmul_rn((float)bits16, 1.0f / 65536.0f) ? 1u : 0u;
-    const uint32_t c_half = 1u + ((m > (bits16 << 7)) ? 1u : 0u);
-    const uint32_t c_norm = 2u + 2u * (uint32_t)max(e, 0) + (m >> 22) + (((m & 0x3FFFFFu) > (bits16 << 6)) ? 1u : 0u);
-    uint32_t code = e < 0 ? c_half : c_norm;
-    code = a < 0.5f ? c_small : code;
-    code = a >= 6.0f ? 7u : code;
+    const uint32_t c_norm = min(((u + (0x3FFFFFu - (bits16 << 6))) >> 22) - 252u, 7u);
+    const uint32_t c_half = ((u + (0x7FFFFFu - (bits16 << 7))) >> 23) - 125u;
+    const float fbits = __fsub_rn(__uint_as_float(0x4B000000u | bits16), 8388608.0f);   // bits16 as FP32, exactly
+    const uint32_t c_small = __fmul_rn(__uint_as_float(u), 131072.0f) > fbits ? 1u : 0u;
+    const uint32_t code = u >= 0x3F800000u ? c_norm : (u >= 0x3F000000u ? c_half : c_small);
     return code | ((__float_as_uint(v) >> 28) & 8u);
 }
 
@@ -116,8 +114,11 @@ __device__ __forceinline__ U4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c
                                             uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int rnd = 0; rnd < 10; ++rnd) {
-        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
-        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+        // one widening multiply gives both halves of each 64-bit product
+        const unsigned long long p0 = (unsigned long long)0xD2511F53u * c0;
+        const unsigned long long p1 = (unsigned long long)0xCD9E8D57u * c2;
+        const uint32_t lo0 = (uint32_t)p0, hi0 = (uint32_t)(p0 >> 32);
+        const uint32_t lo1 = (uint32_t)p1, hi1 = (uint32_t)(p1 >> 32);
         const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
         c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
         k0 += 0x9E3779B9u; k1 += 0xBB67AE85u;

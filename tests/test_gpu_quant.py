@@ -162,6 +162,43 @@ def test_nvfp4_rowwise_per_tensor(mx, orc, sr):
     assert np.array_equal(to_np(s), orc.scales_to_gemm_layout(so))
 
 
+def sr_grid_tensor(T, N, seed):
+    """Blocks whose maximum is 6 units and whose other values sweep the E2M1 range densely: exact grid
+    points, values just above / below each grid point and each binade edge (0.5, 1, 2, 4), tiny values
+    and zeros, random signs -- every branch of the stochastic-rounding decision, under many random bits."""
+    rng = np.random.default_rng(seed)
+    unit = np.float32(2.0) ** rng.integers(-20, 20, size=(T, N // 16, 1)).astype(np.float32)
+    frac = rng.random((T, N // 16, 16)).astype(np.float32) * 6.0
+    grid = np.array([0, .5, 1, 1.5, 2, 3, 4, 6], dtype=np.float32)
+    pick = rng.integers(0, 8, size=frac.shape)
+    near = grid[pick] * (1 + rng.choice([-1, 0, 1], size=frac.shape) * np.float32(2.0 ** -7))
+    vals = np.where(rng.random(frac.shape) < 0.4, near, frac)
+    vals[..., 1] = rng.random((T, N // 16)) * 1e-3              # tiny values
+    vals[..., 2] = 0.0
+    vals[..., 0] = 6.0                                          # the block maximum
+    vals = vals * unit * rng.choice([-1.0, 1.0], size=frac.shape).astype(np.float32)
+    f = vals.reshape(T, N).astype(np.float32)
+    return ((f.view(np.uint32) + 0x7FFF + ((f.view(np.uint32) >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("colwise", [False, True])
+def test_nvfp4_sr_dense_grid(mx, orc, colwise):
+    """Stochastic rounding bit-exact against the oracle on values covering every E2M1 interval."""
+    T, N = (512, 1024)
+    x = sr_grid_tensor(T, N, 5 + colwise)
+    if colwise:
+        x = np.ascontiguousarray(x.T)                           # blocks of 16 along the rows for column-wise
+        T, N = N, T
+    q = torch.empty((N, T // 2) if colwise else (T, N // 2), dtype=torch.uint8, device=DEV)
+    s = torch.empty(mx.scale_bytes(N, T, 16) if colwise else mx.scale_bytes(T, N, 16), dtype=torch.uint8, device=DEV)
+    S = torch.empty(1, dtype=torch.float32, device=DEV)
+    ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+    mx.mx_nvfp4_quantize_1x16(bf16_dev(x), colwise, False, 0, True, 4321, q, s, S, ws)
+    qo, so, So = orc.nvfp4_quantize_1x16(x, colwise=colwise, sr=True, sr_seed=4321)
+    assert np.array_equal(to_np(q), qo), first_mismatch(to_np(q), qo)
+    assert np.array_equal(to_np(s), orc.scales_to_gemm_layout(so))
+
+
 @pytest.mark.parametrize("shape", [(64, 48), (256, 1024), (32, 8)])
 def test_rht16(mx, orc, shape):
     x = synthetic.random_bf16(sum(shape), shape, "student_t")
