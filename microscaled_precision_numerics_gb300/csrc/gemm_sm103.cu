@@ -101,6 +101,13 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Bulk copy from this CTA's shared memory into another CTA's of the cluster, completing `bytes` on
+// the destination CTA's mbarrier.
+__device__ __forceinline__ void bulk_signal_copy(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -194,11 +201,13 @@ __device__ __forceinline__ void epilogue_alphas(const Params& p, int64_t row, bo
 }
 
 // Drain of one tile by an epilogue warp: its 32 TMEM lanes x TN/2 FP32 columns (accumulator at tacc)
-// into packed BF16 registers with the second-level scales applied; then TMEM is handed back
-// (arrive on tempty_bar, in the leader CTA).
+// into packed BF16 registers with the second-level scales applied; then TMEM is handed back by an
+// arrival on a barrier of this CTA (`expect_signal`: the arrival also expects the odd CTA's 16-byte
+// signal copy on the even CTA's barrier).
 template <int TN, bool COL_ALPHA>
 __device__ __forceinline__ void epilogue_drain(const Params& p, uint32_t tacc, int q, int h, int lane, int64_t n0,
-                                               float aa, float ab_g, uint32_t tempty_bar, uint32_t (&packed)[TN / 4]) {
+                                               float aa, float ab_g, uint32_t tempty_bar, bool expect_signal,
+                                               uint32_t (&packed)[TN / 4]) {
     constexpr int EPI_HALF = TN / 2;                // columns per epilogue warp
     const int64_t nh = n0 + h * EPI_HALF;           // first column of this warp's half
 #pragma unroll
@@ -221,7 +230,10 @@ __device__ __forceinline__ void epilogue_drain(const Params& p, uint32_t tacc, i
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive_cluster(tempty_bar);
+    if (lane == 0) {
+        if (expect_signal) mbar_arrive_expect_tx(tempty_bar, 16);
+        else mbar_arrive(tempty_bar);
+    }
 }
 
 // Stores of one drained tile slice: rows [row0 + 32 q, +32) that belong to the tile, columns of the
@@ -316,8 +328,9 @@ struct PairCfg {
     static constexpr int SMEM_SFB = SMEM_SFA + NST * SFA_BYTES;
     static constexpr int SMEM_EPI = (SMEM_SFB + NST * SFB_BYTES + 1023) / 1024 * 1024;
     static constexpr int SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
-    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 5);
-    static constexpr int SMEM_TABLES = SMEM_MISC + 16;     // grouped: row offsets, pair-tile and band prefixes
+    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 7);
+    static constexpr int SMEM_SIGNAL = (SMEM_MISC + 16 + 15) / 16 * 16;   // 16-byte signal source / target
+    static constexpr int SMEM_TABLES = SMEM_SIGNAL + 16;   // grouped: row offsets, pair-tile and band prefixes
     static constexpr int SMEM_TOTAL = SMEM_TABLES + (GROUPED ? 8 * (MAX_GROUPS + 1) + 4 * (2 * (MAX_GROUPS + 1) + 32) : 0);
     static constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;
     static_assert(SMEM_B % 1024 == 0 && SMEM_EPI % 1024 == 0, "operand and staging alignment");
@@ -383,6 +396,7 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t bar_tfull = bar_empty + 8 * NST;                // 2 barriers (one per accumulator)
     const uint32_t bar_tempty = bar_tfull + 16;                    // 2 barriers (used in the leader)
     const uint32_t bar_done = bar_tempty + 16;
+    const uint32_t bar_tempty_odd = bar_done + 8;                  // 2 barriers (odd CTA): its epilogue drained
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
     int64_t* s_off = reinterpret_cast<int64_t*>(smem + C::SMEM_TABLES);
@@ -401,7 +415,9 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_tfull + 8 * b, 1);
-            mbar_init(bar_tempty + 8 * b, 2 * EPI_WARPS);   // the epilogue warps of both CTAs
+            // the even CTA's epilogue warps (one of them also expects the odd CTA's 16-byte signal)
+            mbar_init(bar_tempty + 8 * b, EPI_WARPS);
+            mbar_init(bar_tempty_odd + 8 * b, EPI_WARPS);
         }
         mbar_init(bar_done, 1);
         *abort_flag = 0;
@@ -530,12 +546,28 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 __syncwarp();
             }
+        } else {
+            // odd CTA: each time its epilogue warps have drained a tile (a local barrier), a 16-byte bulk
+            // copy completes on the even CTA's TMEM-empty barrier (cluster-scope release arrivals from
+            // each epilogue warp stall their warps for thousands of cycles)
+            const uint32_t tempty_leader = map_to_cta(bar_tempty, 0);
+            const uint32_t sig_dst = map_to_cta(sbase + C::SMEM_SIGNAL, 0);
+            bool ok = true;
+            int64_t ti = 0;
+            for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs, ++ti) {
+                const uint32_t ab = (uint32_t)(ti % C::ACC);
+                const uint32_t use = (uint32_t)(ti / C::ACC);
+                if (!warp_wait(bar_tempty_odd + 8 * ab, use & 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                if (lane == 0) bulk_signal_copy(sig_dst, sbase + C::SMEM_SIGNAL, 16, tempty_leader + 8 * ab);
+                __syncwarp();
+            }
+            if (!ok && lane == 0) *abort_flag = 1;
         }
     } else {
         // ------------------------------- epilogue (both CTAs) -------------------------------
         const int q = warp & 3;                     // TMEM lane quadrant this warp may access
         const int h = (warp - 2) >> 2;              // column half
-        const uint32_t tempty_leader = map_to_cta(bar_tempty, 0);
+        const uint32_t tempty_mine = leader ? bar_tempty : bar_tempty_odd;
         const uint32_t ebase = sbase + C::SMEM_EPI + (uint32_t)((warp - 2) * 2 * EPI_BUF_BYTES);
         uint32_t epi_chunk = 0;
         // tile coordinates and row scales of the next tile are fetched while this tile's stores run
@@ -553,7 +585,8 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (!mbar_wait(bar_tfull + 8 * ab, use & 1u, abort_flag, &g_mx_device_status)) break;
             tc_fence_after();
             uint32_t packed[TN / 4];
-            epilogue_drain<TN, COL_ALPHA>(p, tmem + ab * TN, q, h, lane, tile.n0, aa, ab_g, tempty_leader + 8 * ab, packed);
+            epilogue_drain<TN, COL_ALPHA>(p, tmem + ab * TN, q, h, lane, tile.n0, aa, ab_g, tempty_mine + 8 * ab,
+                                          leader && warp == 2, packed);
             const PairTile cur = tile;
             const int64_t tn = t + n_pairs;
             if (tn < total_tiles) {
@@ -678,13 +711,6 @@ __device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t byte) {
     uint32_t r;
     asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(r) : "r"(byte * 0x0101u));
     return r;
-}
-
-// Bulk copy from this CTA's shared memory into another CTA's of the cluster, completing `bytes` on
-// the destination CTA's mbarrier.
-__device__ __forceinline__ void bulk_signal_copy(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
-    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster) : "memory");
 }
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
