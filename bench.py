@@ -491,7 +491,8 @@ class DenseNVFP4:
     (both orientations), X and dY 1x16 row-wise under per-tensor scales (RNE for X, SR for dY), FPROP and
     DGRAD as NVFP4 GEMMs with the 2D weight, RHT16 + column-wise 1x16 of dY (SR) and X (RNE) and the NVFP4
     WGRAD.  Aux: the dequantized-backward DGRAD (BF16 dY times DQ(W) expanded inside the GEMM, no BF16
-    weight copy) and, for comparison, the materialized DQ(W) it avoids."""
+    weight copy) and WGRAD (BF16 dY^T times DQ(X) of the forward's X codes) and, for comparison, the
+    materialized DQ(W) the DGRAD avoids."""
     name = "dense_nvfp4"
 
     def __init__(self, mx, torch, dev):
@@ -517,6 +518,7 @@ class DenseNVFP4:
         self.dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         self.dw = torch.empty((F, H), dtype=torch.bfloat16, device=dev)
         self.dx_dq = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.dw_dq = torch.empty((F, H), dtype=torch.bfloat16, device=dev)
         self.wdq = torch.empty((H, F), dtype=torch.bfloat16, device=dev)
         self.launches_per_step = 13
 
@@ -559,6 +561,8 @@ class DenseNVFP4:
             ("gemm16", "DGRAD dequantized backward (BF16 dY x DQ(W) in the mainloop)", 0, 2.0 * T * H * F,
              lambda: mx.mx_gemm_bf16_dq_nvfp4(self.dy, qw["q_col"][0], qw["s_col"], qw["s_w"], mx.MX_SCOPE_TENSOR,
                                               T, H, F, self.dx_dq)),
+            ("gemm16", "WGRAD dequantized backward (BF16 dY^T x DQ(X) in the mainloop)", 0, 2.0 * F * H * T,
+             lambda: mx.mx_wgrad_bf16_dq_nvfp4(self.dy, self.qx, self.sx, self.Sx, mx.MX_SCOPE_TENSOR, self.dw_dq)),
             ("quant", "DQ(W) materialized (the BF16 copy the fused GEMM avoids)", 1, F * H * (0.5 + 1 / 16 + 2),
              lambda: mx.mx_dequantize_bf16(mx.MX_FMT_NVFP4, qw["q_col"][0], qw["s_col"], qw["s_w"], mx.MX_SCOPE_TENSOR,
                                            H, F, self.wdq)),

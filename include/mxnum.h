@@ -283,6 +283,23 @@ mx_status mx_gemm_bf16_dq_nvfp4(const void* a, const float* alpha_a, mx_scope al
                                 const uint8_t* sb, const float* sb2, mx_scope sb2_scope, int64_t M, int64_t N,
                                 int64_t K, void* d, int64_t ldd, cudaStream_t stream);
 
+/* Weight gradient of the dequantized backward, X's NVFP4 codes expanded inside the GEMM:
+ *   dW[o, h] = BF16( sum_t dY[t, o] * DQ(X)[t, h] ),  DQ(X)[t, h] = BF16( fp32(val(q) * val(bs)) * S ),
+ * the values mx_dequantize_bf16 writes for X quantized 1x16 along h (per-token S: MX_SCOPE_ROW, one S per
+ * token row; per-tensor: MX_SCOPE_TENSOR).  Both operands are read as stored (tokens along K, neither
+ * transposed): dY through 64 x 64 TMA boxes into MN-major tiles, X's codes expanded into MN-major BF16 tiles.
+ * Source: 4-bitter page, "dequantized backward" (the backward GEMMs run on BF16 operands rebuilt from the
+ * forward's exact NVFP4 values).
+ *   dy     [T, O] BF16, contiguous
+ *   qx     [T, H/2] E2M1 codes; sx mx_scale_bytes(T, H, 16) E4M3 scales in the GEMM layout; sx2 T FP32
+ *          (MX_SCOPE_ROW) or one FP32 (MX_SCOPE_TENSOR)
+ *   dw     [O, ldd] BF16
+ * FP32 accumulation in the tensor core.  Requires T % 64 == 0, H % 32 == 0, ldd % 8 == 0, ldd >= H,
+ * O, H < 2^31; dy, qx, sx, dw 16-byte aligned. */
+mx_status mx_wgrad_bf16_dq_nvfp4(const void* dy, const uint8_t* qx, const uint8_t* sx, const float* sx2,
+                                 mx_scope sx2_scope, int64_t T, int64_t O, int64_t H, void* dw, int64_t ldd,
+                                 cudaStream_t stream);
+
 /* Grouped block-scaled GEMM over expert-sorted rows: for every group g,
  *   D[rows of g] = BF16( alpha_a[row] * alpha_b[g] * A[rows of g] . B_g^T ).
  * Source: Miles page -- NVFP4 on the routed experts' weights and activations with a per-token

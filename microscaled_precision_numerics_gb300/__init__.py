@@ -63,6 +63,7 @@ def lib() -> ctypes.CDLL:
                 "mx_grouped_scaled_gemm": (I32, [I32, I64, P, I64, P, P, P, P, P, P, I64, I64, P, P]),
                 "mx_count_mismatch": (I32, [P, P, I64, P, P]),
                 "mx_gemm_bf16_dq_nvfp4": (I32, [P, P, I32, P, P, P, I32, I64, I64, I64, P, I64, P]),
+                "mx_wgrad_bf16_dq_nvfp4": (I32, [P, P, P, P, I32, I64, I64, I64, P, I64, P]),
                 "mx_check_device_status": (I32, []),
             }
             for name, (res, args) in sigs.items():
@@ -247,6 +248,18 @@ def mx_gemm_bf16_dq_nvfp4(a, qb, sb, sb2, sb2_scope, M: int, N: int, K: int, d, 
     _check("mx_gemm_bf16_dq_nvfp4", lib().mx_gemm_bf16_dq_nvfp4(
         _p(a), _p(alpha_a), int(alpha_a_scope), _p(qb), _p(sb), _p(sb2), int(sb2_scope), M, N, K, _p(d), d.stride(0),
         _stream(stream)))
+
+
+def mx_wgrad_bf16_dq_nvfp4(dy, qx, sx, sx2, sx2_scope, dw, stream=None):
+    """dW = BF16(dY^T @ DQ(X)) with dY BF16 [T, O] and X as NVFP4 codes [T, H/2] + GEMM-layout scales + FP32
+    second-level scale(s) (MX_SCOPE_ROW: per token, MX_SCOPE_TENSOR), X expanded to BF16 inside the GEMM."""
+    dy = _bf16_bits(dy)
+    T, O = dy.shape
+    H = qx.shape[1] * 2
+    if dy.stride(0) != O or dy.stride(1) != 1:
+        raise ValueError("dY must be a contiguous [T, O] BF16 tensor")
+    _check("mx_wgrad_bf16_dq_nvfp4", lib().mx_wgrad_bf16_dq_nvfp4(
+        _p(dy), _p(qx), _p(sx), _p(sx2), int(sx2_scope), T, O, H, _p(dw), dw.stride(0), _stream(stream)))
 
 
 def mx_grouped_scaled_gemm(fmt: int, group_offsets, a, sa, alpha_a_rows, b, sb, alpha_b_groups, N: int, K: int, d,

@@ -647,12 +647,14 @@ static_assert(DQ_CONV_CHUNKS == 2 || DQ_CONV_CHUNKS == 4 || DQ_CONV_CHUNKS == 8,
 
 struct DqParams {
     const float* alpha_a; int alpha_a_scope;
-    const float* sb2; int sb2_scope;        // B's FP32 second-level scale: 1 = one value, 2 = per B row
+    const float* sb2; int sb2_scope;        // B's FP32 second-level scale: 1 = one value, 2 = per B row,
+                                            // 3 = per K index (per-token scales of a weight-gradient B)
     int64_t M, N, K;
     uint16_t* d; int64_t ldd;
     int64_t m_tiles, n_tiles, k_stages, nct, total_tiles;
 };
 
+template <bool WG>
 struct DqCfg {
     static constexpr int NST = 4;                          // A / B (BF16) ring
     static constexpr int NQ = 3;                           // codes ring
@@ -660,7 +662,9 @@ struct DqCfg {
     static constexpr int A_BYTES = 2 * A_BLOCK;            // this CTA's rows of both 256-row halves of the tile
     static constexpr int B_BYTES = 128 * BKB;              // this CTA's 128 B rows x 64 BF16 (built here)
     static constexpr int Q_BYTES = 128 * 32;               // their codes, 64 E2M1 values per row
-    static constexpr int SF_BYTES = 512;                   // their scale atom (4 scales per row)
+    // their scales: one atom (4 scales per row) for K-major B; for the weight gradient (B = X, tokens
+    // along K) the two atoms holding the 8 block columns of the CTA's 128 B rows for 128 tokens
+    static constexpr int SF_BYTES = WG ? 1024 : 512;
     static constexpr uint32_t A_TX = 2u * A_BYTES;         // both CTAs' A rows, on the even CTA's barrier
     static constexpr uint32_t Q_TX = Q_BYTES + SF_BYTES;   // per CTA, on its own barrier
     static constexpr int FULL_ARRIVALS = 1 + DQ_CONV_WARPS;      // producer and the even CTA's converter warps
@@ -695,9 +699,19 @@ __device__ __forceinline__ PairTile dq_tile(const DqParams& p, int64_t t, uint32
 
 // kind::f16 instruction descriptor: D FP32 (bits 4-5 = 1), A and B BF16 (7-9, 10-12 = 1), K-major
 // A and B, N >> 3 (17-22), M >> 4 (24-28).
-template <int MMA_M, int MMA_N>
+template <int MMA_M, int MMA_N, bool MN_MAJOR = false>
 __device__ __forceinline__ uint32_t make_idesc_bf16() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(MMA_N >> 3) << 17) | ((uint32_t)(MMA_M >> 4) << 24);
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((MN_MAJOR ? 1u : 0u) << 15) | ((MN_MAJOR ? 1u : 0u) << 16) |
+           ((uint32_t)(MMA_N >> 3) << 17) | ((uint32_t)(MMA_M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor, MN-major, 128-byte swizzle (16-bit elements): atoms of 64 MN
+// elements (one 128-byte row) x 8 K rows; MN atoms DQ_MN_ATOM bytes apart (leading byte offset), 8-row
+// K groups 1024 bytes apart (stride byte offset).
+constexpr int DQ_MN_ATOM = 64 * 128;
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(DQ_MN_ATOM >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
 __device__ __forceinline__ void tc2_mma_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
@@ -736,11 +750,12 @@ __device__ __forceinline__ uint4 dq_word(uint32_t w, uint32_t bs_h2, float S) {
 
 
 
+template <bool WG>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DQ_THREADS, 1)
 dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmSB, const __grid_constant__ CUtensorMap tmD,
                     const DqParams p) {
-    using C = DqCfg;
+    using C = DqCfg<WG>;
     constexpr int NST = C::NST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -809,8 +824,18 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t fb = map_to_cta(bar_full + 8 * stage, 0);
                     if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_TX + C::SIGNAL_TX);
                     const uint32_t sA = sbase + C::SMEM_A + stage * C::A_BYTES;
-                    tma_load_2d_pair(sA, &tmA, (int32_t)(ks * BKB), (int32_t)tile.row0, fb);
-                    tma_load_2d_pair(sA + C::A_BLOCK, &tmA, (int32_t)(ks * BKB), (int32_t)(tile.row0 + 256), fb);
+                    if constexpr (WG) {
+                        // A = dY^T: boxes of 64 tokens x 64 output features of dY [T, O] (MN-major)
+#pragma unroll
+                        for (int b = 0; b < 2; ++b)
+#pragma unroll
+                            for (int j = 0; j < 2; ++j)
+                                tma_load_2d_pair(sA + b * C::A_BLOCK + j * DQ_MN_ATOM, &tmA,
+                                                 (int32_t)(tile.row0 + 256 * b + 64 * j), (int32_t)(ks * 64), fb);
+                    } else {
+                        tma_load_2d_pair(sA, &tmA, (int32_t)(ks * BKB), (int32_t)tile.row0, fb);
+                        tma_load_2d_pair(sA + C::A_BLOCK, &tmA, (int32_t)(ks * BKB), (int32_t)(tile.row0 + 256), fb);
+                    }
                 }
                 __syncwarp();
                 if (++stage == NST) { stage = 0; phase ^= 1; }
@@ -836,11 +861,14 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES;
 #pragma unroll
                         for (int j = 0; j < BKB / 32; ++j) {
-                            const uint64_t bd = desc_sw128(sB + 32 * j);
+                            // K = 16 per MMA: 32 bytes along a K-major row, or two 8-row K groups MN-major
+                            const uint32_t koff = WG ? 2048u * j : 32u * j;
+                            const uint64_t bd = WG ? desc_mn_sw128(sB + koff) : desc_sw128(sB + koff);
+                            const uint64_t ad0 = WG ? desc_mn_sw128(sA + koff) : desc_sw128(sA + koff);
+                            const uint64_t ad1 = WG ? desc_mn_sw128(sA + C::A_BLOCK + koff) : desc_sw128(sA + C::A_BLOCK + koff);
                             const uint32_t acc = (ks > 0 || j > 0) ? 1u : 0u;
-                            tc2_mma_bf16(tmem, desc_sw128(sA + 32 * j), bd, make_idesc_bf16<2 * BM, DQ_TN>(), acc);
-                            tc2_mma_bf16(tmem + DQ_TN, desc_sw128(sA + C::A_BLOCK + 32 * j), bd,
-                                         make_idesc_bf16<2 * BM, DQ_TN>(), acc);
+                            tc2_mma_bf16(tmem, ad0, bd, make_idesc_bf16<2 * BM, DQ_TN, WG>(), acc);
+                            tc2_mma_bf16(tmem + DQ_TN, ad1, bd, make_idesc_bf16<2 * BM, DQ_TN, WG>(), acc);
                         }
                         tc2_commit_mc(bar_empty + 8 * stage, (uint16_t)3);
                     }
@@ -943,55 +971,97 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         __syncwarp();
     } else if (warp < DQ_QPROD_WARP) {
         // ------------------------------- converters (both CTAs) -------------------------------
-        // thread ct: B row r of this CTA's half, chunks [part * DQ_CONV_CHUNKS, +DQ_CONV_CHUNKS) of its 8
-        const int ct = threadIdx.x - 32 * DQ_CONV_WARP0;
-        const int r = ct / (8 / DQ_CONV_CHUNKS), part = ct % (8 / DQ_CONV_CHUNKS);
-        const uint32_t row_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
-        const uint32_t sf_off = (uint32_t)((r & 31) * 16 + ((r >> 5) & 3) * 4);
-        int stage = 0, qstage = 0;
-        uint32_t phase = 0, qphase = 0;
-        bool ok = true;
-        for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
-            const PairTile tile = dq_tile(p, t, rank);
-            const int64_t brow = tile.n0 + 128 * (int64_t)rank + r;
-            float S = 0.0f;
-            if (p.sb2_scope == 1) S = __ldg(p.sb2);
-            else if (brow < p.N) S = __ldg(p.sb2 + brow);
-            for (int64_t ks = 0; ks < p.k_stages; ++ks) {
-                if (!warp_wait(bar_qfull + 8 * qstage, qphase, abort_flag, &g_mx_device_status)) { ok = false; break; }
-                if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
-                const uint8_t* qsrc = smem + C::SMEM_Q + qstage * C::Q_BYTES + r * 32 + part * 4 * DQ_CONV_CHUNKS;
-                uint32_t w[DQ_CONV_CHUNKS];
-                if constexpr (DQ_CONV_CHUNKS >= 4) {
+        if constexpr (WG) {
+            // B = X (tokens along K): thread ct expands token row t = ct / 4 of the stage, values
+            // 32 (ct % 4) .. + 31 of this CTA's 128 B columns, into the MN-major tile (64 B columns per
+            // 128-byte row, one row per token, 128-byte swizzle); S is the token's second-level scale.
+            const int ct = threadIdx.x - 32 * DQ_CONV_WARP0;
+            const int t = ct >> 2, quarter = ct & 3;
+            const uint32_t sf_col = (uint32_t)((quarter >> 1) * 512 + (quarter & 1) * 2);
+            const uint32_t row_off = (uint32_t)((quarter >> 1) * DQ_MN_ATOM + t * 128);
+            int stage = 0, qstage = 0;
+            uint32_t phase = 0, qphase = 0;
+            bool ok = true;
+            for (int64_t tt = pair_id; tt < total_tiles && ok; tt += n_pairs) {
+                for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                    if (!warp_wait(bar_qfull + 8 * qstage, qphase, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                    if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                    const int64_t tok = ks * 64 + t;
+                    const float S = p.sb2_scope == 1 ? __ldg(p.sb2) : (tok < p.K ? __ldg(p.sb2 + tok) : 0.0f);
+                    const uint4 c4 = *reinterpret_cast<const uint4*>(smem + C::SMEM_Q + qstage * C::Q_BYTES + t * 64 + quarter * 16);
+                    const uint32_t tb = (uint32_t)(tok & 127);
+                    const uint32_t bs2 = *reinterpret_cast<const uint16_t*>(
+                        smem + C::SMEM_SF + qstage * C::SF_BYTES + sf_col + (tb & 31) * 16 + ((tb >> 5) & 3) * 4);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_qempty + 8 * qstage);
+                    if (++qstage == C::NQ) { qstage = 0; qphase ^= 1; }
+                    const uint32_t w[4] = {c4.x, c4.y, c4.z, c4.w};
+                    const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES + row_off;
 #pragma unroll
-                    for (int i = 0; i < DQ_CONV_CHUNKS; i += 4) {
-                        const uint4 c4 = *reinterpret_cast<const uint4*>(qsrc + 4 * i);
-                        w[i] = c4.x; w[i + 1] = c4.y; w[i + 2] = c4.z; w[i + 3] = c4.w;
+                    for (int i2 = 0; i2 < 4; ++i2) {
+                        const uint32_t c = (uint32_t)((quarter & 1) * 4 + i2);      // 16-byte chunk of the row
+                        const uint32_t bs_h2 = e4m3_to_f16x2_bcast((bs2 >> (8 * (i2 >> 1))) & 0xFFu);
+                        const uint4 o = dq_word(w[i2], bs_h2, S);
+                        st_shared_v4(sB + 16u * (c ^ (uint32_t)(t & 7)), o.x, o.y, o.z, o.w);
                     }
-                } else {
-                    const uint2 c2 = *reinterpret_cast<const uint2*>(qsrc);
-                    w[0] = c2.x; w[1] = c2.y;
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(leader ? bar_full + 8 * stage : bar_bconv + 8 * stage);
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
                 }
-                const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + C::SMEM_SF + qstage * C::SF_BYTES + sf_off);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_qempty + 8 * qstage);            // codes slot read
-                if (++qstage == C::NQ) { qstage = 0; qphase ^= 1; }
-                const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES + row_off;
-#pragma unroll
-                for (int i = 0; i < DQ_CONV_CHUNKS; ++i) {
-                    // chunk ci = values 8 ci .. 8 ci + 7 of the stage, block ci / 2 of the row's four
-                    const int ci = part * DQ_CONV_CHUNKS + i;
-                    const uint32_t bs_h2 = e4m3_to_f16x2_bcast((sc >> (8 * (ci >> 1))) & 0xFFu);
-                    const uint4 o = dq_word(w[i], bs_h2, S);
-                    st_shared_v4(sB + 16u * ((uint32_t)ci ^ (uint32_t)(r & 7)), o.x, o.y, o.z, o.w);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(leader ? bar_full + 8 * stage : bar_bconv + 8 * stage);
-                if (++stage == NST) { stage = 0; phase ^= 1; }
             }
+            if (!ok && lane == 0) *abort_flag = 1;
+        } else {
+            // thread ct: B row r of this CTA's half, chunks [part * DQ_CONV_CHUNKS, +DQ_CONV_CHUNKS) of its 8
+            const int ct = threadIdx.x - 32 * DQ_CONV_WARP0;
+            const int r = ct / (8 / DQ_CONV_CHUNKS), part = ct % (8 / DQ_CONV_CHUNKS);
+            const uint32_t row_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+            const uint32_t sf_off = (uint32_t)((r & 31) * 16 + ((r >> 5) & 3) * 4);
+            int stage = 0, qstage = 0;
+            uint32_t phase = 0, qphase = 0;
+            bool ok = true;
+            for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
+                const PairTile tile = dq_tile(p, t, rank);
+                const int64_t brow = tile.n0 + 128 * (int64_t)rank + r;
+                float S = 0.0f;
+                if (p.sb2_scope == 1) S = __ldg(p.sb2);
+                else if (brow < p.N) S = __ldg(p.sb2 + brow);
+                for (int64_t ks = 0; ks < p.k_stages; ++ks) {
+                    if (!warp_wait(bar_qfull + 8 * qstage, qphase, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                    if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                    const uint8_t* qsrc = smem + C::SMEM_Q + qstage * C::Q_BYTES + r * 32 + part * 4 * DQ_CONV_CHUNKS;
+                    uint32_t w[DQ_CONV_CHUNKS];
+                    if constexpr (DQ_CONV_CHUNKS >= 4) {
+#pragma unroll
+                        for (int i = 0; i < DQ_CONV_CHUNKS; i += 4) {
+                            const uint4 c4 = *reinterpret_cast<const uint4*>(qsrc + 4 * i);
+                            w[i] = c4.x; w[i + 1] = c4.y; w[i + 2] = c4.z; w[i + 3] = c4.w;
+                        }
+                    } else {
+                        const uint2 c2 = *reinterpret_cast<const uint2*>(qsrc);
+                        w[0] = c2.x; w[1] = c2.y;
+                    }
+                    const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + C::SMEM_SF + qstage * C::SF_BYTES + sf_off);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_qempty + 8 * qstage);            // codes slot read
+                    if (++qstage == C::NQ) { qstage = 0; qphase ^= 1; }
+                    const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES + row_off;
+#pragma unroll
+                    for (int i = 0; i < DQ_CONV_CHUNKS; ++i) {
+                        // chunk ci = values 8 ci .. 8 ci + 7 of the stage, block ci / 2 of the row's four
+                        const int ci = part * DQ_CONV_CHUNKS + i;
+                        const uint32_t bs_h2 = e4m3_to_f16x2_bcast((sc >> (8 * (ci >> 1))) & 0xFFu);
+                        const uint4 o = dq_word(w[i], bs_h2, S);
+                        st_shared_v4(sB + 16u * ((uint32_t)ci ^ (uint32_t)(r & 7)), o.x, o.y, o.z, o.w);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(leader ? bar_full + 8 * stage : bar_bconv + 8 * stage);
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok && lane == 0) *abort_flag = 1;
         }
-        if (!ok && lane == 0) *abort_flag = 1;
     } else {
         // ------------------------------- codes producer (both CTAs) -------------------------------
         // codes and scale atom of this CTA's 128 B rows, up to NQ stages ahead of the converters
@@ -1007,8 +1077,16 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (elect_one()) {
                     const uint32_t qb = bar_qfull + 8 * qstage;
                     mbar_arrive_expect_tx(qb, C::Q_TX);
-                    tma_load_2d(sbase + C::SMEM_Q + qstage * C::Q_BYTES, &tmQ, (int32_t)(ks * 32), (int32_t)brow, qb);
-                    tma_load_2d(sbase + C::SMEM_SF + qstage * C::SF_BYTES, &tmSB, 0, (int32_t)((band * p.nct + ks) * 2), qb);
+                    if constexpr (WG) {
+                        // 64 tokens x this CTA's 128 B columns of X's codes; the two scale atoms of those
+                        // columns in the tokens' 128-row band
+                        tma_load_2d(sbase + C::SMEM_Q + qstage * C::Q_BYTES, &tmQ, (int32_t)(brow / 2), (int32_t)(ks * 64), qb);
+                        tma_load_2d(sbase + C::SMEM_SF + qstage * C::SF_BYTES, &tmSB, 0,
+                                    (int32_t)((((ks * 64) / 128) * p.nct + brow / 64) * 2), qb);
+                    } else {
+                        tma_load_2d(sbase + C::SMEM_Q + qstage * C::Q_BYTES, &tmQ, (int32_t)(ks * 32), (int32_t)brow, qb);
+                        tma_load_2d(sbase + C::SMEM_SF + qstage * C::SF_BYTES, &tmSB, 0, (int32_t)((band * p.nct + ks) * 2), qb);
+                    }
                 }
                 __syncwarp();
                 if (++qstage == C::NQ) { qstage = 0; qphase ^= 1; }
@@ -1114,13 +1192,14 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
     return cudaGetLastError();
 }
 
+template <bool WG>
 cudaError_t launch_dq_impl(const DqGemmArgs& a, int num_sms, cudaStream_t stream) {
-    using C = DqCfg;
+    using C = DqCfg<WG>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     static int resident_pairs = 0;
     std::call_once(attr_once, [num_sms] {
-        attr_err = cudaFuncSetAttribute(dq_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        attr_err = cudaFuncSetAttribute(dq_gemm_pair_kernel<WG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
         if (attr_err != cudaSuccess) return;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(num_sms & ~1));
@@ -1131,7 +1210,7 @@ cudaError_t launch_dq_impl(const DqGemmArgs& a, int num_sms, cudaStream_t stream
         attr[0].val.clusterDim.x = 2; attr[0].val.clusterDim.y = 1; attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr; cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, dq_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&n, dq_gemm_pair_kernel<WG>, &cfg) != cudaSuccess || n <= 0) {
             cudaGetLastError();
             n = num_sms / 2;
         }
@@ -1139,11 +1218,23 @@ cudaError_t launch_dq_impl(const DqGemmArgs& a, int num_sms, cudaStream_t stream
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap tmA, tmQ, tmSB, tmD;
-    if (!make_map(&tmA, reinterpret_cast<const uint8_t*>(a.a), a.K * 2, a.M, 128)) return cudaErrorInvalidValue;
-    if (!encode_tensor_map_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qb, (uint64_t)(a.K / 2), (uint64_t)a.N,
-                              (uint64_t)(a.K / 2), 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
-        return cudaErrorInvalidValue;
-    if (!make_sf_map(&tmSB, a.sb, host_scale_bytes(a.N, a.K, 16), 1)) return cudaErrorInvalidValue;
+    if constexpr (WG) {
+        // A = dY [K = T, M = O] read in 64 x 64 boxes (MN-major); B codes = X [K = T, N/2] in boxes of
+        // 64 tokens x 64 bytes; X's scales (T, N, 16) in two-atom boxes
+        if (!encode_tensor_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.a, (uint64_t)a.M, (uint64_t)a.K,
+                                  (uint64_t)(a.M * 2), 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+            return cudaErrorInvalidValue;
+        if (!encode_tensor_map_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qb, (uint64_t)(a.N / 2), (uint64_t)a.K,
+                                  (uint64_t)(a.N / 2), 64, 64, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+            return cudaErrorInvalidValue;
+        if (!make_sf_map(&tmSB, a.sb, host_scale_bytes(a.K, a.N, 16), 2)) return cudaErrorInvalidValue;
+    } else {
+        if (!make_map(&tmA, reinterpret_cast<const uint8_t*>(a.a), a.K * 2, a.M, 128)) return cudaErrorInvalidValue;
+        if (!encode_tensor_map_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qb, (uint64_t)(a.K / 2), (uint64_t)a.N,
+                                  (uint64_t)(a.K / 2), 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+            return cudaErrorInvalidValue;
+        if (!make_sf_map(&tmSB, a.sb, host_scale_bytes(a.N, a.K, 16), 1)) return cudaErrorInvalidValue;
+    }
     if (!make_out_map(&tmD, a.d, a.M, a.N, a.ldd, (uint32_t)EPI_COLS)) return cudaErrorInvalidValue;
     DqParams p{};
     p.alpha_a = a.alpha_a; p.alpha_a_scope = a.alpha_a_scope;
@@ -1152,12 +1243,13 @@ cudaError_t launch_dq_impl(const DqGemmArgs& a, int num_sms, cudaStream_t stream
     p.m_tiles = (a.M + 511) / 512;
     p.n_tiles = (a.N + DQ_TN - 1) / DQ_TN;
     p.k_stages = a.K / 64;
-    p.nct = (a.K / 16 + 3) / 4;
+    p.nct = WG ? (a.N / 16 + 3) / 4 : (a.K / 16 + 3) / 4;
     p.total_tiles = p.m_tiles * p.n_tiles;
     const int64_t pairs = max64(1, min64(p.total_tiles, (int64_t)min(resident_pairs, num_sms / 2)));
-    dq_gemm_pair_kernel<<<(unsigned)(2 * pairs), DQ_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmQ, tmSB, tmD, p);
+    dq_gemm_pair_kernel<WG><<<(unsigned)(2 * pairs), DQ_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmQ, tmSB, tmD, p);
     return cudaGetLastError();
 }
+
 
 }  // namespace
 
@@ -1206,7 +1298,7 @@ cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t s
 }
 
 cudaError_t launch_dq_gemm(const DqGemmArgs& args, int num_sms, cudaStream_t stream) {
-    return launch_dq_impl(args, num_sms, stream);
+    return args.wgrad ? launch_dq_impl<true>(args, num_sms, stream) : launch_dq_impl<false>(args, num_sms, stream);
 }
 
 uint32_t read_and_clear_device_status() {

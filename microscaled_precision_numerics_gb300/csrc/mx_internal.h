@@ -57,13 +57,16 @@ struct GemmArgs {
 };
 cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream);
 
-// BF16 x dequantized-NVFP4 GEMM: A BF16 [M, K]; B NVFP4 codes [N, K/2], E4M3 scales in the GEMM layout and an
-// FP32 second-level scale (sb2_scope 1: one value, 2: per B row); alpha_a as in GemmArgs.
+// BF16 x dequantized-NVFP4 GEMM.  K-major form: A BF16 [M, K]; B NVFP4 codes [N, K/2], E4M3 scales in the GEMM
+// layout and an FP32 second-level scale (sb2_scope 1: one value, 2: per B row).  Weight-gradient form
+// (wgrad): A BF16 [K, M] (dY), B codes [K, N/2] with scales (K, N, 16) (X quantized along N) and sb2_scope
+// 1 or 3 (per K row, i.e. per token); D = A^T DQ(B).  alpha_a as in GemmArgs.
 struct DqGemmArgs {
     const uint16_t* a; const float* alpha_a; int alpha_a_scope;
     const uint8_t* qb; const uint8_t* sb; const float* sb2; int sb2_scope;
     int64_t M, N, K;
     uint16_t* d; int64_t ldd;
+    bool wgrad;
 };
 cudaError_t launch_dq_gemm(const DqGemmArgs& args, int num_sms, cudaStream_t stream);
 uint32_t read_and_clear_device_status();

@@ -291,6 +291,25 @@ mx_status mx_gemm_bf16_dq_nvfp4(const void* a, const float* alpha_a, mx_scope al
     return from_cuda(mxk::launch_dq_gemm(g, mxk::device_sm_count(), stream));
 }
 
+mx_status mx_wgrad_bf16_dq_nvfp4(const void* dy, const uint8_t* qx, const uint8_t* sx, const float* sx2,
+                                 mx_scope sx2_scope, int64_t T, int64_t O, int64_t H, void* dw, int64_t ldd,
+                                 cudaStream_t stream) {
+    if (!dy || !qx || !sx || !sx2 || !dw || T <= 0 || O <= 0 || H <= 0 || ldd < H) return MX_ERR_INVALID_ARG;
+    if (sx2_scope != MX_SCOPE_TENSOR && sx2_scope != MX_SCOPE_ROW) return MX_ERR_INVALID_ARG;
+    if (!aligned16(dy) || !aligned16(qx) || !aligned16(sx) || !aligned16(dw) || (ldd % 8) != 0 || (O % 8) != 0)
+        return MX_ERR_ALIGNMENT;
+    if ((T % 64) != 0 || (H % 32) != 0 || O >= (int64_t(1) << 31) || H >= (int64_t(1) << 31) ||
+        T >= (int64_t(1) << 31))
+        return MX_ERR_UNSUPPORTED;
+    mxk::DqGemmArgs g{};
+    g.a = static_cast<const uint16_t*>(dy);
+    g.alpha_a = nullptr; g.alpha_a_scope = 0;
+    g.qb = qx; g.sb = sx; g.sb2 = sx2; g.sb2_scope = sx2_scope == MX_SCOPE_TENSOR ? 1 : 3;
+    g.M = O; g.N = H; g.K = T; g.d = static_cast<uint16_t*>(dw); g.ldd = ldd;
+    g.wgrad = true;
+    return from_cuda(mxk::launch_dq_gemm(g, mxk::device_sm_count(), stream));
+}
+
 mx_status mx_grouped_scaled_gemm(mx_format fmt, int64_t G, const int64_t* group_offsets, int64_t total_rows,
                                  const uint8_t* a, const uint8_t* sa, const float* alpha_a_rows, const uint8_t* b,
                                  const uint8_t* sb, const float* alpha_b_groups, int64_t N, int64_t K, void* d,

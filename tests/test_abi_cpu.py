@@ -28,7 +28,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ["mx_quantize_mxfp8", "mx_nvfp4_quantize_per_token", "mx_nvfp4_quantize_weight_2d", "mx_rht16",
                      "mx_nvfp4_quantize_1x16", "mx_dequantize_bf16", "mx_scaled_gemm", "mx_grouped_scaled_gemm",
-                     "mx_fp8_blockwise_quantize_1x128", "mx_fp8_blockwise_quantize_128x128"]:
+                     "mx_fp8_blockwise_quantize_1x128", "mx_fp8_blockwise_quantize_128x128", "mx_gemm_bf16_dq_nvfp4",
+                     "mx_wgrad_bf16_dq_nvfp4"]:
         assert required in names
 
 
@@ -115,6 +116,21 @@ def test_gemm_validation(lib):
     assert gg(1, 0, A16, 16, A16, A16, NUL, A16, A16, NUL, 256, 256, A16, NUL) == 1      # G = 0
     assert gg(1, 5000, A16, 16, A16, A16, NUL, A16, A16, NUL, 256, 256, A16, NUL) == 1   # too many groups
     assert gg(1, 4, A16, 16, A16, A16, NUL, A16, A16, NUL, 256, 200, A16, NUL) == 3      # K % 256
+
+
+def test_dq_gemm_validation(lib):
+    g = lib.mx_gemm_bf16_dq_nvfp4
+    assert g(A16, NUL, 0, A16, A16, A16, 1, 128, 128, 96, A16, 128, NUL) == 3      # K % 64
+    assert g(A16, NUL, 0, A16, A16, A16, 0, 128, 128, 128, A16, 128, NUL) == 1     # second-level scope
+    assert g(A16, NUL, 2, A16, A16, A16, 1, 128, 128, 128, A16, 128, NUL) == 1     # alpha scope without pointer
+    assert g(A16, NUL, 0, A16, A16, A16, 1, 128, 100, 128, A16, 100, NUL) == 2     # N % 8
+    assert g(A8, NUL, 0, A16, A16, A16, 1, 128, 128, 128, A16, 128, NUL) == 2
+    w = lib.mx_wgrad_bf16_dq_nvfp4
+    assert w(A16, A16, A16, A16, 2, 96, 128, 128, A16, 128, NUL) == 3              # T % 64
+    assert w(A16, A16, A16, A16, 2, 128, 128, 80, A16, 80, NUL) == 3               # H % 32
+    assert w(A16, A16, A16, A16, 2, 128, 100, 128, A16, 128, NUL) == 2             # O % 8 (dY row pitch)
+    assert w(A16, A16, A16, A16, 3, 128, 128, 128, A16, 128, NUL) == 1             # scope
+    assert w(A16, A16, A16, NUL, 2, 128, 128, 128, A16, 128, NUL) == 1             # no scales
 
 
 def test_mismatch_validation(lib):

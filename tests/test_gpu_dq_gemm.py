@@ -110,3 +110,37 @@ def test_fed_by_the_gpu_weight_quantizer(mx, orc):
     _, q_col, st, s_w = orc.nvfp4_quantize_weight_2d(w)
     ref = orc.gemm_ref_bf16_dq_nvfp4(dy, q_col, orc.weight_2d_operand_scales(st, "col"), s_w, False)
     assert orc.rel_fro_error(d.float().cpu().numpy().astype(np.float64), ref) <= TOL
+
+
+def run_wgrad(mx, orc, dy, qx, sx_compact, sx2, per_row):
+    T, O = dy.shape
+    H = qx.shape[1] * 2
+    dw = torch.full((O, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mx.mx_wgrad_bf16_dq_nvfp4(bf16_dev(dy), dev_u8(qx), dev_u8(orc.scales_to_gemm_layout(sx_compact)), dev_f32(sx2),
+                              mx.MX_SCOPE_ROW if per_row else mx.MX_SCOPE_TENSOR, dw)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    Y = orc.bf16_to_f32(dy).astype(np.float64)
+    X = orc.bf16_to_f32(orc.dequant_nvfp4(qx, sx_compact, sx2, per_row)).astype(np.float64)
+    ref = Y.T @ X                  # the dequantized-backward weight gradient: dY^T DQ(X), FP64
+    return dw.float().cpu().numpy().astype(np.float64), ref, np.abs(Y).T @ np.abs(X)
+
+
+@pytest.mark.parametrize("T,O,H", [(256, 256, 256), (512, 384, 320), (64, 128, 64), (1024, 640, 1024),
+                                   (2048, 1536, 768)])
+def test_wgrad_per_token_activations(mx, orc, T, O, H):
+    """dW = dY^T DQ(X): X quantized per token (1x16 along H, one FP32 scale per token), tokens along K."""
+    x = synthetic.random_bf16(T + O + H, (T, H), "student_t")
+    qx, sx, sx2 = orc.nvfp4_quantize_per_token(x)
+    dy = synthetic.random_bf16(T * 3 + O, (T, O), "normal", 1e-3)
+    got, ref, absprod = run_wgrad(mx, orc, dy, qx, sx, sx2, True)
+    check(orc, got, ref, absprod)
+
+
+def test_wgrad_per_tensor_scale(mx, orc):
+    T, O, H = 512, 256, 512
+    x = synthetic.random_bf16(41, (T, H), "normal")
+    qx, sx, S = orc.nvfp4_quantize_1x16(x, colwise=False)
+    dy = synthetic.random_bf16(42, (T, O), "normal", 1e-2)
+    got, ref, absprod = run_wgrad(mx, orc, dy, qx, sx, S, False)
+    check(orc, got, ref, absprod)
