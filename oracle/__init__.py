@@ -507,6 +507,23 @@ def gemm_ref_bf16_dq_nvfp4(a: np.ndarray, qb, sb, sb2, per_row: bool, alpha_a=No
     return ref
 
 
+def fp8_blockwise_decode_f64(q: np.ndarray, s: np.ndarray, block_rows: int, block_cols: int) -> np.ndarray:
+    """Exact values of blockwise FP8 codes: E4M3 value of each code times its block's FP32 scale, with one
+    scale per block_rows x block_cols block (1 x 128 for activations and gradients, 128 x 128 for weights;
+    s holds ceil(R / block_rows) x ceil(C / block_cols) scales)."""
+    q = np.asarray(q, dtype=np.uint8)
+    R, C = q.shape
+    mag = e4m3_table()[q & 0x7F].astype(np.float64) * np.where(q & 0x80, -1.0, 1.0)
+    sx = np.repeat(np.repeat(np.asarray(s, dtype=np.float64), block_rows, 0), block_cols, 1)[:R, :C]
+    return mag * sx
+
+
+def gemm_ref_fp8_blockwise(qa, sa, qb, sb) -> np.ndarray:
+    """The blockwise FP8 GEMM (NeMo RL FP8 page, DeepSeek-V3 recipe: [1, 128] activation tiles, [128, 128]
+    weight blocks, FP32 scales): ref = DQ(A) @ DQ(B)^T in FP64, DQ the exact decoded values."""
+    return fp8_blockwise_decode_f64(qa, sa, 1, 128) @ fp8_blockwise_decode_f64(qb, sb, 128, 128).T
+
+
 def rel_fro_error(d: np.ndarray, ref: np.ndarray) -> float:
     """||D - ref||_F / ||ref||_F."""
     d = np.asarray(d, dtype=np.float64)

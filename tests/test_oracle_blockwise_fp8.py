@@ -200,3 +200,27 @@ def test_pow2_scales_feed_the_mxfp8_layout(orc):
     assert np.array_equal(orc.decode_mxfp8_f64(q_col, col_mx), wd.T)
     assert np.array_equal(wd, E4M3[q_row & 0x7F] * np.where(q_row & 0x80, -1.0, 1.0)
                           * np.repeat(np.repeat(ws.astype(np.float64), 128, 0), 128, 1))
+
+
+def test_blockwise_gemm_reference(orc):
+    """The FP32-scale blockwise GEMM reference: the exact product of the decoded operands.  Pinned by a
+    triple loop over hand-decoded values (code value from the field table times its tile's scale) and by the
+    block-scaled MXFP8 reference on the same codes when every scale is a power of two."""
+    rng = np.random.default_rng(3)
+    M, N, K = 5, 130, 256
+    qa = rng.integers(0, 0x7F, size=(M, K), dtype=np.uint8) | (rng.integers(0, 2, size=(M, K), dtype=np.uint8) << 7)
+    qb = rng.integers(0, 0x7F, size=(N, K), dtype=np.uint8)
+    sa = rng.random((M, K // 128)).astype(np.float32) + np.float32(0.5)
+    sb = rng.random(((N + 127) // 128, K // 128)).astype(np.float32)
+    ref = orc.gemm_ref_fp8_blockwise(qa, sa, qb, sb)
+    val = lambda c: (-1.0 if c & 0x80 else 1.0) * E4M3[c & 0x7F]
+    for (m, n) in [(0, 0), (4, 129), (2, 77)]:
+        want = sum(val(qa[m, k]) * float(sa[m, k // 128]) * val(qb[n, k]) * float(sb[n // 128, k // 128])
+                   for k in range(K))
+        assert ref[m, n] == pytest.approx(want, rel=1e-12, abs=1e-300)
+    e_a = rng.integers(120, 135, size=(M, K // 128))
+    e_b = rng.integers(120, 135, size=((N + 127) // 128, K // 128))
+    p2 = orc.gemm_ref_fp8_blockwise(qa, 2.0 ** (e_a - 127.0), qb, 2.0 ** (e_b - 127.0))
+    mx_a = orc.fp8_blockwise_e8m0_rowwise(e_a.astype(np.uint8))
+    mx_b = np.repeat(np.repeat(e_b.astype(np.uint8), 128, 0)[:N], 4, 1)
+    assert np.array_equal(p2, orc.gemm_ref_mxfp8(qa, mx_a, qb, mx_b))
