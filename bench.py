@@ -416,7 +416,7 @@ class DenseBlockwise:
     scales (the learner's form on Blackwell): [1, 128] row + column tiles of X and dY from one read each,
     [128, 128] blocks of W in both orientations, E8M0 scale bytes written straight into the MXFP8 GEMM
     layout, then FPROP, DGRAD and WGRAD on the MXFP8 tensor-core GEMM.  Aux: the FP32-scale quantizers
-    (the sampler's form) of X and W."""
+    (the sampler's form) of X and W and the FP32-scale FPROP (per-K-block scaling around the tensor cores)."""
     name = "dense_fp8_blockwise"
     dtype = "e4m3 (f32 accumulate, bf16 out)"
 
@@ -478,6 +478,9 @@ class DenseBlockwise:
             ("quant", "blockwise 128x128 FP32-scale W", 1, F * H * 4,
              lambda: mx.mx_fp8_blockwise_quantize_128x128(self.w[None], False, self.fw["q_row"], self.fw["q_col"],
                                                           self.fw["s"])),
+            ("gemm8", "FPROP FP32-scale blockwise (scaling around the tensor cores)", 0, 2.0 * T * F * H,
+             lambda: mx.mx_fp8_blockwise_gemm(self.fx["q_row"], self.fx["s_row"], self.fw["q_row"][0], self.fw["s"][0],
+                                              T, F, H, self.y)),
         ]
 
     def config(self):

@@ -300,6 +300,21 @@ mx_status mx_wgrad_bf16_dq_nvfp4(const void* dy, const uint8_t* qx, const uint8_
                                  mx_scope sx2_scope, int64_t T, int64_t O, int64_t H, void* dw, int64_t ldd,
                                  cudaStream_t stream);
 
+/* Blockwise FP8 GEMM with FP32 scales (the DeepSeek-V3 form):
+ *   D[m, n] = BF16( sum_kb sa[m, kb] * sb[n / 128, kb] * sum_{k in kb} A[m, k] * B[n, k] ),  kb = k / 128
+ * Source: NeMo RL FP8 page, "FP8 nas camadas lineares" -- [1, 128] activation / gradient tiles and [128, 128]
+ * weight blocks, each with an FP32 scale (the DeepSeek-V3 recipe); E2E page Table 1 -- with FP32 scales (as
+ * opposed to power-of-two ones) the scaling runs around the tensor cores on SM100.  Each 128-deep K block
+ * is multiplied on the tensor cores (E4M3, FP32 accumulation) and promoted into FP32 accumulators with its
+ * scale product.  Forward: A = X row-wise codes with their [R, K/128] scales, B = W's row-wise codes of the
+ * [128, 128] quantizer with its block scales s; data gradient: A = dY row-wise, B = W's column-wise codes with
+ * the transposed block-scale matrix (sᵀ).
+ *   a  [M, K] E4M3, sa [M, K/128] FP32;  b [N, K] E4M3, sb [ceil(N/128), K/128] FP32;  d [M, ldd] BF16
+ * Requires K % 128 == 0, N % 8 == 0, ldd % 8 == 0, ldd >= N; a, b, d 16-byte aligned, sa and sb 4-byte
+ * aligned.  Persistent clusters of two CTAs on 256 x 256 tiles. */
+mx_status mx_fp8_blockwise_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb, int64_t M,
+                                int64_t N, int64_t K, void* d, int64_t ldd, cudaStream_t stream);
+
 /* Grouped block-scaled GEMM over expert-sorted rows: for every group g,
  *   D[rows of g] = BF16( alpha_a[row] * alpha_b[g] * A[rows of g] . B_g^T ).
  * Source: Miles page -- NVFP4 on the routed experts' weights and activations with a per-token

@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
                 "mx_count_mismatch": (I32, [P, P, I64, P, P]),
                 "mx_gemm_bf16_dq_nvfp4": (I32, [P, P, I32, P, P, P, I32, I64, I64, I64, P, I64, P]),
                 "mx_wgrad_bf16_dq_nvfp4": (I32, [P, P, P, P, I32, I64, I64, I64, P, I64, P]),
+                "mx_fp8_blockwise_gemm": (I32, [P, P, P, P, I64, I64, I64, P, I64, P]),
                 "mx_check_device_status": (I32, []),
             }
             for name, (res, args) in sigs.items():
@@ -260,6 +261,13 @@ def mx_wgrad_bf16_dq_nvfp4(dy, qx, sx, sx2, sx2_scope, dw, stream=None):
         raise ValueError("dY must be a contiguous [T, O] BF16 tensor")
     _check("mx_wgrad_bf16_dq_nvfp4", lib().mx_wgrad_bf16_dq_nvfp4(
         _p(dy), _p(qx), _p(sx), _p(sx2), int(sx2_scope), T, O, H, _p(dw), dw.stride(0), _stream(stream)))
+
+
+def mx_fp8_blockwise_gemm(a, sa, b, sb, M: int, N: int, K: int, d, stream=None):
+    """D = BF16(sum over 128-deep K blocks of sa[m, kb] * sb[n / 128, kb] * A_kb B_kb^T): E4M3 a [M, K] with
+    FP32 [1, 128]-tile scales sa [M, K/128], E4M3 b [N, K] with FP32 [128, 128]-block scales sb."""
+    _check("mx_fp8_blockwise_gemm", lib().mx_fp8_blockwise_gemm(
+        _p(a), _p(sa), _p(b), _p(sb), M, N, K, _p(d), d.stride(0), _stream(stream)))
 
 
 def mx_grouped_scaled_gemm(fmt: int, group_offsets, a, sa, alpha_a_rows, b, sb, alpha_b_groups, N: int, K: int, d,

@@ -536,6 +536,13 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (elect_one()) tc2_commit_mc(bar_tfull + 8 * ab, (uint16_t)3);
                 __syncwarp();
             }
+            // the odd CTA's last TMEM-release copies land on these barriers after the final MMAs: wait for
+            // them, so that neither CTA leaves while a copy into or out of its shared memory is in flight
+            for (int b = 0; b < C::ACC && ok; ++b) {
+                const int64_t uses = (ti - b + C::ACC - 1) / C::ACC;
+                if (uses > 0 && !warp_wait(bar_tempty + 8 * b, (uint32_t)((uses - 1) & 1), abort_flag, &g_mx_device_status))
+                    ok = false;
+            }
             if (issued_any) {
                 // the pair's MMAs read the peer's shared memory: all of them complete before either
                 // CTA leaves the final cluster barrier
@@ -1109,6 +1116,249 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 }
 
 // ---------------------------------------------------------------------------------------------
+// Blockwise FP8 GEMM with FP32 scales (NeMo RL FP8 page, "FP8 nas camadas lineares": the DeepSeek-V3
+// recipe, [1, 128] activation / gradient tiles and [128, 128] weight blocks with FP32 scales; E2E page
+// Table 1: on SM100 the tensor cores take power-of-two block scales natively, FP32 ones are applied
+// around them):
+//   D[m, n] = BF16( sum_kb sa[m, kb] * sb[n / 128, kb] * P_kb[m, n] ),   P_kb = sum_{k in kb} A[m, k] B[n, k]
+// Each 128-deep K block's P_kb comes from plain E4M3 pair MMAs (kind::f8f6f4, FP32 accumulation) into
+// one of two TMEM buffers (2 x 256 columns); the 8 epilogue warps promote it into FP32 register
+// accumulators with the block's scale product while the tensor core fills the other buffer, and write
+// the tile once all K blocks are in.  Warp 0 loads A and B by TMA (as the block-scaled kernel, without
+// scale atoms); warp 1 of the even CTA issues the MMAs; warp 1 of the odd CTA forwards its epilogue's
+// "buffer read" to the even CTA as a 16-byte bulk copy.
+// ---------------------------------------------------------------------------------------------
+struct BwParams {
+    const float* sa; const float* sb;       // sa [M, K/128]; sb [ceil(N/128), K/128]
+    int64_t M, N, K, kb_n, nb_n;
+    uint16_t* d; int64_t ldd;
+    int64_t m_tiles, n_tiles, total_tiles;
+};
+
+struct BwCfg {
+    static constexpr int NST = 6;
+    static constexpr int A_BYTES = 128 * BKB;              // 128 rows x 128 E4M3
+    static constexpr int B_BYTES = 128 * BKB;              // this CTA's 128 of the 256 B rows
+    static constexpr uint32_t STAGE_TX = 2u * (A_BYTES + B_BYTES);
+    static constexpr int SMEM_A = 0;
+    static constexpr int SMEM_B = SMEM_A + NST * A_BYTES;
+    static constexpr int SMEM_EPI = SMEM_B + NST * B_BYTES;
+    static constexpr int SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
+    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 7);
+    static constexpr int SMEM_SIGNAL = (SMEM_MISC + 16 + 15) / 16 * 16;
+    static constexpr int SMEM_ALLOC = SMEM_SIGNAL + 16 + 1024;
+    static_assert(SMEM_B % 1024 == 0 && SMEM_EPI % 1024 == 0, "alignment");
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+// kind::f8f6f4 without block scaling: D FP32 (bits 4-5 = 1), A and B E4M3 (format 0), K-major.
+template <int MMA_M, int MMA_N>
+__device__ __forceinline__ uint32_t make_idesc_e4m3() {
+    return (1u << 4) | ((uint32_t)(MMA_N >> 3) << 17) | ((uint32_t)(MMA_M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc2_mma_e4m3(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmD, const BwParams p) {
+    using C = BwCfg;
+    constexpr int NST = C::NST;
+    constexpr int TN = 256;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + C::SMEM_BAR;            // NST (even CTA): both CTAs' A and B bytes
+    const uint32_t bar_empty = bar_full + 8 * NST;            // NST (each CTA)
+    const uint32_t bar_pfull = bar_empty + 8 * NST;           // 2 (each CTA): a K block's partial product is in TMEM
+    const uint32_t bar_pempty = bar_pfull + 16;               // 2 (even CTA): both epilogues have read it
+    const uint32_t bar_pempty_odd = bar_pempty + 16;          // 2 (odd CTA): its epilogue has read it
+    const uint32_t bar_done = bar_pempty_odd + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_pfull + 8 * b, 1);
+            mbar_init(bar_pempty + 8 * b, EPI_WARPS);             // one arrival also expects the odd CTA's copy
+            mbar_init(bar_pempty_odd + 8 * b, EPI_WARPS);
+        }
+        mbar_init(bar_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmB) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(&tmD) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int64_t total_tiles = p.total_tiles;
+    const int64_t pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    Params tp{};
+    tp.M = p.M; tp.N = p.N; tp.m_tiles = p.m_tiles; tp.n_tiles = p.n_tiles; tp.d = p.d; tp.ldd = p.ldd;
+
+    if (warp == 0) {
+        // ------------------------------- producer (both CTAs) -------------------------------
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
+            const PairTile tile = pair_dense_tile<TN>(tp, t, rank);
+            const int64_t brow = tile.n0 + 128 * (int64_t)rank;
+            for (int64_t kb = 0; kb < p.kb_n; ++kb) {
+                if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                if (elect_one()) {
+                    const uint32_t fb = map_to_cta(bar_full + 8 * stage, 0);
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::STAGE_TX);
+                    tma_load_2d_pair(sbase + C::SMEM_A + stage * C::A_BYTES, &tmA, (int32_t)(kb * BKB), (int32_t)tile.row0, fb);
+                    tma_load_2d_pair(sbase + C::SMEM_B + stage * C::B_BYTES, &tmB, (int32_t)(kb * BKB), (int32_t)brow, fb);
+                }
+                __syncwarp();
+                if (++stage == NST) { stage = 0; phase ^= 1; }
+            }
+        }
+        if (!ok && lane == 0) *abort_flag = 1;
+    } else if (warp == 1) {
+        if (leader) {
+            // ------------------------------- MMA (even CTA) -------------------------------
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true, issued_any = false;
+            int64_t g = 0;                                   // K blocks issued so far: buffer g % 2
+            for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
+                for (int64_t kb = 0; kb < p.kb_n; ++kb, ++g) {
+                    const uint32_t pb = (uint32_t)(g & 1), use = (uint32_t)(g >> 1);
+                    if (!warp_wait(bar_pempty + 8 * pb, (use & 1u) ^ 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                    if (!warp_wait(bar_full + 8 * stage, phase, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                    tc_fence_after();
+                    if (elect_one()) {
+                        const uint32_t sA = sbase + C::SMEM_A + stage * C::A_BYTES;
+                        const uint32_t sB = sbase + C::SMEM_B + stage * C::B_BYTES;
+#pragma unroll
+                        for (int j = 0; j < BKB / 32; ++j)
+                            tc2_mma_e4m3(tmem + pb * TN, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j),
+                                         make_idesc_e4m3<2 * BM, TN>(), j > 0 ? 1u : 0u);
+                        tc2_commit_mc(bar_empty + 8 * stage, (uint16_t)3);
+                        tc2_commit_mc(bar_pfull + 8 * pb, (uint16_t)3);
+                    }
+                    __syncwarp();
+                    issued_any = true;
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
+                }
+            }
+            // the last buffer releases (the odd CTA's arrive as copies) complete before either CTA leaves
+            for (int b = 0; b < 2 && ok; ++b) {
+                const int64_t uses = (g - b + 1) / 2;
+                if (uses > 0 && !warp_wait(bar_pempty + 8 * b, (uint32_t)((uses - 1) & 1), abort_flag, &g_mx_device_status))
+                    ok = false;
+            }
+            if (issued_any) {
+                if (elect_one()) {
+                    tc2_commit_mc(bar_done, (uint16_t)1);
+                    const unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(bar_done, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
+                }
+                __syncwarp();
+            }
+        } else {
+            // odd CTA: forward each "partial buffer read" of this CTA's epilogue to the even CTA
+            const uint32_t pempty_leader = map_to_cta(bar_pempty, 0);
+            const uint32_t sig_dst = map_to_cta(sbase + C::SMEM_SIGNAL, 0);
+            bool ok = true;
+            int64_t g = 0;
+            for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
+                for (int64_t kb = 0; kb < p.kb_n; ++kb, ++g) {
+                    const uint32_t pb = (uint32_t)(g & 1), use = (uint32_t)(g >> 1);
+                    if (!warp_wait(bar_pempty_odd + 8 * pb, use & 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                    if (lane == 0) bulk_signal_copy(sig_dst, sbase + C::SMEM_SIGNAL, 16, pempty_leader + 8 * pb);
+                    __syncwarp();
+                }
+            }
+            if (!ok && lane == 0) *abort_flag = 1;
+        }
+    } else {
+        // ------------------------------- promotion + epilogue (both CTAs) -------------------------------
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        const uint32_t ebase = sbase + C::SMEM_EPI + (uint32_t)((warp - 2) * 2 * EPI_BUF_BYTES);
+        const uint32_t my_pempty = leader ? bar_pempty : bar_pempty_odd;
+        uint32_t epi_chunk = 0;
+        int64_t g = 0;
+        bool ok = true;
+        for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
+            const PairTile tile = pair_dense_tile<TN>(tp, t, rank);
+            const int64_t row = tile.row0 + q * 32 + lane;
+            const int64_t nblk = (tile.n0 + h * (TN / 2)) / 128;
+            const float* sa_row = p.sa + (row < p.M ? row : 0) * p.kb_n;
+            const float* sb_blk = p.sb + (nblk < p.nb_n ? nblk : 0) * p.kb_n;
+            const bool valid = row < p.M && nblk < p.nb_n;
+            float acc[TN / 2];
+#pragma unroll
+            for (int i = 0; i < TN / 2; ++i) acc[i] = 0.0f;
+            for (int64_t kb = 0; kb < p.kb_n; ++kb, ++g) {
+                const uint32_t pb = (uint32_t)(g & 1), use = (uint32_t)(g >> 1);
+                const float scale = valid ? __fmul_rn(__ldg(sa_row + kb), __ldg(sb_blk + kb)) : 0.0f;
+                if (!mbar_wait(bar_pfull + 8 * pb, use & 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < TN / 2 / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(tmem + pb * TN + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * (TN / 2) + c * 32), v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[c * 32 + i] = __fmaf_rn(v[i], scale, acc[c * 32 + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader && warp == 2) mbar_arrive_expect_tx(my_pempty + 8 * pb, 16);
+                    else mbar_arrive(my_pempty + 8 * pb);
+                }
+            }
+            if (!ok) break;
+            uint32_t packed[TN / 4];
+#pragma unroll
+            for (int i = 0; i < TN / 4; ++i) packed[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+            epilogue_store<TN, false>(tp, &tmD, q, h, lane, tile.row0, tile.row_end, tile.n0, ebase, epi_chunk, packed);
+        }
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        const unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {}
+    }
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------------
 bool make_map(CUtensorMap* map, const uint8_t* base, int64_t k_bytes, int64_t rows, uint32_t box_rows) {
@@ -1251,6 +1501,46 @@ cudaError_t launch_dq_impl(const DqGemmArgs& a, int num_sms, cudaStream_t stream
 }
 
 
+cudaError_t launch_bw_impl(const BwGemmArgs& a, int num_sms, cudaStream_t stream) {
+    using C = BwCfg;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    static int resident_pairs = 0;
+    std::call_once(attr_once, [num_sms] {
+        attr_err = cudaFuncSetAttribute(fp8bw_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        if (attr_err != cudaSuccess) return;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(num_sms & ~1));
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2; attr[0].val.clusterDim.y = 1; attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr; cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, fp8bw_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = num_sms / 2;
+        }
+        resident_pairs = n;
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    CUtensorMap tmA, tmB, tmD;
+    if (!make_map(&tmA, a.a, a.K, a.M, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&tmB, a.b, a.K, a.N, 128)) return cudaErrorInvalidValue;
+    if (!make_out_map(&tmD, a.d, a.M, a.N, a.ldd, (uint32_t)EPI_COLS)) return cudaErrorInvalidValue;
+    BwParams p{};
+    p.sa = a.sa; p.sb = a.sb;
+    p.M = a.M; p.N = a.N; p.K = a.K; p.kb_n = a.K / 128; p.nb_n = (a.N + 127) / 128;
+    p.d = a.d; p.ldd = a.ldd;
+    p.m_tiles = (a.M + 2 * BM - 1) / (2 * BM);
+    p.n_tiles = (a.N + 255) / 256;
+    p.total_tiles = p.m_tiles * p.n_tiles;
+    const int64_t pairs = max64(1, min64(p.total_tiles, (int64_t)min(resident_pairs, num_sms / 2)));
+    fp8bw_gemm_pair_kernel<<<(unsigned)(2 * pairs), NUM_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmB, tmD, p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 
@@ -1299,6 +1589,10 @@ cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t s
 
 cudaError_t launch_dq_gemm(const DqGemmArgs& args, int num_sms, cudaStream_t stream) {
     return args.wgrad ? launch_dq_impl<true>(args, num_sms, stream) : launch_dq_impl<false>(args, num_sms, stream);
+}
+
+cudaError_t launch_fp8_blockwise_gemm(const BwGemmArgs& args, int num_sms, cudaStream_t stream) {
+    return launch_bw_impl(args, num_sms, stream);
 }
 
 uint32_t read_and_clear_device_status() {

@@ -69,6 +69,15 @@ struct DqGemmArgs {
     bool wgrad;
 };
 cudaError_t launch_dq_gemm(const DqGemmArgs& args, int num_sms, cudaStream_t stream);
+
+// Blockwise FP8 GEMM with FP32 scales: a [M, K] and b [N, K] E4M3 (K-major); sa [M, K/128] FP32 (one per
+// [1, 128] tile of a), sb [ceil(N/128), K/128] FP32 (one per [128, 128] block of b).
+struct BwGemmArgs {
+    const uint8_t* a; const float* sa; const uint8_t* b; const float* sb;
+    int64_t M, N, K;
+    uint16_t* d; int64_t ldd;
+};
+cudaError_t launch_fp8_blockwise_gemm(const BwGemmArgs& args, int num_sms, cudaStream_t stream);
 uint32_t read_and_clear_device_status();
 uint32_t read_and_clear_mxfp8_status();
 

@@ -29,7 +29,7 @@ def test_header_declares_the_boundary():
     for required in ["mx_quantize_mxfp8", "mx_nvfp4_quantize_per_token", "mx_nvfp4_quantize_weight_2d", "mx_rht16",
                      "mx_nvfp4_quantize_1x16", "mx_dequantize_bf16", "mx_scaled_gemm", "mx_grouped_scaled_gemm",
                      "mx_fp8_blockwise_quantize_1x128", "mx_fp8_blockwise_quantize_128x128", "mx_gemm_bf16_dq_nvfp4",
-                     "mx_wgrad_bf16_dq_nvfp4"]:
+                     "mx_wgrad_bf16_dq_nvfp4", "mx_fp8_blockwise_gemm"]:
         assert required in names
 
 
@@ -131,6 +131,15 @@ def test_dq_gemm_validation(lib):
     assert w(A16, A16, A16, A16, 2, 128, 100, 128, A16, 128, NUL) == 2             # O % 8 (dY row pitch)
     assert w(A16, A16, A16, A16, 3, 128, 128, 128, A16, 128, NUL) == 1             # scope
     assert w(A16, A16, A16, NUL, 2, 128, 128, 128, A16, 128, NUL) == 1             # no scales
+
+
+def test_fp8_blockwise_gemm_validation(lib):
+    f = lib.mx_fp8_blockwise_gemm
+    assert f(A16, A16, A16, A16, 128, 128, 96, A16, 128, NUL) == 3      # K % 128
+    assert f(A16, A16, A16, NUL, 128, 128, 128, A16, 128, NUL) == 1     # no B scales
+    assert f(A16, A16, A16, A16, 128, 100, 128, A16, 100, NUL) == 2     # N % 8
+    assert f(A8, A16, A16, A16, 128, 128, 128, A16, 128, NUL) == 2      # misaligned codes
+    assert f(A16, A16, A16, A16, 128, 128, 128, A16, 120, NUL) == 1     # ldd < N
 
 
 def test_mismatch_validation(lib):

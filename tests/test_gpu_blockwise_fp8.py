@@ -192,3 +192,49 @@ def test_linear_layer_gemms_pow2(mx, orc):
     # and against the unquantized product, loosely (E4M3 operands)
     xf, wf = orc.bf16_to_f32(x).astype(np.float64), orc.bf16_to_f32(w).astype(np.float64)
     assert orc.rel_fro_error(y, xf @ wf.T) <= 0.1
+
+
+# ------------------------------------------------------------------------------------------------
+# FP32-scale blockwise GEMM (scaling around the tensor cores)
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (512, 640, 1024), (200, 296, 384), (1, 8, 128),
+                                   (1024, 1280, 4096)])
+def test_fp32_scale_gemm(mx, orc, M, N, K):
+    """Operands from the oracle quantizers (X [1,128] row-wise, W [128,128]); FPROP D = X W^T."""
+    x = synthetic.random_bf16(M + N + K, (M, K), "student_t")
+    w = synthetic.random_bf16(M + 2 * N + K, (N, K), "normal", 0.02)
+    qx, sx, _ = orc.fp8_blockwise_1x128(x, False)
+    qw, _, sw, _ = orc.fp8_blockwise_128x128(w, False)
+    d = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mx.mx_fp8_blockwise_gemm(torch.from_numpy(qx).to(DEV), torch.from_numpy(sx).to(DEV),
+                             torch.from_numpy(qw).to(DEV), torch.from_numpy(np.ascontiguousarray(sw)).to(DEV),
+                             M, N, K, d)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    ref = orc.gemm_ref_fp8_blockwise(qx, sx, qw, sw)
+    got = d.float().cpu().numpy().astype(np.float64)
+    assert orc.rel_fro_error(got, ref) <= TOL
+    A = orc.fp8_blockwise_decode_f64(qx, sx, 1, 128)
+    B = orc.fp8_blockwise_decode_f64(qw, sw, 128, 128)
+    bound = 2.0 ** -7 * np.abs(ref) + 2.0 ** -15 * (np.abs(A) @ np.abs(B).T) + 1e-30
+    assert not (np.abs(got - ref) > bound).any()
+
+
+def test_fp32_scale_gemm_dgrad_with_gpu_quantizers(mx, orc):
+    """DGRAD dX = dY W with the GPU quantizers' outputs: dY [1,128] row-wise, W's column-wise codes with the
+    transposed block scales."""
+    T, O, H = 512, 768, 384
+    w = synthetic.random_bf16(51, (O, H), "normal", 0.02)
+    dy = synthetic.random_bf16(52, (T, O), "normal", 1e-3)
+    q_row, q_col, s = u8((1, O, H)), u8((1, H, O)), f32((1, O // 128, H // 128))
+    mx.mx_fp8_blockwise_quantize_128x128(bf16_dev(w[None]), False, q_row, q_col, s)
+    qg, sg = u8((T, O)), f32((T, O // 128))
+    mx.mx_fp8_blockwise_quantize_1x128(bf16_dev(dy), False, q_row=qg, s_row=sg)
+    d = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mx.mx_fp8_blockwise_gemm(qg, sg, q_col[0], s[0].t().contiguous(), T, H, O, d)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    rq, rs, _ = orc.fp8_blockwise_1x128(dy, False)
+    _, wc, ws, _ = orc.fp8_blockwise_128x128(w, False)
+    ref = orc.gemm_ref_fp8_blockwise(rq, rs, wc, np.ascontiguousarray(ws.T))
+    assert orc.rel_fro_error(d.float().cpu().numpy().astype(np.float64), ref) <= TOL
