@@ -1135,16 +1135,18 @@ struct BwParams {
     int64_t m_tiles, n_tiles, total_tiles;
 };
 
+template <int TN>
 struct BwCfg {
-    static constexpr int NST = 6;
+    static constexpr int NP = TMEM_COLS / TN;              // partial-product buffers in TMEM
+    static constexpr int NST = TN == 256 ? 6 : 8;
     static constexpr int A_BYTES = 128 * BKB;              // 128 rows x 128 E4M3
-    static constexpr int B_BYTES = 128 * BKB;              // this CTA's 128 of the 256 B rows
+    static constexpr int B_BYTES = (TN / 2) * BKB;         // this CTA's half of the TN B rows
     static constexpr uint32_t STAGE_TX = 2u * (A_BYTES + B_BYTES);
     static constexpr int SMEM_A = 0;
     static constexpr int SMEM_B = SMEM_A + NST * A_BYTES;
     static constexpr int SMEM_EPI = SMEM_B + NST * B_BYTES;
     static constexpr int SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
-    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 7);
+    static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 3 * NP + 1);
     static constexpr int SMEM_SIGNAL = (SMEM_MISC + 16 + 15) / 16 * 16;
     static constexpr int SMEM_ALLOC = SMEM_SIGNAL + 16 + 1024;
     static_assert(SMEM_B % 1024 == 0 && SMEM_EPI % 1024 == 0, "alignment");
@@ -1163,21 +1165,22 @@ __device__ __forceinline__ void tc2_mma_e4m3(uint32_t d, uint64_t adesc, uint64_
                  :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
 }
 
+template <int TN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmD, const BwParams p) {
-    using C = BwCfg;
+    using C = BwCfg<TN>;
     constexpr int NST = C::NST;
-    constexpr int TN = 256;
+    constexpr int NP = C::NP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase + C::SMEM_BAR;            // NST (even CTA): both CTAs' A and B bytes
     const uint32_t bar_empty = bar_full + 8 * NST;            // NST (each CTA)
-    const uint32_t bar_pfull = bar_empty + 8 * NST;           // 2 (each CTA): a K block's partial product is in TMEM
-    const uint32_t bar_pempty = bar_pfull + 16;               // 2 (even CTA): both epilogues have read it
-    const uint32_t bar_pempty_odd = bar_pempty + 16;          // 2 (odd CTA): its epilogue has read it
-    const uint32_t bar_done = bar_pempty_odd + 16;
+    const uint32_t bar_pfull = bar_empty + 8 * NST;           // NP (each CTA): a K block's partial product is in TMEM
+    const uint32_t bar_pempty = bar_pfull + 8 * NP;           // NP (even CTA): both epilogues have read it
+    const uint32_t bar_pempty_odd = bar_pempty + 8 * NP;      // NP (odd CTA): its epilogue has read it
+    const uint32_t bar_done = bar_pempty_odd + 8 * NP;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
 
@@ -1190,7 +1193,7 @@ fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NP; ++b) {
             mbar_init(bar_pfull + 8 * b, 1);
             mbar_init(bar_pempty + 8 * b, EPI_WARPS);             // one arrival also expects the odd CTA's copy
             mbar_init(bar_pempty_odd + 8 * b, EPI_WARPS);
@@ -1225,7 +1228,7 @@ fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         bool ok = true;
         for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
             const PairTile tile = pair_dense_tile<TN>(tp, t, rank);
-            const int64_t brow = tile.n0 + 128 * (int64_t)rank;
+            const int64_t brow = tile.n0 + (TN / 2) * (int64_t)rank;
             for (int64_t kb = 0; kb < p.kb_n; ++kb) {
                 if (!warp_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, &g_mx_device_status)) { ok = false; break; }
                 if (elect_one()) {
@@ -1245,10 +1248,10 @@ fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true, issued_any = false;
-            int64_t g = 0;                                   // K blocks issued so far: buffer g % 2
+            int64_t g = 0;                                   // K blocks issued so far: buffer g % NP
             for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
                 for (int64_t kb = 0; kb < p.kb_n; ++kb, ++g) {
-                    const uint32_t pb = (uint32_t)(g & 1), use = (uint32_t)(g >> 1);
+                    const uint32_t pb = (uint32_t)(g % NP), use = (uint32_t)(g / NP);
                     if (!warp_wait(bar_pempty + 8 * pb, (use & 1u) ^ 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
                     if (!warp_wait(bar_full + 8 * stage, phase, abort_flag, &g_mx_device_status)) { ok = false; break; }
                     tc_fence_after();
@@ -1268,8 +1271,8 @@ fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 }
             }
             // the last buffer releases (the odd CTA's arrive as copies) complete before either CTA leaves
-            for (int b = 0; b < 2 && ok; ++b) {
-                const int64_t uses = (g - b + 1) / 2;
+            for (int b = 0; b < NP && ok; ++b) {
+                const int64_t uses = (g - b + NP - 1) / NP;
                 if (uses > 0 && !warp_wait(bar_pempty + 8 * b, (uint32_t)((uses - 1) & 1), abort_flag, &g_mx_device_status))
                     ok = false;
             }
@@ -1289,7 +1292,7 @@ fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             int64_t g = 0;
             for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
                 for (int64_t kb = 0; kb < p.kb_n; ++kb, ++g) {
-                    const uint32_t pb = (uint32_t)(g & 1), use = (uint32_t)(g >> 1);
+                    const uint32_t pb = (uint32_t)(g % NP), use = (uint32_t)(g / NP);
                     if (!warp_wait(bar_pempty_odd + 8 * pb, use & 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
                     if (lane == 0) bulk_signal_copy(sig_dst, sbase + C::SMEM_SIGNAL, 16, pempty_leader + 8 * pb);
                     __syncwarp();
@@ -1317,7 +1320,7 @@ fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
 #pragma unroll
             for (int i = 0; i < TN / 2; ++i) acc[i] = 0.0f;
             for (int64_t kb = 0; kb < p.kb_n; ++kb, ++g) {
-                const uint32_t pb = (uint32_t)(g & 1), use = (uint32_t)(g >> 1);
+                const uint32_t pb = (uint32_t)(g % NP), use = (uint32_t)(g / NP);
                 const float scale = valid ? __fmul_rn(__ldg(sa_row + kb), __ldg(sb_blk + kb)) : 0.0f;
                 if (!mbar_wait(bar_pfull + 8 * pb, use & 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
                 tc_fence_after();
@@ -1501,13 +1504,14 @@ cudaError_t launch_dq_impl(const DqGemmArgs& a, int num_sms, cudaStream_t stream
 }
 
 
+template <int TN>
 cudaError_t launch_bw_impl(const BwGemmArgs& a, int num_sms, cudaStream_t stream) {
-    using C = BwCfg;
+    using C = BwCfg<TN>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     static int resident_pairs = 0;
     std::call_once(attr_once, [num_sms] {
-        attr_err = cudaFuncSetAttribute(fp8bw_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        attr_err = cudaFuncSetAttribute(fp8bw_gemm_pair_kernel<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
         if (attr_err != cudaSuccess) return;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(num_sms & ~1));
@@ -1518,7 +1522,7 @@ cudaError_t launch_bw_impl(const BwGemmArgs& a, int num_sms, cudaStream_t stream
         attr[0].val.clusterDim.x = 2; attr[0].val.clusterDim.y = 1; attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr; cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, fp8bw_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&n, fp8bw_gemm_pair_kernel<TN>, &cfg) != cudaSuccess || n <= 0) {
             cudaGetLastError();
             n = num_sms / 2;
         }
@@ -1527,17 +1531,17 @@ cudaError_t launch_bw_impl(const BwGemmArgs& a, int num_sms, cudaStream_t stream
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap tmA, tmB, tmD;
     if (!make_map(&tmA, a.a, a.K, a.M, 128)) return cudaErrorInvalidValue;
-    if (!make_map(&tmB, a.b, a.K, a.N, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&tmB, a.b, a.K, a.N, TN / 2)) return cudaErrorInvalidValue;
     if (!make_out_map(&tmD, a.d, a.M, a.N, a.ldd, (uint32_t)EPI_COLS)) return cudaErrorInvalidValue;
     BwParams p{};
     p.sa = a.sa; p.sb = a.sb;
     p.M = a.M; p.N = a.N; p.K = a.K; p.kb_n = a.K / 128; p.nb_n = (a.N + 127) / 128;
     p.d = a.d; p.ldd = a.ldd;
     p.m_tiles = (a.M + 2 * BM - 1) / (2 * BM);
-    p.n_tiles = (a.N + 255) / 256;
+    p.n_tiles = (a.N + TN - 1) / TN;
     p.total_tiles = p.m_tiles * p.n_tiles;
     const int64_t pairs = max64(1, min64(p.total_tiles, (int64_t)min(resident_pairs, num_sms / 2)));
-    fp8bw_gemm_pair_kernel<<<(unsigned)(2 * pairs), NUM_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmB, tmD, p);
+    fp8bw_gemm_pair_kernel<TN><<<(unsigned)(2 * pairs), NUM_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmB, tmD, p);
     return cudaGetLastError();
 }
 
@@ -1592,7 +1596,7 @@ cudaError_t launch_dq_gemm(const DqGemmArgs& args, int num_sms, cudaStream_t str
 }
 
 cudaError_t launch_fp8_blockwise_gemm(const BwGemmArgs& args, int num_sms, cudaStream_t stream) {
-    return launch_bw_impl(args, num_sms, stream);
+    return launch_bw_impl<128>(args, num_sms, stream);
 }
 
 uint32_t read_and_clear_device_status() {
