@@ -83,26 +83,38 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// Stochastic rounding onto the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6} with 16 random bits.
+// Stochastic rounding onto the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6} with 16 random bits k.
 // a = |v|; a >= 6 -> 6; else lo/hi are the neighbouring grid points, f = (a - lo) / (hi - lo)
-// (exact), and the result rounds up iff f > bits * 2^-16.  Returns the 4-bit code (sign kept).
-// Evaluated on the FP32 bit fields (same decisions as the quotient form).
+// (exact), and the result rounds up iff f > k * 2^-16.  Returns the 4-bit code (sign kept).
+//
+// Evaluated on one FP32 bit pattern.  z = a * 2^-126 rounded up: for a >= 1 the product is exact and
+// normal, its exponent field is e + 1 for a in [2^e, 2^(e+1)) and its top mantissa bit picks 2^e or
+// 1.5 * 2^e, so bits(z) >> 22 = 2 + 2e + m is the code of lo, and the low 22 bits are f * 2^22.  For
+// a < 1 the product is subnormal, bits(z) = ceil(a * 2^23): bits >> 22 = floor(2a) is again the code of
+// lo (grid step 0.5) and the low 22 bits are ceil(f * 2^22).  Since 64k is an integer, ceil(f * 2^22)
+// > 64k iff f * 2^22 > 64k iff f > k * 2^-16, so adding 2^22 - 1 - 64k carries into bit 22 exactly
+// when the value rounds up (a ceiling that reaches 2^22 lands on hi, which is also the SR result, as f
+// > 1 - 2^-22 exceeds every k * 2^-16).  From a = 6 up the sum is at least 7 << 22, so clamping it to
+// (8 << 22) - 1 gives code 7 for every a >= 6 (and for infinities and NaN).
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t bits16) {
-    // For a in [1, 6) the two grid points of each binade [2^e, 2^(e+1)) are 2^e and 1.5 * 2^e: the top
-    // mantissa bit picks the lower one and f is the remaining 22 mantissa bits over 2^22, so f > bits16 *
-    // 2^-16 exactly when adding 2^22 - 1 - (bits16 << 6) to the FP32 bits carries into that top bit; the
-    // code 2 + 2e + m is then read off the sum (a carry out of the binade lands on the next grid point,
-    // and anything from 6 up clamps to 7).  In [0.5, 1) the grid points are 0.5 and 1 and f is the whole
-    // 23-bit mantissa over 2^23: the same carry test one bit up.  Below 0.5 (grid 0 and 0.5) f = 2a, and
-    // 2a > bits16 * 2^-16 is compared as a * 2^17 > bits16 in FP32 (both sides exact).
-    const uint32_t u = __float_as_uint(v) & 0x7FFFFFFFu;
-    const uint32_t c_norm = min(((u + (0x3FFFFFu - (bits16 << 6))) >> 22) - 252u, 7u);
-    const uint32_t c_half = ((u + (0x7FFFFFu - (bits16 << 7))) >> 23) - 125u;
-    const float fbits = __fsub_rn(__uint_as_float(0x4B000000u | bits16), 8388608.0f);   // bits16 as FP32, exactly
-    const uint32_t c_small = __fmul_rn(__uint_as_float(u), 131072.0f) > fbits ? 1u : 0u;
-    const uint32_t code = u >= 0x3F800000u ? c_norm : (u >= 0x3F000000u ? c_half : c_small);
-    return code | ((__float_as_uint(v) >> 28) & 8u);
+
+// 2^22 - 1 - 64k for the k held in the low (high = false) or high half of a random word; 64k is a
+// sub-mask of 2^22 - 1, so the difference is an XOR.
+__device__ __forceinline__ uint32_t sr_kterm(uint32_t word, bool high) {
+    return (high ? ((word >> 10) & 0x3FFFC0u) : ((word << 6) & 0x3FFFC0u)) ^ 0x3FFFFFu;
+}
+
+__device__ __forceinline__ uint32_t e2m1_sr_kterm(float v, uint32_t kterm) {
+    const uint32_t z = __float_as_uint(__fmul_ru(fabsf(v), __uint_as_float(0x00800000u)));   // a * 2^-126, rounded up
+    const uint32_t u = min(z + kterm, 0x01FFFFFFu);       // a >= 6: code 7
+    return (u >> 22) | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// acc + code * 2^(4 j) as one integer multiply-add (keeps the nibble packing off the logic pipe).
+__device__ __forceinline__ uint32_t pack_nibble(uint32_t acc, uint32_t code, int j) {
+    uint32_t r;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(code), "r"(1u << (4 * j)), "r"(acc));
+    return r;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -114,11 +126,10 @@ __device__ __forceinline__ U4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c
                                             uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int rnd = 0; rnd < 10; ++rnd) {
-        // one widening multiply gives both halves of each 64-bit product
-        const unsigned long long p0 = (unsigned long long)0xD2511F53u * c0;
-        const unsigned long long p1 = (unsigned long long)0xCD9E8D57u * c2;
-        const uint32_t lo0 = (uint32_t)p0, hi0 = (uint32_t)(p0 >> 32);
-        const uint32_t lo1 = (uint32_t)p1, hi1 = (uint32_t)(p1 >> 32);
+        // the low and high words of each 64-bit product as two 32-bit multiplies (faster here than one
+        // widening multiply)
+        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
         const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
         c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
         k0 += 0x9E3779B9u; k1 += 0xBB67AE85u;
@@ -159,7 +170,19 @@ __device__ __forceinline__ void rht16_inplace(float v[16], uint32_t signmask) {
 // ---------------------------------------------------------------------------------------------
 // NVFP4 block-scale arithmetic (FP32, round to nearest, in the documented order).
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ float nvfp4_second_scale(float amax) { return __fdiv_rn(amax, 2688.0f); }
+
+// RN(a / m) for a BF16 value a and a constant m, rm = RN(1 / m): the product a * rm followed by one
+// correction step with the exact residual a - q0 * m (Markstein) gives the correctly rounded quotient
+// for every finite BF16 a when m is 6, 4 or 2688 (checked exhaustively against the IEEE quotient).
+// Infinities and NaN take the IEEE division.
+__device__ __forceinline__ float div_bf16_by_const(float a, float m, float rm) {
+    if (!(a <= FLT_MAX)) return __fdiv_rn(a, m);
+    const float q0 = __fmul_rn(a, rm);
+    return __fmaf_rn(__fmaf_rn(-q0, m, a), rm, q0);
+}
+
+// S = fp32(amax / 2688) for a BF16 amax.
+__device__ __forceinline__ float nvfp4_second_scale(float amax) { return div_bf16_by_const(amax, 2688.0f, 1.0f / 2688.0f); }
 
 // bs = E4M3(fp32(fp32(amax_b / m) / S)) with m = 6 (the block maximum maps to the E2M1 maximum) or,
 // for the Four-over-Six alternative, m = 4.
@@ -167,7 +190,34 @@ __device__ __forceinline__ uint32_t nvfp4_block_scale_m(float amax_b, float S, f
     if (S == 0.0f) return 0u;
     return cvt_e4m3(__fdiv_rn(__fdiv_rn(amax_b, m), S));
 }
-__device__ __forceinline__ uint32_t nvfp4_block_scale(float amax_b, float S) { return nvfp4_block_scale_m(amax_b, S, 6.0f); }
+
+// RN(1 / S) for nvfp4_block_scale_fast, or 0 where the fast path does not apply (S zero, below 2^-125,
+// or not finite).
+__device__ __forceinline__ float nvfp4_fast_rs(float S) {
+    return (S >= 1.17549435e-38f * 2.0f && S <= FLT_MAX) ? __frcp_rn(S) : 0.0f;
+}
+
+// The same block scale for a BF16 amax_b with rS = nvfp4_fast_rs(S).  fp32(amax_b / m) by the constant
+// division above; the quotient by S from y * rS and one Markstein correction, which lands within one unit
+// in the last place of fp32(y / S), i.e. within two bit patterns of it (two below a power of two).  E4M3
+// rounding is monotone, so when the patterns two below and two above give the same code that is the code
+// of fp32(y / S); otherwise (near an E4M3 rounding boundary; 0.07 % of the blocks in a sweep over all BF16
+// block and tensor maxima) the IEEE divisions decide.
+__device__ __forceinline__ uint32_t nvfp4_block_scale_fast(float amax_b, float S, float rS, float m = 6.0f,
+                                                          float rm = 1.0f / 6.0f) {
+    if (rS != 0.0f && amax_b <= FLT_MAX) {
+        const float y = div_bf16_by_const(amax_b, m, rm);
+        const float q0 = __fmul_rn(y, rS);
+        const float q = __fmaf_rn(__fmaf_rn(-q0, S, y), rS, q0);
+        const uint32_t qb = __float_as_uint(q);
+        uint16_t c2;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c2)
+            : "f"(__uint_as_float(qb + 2u)), "f"(__uint_as_float(qb >= 2u ? qb - 2u : 0u)));
+        const uint32_t lo = c2 & 0xFFu, hi = (uint32_t)c2 >> 8;
+        if (lo == hi && lo != 0x7Fu) return lo;
+    }
+    return nvfp4_block_scale_m(amax_b, S, m);
+}
 
 __device__ __forceinline__ float nvfp4_block_recip(uint32_t bs, float S) {
     const float d = __fmul_rn(e4m3_to_f32(bs), S);

@@ -17,7 +17,7 @@ namespace mxk {
 namespace {
 
 // ------------------------------------------------------------------------------------------------
-// Row-wise 1x16 (per token or per tensor).  One warp per row (grid-stride over rows); lane l owns
+// Row-wise 1x16 with a per-token scale.  One warp per row (grid-stride over rows); lane l owns
 // the 16-element blocks l, l + 32, ..., so the block-scale arithmetic runs once per 16 elements.
 // Rows of up to 32 * RW_MAXB blocks stay in registers between the amax and the quantize pass;
 // longer rows are read twice (the second read hits L1/L2).
@@ -47,8 +47,7 @@ __device__ __forceinline__ uint2 quant_block16(const uint4& a, const uint4& b, f
             const uint32_t rw[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const uint32_t bits = (j & 1) ? (rw[j >> 1] >> 16) : (rw[j >> 1] & 0xFFFFu);
-                c[h] |= e2m1_sr(v[8 * h + j], bits) << (4 * j);
+                c[h] = pack_nibble(c[h], e2m1_sr_kterm(v[8 * h + j], sr_kterm(rw[j >> 1], j & 1)), j);
             }
         }
         return make_uint2(c[0], c[1]);
@@ -72,7 +71,8 @@ __device__ __forceinline__ float nvfp4_max_dq_error(const float* x, const uint32
 // Four-over-Six (NVIDIA RL blog, "Four-Over-Six (4/6)"): the block is quantized with its maximum mapped
 // to 6 and to 4, and the candidate with the smaller largest dequantization error is kept (a tie keeps
 // 6).  Returns the 8 code bytes and the chosen scale.
-__device__ __forceinline__ uint2 quant_block16_46(const uint4& a, const uint4& c, float amax_b, float S, uint32_t& bs_out) {
+__device__ __forceinline__ uint2 quant_block16_46(const uint4& a, const uint4& c, float amax_b, float S, float rS,
+                                                  uint32_t& bs_out) {
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
     float x[16];
 #pragma unroll
@@ -81,7 +81,7 @@ __device__ __forceinline__ uint2 quant_block16_46(const uint4& a, const uint4& c
     float err_best = 0.0f;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-        const uint32_t bs = nvfp4_block_scale_m(amax_b, S, k == 0 ? 6.0f : 4.0f);
+        const uint32_t bs = k == 0 ? nvfp4_block_scale_fast(amax_b, S, rS) : nvfp4_block_scale_fast(amax_b, S, rS, 4.0f, 0.25f);
         const float r = nvfp4_block_recip(bs, S);
         float v[16];
 #pragma unroll
@@ -94,11 +94,10 @@ __device__ __forceinline__ uint2 quant_block16_46(const uint4& a, const uint4& c
     return make_uint2(best[0], best[1]);
 }
 
-template <bool PER_TENSOR, bool SR, bool GROUPED, int LPR, bool FOUR_SIX = false>
+template <bool GROUPED, int LPR, bool FOUR_SIX = false>
 __global__ void __launch_bounds__(RW_WARPS * 32, RW_CTAS_PER_SM)
 nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64_t ldx,
                      uint8_t* __restrict__ q, uint8_t* __restrict__ s, float* __restrict__ s_tok,
-                     const uint32_t* __restrict__ tensor_amax, float* __restrict__ s_tensor, uint64_t sr_seed,
                      int G, const int64_t* __restrict__ group_offsets) {
     // LPR lanes per row (32 or 16): a warp works on 32 / LPR rows at once
     constexpr int RPW = 32 / LPR;
@@ -115,7 +114,6 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
     const int64_t nblk = H / 16;
     const int64_t nct = sf_col_tiles(H, 16);
     const bool cached = nblk <= LPR * RW_MAXB;
-    const uint32_t k0 = (uint32_t)sr_seed, k1 = (uint32_t)(sr_seed >> 32);
     for (int64_t tw = ((int64_t)blockIdx.x * RW_WARPS + (threadIdx.x >> 5)) * RPW; tw < T;
          tw += (int64_t)gridDim.x * RW_WARPS * RPW) {
         const int64_t t = tw + half;
@@ -124,10 +122,6 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
         uint4 ra[RW_MAXB], rb[RW_MAXB];
         uint32_t bam[RW_MAXB];                       // block amax bits of the cached blocks
         float S;
-        if (PER_TENSOR) {
-            S = nvfp4_second_scale(__uint_as_float(*tensor_amax));
-            if (t == 0 && sub == 0) *s_tensor = S;
-        }
         if (cached) {
             uint32_t m = 0;
 #pragma unroll
@@ -143,12 +137,10 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
                 bam[i] = fold_halves(m2);
                 m = max(m, bam[i]);
             }
-            if (!PER_TENSOR) {
-                const uint32_t amax16 = __reduce_max_sync(gmask, m);
-                S = nvfp4_second_scale(__uint_as_float(amax16 << 16));
-                if (row_ok && sub == 0) s_tok[t] = S;
-            }
-        } else if (!PER_TENSOR) {
+            const uint32_t amax16 = __reduce_max_sync(gmask, m);
+            S = nvfp4_second_scale(__uint_as_float(amax16 << 16));
+            if (row_ok && sub == 0) s_tok[t] = S;
+        } else {
             uint32_t m2 = 0;
             if (row_ok) {
                 for (int64_t b = sub; b < nblk; b += LPR) {
@@ -164,12 +156,13 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
             if (row_ok && sub == 0) s_tok[t] = S;
         }
         const int64_t srow = (GROUPED && row_ok) ? grouped_scale_row(s_off, s_ptile, G, t) : t;
+        const float rS = nvfp4_fast_rs(S);
 
         // codes, and the four consecutive block scales of lanes 4m .. 4m+3 of the row group as one word
         auto emit = [&](int64_t b, bool valid, const uint4& a, const uint4& c, uint32_t bs, float r, uint32_t amax_bits) {
             uint2 codes;
-            if (FOUR_SIX) codes = quant_block16_46(a, c, __uint_as_float(amax_bits << 16), S, bs);
-            else codes = quant_block16<SR>(a, c, r, (uint64_t)t * (uint64_t)H + (uint64_t)b * 16, k0, k1);
+            if (FOUR_SIX) codes = quant_block16_46(a, c, __uint_as_float(amax_bits << 16), S, rS, bs);
+            else codes = quant_block16<false>(a, c, r, 0, 0u, 0u);
             if (valid) __stcs(reinterpret_cast<uint2*>(q + t * (H / 2) + b * 8), codes);
             const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 1);
             const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
@@ -190,7 +183,7 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
             float rv[RW_MAXB];
 #pragma unroll
             for (int i = 0; i < RW_MAXB; ++i) {
-                bsv[i] = FOUR_SIX ? 0u : nvfp4_block_scale(__uint_as_float(bam[i] << 16), S);
+                bsv[i] = FOUR_SIX ? 0u : nvfp4_block_scale_fast(__uint_as_float(bam[i] << 16), S, rS);
                 rv[i] = FOUR_SIX ? 0.0f : nvfp4_block_recip(bsv[i], S);
             }
             const int64_t nrounds = (nblk + LPR - 1) / LPR;
@@ -212,25 +205,83 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
                 m2 = absmax_bf16x2(m2, a.x); m2 = absmax_bf16x2(m2, a.y); m2 = absmax_bf16x2(m2, a.z); m2 = absmax_bf16x2(m2, a.w);
                 m2 = absmax_bf16x2(m2, c.x); m2 = absmax_bf16x2(m2, c.y); m2 = absmax_bf16x2(m2, c.z); m2 = absmax_bf16x2(m2, c.w);
                 const uint32_t am = fold_halves(m2);
-                const uint32_t bs = FOUR_SIX ? 0u : nvfp4_block_scale(__uint_as_float(am << 16), S);
+                const uint32_t bs = FOUR_SIX ? 0u : nvfp4_block_scale_fast(__uint_as_float(am << 16), S, rS);
                 emit(b, valid, a, c, bs, FOUR_SIX ? 0.0f : nvfp4_block_recip(bs, S), am);
             }
         }
     }
 }
 
-template <bool PER_TENSOR, bool SR, bool GROUPED, bool FOUR_SIX = false>
+template <bool GROUPED, bool FOUR_SIX = false>
 void launch_rowwise(int64_t T, int64_t H, unsigned grid_cap, size_t smem, cudaStream_t stream, const uint16_t* x,
-                    int64_t ldx, uint8_t* q, uint8_t* s, float* s_tok, const uint32_t* amax, float* s_tensor,
-                    uint64_t sr_seed, int G, const int64_t* offs) {
+                    int64_t ldx, uint8_t* q, uint8_t* s, float* s_tok, int G, const int64_t* offs) {
     if (H / 16 <= 64) {
         const int64_t blocks = (T + RW_WARPS * 2 - 1) / (RW_WARPS * 2);
-        nvfp4_rowwise_kernel<PER_TENSOR, SR, GROUPED, 16, FOUR_SIX><<<(unsigned)min64(blocks, grid_cap), RW_WARPS * 32, smem, stream>>>(
-            x, T, H, ldx, q, s, s_tok, amax, s_tensor, sr_seed, G, offs);
+        nvfp4_rowwise_kernel<GROUPED, 16, FOUR_SIX><<<(unsigned)min64(blocks, grid_cap), RW_WARPS * 32, smem, stream>>>(
+            x, T, H, ldx, q, s, s_tok, G, offs);
     } else {
         const int64_t blocks = (T + RW_WARPS - 1) / RW_WARPS;
-        nvfp4_rowwise_kernel<PER_TENSOR, SR, GROUPED, 32, FOUR_SIX><<<(unsigned)min64(blocks, grid_cap), RW_WARPS * 32, smem, stream>>>(
-            x, T, H, ldx, q, s, s_tok, amax, s_tensor, sr_seed, G, offs);
+        nvfp4_rowwise_kernel<GROUPED, 32, FOUR_SIX><<<(unsigned)min64(blocks, grid_cap), RW_WARPS * 32, smem, stream>>>(
+            x, T, H, ldx, q, s, s_tok, G, offs);
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Row-wise 1x16 with a per-tensor scale.  With S fixed for the whole tensor the 16-element blocks are
+// independent, and a contiguous [T, N] tensor is a flat sequence of them: thread = one block per step
+// of a grid-stride loop, the next block's two 16-byte loads issued before the current block is
+// quantized.  The reciprocal r of each possible block scale (128 E4M3 codes) is computed once per CTA.
+// Block f covers elements 16f .. 16f + 15 (the stochastic-rounding index), row f / (N/16).
+// ------------------------------------------------------------------------------------------------
+constexpr int FL_THREADS = 256;
+constexpr int FL_CTAS_PER_SM = 4;
+
+template <bool SR>
+__global__ void __launch_bounds__(FL_THREADS, FL_CTAS_PER_SM)
+nvfp4_1x16_flat_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, const uint32_t* __restrict__ tensor_amax,
+                       float* __restrict__ s_tensor, uint64_t sr_seed, uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+    __shared__ float rtab[128];
+    const float S = nvfp4_second_scale(__uint_as_float(*tensor_amax));
+    const float rS = nvfp4_fast_rs(S);
+    if (threadIdx.x < 128) rtab[threadIdx.x] = nvfp4_block_recip(threadIdx.x, S);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *s_tensor = S;
+    __syncthreads();
+
+    const int64_t nb = N / 16, total = T * nb, nct = sf_col_tiles(N, 16);
+    const int64_t stride = (int64_t)gridDim.x * FL_THREADS;
+    const int64_t stride_t = stride / nb, stride_b = stride % nb;
+    const bool word_scales = (nb % 4) == 0;        // 4 consecutive blocks from lane 4m share a row
+    const uint32_t k0 = (uint32_t)sr_seed, k1 = (uint32_t)(sr_seed >> 32);
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    const int lane = threadIdx.x & 31;
+
+    int64_t f = (int64_t)blockIdx.x * FL_THREADS + threadIdx.x;
+    int64_t t = f / nb, b = f % nb;
+    uint4 a = make_uint4(0u, 0u, 0u, 0u), c = a;
+    if (f < total) { a = __ldcs(xv + 2 * f); c = __ldcs(xv + 2 * f + 1); }
+    // warp-uniform trip count (the scale words below use full-warp shuffles)
+    for (int64_t fw = f - lane; fw < total; fw += stride) {
+        const bool valid = f < total;
+        uint4 na = make_uint4(0u, 0u, 0u, 0u), nc = na;
+        if (f + stride < total) { na = __ldcs(xv + 2 * (f + stride)); nc = __ldcs(xv + 2 * (f + stride) + 1); }
+        uint32_t m2 = 0;
+        m2 = absmax_bf16x2(m2, a.x); m2 = absmax_bf16x2(m2, a.y); m2 = absmax_bf16x2(m2, a.z); m2 = absmax_bf16x2(m2, a.w);
+        m2 = absmax_bf16x2(m2, c.x); m2 = absmax_bf16x2(m2, c.y); m2 = absmax_bf16x2(m2, c.z); m2 = absmax_bf16x2(m2, c.w);
+        const uint32_t bs = nvfp4_block_scale_fast(__uint_as_float(fold_halves(m2) << 16), S, rS);
+        const uint2 codes = quant_block16<SR>(a, c, rtab[bs], (uint64_t)f * 16u, k0, k1);
+        if (valid) __stcs(reinterpret_cast<uint2*>(q) + f, codes);
+        if (word_scales) {
+            const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 1);
+            const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
+            const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 3);
+            if (valid && (lane & 3) == 0)
+                *reinterpret_cast<uint32_t*>(s + sf_offset(t, b, nct)) = bs | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        } else if (valid) {
+            s[sf_offset(t, b, nct)] = (uint8_t)bs;
+        }
+        a = na; c = nc;
+        f += stride; t += stride_t; b += stride_b;
+        if (b >= nb) { b -= nb; ++t; }
     }
 }
 
@@ -339,6 +390,7 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
     const bool valid = (t0 < T) && (n0 < N);
 
     const float S = nvfp4_second_scale(__uint_as_float(*tensor_amax));
+    const float rS = nvfp4_fast_rs(S);
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *s_tensor = S;
 
     uint32_t xw[16][CPT / 2];
@@ -362,7 +414,7 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
         uint32_t m = 0;
 #pragma unroll
         for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
-        const uint32_t bs = nvfp4_block_scale(__uint_as_float(m), S);
+        const uint32_t bs = nvfp4_block_scale_fast(__uint_as_float(m), S, rS);
         rcp[j] = nvfp4_block_recip(bs, S);
         ss[warp][lane * CPT + j] = (uint8_t)bs;
         if (!SR) {
@@ -389,8 +441,7 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
             for (int j = 0; j < CPT; ++j) {
                 const uint32_t w = xw[i][j >> 1];
                 const float v = (j & 1) ? bf16_hi(w) : bf16_lo(w);
-                const uint32_t bits = (j & 1) ? (rw[j >> 1] >> 16) : (rw[j >> 1] & 0xFFFFu);
-                code[j][i >> 3] |= e2m1_sr(__fmul_rn(v, rcp[j]), bits) << (4 * (i & 7));
+                code[j][i >> 3] = pack_nibble(code[j][i >> 3], e2m1_sr_kterm(__fmul_rn(v, rcp[j]), sr_kterm(rw[j >> 1], j & 1)), i & 7);
             }
         }
         if (valid) {
@@ -656,15 +707,13 @@ cudaError_t launch_nvfp4_per_token(const uint16_t* x, int64_t T, int64_t H, int6
     }
     const unsigned cap = (unsigned)num_sms * 16;
     if (G > 0 && four_six)
-        launch_rowwise<false, false, true, true>(T, H, cap, (size_t)12 * (G + 1) + 128, stream, x, ldx, q, s, s_tok, nullptr,
-                                                 nullptr, 0, G, group_offsets);
+        launch_rowwise<true, true>(T, H, cap, (size_t)12 * (G + 1) + 128, stream, x, ldx, q, s, s_tok, G, group_offsets);
     else if (G > 0)
-        launch_rowwise<false, false, true>(T, H, cap, (size_t)12 * (G + 1) + 128, stream, x, ldx, q, s, s_tok, nullptr,
-                                           nullptr, 0, G, group_offsets);
+        launch_rowwise<true>(T, H, cap, (size_t)12 * (G + 1) + 128, stream, x, ldx, q, s, s_tok, G, group_offsets);
     else if (four_six)
-        launch_rowwise<false, false, false, true>(T, H, cap, 0, stream, x, ldx, q, s, s_tok, nullptr, nullptr, 0, 0, nullptr);
+        launch_rowwise<false, true>(T, H, cap, 0, stream, x, ldx, q, s, s_tok, 0, nullptr);
     else
-        launch_rowwise<false, false, false>(T, H, cap, 0, stream, x, ldx, q, s, s_tok, nullptr, nullptr, 0, 0, nullptr);
+        launch_rowwise<false>(T, H, cap, 0, stream, x, ldx, q, s, s_tok, 0, nullptr);
     return cudaGetLastError();
 }
 
@@ -692,9 +741,10 @@ cudaError_t launch_nvfp4_1x16(const uint16_t* x, int64_t T, int64_t N, bool colw
     } else {
         amax_kernel<<<num_sms * 4, 256, 0, stream>>>(x, T * N, ws);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        const unsigned cap = (unsigned)num_sms * 16;
-        if (sr) launch_rowwise<true, true, false>(T, N, cap, 0, stream, x, N, q, s, nullptr, ws, s_tensor, sr_seed, 0, nullptr);
-        else launch_rowwise<true, false, false>(T, N, cap, 0, stream, x, N, q, s, nullptr, ws, s_tensor, sr_seed, 0, nullptr);
+        const int64_t blocks = T * (N / 16);
+        const unsigned grid = (unsigned)max64(1, min64((blocks + FL_THREADS - 1) / FL_THREADS, (int64_t)num_sms * FL_CTAS_PER_SM));
+        if (sr) nvfp4_1x16_flat_kernel<true><<<grid, FL_THREADS, 0, stream>>>(x, T, N, ws, s_tensor, sr_seed, q, s);
+        else nvfp4_1x16_flat_kernel<false><<<grid, FL_THREADS, 0, stream>>>(x, T, N, ws, s_tensor, sr_seed, q, s);
     }
     return cudaGetLastError();
 }
