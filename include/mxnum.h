@@ -75,6 +75,26 @@ mx_status mx_quantize_mxfp8(const void* x, int64_t rows, int64_t cols, int64_t l
                             uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                             cudaStream_t stream);
 
+/* Several tensors through mx_quantize_mxfp8 in one launch (for instance the input, weight and output
+ * gradient of a linear layer, which the training step quantizes back to back): the tiles of all the
+ * tensors share one persistent grid, so the launch ramps up and drains once.  Codes and scales are
+ * exactly those of one mx_quantize_mxfp8 call per tensor.
+ *   tensors  HOST array of `count` descriptors (1 <= count <= MX_MXFP8_MAX_BATCH), each with the
+ *            arguments and requirements of mx_quantize_mxfp8; every tensor must request the same
+ *            outputs (all row-wise, all column-wise or all both), else MX_ERR_INVALID_ARG.
+ * The descriptors are read before the call returns; the device buffers they name must stay valid
+ * until the work on `stream` completes. */
+#define MX_MXFP8_MAX_BATCH 4
+typedef struct {
+    const void* x;
+    int64_t rows, cols, ldx;
+    uint8_t* q_row;
+    uint8_t* s_row;
+    uint8_t* q_col;
+    uint8_t* s_col;
+} mx_mxfp8_tensor;
+mx_status mx_quantize_mxfp8_batched(const mx_mxfp8_tensor* tensors, int count, cudaStream_t stream);
+
 /* NVFP4 1x16 quantize with a per-token FP32 second-level scale, fused in one kernel.
  * Source: Miles page -- NVFP4 = E2M1 values, one E4M3 scale per 16, a second FP32 scale computed
  * separately for each token, online, fused into the activation quantizer that emits packed FP4,

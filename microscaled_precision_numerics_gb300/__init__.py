@@ -47,6 +47,7 @@ def lib() -> ctypes.CDLL:
                 "mx_scale_bytes": (I64, [I64, I64, I32]),
                 "mx_workspace_bytes": (SZ, [I32, I64, I64]),
                 "mx_quantize_mxfp8": (I32, [P, I64, I64, I64, P, P, P, P, P]),
+                "mx_quantize_mxfp8_batched": (I32, [P, I32, P]),
                 "mx_nvfp4_quantize_per_token": (I32, [P, I64, I64, I64, P, P, P, P]),
                 "mx_nvfp4_quantize_per_token_46": (I32, [P, I64, I64, I64, P, P, P, P]),
                 "mx_nvfp4_quantize_per_token_grouped": (I32, [P, I64, I64, I64, I64, P, P, P, P, P]),
@@ -122,6 +123,31 @@ def mx_quantize_mxfp8(x, q_row=None, s_row=None, q_col=None, s_col=None, stream=
     rows, cols = x.shape
     _check("mx_quantize_mxfp8", lib().mx_quantize_mxfp8(
         _p(x), rows, cols, x.stride(0), _p(q_row), _p(s_row), _p(q_col), _p(s_col), _stream(stream)))
+
+
+MX_MXFP8_MAX_BATCH = 4
+
+
+class _Mxfp8Tensor(ctypes.Structure):
+    """mx_mxfp8_tensor: one tensor of mx_quantize_mxfp8_batched."""
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("ldx", ctypes.c_int64),
+                ("q_row", ctypes.c_void_p), ("s_row", ctypes.c_void_p), ("q_col", ctypes.c_void_p),
+                ("s_col", ctypes.c_void_p)]
+
+
+def mx_quantize_mxfp8_batched(jobs, stream=None):
+    """mx_quantize_mxfp8 over several tensors in one launch.  `jobs`: a list of (x, outputs) pairs, outputs a
+    dict with the keyword arguments of mx_quantize_mxfp8 (q_row, s_row, q_col, s_col)."""
+    arr = (_Mxfp8Tensor * max(len(jobs), 1))()
+    keep = []
+    for i, (x, out) in enumerate(jobs):
+        x = _bf16_bits(x)
+        keep.append(x)
+        rows, cols = x.shape
+        arr[i] = _Mxfp8Tensor(_p(x), rows, cols, x.stride(0), _p(out.get("q_row")), _p(out.get("s_row")),
+                              _p(out.get("q_col")), _p(out.get("s_col")))
+    _check("mx_quantize_mxfp8_batched", lib().mx_quantize_mxfp8_batched(ctypes.cast(arr, ctypes.c_void_p),
+                                                                        len(jobs), _stream(stream)))
 
 
 def mx_nvfp4_quantize_per_token(x, q, s, s_tok, stream=None):

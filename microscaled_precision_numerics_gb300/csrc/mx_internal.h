@@ -19,6 +19,15 @@ __host__ __device__ inline int64_t host_scale_bytes_dev(int64_t rows, int64_t k,
 // RHT sign mask computed on the host with the same Philox4x32-10 definition as the device.
 uint32_t host_rht_sign_mask(uint64_t seed);
 
+// One tensor of an MXFP8 quantize launch (null q_row / q_col: that orientation is skipped).
+struct Mx8Tensor {
+    const uint16_t* x;
+    int64_t R, K, ldx;
+    uint8_t *q_row, *s_row, *q_col, *s_col;
+};
+constexpr int MX8_MAX_BATCH = 4;
+// Several tensors in one launch; all of them must request the same orientations.
+cudaError_t launch_mxfp8_quantize_batched(const Mx8Tensor* ts, int n, cudaStream_t stream);
 cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q_row,
                                   uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int G, const int64_t* group_offsets,
                                   cudaStream_t stream);

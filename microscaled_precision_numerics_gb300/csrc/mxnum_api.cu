@@ -63,8 +63,8 @@ size_t mx_workspace_bytes(mx_workspace_op op, int64_t groups, int64_t /*unused*/
     return 0;
 }
 
-mx_status mx_quantize_mxfp8(const void* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q_row, uint8_t* s_row,
-                            uint8_t* q_col, uint8_t* s_col, cudaStream_t stream) {
+static mx_status check_mxfp8_args(const void* x, int64_t rows, int64_t cols, int64_t ldx, const uint8_t* q_row,
+                                  const uint8_t* s_row, const uint8_t* q_col, const uint8_t* s_col) {
     if (!x || rows <= 0 || cols <= 0 || ldx < cols) return MX_ERR_INVALID_ARG;
     if (!q_row && !q_col) return MX_ERR_INVALID_ARG;
     if ((q_row && !s_row) || (q_col && !s_col)) return MX_ERR_INVALID_ARG;
@@ -74,8 +74,30 @@ mx_status mx_quantize_mxfp8(const void* x, int64_t rows, int64_t cols, int64_t l
         return MX_ERR_ALIGNMENT;
     if (q_row && (cols % 32) != 0) return MX_ERR_UNSUPPORTED;
     if (q_col && (rows % 32) != 0) return MX_ERR_UNSUPPORTED;
+    return MX_OK;
+}
+
+mx_status mx_quantize_mxfp8(const void* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q_row, uint8_t* s_row,
+                            uint8_t* q_col, uint8_t* s_col, cudaStream_t stream) {
+    const mx_status st = check_mxfp8_args(x, rows, cols, ldx, q_row, s_row, q_col, s_col);
+    if (st != MX_OK) return st;
     return from_cuda(mxk::launch_mxfp8_quantize(static_cast<const uint16_t*>(x), rows, cols, ldx, q_row, s_row,
                                                  q_col, s_col, 0, nullptr, stream));
+}
+
+mx_status mx_quantize_mxfp8_batched(const mx_mxfp8_tensor* tensors, int count, cudaStream_t stream) {
+    static_assert(MX_MXFP8_MAX_BATCH == mxk::MX8_MAX_BATCH, "batch limit");
+    if (!tensors || count < 1 || count > MX_MXFP8_MAX_BATCH) return MX_ERR_INVALID_ARG;
+    mxk::Mx8Tensor ts[MX_MXFP8_MAX_BATCH];
+    for (int i = 0; i < count; ++i) {
+        const mx_mxfp8_tensor& t = tensors[i];
+        const mx_status st = check_mxfp8_args(t.x, t.rows, t.cols, t.ldx, t.q_row, t.s_row, t.q_col, t.s_col);
+        if (st != MX_OK) return st;
+        if ((t.q_row != nullptr) != (tensors[0].q_row != nullptr) || (t.q_col != nullptr) != (tensors[0].q_col != nullptr))
+            return MX_ERR_INVALID_ARG;
+        ts[i] = mxk::Mx8Tensor{static_cast<const uint16_t*>(t.x), t.rows, t.cols, t.ldx, t.q_row, t.s_row, t.q_col, t.s_col};
+    }
+    return from_cuda(mxk::launch_mxfp8_quantize_batched(ts, count, stream));
 }
 
 mx_status mx_quantize_mxfp8_grouped(const void* x, int64_t rows, int64_t cols, int64_t ldx, int64_t G,

@@ -16,6 +16,7 @@
 #include "mx_internal.h"
 #include "mx_async.cuh"
 
+#include <cstring>
 #include <mutex>
 
 namespace mxk {
@@ -64,6 +65,34 @@ constexpr int QT_CTAS_PER_SM = 3;                      // occupancy hides the pa
 constexpr int QT_TILE_BYTES = QT_ROWS * QT_COLS * 2;
 constexpr int QT_BOX_BYTES = QT_TILE_BYTES / 2;        // 128 rows x 64 columns (128 bytes)
 
+// Up to MX8_MAX_BATCH tensors quantized by one launch: their 128 x 128 tiles are numbered one tensor
+// after the other (tile_end = running totals), and each tile is looked up here by its number.
+struct alignas(64) Mx8Params {
+    CUtensorMap tm[MX8_MAX_BATCH];      // [R, K] BF16 with row pitch ldx, 128 x 64 boxes, 128-byte swizzle
+    int64_t R[MX8_MAX_BATCH], K[MX8_MAX_BATCH], tiles_c[MX8_MAX_BATCH], tile_end[MX8_MAX_BATCH];
+    uint8_t* q_row[MX8_MAX_BATCH];
+    uint8_t* s_row[MX8_MAX_BATCH];
+    uint8_t* q_col[MX8_MAX_BATCH];
+    uint8_t* s_col[MX8_MAX_BATCH];
+    int n;
+};
+
+template <typename T>
+__device__ __forceinline__ T pick(const T (&a)[MX8_MAX_BATCH], int i) {
+    T v = a[0];
+#pragma unroll
+    for (int j = 1; j < MX8_MAX_BATCH; ++j) v = (i == j) ? a[j] : v;
+    return v;
+}
+
+// The tensor that tile number t belongs to.
+__device__ __forceinline__ int tile_tensor(const Mx8Params& p, int64_t t) {
+    int i = 0;
+#pragma unroll
+    for (int j = 1; j < MX8_MAX_BATCH; ++j) i = (j < p.n && t >= p.tile_end[j - 1]) ? j : i;
+    return i;
+}
+
 // Byte offset of 16-byte chunk c (0..15 along the 128 columns) of tile row r in a staged tile: two TMA
 // boxes of 128 rows x 128 bytes (columns 0..63, 64..127), each with the 128-byte swizzle (chunk index
 // XOR row & 7), which keeps both passes' 16-byte shared loads free of bank conflicts.
@@ -80,10 +109,7 @@ __device__ __forceinline__ void named_sync_consumers() { asm volatile("bar.sync 
 //                loads; the 32-row amax combines the 4 quarters (lanes l, l^8, l^16, l^24)
 template <bool ROW, bool COL, bool GROUPED>
 __global__ void __launch_bounds__(QT_BLOCK, QT_CTAS_PER_SM)
-mxfp8_quantize_kernel(const __grid_constant__ CUtensorMap tmX, int64_t R, int64_t K,
-                      uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
-                      uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, int64_t tiles_c, int64_t tiles,
-                      int G, const int64_t* __restrict__ group_offsets) {
+mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t* __restrict__ group_offsets) {
     using namespace async;
     extern __shared__ uint8_t qsm_raw[];
     uint8_t* qsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~uintptr_t(1023));
@@ -107,19 +133,22 @@ mxfp8_quantize_kernel(const __grid_constant__ CUtensorMap tmX, int64_t R, int64_
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tiles = p.tile_end[p.n - 1];
     if (warp == 0) {
         // ------------------------------- producer -------------------------------
-        if (lane == 0) asm volatile("prefetch.tensormap [%0];" :: "l"(&tmX) : "memory");
+        if (lane < p.n) asm volatile("prefetch.tensormap [%0];" :: "l"(&p.tm[lane]) : "memory");
         uint32_t k = 0;
         for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++k) {
             const uint32_t stage = k % QT_NST, phase = (k / QT_NST) & 1u;
             if (!warp_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, &g_mx8_status)) break;
             if (elect_one()) {
-                const int32_t r0 = (int32_t)((t / tiles_c) * QT_ROWS), c0 = (int32_t)((t % tiles_c) * QT_COLS);
+                const int i = tile_tensor(p, t);
+                const int64_t lt = t - (i > 0 ? pick(p.tile_end, i - 1) : 0), tc = pick(p.tiles_c, i);
+                const int32_t r0 = (int32_t)((lt / tc) * QT_ROWS), c0 = (int32_t)((lt % tc) * QT_COLS);
                 const uint32_t dst = smem_u32(qsm + stage * QT_TILE_BYTES);
                 mbar_arrive_expect_tx(full0 + 8 * stage, QT_TILE_BYTES);
-                tma_load_2d(dst, &tmX, c0, r0, full0 + 8 * stage);
-                tma_load_2d(dst + QT_BOX_BYTES, &tmX, c0 + 64, r0, full0 + 8 * stage);
+                tma_load_2d(dst, &p.tm[i], c0, r0, full0 + 8 * stage);
+                tma_load_2d(dst + QT_BOX_BYTES, &p.tm[i], c0 + 64, r0, full0 + 8 * stage);
             }
             __syncwarp();
         }
@@ -132,8 +161,15 @@ mxfp8_quantize_kernel(const __grid_constant__ CUtensorMap tmX, int64_t R, int64_
         // warp-uniform: the passes below use full-warp shuffles
         const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * stage, phase, abort_flag, &g_mx8_status)) != 0;
         const uint8_t* tile = qsm + stage * QT_TILE_BYTES;
-        const int64_t r0 = (t / tiles_c) * QT_ROWS;
-        const int64_t c0 = (t % tiles_c) * QT_COLS;
+        const int ti = tile_tensor(p, t);
+        const int64_t lt = t - (ti > 0 ? pick(p.tile_end, ti - 1) : 0), tiles_c = pick(p.tiles_c, ti);
+        const int64_t R = pick(p.R, ti), K = pick(p.K, ti);
+        uint8_t* __restrict__ q_row = pick(p.q_row, ti);
+        uint8_t* __restrict__ s_row = pick(p.s_row, ti);
+        uint8_t* __restrict__ q_col = pick(p.q_col, ti);
+        uint8_t* __restrict__ s_col = pick(p.s_col, ti);
+        const int64_t r0 = (lt / tiles_c) * QT_ROWS;
+        const int64_t c0 = (lt % tiles_c) * QT_COLS;
 
         if (ROW && ok) {
             // lanes 0..7 take 8 different rows of the same 64-column half
@@ -236,27 +272,45 @@ mxfp8_quantize_kernel(const __grid_constant__ CUtensorMap tmX, int64_t R, int64_
     }
 }
 
-}  // namespace
+// Scale padding that the kernel does not write (rows beyond R up to a multiple of 128, scale columns up to
+// a multiple of 4; in the grouped layout also the rows between groups) is zeroed first.
+static cudaError_t mx8_zero_padding(const Mx8Tensor& t, int G, cudaStream_t stream) {
+    if (t.q_row && (G > 0 || (t.R % 128) != 0 || ((t.K / 32) % 4) != 0)) {
+        cudaError_t e = cudaMemsetAsync(t.s_row, 0, (size_t)host_scale_bytes(t.R + 127 * (int64_t)G, t.K, 32), stream);
+        if (e != cudaSuccess) return e;
+    }
+    if (t.q_col && ((t.K % 128) != 0 || ((t.R / 32) % 4) != 0)) {
+        cudaError_t e = cudaMemsetAsync(t.s_col, 0, (size_t)host_scale_bytes(t.K, t.R, 32), stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 
-cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q_row,
-                                  uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int G, const int64_t* group_offsets,
-                                  cudaStream_t stream) {
-    const bool row = q_row != nullptr, col = q_col != nullptr;
-    // zero the scale padding (rows beyond R up to a multiple of 128, scale columns up to a multiple of 4;
-    // in the grouped layout also the rows between groups)
-    if (row && (G > 0 || (R % 128) != 0 || ((K / 32) % 4) != 0)) {
-        cudaError_t e = cudaMemsetAsync(s_row, 0, (size_t)host_scale_bytes(R + 127 * (int64_t)G, K, 32), stream);
+static cudaError_t launch_mx8(const Mx8Tensor* ts, int n, int G, const int64_t* group_offsets, cudaStream_t stream) {
+    if (n < 1 || n > MX8_MAX_BATCH) return cudaErrorInvalidValue;
+    const bool row = ts[0].q_row != nullptr, col = ts[0].q_col != nullptr;
+    Mx8Params p;
+    memset(&p, 0, sizeof(p));
+    p.n = n;
+    int64_t tiles = 0;
+    for (int i = 0; i < n; ++i) {
+        const Mx8Tensor& t = ts[i];
+        if ((t.q_row != nullptr) != row || (t.q_col != nullptr) != col) return cudaErrorInvalidValue;
+        if (!encode_tensor_map_2d(&p.tm[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, t.x, (uint64_t)t.K, (uint64_t)t.R,
+                                  (uint64_t)(t.ldx * 2), 64, QT_ROWS, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+            return cudaErrorInvalidValue;
+        p.R[i] = t.R; p.K[i] = t.K;
+        p.tiles_c[i] = (t.K + QT_COLS - 1) / QT_COLS;
+        tiles += p.tiles_c[i] * ((t.R + QT_ROWS - 1) / QT_ROWS);
+        p.tile_end[i] = tiles;
+        p.q_row[i] = t.q_row; p.s_row[i] = t.s_row; p.q_col[i] = t.q_col; p.s_col[i] = t.s_col;
+    }
+    // every descriptor is valid: only now enqueue anything
+    for (int i = 0; i < n; ++i) {
+        cudaError_t e = mx8_zero_padding(ts[i], G, stream);
         if (e != cudaSuccess) return e;
     }
-    if (col && ((K % 128) != 0 || ((R / 32) % 4) != 0)) {
-        cudaError_t e = cudaMemsetAsync(s_col, 0, (size_t)host_scale_bytes(K, R, 32), stream);
-        if (e != cudaSuccess) return e;
-    }
-    CUtensorMap tmX;     // [R, K] BF16 with row pitch ldx, 128 x 64 boxes, 128-byte swizzle
-    if (!encode_tensor_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, (uint64_t)K, (uint64_t)R, (uint64_t)(ldx * 2), 64,
-                              QT_ROWS, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
-        return cudaErrorInvalidValue;
-    const int64_t tiles_c = (K + QT_COLS - 1) / QT_COLS, tiles = tiles_c * ((R + QT_ROWS - 1) / QT_ROWS);
     const size_t base = (size_t)QT_NST * QT_TILE_BYTES + 4 * QT_COLS + 64 + 1024;
     const size_t smem = base + (G > 0 ? (size_t)12 * (G + 1) + 128 : 0);
     static std::once_flag once;
@@ -271,18 +325,27 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64
     if (attr_err != cudaSuccess) return attr_err;
     const unsigned grid = (unsigned)min64(tiles, (int64_t)device_sm_count() * QT_CTAS_PER_SM);
     if (G > 0)
-        mxfp8_quantize_kernel<true, false, true><<<grid, QT_BLOCK, smem, stream>>>(tmX, R, K, q_row, s_row, nullptr, nullptr,
-                                                                                    tiles_c, tiles, G, group_offsets);
+        mxfp8_quantize_kernel<true, false, true><<<grid, QT_BLOCK, smem, stream>>>(p, G, group_offsets);
     else if (row && col)
-        mxfp8_quantize_kernel<true, true, false><<<grid, QT_BLOCK, smem, stream>>>(tmX, R, K, q_row, s_row, q_col, s_col,
-                                                                                    tiles_c, tiles, 0, nullptr);
+        mxfp8_quantize_kernel<true, true, false><<<grid, QT_BLOCK, smem, stream>>>(p, 0, nullptr);
     else if (row)
-        mxfp8_quantize_kernel<true, false, false><<<grid, QT_BLOCK, smem, stream>>>(tmX, R, K, q_row, s_row, q_col, s_col,
-                                                                                     tiles_c, tiles, 0, nullptr);
+        mxfp8_quantize_kernel<true, false, false><<<grid, QT_BLOCK, smem, stream>>>(p, 0, nullptr);
     else
-        mxfp8_quantize_kernel<false, true, false><<<grid, QT_BLOCK, smem, stream>>>(tmX, R, K, q_row, s_row, q_col, s_col,
-                                                                                     tiles_c, tiles, 0, nullptr);
+        mxfp8_quantize_kernel<false, true, false><<<grid, QT_BLOCK, smem, stream>>>(p, 0, nullptr);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q_row,
+                                  uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int G, const int64_t* group_offsets,
+                                  cudaStream_t stream) {
+    const Mx8Tensor t{x, R, K, ldx, q_row, s_row, q_col, s_col};
+    return launch_mx8(&t, 1, G, group_offsets, stream);
+}
+
+cudaError_t launch_mxfp8_quantize_batched(const Mx8Tensor* ts, int n, cudaStream_t stream) {
+    return launch_mx8(ts, n, 0, nullptr, stream);
 }
 
 uint32_t read_and_clear_mxfp8_status() {

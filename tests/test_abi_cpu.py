@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for required in ["mx_quantize_mxfp8", "mx_nvfp4_quantize_per_token", "mx_nvfp4_quantize_weight_2d", "mx_rht16",
+    for required in ["mx_quantize_mxfp8", "mx_quantize_mxfp8_batched", "mx_nvfp4_quantize_per_token", "mx_nvfp4_quantize_weight_2d", "mx_rht16",
                      "mx_nvfp4_quantize_1x16", "mx_dequantize_bf16", "mx_scaled_gemm", "mx_grouped_scaled_gemm",
                      "mx_fp8_blockwise_quantize_1x128", "mx_fp8_blockwise_quantize_128x128", "mx_gemm_bf16_dq_nvfp4",
                      "mx_wgrad_bf16_dq_nvfp4", "mx_fp8_blockwise_gemm"]:
@@ -70,6 +70,25 @@ def test_mxfp8_validation(lib):
     assert f(A16, 48, 32, 32, NUL, NUL, A16, A16, NUL) == 3            # rows % 32 for column-wise
     assert f(A16, 32, 36, 36, A16, A16, NUL, NUL, NUL) == 2            # cols % 8 (16-byte rows)
     assert f(A16, -1, 32, 32, A16, A16, NUL, NUL, NUL) == 1
+
+
+def test_mxfp8_batched_validation(lib):
+    from microscaled_precision_numerics_gb300 import _Mxfp8Tensor
+    f = lib.mx_quantize_mxfp8_batched
+    both = _Mxfp8Tensor(0x10000, 32, 32, 32, 0x10000, 0x10000, 0x10000, 0x10000)
+    row = _Mxfp8Tensor(0x10000, 32, 32, 32, 0x10000, 0x10000, None, None)
+    bad = _Mxfp8Tensor(0x10008, 32, 32, 32, 0x10000, 0x10000, 0x10000, 0x10000)
+
+    def call(items, count=None):
+        arr = (_Mxfp8Tensor * max(len(items), 1))(*items)
+        return f(ctypes.cast(arr, ctypes.c_void_p), len(items) if count is None else count, None)
+
+    assert f(None, 1, None) == 1                                        # no descriptors
+    assert call([both], 0) == 1                                         # empty batch
+    assert call([both] * 5) == 1                                        # above MX_MXFP8_MAX_BATCH
+    assert call([both, row]) == 1                                       # mixed orientations
+    assert call([both, bad]) == 2                                       # one descriptor misaligned
+    assert call([both, _Mxfp8Tensor(0x10000, 32, 48, 48, 0x10000, 0x10000, 0x10000, 0x10000)]) == 3
 
 
 def test_nvfp4_validation(lib):

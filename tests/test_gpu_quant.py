@@ -60,6 +60,38 @@ def test_mxfp8_row_and_col(mx, orc, shape):
     assert np.array_equal(to_np(out["s_col"]), orc.scales_to_gemm_layout(sc))
 
 
+@pytest.mark.parametrize("which", ["both", "row", "col"])
+def test_mxfp8_batched(mx, orc, which):
+    """One launch over tensors of different shapes (ragged tiles, one strided) gives each tensor exactly the
+    codes and scales of the oracle's per-tensor quantizer."""
+    shapes = [(256, 1024), (96, 160), (384, 416), (64, 128)]
+    xs = [edge_tensor(31 * i + R + K, (R, K)) for i, (R, K) in enumerate(shapes)]
+    jobs, outs = [], []
+    for i, ((R, K), x) in enumerate(zip(shapes, xs)):
+        out = mx.alloc_mxfp8(R, K, DEV, rowwise=which != "col", colwise=which != "row")
+        for v in out.values():
+            v.fill_(0xAB)
+        xd = bf16_dev(x)
+        if i == 3:                                # a row pitch of 192 elements
+            wide = torch.zeros((R, 192), dtype=torch.bfloat16, device=DEV)
+            wide[:, :K] = xd
+            xd = wide[:, :K]
+        jobs.append((xd, out))
+        outs.append(out)
+    mx.mx_quantize_mxfp8_batched(jobs)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    for x, out in zip(xs, outs):
+        if which != "col":
+            qr, sr = orc.mxfp8_quantize_rowwise(x)
+            assert np.array_equal(to_np(out["q_row"]), qr), first_mismatch(to_np(out["q_row"]), qr)
+            assert np.array_equal(to_np(out["s_row"]), orc.scales_to_gemm_layout(sr))
+        if which != "row":
+            qc, sc = orc.mxfp8_quantize_colwise(x)
+            assert np.array_equal(to_np(out["q_col"]), qc), first_mismatch(to_np(out["q_col"]), qc)
+            assert np.array_equal(to_np(out["s_col"]), orc.scales_to_gemm_layout(sc))
+
+
 def test_mxfp8_rowwise_only_ragged_rows(mx, orc):
     x = edge_tensor(5, (37, 96))
     out = mx.alloc_mxfp8(37, 96, DEV, colwise=False)
