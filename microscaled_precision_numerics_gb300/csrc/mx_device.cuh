@@ -313,5 +313,51 @@ __device__ __forceinline__ int64_t grouped_scale_row(const int64_t* s_off, const
     return (int64_t)s_ptile[g] * 128 + (r - s_off[g]);
 }
 
+// Zero what a grouped quantizer does not write in its scale layout of `tile_bound` 128-row tiles (nct
+// 4-column words per row, scale columns a multiple of 4): the padded rows after group g's m_g rows up
+// to the end of its last tile, and every tile after the last group's (a contiguous byte range).  The
+// work is shared by `nwarps` warps of the grid; this is warp `wid` of them.  The tables come from
+// load_group_tables (s_ptile[G] = the total number of group tiles).
+__device__ __forceinline__ void zero_grouped_padding(uint8_t* __restrict__ s, const int64_t* s_off, const int* s_ptile,
+                                                     int G, int64_t nct, int64_t tile_bound, int64_t wid,
+                                                     int64_t nwarps) {
+    // (offsets that are not non-decreasing are invalid input; the clamps keep every store inside the
+    // layout all the same)
+    const int lane = threadIdx.x & 31;
+    for (int64_t g = wid; g < G; g += nwarps) {
+        const int64_t first = max64(0, (int64_t)s_ptile[g] * 128 + (s_off[g + 1] - s_off[g]));
+        const int64_t end = min64((int64_t)s_ptile[g + 1] * 128, tile_bound * 128);
+        const int64_t n = (end - first) * nct;                                   // < 128 rows, in one tile
+        for (int64_t i = lane; i < n; i += 32)
+            *reinterpret_cast<uint32_t*>(s + sf_offset(first + i / nct, 4 * (i % nct), nct)) = 0u;
+    }
+    const int64_t used = min64(max64(0, (int64_t)s_ptile[G]), tile_bound);
+    uint4* tail = reinterpret_cast<uint4*>(s + used * nct * 512);
+    const int64_t n16 = (tile_bound - used) * nct * 32;                         // 512-byte tiles as 16-byte words
+    for (int64_t i = wid * 32 + lane; i < n16; i += nwarps * 32) tail[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// The same for a row r shared by the N lanes [base, base + N) of the warp (lane `sub` of them; N = 16
+// or 32, all lanes of the warp calling together): each round the N lanes test N evenly spaced offsets
+// of the remaining range and a ballot keeps the span after the last offset <= r, so G = 128 groups take
+// two rounds instead of seven dependent steps.
+template <int N>
+__device__ __forceinline__ int64_t grouped_scale_row_lanes(const int64_t* s_off, const int* s_ptile, int G, int64_t r,
+                                                           int sub, int base) {
+    int lo = 0, span = G;                              // invariant: s_off[lo] <= r, group in [lo, lo + span)
+    // a round count that depends on G only keeps the warp converged for the ballot when the two rows of
+    // a warp narrow at different speeds (a finished search repeats as a no-op)
+    for (int reach = 1; reach < G; reach *= N) {
+        const int step = (span + N - 1) / N;
+        const int g = lo + sub * step;
+        const bool le = g < lo + span && s_off[g] <= r;
+        const uint32_t bits = (__ballot_sync(0xFFFFFFFFu, le) >> base) & (N == 32 ? 0xFFFFFFFFu : ((1u << N) - 1u));
+        const int k = 31 - __clz(bits);               // lane 0 always passes (g = lo)
+        lo += k * step;
+        span = min(step, span - k * step);
+    }
+    return (int64_t)s_ptile[lo] * 128 + (r - s_off[lo]);
+}
+
 }  // namespace mxk
 

@@ -109,7 +109,8 @@ __device__ __forceinline__ void named_sync_consumers() { asm volatile("bar.sync 
 //                loads; the 32-row amax combines the 4 quarters (lanes l, l^8, l^16, l^24)
 template <bool ROW, bool COL, bool GROUPED>
 __global__ void __launch_bounds__(QT_BLOCK, QT_CTAS_PER_SM)
-mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t* __restrict__ group_offsets) {
+mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t* __restrict__ group_offsets,
+                      bool zero_pad) {
     using namespace async;
     extern __shared__ uint8_t qsm_raw[];
     uint8_t* qsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~uintptr_t(1023));
@@ -197,10 +198,11 @@ mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t*
             // the row's 4 scales: this thread's two and those of lane + 8 (the other half)
             const uint32_t mine = s2[0] | (s2[1] << 8);
             const uint32_t other = __shfl_down_sync(0xFFFFFFFFu, mine, 8);
-            if (half == 0 && r < R) {
+            const int64_t srow = GROUPED ? grouped_scale_row(s_off, s_ptile, G, r) : r;
+            // (a grouped row stays inside the layout even for offsets that are not non-decreasing)
+            if (half == 0 && r < R && srow >= 0 && srow < R + 127 * (int64_t)G) {
                 const int64_t nct = sf_col_tiles(K, 32);
                 const int nvalid = (int)min64(4, (K - c0) / 32);
-                const int64_t srow = GROUPED ? grouped_scale_row(s_off, s_ptile, G, r) : r;
                 uint8_t* p = s_row + sf_offset(srow, c0 / 32, nct);
                 const uint32_t word = mine | (other << 16);
                 if (nvalid == 4) *reinterpret_cast<uint32_t*>(p) = word;
@@ -265,6 +267,9 @@ mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t*
             named_sync_consumers();   // colsc is rewritten by the next tile
         }
     }
+    if (GROUPED && zero_pad)
+        zero_grouped_padding(p.s_row[0], s_off, s_ptile, G, sf_col_tiles(p.K[0], 32), (p.R[0] + 127 * (int64_t)G + 127) / 128,
+                             (int64_t)blockIdx.x * (QT_CONSUMERS / 32) + cw, (int64_t)gridDim.x * (QT_CONSUMERS / 32));
     if (*abort_flag && tid == 0) {
         // after an expired wait: give loads already issued by this CTA time to land before exit
         const unsigned long long t0 = globaltimer();
@@ -275,7 +280,8 @@ mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t*
 // Scale padding that the kernel does not write (rows beyond R up to a multiple of 128, scale columns up to
 // a multiple of 4; in the grouped layout also the rows between groups) is zeroed first.
 static cudaError_t mx8_zero_padding(const Mx8Tensor& t, int G, cudaStream_t stream) {
-    if (t.q_row && (G > 0 || (t.R % 128) != 0 || ((t.K / 32) % 4) != 0)) {
+    // grouped with whole scale words: the kernel zeroes the padding rows between groups and the tail
+    if (t.q_row && ((G > 0 && ((t.K / 32) % 4) != 0) || (G == 0 && ((t.R % 128) != 0 || ((t.K / 32) % 4) != 0)))) {
         cudaError_t e = cudaMemsetAsync(t.s_row, 0, (size_t)host_scale_bytes(t.R + 127 * (int64_t)G, t.K, 32), stream);
         if (e != cudaSuccess) return e;
     }
@@ -325,13 +331,14 @@ static cudaError_t launch_mx8(const Mx8Tensor* ts, int n, int G, const int64_t* 
     if (attr_err != cudaSuccess) return attr_err;
     const unsigned grid = (unsigned)min64(tiles, (int64_t)device_sm_count() * QT_CTAS_PER_SM);
     if (G > 0)
-        mxfp8_quantize_kernel<true, false, true><<<grid, QT_BLOCK, smem, stream>>>(p, G, group_offsets);
+        mxfp8_quantize_kernel<true, false, true><<<grid, QT_BLOCK, smem, stream>>>(p, G, group_offsets,
+                                                                                    ((ts[0].K / 32) % 4) == 0);
     else if (row && col)
-        mxfp8_quantize_kernel<true, true, false><<<grid, QT_BLOCK, smem, stream>>>(p, 0, nullptr);
+        mxfp8_quantize_kernel<true, true, false><<<grid, QT_BLOCK, smem, stream>>>(p, 0, nullptr, false);
     else if (row)
-        mxfp8_quantize_kernel<true, false, false><<<grid, QT_BLOCK, smem, stream>>>(p, 0, nullptr);
+        mxfp8_quantize_kernel<true, false, false><<<grid, QT_BLOCK, smem, stream>>>(p, 0, nullptr, false);
     else
-        mxfp8_quantize_kernel<false, true, false><<<grid, QT_BLOCK, smem, stream>>>(p, 0, nullptr);
+        mxfp8_quantize_kernel<false, true, false><<<grid, QT_BLOCK, smem, stream>>>(p, 0, nullptr, false);
     return cudaGetLastError();
 }
 

@@ -98,7 +98,7 @@ template <bool GROUPED, int LPR, bool FOUR_SIX = false>
 __global__ void __launch_bounds__(RW_WARPS * 32, RW_CTAS_PER_SM)
 nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64_t ldx,
                      uint8_t* __restrict__ q, uint8_t* __restrict__ s, float* __restrict__ s_tok,
-                     int G, const int64_t* __restrict__ group_offsets) {
+                     int G, const int64_t* __restrict__ group_offsets, bool zero_pad) {
     // LPR lanes per row (32 or 16): a warp works on 32 / LPR rows at once
     constexpr int RPW = 32 / LPR;
     extern __shared__ __align__(16) uint8_t rw_sm[];
@@ -155,7 +155,12 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
             S = nvfp4_second_scale(__uint_as_float(amax16 << 16));
             if (row_ok && sub == 0) s_tok[t] = S;
         }
-        const int64_t srow = (GROUPED && row_ok) ? grouped_scale_row(s_off, s_ptile, G, t) : t;
+        int64_t srow = t;
+        bool srow_ok = true;
+        if (GROUPED) {
+            srow = grouped_scale_row_lanes<LPR>(s_off, s_ptile, G, row_ok ? t : T - 1, sub, half * LPR);
+            srow_ok = srow >= 0 && srow < T + 127 * (int64_t)G;   // stays inside the layout (offsets not checked)
+        }
         const float rS = nvfp4_fast_rs(S);
 
         // codes, and the four consecutive block scales of lanes 4m .. 4m+3 of the row group as one word
@@ -167,7 +172,7 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
             const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, bs, 1);
             const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, bs, 2);
             const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, bs, 3);
-            if (valid && (b & 3) == 0) {
+            if (valid && srow_ok && (b & 3) == 0) {
                 uint8_t* p = s + sf_offset(srow, b, nct);
                 if (b + 4 <= nblk) {
                     *reinterpret_cast<uint32_t*>(p) = bs | (b1 << 8) | (b2 << 16) | (b3 << 24);
@@ -210,19 +215,23 @@ nvfp4_rowwise_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64
             }
         }
     }
+    if (GROUPED && zero_pad)
+        zero_grouped_padding(s, s_off, s_ptile, G, nct, (T + 127 * (int64_t)G + 127) / 128,
+                             (int64_t)blockIdx.x * RW_WARPS + (threadIdx.x >> 5), (int64_t)gridDim.x * RW_WARPS);
+
 }
 
 template <bool GROUPED, bool FOUR_SIX = false>
 void launch_rowwise(int64_t T, int64_t H, unsigned grid_cap, size_t smem, cudaStream_t stream, const uint16_t* x,
-                    int64_t ldx, uint8_t* q, uint8_t* s, float* s_tok, int G, const int64_t* offs) {
+                    int64_t ldx, uint8_t* q, uint8_t* s, float* s_tok, int G, const int64_t* offs, bool zero_pad = false) {
     if (H / 16 <= 64) {
         const int64_t blocks = (T + RW_WARPS * 2 - 1) / (RW_WARPS * 2);
         nvfp4_rowwise_kernel<GROUPED, 16, FOUR_SIX><<<(unsigned)min64(blocks, grid_cap), RW_WARPS * 32, smem, stream>>>(
-            x, T, H, ldx, q, s, s_tok, G, offs);
+            x, T, H, ldx, q, s, s_tok, G, offs, zero_pad);
     } else {
         const int64_t blocks = (T + RW_WARPS - 1) / RW_WARPS;
         nvfp4_rowwise_kernel<GROUPED, 32, FOUR_SIX><<<(unsigned)min64(blocks, grid_cap), RW_WARPS * 32, smem, stream>>>(
-            x, T, H, ldx, q, s, s_tok, G, offs);
+            x, T, H, ldx, q, s, s_tok, G, offs, zero_pad);
     }
 }
 
@@ -697,19 +706,23 @@ weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, cons
 cudaError_t launch_nvfp4_per_token(const uint16_t* x, int64_t T, int64_t H, int64_t ldx, uint8_t* q, uint8_t* s,
                                    float* s_tok, int G, const int64_t* group_offsets, int num_sms, cudaStream_t stream,
                                    bool four_six) {
-    if (G > 0) {
-        // grouped layout: the padding between groups is zero
+    // grouped layout: the padding rows between groups and the unused tail are zeroed by the kernel when
+    // the scale columns fill whole words; otherwise the whole layout is cleared first
+    const bool kernel_pads = G > 0 && ((H / 16) % 4) == 0;
+    if (G > 0 && !kernel_pads) {
         cudaError_t e = cudaMemsetAsync(s, 0, (size_t)host_scale_bytes(T + 127 * (int64_t)G, H, 16), stream);
         if (e != cudaSuccess) return e;
-    } else if ((T % 128) != 0 || ((H / 16) % 4) != 0) {
+    } else if (G == 0 && ((T % 128) != 0 || ((H / 16) % 4) != 0)) {
         cudaError_t e = cudaMemsetAsync(s, 0, (size_t)host_scale_bytes(T, H, 16), stream);
         if (e != cudaSuccess) return e;
     }
     const unsigned cap = (unsigned)num_sms * 16;
     if (G > 0 && four_six)
-        launch_rowwise<true, true>(T, H, cap, (size_t)12 * (G + 1) + 128, stream, x, ldx, q, s, s_tok, G, group_offsets);
+        launch_rowwise<true, true>(T, H, cap, (size_t)12 * (G + 1) + 128, stream, x, ldx, q, s, s_tok, G, group_offsets,
+                                   kernel_pads);
     else if (G > 0)
-        launch_rowwise<true>(T, H, cap, (size_t)12 * (G + 1) + 128, stream, x, ldx, q, s, s_tok, G, group_offsets);
+        launch_rowwise<true>(T, H, cap, (size_t)12 * (G + 1) + 128, stream, x, ldx, q, s, s_tok, G, group_offsets,
+                             kernel_pads);
     else if (four_six)
         launch_rowwise<false, true>(T, H, cap, 0, stream, x, ldx, q, s, s_tok, 0, nullptr);
     else

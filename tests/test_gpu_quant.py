@@ -344,12 +344,15 @@ def test_dequant_nvfp4_stacked_2d_weights_group_scope(mx, orc):
         assert np.array_equal(got[g], ref), first_mismatch(got[g], ref)
 
 
+@pytest.mark.parametrize("K", [256, 96])
 @pytest.mark.parametrize("sizes", [[0, 130, 7, 300, 128, 1], [512] * 3, [1] * 40])
-def test_grouped_quantizers_write_grouped_layout(mx, orc, sizes):
-    """The *_grouped quantizers give the plain codes and the scales in the grouped layout."""
+def test_grouped_quantizers_write_grouped_layout(mx, orc, sizes, K):
+    """The *_grouped quantizers give the plain codes and the scales in the grouped layout, padding rows
+    between groups and the unused tail zero (K = 256: whole scale words, zeroed by the kernels; K = 96:
+    partial words, the layout cleared before the kernel)."""
     G = len(sizes)
     offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
-    R, K = int(offs[-1]), 256
+    R = int(offs[-1])
     x = edge_tensor(R + G, (R, K))
     offs_d = torch.from_numpy(offs).to(DEV)
     q = torch.empty((R, K // 2), dtype=torch.uint8, device=DEV)
