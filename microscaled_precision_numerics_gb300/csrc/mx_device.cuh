@@ -142,10 +142,8 @@ __device__ __forceinline__ uint32_t rht_sign_mask(uint64_t seed) {
     return philox4x32_10(0u, 0u, 1u, 0u, (uint32_t)seed, (uint32_t)(seed >> 32)).x & 0xFFFFu;
 }
 
-// In-register 16-point transform without the final 1/4: signs, then butterflies with strides 1, 2, 4, 8.
-__device__ __forceinline__ void rht16_unscaled(float v[16], uint32_t signmask) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = ((signmask >> j) & 1u) ? -v[j] : v[j];
+// In-register 16-point Walsh-Hadamard butterflies with strides 1, 2, 4, 8 (no signs, no 1/4).
+__device__ __forceinline__ void fwht16_unscaled(float v[16]) {
 #pragma unroll
     for (int h = 1; h < 16; h *= 2) {
 #pragma unroll
@@ -160,11 +158,11 @@ __device__ __forceinline__ void rht16_unscaled(float v[16], uint32_t signmask) {
     }
 }
 
-// In-register 16-point transform: signs, butterflies with strides 1, 2, 4, 8, then x 1/4.
-__device__ __forceinline__ void rht16_inplace(float v[16], uint32_t signmask) {
-    rht16_unscaled(v, signmask);
+// In-register 16-point transform without the final 1/4: signs, then butterflies with strides 1, 2, 4, 8.
+__device__ __forceinline__ void rht16_unscaled(float v[16], uint32_t signmask) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+    for (int j = 0; j < 16; ++j) v[j] = ((signmask >> j) & 1u) ? -v[j] : v[j];
+    fwht16_unscaled(v);
 }
 
 // ---------------------------------------------------------------------------------------------

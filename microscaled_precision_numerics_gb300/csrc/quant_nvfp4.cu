@@ -321,20 +321,22 @@ __device__ __forceinline__ void load_16(const uint16_t* __restrict__ x, int64_t 
     }
 }
 
-// Column j of the micro-tile as 16 floats, optionally transformed and re-rounded to BF16.
-template <bool RHT, int CPT>
-__device__ __forceinline__ void column_values(const uint32_t (&xw)[16][CPT / 2], int j, uint32_t signmask, float v[16]) {
+// The two columns held in word column w of a 16-token micro-tile, transformed in place along the tokens:
+// signs applied to the packed BF16 words (a sign flip is exact), butterflies in FP32, x 1/4, and the
+// pair packed back to BF16 (RNE), so each word again holds the two columns' values of one token.
+template <int NW>
+__device__ __forceinline__ void rht16_pair_inplace(uint32_t (&xw)[16][NW], int w, uint32_t signmask) {
+    float a[16], b[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = (j & 1) ? bf16_hi(xw[i][j >> 1]) : bf16_lo(xw[i][j >> 1]);
-    if (RHT) {
-        rht16_inplace(v, signmask);
-#pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-            const uint32_t p = pack_bf16x2(v[i], v[i + 1]);
-            v[i] = bf16_lo(p);
-            v[i + 1] = bf16_hi(p);
-        }
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t v = xw[i][w] ^ (((signmask >> i) & 1u) ? 0x80008000u : 0u);
+        a[i] = bf16_lo(v);
+        b[i] = bf16_hi(v);
     }
+    fwht16_unscaled(a);
+    fwht16_unscaled(b);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) xw[i][w] = pack_bf16x2(__fmul_rn(a[i], 0.25f), __fmul_rn(b[i], 0.25f));
 }
 
 // Tensor amax of the (transformed) input.  With the transform, the maximum is taken over the FP32
@@ -405,34 +407,30 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
     uint32_t xw[16][CPT / 2];
     load_16<CPT>(x, N, t0, n0, valid, xw);
 
-    // Phase A, per column j: (transform and re-round in place,) block amax, block scale, reciprocal.
+    // Phase A, per pair of columns (2 jp, 2 jp + 1), whose values share one BF16 word per token:
+    // (transform and re-round in place,) block amax of both columns from the packed words, block
+    // scales, reciprocals.
     float rcp[CPT];
 #pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-        float v[16];
-        column_values<RHT, CPT>(xw, j, signmask, v);
-        if (RHT) {
-            // store the BF16-rounded transformed values back in place of the inputs
+    for (int jp = 0; jp < CPT / 2; ++jp) {
+        if (RHT) rht16_pair_inplace<CPT / 2>(xw, jp, signmask);
+        uint32_t m2 = 0;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                uint32_t& w = xw[i][j >> 1];
-                const uint32_t b = __float_as_uint(v[i]) >> 16;
-                w = (j & 1) ? ((w & 0x0000FFFFu) | (b << 16)) : ((w & 0xFFFF0000u) | b);
+        for (int i = 0; i < 16; ++i) m2 = absmax_bf16x2(m2, xw[i][jp]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int j = 2 * jp + h;
+            const uint32_t bs = nvfp4_block_scale_fast(__uint_as_float((h ? (m2 >> 16) : (m2 & 0xFFFFu)) << 16), S, rS);
+            rcp[j] = nvfp4_block_recip(bs, S);
+            ss[warp][lane * CPT + j] = (uint8_t)bs;
+            if (!SR) {
+                float p[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) p[i] = __fmul_rn(h ? bf16_hi(xw[i][jp]) : bf16_lo(xw[i][jp]), rcp[j]);
+                // the 16 tokens of column n0 + j: 8 bytes, stored straight to the transposed output
+                if (valid) __stcs(reinterpret_cast<uint2*>(q + (n0 + j) * (T / 2) + t0 / 2),
+                                  make_uint2(cvt_e2m1x8(p), cvt_e2m1x8(p + 8)));
             }
-        }
-        uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
-        const uint32_t bs = nvfp4_block_scale_fast(__uint_as_float(m), S, rS);
-        rcp[j] = nvfp4_block_recip(bs, S);
-        ss[warp][lane * CPT + j] = (uint8_t)bs;
-        if (!SR) {
-            float p[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) p[i] = __fmul_rn(v[i], rcp[j]);
-            // the 16 tokens of column n0 + j: 8 bytes, stored straight to the transposed output
-            if (valid) __stcs(reinterpret_cast<uint2*>(q + (n0 + j) * (T / 2) + t0 / 2),
-                              make_uint2(cvt_e2m1x8(p), cvt_e2m1x8(p + 8)));
         }
     }
     if (SR) {
@@ -513,18 +511,11 @@ rht16_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint32_t sign
     if (t0 >= T) return;
     uint32_t xw[16][4];
     load_16<8>(x, N, t0, n0, true, xw);
-    uint32_t out[16][4];
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-        float a[16], b[16];
-        column_values<true, 8>(xw, j, signmask, a);
-        column_values<true, 8>(xw, j + 1, signmask, b);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) out[i][j >> 1] = pack_bf16x2(a[i], b[i]);
-    }
+    for (int w = 0; w < 4; ++w) rht16_pair_inplace<4>(xw, w, signmask);
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-        __stcs(reinterpret_cast<uint4*>(y + (t0 + i) * N + n0), make_uint4(out[i][0], out[i][1], out[i][2], out[i][3]));
+        __stcs(reinterpret_cast<uint4*>(y + (t0 + i) * N + n0), make_uint4(xw[i][0], xw[i][1], xw[i][2], xw[i][3]));
 }
 
 // ------------------------------------------------------------------------------------------------
