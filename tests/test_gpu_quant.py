@@ -149,6 +149,53 @@ def test_nvfp4_per_token(mx, orc, shape):
     assert np.array_equal(to_np(out["s2"]).view(np.uint32), st.view(np.uint32))
 
 
+def e4m3_tie_tensor(seed, T, H, per_tensor):
+    """Blocks whose scale quotient amax_b / 6 / S lands exactly on an E4M3 rounding midpoint (and one BF16
+    step either side of it): S is a power of two (token or tensor amax 2688 * 2^k), so the quotient is
+    exact, and the device's fast block-scale path must hand these blocks to the IEEE divisions."""
+    rng = np.random.default_rng(seed)
+    e4 = np.array([(1 + i / 8) * 2.0 ** e for e in range(-6, 9) for i in range(8)] + [i * 2.0 ** -9 for i in range(1, 8)])
+    e4 = np.unique(e4[e4 <= 448])
+    mids = (e4[:-1] + e4[1:]) / 2                                   # all exactly representable
+    x = np.zeros((T, H), dtype=np.float32)
+    k_all = rng.integers(-20, 20)
+    for t in range(T):
+        k = k_all if per_tensor else rng.integers(-20, 20)
+        for b in range(H // 16):
+            blk = x[t, 16 * b:16 * b + 16]
+            if b == 0:
+                amax = 2688.0 * 2.0 ** k                            # the token (tensor) maximum: S = 2^k
+            else:
+                m = mids[rng.integers(0, mids.size)] * 6.0 * 2.0 ** k
+                step = rng.integers(-1, 2)                          # on the midpoint or one BF16 step off
+                amax = float(np.float32(m)) * (1 + step * 2.0 ** -7)
+            blk[:] = rng.uniform(-1, 1, 16).astype(np.float32) * amax * 0.9
+            blk[rng.integers(0, 16)] = amax * rng.choice([-1.0, 1.0])
+    u = x.view(np.uint32)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def test_nvfp4_block_scale_ties(mx, orc):
+    """Block scales at E4M3 rounding midpoints take the exact path on the device, per token and per tensor."""
+    T, H = 96, 256
+    x = e4m3_tie_tensor(11, T, H, per_tensor=False)
+    out = mx.alloc_nvfp4_rows(T, H, DEV)
+    mx.mx_nvfp4_quantize_per_token(bf16_dev(x), out["q"], out["s"], out["s2"])
+    q, s, st = orc.nvfp4_quantize_per_token(x)
+    assert np.array_equal(to_np(out["q"]), q), first_mismatch(to_np(out["q"]), q)
+    assert np.array_equal(to_np(out["s"]), orc.scales_to_gemm_layout(s))
+    xt = e4m3_tie_tensor(12, T, H, per_tensor=True)
+    qd = torch.empty((T, H // 2), dtype=torch.uint8, device=DEV)
+    sd = torch.empty(mx.scale_bytes(T, H, 16), dtype=torch.uint8, device=DEV)
+    S = torch.empty(1, dtype=torch.float32, device=DEV)
+    ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+    mx.mx_nvfp4_quantize_1x16(bf16_dev(xt), False, False, 0, False, 0, qd, sd, S, ws)
+    qo, so, So = orc.nvfp4_quantize_1x16(xt, colwise=False)
+    assert to_np(S)[0] == So
+    assert np.array_equal(to_np(qd), qo), first_mismatch(to_np(qd), qo)
+    assert np.array_equal(to_np(sd), orc.scales_to_gemm_layout(so))
+
+
 def test_nvfp4_per_token_moe_gather_commutes(mx, orc):
     """quantize(gather(X)) == gather(quantize(X)) on the device (per-token scaling)."""
     d = synthetic.moe(tokens=256, hidden=512, ffn=128, experts=16, topk=4, with_weights=False)
