@@ -235,11 +235,25 @@ __host__ __device__ __forceinline__ int64_t sf_col_tiles(int64_t k, int block) {
     return (k / block + 3) / 4;
 }
 
-// Max of |bf16| over the two halves of each word, as 16-bit integers (NaN-free inputs).
+// Running max of |bf16| over the two halves of each word in one instruction (max.xorsign.abs: BF16 has
+// no flush-to-zero, so subnormals compare exactly; NaN inputs are skipped as in fmax).  The sign bits
+// of the result are meaningless: read it through fold_halves or abs_halves.
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(acc), "r"(w));
+    return d;
+}
+// The same on the integer pipe (mask, then unsigned 16-bit max; exact magnitudes in the halves), for
+// kernels whose floating-point pipe is the busier one.
+__device__ __forceinline__ uint32_t absmax_bf16x2_int(uint32_t acc, uint32_t w) {
     return __vmaxu2(acc, w & 0x7FFF7FFFu);
 }
-__device__ __forceinline__ uint32_t fold_halves(uint32_t m2) { return max(m2 & 0xFFFFu, m2 >> 16); }
+__device__ __forceinline__ uint32_t abs_halves(uint32_t m2) { return m2 & 0x7FFF7FFFu; }
+// The larger magnitude of the two halves, as BF16 bits in the low 16 bits.
+__device__ __forceinline__ uint32_t fold_halves(uint32_t m2) {
+    m2 = abs_halves(m2);
+    return max(m2 & 0xFFFFu, m2 >> 16);
+}
 
 // ---------------------------------------------------------------------------------------------
 // Expert-group tables for the grouped scale layout: group g's rows [off[g], off[g+1]) start at

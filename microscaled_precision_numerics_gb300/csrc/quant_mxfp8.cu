@@ -35,20 +35,12 @@ __device__ __forceinline__ uint32_t e8m0_from_amax_bits(uint32_t amax16) {
 // 2^-e for scale byte s (e = s - 127): exponent field 254 - s, always a normal FP32.
 __device__ __forceinline__ float inv_scale_from_e8m0(uint32_t s) { return __uint_as_float((254u - s) << 23); }
 
-// max(|a|, |b|) of each BF16 half of two packed pairs in one instruction; the sign bits of the result
-// are meaningless (masked once at the end of a reduction).
-__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
 // Quantize 32 BF16 values held as 16 packed words; writes 32 code bytes into out[8] words.
 __device__ __forceinline__ uint32_t mxfp8_block32(const uint32_t w[16], uint32_t out[8]) {
-    uint32_t m2 = max_abs_bf16x2(w[0], w[1]);
+    uint32_t m2 = absmax_bf16x2(w[0], w[1]);
 #pragma unroll
-    for (int i = 2; i < 16; ++i) m2 = max_abs_bf16x2(m2, w[i]);
-    const uint32_t s = e8m0_from_amax_bits(fold_halves(m2 & 0x7FFF7FFFu));
+    for (int i = 2; i < 16; ++i) m2 = absmax_bf16x2(m2, w[i]);
+    const uint32_t s = e8m0_from_amax_bits(fold_halves(m2));
     const float f = inv_scale_from_e8m0(s);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -228,13 +220,13 @@ mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t*
             uint32_t m[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
 #pragma unroll
             for (int i = 1; i < 8; ++i) {
-                m[0] = max_abs_bf16x2(m[0], v[i].x); m[1] = max_abs_bf16x2(m[1], v[i].y);
-                m[2] = max_abs_bf16x2(m[2], v[i].z); m[3] = max_abs_bf16x2(m[3], v[i].w);
+                m[0] = absmax_bf16x2(m[0], v[i].x); m[1] = absmax_bf16x2(m[1], v[i].y);
+                m[2] = absmax_bf16x2(m[2], v[i].z); m[3] = absmax_bf16x2(m[3], v[i].w);
             }
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                m[kk] = max_abs_bf16x2(m[kk], __shfl_xor_sync(0xFFFFFFFFu, m[kk], 8));
-                m[kk] = max_abs_bf16x2(m[kk], __shfl_xor_sync(0xFFFFFFFFu, m[kk], 16)) & 0x7FFF7FFFu;
+                m[kk] = absmax_bf16x2(m[kk], __shfl_xor_sync(0xFFFFFFFFu, m[kk], 8));
+                m[kk] = abs_halves(absmax_bf16x2(m[kk], __shfl_xor_sync(0xFFFFFFFFu, m[kk], 16)));
             }
             const int64_t rbase = r0 + rb * 32;
             const bool rows_ok = rbase < R;

@@ -414,9 +414,11 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
 #pragma unroll
     for (int jp = 0; jp < CPT / 2; ++jp) {
         if (RHT) rht16_pair_inplace<CPT / 2>(xw, jp, signmask);
+        // block maxima of both columns over the 16 packed words (integer pipe: the transform keeps the
+        // floating-point pipe busy here)
         uint32_t m2 = 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) m2 = absmax_bf16x2(m2, xw[i][jp]);
+        for (int i = 0; i < 16; ++i) m2 = absmax_bf16x2_int(m2, xw[i][jp]);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int j = 2 * jp + h;

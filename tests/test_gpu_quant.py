@@ -175,6 +175,34 @@ def e4m3_tie_tensor(seed, T, H, per_tensor):
     return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
 
 
+def test_nvfp4_subnormal_tokens_and_blocks(mx, orc):
+    """Tokens made only of BF16 subnormals (so S, the block scales and every maximum come from subnormal
+    values) and subnormal-only blocks inside ordinary tokens, per token and per tensor."""
+    T, H = 64, 128
+    rng = np.random.default_rng(21)
+    x = synthetic.random_bf16(22, (T, H), "normal")
+    sub = (rng.integers(1, 128, size=(T, H)) | (rng.integers(0, 2, size=(T, H)) << 15)).astype(np.uint16)
+    x[::3] = sub[::3]                                   # whole tokens of subnormals
+    x[1::3, 16:32] = sub[1::3, 16:32]                   # one subnormal-only block in other tokens
+    out = mx.alloc_nvfp4_rows(T, H, DEV)
+    mx.mx_nvfp4_quantize_per_token(bf16_dev(x), out["q"], out["s"], out["s2"])
+    q, s, st = orc.nvfp4_quantize_per_token(x)
+    assert np.array_equal(to_np(out["q"]), q), first_mismatch(to_np(out["q"]), q)
+    assert np.array_equal(to_np(out["s"]), orc.scales_to_gemm_layout(s))
+    assert np.array_equal(to_np(out["s2"]).view(np.uint32), st.view(np.uint32))
+    xs = np.ascontiguousarray(sub)                      # a whole tensor of subnormals, row- and column-wise
+    for colwise in (False, True):
+        qd = torch.empty((H, T // 2) if colwise else (T, H // 2), dtype=torch.uint8, device=DEV)
+        sd = torch.empty(mx.scale_bytes(H, T, 16) if colwise else mx.scale_bytes(T, H, 16), dtype=torch.uint8, device=DEV)
+        S = torch.empty(1, dtype=torch.float32, device=DEV)
+        ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+        mx.mx_nvfp4_quantize_1x16(bf16_dev(xs), colwise, False, 0, False, 0, qd, sd, S, ws)
+        qo, so, So = orc.nvfp4_quantize_1x16(xs, colwise=colwise)
+        assert to_np(S).view(np.uint32)[0] == np.float32(So).view(np.uint32)
+        assert np.array_equal(to_np(qd), qo), first_mismatch(to_np(qd), qo)
+        assert np.array_equal(to_np(sd), orc.scales_to_gemm_layout(so))
+
+
 def test_nvfp4_block_scale_ties(mx, orc):
     """Block scales at E4M3 rounding midpoints take the exact path on the device, per token and per tensor."""
     T, H = 96, 256
