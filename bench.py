@@ -614,8 +614,10 @@ class DenseNVFP4:
 class WeightSync:
     """Weight-sync sweep: 48 layers of 128 experts x {2048x768, 768x2048, 768x2048}; per matrix
     stack MXFP8 row+col quantize, dequantize, re-quantize and byte compare; NVFP4 2D quantize,
-    dequantize, re-quantize and byte compare.  One layer's weights are drawn on the device per step
-    (torch generator seeded 1000 + layer) outside the timed kernels."""
+    dequantize, re-quantize and byte compare.  The per-matrix maxima that the NVFP4 2D quantizer needs
+    come from the calls that already read the values (the MXFP8 quantize of the weights, the NVFP4
+    dequantize for the re-quantize), so the 2D quantizer reads its input once.  One layer's weights are
+    drawn on the device per step (torch generator seeded 1000 + layer) outside the timed kernels."""
     name = "weight_sync"
 
     def __init__(self, mx, torch, dev, layers=48, experts=128):
@@ -628,10 +630,12 @@ class WeightSync:
             b = {"w": torch.empty((G, O, H), dtype=torch.bfloat16, device=dev),
                  "m8": mx.alloc_mxfp8(G * O, H, dev), "m8b": mx.alloc_mxfp8(G * O, H, dev, colwise=False),
                  "n4": mx.alloc_nvfp4_weight_2d(G, O, H, dev), "n4b": mx.alloc_nvfp4_weight_2d(G, O, H, dev),
-                 "y": torch.empty((G * O, H), dtype=torch.bfloat16, device=dev)}
+                 "y": torch.empty((G * O, H), dtype=torch.bfloat16, device=dev),
+                 "amax_w": torch.empty(G, dtype=torch.int32, device=dev), "amax_y": torch.empty(G, dtype=torch.int32, device=dev)}
             self.bufs.append(b)
         self.count = torch.zeros(1, dtype=torch.int64, device=dev)
-        self.launches_per_step = 3 * (2 + 1 + 1 + 2 + 1 + 2 + 2 + 3)
+        # per shape: Q, DQ, re-Q, 2 compares (MXFP8); Q, DQ, re-Q, 3 compares (NVFP4 2D)
+        self.launches_per_step = 3 * (1 + 1 + 1 + 2 + 1 + 1 + 1 + 3)
 
     def draw(self, layer):
         gen = self.torch.Generator(device=self.dev)
@@ -648,7 +652,8 @@ class WeightSync:
             m8, m8b, n4, n4b = b["m8"], b["m8b"], b["n4"], b["n4b"]
             w2 = b["w"].view(R, H)
             out += [
-                ("quant", f"mxfp8 Q {O}x{H}", 1, n * (2 + 2 + 2 / 32), lambda w2=w2, m8=m8: mx.mx_quantize_mxfp8(w2, **m8)),
+                ("quant", f"mxfp8 Q {O}x{H} (+ matrix maxima)", 1, n * (2 + 2 + 2 / 32),
+                 lambda w2=w2, m8=m8, b=b, O=O: mx.mx_quantize_mxfp8_amax(w2, O, b["amax_w"], **m8)),
                 ("dq", f"mxfp8 DQ {O}x{H}", 1, n * (1 + 1 / 32 + 2),
                  lambda m8=m8, b=b, R=R, H=H: mx.mx_dequantize_bf16(mx.MX_FMT_MXFP8, m8["q_row"], m8["s_row"], None, 0, R, H, b["y"])),
                 ("quant", f"mxfp8 re-Q {O}x{H}", 1, n * (2 + 1 + 1 / 32), lambda b=b, m8b=m8b: mx.mx_quantize_mxfp8(b["y"], **m8b)),
@@ -656,14 +661,14 @@ class WeightSync:
                  lambda m8=m8, m8b=m8b: (mx.mx_count_mismatch(m8["q_row"], m8b["q_row"], self.count),
                                          mx.mx_count_mismatch(m8["s_row"], m8b["s_row"], self.count))),
                 ("quant", f"nvfp4 2D Q {O}x{H}", 1, n * (2 + 1 + 2 / 16),
-                 lambda b=b, n4=n4: mx.mx_nvfp4_quantize_weight_2d(b["w"], n4["q_row"], n4["s_row"], n4["q_col"], n4["s_col"],
-                                                                    n4["s_w"], n4["ws"])),
-                ("dq", f"nvfp4 DQ {O}x{H}", 1, n * (0.5 + 1 / 16 + 2),
-                 lambda n4=n4, b=b, R=R, H=H, O=O: mx.mx_dequantize_bf16(mx.MX_FMT_NVFP4, n4["q_row"], n4["s_row"], n4["s_w"],
-                                                                       mx.MX_SCOPE_GROUP, R, H, b["y"], group_rows=O)),
+                 lambda b=b, n4=n4: mx.mx_nvfp4_quantize_weight_2d_given_amax(b["w"], n4["q_row"], n4["s_row"], n4["q_col"],
+                                                                               n4["s_col"], n4["s_w"], b["amax_w"])),
+                ("dq", f"nvfp4 DQ {O}x{H} (+ matrix maxima)", 1, n * (0.5 + 1 / 16 + 2),
+                 lambda n4=n4, b=b, R=R, H=H, O=O: mx.mx_dequantize_nvfp4_amax(n4["q_row"], n4["s_row"], n4["s_w"], O, R, H,
+                                                                             b["y"], b["amax_y"])),
                 ("quant", f"nvfp4 2D re-Q {O}x{H}", 1, n * (2 + 1 + 2 / 16),
-                 lambda b=b, n4b=n4b, G=G, O=O, H=H: mx.mx_nvfp4_quantize_weight_2d(b["y"].view(G, O, H), n4b["q_row"], n4b["s_row"],
-                                                                                   n4b["q_col"], n4b["s_col"], n4b["s_w"], n4b["ws"])),
+                 lambda b=b, n4b=n4b, G=G, O=O, H=H: mx.mx_nvfp4_quantize_weight_2d_given_amax(
+                     b["y"].view(G, O, H), n4b["q_row"], n4b["s_row"], n4b["q_col"], n4b["s_col"], n4b["s_w"], b["amax_y"])),
                 ("cmp", f"nvfp4 compare {O}x{H}", 1, 2 * n * (0.5 + 0.5 + 2 / 16),
                  lambda n4=n4, n4b=n4b: (mx.mx_count_mismatch(n4["q_row"], n4b["q_row"], self.count),
                                          mx.mx_count_mismatch(n4["q_col"], n4b["q_col"], self.count),
@@ -673,7 +678,8 @@ class WeightSync:
 
     def config(self):
         return {"workload": "weight_sync: 48 layers x 128 experts x {2048x768, 768x2048, 768x2048}, MXFP8 + NVFP4-2D "
-                            "quantize, dequantize, re-quantize, byte compare", "layers": self.layers}
+                            "quantize, dequantize, re-quantize, byte compare (matrix maxima carried into the 2D quantizer)",
+                "layers": self.layers}
 
 
 def max_over_ranks(x: float, dist=None, device=None) -> float:

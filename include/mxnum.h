@@ -360,6 +360,34 @@ mx_status mx_grouped_scaled_gemm(mx_format fmt, int64_t G, const int64_t* group_
 mx_status mx_count_mismatch(const uint8_t* x, const uint8_t* y, int64_t nbytes,
                             unsigned long long* count, cudaStream_t stream);
 
+/* The weight-sync sweep (E2E page abstract and Table 11: synchronized weights quantized to MXFP8 and
+ * NVFP4-2D, dequantized and re-quantized, compared byte for byte) reads each weight stack for its
+ * MXFP8 quantization and again, twice, for the NVFP4 2D quantization (whose per-matrix second-level
+ * scale needs the matrix maximum first).  These three calls carry that maximum from the pass that
+ * already reads the values to the 2D quantizer, which then reads the weights once.  Maxima are
+ * 32-bit words holding the BF16 bits of max |x| in the high half (low half zero); DEVICE arrays of
+ * one word per matrix, written (not accumulated) by the producing call.
+ *
+ * mx_quantize_mxfp8 of a stack of matrices [rows = G * matrix_rows, cols], row-wise output required
+ * (column-wise optional), plus amax[g] = max |x| over matrix g.  matrix_rows % 128 == 0 and
+ * rows % matrix_rows == 0; otherwise the rules of mx_quantize_mxfp8. */
+mx_status mx_quantize_mxfp8_amax(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                 uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                 int64_t matrix_rows, uint32_t* amax, cudaStream_t stream);
+
+/* mx_nvfp4_quantize_weight_2d with each matrix's maximum supplied (amax[g], as above) instead of
+ * measured: identical results when amax[g] is the true max |w_g|, and one read of the weights. */
+mx_status mx_nvfp4_quantize_weight_2d_given_amax(const void* w, int64_t G, int64_t O, int64_t H,
+                                                 uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                                                 uint8_t* s_col, float* s_w, const uint32_t* amax,
+                                                 cudaStream_t stream);
+
+/* mx_dequantize_bf16 of NVFP4 with one second-level scale per group of group_rows rows
+ * (MX_SCOPE_GROUP), plus amax[g] = max |y| over group g of the BF16 output.  group_rows % 128 == 0,
+ * rows % group_rows == 0, cols % 16 == 0. */
+mx_status mx_dequantize_nvfp4_amax(const uint8_t* q, const uint8_t* s, const float* s2, int64_t group_rows,
+                                   int64_t rows, int64_t cols, void* y, uint32_t* amax, cudaStream_t stream);
+
 /* Workspace sizes (bytes) for the ops that take one. */
 typedef enum { MX_WS_WEIGHT_2D = 0, MX_WS_1X16 = 1 } mx_workspace_op;
 size_t mx_workspace_bytes(mx_workspace_op op, int64_t groups, int64_t unused);

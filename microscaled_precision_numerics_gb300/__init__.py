@@ -48,6 +48,9 @@ def lib() -> ctypes.CDLL:
                 "mx_workspace_bytes": (SZ, [I32, I64, I64]),
                 "mx_quantize_mxfp8": (I32, [P, I64, I64, I64, P, P, P, P, P]),
                 "mx_quantize_mxfp8_batched": (I32, [P, I32, P]),
+                "mx_quantize_mxfp8_amax": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, P]),
+                "mx_nvfp4_quantize_weight_2d_given_amax": (I32, [P, I64, I64, I64, P, P, P, P, P, P, P]),
+                "mx_dequantize_nvfp4_amax": (I32, [P, P, P, I64, I64, I64, P, P, P]),
                 "mx_nvfp4_quantize_per_token": (I32, [P, I64, I64, I64, P, P, P, P]),
                 "mx_nvfp4_quantize_per_token_46": (I32, [P, I64, I64, I64, P, P, P, P]),
                 "mx_nvfp4_quantize_per_token_grouped": (I32, [P, I64, I64, I64, I64, P, P, P, P, P]),
@@ -148,6 +151,27 @@ def mx_quantize_mxfp8_batched(jobs, stream=None):
                               _p(out.get("q_col")), _p(out.get("s_col")))
     _check("mx_quantize_mxfp8_batched", lib().mx_quantize_mxfp8_batched(ctypes.cast(arr, ctypes.c_void_p),
                                                                         len(jobs), _stream(stream)))
+
+
+def mx_quantize_mxfp8_amax(x, matrix_rows: int, amax, q_row=None, s_row=None, q_col=None, s_col=None, stream=None):
+    """mx_quantize_mxfp8 of stacked matrices plus each matrix's max |x| (int32 words, BF16 bits << 16)."""
+    x = _bf16_bits(x)
+    rows, cols = x.shape
+    _check("mx_quantize_mxfp8_amax", lib().mx_quantize_mxfp8_amax(
+        _p(x), rows, cols, x.stride(0), _p(q_row), _p(s_row), _p(q_col), _p(s_col), matrix_rows, _p(amax),
+        _stream(stream)))
+
+
+def mx_nvfp4_quantize_weight_2d_given_amax(w, q_row, s_row, q_col, s_col, s_w, amax, stream=None):
+    w = _bf16_bits(w)
+    G, O, H = w.shape
+    _check("mx_nvfp4_quantize_weight_2d_given_amax", lib().mx_nvfp4_quantize_weight_2d_given_amax(
+        _p(w), G, O, H, _p(q_row), _p(s_row), _p(q_col), _p(s_col), _p(s_w), _p(amax), _stream(stream)))
+
+
+def mx_dequantize_nvfp4_amax(q, s, s2, group_rows: int, rows: int, cols: int, y, amax, stream=None):
+    _check("mx_dequantize_nvfp4_amax", lib().mx_dequantize_nvfp4_amax(
+        _p(q), _p(s), _p(s2), group_rows, rows, cols, _p(y), _p(amax), _stream(stream)))
 
 
 def mx_nvfp4_quantize_per_token(x, q, s, s_tok, stream=None):

@@ -28,6 +28,9 @@ struct Mx8Tensor {
 constexpr int MX8_MAX_BATCH = 4;
 // Several tensors in one launch; all of them must request the same orientations.
 cudaError_t launch_mxfp8_quantize_batched(const Mx8Tensor* ts, int n, cudaStream_t stream);
+// One tensor of stacked matrices (matrix_rows rows each, a multiple of 128), row-wise output required;
+// also writes each matrix's max |x| (BF16 bits << 16) to amax.
+cudaError_t launch_mxfp8_quantize_amax(const Mx8Tensor& t, int64_t matrix_rows, uint32_t* amax, cudaStream_t stream);
 cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q_row,
                                   uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int G, const int64_t* group_offsets,
                                   cudaStream_t stream);
@@ -87,6 +90,11 @@ struct BwGemmArgs {
     uint16_t* d; int64_t ldd;
 };
 cudaError_t launch_fp8_blockwise_gemm(const BwGemmArgs& args, int num_sms, cudaStream_t stream);
+cudaError_t launch_nvfp4_weight_2d_given_amax(const uint16_t* w, int64_t G, int64_t O, int64_t H, uint8_t* q_row,
+                                              uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, float* s_w,
+                                              const uint32_t* amax, cudaStream_t stream);
+cudaError_t launch_dequant_nvfp4_amax(const uint8_t* q, const uint8_t* s, const float* s2, int64_t group_rows, int64_t R,
+                                      int64_t K, uint16_t* y, uint32_t* amax, cudaStream_t stream);
 uint32_t read_and_clear_device_status();
 uint32_t read_and_clear_mxfp8_status();
 

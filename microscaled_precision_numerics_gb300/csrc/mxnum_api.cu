@@ -85,6 +85,17 @@ mx_status mx_quantize_mxfp8(const void* x, int64_t rows, int64_t cols, int64_t l
                                                  q_col, s_col, 0, nullptr, stream));
 }
 
+mx_status mx_quantize_mxfp8_amax(const void* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q_row, uint8_t* s_row,
+                                 uint8_t* q_col, uint8_t* s_col, int64_t matrix_rows, uint32_t* amax, cudaStream_t stream) {
+    const mx_status st = check_mxfp8_args(x, rows, cols, ldx, q_row, s_row, q_col, s_col);
+    if (st != MX_OK) return st;
+    if (!q_row || !amax || matrix_rows <= 0) return MX_ERR_INVALID_ARG;
+    if (!aligned16(amax)) return MX_ERR_ALIGNMENT;
+    if ((matrix_rows % 128) != 0 || (rows % matrix_rows) != 0) return MX_ERR_UNSUPPORTED;
+    const mxk::Mx8Tensor t{static_cast<const uint16_t*>(x), rows, cols, ldx, q_row, s_row, q_col, s_col};
+    return from_cuda(mxk::launch_mxfp8_quantize_amax(t, matrix_rows, amax, stream));
+}
+
 mx_status mx_quantize_mxfp8_batched(const mx_mxfp8_tensor* tensors, int count, cudaStream_t stream) {
     static_assert(MX_MXFP8_MAX_BATCH == mxk::MX8_MAX_BATCH, "batch limit");
     if (!tensors || count < 1 || count > MX_MXFP8_MAX_BATCH) return MX_ERR_INVALID_ARG;
@@ -261,6 +272,28 @@ mx_status mx_dequantize_bf16(mx_format fmt, const uint8_t* q, const uint8_t* s, 
     }
     return from_cuda(mxk::launch_dequant(fmt == MX_FMT_MXFP8 ? 0 : 1, q, s, s2, per, rows, cols,
                                          static_cast<uint16_t*>(y), stream));
+}
+
+mx_status mx_nvfp4_quantize_weight_2d_given_amax(const void* w, int64_t G, int64_t O, int64_t H, uint8_t* q_row,
+                                                 uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, float* s_w,
+                                                 const uint32_t* amax, cudaStream_t stream) {
+    if (!w || !q_row || !s_row || !q_col || !s_col || !s_w || !amax) return MX_ERR_INVALID_ARG;
+    if (G <= 0 || O <= 0 || H <= 0) return MX_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q_row) || !aligned16(s_row) || !aligned16(q_col) || !aligned16(s_col) ||
+        !aligned16(s_w) || !aligned16(amax))
+        return MX_ERR_ALIGNMENT;
+    if ((O % 16) != 0 || (H % 16) != 0) return MX_ERR_UNSUPPORTED;
+    return from_cuda(mxk::launch_nvfp4_weight_2d_given_amax(static_cast<const uint16_t*>(w), G, O, H, q_row, s_row,
+                                                            q_col, s_col, s_w, amax, stream));
+}
+
+mx_status mx_dequantize_nvfp4_amax(const uint8_t* q, const uint8_t* s, const float* s2, int64_t group_rows,
+                                   int64_t rows, int64_t cols, void* y, uint32_t* amax, cudaStream_t stream) {
+    if (!q || !s || !s2 || !y || !amax || rows <= 0 || cols <= 0 || group_rows <= 0) return MX_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(y) || !aligned16(amax)) return MX_ERR_ALIGNMENT;
+    if ((cols % 16) != 0 || (group_rows % 128) != 0 || (rows % group_rows) != 0) return MX_ERR_UNSUPPORTED;
+    return from_cuda(mxk::launch_dequant_nvfp4_amax(q, s, s2, group_rows, rows, cols, static_cast<uint16_t*>(y), amax,
+                                                    stream));
 }
 
 static mx_status validate_gemm_common(mx_format fmt, const uint8_t* a, const uint8_t* sa, const uint8_t* b,

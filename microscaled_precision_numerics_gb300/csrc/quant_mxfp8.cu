@@ -36,11 +36,12 @@ __device__ __forceinline__ uint32_t e8m0_from_amax_bits(uint32_t amax16) {
 __device__ __forceinline__ float inv_scale_from_e8m0(uint32_t s) { return __uint_as_float((254u - s) << 23); }
 
 // Quantize 32 BF16 values held as 16 packed words; writes 32 code bytes into out[8] words.
-__device__ __forceinline__ uint32_t mxfp8_block32(const uint32_t w[16], uint32_t out[8]) {
+__device__ __forceinline__ uint32_t mxfp8_block32(const uint32_t w[16], uint32_t out[8], uint32_t& amax16) {
     uint32_t m2 = absmax_bf16x2(w[0], w[1]);
 #pragma unroll
     for (int i = 2; i < 16; ++i) m2 = absmax_bf16x2(m2, w[i]);
-    const uint32_t s = e8m0_from_amax_bits(fold_halves(m2));
+    amax16 = fold_halves(m2);
+    const uint32_t s = e8m0_from_amax_bits(amax16);
     const float f = inv_scale_from_e8m0(s);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -74,6 +75,8 @@ struct alignas(64) Mx8Params {
     uint8_t* s_row[MX8_MAX_BATCH];
     uint8_t* q_col[MX8_MAX_BATCH];
     uint8_t* s_col[MX8_MAX_BATCH];
+    uint32_t* amax;           // optional (one tensor): per-matrix max |x| as BF16 bits << 16
+    int64_t matrix_rows;      // rows per matrix for `amax` (a multiple of 128)
     int n;
 };
 
@@ -117,6 +120,7 @@ mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t*
     uint8_t (*colsc)[QT_COLS] = reinterpret_cast<uint8_t (*)[QT_COLS]>(qsm + QT_NST * QT_TILE_BYTES);
     uint64_t* bars = reinterpret_cast<uint64_t*>(qsm + QT_NST * QT_TILE_BYTES + 4 * QT_COLS);   // full[3], empty[3]
     int* abort_flag = reinterpret_cast<int*>(bars + 2 * QT_NST);
+    __shared__ uint32_t tile_amax[2];                       // per-tile maxima (optional output), by tile parity
     // expert-group tables (grouped row-wise scale layout)
     int64_t* s_off = reinterpret_cast<int64_t*>(qsm + QT_NST * QT_TILE_BYTES + 4 * QT_COLS + 64);
     int* s_ptile = reinterpret_cast<int*>(s_off + (G + 1));
@@ -128,6 +132,7 @@ mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t*
             mbar_init(empty0 + 8 * st, 1);
         }
         *abort_flag = 0;
+        tile_amax[0] = tile_amax[1] = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (GROUPED) load_group_tables(group_offsets, G, s_off, s_ptile, s_warp);
@@ -177,7 +182,7 @@ mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t*
             const int half = (tid >> 3) & 1;
             const int rr = (tid & 7) + 8 * (tid >> 4);
             const int64_t r = r0 + rr;
-            uint32_t s2[2];
+            uint32_t s2[2], am = 0;
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
                 uint32_t w[16];
@@ -186,14 +191,20 @@ mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t*
                     const uint4 v = *reinterpret_cast<const uint4*>(tile + qt_off(rr, half * 8 + b * 4 + i));
                     w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
                 }
-                uint32_t codes[8];
-                s2[b] = mxfp8_block32(w, codes);
+                uint32_t codes[8], a16;
+                s2[b] = mxfp8_block32(w, codes, a16);
+                am = max(am, a16);
                 const int64_t c = c0 + half * 64 + b * 32;
                 if (r < R && c < K) {
                     uint4* dst = reinterpret_cast<uint4*>(q_row + r * K + c);
                     __stcs(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
                     __stcs(dst + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
                 }
+            }
+            if (p.amax != nullptr) {
+                // the tile's maximum gathers in shared memory (one global atomic per tile, below)
+                am = __reduce_max_sync(0xFFFFFFFFu, am);
+                if (lane == 0) atomicMax(&tile_amax[k & 1], am);
             }
             // the row's 4 scales: this thread's two and those of lane + 8 (the other half)
             const uint32_t mine = s2[0] | (s2[1] << 8);
@@ -248,6 +259,12 @@ mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t*
         // both passes have read the stage: hand it back to the producer
         named_sync_consumers();
         if (tid == 0) mbar_arrive(empty0 + 8 * stage);
+        if (p.amax != nullptr && tid == 0) {
+            // the tile lies in one matrix (128-row tiles, matrices a multiple of 128 rows); this slot is
+            // next written two tiles on, after this thread has passed the next tile's barrier
+            if (ok && r0 < R) atomicMax(p.amax + r0 / p.matrix_rows, tile_amax[k & 1] << 16);
+            tile_amax[k & 1] = 0u;
+        }
         if (COL) {
             // one 32-bit word of 4 row-block scales per column (r0 / 32 is a multiple of 4)
             if (ok && tid < QT_COLS) {
@@ -292,8 +309,12 @@ static cudaError_t mx8_zero_padding(const Mx8Tensor& t, int G, cudaStream_t stre
     return cudaSuccess;
 }
 
-static cudaError_t launch_mx8(const Mx8Tensor* ts, int n, int G, const int64_t* group_offsets, cudaStream_t stream) {
+static cudaError_t launch_mx8(const Mx8Tensor* ts, int n, int G, const int64_t* group_offsets, cudaStream_t stream,
+                              uint32_t* amax = nullptr, int64_t matrix_rows = 0) {
     if (n < 1 || n > MX8_MAX_BATCH) return cudaErrorInvalidValue;
+    if (amax && (n != 1 || G > 0 || !ts[0].q_row || matrix_rows <= 0 || (matrix_rows % 128) != 0 ||
+                 (ts[0].R % matrix_rows) != 0))
+        return cudaErrorInvalidValue;
     const bool row = ts[0].q_row != nullptr, col = ts[0].q_col != nullptr;
     Mx8Params p;
     memset(&p, 0, sizeof(p));
@@ -312,9 +333,15 @@ static cudaError_t launch_mx8(const Mx8Tensor* ts, int n, int G, const int64_t* 
         p.tile_end[i] = tiles;
         p.q_row[i] = t.q_row; p.s_row[i] = t.s_row; p.q_col[i] = t.q_col; p.s_col[i] = t.s_col;
     }
+    p.amax = amax;
+    p.matrix_rows = matrix_rows;
     // every descriptor is valid: only now enqueue anything
     for (int i = 0; i < n; ++i) {
         cudaError_t e = mx8_zero_padding(ts[i], G, stream);
+        if (e != cudaSuccess) return e;
+    }
+    if (amax) {
+        cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(uint32_t) * (size_t)(ts[0].R / matrix_rows), stream);
         if (e != cudaSuccess) return e;
     }
     const size_t base = (size_t)QT_NST * QT_TILE_BYTES + 4 * QT_COLS + 64 + 1024;
@@ -353,6 +380,10 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t K, int64
 
 cudaError_t launch_mxfp8_quantize_batched(const Mx8Tensor* ts, int n, cudaStream_t stream) {
     return launch_mx8(ts, n, 0, nullptr, stream);
+}
+
+cudaError_t launch_mxfp8_quantize_amax(const Mx8Tensor& t, int64_t matrix_rows, uint32_t* amax, cudaStream_t stream) {
+    return launch_mx8(&t, 1, 0, nullptr, stream, amax, matrix_rows);
 }
 
 uint32_t read_and_clear_mxfp8_status() {

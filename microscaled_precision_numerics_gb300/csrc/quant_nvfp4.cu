@@ -762,6 +762,22 @@ cudaError_t launch_rht16(const uint16_t* x, int64_t T, int64_t N, uint64_t seed,
     return cudaGetLastError();
 }
 
+cudaError_t launch_nvfp4_weight_2d_given_amax(const uint16_t* w, int64_t G, int64_t O, int64_t H, uint8_t* q_row,
+                                              uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, float* s_w,
+                                              const uint32_t* amax, cudaStream_t stream) {
+    if ((O % 128) != 0 || ((H / 16) % 4) != 0) {
+        cudaError_t e = cudaMemsetAsync(s_row, 0, (size_t)(host_scale_bytes(O, H, 16) * G), stream);
+        if (e != cudaSuccess) return e;
+    }
+    if ((H % 128) != 0 || ((O / 16) % 4) != 0) {
+        cudaError_t e = cudaMemsetAsync(s_col, 0, (size_t)(host_scale_bytes(H, O, 16) * G), stream);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid((unsigned)((H + W2_COLS - 1) / W2_COLS), (unsigned)((O + W2_ROWS - 1) / W2_ROWS), (unsigned)G);
+    weight2d_quant_kernel<false><<<grid, 128, 0, stream>>>(w, O, H, amax, q_row, s_row, q_col, s_col, s_w);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_nvfp4_weight_2d(const uint16_t* w, int64_t G, int64_t O, int64_t H, uint8_t* q_row, uint8_t* s_row,
                                    uint8_t* q_col, uint8_t* s_col, float* s_w, uint32_t* ws, int num_sms,
                                    cudaStream_t stream, bool four_six) {

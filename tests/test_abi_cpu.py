@@ -26,7 +26,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for required in ["mx_quantize_mxfp8", "mx_quantize_mxfp8_batched", "mx_nvfp4_quantize_per_token", "mx_nvfp4_quantize_weight_2d", "mx_rht16",
+    for required in ["mx_quantize_mxfp8", "mx_quantize_mxfp8_batched", "mx_quantize_mxfp8_amax",
+                     "mx_nvfp4_quantize_weight_2d_given_amax", "mx_dequantize_nvfp4_amax", "mx_nvfp4_quantize_per_token", "mx_nvfp4_quantize_weight_2d", "mx_rht16",
                      "mx_nvfp4_quantize_1x16", "mx_dequantize_bf16", "mx_scaled_gemm", "mx_grouped_scaled_gemm",
                      "mx_fp8_blockwise_quantize_1x128", "mx_fp8_blockwise_quantize_128x128", "mx_gemm_bf16_dq_nvfp4",
                      "mx_wgrad_bf16_dq_nvfp4", "mx_fp8_blockwise_gemm"]:
@@ -89,6 +90,21 @@ def test_mxfp8_batched_validation(lib):
     assert call([both, row]) == 1                                       # mixed orientations
     assert call([both, bad]) == 2                                       # one descriptor misaligned
     assert call([both, _Mxfp8Tensor(0x10000, 32, 48, 48, 0x10000, 0x10000, 0x10000, 0x10000)]) == 3
+
+
+def test_fused_maxima_validation(lib):
+    f = lib.mx_quantize_mxfp8_amax
+    assert f(A16, 256, 64, 64, A16, A16, NUL, NUL, 128, NUL, NUL) == 1          # no maxima buffer
+    assert f(A16, 256, 64, 64, NUL, NUL, A16, A16, 128, A16, NUL) == 1          # row-wise output required
+    assert f(A16, 256, 64, 64, A16, A16, NUL, NUL, 96, A16, NUL) == 3           # matrix_rows % 128
+    assert f(A16, 384, 64, 64, A16, A16, NUL, NUL, 256, A16, NUL) == 3          # rows % matrix_rows
+    assert f(A16, 256, 64, 64, A16, A16, NUL, NUL, 128, A8, NUL) == 2           # misaligned maxima
+    g = lib.mx_nvfp4_quantize_weight_2d_given_amax
+    assert g(A16, 2, 32, 32, A16, A16, A16, A16, A16, NUL, NUL) == 1
+    assert g(A16, 2, 24, 32, A16, A16, A16, A16, A16, A16, NUL) == 3            # O % 16
+    d = lib.mx_dequantize_nvfp4_amax
+    assert d(A16, A16, A16, 128, 256, 64, A16, NUL, NUL) == 1
+    assert d(A16, A16, A16, 64, 256, 64, A16, A16, NUL) == 3                    # group_rows % 128
 
 
 def test_nvfp4_validation(lib):

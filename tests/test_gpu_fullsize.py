@@ -260,7 +260,8 @@ def test_wgrad_fullsize_sampled(mx, orc):
 # weight_sync: Q -> DQ -> re-Q byte identity on sampled layers, and codes vs the oracle
 # ------------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("layer", [0, 47])
-def test_weight_sync_layer(mx, orc, layer):
+@pytest.mark.parametrize("fused", [False, True])
+def test_weight_sync_layer(mx, orc, layer, fused):
     d = synthetic.weight_sync_layer(layer)
     cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
     for name in ("down", "gate", "up"):
@@ -268,7 +269,11 @@ def test_weight_sync_layer(mx, orc, layer):
         G, O, H = w.shape
         wd = bf16_dev(w)
         m8 = mx.alloc_mxfp8(G * O, H, DEV)
-        mx.mx_quantize_mxfp8(wd.view(G * O, H), **m8)
+        amax_w = torch.empty(G, dtype=torch.int32, device=DEV)
+        if fused:
+            mx.mx_quantize_mxfp8_amax(wd.view(G * O, H), O, amax_w, **m8)
+        else:
+            mx.mx_quantize_mxfp8(wd.view(G * O, H), **m8)
         y = torch.empty((G * O, H), dtype=torch.bfloat16, device=DEV)
         mx.mx_dequantize_bf16(mx.MX_FMT_MXFP8, m8["q_row"], m8["s_row"], None, 0, G * O, H, y)
         m8b = mx.alloc_mxfp8(G * O, H, DEV, colwise=False)
@@ -276,13 +281,22 @@ def test_weight_sync_layer(mx, orc, layer):
         mx.mx_count_mismatch(m8["q_row"], m8b["q_row"], cnt)
         mx.mx_count_mismatch(m8["s_row"], m8b["s_row"], cnt)
         n4 = mx.alloc_nvfp4_weight_2d(G, O, H, DEV)
-        mx.mx_nvfp4_quantize_weight_2d(wd, n4["q_row"], n4["s_row"], n4["q_col"], n4["s_col"], n4["s_w"], n4["ws"])
         y2 = torch.empty((G * O, H), dtype=torch.bfloat16, device=DEV)
-        mx.mx_dequantize_bf16(mx.MX_FMT_NVFP4, n4["q_row"], n4["s_row"], n4["s_w"], mx.MX_SCOPE_GROUP, G * O, H, y2,
-                              group_rows=O)
         n4b = mx.alloc_nvfp4_weight_2d(G, O, H, DEV)
-        mx.mx_nvfp4_quantize_weight_2d(y2.view(G, O, H), n4b["q_row"], n4b["s_row"], n4b["q_col"], n4b["s_col"],
-                                       n4b["s_w"], n4b["ws"])
+        if fused:
+            # the maxima carried from the MXFP8 quantize and the NVFP4 dequantize (the weight-sync bench's chain)
+            amax_y = torch.empty(G, dtype=torch.int32, device=DEV)
+            mx.mx_nvfp4_quantize_weight_2d_given_amax(wd, n4["q_row"], n4["s_row"], n4["q_col"], n4["s_col"], n4["s_w"],
+                                                      amax_w)
+            mx.mx_dequantize_nvfp4_amax(n4["q_row"], n4["s_row"], n4["s_w"], O, G * O, H, y2, amax_y)
+            mx.mx_nvfp4_quantize_weight_2d_given_amax(y2.view(G, O, H), n4b["q_row"], n4b["s_row"], n4b["q_col"],
+                                                      n4b["s_col"], n4b["s_w"], amax_y)
+        else:
+            mx.mx_nvfp4_quantize_weight_2d(wd, n4["q_row"], n4["s_row"], n4["q_col"], n4["s_col"], n4["s_w"], n4["ws"])
+            mx.mx_dequantize_bf16(mx.MX_FMT_NVFP4, n4["q_row"], n4["s_row"], n4["s_w"], mx.MX_SCOPE_GROUP, G * O, H, y2,
+                                  group_rows=O)
+            mx.mx_nvfp4_quantize_weight_2d(y2.view(G, O, H), n4b["q_row"], n4b["s_row"], n4b["q_col"], n4b["s_col"],
+                                           n4b["s_w"], n4b["ws"])
         for k in ("q_row", "s_row", "q_col", "s_col"):
             mx.mx_count_mismatch(n4[k], n4b[k], cnt)
         torch.cuda.synchronize()

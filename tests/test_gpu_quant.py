@@ -203,6 +203,50 @@ def test_nvfp4_subnormal_tokens_and_blocks(mx, orc):
         assert np.array_equal(to_np(sd), orc.scales_to_gemm_layout(so))
 
 
+def test_weight_sync_fused_maxima(mx, orc):
+    """The weight-sync chain with the matrix maxima carried between calls: MXFP8 quantize that also
+    returns each matrix's max |w|, the 2D NVFP4 quantizer fed that maximum, and the NVFP4 dequantize that
+    returns each matrix's max |y| -- every output identical to the plain calls and to the oracle, the
+    maxima equal to the exact ones."""
+    G, O, H = 3, 256, 384
+    w = synthetic.random_bf16(31, (G, O, H), "normal", 0.02)
+    w[1, 5, 7] = 0x4100                                      # a spike in one matrix (8.0)
+    wd = bf16_dev(w)
+    exact = (w.astype(np.uint32) & 0x7FFF).reshape(G, -1).max(axis=1) << 16
+    # MXFP8 with the maxima
+    m8 = mx.alloc_mxfp8(G * O, H, DEV)
+    amax = torch.full((G,), -1, dtype=torch.int32, device=DEV)
+    mx.mx_quantize_mxfp8_amax(wd.view(G * O, H), O, amax, **m8)
+    ref8 = mx.alloc_mxfp8(G * O, H, DEV)
+    mx.mx_quantize_mxfp8(wd.view(G * O, H), **ref8)
+    for k in ("q_row", "s_row", "q_col", "s_col"):
+        assert torch.equal(m8[k], ref8[k]), k
+    assert np.array_equal(to_np(amax).view(np.uint32), exact.astype(np.uint32))
+    # the 2D quantizer given those maxima
+    n4 = mx.alloc_nvfp4_weight_2d(G, O, H, DEV)
+    mx.mx_nvfp4_quantize_weight_2d_given_amax(wd, n4["q_row"], n4["s_row"], n4["q_col"], n4["s_col"], n4["s_w"], amax)
+    ref4 = mx.alloc_nvfp4_weight_2d(G, O, H, DEV)
+    mx.mx_nvfp4_quantize_weight_2d(wd, ref4["q_row"], ref4["s_row"], ref4["q_col"], ref4["s_col"], ref4["s_w"], ref4["ws"])
+    for k in ("q_row", "s_row", "q_col", "s_col", "s_w"):
+        assert torch.equal(n4[k], ref4[k]), k
+    for g in range(G):
+        qr, qc, st, sw = orc.nvfp4_quantize_weight_2d(np.ascontiguousarray(w[g]))
+        assert np.array_equal(to_np(n4["q_row"][g]), qr)
+        assert np.float32(to_np(n4["s_w"])[g]) == np.float32(sw)
+    # the NVFP4 dequantize with the maxima of its output
+    y = torch.empty((G * O, H), dtype=torch.bfloat16, device=DEV)
+    amy = torch.full((G,), -1, dtype=torch.int32, device=DEV)
+    mx.mx_dequantize_nvfp4_amax(n4["q_row"], n4["s_row"], n4["s_w"], O, G * O, H, y, amy)
+    yref = torch.empty_like(y)
+    mx.mx_dequantize_bf16(mx.MX_FMT_NVFP4, n4["q_row"], n4["s_row"], n4["s_w"], mx.MX_SCOPE_GROUP, G * O, H, yref,
+                          group_rows=O)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    assert torch.equal(y.view(torch.int16), yref.view(torch.int16))
+    yb = to_np_u16(y).astype(np.uint32)
+    assert np.array_equal(to_np(amy).view(np.uint32), ((yb & 0x7FFF).reshape(G, -1).max(axis=1) << 16).astype(np.uint32))
+
+
 def test_nvfp4_block_scale_ties(mx, orc):
     """Block scales at E4M3 rounding midpoints take the exact path on the device, per token and per tensor."""
     T, H = 96, 256
