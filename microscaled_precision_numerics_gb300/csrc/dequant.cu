@@ -173,10 +173,10 @@ cudaError_t launch_dequant_nvfp4_amax(const uint8_t* q, const uint8_t* s, const 
                                       int64_t K, uint16_t* y, uint32_t* amax, cudaStream_t stream) {
     cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(uint32_t) * (size_t)(R / group_rows), stream);
     if (e != cudaSuccess) return e;
-    // about sixteen CTAs of 8 warps per SM in all, split evenly over the groups
+    // about 32 CTAs of 8 warps per SM in all (queued, not resident), split evenly over the groups
     const int64_t G = R / group_rows;
     if (G > 65535) return cudaErrorInvalidValue;                     // one grid row per group
-    const int64_t per_group = max64(1, (int64_t)device_sm_count() * 16 / G);
+    const int64_t per_group = max64(1, (int64_t)device_sm_count() * 32 / G);
     const int64_t need = (group_rows * (K / 16) + 255) / 256;       // no more CTAs than 16-blocks / 256
     dequant_nvfp4_amax_kernel<<<dim3((unsigned)min64(per_group, need), (unsigned)G), 256, 0, stream>>>(q, s, s2, group_rows,
                                                                                                      K, y, amax);
