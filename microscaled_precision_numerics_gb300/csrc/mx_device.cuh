@@ -338,10 +338,18 @@ __device__ __forceinline__ void zero_grouped_padding(uint8_t* __restrict__ s, co
     const int lane = threadIdx.x & 31;
     for (int64_t g = wid; g < G; g += nwarps) {
         const int64_t first = max64(0, (int64_t)s_ptile[g] * 128 + (s_off[g + 1] - s_off[g]));
-        const int64_t end = min64((int64_t)s_ptile[g + 1] * 128, tile_bound * 128);
-        const int64_t n = (end - first) * nct;                                   // < 128 rows, in one tile
-        for (int64_t i = lane; i < n; i += 32)
-            *reinterpret_cast<uint32_t*>(s + sf_offset(first + i / nct, 4 * (i % nct), nct)) = 0u;
+        const int64_t end = min64((int64_t)s_ptile[g + 1] * 128, tile_bound * 128);   // < 128 rows, one tile
+        // lanes over (row, 4-column word) pairs without divisions: 32 / nct rows at a time when nct <= 32
+        if (nct <= 32) {
+            const int rows_per = 32 / (int)nct;
+            const int rr = lane / (int)nct, kc = lane % (int)nct;
+            if (rr < rows_per)
+                for (int64_t r = first + rr; r < end; r += rows_per)
+                    *reinterpret_cast<uint32_t*>(s + sf_offset(r, 4 * kc, nct)) = 0u;
+        } else {
+            for (int64_t r = first; r < end; ++r)
+                for (int64_t c = lane; c < nct; c += 32) *reinterpret_cast<uint32_t*>(s + sf_offset(r, 4 * c, nct)) = 0u;
+        }
     }
     const int64_t used = min64(max64(0, (int64_t)s_ptile[G]), tile_bound);
     uint4* tail = reinterpret_cast<uint4*>(s + used * nct * 512);
