@@ -1387,13 +1387,12 @@ bool make_sf_map(CUtensorMap* map, const uint8_t* base, int64_t bytes, uint32_t 
 template <int FMT, bool GROUPED, bool COL_ALPHA, int TN>
 cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
     using C = PairCfg<FMT, GROUPED, TN>;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    static int resident_pairs = 0;          // CTA pairs that fit on the GPU at once
-    std::call_once(attr_once, [num_sms] {
+    static PerDevice setup;                 // attributes, and the CTA pairs that fit on the GPU at once
+    int resident_pairs = 0;
+    const cudaError_t attr_err = per_device_once(setup, resident_pairs, [num_sms](int& rp) -> cudaError_t {
         auto kern = bs_gemm_pair_kernel<FMT, GROUPED, COL_ALPHA, TN>;
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-        if (attr_err != cudaSuccess) return;
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(num_sms & ~1));
         cfg.blockDim = dim3(NUM_THREADS);
@@ -1407,7 +1406,8 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
             cudaGetLastError();
             n = num_sms / 2;
         }
-        resident_pairs = n;
+        rp = n;
+        return cudaSuccess;
     });
     if (attr_err != cudaSuccess) return attr_err;
 
@@ -1448,12 +1448,11 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
 template <bool WG>
 cudaError_t launch_dq_impl(const DqGemmArgs& a, int num_sms, cudaStream_t stream) {
     using C = DqCfg<WG>;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    static int resident_pairs = 0;
-    std::call_once(attr_once, [num_sms] {
-        attr_err = cudaFuncSetAttribute(dq_gemm_pair_kernel<WG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-        if (attr_err != cudaSuccess) return;
+    static PerDevice setup;                 // attributes, and the CTA pairs that fit on the GPU at once
+    int resident_pairs = 0;
+    const cudaError_t attr_err = per_device_once(setup, resident_pairs, [num_sms](int& rp) -> cudaError_t {
+        const cudaError_t e = cudaFuncSetAttribute(dq_gemm_pair_kernel<WG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(num_sms & ~1));
         cfg.blockDim = dim3(DQ_THREADS);
@@ -1467,7 +1466,8 @@ cudaError_t launch_dq_impl(const DqGemmArgs& a, int num_sms, cudaStream_t stream
             cudaGetLastError();
             n = num_sms / 2;
         }
-        resident_pairs = n;
+        rp = n;
+        return cudaSuccess;
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap tmA, tmQ, tmSB, tmD;
@@ -1507,12 +1507,11 @@ cudaError_t launch_dq_impl(const DqGemmArgs& a, int num_sms, cudaStream_t stream
 template <int TN>
 cudaError_t launch_bw_impl(const BwGemmArgs& a, int num_sms, cudaStream_t stream) {
     using C = BwCfg<TN>;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    static int resident_pairs = 0;
-    std::call_once(attr_once, [num_sms] {
-        attr_err = cudaFuncSetAttribute(fp8bw_gemm_pair_kernel<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-        if (attr_err != cudaSuccess) return;
+    static PerDevice setup;                 // attributes, and the CTA pairs that fit on the GPU at once
+    int resident_pairs = 0;
+    const cudaError_t attr_err = per_device_once(setup, resident_pairs, [num_sms](int& rp) -> cudaError_t {
+        const cudaError_t e = cudaFuncSetAttribute(fp8bw_gemm_pair_kernel<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(num_sms & ~1));
         cfg.blockDim = dim3(NUM_THREADS);
@@ -1526,7 +1525,8 @@ cudaError_t launch_bw_impl(const BwGemmArgs& a, int num_sms, cudaStream_t stream
             cudaGetLastError();
             n = num_sms / 2;
         }
-        resident_pairs = n;
+        rp = n;
+        return cudaSuccess;
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap tmA, tmB, tmD;

@@ -2,11 +2,32 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "mx_device.cuh"
 
 namespace mxk {
+
+// One-time setup per device: kernel attributes (and the occupancy read after them) belong to each
+// device's context, so a process that drives several GPUs sets them once on every device.  The first
+// call with a device current runs f(value), which returns a CUDA status and may store one integer.
+constexpr int MX_MAX_DEVICES = 64;
+struct PerDevice {
+    std::once_flag once[MX_MAX_DEVICES];
+    cudaError_t err[MX_MAX_DEVICES] = {};
+    int value[MX_MAX_DEVICES] = {};
+};
+template <typename F>
+inline cudaError_t per_device_once(PerDevice& pd, int& value, F&& f) {
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= MX_MAX_DEVICES) return cudaErrorInvalidDevice;
+    std::call_once(pd.once[dev], [&] { pd.err[dev] = f(pd.value[dev]); });
+    value = pd.value[dev];
+    return pd.err[dev];
+}
 
 // Bytes of a GEMM-layout scale tensor (see include/mxnum.h).
 __host__ __device__ inline int64_t host_scale_bytes(int64_t rows, int64_t k, int block) {

@@ -17,7 +17,6 @@
 #include "mx_async.cuh"
 
 #include <cstring>
-#include <mutex>
 
 namespace mxk {
 
@@ -346,14 +345,17 @@ static cudaError_t launch_mx8(const Mx8Tensor* ts, int n, int G, const int64_t* 
     }
     const size_t base = (size_t)QT_NST * QT_TILE_BYTES + 4 * QT_COLS + 64 + 1024;
     const size_t smem = base + (G > 0 ? (size_t)12 * (G + 1) + 128 : 0);
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [base] {
+    static PerDevice setup;
+    int unused = 0;
+    const cudaError_t attr_err = per_device_once(setup, unused, [base](int&) -> cudaError_t {
         const int max_smem = (int)(base + 12 * (MX_MAX_GROUPS + 1) + 128);
         const void* ks[] = {(const void*)mxfp8_quantize_kernel<true, true, false>, (const void*)mxfp8_quantize_kernel<true, false, false>,
                             (const void*)mxfp8_quantize_kernel<false, true, false>, (const void*)mxfp8_quantize_kernel<true, false, true>};
-        for (const void* kf : ks)
-            if (attr_err == cudaSuccess) attr_err = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        for (const void* kf : ks) {
+            const cudaError_t e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
     });
     if (attr_err != cudaSuccess) return attr_err;
     const unsigned grid = (unsigned)min64(tiles, (int64_t)device_sm_count() * QT_CTAS_PER_SM);
