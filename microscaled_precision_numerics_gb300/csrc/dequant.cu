@@ -12,14 +12,17 @@ namespace mxk {
 
 namespace {
 
-// MXFP8: thread = 16 codes (one uint4) -> 16 BF16 (two uint4).
+// MXFP8: thread = 16 codes (one uint4) -> 16 BF16 (two uint4).  Idx is the type of the thread index and
+// of its split into (row, column): 32-bit whenever the tensor has fewer than 2^32 such threads, since a
+// 64-bit division costs several times the rest of the thread's work.
+template <typename Idx>
 __global__ void __launch_bounds__(256)
 dequant_mxfp8_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t R, int64_t K,
                      uint16_t* __restrict__ y) {
-    const int64_t per_row = K / 16;
-    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (gid >= R * per_row) return;
-    const int64_t r = gid / per_row, k0 = (gid % per_row) * 16;
+    const Idx per_row = (Idx)(K / 16);
+    const Idx gid = (Idx)blockIdx.x * (Idx)blockDim.x + (Idx)threadIdx.x;
+    if ((int64_t)gid >= R * (int64_t)per_row) return;
+    const int64_t r = (int64_t)(gid / per_row), k0 = (int64_t)(gid % per_row) * 16;
     const uint32_t sc = __ldg(s + sf_offset(r, k0 / 32, sf_col_tiles(K, 32)));
     // 2^(sc - 127) as FP32; sc = 0 gives the subnormal 2^-127
     const float f = sc == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(sc << 23);
@@ -40,15 +43,17 @@ dequant_mxfp8_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ 
     __stcs(dst + 1, make_uint4(out[4], out[5], out[6], out[7]));
 }
 
-// NVFP4: thread = one 16-block (8 code bytes) -> 16 BF16.
+// NVFP4: thread = one 16-block (8 code bytes) -> 16 BF16 (Idx as above).
+template <typename Idx>
 __global__ void __launch_bounds__(256)
 dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, const float* __restrict__ s2,
                      int64_t rows_per_scale, int64_t R, int64_t K, uint16_t* __restrict__ y) {
-    const int64_t per_row_blk = K / 16;
-    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (gid >= R * per_row_blk) return;
-    const int64_t r = gid / per_row_blk, b = gid % per_row_blk;
-    const float S = rows_per_scale > 0 ? __ldg(s2 + r / rows_per_scale) : __ldg(s2);
+    const Idx per_row_blk = (Idx)(K / 16);
+    const Idx gid = (Idx)blockIdx.x * (Idx)blockDim.x + (Idx)threadIdx.x;
+    if ((int64_t)gid >= R * (int64_t)per_row_blk) return;
+    const Idx r_ = gid / per_row_blk;
+    const int64_t r = (int64_t)r_, b = (int64_t)(gid - r_ * per_row_blk);
+    const float S = rows_per_scale > 0 ? __ldg(s2 + (int64_t)(r_ / (Idx)rows_per_scale)) : __ldg(s2);
     const float bs = e4m3_to_f32(__ldg(s + sf_offset(r, b, sf_col_tiles(K, 16))));
     const uint2 c = __ldcs(reinterpret_cast<const uint2*>(q + r * (K / 2) + b * 8));
     const uint32_t cw[2] = {c.x, c.y};
@@ -69,63 +74,72 @@ dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ 
 }
 
 // The same for groups of `group_rows` rows sharing one second-level scale, also writing each group's
-// max |y| (BF16 bits << 16).  Grid (WPG-warp slices, groups): warp w of group g walks a contiguous slice of
-// the group's 16-blocks, lanes on consecutive blocks, and ends with one atomic max, so a group's word
-// takes a few dozen atomics rather than one per warp of blocks.
+// max |y| (BF16 bits << 16).  One 16-block per thread as above; the maxima gather per warp and then per
+// CTA (its warps' groups run in order), so a CTA inside one group makes one atomic.  A warp whose lanes
+// straddle two groups leaves its maxima to per-lane atomics.
+template <typename Idx>
 __global__ void __launch_bounds__(256)
 dequant_nvfp4_amax_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, const float* __restrict__ s2,
-                          int64_t group_rows, int64_t K, uint16_t* __restrict__ y, uint32_t* __restrict__ amax) {
-    const int64_t g = blockIdx.y;
-    const int64_t per_row_blk = K / 16;
-    const int64_t nblk = group_rows * per_row_blk;                   // 16-blocks of the group
-    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int64_t slice = (nblk + nwarps - 1) / nwarps;
-    const int64_t b0 = wid * slice, b1 = min64(nblk, b0 + slice);
-    const float S = __ldg(s2 + g);
-    const int64_t nct = sf_col_tiles(K, 16);
-    uint32_t m2 = 0;
-    constexpr int U = 4;                                             // blocks in flight per lane
-    for (int64_t gb0 = b0 + (threadIdx.x & 31); gb0 < b1; gb0 += 32 * U) {
-        uint2 c[U];
-        uint32_t sc[U];
+                          int64_t group_rows, int64_t R, int64_t K, uint16_t* __restrict__ y,
+                          uint32_t* __restrict__ amax) {
+    __shared__ uint32_t w_max[8];
+    __shared__ int64_t w_grp[8];                                     // -1: nothing left for the CTA to add
+    const Idx per_row_blk = (Idx)(K / 16);
+    const Idx gid = (Idx)blockIdx.x * (Idx)blockDim.x + (Idx)threadIdx.x;
+    // valid threads are a prefix of the grid, so lane 0 of a warp with any valid lane is valid
+    const bool valid = (int64_t)gid < R * (int64_t)per_row_blk;
+    uint32_t m = 0;
+    int64_t g = 0;
+    if (valid) {
+        const Idx r_ = gid / per_row_blk;
+        const int64_t r = (int64_t)r_, b = (int64_t)(gid - r_ * per_row_blk);
+        g = (int64_t)(r_ / (Idx)group_rows);
+        const float S = __ldg(s2 + g);
+        const float bs = e4m3_to_f32(__ldg(s + sf_offset(r, b, sf_col_tiles(K, 16))));
+        const uint2 c = __ldcs(reinterpret_cast<const uint2*>(q + r * (K / 2) + b * 8));
+        const uint32_t cw[2] = {c.x, c.y};
+        uint32_t out[8], m2 = 0;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t gb = gb0 + 32 * u;
-            c[u] = make_uint2(0u, 0u);
-            sc[u] = 0u;
-            if (gb < b1) {
-                const int64_t r = g * group_rows + gb / per_row_blk, b = gb % per_row_blk;
-                sc[u] = __ldg(s + sf_offset(r, b, nct));
-                c[u] = __ldcs(reinterpret_cast<const uint2*>(q + r * (K / 2) + b * 8));
+        for (int i = 0; i < 2; ++i) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t h2 = e2m1x2_to_f16x2((cw[i] >> (8 * j)) & 0xFFu);
+                const float v0 = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+                const float v1 = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+                out[4 * i + j] = pack_bf16x2(__fmul_rn(__fmul_rn(v0, bs), S), __fmul_rn(__fmul_rn(v1, bs), S));
+                m2 = absmax_bf16x2(m2, out[4 * i + j]);
             }
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t gb = gb0 + 32 * u;
-            if (gb >= b1) break;
-            const int64_t r = g * group_rows + gb / per_row_blk, b = gb % per_row_blk;
-            const float bs = e4m3_to_f32(sc[u]);
-            const uint32_t cw[2] = {c[u].x, c[u].y};
-            uint32_t out[8];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t h2 = e2m1x2_to_f16x2((cw[i] >> (8 * j)) & 0xFFu);
-                    const float v0 = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
-                    const float v1 = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
-                    out[4 * i + j] = pack_bf16x2(__fmul_rn(__fmul_rn(v0, bs), S), __fmul_rn(__fmul_rn(v1, bs), S));
-                    m2 = absmax_bf16x2(m2, out[4 * i + j]);
-                }
-            }
-            uint4* dst = reinterpret_cast<uint4*>(y + r * K + b * 16);
-            __stcs(dst, make_uint4(out[0], out[1], out[2], out[3]));
-            __stcs(dst + 1, make_uint4(out[4], out[5], out[6], out[7]));
-        }
+        m = fold_halves(m2);
+        uint4* dst = reinterpret_cast<uint4*>(y + r * K + b * 16);
+        __stcs(dst, make_uint4(out[0], out[1], out[2], out[3]));
+        __stcs(dst + 1, make_uint4(out[4], out[5], out[6], out[7]));
     }
-    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, fold_halves(m2));
-    if ((threadIdx.x & 31) == 0 && b0 < b1) atomicMax(amax + g, m << 16);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t g0 = __shfl_sync(0xFFFFFFFFu, g, 0);
+    const bool one_group = __all_sync(0xFFFFFFFFu, !valid || g == g0);
+    const uint32_t mw = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (!one_group && valid && m != 0) atomicMax(amax + g, m << 16);
+    if (lane == 0) {
+        w_max[warp] = mw;
+        w_grp[warp] = (one_group && valid) ? g0 : -1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // runs of warps in one group: one atomic per run
+        int64_t gc = -1;
+        uint32_t mc = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+            if (w_grp[w] < 0) continue;
+            if (w_grp[w] != gc) {
+                if (gc >= 0 && mc != 0) atomicMax(amax + gc, mc << 16);
+                gc = w_grp[w];
+                mc = 0;
+            }
+            mc = max(mc, w_max[w]);
+        }
+        if (gc >= 0 && mc != 0) atomicMax(amax + gc, mc << 16);
+    }
 }
 
 __global__ void __launch_bounds__(256)
@@ -134,12 +148,25 @@ mismatch_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ y, in
     unsigned long long local = 0;
     const int64_t nvec = nbytes / 16;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-        const uint4 a = __ldcs(reinterpret_cast<const uint4*>(x) + i);
-        const uint4 b = __ldcs(reinterpret_cast<const uint4*>(y) + i);
-        // __vcmpne4 gives 0xFF per differing byte
-        local += __popc(__vcmpne4(a.x, b.x)) + __popc(__vcmpne4(a.y, b.y)) +
-                 __popc(__vcmpne4(a.z, b.z)) + __popc(__vcmpne4(a.w, b.w));
+    // MU vector pairs in flight per thread before the first compare
+    constexpr int MU = 4;
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < nvec; i0 += MU * stride) {
+        uint4 a[MU], b[MU];
+#pragma unroll
+        for (int u = 0; u < MU; ++u) {
+            const int64_t i = i0 + u * stride;
+            a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < nvec) {
+                a[u] = __ldcs(reinterpret_cast<const uint4*>(x) + i);
+                b[u] = __ldcs(reinterpret_cast<const uint4*>(y) + i);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < MU; ++u) {
+            // __vcmpne4 gives 0xFF per differing byte
+            local += __popc(__vcmpne4(a[u].x, b[u].x)) + __popc(__vcmpne4(a[u].y, b[u].y)) +
+                     __popc(__vcmpne4(a[u].z, b[u].z)) + __popc(__vcmpne4(a[u].w, b[u].w));
+        }
     }
     local /= 8;
     for (int64_t i = nvec * 16 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nbytes; i += stride)
@@ -159,12 +186,15 @@ mismatch_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ y, in
 
 cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const float* s2, int64_t rows_per_scale,
                            int64_t R, int64_t K, uint16_t* y, cudaStream_t stream) {
+    const int64_t threads = R * (K / 16);
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    const bool idx32 = threads + 256 <= (int64_t)UINT32_MAX;       // every thread index fits 32 bits
     if (fmt == 0) {
-        const int64_t threads = R * (K / 16);
-        dequant_mxfp8_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(q, s, R, K, y);
+        if (idx32) dequant_mxfp8_kernel<uint32_t><<<blocks, 256, 0, stream>>>(q, s, R, K, y);
+        else dequant_mxfp8_kernel<int64_t><<<blocks, 256, 0, stream>>>(q, s, R, K, y);
     } else {
-        const int64_t threads = R * (K / 16);
-        dequant_nvfp4_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(q, s, s2, rows_per_scale, R, K, y);
+        if (idx32) dequant_nvfp4_kernel<uint32_t><<<blocks, 256, 0, stream>>>(q, s, s2, rows_per_scale, R, K, y);
+        else dequant_nvfp4_kernel<int64_t><<<blocks, 256, 0, stream>>>(q, s, s2, rows_per_scale, R, K, y);
     }
     return cudaGetLastError();
 }
@@ -173,20 +203,20 @@ cudaError_t launch_dequant_nvfp4_amax(const uint8_t* q, const uint8_t* s, const 
                                       int64_t K, uint16_t* y, uint32_t* amax, cudaStream_t stream) {
     cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(uint32_t) * (size_t)(R / group_rows), stream);
     if (e != cudaSuccess) return e;
-    // about 32 CTAs of 8 warps per SM in all (queued, not resident), split evenly over the groups
-    const int64_t G = R / group_rows;
-    if (G > 65535) return cudaErrorInvalidValue;                     // one grid row per group
-    const int64_t per_group = max64(1, (int64_t)device_sm_count() * 32 / G);
-    const int64_t need = (group_rows * (K / 16) + 255) / 256;       // no more CTAs than 16-blocks / 256
-    dequant_nvfp4_amax_kernel<<<dim3((unsigned)min64(per_group, need), (unsigned)G), 256, 0, stream>>>(q, s, s2, group_rows,
-                                                                                                     K, y, amax);
+    const int64_t threads = R * (K / 16);
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    if (threads + 256 <= (int64_t)UINT32_MAX)
+        dequant_nvfp4_amax_kernel<uint32_t><<<blocks, 256, 0, stream>>>(q, s, s2, group_rows, R, K, y, amax);
+    else
+        dequant_nvfp4_amax_kernel<int64_t><<<blocks, 256, 0, stream>>>(q, s, s2, group_rows, R, K, y, amax);
     return cudaGetLastError();
 }
 
 cudaError_t launch_mismatch(const uint8_t* x, const uint8_t* y, int64_t nbytes, unsigned long long* count,
                             int num_sms, cudaStream_t stream) {
+    // one wave: 40 registers a thread leave room for 6 CTAs of 256 threads per SM
     int64_t blocks = (nbytes / 16 + 255) / 256;
-    blocks = max64(1, min64(blocks, (int64_t)num_sms * 8));
+    blocks = max64(1, min64(blocks, (int64_t)num_sms * 6));
     mismatch_kernel<<<(unsigned)blocks, 256, 0, stream>>>(x, y, nbytes, count);
     return cudaGetLastError();
 }

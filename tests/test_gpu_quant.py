@@ -247,6 +247,29 @@ def test_weight_sync_fused_maxima(mx, orc):
     assert np.array_equal(to_np(amy).view(np.uint32), ((yb & 0x7FFF).reshape(G, -1).max(axis=1) << 16).astype(np.uint32))
 
 
+@pytest.mark.parametrize("H", [16, 48, 2064])
+def test_dequant_nvfp4_amax_row_widths(mx, H):
+    """The dequantize that also returns each matrix's max |y| walks its blocks with a running
+    (row, block column) pair: rows of 1, 3 and 129 blocks (fewer, and not a multiple of, the 32 blocks a
+    warp steps by) give the same bytes as the plain dequantize, which the oracle pins, and exact maxima."""
+    G, O = 3, 128
+    w = synthetic.random_bf16(40 + H, (G, O, H), "normal", 0.02)
+    w[2, 100, H - 1] = 0xC0C0                                # a spike in the last matrix (-6.0)
+    n4 = mx.alloc_nvfp4_weight_2d(G, O, H, DEV)
+    mx.mx_nvfp4_quantize_weight_2d(bf16_dev(w), n4["q_row"], n4["s_row"], n4["q_col"], n4["s_col"], n4["s_w"], n4["ws"])
+    y = torch.empty((G * O, H), dtype=torch.bfloat16, device=DEV)
+    amy = torch.full((G,), -1, dtype=torch.int32, device=DEV)
+    mx.mx_dequantize_nvfp4_amax(n4["q_row"], n4["s_row"], n4["s_w"], O, G * O, H, y, amy)
+    yref = torch.empty_like(y)
+    mx.mx_dequantize_bf16(mx.MX_FMT_NVFP4, n4["q_row"], n4["s_row"], n4["s_w"], mx.MX_SCOPE_GROUP, G * O, H, yref,
+                          group_rows=O)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    assert torch.equal(y.view(torch.int16), yref.view(torch.int16))
+    yb = to_np_u16(y).astype(np.uint32)
+    assert np.array_equal(to_np(amy).view(np.uint32), ((yb & 0x7FFF).reshape(G, -1).max(axis=1) << 16).astype(np.uint32))
+
+
 def test_nvfp4_block_scale_ties(mx, orc):
     """Block scales at E4M3 rounding midpoints take the exact path on the device, per token and per tensor."""
     T, H = 96, 256
@@ -438,6 +461,23 @@ def test_weight_sync_round_trip_on_device(mx, orc):
     cnt.zero_()
     mx.mx_count_mismatch(a["q_row"].view(-1)[:1001], c.view(-1)[:1001], cnt)
     assert int(cnt.item()) == 3
+
+
+def test_count_mismatch_many_vectors_per_thread(mx):
+    """The byte comparator over a buffer of several 16-byte vectors per thread and a ragged tail counts
+    exactly the planted differences (one to four per touched 16-byte vector)."""
+    n = 152 * 6 * 256 * 16 * 9 + 12345
+    g = torch.Generator(device="cpu").manual_seed(7)
+    a = torch.randint(0, 256, (n,), dtype=torch.uint8, generator=g)
+    pos = torch.randperm(n, generator=g)[:5000]
+    b = a.clone()
+    b[pos] ^= torch.randint(1, 256, (5000,), dtype=torch.uint8, generator=g)
+    cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
+    mx.mx_count_mismatch(a.to(DEV), b.to(DEV), cnt)
+    assert int(cnt.item()) == 5000
+    cnt.zero_()
+    mx.mx_count_mismatch(a.to(DEV), a.to(DEV), cnt)
+    assert int(cnt.item()) == 0
 
 
 def test_device_status_clean(mx):
