@@ -91,7 +91,29 @@ def _p(t):
         raise TypeError("expected a torch.Tensor")
     if not t.is_cuda:
         raise ValueError("mxnum operates on CUDA tensors only (no CPU path)")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensor on {t.device} but the current device is cuda:{torch.cuda.current_device()}")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(fn: str, name: str, t, nbytes) -> None:
+    """Raise unless t (when given) is contiguous and holds at least nbytes bytes: the C ABI takes bare
+    pointers, so the sizes of the buffers it reads and writes are checked here."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{fn}: {name} must be a torch.Tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{fn}: {name} must be contiguous")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{fn}: {name} holds {have} bytes, {int(nbytes)} needed")
+
+
+def _need_out2d(fn: str, name: str, d, rows: int, cols: int) -> None:
+    """A row-major [rows, cols] output that may be a view with a row stride (unit column stride)."""
+    if d.dim() != 2 or d.shape[0] < rows or d.shape[1] < cols or d.stride(1) != 1:
+        raise ValueError(f"{fn}: {name} must be a 2-D view of at least [{rows}, {cols}] with unit column stride")
 
 
 def _stream(stream=None):
@@ -99,14 +121,28 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _bf16_bits(t: torch.Tensor) -> torch.Tensor:
+def _bf16_bits(t: torch.Tensor, dims: int = 2) -> torch.Tensor:
+    """A BF16 input: [rows, cols] with unit column stride (any row stride), or a contiguous [G, rows, cols]."""
     if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
         raise TypeError("BF16 input expected (bfloat16 or its 16-bit bit pattern)")
+    if t.dim() != dims:
+        raise ValueError(f"a {dims}-D BF16 tensor expected, got shape {tuple(t.shape)}")
+    if dims == 2 and t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("BF16 input must have unit column stride")
+    if dims != 2 and not t.is_contiguous():
+        raise ValueError("stacked BF16 input must be contiguous")
     return t
 
 
 def scale_bytes(rows: int, k: int, block: int) -> int:
     return int(lib().mx_scale_bytes(rows, k, block))
+
+
+def _mxfp8_outputs(fn, rows, cols, q_row, s_row, q_col, s_col):
+    _need(fn, "q_row", q_row, rows * cols)
+    _need(fn, "s_row", s_row, scale_bytes(rows, cols, 32))
+    _need(fn, "q_col", q_col, rows * cols)
+    _need(fn, "s_col", s_col, scale_bytes(cols, rows, 32))
 
 
 def workspace_bytes(op: int, groups: int = 0) -> int:
@@ -124,6 +160,7 @@ def check_device_status() -> None:
 def mx_quantize_mxfp8(x, q_row=None, s_row=None, q_col=None, s_col=None, stream=None):
     x = _bf16_bits(x)
     rows, cols = x.shape
+    _mxfp8_outputs("mx_quantize_mxfp8", rows, cols, q_row, s_row, q_col, s_col)
     _check("mx_quantize_mxfp8", lib().mx_quantize_mxfp8(
         _p(x), rows, cols, x.stride(0), _p(q_row), _p(s_row), _p(q_col), _p(s_col), _stream(stream)))
 
@@ -147,6 +184,8 @@ def mx_quantize_mxfp8_batched(jobs, stream=None):
         x = _bf16_bits(x)
         keep.append(x)
         rows, cols = x.shape
+        _mxfp8_outputs("mx_quantize_mxfp8_batched", rows, cols, out.get("q_row"), out.get("s_row"), out.get("q_col"),
+                       out.get("s_col"))
         arr[i] = _Mxfp8Tensor(_p(x), rows, cols, x.stride(0), _p(out.get("q_row")), _p(out.get("s_row")),
                               _p(out.get("q_col")), _p(out.get("s_col")))
     _check("mx_quantize_mxfp8_batched", lib().mx_quantize_mxfp8_batched(ctypes.cast(arr, ctypes.c_void_p),
@@ -157,26 +196,51 @@ def mx_quantize_mxfp8_amax(x, matrix_rows: int, amax, q_row=None, s_row=None, q_
     """mx_quantize_mxfp8 of stacked matrices plus each matrix's max |x| (int32 words, BF16 bits << 16)."""
     x = _bf16_bits(x)
     rows, cols = x.shape
+    _mxfp8_outputs("mx_quantize_mxfp8_amax", rows, cols, q_row, s_row, q_col, s_col)
+    _need("mx_quantize_mxfp8_amax", "amax", amax, 4 * (rows // max(int(matrix_rows), 1)))
     _check("mx_quantize_mxfp8_amax", lib().mx_quantize_mxfp8_amax(
         _p(x), rows, cols, x.stride(0), _p(q_row), _p(s_row), _p(q_col), _p(s_col), matrix_rows, _p(amax),
         _stream(stream)))
 
 
+def _weight_2d_outputs(fn, G, O, H, q_row, s_row, q_col, s_col, s_w):
+    _need(fn, "q_row", q_row, G * O * H // 2)
+    _need(fn, "s_row", s_row, G * scale_bytes(O, H, 16))
+    _need(fn, "q_col", q_col, G * O * H // 2)
+    _need(fn, "s_col", s_col, G * scale_bytes(H, O, 16))
+    _need(fn, "s_w", s_w, 4 * G)
+
+
 def mx_nvfp4_quantize_weight_2d_given_amax(w, q_row, s_row, q_col, s_col, s_w, amax, stream=None):
-    w = _bf16_bits(w)
+    w = _bf16_bits(w, 3)
     G, O, H = w.shape
+    _weight_2d_outputs("mx_nvfp4_quantize_weight_2d_given_amax", G, O, H, q_row, s_row, q_col, s_col, s_w)
+    _need("mx_nvfp4_quantize_weight_2d_given_amax", "amax", amax, 4 * G)
     _check("mx_nvfp4_quantize_weight_2d_given_amax", lib().mx_nvfp4_quantize_weight_2d_given_amax(
         _p(w), G, O, H, _p(q_row), _p(s_row), _p(q_col), _p(s_col), _p(s_w), _p(amax), _stream(stream)))
 
 
 def mx_dequantize_nvfp4_amax(q, s, s2, group_rows: int, rows: int, cols: int, y, amax, stream=None):
+    fn, ng = "mx_dequantize_nvfp4_amax", rows // max(int(group_rows), 1)
+    _need(fn, "q", q, rows * cols // 2)
+    _need(fn, "s", s, scale_bytes(rows, cols, 16))
+    _need(fn, "s2", s2, 4 * ng)
+    _need(fn, "y", y, 2 * rows * cols)
+    _need(fn, "amax", amax, 4 * ng)
     _check("mx_dequantize_nvfp4_amax", lib().mx_dequantize_nvfp4_amax(
         _p(q), _p(s), _p(s2), group_rows, rows, cols, _p(y), _p(amax), _stream(stream)))
+
+
+def _per_token_outputs(fn, T, H, q, s_bytes, s, s_tok):
+    _need(fn, "q", q, T * H // 2)
+    _need(fn, "s", s, s_bytes)
+    _need(fn, "s_tok", s_tok, 4 * T)
 
 
 def mx_nvfp4_quantize_per_token(x, q, s, s_tok, stream=None):
     x = _bf16_bits(x)
     T, H = x.shape
+    _per_token_outputs("mx_nvfp4_quantize_per_token", T, H, q, scale_bytes(T, H, 16), s, s_tok)
     _check("mx_nvfp4_quantize_per_token", lib().mx_nvfp4_quantize_per_token(
         _p(x), T, H, x.stride(0), _p(q), _p(s), _p(s_tok), _stream(stream)))
 
@@ -184,6 +248,7 @@ def mx_nvfp4_quantize_per_token(x, q, s, s_tok, stream=None):
 def mx_nvfp4_quantize_per_token_46(x, q, s, s_tok, stream=None):
     x = _bf16_bits(x)
     T, H = x.shape
+    _per_token_outputs("mx_nvfp4_quantize_per_token_46", T, H, q, scale_bytes(T, H, 16), s, s_tok)
     _check("mx_nvfp4_quantize_per_token_46", lib().mx_nvfp4_quantize_per_token_46(
         _p(x), T, H, x.stride(0), _p(q), _p(s), _p(s_tok), _stream(stream)))
 
@@ -191,6 +256,9 @@ def mx_nvfp4_quantize_per_token_46(x, q, s, s_tok, stream=None):
 def mx_nvfp4_quantize_per_token_grouped(x, group_offsets, q, s, s_tok, stream=None):
     x = _bf16_bits(x)
     T, H = x.shape
+    G = group_offsets.numel() - 1
+    _need("mx_nvfp4_quantize_per_token_grouped", "group_offsets", group_offsets, 8 * (G + 1))
+    _per_token_outputs("mx_nvfp4_quantize_per_token_grouped", T, H, q, grouped_scale_bytes(T, G, H, 16), s, s_tok)
     _check("mx_nvfp4_quantize_per_token_grouped", lib().mx_nvfp4_quantize_per_token_grouped(
         _p(x), T, H, x.stride(0), group_offsets.numel() - 1, _p(group_offsets), _p(q), _p(s), _p(s_tok),
         _stream(stream)))
@@ -199,6 +267,10 @@ def mx_nvfp4_quantize_per_token_grouped(x, group_offsets, q, s, s_tok, stream=No
 def mx_quantize_mxfp8_grouped(x, group_offsets, q_row, s_row, stream=None):
     x = _bf16_bits(x)
     rows, cols = x.shape
+    G = group_offsets.numel() - 1
+    _need("mx_quantize_mxfp8_grouped", "group_offsets", group_offsets, 8 * (G + 1))
+    _need("mx_quantize_mxfp8_grouped", "q_row", q_row, rows * cols)
+    _need("mx_quantize_mxfp8_grouped", "s_row", s_row, grouped_scale_bytes(rows, G, cols, 32))
     _check("mx_quantize_mxfp8_grouped", lib().mx_quantize_mxfp8_grouped(
         _p(x), rows, cols, x.stride(0), group_offsets.numel() - 1, _p(group_offsets), _p(q_row), _p(s_row),
         _stream(stream)))
@@ -209,16 +281,18 @@ def grouped_scale_bytes(rows: int, G: int, k: int, block: int) -> int:
 
 
 def mx_nvfp4_quantize_weight_2d(w, q_row, s_row, q_col, s_col, s_w, workspace, stream=None):
-    w = _bf16_bits(w)
+    w = _bf16_bits(w, 3)
     G, O, H = w.shape
+    _weight_2d_outputs("mx_nvfp4_quantize_weight_2d", G, O, H, q_row, s_row, q_col, s_col, s_w)
     _check("mx_nvfp4_quantize_weight_2d", lib().mx_nvfp4_quantize_weight_2d(
         _p(w), G, O, H, _p(q_row), _p(s_row), _p(q_col), _p(s_col), _p(s_w), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def mx_nvfp4_quantize_weight_2d_46(w, q_row, s_row, q_col, s_col, s_w, workspace, stream=None):
-    w = _bf16_bits(w)
+    w = _bf16_bits(w, 3)
     G, O, H = w.shape
+    _weight_2d_outputs("mx_nvfp4_quantize_weight_2d_46", G, O, H, q_row, s_row, q_col, s_col, s_w)
     _check("mx_nvfp4_quantize_weight_2d_46", lib().mx_nvfp4_quantize_weight_2d_46(
         _p(w), G, O, H, _p(q_row), _p(s_row), _p(q_col), _p(s_col), _p(s_w), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
@@ -229,8 +303,9 @@ def mx_nvfp4_quantize_weight_2d_noalloc(w, q_row, s_row, q_col, s_col, s_w, stre
     device memory: the library keeps the per-matrix scratch in a fixed internal array (at most
     MX_NOALLOC_MAX_MATRICES matrices per call).  Calls that may overlap on the GPU share that array
     and must be serialized by the caller."""
-    w = _bf16_bits(w)
+    w = _bf16_bits(w, 3)
     G, O, H = w.shape
+    _weight_2d_outputs("mx_nvfp4_quantize_weight_2d_noalloc", G, O, H, q_row, s_row, q_col, s_col, s_w)
     f = lib().mx_nvfp4_quantize_weight_2d_noalloc
     P, I64 = ctypes.c_void_p, ctypes.c_int64
     f.restype = ctypes.c_int
@@ -248,6 +323,13 @@ def mx_fp8_blockwise_quantize_1x128(x, pow2: bool, q_row=None, s_row=None, sf_ro
     E8M0 scales may also be written in the MXFP8 GEMM layout (sf_row / sf_col)."""
     x = _bf16_bits(x)
     rows, cols = x.shape
+    fn = "mx_fp8_blockwise_quantize_1x128"
+    _need(fn, "q_row", q_row, rows * cols)
+    _need(fn, "s_row", s_row, 4 * rows * (cols // 128))
+    _need(fn, "sf_row", sf_row, scale_bytes(rows, cols, 32))
+    _need(fn, "q_col", q_col, rows * cols)
+    _need(fn, "s_col", s_col, 4 * cols * (rows // 128))
+    _need(fn, "sf_col", sf_col, scale_bytes(cols, rows, 32))
     _check("mx_fp8_blockwise_quantize_1x128", lib().mx_fp8_blockwise_quantize_1x128(
         _p(x), rows, cols, x.stride(0), int(bool(pow2)), _p(q_row), _p(s_row), _p(sf_row), _p(q_col), _p(s_col),
         _p(sf_col), _stream(stream)))
@@ -256,8 +338,14 @@ def mx_fp8_blockwise_quantize_1x128(x, pow2: bool, q_row=None, s_row=None, sf_ro
 def mx_fp8_blockwise_quantize_128x128(w, pow2: bool, q_row, q_col, s, sf_row=None, sf_col=None, stream=None):
     """Blockwise FP8 of G stacked weights [G, O, H] in [128, 128] blocks: q_row [G, O, H], q_col
     [G, H, O], s [G, ceil(O/128), ceil(H/128)]; with pow2 optionally the MXFP8-layout E8M0 scales."""
-    w = _bf16_bits(w)
+    w = _bf16_bits(w, 3)
     G, O, H = w.shape
+    fn = "mx_fp8_blockwise_quantize_128x128"
+    _need(fn, "q_row", q_row, G * O * H)
+    _need(fn, "q_col", q_col, G * O * H)
+    _need(fn, "s", s, 4 * G * ((O + 127) // 128) * ((H + 127) // 128))
+    _need(fn, "sf_row", sf_row, G * scale_bytes(O, H, 32))
+    _need(fn, "sf_col", sf_col, G * scale_bytes(H, O, 32))
     _check("mx_fp8_blockwise_quantize_128x128", lib().mx_fp8_blockwise_quantize_128x128(
         _p(w), G, O, H, int(bool(pow2)), _p(q_row), _p(q_col), _p(s), _p(sf_row), _p(sf_col), _stream(stream)))
 
@@ -265,6 +353,8 @@ def mx_fp8_blockwise_quantize_128x128(w, pow2: bool, q_row, q_col, s, sf_row=Non
 def mx_rht16(x, seed: int, y, stream=None):
     x = _bf16_bits(x)
     T, N = x.shape
+    _need("mx_rht16", "x", x, 2 * T * N)
+    _need("mx_rht16", "y", y, 2 * T * N)
     _check("mx_rht16", lib().mx_rht16(_p(x), T, N, seed, _p(y), _stream(stream)))
 
 
@@ -272,18 +362,42 @@ def mx_nvfp4_quantize_1x16(x, colwise: bool, rht: bool, rht_seed: int, sr: bool,
                            workspace, stream=None):
     x = _bf16_bits(x)
     T, N = x.shape
+    fn = "mx_nvfp4_quantize_1x16"
+    _need(fn, "x", x, 2 * T * N)
+    _need(fn, "q", q, T * N // 2)
+    _need(fn, "s", s, scale_bytes(N, T, 16) if colwise else scale_bytes(T, N, 16))
+    _need(fn, "s_tensor", s_tensor, 4)
     _check("mx_nvfp4_quantize_1x16", lib().mx_nvfp4_quantize_1x16(
         _p(x), T, N, int(colwise), int(rht), rht_seed, MX_ROUND_SR if sr else MX_ROUND_RNE, sr_seed,
         _p(q), _p(s), _p(s_tensor), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def mx_dequantize_bf16(fmt: int, q, s, s2, s2_scope: int, rows: int, cols: int, y, stream=None, group_rows: int = 0):
+    fn, fp4 = "mx_dequantize_bf16", fmt == MX_FMT_NVFP4
+    _need(fn, "q", q, rows * cols // 2 if fp4 else rows * cols)
+    _need(fn, "s", s, scale_bytes(rows, cols, 16 if fp4 else 32))
+    if fp4:
+        n2 = {MX_SCOPE_ROW: rows, MX_SCOPE_GROUP: rows // max(int(group_rows), 1)}.get(s2_scope, 1)
+        _need(fn, "s2", s2, 4 * n2)
+    _need(fn, "y", y, 2 * rows * cols)
     _check("mx_dequantize_bf16", lib().mx_dequantize_bf16(
         fmt, _p(q), _p(s), _p(s2), s2_scope, group_rows, rows, cols, _p(y), _stream(stream)))
 
 
+def _alpha_count(scope: int, n: int) -> int:
+    return n if scope == MX_SCOPE_ROW else (1 if scope == MX_SCOPE_TENSOR else 0)
+
+
 def mx_scaled_gemm(fmt: int, a, sa, alpha_a, alpha_a_scope: int, b, sb, alpha_b, alpha_b_scope: int,
                    M: int, N: int, K: int, d, stream=None):
+    fn, fp4 = "mx_scaled_gemm", fmt == MX_FMT_NVFP4
+    _need(fn, "a", a, M * K // 2 if fp4 else M * K)
+    _need(fn, "b", b, N * K // 2 if fp4 else N * K)
+    _need(fn, "sa", sa, scale_bytes(M, K, 16 if fp4 else 32))
+    _need(fn, "sb", sb, scale_bytes(N, K, 16 if fp4 else 32))
+    _need(fn, "alpha_a", alpha_a, 4 * _alpha_count(alpha_a_scope, M))
+    _need(fn, "alpha_b", alpha_b, 4 * _alpha_count(alpha_b_scope, N))
+    _need_out2d(fn, "d", d, M, N)
     _check("mx_scaled_gemm", lib().mx_scaled_gemm(
         fmt, _p(a), _p(sa), _p(alpha_a), alpha_a_scope, _p(b), _p(sb), _p(alpha_b), alpha_b_scope,
         M, N, K, _p(d), d.stride(0), _stream(stream)))
@@ -296,6 +410,13 @@ def mx_gemm_bf16_dq_nvfp4(a, qb, sb, sb2, sb2_scope, M: int, N: int, K: int, d, 
     a = _bf16_bits(a)
     if a.stride(0) != K or a.stride(1) != 1:
         raise ValueError("A must be a contiguous [M, K] BF16 tensor")
+    fn = "mx_gemm_bf16_dq_nvfp4"
+    _need(fn, "a", a, 2 * M * K)
+    _need(fn, "alpha_a", alpha_a, 4 * _alpha_count(alpha_a_scope, M))
+    _need(fn, "qb", qb, N * K // 2)
+    _need(fn, "sb", sb, scale_bytes(N, K, 16))
+    _need(fn, "sb2", sb2, 4 * _alpha_count(sb2_scope, N))
+    _need_out2d(fn, "d", d, M, N)
     _check("mx_gemm_bf16_dq_nvfp4", lib().mx_gemm_bf16_dq_nvfp4(
         _p(a), _p(alpha_a), int(alpha_a_scope), _p(qb), _p(sb), _p(sb2), int(sb2_scope), M, N, K, _p(d), d.stride(0),
         _stream(stream)))
@@ -309,6 +430,11 @@ def mx_wgrad_bf16_dq_nvfp4(dy, qx, sx, sx2, sx2_scope, dw, stream=None):
     H = qx.shape[1] * 2
     if dy.stride(0) != O or dy.stride(1) != 1:
         raise ValueError("dY must be a contiguous [T, O] BF16 tensor")
+    fn = "mx_wgrad_bf16_dq_nvfp4"
+    _need(fn, "qx", qx, T * H // 2)
+    _need(fn, "sx", sx, scale_bytes(T, H, 16))
+    _need(fn, "sx2", sx2, 4 * _alpha_count(sx2_scope, T))
+    _need_out2d(fn, "dw", dw, O, H)
     _check("mx_wgrad_bf16_dq_nvfp4", lib().mx_wgrad_bf16_dq_nvfp4(
         _p(dy), _p(qx), _p(sx), _p(sx2), int(sx2_scope), T, O, H, _p(dw), dw.stride(0), _stream(stream)))
 
@@ -316,6 +442,12 @@ def mx_wgrad_bf16_dq_nvfp4(dy, qx, sx, sx2, sx2_scope, dw, stream=None):
 def mx_fp8_blockwise_gemm(a, sa, b, sb, M: int, N: int, K: int, d, stream=None):
     """D = BF16(sum over 128-deep K blocks of sa[m, kb] * sb[n / 128, kb] * A_kb B_kb^T): E4M3 a [M, K] with
     FP32 [1, 128]-tile scales sa [M, K/128], E4M3 b [N, K] with FP32 [128, 128]-block scales sb."""
+    fn = "mx_fp8_blockwise_gemm"
+    _need(fn, "a", a, M * K)
+    _need(fn, "sa", sa, 4 * M * (K // 128))
+    _need(fn, "b", b, N * K)
+    _need(fn, "sb", sb, 4 * ((N + 127) // 128) * (K // 128))
+    _need_out2d(fn, "d", d, M, N)
     _check("mx_fp8_blockwise_gemm", lib().mx_fp8_blockwise_gemm(
         _p(a), _p(sa), _p(b), _p(sb), M, N, K, _p(d), d.stride(0), _stream(stream)))
 
@@ -323,6 +455,13 @@ def mx_fp8_blockwise_gemm(a, sa, b, sb, M: int, N: int, K: int, d, stream=None):
 def mx_grouped_scaled_gemm(fmt: int, group_offsets, a, sa, alpha_a_rows, b, sb, alpha_b_groups, N: int, K: int, d,
                            stream=None):
     G = group_offsets.numel() - 1
+    fn, fp4, rows = "mx_grouped_scaled_gemm", fmt == MX_FMT_NVFP4, a.shape[0]
+    _need(fn, "group_offsets", group_offsets, 8 * (G + 1))
+    _need(fn, "a", a, rows * K // 2 if fp4 else rows * K)
+    _need(fn, "b", b, G * N * K // 2 if fp4 else G * N * K)
+    _need(fn, "alpha_a_rows", alpha_a_rows, 4 * rows if alpha_a_rows is not None else 0)
+    _need(fn, "alpha_b_groups", alpha_b_groups, 4 * G if alpha_b_groups is not None else 0)
+    _need(fn, "d", d, 2 * rows * N)
     _check("mx_grouped_scaled_gemm", lib().mx_grouped_scaled_gemm(
         fmt, G, _p(group_offsets), a.shape[0], _p(a), _p(sa), _p(alpha_a_rows), _p(b), _p(sb), _p(alpha_b_groups),
         N, K, _p(d), _stream(stream)))
@@ -332,6 +471,9 @@ def mx_count_mismatch(x, y, count, stream=None):
     n = x.numel() * x.element_size()
     if y.numel() * y.element_size() != n:
         raise ValueError("byte sizes differ")
+    _need("mx_count_mismatch", "x", x, n)
+    _need("mx_count_mismatch", "y", y, n)
+    _need("mx_count_mismatch", "count", count, 8)
     _check("mx_count_mismatch", lib().mx_count_mismatch(_p(x), _p(y), n, _p(count), _stream(stream)))
 
 

@@ -189,3 +189,37 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros((32, 32), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         mx.mx_quantize_mxfp8(x, q_row=torch.zeros((32, 32), dtype=torch.uint8), s_row=torch.zeros(512, dtype=torch.uint8))
+
+
+def test_binding_checks_buffer_sizes_before_any_device_call():
+    """The C ABI takes bare pointers, so the binding refuses undersized or non-contiguous buffers and
+    badly strided inputs itself (checked here on host tensors: the checks run before any pointer is taken)."""
+    import torch
+    import microscaled_precision_numerics_gb300 as mx
+    x = torch.zeros((256, 64), dtype=torch.bfloat16)
+    sb = mx.scale_bytes(256, 64, 32)
+    with pytest.raises(ValueError, match="q_row holds 16383 bytes, 16384 needed"):
+        mx.mx_quantize_mxfp8(x, q_row=torch.zeros(256 * 64 - 1, dtype=torch.uint8), s_row=torch.zeros(sb, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="s_col holds"):
+        mx.mx_quantize_mxfp8(x, q_col=torch.zeros(256 * 64, dtype=torch.uint8),
+                             s_col=torch.zeros(mx.scale_bytes(64, 256, 32) - 16, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="unit column stride"):
+        mx.mx_quantize_mxfp8(torch.zeros((64, 256), dtype=torch.bfloat16).t())
+    with pytest.raises(ValueError, match="contiguous"):
+        mx.mx_nvfp4_quantize_weight_2d(torch.zeros((2, 32, 64), dtype=torch.bfloat16).transpose(1, 2), None, None,
+                                       None, None, None, torch.zeros(16, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="s_tok holds"):
+        mx.mx_nvfp4_quantize_per_token(x, torch.zeros(256 * 32, dtype=torch.uint8),
+                                       torch.zeros(mx.scale_bytes(256, 64, 16), dtype=torch.uint8),
+                                       torch.zeros(255, dtype=torch.float32))
+    with pytest.raises(ValueError, match="y holds"):
+        mx.mx_dequantize_bf16(mx.MX_FMT_MXFP8, torch.zeros(256 * 64, dtype=torch.uint8),
+                              torch.zeros(sb, dtype=torch.uint8), None, 0, 256, 64, torch.zeros((255, 64), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="d must be a 2-D view"):
+        mx.mx_scaled_gemm(mx.MX_FMT_MXFP8, torch.zeros(128 * 128, dtype=torch.uint8),
+                          torch.zeros(mx.scale_bytes(128, 128, 32), dtype=torch.uint8), None, 0,
+                          torch.zeros(64 * 128, dtype=torch.uint8), torch.zeros(mx.scale_bytes(64, 128, 32), dtype=torch.uint8),
+                          None, 0, 128, 64, 128, torch.zeros((128, 32), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="count holds"):
+        mx.mx_count_mismatch(torch.zeros(64, dtype=torch.uint8), torch.zeros(64, dtype=torch.uint8),
+                             torch.zeros(1, dtype=torch.int32))
