@@ -139,7 +139,8 @@ mx_status mx_quantize_mxfp8_grouped(const void* x, int64_t rows, int64_t cols, i
  *   q_col  [G, H, O/2];  s_col G * mx_scale_bytes(H, O, 16)   (the same codes, transposed)
  *   s_w    [G] FP32
  *   workspace: mx_workspace_bytes(MX_WS_WEIGHT_2D, G, 0) bytes, 16-byte aligned, caller-owned.
- * Requires O % 16 == 0 and H % 16 == 0. */
+ * Requires O % 16 == 0 and H % 16 == 0; G <= 65535 and O <= 65535 * 64 (grid limits), else
+ * MX_ERR_UNSUPPORTED.  The same limits hold for every 2D weight entry point below. */
 mx_status mx_nvfp4_quantize_weight_2d(const void* w, int64_t G, int64_t O, int64_t H,
                                       uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                                       float* s_w, void* workspace, size_t workspace_bytes,
@@ -240,7 +241,8 @@ mx_status mx_rht16(const void* x, int64_t T, int64_t N, uint64_t seed, void* y, 
  * ctr = (i>>3 low, i>>3 high, 0, 0)); with a = |x*r| < 6 between grid points lo < hi, the code
  * rounds up iff (a - lo)/(hi - lo) > bits * 2^-16.
  *   x [T, N] BF16
- *   colwise = 1: q [N, T/2], s mx_scale_bytes(N, T, 16); requires T % 16 == 0, N % 8 == 0
+ *   colwise = 1: q [N, T/2], s mx_scale_bytes(N, T, 16); requires T % 16 == 0, N % 8 == 0,
+ *                T <= 65535 * 128 (grid limit)
  *   colwise = 0: q [T, N/2], s mx_scale_bytes(T, N, 16); requires N % 16 == 0; rht must be 0
  *   s_tensor: one FP32 (written);  workspace: mx_workspace_bytes(MX_WS_1X16, 0, 0) bytes. */
 mx_status mx_nvfp4_quantize_1x16(const void* x, int64_t T, int64_t N, int colwise, int rht,

@@ -29,6 +29,17 @@ inline cudaError_t per_device_once(PerDevice& pd, int& value, F&& f) {
     return pd.err[dev];
 }
 
+// Grid limits (grid y and z are at most 65535): the 2D weight quantizer launches one grid row per
+// W2D_TILE_ROWS matrix rows and one grid layer per matrix, the column-wise 1x16 quantizer one grid row
+// per CW_TILE_TOKENS tokens.  The entry points refuse larger shapes.
+constexpr int64_t MX_GRID_YZ_MAX = 65535;
+constexpr int W2D_TILE_ROWS = 64;
+constexpr int CW_TILE_TOKENS = 128;
+inline bool weight_2d_grid_ok(int64_t G, int64_t O) {
+    return G <= MX_GRID_YZ_MAX && (O + W2D_TILE_ROWS - 1) / W2D_TILE_ROWS <= MX_GRID_YZ_MAX;
+}
+inline bool colwise_grid_ok(int64_t T) { return (T + CW_TILE_TOKENS - 1) / CW_TILE_TOKENS <= MX_GRID_YZ_MAX; }
+
 // Bytes of a GEMM-layout scale tensor (see include/mxnum.h).
 __host__ __device__ inline int64_t host_scale_bytes(int64_t rows, int64_t k, int block) {
     return ((rows + 127) / 128) * ((k / block + 3) / 4) * 512;

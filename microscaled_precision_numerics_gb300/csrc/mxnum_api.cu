@@ -159,7 +159,7 @@ mx_status mx_nvfp4_quantize_weight_2d(const void* w, int64_t G, int64_t O, int64
     if (!aligned16(w) || !aligned16(q_row) || !aligned16(s_row) || !aligned16(q_col) || !aligned16(s_col) ||
         !aligned16(s_w) || !aligned16(workspace))
         return MX_ERR_ALIGNMENT;
-    if ((O % 16) != 0 || (H % 16) != 0) return MX_ERR_UNSUPPORTED;
+    if ((O % 16) != 0 || (H % 16) != 0 || !mxk::weight_2d_grid_ok(G, O)) return MX_ERR_UNSUPPORTED;
     return from_cuda(mxk::launch_nvfp4_weight_2d(static_cast<const uint16_t*>(w), G, O, H, q_row, s_row, q_col, s_col,
                                                   s_w, static_cast<uint32_t*>(workspace), mxk::device_sm_count(),
                                                   stream));
@@ -183,7 +183,7 @@ mx_status mx_nvfp4_quantize_weight_2d_46(const void* w, int64_t G, int64_t O, in
     if (!aligned16(w) || !aligned16(q_row) || !aligned16(s_row) || !aligned16(q_col) || !aligned16(s_col) ||
         !aligned16(s_w) || !aligned16(workspace))
         return MX_ERR_ALIGNMENT;
-    if ((O % 16) != 0 || (H % 16) != 0) return MX_ERR_UNSUPPORTED;
+    if ((O % 16) != 0 || (H % 16) != 0 || !mxk::weight_2d_grid_ok(G, O)) return MX_ERR_UNSUPPORTED;
     return from_cuda(mxk::launch_nvfp4_weight_2d(static_cast<const uint16_t*>(w), G, O, H, q_row, s_row, q_col, s_col,
                                                   s_w, static_cast<uint32_t*>(workspace), mxk::device_sm_count(),
                                                   stream, true));
@@ -242,7 +242,7 @@ mx_status mx_nvfp4_quantize_1x16(const void* x, int64_t T, int64_t N, int colwis
     if (!aligned16(x) || !aligned16(q) || !aligned16(s) || !aligned16(workspace)) return MX_ERR_ALIGNMENT;
     if (colwise) {
         if ((N % 8) != 0) return MX_ERR_ALIGNMENT;
-        if ((T % 16) != 0) return MX_ERR_UNSUPPORTED;
+        if ((T % 16) != 0 || !mxk::colwise_grid_ok(T)) return MX_ERR_UNSUPPORTED;
     } else {
         if (rht) return MX_ERR_UNSUPPORTED;
         if ((N % 16) != 0) return MX_ERR_UNSUPPORTED;
@@ -282,7 +282,7 @@ mx_status mx_nvfp4_quantize_weight_2d_given_amax(const void* w, int64_t G, int64
     if (!aligned16(w) || !aligned16(q_row) || !aligned16(s_row) || !aligned16(q_col) || !aligned16(s_col) ||
         !aligned16(s_w) || !aligned16(amax))
         return MX_ERR_ALIGNMENT;
-    if ((O % 16) != 0 || (H % 16) != 0) return MX_ERR_UNSUPPORTED;
+    if ((O % 16) != 0 || (H % 16) != 0 || !mxk::weight_2d_grid_ok(G, O)) return MX_ERR_UNSUPPORTED;
     return from_cuda(mxk::launch_nvfp4_weight_2d_given_amax(static_cast<const uint16_t*>(w), G, O, H, q_row, s_row,
                                                             q_col, s_col, s_w, amax, stream));
 }

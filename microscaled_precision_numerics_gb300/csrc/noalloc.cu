@@ -54,7 +54,7 @@ extern "C" mx_status mx_nvfp4_quantize_weight_2d_noalloc(const void* w, int64_t 
     if (!aligned16_na(w) || !aligned16_na(q_row) || !aligned16_na(s_row) || !aligned16_na(q_col) ||
         !aligned16_na(s_col) || !aligned16_na(s_w))
         return MX_ERR_ALIGNMENT;
-    if ((O % 16) != 0 || (H % 16) != 0) return MX_ERR_UNSUPPORTED;
+    if ((O % 16) != 0 || (H % 16) != 0 || !mxk::weight_2d_grid_ok(G, O)) return MX_ERR_UNSUPPORTED;
     uint32_t* scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess) return MX_ERR_CUDA;
     // the launcher zeroes scratch[0, G) on `stream` before accumulating into it

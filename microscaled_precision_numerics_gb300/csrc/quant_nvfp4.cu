@@ -302,7 +302,7 @@ nvfp4_1x16_flat_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, con
 // straight from registers into the transposed output (the 8 warps fill 64 contiguous bytes per
 // column, merged in L2); block scales are staged in shared memory and written as words.
 // ------------------------------------------------------------------------------------------------
-constexpr int CW_TOK = 128;
+constexpr int CW_TOK = CW_TILE_TOKENS;
 constexpr int CW_THREADS = 256;
 
 // Load a 16 x CPT micro-tile: xw[i] holds row i's CPT BF16 values as CPT / 2 words.
@@ -525,7 +525,7 @@ rht16_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint32_t sign
 // columns; lane l reads chunk (l & 15) of rows 2i + (l >> 4); the 16x16 tile amax combines lanes
 // l, l^1, l^16 over the 8 iterations.
 // ------------------------------------------------------------------------------------------------
-constexpr int W2_ROWS = 64;
+constexpr int W2_ROWS = W2D_TILE_ROWS;
 constexpr int W2_COLS = 128;
 
 __global__ void __launch_bounds__(256)

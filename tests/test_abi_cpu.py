@@ -223,3 +223,18 @@ def test_binding_checks_buffer_sizes_before_any_device_call():
     with pytest.raises(ValueError, match="count holds"):
         mx.mx_count_mismatch(torch.zeros(64, dtype=torch.uint8), torch.zeros(64, dtype=torch.uint8),
                              torch.zeros(1, dtype=torch.int32))
+
+
+def test_grid_limits_refused_before_launch(lib):
+    """Shapes beyond the launch grids' y / z limits are refused on the host (MX_ERR_UNSUPPORTED)."""
+    w2 = lib.mx_nvfp4_quantize_weight_2d
+    assert w2(A16, 65536, 32, 32, A16, A16, A16, A16, A16, A16, 1 << 20, NUL) == 3     # G > 65535
+    assert w2(A16, 1, 65535 * 64 + 16, 32, A16, A16, A16, A16, A16, A16, 16, NUL) == 3  # O / 64 > 65535
+    assert lib.mx_nvfp4_quantize_weight_2d_46(A16, 65536, 32, 32, A16, A16, A16, A16, A16, A16, 1 << 20, NUL) == 3
+    assert lib.mx_nvfp4_quantize_weight_2d_given_amax(A16, 65536, 32, 32, A16, A16, A16, A16, A16, A16, NUL) == 3
+    f = lib.mx_nvfp4_quantize_weight_2d_noalloc
+    f.restype, f.argtypes = ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + \
+        [ctypes.c_void_p] * 6
+    assert f(A16, 1, 65535 * 64 + 16, 32, A16, A16, A16, A16, A16, NUL) == 3
+    # column-wise 1x16: one grid row per 128 tokens
+    assert lib.mx_nvfp4_quantize_1x16(A16, 65535 * 128 + 16, 32, 1, 0, 0, 0, 0, A16, A16, A16, A16, 16, NUL) == 3
