@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import synthetic
-from gpu_util import DEV, bf16_dev, to_np
+from gpu_util import DEV, bf16_dev
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2

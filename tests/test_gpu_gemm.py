@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import synthetic
-from gpu_util import DEV, bf16_dev, first_mismatch, to_np
+from gpu_util import DEV, first_mismatch
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2

@@ -7,7 +7,6 @@ closed-form tie points.
 import math
 
 import numpy as np
-import pytest
 import torch
 
 from conftest import read_golden
