@@ -238,3 +238,30 @@ def test_grid_limits_refused_before_launch(lib):
     assert f(A16, 1, 65535 * 64 + 16, 32, A16, A16, A16, A16, A16, NUL) == 3
     # column-wise 1x16: one grid row per 128 tokens
     assert lib.mx_nvfp4_quantize_1x16(A16, 65535 * 128 + 16, 32, 1, 0, 0, 0, 0, A16, A16, A16, A16, 16, NUL) == 3
+
+
+def test_binding_alloc_helpers_satisfy_its_size_checks():
+    """Buffers from the alloc_* helpers pass the binding's size checks for ragged shapes: on host tensors the
+    call then stops only at the device check."""
+    import torch
+    import microscaled_precision_numerics_gb300 as mx
+    cpu = "cpu"
+    only_cuda = "CUDA tensors only"
+    for R, K in [(130, 96), (256, 1024), (1, 32)]:
+        x = torch.zeros((R, K), dtype=torch.bfloat16)
+        with pytest.raises(ValueError, match=only_cuda):
+            mx.mx_quantize_mxfp8(x, **mx.alloc_mxfp8(R, K, cpu, colwise=R % 32 == 0))
+        if K % 16 == 0:
+            o = mx.alloc_nvfp4_rows(R, K, cpu)
+            with pytest.raises(ValueError, match=only_cuda):
+                mx.mx_nvfp4_quantize_per_token(x, o["q"], o["s"], o["s2"])
+    for G, O, H in [(3, 48, 96), (1, 256, 2048)]:
+        w = torch.zeros((G, O, H), dtype=torch.bfloat16)
+        with pytest.raises(ValueError, match=only_cuda):
+            mx.mx_nvfp4_quantize_weight_2d(w, **{k: v for k, v in mx.alloc_nvfp4_weight_2d(G, O, H, cpu).items()
+                                                 if k != "ws"}, workspace=mx.alloc_nvfp4_weight_2d(G, O, H, cpu)["ws"])
+    offs = torch.tensor([0, 100, 100, 300], dtype=torch.int64)
+    x = torch.zeros((300, 64), dtype=torch.bfloat16)
+    o = mx.alloc_nvfp4_rows_grouped(300, 3, 64, cpu)
+    with pytest.raises(ValueError, match=only_cuda):
+        mx.mx_nvfp4_quantize_per_token_grouped(x, offs, o["q"], o["s"], o["s2"])
