@@ -58,6 +58,7 @@ def lib() -> ctypes.CDLL:
                 "mx_grouped_scale_bytes": (I64, [I64, I64, I64, I32]),
                 "mx_nvfp4_quantize_weight_2d": (I32, [P, I64, I64, I64, P, P, P, P, P, P, SZ, P]),
                 "mx_nvfp4_quantize_weight_2d_46": (I32, [P, I64, I64, I64, P, P, P, P, P, P, SZ, P]),
+                "mx_nvfp4_quantize_weight_2d_noalloc": (I32, [P, I64, I64, I64, P, P, P, P, P, P]),
                 "mx_rht16": (I32, [P, I64, I64, U64, P, P]),
                 "mx_fp8_blockwise_quantize_1x128": (I32, [P, I64, I64, I64, I32, P, P, P, P, P, P, P]),
                 "mx_fp8_blockwise_quantize_128x128": (I32, [P, I64, I64, I64, I32, P, P, P, P, P, P]),
@@ -307,9 +308,6 @@ def mx_nvfp4_quantize_weight_2d_noalloc(w, q_row, s_row, q_col, s_col, s_w, stre
     G, O, H = w.shape
     _weight_2d_outputs("mx_nvfp4_quantize_weight_2d_noalloc", G, O, H, q_row, s_row, q_col, s_col, s_w)
     f = lib().mx_nvfp4_quantize_weight_2d_noalloc
-    P, I64 = ctypes.c_void_p, ctypes.c_int64
-    f.restype = ctypes.c_int
-    f.argtypes = [P, I64, I64, I64, P, P, P, P, P, P]
     if G > MX_NOALLOC_MAX_MATRICES:
         raise ValueError(f"{G} matrices exceed the allocation-free limit of {MX_NOALLOC_MAX_MATRICES}")
     _check("mx_nvfp4_quantize_weight_2d_noalloc", f(
