@@ -33,7 +33,7 @@ def _rank_main(rank, world, port, out):
 
 def test_slowest_rank_sets_the_step_time_two_gloo_ranks():
     world, port = 2, _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()          # no fork of this multi-threaded process
     mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
     for rank in range(world):
         ms, rate = out[rank]
