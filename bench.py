@@ -34,8 +34,16 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "quantize GB/s vs ~8 TB/s HBM; MXFP8/NVFP4 scaled-GEMM TFLOP/s vs dense peak"
-FP8_OVER_BF16 = 2.0      # nominal dense ratio: 4.5 / 2.25 PFLOP/s
-FP4_OVER_BF16 = 6.0      # nominal dense ratio: 13.5 / 2.25 PFLOP/s
+# Tensor peaks of the GEMMs' own types from the measured BF16 peak: NVIDIA's per-GPU dense figures for
+# the 8-GPU HGX B300 board (BF16 2.25, FP8 4.5, NVFP4 13.5 PFLOP/s; its datasheet prints 36 / 72 / 144
+# PFLOP/s per board with 2:4 sparsity for BF16 and FP8, and 108 dense for FP4) fix the ratios.
+FP8_OVER_BF16 = 2.0
+FP4_OVER_BF16 = 6.0
+# Published dense peaks of one GB300 (the GB300 NVL72 specification: FP4 1,080 PFLOP/s dense, FP8/FP6
+# 720 and FP16/BF16 360 PFLOP/s with 2:4 sparsity, per 72 GPUs), the denominators of the >= 60 % bar.
+DATASHEET = {"bf16": 2500.0, "fp8": 5000.0, "fp4": 15000.0,
+             "source": "GB300 NVL72 specification / 72 GPUs, dense (FP4 1080 PF dense; FP8 720 and BF16 360 PF "
+                       "sparse, halved)"}
 
 
 def recorded_traffic(kernel: str):
@@ -126,6 +134,52 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------------------
 # workloads on the device
 # ------------------------------------------------------------------------------------------------
+class Tiny:
+    """The tiny check: MXFP8 row + column quantize of X [256, 1024] (N(0, 1) with 0.5 % outliers x50, an
+    all-zero block and a subnormal-only block) and W [512, 1024] N(0, 0.02) in one launch, the
+    dequantize round trip of X, and the MXFP8 FPROP GEMM 256 x 512 x 1024 with BF16 output.  Every
+    kernel here is latency-bound (a few microseconds each)."""
+    name = "tiny"
+    unit = "TFLOP/s"
+    dtype = "e4m3 (f32 accumulate, bf16 out)"
+
+    def __init__(self, mx, torch, dev, data=None):
+        import synthetic
+        self.mx, self.torch, self.dev = mx, torch, dev
+        d = data or synthetic.tiny()
+        bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.x, self.w = bf(d["x"]), bf(d["w"])
+        self.M, self.K = self.x.shape
+        self.N = self.w.shape[0]
+        self.qx = mx.alloc_mxfp8(self.M, self.K, dev)
+        self.qw = mx.alloc_mxfp8(self.N, self.K, dev)
+        self.xdq = torch.empty_like(self.x)
+        self.y = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=dev)
+        self.launches_per_step = 3
+
+    def ops(self):
+        mx, M, N, K = self.mx, self.M, self.N, self.K
+        return [
+            ("quant", "mxfp8 row+col X+W (one launch)", 1, (M + N) * K * (2 + 2 + 2 / 32),
+             lambda: mx.mx_quantize_mxfp8_batched([(self.x, self.qx), (self.w, self.qw)])),
+            ("dq", "mxfp8 DQ X", 1, M * K * (1 + 1 / 32 + 2),
+             lambda: mx.mx_dequantize_bf16(mx.MX_FMT_MXFP8, self.qx["q_row"], self.qx["s_row"], None, 0, M, K, self.xdq)),
+            ("gemm8", "FPROP", 0, 2.0 * M * N * K,
+             lambda: mx.mx_scaled_gemm(mx.MX_FMT_MXFP8, self.qx["q_row"], self.qx["s_row"], None, 0, self.qw["q_row"],
+                                       self.qw["s_row"], None, 0, M, N, K, self.y)),
+        ]
+
+    def e2e_inputs(self):
+        return [self.x, self.w]
+
+    def e2e_outputs(self):
+        return [self.y, self.xdq]
+
+    def config(self):
+        return {"workload": "tiny: MXFP8 row+col quantize X 256x1024 + W 512x1024, DQ round trip, FPROP 256x512x1024",
+                "note": "latency-bound at this size (parity case)"}
+
+
 class DenseMLP:
     """MXFP8 quantize X, W, dY (row + column) + FPROP, DGRAD, WGRAD (Qwen3-8B MLP shapes)."""
     name = "dense_mlp"
@@ -238,15 +292,18 @@ class MoE:
     down-projection input, and DQ(Q(w)) of both weight stacks."""
     name = "moe"
 
-    def __init__(self, mx, torch, dev, experts=128):
+    unit = "TFLOP/s"
+
+    def __init__(self, mx, torch, dev, experts=128, data=None):
         import synthetic
         self.mx, self.torch, self.dev = mx, torch, dev
-        d = synthetic.moe(experts=experts)
+        d = data or synthetic.moe(experts=experts)
         bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
         x = bf(d["x"])
         self.rows = int(d["group_offsets"][-1])
         # the expert-sorted activation rows are the GEMM's input (the routing gather is setup)
         self.a = x.index_select(0, torch.from_numpy(d["row_token"]).to(dev)).contiguous()
+        del x
         self.down_in = bf(d["down_in"])
         self.wgu = bf(d["w_gate_up"])
         self.wd = bf(d["w_down"])
@@ -304,6 +361,12 @@ class MoE:
     def config(self):
         return {"workload": "moe: Qwen3-30B-A3B expert layer, NVFP4 per-token + 2D weights + grouped GEMMs + DQ(Q(w))",
                 "tokens": 8192, "routed_rows": self.rows, "experts": self.G, "hidden": self.H, "ffn": self.F}
+
+    def e2e_inputs(self):
+        return [self.a, self.down_in, self.wgu, self.wd]
+
+    def e2e_outputs(self):
+        return [self.y1, self.y2, self.dq_gu, self.dq_d]
 
 
     def aux_ops(self):
@@ -397,11 +460,12 @@ class WGrad:
     """Llama-3-8B MLP WGRAD in NVFP4: RHT16 along tokens + 1x16 column-wise quantize with a
     per-tensor scale (SR on dY, RNE on X), then dW = dY^T X over K = 32768 tokens."""
     name = "wgrad"
+    unit = "TFLOP/s"
 
-    def __init__(self, mx, torch, dev):
+    def __init__(self, mx, torch, dev, data=None):
         import synthetic
         self.mx, self.torch, self.dev = mx, torch, dev
-        d = synthetic.wgrad()
+        d = data or synthetic.wgrad()
         bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
         self.x, self.dy = bf(d["x"]), bf(d["dy"])
         self.rht_seed, self.sr_seed = d["rht_seed"], d["sr_seed"]
@@ -442,6 +506,12 @@ class WGrad:
     def config(self):
         return {"workload": "wgrad: Llama-3-8B MLP WGRAD, RHT16 + NVFP4 1x16 colwise (SR dY, RNE X) + NVFP4 GEMM",
                 "tokens": self.T, "hidden": self.H, "ffn": self.F}
+
+    def e2e_inputs(self):
+        return [self.x, self.dy]
+
+    def e2e_outputs(self):
+        return [self.dw]
 
 
 class DenseBlockwise:
@@ -618,6 +688,7 @@ class WeightSync:
     dequantize for the re-quantize), so the 2D quantizer reads its input once.  One layer's weights are
     drawn on the device per step (torch generator seeded 1000 + layer) outside the timed kernels."""
     name = "weight_sync"
+    unit = "GB/s"
 
     def __init__(self, mx, torch, dev, layers=48, experts=128):
         self.mx, self.torch, self.dev = mx, torch, dev
@@ -679,6 +750,12 @@ class WeightSync:
         return {"workload": "weight_sync: 48 layers x 128 experts x {2048x768, 768x2048, 768x2048}, MXFP8 + NVFP4-2D "
                             "quantize, dequantize, re-quantize, byte compare (matrix maxima carried into the 2D quantizer)",
                 "layers": self.layers}
+
+    def e2e_inputs(self):
+        return [b["w"] for b in self.bufs]
+
+    def e2e_outputs(self):
+        return [self.count]
 
 
 def max_over_ranks(x: float, dist=None, device=None) -> float:
@@ -748,6 +825,16 @@ def time_ops(ops, torch, steps, warmup):
     return start.elapsed_time(end), per_op
 
 
+def tensor_peaks(kind, peaks):
+    """(measured-derived peak, published dense peak, report key) in TFLOP/s for a GEMM op kind:
+    gemm8 = FP8, gemm16 = BF16, otherwise NVFP4."""
+    if kind == "gemm8":
+        return peaks["bf16_tflops"] * FP8_OVER_BF16, DATASHEET["fp8"], "frac_fp8_peak"
+    if kind == "gemm16":
+        return peaks["bf16_tflops"], DATASHEET["bf16"], "frac_bf16_peak"
+    return peaks["bf16_tflops"] * FP4_OVER_BF16, DATASHEET["fp4"], "frac_fp4_peak"
+
+
 def op_report(ops, per_op, peaks):
     """Achieved rate and roofline fraction per op: byte-moving ops against the HBM copy bandwidth;
     FP4 GEMMs against the FP4 peak and, when the op carries its minimum HBM traffic (a sixth tuple
@@ -761,11 +848,10 @@ def op_report(ops, per_op, peaks):
             ach = units / (ms / 1e3) / 1e9
             rep[label] = {"ms": round(ms, 4), "GBps": round(ach, 1), "frac_hbm": round(ach / peaks["hbm_gbs"], 4)}
         else:
-            ratio, tag = {"gemm8": (FP8_OVER_BF16, "frac_fp8_peak"), "gemm16": (1.0, "frac_bf16_peak")}.get(
-                kind, (FP4_OVER_BF16, "frac_fp4_peak"))
-            peak = peaks["bf16_tflops"] * ratio
+            peak, ds, tag = tensor_peaks(kind, peaks)
             ach = units / (ms / 1e3) / 1e12
-            rep[label] = {"ms": round(ms, 4), "TFLOPs": round(ach, 1), tag: round(ach / peak, 4)}
+            rep[label] = {"ms": round(ms, 4), "TFLOPs": round(ach, 1), tag: round(ach / peak, 4),
+                          "frac_datasheet": round(ach / ds, 4)}
             if mem:
                 t_flop = units / (peak * 1e12) * 1e3
                 t_mem = mem / (peaks["hbm_gbs"] * 1e9) * 1e3
@@ -779,6 +865,169 @@ def op_report(ops, per_op, peaks):
     return rep, by_kind
 
 
+def kind_roofline(kind, kms, kunits, is_bytes, kmem, peaks):
+    """Roofline of the ops of one kind taken together: HBM for byte-moving ops; for GEMMs the tensor
+    peak of their type, or HBM on their minimum traffic when that takes longer at peak."""
+    if is_bytes:
+        ach = kunits / (kms / 1e3) / 1e9
+        return {"kernel": kind, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                "peak_source": f"{peaks['source']} copy bandwidth"}
+    tpeak, ds, _ = tensor_peaks(kind, peaks)
+    ach = kunits / (kms / 1e3) / 1e12
+    ratio = tpeak / peaks["bf16_tflops"]
+    roof = {"kernel": kind, "bound": "tensor", "achieved": round(ach, 1), "peak": round(tpeak, 1), "unit": "TFLOP/s",
+            "frac": round(ach / tpeak, 4), "traffic": None,
+            "peak_source": f"{peaks['source']} bf16 burst x {ratio:g} (nominal dense ratio)",
+            "datasheet_peak": ds, "frac_datasheet": round(ach / ds, 4), "datasheet_source": DATASHEET["source"]}
+    if kmem and kmem / (peaks["hbm_gbs"] * 1e9) > kunits / (tpeak * 1e12):
+        gbs = kmem / (kms / 1e3) / 1e9
+        roof.update({"bound": "hbm", "min_hbm_bytes": int(kmem), "achieved_GBps": round(gbs, 1),
+                     "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "note": "the minimum HBM traffic takes longer at peak than the flops: frac is against HBM"})
+    return roof
+
+
+def step_units(work, ops):
+    """Work per step in the config's unit base: its GEMM flops (reported in TFLOP/s) or its algorithmic
+    bytes (reported in GB/s)."""
+    if work.unit == "GB/s":
+        return sum(op[3] for op in ops if op[2])
+    return sum(op[3] for op in ops if not op[2])
+
+
+def unit_scale(unit):
+    return 1e9 if unit == "GB/s" else 1e12
+
+
+def step_value(work, ops, ms):
+    return step_units(work, ops) / (ms / 1e3) / unit_scale(work.unit)
+
+
+def dominant_roofline(ops, per_op, peaks):
+    kinds = {}
+    for op, ms in zip(ops, per_op):
+        k = kinds.setdefault(op[0], [0.0, 0.0, op[2], 0.0])
+        k[0] += ms
+        k[1] += op[3]
+        k[3] += op[5] if len(op) > 5 and op[5] else 0.0
+    kind, (kms, kunits, is_bytes, kmem) = max(kinds.items(), key=lambda kv: kv[1][0])
+    return kind_roofline(kind, kms, kunits, is_bytes, kmem, peaks)
+
+
+def e2e_generic(work, torch, steps, ops=None, units_per_step=None, warmup=2):
+    """End to end through the same calls: every step copies the step's inputs in from pinned host
+    memory, runs the ops and copies the results out to pinned host memory, one after the other on the
+    current stream (no overlap); CUDA events around all steps."""
+    ins, outs = work.e2e_inputs(), work.e2e_outputs()
+    ops = ops if ops is not None else work.ops()
+    h_in = [t.cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+
+    def step():
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        for op in ops:
+            op[4]()
+        for d, h in zip(outs, h_out):
+            h.copy_(d, non_blocking=True)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    units = units_per_step if units_per_step is not None else step_units(work, ops)
+    value = units / (ms / 1e3) / unit_scale(work.unit)
+    out = {"value": round(value, 2), "unit": work.unit, "ms_per_step": round(ms, 4), "steps": steps,
+           "h2d_bytes_per_step": int(sum(h.numel() * h.element_size() for h in h_in)),
+           "d2h_bytes_per_step": int(sum(h.numel() * h.element_size() for h in h_out)),
+           "note": "inputs copied in from pinned host memory, kernels, results copied out, every step, serially"}
+    del h_in, h_out
+    return out
+
+
+def measure(work, torch, mx, peaks, steps, warmup, e2e=True, gpu_index=0):
+    """Device-timed steps of a workload (CUDA events per op), its roofline, clocks and end-to-end run."""
+    ops = work.ops()
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    total_ms, per_op = time_ops(ops, torch, steps, warmup)
+    clocks = sampler.stop()
+    status = mx.mx_check_device_status()
+    ms = total_ms / steps
+    rep, _ = op_report(ops, per_op, peaks)
+    out = {"value": round(step_value(work, ops, ms), 2), "unit": work.unit, "ms_per_step": round(ms, 4),
+           "steps": steps, "warmup": warmup, "dtype": getattr(work, "dtype", "e2m1 (f32 accumulate, bf16 out)"),
+           "config": work.config(), "per_op": rep, "roofline": dominant_roofline(ops, per_op, peaks),
+           "clocks": clocks, "gpu_launches": work.launches_per_step * steps,
+           "watchdog": "ok" if status == 0 else f"status {status}"}
+    if hasattr(work, "aux_ops"):
+        aops = work.aux_ops()
+        if aops:
+            _, aper = time_ops(aops, torch, steps, warmup)
+            out["aux"], _ = op_report(aops, aper, peaks)
+    if e2e and hasattr(work, "e2e_inputs"):
+        out["e2e"] = e2e_generic(work, torch, steps, ops)
+    return out
+
+
+def measure_weight_sync(work, torch, mx, peaks, warmup, e2e=True, gpu_index=0):
+    """The weight-sync sweep: one layer per step (its weights drawn on the device before its ops, outside
+    the timed kernels), every layer once; the value is all layers' algorithmic bytes over their time."""
+    ops = work.ops()
+    acc = [0.0] * len(ops)
+    sampler = ClockSampler(gpu_index)
+    work.count.zero_()
+    sampler.start()
+    for layer in range(work.layers):
+        work.draw(layer)
+        _, per = time_ops(ops, torch, 1, warmup if layer == 0 else 0)
+        acc = [a + b for a, b in zip(acc, per)]
+    clocks = sampler.stop()
+    status = mx.mx_check_device_status()
+    mismatched = int(work.count.item())
+    total_ms = sum(acc)
+    bytes_layer = sum(op[3] for op in ops)
+    value = bytes_layer * work.layers / (total_ms / 1e3) / 1e9
+    per_op = [a / work.layers for a in acc]
+    rep, _ = op_report(ops, per_op, peaks)
+    out = {"value": round(value, 1), "unit": "GB/s", "ms_per_step": round(total_ms / work.layers, 4),
+           "steps": work.layers, "warmup": warmup, "dtype": "bf16 -> e4m3/e2m1 codes",
+           "config": work.config(), "per_op": rep, "roofline": dominant_roofline(ops, per_op, peaks),
+           "frac_hbm": round(value / peaks["hbm_gbs"], 4), "mismatched_bytes": mismatched, "clocks": clocks,
+           "gpu_launches": work.launches_per_step * work.layers,
+           "watchdog": "ok" if status == 0 else f"status {status}",
+           "data": "per-layer N(0, 0.02) draws on the device, seed 1000 + layer"}
+    if e2e:
+        work.draw(0)
+        out["e2e"] = e2e_generic(work, torch, work.layers, ops, units_per_step=bytes_layer)
+        out["e2e"]["note"] += "; one layer per step (layer 0's bytes from the host each time)"
+    return out
+
+
+def make_workload(name, mx, torch, dev, args, data=None):
+    if name == "tiny":
+        return Tiny(mx, torch, dev, data=data)
+    if name == "moe":
+        return MoE(mx, torch, dev, experts=args.experts, data=data)
+    if name == "moe_mxfp8":
+        return MoE8(mx, torch, dev, experts=args.experts)
+    if name == "dense_fp8_blockwise":
+        return DenseBlockwise(mx, torch, dev)
+    if name == "dense_nvfp4":
+        return DenseNVFP4(mx, torch, dev)
+    if name == "wgrad":
+        return WGrad(mx, torch, dev, data=data)
+    if name == "weight_sync":
+        return WeightSync(mx, torch, dev, layers=args.layers, experts=args.experts)
+    raise ValueError(name)
+
+
 def run_workload(args):
     import torch
     import microscaled_precision_numerics_gb300 as mx
@@ -786,76 +1035,16 @@ def run_workload(args):
     dev = torch.device("cuda:0")
     mx.lib()
     peaks = load_peaks()
-    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
-    sampler = ClockSampler(0)
+    work = make_workload(args.workload, mx, torch, dev, args)
     if args.workload == "weight_sync":
-        work = WeightSync(mx, torch, dev, layers=args.layers, experts=args.experts)
-        ops = work.ops()
-        acc = [0.0] * len(ops)
-        total_ms = 0.0
-        sampler.start()
-        for layer in range(work.layers):
-            work.draw(layer)
-            t_ms, per = time_ops(ops, torch, 1, args.warmup if layer == 0 else 0)
-            total_ms += sum(per)
-            acc = [a + b for a, b in zip(acc, per)]
-        clocks = sampler.stop()
-        mx.check_device_status()
-        per_op = acc
-        bytes_total = sum(op[3] for op in ops) * work.layers
-        value = bytes_total / (total_ms / 1e3) / 1e9
-        rep, by_kind = op_report(ops, [p / work.layers for p in per_op], peaks)
-        line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": work.layers,
-                "warmup": args.warmup, "ms_per_step": round(total_ms / work.layers, 4), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16 -> e4m3/e2m1 codes",
-                "data": "synthetic (per-layer N(0, 0.02) draws on the device, seed 1000 + layer)",
-                "config": work.config(), "frac_hbm": round(value / peaks["hbm_gbs"], 4),
-                "mismatched_bytes": int(work.count.item()), "per_op": rep, "clocks": clocks,
-                "gpu_launches": work.launches_per_step * work.layers}
-        print(json.dumps(line), flush=True)
-        return
-    if args.workload == "moe":
-        work = MoE(mx, torch, dev, experts=args.experts)
-    elif args.workload == "moe_mxfp8":
-        work = MoE8(mx, torch, dev, experts=args.experts)
-    elif args.workload == "dense_fp8_blockwise":
-        work = DenseBlockwise(mx, torch, dev)
-    elif args.workload == "dense_nvfp4":
-        work = DenseNVFP4(mx, torch, dev)
+        res = measure_weight_sync(work, torch, mx, peaks, args.warmup, e2e=not args.no_e2e)
     else:
-        work = WGrad(mx, torch, dev)
-    ops = work.ops()
-    sampler.start()
-    total_ms, per_op = time_ops(ops, torch, args.steps, args.warmup)
-    clocks = sampler.stop()
-    aux = {}
-    if hasattr(work, "aux_ops"):
-        aops = work.aux_ops()
-        _, aper = time_ops(aops, torch, args.steps, args.warmup)
-        aux, _ = op_report(aops, aper, peaks)
-    mx.check_device_status()
-    rep, by_kind = op_report(ops, per_op, peaks)
-    flops = sum(op[3] for op in ops if not op[2])
-    ms = total_ms / args.steps
-    value = flops / (ms / 1e3) / 1e12
-    dominant = max(by_kind.items(), key=lambda kv: kv[1][0])
-    kind, (kms, kunits, is_bytes) = dominant
-    if is_bytes:
-        ach = kunits / (kms / 1e3) / 1e9
-        roof = {"kernel": kind, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None}
-    else:
-        ratio = FP8_OVER_BF16 if kind == "gemm8" else FP4_OVER_BF16
-        tpeak = peaks["bf16_tflops"] * ratio
-        ach = kunits / (kms / 1e3) / 1e12
-        roof = {"kernel": kind, "bound": "tensor", "achieved": round(ach, 1), "peak": round(tpeak, 1),
-                "unit": "TFLOP/s", "frac": round(ach / tpeak, 4), "traffic": None,
-                "peak_source": f"{peaks['source']} bf16 burst x {ratio:g} (nominal {'FP8' if ratio == FP8_OVER_BF16 else 'FP4'}/BF16)"}
-    line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": getattr(work, "dtype", "e2m1 (f32 accumulate, bf16 out)"), "data": "synthetic (seeded numpy draws)",
-            "config": work.config(), "per_op": rep, "aux": aux, "roofline": roof, "clocks": clocks,
-            "gpu_launches": work.launches_per_step * args.steps}
+        res = measure(work, torch, mx, peaks, args.steps, args.warmup, e2e=not args.no_e2e)
+    line = {"metric": METRIC, "value": res.pop("value"), "unit": res.pop("unit"), "n_gpus": 1,
+            "steps": res.pop("steps"), "warmup": res.pop("warmup"), "ms_per_step": res.pop("ms_per_step"),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": res.pop("dtype"),
+            "data": res.pop("data", "synthetic (seeded draws)")}
+    line.update(res)
     print(json.dumps(line), flush=True)
 
 
@@ -875,10 +1064,16 @@ def run_device(args):
     dev = torch.device(f"cuda:{local}")
     mx.lib()
 
-    # the CPU baseline runs before any GPU work (oracle threads, no forked pool after CUDA init)
+    # the CPU baselines run before any GPU work (oracle threads, no forked pool after CUDA init)
     cpu = None
+    run_configs = world == 1 and not args.no_configs
+    cfg_data, cfg_cpu = {}, {}
+    if run_configs:
+        cfg_data = config_inputs()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload)
+        if run_configs:
+            cfg_cpu = cpu_baseline_configs(cfg_data)
 
     work = DenseMLP(mx, torch, dev)
     peaks = load_peaks()
@@ -911,6 +1106,12 @@ def run_device(args):
                     "traffic": recorded_traffic("mxfp8_quantize_kernel<row,col> batched"),
                     "peak_source": f"{peaks['source']} copy bandwidth"}
 
+    launches = work.launches_per_step * args.steps
+    T, H, F, gemm_flops = work.T, work.H, work.F, list(work.gemm_flops)
+    labels = [(k, lbl) for (k, lbl, _) in ops]
+    del ops
+    roofline.update({"datasheet_peak": DATASHEET["fp8"], "frac_datasheet": round(gemm_tflops / DATASHEET["fp8"], 4),
+                     "datasheet_source": DATASHEET["source"]} if dominant == "gemm" else {})
     e2e = None
     if not args.no_e2e:
         work.e2e_setup()
@@ -925,6 +1126,23 @@ def run_device(args):
                "h2d_bytes_per_step": work.h2d, "d2h_bytes_per_step": work.d2h,
                "note": "pinned host inputs in, BF16 results out, every step; copies of neighbouring steps overlap the kernels"}
 
+    # the other four configurations, one after the other on this GPU (single-GPU runs only)
+    configs = {}
+    if run_configs:
+        del work
+        torch.cuda.empty_cache()
+        for key, name in (("C1_tiny", "tiny"), ("C3_moe", "moe"), ("C4_wgrad", "wgrad"),
+                          ("C5_weight_sync", "weight_sync")):
+            w = make_workload(name, mx, torch, dev, args, data=cfg_data.pop(name, None))
+            if name == "weight_sync":
+                res = measure_weight_sync(w, torch, mx, peaks, args.warmup, e2e=not args.no_e2e, gpu_index=local)
+            else:
+                res = measure(w, torch, mx, peaks, args.steps, args.warmup, e2e=not args.no_e2e, gpu_index=local)
+            res["cpu_baseline"] = cfg_cpu.get(name)
+            configs[key] = res
+            del w
+            torch.cuda.empty_cache()
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -932,22 +1150,24 @@ def run_device(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (f32 accumulate, bf16 out)",
             "data": "synthetic (seeded numpy draws; no dataset or trained weights needed)",
             "config": {"workload": "dense_mlp: Qwen3-8B MLP linear, MXFP8 quantize X/W/dY row+col + FPROP/DGRAD/WGRAD",
-                       "tokens": work.T, "hidden": work.H, "ffn": work.F, "parallelism": f"replicas x{world}",
+                       "tokens": T, "hidden": H, "ffn": F, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (369 MB BF16 read per step, 129 MB L2)"},
             "components": {
                 "quantize_ms": round(quant_ms, 4), "quantize_GBps": round(quant_gbs, 1),
                 "quantize_frac_hbm": round(quant_gbs / peaks["hbm_gbs"], 4),
                 "gemm_ms": round(gemm_ms, 4), "gemm_TFLOPs": round(gemm_tflops, 1),
-                "per_op_ms": {lbl: round(per_op[i], 4) for i, (_, lbl, _) in enumerate(ops)},
-                "per_gemm_TFLOPs": {lbl: round(work.gemm_flops[j] / (per_op[i] / 1e3) / 1e12, 1)
-                                    for j, (i, (_, lbl, _)) in enumerate([(i, o) for i, o in enumerate(ops) if o[0] == "gemm"])},
+                "per_op_ms": {lbl: round(per_op[i], 4) for i, (_, lbl) in enumerate(labels)},
+                "per_gemm_TFLOPs": {lbl: round(gemm_flops[j] / (per_op[i] / 1e3) / 1e12, 1)
+                                    for j, (i, (_, lbl)) in enumerate([(i, o) for i, o in enumerate(labels) if o[0] == "gemm"])},
             },
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": work.launches_per_step * args.steps,
+            "gpu_launches": launches,
             "clocks": clocks,
         }
+        if configs:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
@@ -1009,6 +1229,127 @@ def cpu_baseline(workload: str, data=None):
             "seconds": round(dt, 2), "repetitions": reps, "sample": sample_text(data)}
 
 
+# Algorithmic bytes per element of one weight-sync pass, the sum of the per-op counts WeightSync.ops()
+# uses: MXFP8 quantize row+col, dequantize, re-quantize row-wise, compare codes and scales; NVFP4 2D
+# quantize, dequantize, re-quantize, compare both code copies and the row scales.
+WS_BYTES_PER_ELEM = ((2 + 2 + 2 / 32) + (1 + 1 / 32 + 2) + (2 + 1 + 1 / 32) + 2 * (1 + 1 / 32)
+                     + (2 + 1 + 2 / 16) + (0.5 + 1 / 16 + 2) + (2 + 1 + 2 / 16) + 2 * (0.5 + 0.5 + 2 / 16))
+
+
+def oracle_tiny(orc, d):
+    """The whole tiny check on the oracle: MXFP8 row + column quantize of X and W, the dequantize of X,
+    the FP64 FPROP reference.  Returns the step's GEMM flops."""
+    x, w = d["x"], d["w"]
+    qx, sx = orc.mxfp8_quantize_rowwise(x)
+    orc.mxfp8_quantize_colwise(x)
+    qw, sw = orc.mxfp8_quantize_rowwise(w)
+    orc.mxfp8_quantize_colwise(w)
+    orc.dequant_mxfp8(qx, sx)
+    orc.gemm_ref_mxfp8(qx, sx, qw, sw)
+    return 2.0 * x.shape[0] * w.shape[0] * x.shape[1]
+
+
+def oracle_moe(orc, d):
+    """Expert 0's slice of the MoE layer: its routed rows (per-token NVFP4 of the activations and of the
+    down-projection input), its gate|up and down weights (16x16 NVFP4, DQ(Q(w))), and the FP64 references
+    of its two grouped GEMMs.  Returns their flops."""
+    o0, o1 = int(d["group_offsets"][0]), int(d["group_offsets"][1])
+    a = np.ascontiguousarray(d["x"][d["row_token"][o0:o1]])
+    dn = np.ascontiguousarray(d["down_in"][o0:o1])
+    qa, sa, ta = orc.nvfp4_quantize_per_token(a)
+    qd, sd, td = orc.nvfp4_quantize_per_token(dn)
+    wgu, wd = np.ascontiguousarray(d["w_gate_up"][0]), np.ascontiguousarray(d["w_down"][0])
+    q1, _, t1, s1 = orc.nvfp4_quantize_weight_2d(wgu)
+    q2, _, t2, s2 = orc.nvfp4_quantize_weight_2d(wd)
+    r1, r2 = orc.weight_2d_operand_scales(t1, "row"), orc.weight_2d_operand_scales(t2, "row")
+    orc.dequant_nvfp4(q1, r1, s1, per_row=False)
+    orc.dequant_nvfp4(q2, r2, s2, per_row=False)
+    orc.gemm_ref_nvfp4(qa, sa, ta, q1, r1, s1)
+    orc.gemm_ref_nvfp4(qd, sd, td, q2, r2, s2)
+    m = o1 - o0
+    return 2.0 * m * wgu.shape[0] * wgu.shape[1] + 2.0 * m * wd.shape[0] * wd.shape[1]
+
+
+WGRAD_SLICE = 32
+
+
+def oracle_wgrad(orc, d):
+    """1/32 of the columns of the WGRAD path over all 32768 tokens: RHT16 + column-wise NVFP4 (both passes)
+    of X[:, :128] (RNE) and dY[:, :448] (SR), each slab taken as its own tensor, and the FP64 reference of
+    dW[:448, :128].  Returns its flops."""
+    H, F = d["x"].shape[1] // WGRAD_SLICE, d["dy"].shape[1] // WGRAD_SLICE
+    x = np.ascontiguousarray(d["x"][:, :H])
+    dy = np.ascontiguousarray(d["dy"][:, :F])
+    qx, sx, Sx = orc.nvfp4_quantize_1x16(x, True, True, d["rht_seed"], False, 0)
+    qd, sd, Sd = orc.nvfp4_quantize_1x16(dy, True, True, d["rht_seed"], True, d["sr_seed"])
+    orc.gemm_ref_nvfp4(qd, sd, Sd, qx, sx, Sx)
+    return 2.0 * F * H * x.shape[0]
+
+
+def weight_sync_sample(matrices=("down", "gate", "up")):
+    """Expert 0 of the chosen matrices of layer 0 (host draws of the same shape and distribution)."""
+    import synthetic
+    shapes = {"down": (2048, 768), "gate": (768, 2048), "up": (768, 2048)}
+    return [synthetic.normal(np.random.default_rng([1000, i, 0]), shapes[m], 0.02) for i, m in enumerate(matrices)]
+
+
+def oracle_weight_sync(orc, mats):
+    """One weight-sync pass over each matrix: MXFP8 quantize (row + column), dequantize, re-quantize and
+    byte compare; NVFP4 16x16 quantize, dequantize, re-quantize and byte compare.  Returns the algorithmic
+    bytes (the same per-element count as the GPU pass)."""
+    total = 0.0
+    for w in mats:
+        qr, sr = orc.mxfp8_quantize_rowwise(w)
+        orc.mxfp8_quantize_colwise(w)
+        q2, s2 = orc.mxfp8_quantize_rowwise(orc.dequant_mxfp8(qr, sr))
+        assert np.array_equal(q2, qr) and np.array_equal(s2, sr)
+        n1, n1c, t1, sw = orc.nvfp4_quantize_weight_2d(w)
+        y = orc.dequant_nvfp4(n1, orc.weight_2d_operand_scales(t1, "row"), sw, per_row=False)
+        m1, m1c, u1, sw2 = orc.nvfp4_quantize_weight_2d(y)
+        assert np.array_equal(m1, n1) and np.array_equal(m1c, n1c) and np.array_equal(u1, t1) and sw2 == sw
+        total += w.size * WS_BYTES_PER_ELEM
+    return total
+
+
+def timed_oracle(orc, fn, arg, threads, unit, sample):
+    orc.set_threads(threads)
+    t0 = time.perf_counter()
+    units = fn(orc, arg)
+    dt = time.perf_counter() - t0
+    return {"value": round(units / dt / unit_scale(unit), 6), "unit": unit, "cores": threads, "kind": "oracle",
+            "seconds": round(dt, 2), "sample": sample}
+
+
+def config_inputs():
+    """Host inputs of the tiny, MoE and WGRAD configs (the weight-sync sweep draws on the device)."""
+    import synthetic
+    return {"tiny": synthetic.tiny(), "moe": synthetic.moe(), "wgrad": synthetic.wgrad()}
+
+
+def cpu_baseline_configs(data):
+    """The oracle, as it stands, on a bounded sample of each further config, at all cores; the tiny check
+    and a one-matrix slice of a weight-sync layer also on one thread."""
+    import oracle as orc
+    orc.build()
+    cores = os.cpu_count() or 1
+    out = {}
+    out["tiny"] = timed_oracle(orc, oracle_tiny, data["tiny"], cores, "TFLOP/s", "the whole tiny check")
+    out["tiny"]["one_thread"] = timed_oracle(orc, oracle_tiny, data["tiny"], 1, "TFLOP/s", "the whole tiny check")
+    out["moe"] = timed_oracle(orc, oracle_moe, data["moe"], cores, "TFLOP/s",
+                              "expert 0: its routed rows' per-token NVFP4 (activations and down input), its gate|up "
+                              "and down 2D NVFP4 + DQ, FP64 references of its two grouped GEMMs")
+    out["wgrad"] = timed_oracle(orc, oracle_wgrad, data["wgrad"], cores, "TFLOP/s",
+                                f"1/{WGRAD_SLICE} of the columns of X and dY over all tokens: RHT16 + column-wise NVFP4 "
+                                "(RNE X, SR dY, both passes) and the FP64 WGRAD reference of that block")
+    mats = weight_sync_sample()
+    out["weight_sync"] = timed_oracle(orc, oracle_weight_sync, mats, cores, "GB/s",
+                                      "expert 0 of down, gate and up of one layer: MXFP8 + NVFP4-2D Q, DQ, re-Q, compare")
+    out["weight_sync"]["one_thread"] = timed_oracle(orc, oracle_weight_sync, mats[:1], 1, "GB/s",
+                                                    "expert 0 of the down matrix of one layer")
+    orc.set_threads(cores)
+    return out
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -1054,6 +1395,7 @@ def main():
     ap.add_argument("--experts", type=int, default=128, help="moe / weight_sync: experts (fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="dense_mlp only, without the other four configurations")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

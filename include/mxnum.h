@@ -172,7 +172,9 @@ mx_status mx_nvfp4_quantize_weight_2d_46(const void* w, int64_t G, int64_t O, in
  * library, which every GPU that loads the library keeps until the process exits.
  *   - G > MX_NOALLOC_MAX_MATRICES is rejected with MX_ERR_UNSUPPORTED (nothing is enqueued).
  *   - The first call on each device looks up the scratch address on the host (once per device);
- *     make that first call before any stream capture.
+ *     make that first call before any stream capture.  The address is cached for the life of the
+ *     process: after cudaDeviceReset (or anything else that destroys the device's primary context)
+ *     the cached address is stale, so do not call this entry point on that device again.
  *   - The call itself allocates nothing.  It clears the scratch it uses on `stream` before use.
  *   - All calls share the one array: calls that may overlap on the GPU (different streams, or
  *     different host threads, without ordering between them) race and must be serialized by the
@@ -394,10 +396,31 @@ mx_status mx_dequantize_nvfp4_amax(const uint8_t* q, const uint8_t* s, const flo
 typedef enum { MX_WS_WEIGHT_2D = 0, MX_WS_1X16 = 1 } mx_workspace_op;
 size_t mx_workspace_bytes(mx_workspace_op op, int64_t groups, int64_t unused);
 
-/* Synchronizes the device, then reports and clears the device-side watchdog word that bounded
- * waits inside the GEMM kernels set when they give up (MX_ERR_TIMEOUT), or MX_ERR_CUDA if the
- * device reports an error.  Host-side; for tests and health checks. */
+/* Failure detection.  Every mbarrier wait inside the kernels is bounded (2 s): a wait that gives up
+ * sets a device-side watchdog word (one per kernel family: the GEMMs, the MXFP8 quantizer), stops
+ * its CTA from issuing more work, lets the copies already issued land, and the CTA exits; its
+ * outputs are then undefined.  The calls below report and clear those words.
+ * Source: the E2E page, Tables 11-13 (the checks a low-precision RL run keeps and the faults each
+ * catches); the pages describe the failures, not this mechanism.
+ *
+ * mx_check_device_status: synchronizes the device, then returns MX_ERR_TIMEOUT if any watchdog word
+ * is set (and clears them all), MX_ERR_CUDA if the device reports an error, else MX_OK. */
 mx_status mx_check_device_status(void);
+
+/* As mx_check_device_status, waiting for `stream` only: the words are read and cleared by copies
+ * ordered on `stream`, then the stream is synchronized.  The words are shared by every stream of
+ * the device, so a timeout recorded by work on another stream is reported (and cleared) here too. */
+mx_status mx_check_stream_status(cudaStream_t stream);
+
+/* Watchdog self-test (test hook).  Launches, on `stream`, one small kernel of the chosen family
+ * whose waits are on barriers nothing ever arrives on, each bounded by `limit_ns` instead of the
+ * kernels' 2 s: MX_WATCHDOG_GEMM runs a cluster of two CTAs set up as the pair GEMMs are (TMEM
+ * allocated for the pair) and leaves through their exit path; MX_WATCHDOG_MXFP8 runs one CTA of
+ * waits on the MXFP8 quantizer's word.  No copy or MMA is issued, so the expiry is the only fault.
+ * Afterwards mx_check_device_status / mx_check_stream_status return MX_ERR_TIMEOUT once, then MX_OK.
+ *   limit_ns in [1000, 1000000000], else MX_ERR_INVALID_ARG. */
+typedef enum { MX_WATCHDOG_GEMM = 0, MX_WATCHDOG_MXFP8 = 1 } mx_watchdog_unit;
+mx_status mx_watchdog_selftest(mx_watchdog_unit unit, uint64_t limit_ns, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -17,6 +17,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmxnum.so")
 
+MX_OK, MX_ERR_INVALID_ARG, MX_ERR_ALIGNMENT, MX_ERR_UNSUPPORTED, MX_ERR_CUDA, MX_ERR_TIMEOUT = range(6)
 MX_FMT_MXFP8, MX_FMT_NVFP4 = 0, 1
 MX_ROUND_RNE, MX_ROUND_SR = 0, 1
 MX_SCOPE_NONE, MX_SCOPE_TENSOR, MX_SCOPE_ROW, MX_SCOPE_GROUP = 0, 1, 2, 3
@@ -71,6 +72,8 @@ def lib() -> ctypes.CDLL:
                 "mx_wgrad_bf16_dq_nvfp4": (I32, [P, P, P, P, I32, I64, I64, I64, P, I64, P]),
                 "mx_fp8_blockwise_gemm": (I32, [P, P, P, P, I64, I64, I64, P, I64, P]),
                 "mx_check_device_status": (I32, []),
+                "mx_check_stream_status": (I32, [P]),
+                "mx_watchdog_selftest": (I32, [I32, U64, P]),
             }
             for name, (res, args) in sigs.items():
                 f = getattr(L, name)
@@ -152,6 +155,24 @@ def workspace_bytes(op: int, groups: int = 0) -> int:
 
 def check_device_status() -> None:
     _check("mx_check_device_status", lib().mx_check_device_status())
+
+
+def mx_check_device_status() -> int:
+    """The raw status (MX_OK, MX_ERR_TIMEOUT, MX_ERR_CUDA): synchronizes the device, clears the watchdog words."""
+    return int(lib().mx_check_device_status())
+
+
+def mx_check_stream_status(stream=None) -> int:
+    """The raw status after waiting for `stream` (default: the current stream) only."""
+    return int(lib().mx_check_stream_status(_stream(stream)))
+
+
+MX_WATCHDOG_GEMM, MX_WATCHDOG_MXFP8 = 0, 1
+
+
+def mx_watchdog_selftest(unit: int, limit_ns: int, stream=None) -> None:
+    """Test hook: one kernel whose bounded waits expire after limit_ns (see include/mxnum.h)."""
+    _check("mx_watchdog_selftest", lib().mx_watchdog_selftest(int(unit), int(limit_ns), _stream(stream)))
 
 
 # ------------------------------------------------------------------------------------------------

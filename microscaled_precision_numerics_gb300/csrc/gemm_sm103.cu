@@ -1362,6 +1362,54 @@ fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
 }
 
 // ---------------------------------------------------------------------------------------------
+// Watchdog self-test: one cluster of two CTAs set up as the pair GEMMs are (mbarriers initialised
+// for the cluster, the pair's TMEM allocation, a CTA-local abort flag), in which every role waits on
+// a barrier that nothing ever arrives on, with the caller's limit instead of the kernels' 2 s.  The
+// first wait to give up sets the timeout bit of this file's status word and the CTA's abort flag;
+// the other roles see the flag and leave; then the CTAs take the GEMMs' exit path (CTA barrier,
+// cluster barrier, TMEM release).  No copy and no MMA is ever issued, so nothing is in flight at exit.
+// ---------------------------------------------------------------------------------------------
+constexpr uint32_t WATCHDOG_TMEM_COLS = 32;
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+watchdog_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bars[3];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_s;
+    volatile int* abort_flag = &abort_s;
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&bars[i]), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(&tmem_slot)), "r"(WATCHDOG_TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    // phase 0 of each barrier never completes: every wait below ends by its limit or by the abort flag
+    if (warp == 0) {
+        warp_wait(smem_u32(&bars[0]), 0, abort_flag, &g_mx_device_status, limit_ns);        // producer role
+    } else if (warp == 1) {
+        warp_wait(smem_u32(&bars[1]), 0, abort_flag, &g_mx_device_status, limit_ns);        // MMA role
+    } else {
+        mbar_wait_backoff(smem_u32(&bars[2]), 0, abort_flag, &g_mx_device_status, limit_ns);  // epilogue role
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(WATCHDOG_TMEM_COLS) : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------------
 bool make_map(CUtensorMap* map, const uint8_t* base, int64_t k_bytes, int64_t rows, uint32_t box_rows) {
@@ -1604,6 +1652,21 @@ uint32_t read_and_clear_device_status() {
     if (cudaMemcpyFromSymbol(&v, g_mx_device_status, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
     cudaMemcpyToSymbol(g_mx_device_status, &zero, sizeof(zero));
     return v;
+}
+
+uint32_t read_and_clear_device_status_on(cudaStream_t stream) {
+    unsigned int v = 0;
+    static const unsigned int zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_mx_device_status, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_mx_device_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return 0xFFFFFFFFu;
+    return v;
+}
+
+cudaError_t launch_watchdog_selftest(unsigned long long limit_ns, cudaStream_t stream) {
+    watchdog_selftest_kernel<<<2, NUM_THREADS, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
 }
 
 }  // namespace mxk

@@ -35,8 +35,10 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     return t;
 }
 
-// Bounded wait: false when the wait expired or another role of this CTA aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned int* status) {
+// Bounded wait: false when the wait expired or another role of this CTA aborted.  The kernels use the
+// default limit; the watchdog self-test passes a short one.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned int* status,
+                                          unsigned long long limit_ns = WAIT_LIMIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     uint32_t it = 0;
@@ -44,7 +46,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         if (mbar_try_wait(bar, parity)) return true;
         if ((++it & 255u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+            if (globaltimer() - t0 > limit_ns) {
                 atomicOr(status, 1u);
                 *abort_flag = 1;
                 return false;
@@ -56,14 +58,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // The same bounded wait for roles whose wait is long and not latency-critical (an epilogue waiting for
 // a whole tile): between polls the warp sleeps, leaving issue slots to the warps doing work.
 __device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                  unsigned int* status) {
+                                                  unsigned int* status, unsigned long long limit_ns = WAIT_LIMIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (true) {
         __nanosleep(256);
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+        if (globaltimer() - t0 > limit_ns) {
             atomicOr(status, 1u);
             *abort_flag = 1;
             return false;
@@ -72,8 +74,9 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
 }
 
 // All lanes of the warp wait; the result is made warp-uniform (any lane's failure fails all).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned int* status) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status)) != 0;
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned int* status,
+                                          unsigned long long limit_ns = WAIT_LIMIT_NS) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status, limit_ns)) != 0;
 }
 // One lane of a converged warp (always the lowest active lane, so the same lane every time).
 __device__ __forceinline__ bool elect_one() {

@@ -129,6 +129,10 @@ cudaError_t launch_dequant_nvfp4_amax(const uint8_t* q, const uint8_t* s, const 
                                       int64_t K, uint16_t* y, uint32_t* amax, cudaStream_t stream);
 uint32_t read_and_clear_device_status();
 uint32_t read_and_clear_mxfp8_status();
+uint32_t read_and_clear_device_status_on(cudaStream_t stream);
+uint32_t read_and_clear_mxfp8_status_on(cudaStream_t stream);
+cudaError_t launch_watchdog_selftest(unsigned long long limit_ns, cudaStream_t stream);
+cudaError_t launch_mxfp8_watchdog_selftest(unsigned long long limit_ns, cudaStream_t stream);
 
 int device_sm_count();
 

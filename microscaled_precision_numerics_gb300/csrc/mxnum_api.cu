@@ -406,8 +406,23 @@ mx_status mx_count_mismatch(const uint8_t* x, const uint8_t* y, int64_t nbytes, 
 
 mx_status mx_check_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return MX_ERR_CUDA;
-    const uint32_t w = mxk::read_and_clear_device_status() | mxk::read_and_clear_mxfp8_status();
-    return w ? MX_ERR_TIMEOUT : MX_OK;
+    const uint32_t a = mxk::read_and_clear_device_status(), b = mxk::read_and_clear_mxfp8_status();
+    if (a == 0xFFFFFFFFu || b == 0xFFFFFFFFu) return MX_ERR_CUDA;
+    return (a | b) ? MX_ERR_TIMEOUT : MX_OK;
+}
+
+mx_status mx_check_stream_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MX_ERR_CUDA;
+    const uint32_t a = mxk::read_and_clear_device_status_on(stream), b = mxk::read_and_clear_mxfp8_status_on(stream);
+    if (a == 0xFFFFFFFFu || b == 0xFFFFFFFFu) return MX_ERR_CUDA;
+    return (a | b) ? MX_ERR_TIMEOUT : MX_OK;
+}
+
+mx_status mx_watchdog_selftest(mx_watchdog_unit unit, uint64_t limit_ns, cudaStream_t stream) {
+    if (limit_ns < 1000u || limit_ns > 1000000000u) return MX_ERR_INVALID_ARG;
+    if (unit == MX_WATCHDOG_GEMM) return from_cuda(mxk::launch_watchdog_selftest(limit_ns, stream));
+    if (unit == MX_WATCHDOG_MXFP8) return from_cuda(mxk::launch_mxfp8_watchdog_selftest(limit_ns, stream));
+    return MX_ERR_INVALID_ARG;
 }
 
 }  // extern "C"

@@ -395,4 +395,39 @@ uint32_t read_and_clear_mxfp8_status() {
     return v;
 }
 
+uint32_t read_and_clear_mxfp8_status_on(cudaStream_t stream) {
+    unsigned int v = 0;
+    static const unsigned int zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_mx8_status, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_mx8_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return 0xFFFFFFFFu;
+    return v;
+}
+
+namespace {
+// Watchdog self-test of this file's status word: one CTA whose warps wait on a barrier that nothing
+// arrives on (the quantizer's ring waits, with the caller's limit); the first to give up sets the
+// timeout bit and the abort flag, the others leave on the flag.  No copy is ever issued.
+__global__ void __launch_bounds__(288) mx8_watchdog_selftest_kernel(unsigned long long limit_ns) {
+    using namespace async;
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_s;
+    volatile int* abort_flag = &abort_s;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    warp_wait(smem_u32(&bar), 0, abort_flag, &g_mx8_status, limit_ns);
+    __syncthreads();
+}
+}  // namespace
+
+cudaError_t launch_mxfp8_watchdog_selftest(unsigned long long limit_ns, cudaStream_t stream) {
+    mx8_watchdog_selftest_kernel<<<1, 288, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 }  // namespace mxk

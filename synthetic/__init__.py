@@ -30,6 +30,8 @@ because the bytes moved depend only on shapes and value distributions):
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -40,11 +42,49 @@ def to_bf16_bits(a: np.ndarray) -> np.ndarray:
     return t.view(torch.int16).numpy().view(np.uint16)
 
 
+# Tensors of at least this many elements are drawn in fixed chunks of independent streams (seeded from
+# one draw of the caller's generator), filled by a thread pool: the values depend on the seed only, not
+# on the number of threads.  Smaller tensors come straight from the caller's generator.
+_BIG = 1 << 22
+_CHUNK = 1 << 22
+
+
+def _chunked_f32(rng: np.random.Generator, shape, fill) -> np.ndarray:
+    """A float32 array of `shape` whose chunk i is fill(Generator_i, out_chunk_i)."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float32)
+    seeds = np.random.SeedSequence(int(rng.integers(0, 2 ** 63))).spawn((n + _CHUNK - 1) // _CHUNK)
+
+    def work(i):
+        fill(np.random.default_rng(seeds[i]), out[i * _CHUNK:(i + 1) * _CHUNK])
+
+    import concurrent.futures as cf
+    with cf.ThreadPoolExecutor(max_workers=min(len(seeds), os.cpu_count() or 1)) as ex:
+        list(ex.map(work, range(len(seeds))))
+    return out.reshape(shape)
+
+
 def normal(rng: np.random.Generator, shape, std: float) -> np.ndarray:
+    if int(np.prod(shape)) >= _BIG:
+        def fill(g, o):
+            g.standard_normal(out=o, dtype=np.float32)
+            o *= np.float32(std)
+        return to_bf16_bits(_chunked_f32(rng, shape, fill))
     return to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(std))
 
 
 def student_t(rng: np.random.Generator, shape, nu: float = 3.0, scale: float = 1.0) -> np.ndarray:
+    if int(np.prod(shape)) >= _BIG and nu == 3.0:
+        # Student-t with 3 degrees of freedom as z / sqrt(chi2_3 / 3), chi2_3 a sum of three squared
+        # standard normals (the textbook construction; the same distribution as Generator.standard_t(3))
+        def fill(g, o):
+            z = g.standard_normal(o.shape[0], dtype=np.float32)
+            c = np.zeros(o.shape[0], dtype=np.float32)
+            for _ in range(3):
+                u = g.standard_normal(o.shape[0], dtype=np.float32)
+                c += u * u
+            o[:] = z / np.sqrt(c / np.float32(3.0)) * np.float32(scale)
+        return to_bf16_bits(_chunked_f32(rng, shape, fill))
     return to_bf16_bits((rng.standard_t(nu, size=shape) * scale).astype(np.float32))
 
 
@@ -91,14 +131,16 @@ def route_uniform_topk(rng: np.random.Generator, tokens: int, experts: int, topk
     a seeded Fisher-Yates permutation of 0..experts-1.  Rows are then sorted
     stably by (expert, token).  Returns (row_token [tokens*topk] int64,
     group_offsets [experts+1] int64)."""
-    choice = np.empty((tokens, topk), dtype=np.int64)
-    for t in range(tokens):
-        perm = np.arange(experts, dtype=np.int64)
-        u = rng.random(experts - 1)
-        for i in range(experts - 1, 0, -1):       # Fisher-Yates, back to front
-            j = int(u[experts - 1 - i] * (i + 1))
-            perm[i], perm[j] = perm[j], perm[i]
-        choice[t] = perm[:topk]
+    # one Fisher-Yates shuffle per token, back to front, all tokens at once (token t's uniforms are row t)
+    u = rng.random((tokens, experts - 1))
+    perm = np.tile(np.arange(experts, dtype=np.int64), (tokens, 1))
+    rows = np.arange(tokens)
+    for i in range(experts - 1, 0, -1):
+        j = (u[:, experts - 1 - i] * (i + 1)).astype(np.int64)
+        pi = perm[:, i].copy()
+        perm[:, i] = perm[rows, j]
+        perm[rows, j] = pi
+    choice = perm[:, :topk]
     expert_of_row = choice.reshape(-1)
     token_of_row = np.repeat(np.arange(tokens, dtype=np.int64), topk)
     order = np.lexsort((token_of_row, expert_of_row))   # primary: expert, then token

@@ -265,3 +265,11 @@ def test_binding_alloc_helpers_satisfy_its_size_checks():
     o = mx.alloc_nvfp4_rows_grouped(300, 3, 64, cpu)
     with pytest.raises(ValueError, match=only_cuda):
         mx.mx_nvfp4_quantize_per_token_grouped(x, offs, o["q"], o["s"], o["s2"])
+
+
+def test_watchdog_selftest_validation(lib):
+    f = lib.mx_watchdog_selftest
+    assert f(0, 999, NUL) == 1                 # limit below 1 us
+    assert f(0, 1_000_000_001, NUL) == 1       # limit above 1 s
+    assert f(2, 1_000_000, NUL) == 1           # unknown unit
+    assert f(-1, 1_000_000, NUL) == 1
