@@ -391,6 +391,7 @@ class MoE8(MoE):
     expert-sorted rows (grouped scale layout) and of the 128 experts' stacked gate|up and down weights,
     the two grouped MXFP8 GEMMs, row-wise MXFP8 of the down-projection input."""
     name = "moe_mxfp8"
+    unit = "TFLOP/s"
     dtype = "e4m3 (f32 accumulate, bf16 out)"
 
     def __init__(self, mx, torch, dev, experts=128):
@@ -519,8 +520,10 @@ class DenseBlockwise:
     scales (the learner's form on Blackwell): [1, 128] row + column tiles of X and dY from one read each,
     [128, 128] blocks of W in both orientations, E8M0 scale bytes written straight into the MXFP8 GEMM
     layout, then FPROP, DGRAD and WGRAD on the MXFP8 tensor-core GEMM.  Aux: the FP32-scale quantizers
-    (the sampler's form) of X and W and the FP32-scale FPROP (per-K-block scaling around the tensor cores)."""
+    (the sampler's form) of X, dY and W and the FP32-scale FPROP and WGRAD (per-K-block scaling around the
+    tensor cores)."""
     name = "dense_fp8_blockwise"
+    unit = "TFLOP/s"
     dtype = "e4m3 (f32 accumulate, bf16 out)"
 
     def __init__(self, mx, torch, dev, tokens=8192, hidden=4096, ffn=12288):
@@ -540,7 +543,8 @@ class DenseBlockwise:
         self.qx, self.qdy = act(T, H), act(T, F)
         self.qw = {"q_row": u8(1, F, H), "q_col": u8(1, H, F), "s": f32(1, F // 128, H // 128),
                    "sf_row": u8(mx.scale_bytes(F, H, 32)), "sf_col": u8(mx.scale_bytes(H, F, 32))}
-        self.fx = {"q_row": u8(T, H), "s_row": f32(T, H // 128)}
+        self.fx = {"q_row": u8(T, H), "s_row": f32(T, H // 128), "q_col": u8(H, T), "s_col": f32(H, T // 128)}
+        self.fdy = {"q_col": u8(F, T), "s_col": f32(F, T // 128)}
         self.fw = {"q_row": u8(1, F, H), "q_col": u8(1, H, F), "s": f32(1, F // 128, H // 128)}
         self.y = torch.empty((T, F), dtype=torch.bfloat16, device=dev)
         self.dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -573,17 +577,25 @@ class DenseBlockwise:
         ]
 
     def aux_ops(self):
-        """FP32-scale blockwise quantizers (the sampler's form): X row-wise, W both orientations."""
+        """FP32-scale blockwise quantizers (the sampler's form): X row- and column-wise, dY column-wise, W both
+        orientations; the FP32-scale FPROP and WGRAD GEMMs on them."""
         mx, T, H, F = self.mx, self.T, self.H, self.F
         return [
-            ("quant", "blockwise 1x128 row FP32-scale X", 1, T * H * (2 + 1 + 4 / 128),
-             lambda: mx.mx_fp8_blockwise_quantize_1x128(self.x, False, q_row=self.fx["q_row"], s_row=self.fx["s_row"])),
+            ("quant", "blockwise 1x128 row+col FP32-scale X", 1, T * H * (2 + 2 + 2 * 4 / 128),
+             lambda: mx.mx_fp8_blockwise_quantize_1x128(self.x, False, q_row=self.fx["q_row"], s_row=self.fx["s_row"],
+                                                        q_col=self.fx["q_col"], s_col=self.fx["s_col"])),
+            ("quant", "blockwise 1x128 col FP32-scale dY", 1, T * F * (2 + 1 + 4 / 128),
+             lambda: mx.mx_fp8_blockwise_quantize_1x128(self.dy, False, q_col=self.fdy["q_col"], s_col=self.fdy["s_col"])),
             ("quant", "blockwise 128x128 FP32-scale W", 1, F * H * 4,
              lambda: mx.mx_fp8_blockwise_quantize_128x128(self.w[None], False, self.fw["q_row"], self.fw["q_col"],
                                                           self.fw["s"])),
             ("gemm8", "FPROP FP32-scale blockwise (scaling around the tensor cores)", 0, 2.0 * T * F * H,
              lambda: mx.mx_fp8_blockwise_gemm(self.fx["q_row"], self.fx["s_row"], self.fw["q_row"][0], self.fw["s"][0],
                                               T, F, H, self.y)),
+            ("gemm8", "WGRAD FP32-scale blockwise (per-row scales of both operands around the tensor cores)", 0,
+             2.0 * F * H * T,
+             lambda: mx.mx_fp8_blockwise_gemm_wgrad(self.fdy["q_col"], self.fdy["s_col"], self.fx["q_col"],
+                                                    self.fx["s_col"], F, H, T, self.dw)),
         ]
 
     def config(self):
@@ -600,6 +612,7 @@ class DenseNVFP4:
     weight copy) and WGRAD (BF16 dY^T times DQ(X) of the forward's X codes) and, for comparison, the
     materialized DQ(W) the DGRAD avoids."""
     name = "dense_nvfp4"
+    unit = "TFLOP/s"
 
     def __init__(self, mx, torch, dev):
         import synthetic

@@ -339,6 +339,20 @@ mx_status mx_wgrad_bf16_dq_nvfp4(const void* dy, const uint8_t* qx, const uint8_
 mx_status mx_fp8_blockwise_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb, int64_t M,
                                 int64_t N, int64_t K, void* d, int64_t ldd, cudaStream_t stream);
 
+/* Blockwise FP8 weight-gradient GEMM with FP32 scales: both operands are contracted over tokens, so both
+ * are the column-wise [1, 128] copies of mx_fp8_blockwise_quantize_1x128 (tiles along K = tokens), each
+ * row with its own FP32 scale per 128-token block:
+ *   D[m, n] = BF16( sum_kb sa[m, kb] * sb[n, kb] * sum_{k in kb} A[m, k] * B[n, k] ),   kb = k / 128
+ * e.g. dW [O, H] = dY^T X with A = dY's q_col [O, T], sa = its s_col [O, T/128], B = X's q_col [H, T],
+ * sb = its s_col [H, T/128].
+ * Source: NeMo RL FP8 page, "FP8 nas camadas lineares" -- input activations and output gradients in
+ * [1, 128] tiles with an FP32 scale each (the DeepSeek-V3 recipe), which the weight gradient consumes along
+ * tokens; E2E page Table 1 -- FP32 scales are applied around the tensor cores on SM100.
+ *   a [M, K] E4M3, sa [M, K/128] FP32;  b [N, K] E4M3, sb [N, K/128] FP32;  d [M, ldd] BF16
+ * Requirements as mx_fp8_blockwise_gemm. */
+mx_status mx_fp8_blockwise_gemm_wgrad(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb, int64_t M,
+                                      int64_t N, int64_t K, void* d, int64_t ldd, cudaStream_t stream);
+
 /* Grouped block-scaled GEMM over expert-sorted rows: for every group g,
  *   D[rows of g] = BF16( alpha_a[row] * alpha_b[g] * A[rows of g] . B_g^T ).
  * Source: Miles page -- NVFP4 on the routed experts' weights and activations with a per-token

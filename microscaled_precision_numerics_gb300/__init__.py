@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
                 "mx_gemm_bf16_dq_nvfp4": (I32, [P, P, I32, P, P, P, I32, I64, I64, I64, P, I64, P]),
                 "mx_wgrad_bf16_dq_nvfp4": (I32, [P, P, P, P, I32, I64, I64, I64, P, I64, P]),
                 "mx_fp8_blockwise_gemm": (I32, [P, P, P, P, I64, I64, I64, P, I64, P]),
+                "mx_fp8_blockwise_gemm_wgrad": (I32, [P, P, P, P, I64, I64, I64, P, I64, P]),
                 "mx_check_device_status": (I32, []),
                 "mx_check_stream_status": (I32, [P]),
                 "mx_watchdog_selftest": (I32, [I32, U64, P]),
@@ -468,6 +469,19 @@ def mx_fp8_blockwise_gemm(a, sa, b, sb, M: int, N: int, K: int, d, stream=None):
     _need(fn, "sb", sb, 4 * ((N + 127) // 128) * (K // 128))
     _need_out2d(fn, "d", d, M, N)
     _check("mx_fp8_blockwise_gemm", lib().mx_fp8_blockwise_gemm(
+        _p(a), _p(sa), _p(b), _p(sb), M, N, K, _p(d), d.stride(0), _stream(stream)))
+
+
+def mx_fp8_blockwise_gemm_wgrad(a, sa, b, sb, M: int, N: int, K: int, d, stream=None):
+    """D = BF16(sum over 128-deep K blocks of sa[m, kb] * sb[n, kb] * A_kb B_kb^T): both operands column-wise
+    [1, 128]-tile copies (K = tokens) with FP32 scales sa [M, K/128], sb [N, K/128]."""
+    fn = "mx_fp8_blockwise_gemm_wgrad"
+    _need(fn, "a", a, M * K)
+    _need(fn, "sa", sa, 4 * M * (K // 128))
+    _need(fn, "b", b, N * K)
+    _need(fn, "sb", sb, 4 * N * (K // 128))
+    _need_out2d(fn, "d", d, M, N)
+    _check(fn, lib().mx_fp8_blockwise_gemm_wgrad(
         _p(a), _p(sa), _p(b), _p(sb), M, N, K, _p(d), d.stride(0), _stream(stream)))
 
 

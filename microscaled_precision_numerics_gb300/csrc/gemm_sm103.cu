@@ -1121,21 +1121,57 @@ dq_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // Table 1: on SM100 the tensor cores take power-of-two block scales natively, FP32 ones are applied
 // around them):
 //   D[m, n] = BF16( sum_kb sa[m, kb] * sb[n / 128, kb] * P_kb[m, n] ),   P_kb = sum_{k in kb} A[m, k] B[n, k]
+// and, for the weight gradient (both operands contracted over tokens, so both in [1, 128] tiles along K,
+// BROW = true), the same with one B scale per B row:  sb[n, kb] in place of sb[n / 128, kb].
 // Each 128-deep K block's P_kb comes from plain E4M3 pair MMAs (kind::f8f6f4, FP32 accumulation) into
-// one of two TMEM buffers (2 x 256 columns); the 8 epilogue warps promote it into FP32 register
-// accumulators with the block's scale product while the tensor core fills the other buffer, and write
-// the tile once all K blocks are in.  Warp 0 loads A and B by TMA (as the block-scaled kernel, without
-// scale atoms); warp 1 of the even CTA issues the MMAs; warp 1 of the odd CTA forwards its epilogue's
-// "buffer read" to the even CTA as a 16-byte bulk copy.
+// one of four TMEM buffers (4 x 128 columns); the 8 epilogue warps promote it into FP32 register
+// accumulators with the block's scale product (packed two-lane FP32 multiply-adds) while the tensor
+// core fills the other buffers, and write the tile once all K blocks are in.  With per-row B scales each
+// epilogue warp stages the scales of its 64 columns for four K blocks at a time in a slot of its own in
+// shared memory (transposed, so every lane reads them as broadcasts), loading the next four ahead.
+// Warp 0 loads A and B by TMA (as the block-scaled kernel, without scale atoms); warp 1 of the even CTA
+// issues the MMAs; warp 1 of the odd CTA forwards its epilogue's "buffer read" to the even CTA as a
+// 16-byte bulk copy.
 // ---------------------------------------------------------------------------------------------
 struct BwParams {
-    const float* sa; const float* sb;       // sa [M, K/128]; sb [ceil(N/128), K/128]
+    const float* sa; const float* sb;       // sa [M, K/128]; sb [ceil(N/128), K/128], or [N, K/128] (per-row B)
     int64_t M, N, K, kb_n, nb_n;
     uint16_t* d; int64_t ldd;
     int64_t m_tiles, n_tiles, total_tiles;
 };
 
-template <int TN>
+// Packed two-lane FP32 arithmetic (IEEE round-to-nearest per lane, as the scalar forms).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t r[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+template <int TN, bool BROW>
 struct BwCfg {
     static constexpr int NP = TMEM_COLS / TN;              // partial-product buffers in TMEM
     static constexpr int NST = TN == 256 ? 6 : 8;
@@ -1148,8 +1184,11 @@ struct BwCfg {
     static constexpr int SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
     static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 3 * NP + 1);
     static constexpr int SMEM_SIGNAL = (SMEM_MISC + 16 + 15) / 16 * 16;
-    static constexpr int SMEM_ALLOC = SMEM_SIGNAL + 16 + 1024;
-    static_assert(SMEM_B % 1024 == 0 && SMEM_EPI % 1024 == 0, "alignment");
+    // per-row B scales: one slot per epilogue warp of 4 K blocks x TN/2 columns (FP32)
+    static constexpr int SB_SLOT_FLOATS = 4 * (TN / 2);
+    static constexpr int SMEM_SB = SMEM_SIGNAL + 16;
+    static constexpr int SMEM_ALLOC = SMEM_SB + (BROW ? EPI_WARPS * SB_SLOT_FLOATS * 4 : 0) + 1024;
+    static_assert(SMEM_B % 1024 == 0 && SMEM_EPI % 1024 == 0 && SMEM_SB % 16 == 0, "alignment");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -1165,11 +1204,11 @@ __device__ __forceinline__ void tc2_mma_e4m3(uint32_t d, uint64_t adesc, uint64_
                  :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
 }
 
-template <int TN>
+template <int TN, bool BROW>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmD, const BwParams p) {
-    using C = BwCfg<TN>;
+    using C = BwCfg<TN, BROW>;
     constexpr int NST = C::NST;
     constexpr int NP = C::NP;
     extern __shared__ uint8_t smem_raw[];
@@ -1306,42 +1345,112 @@ fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         const int h = (warp - 2) >> 2;
         const uint32_t ebase = sbase + C::SMEM_EPI + (uint32_t)((warp - 2) * 2 * EPI_BUF_BYTES);
         const uint32_t my_pempty = leader ? bar_pempty : bar_pempty_odd;
+        // per-row B scales: this warp's slot, [4 K blocks][TN/2 columns]
+        float* sb_slot = reinterpret_cast<float*>(smem + C::SMEM_SB) + (warp - 2) * C::SB_SLOT_FLOATS;
         uint32_t epi_chunk = 0;
         int64_t g = 0;
         bool ok = true;
         for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
             const PairTile tile = pair_dense_tile<TN>(tp, t, rank);
             const int64_t row = tile.row0 + q * 32 + lane;
-            const int64_t nblk = (tile.n0 + h * (TN / 2)) / 128;
+            const int64_t col0 = tile.n0 + h * (TN / 2);            // first output column of this warp
+            const int64_t nblk = col0 / 128;
             const float* sa_row = p.sa + (row < p.M ? row : 0) * p.kb_n;
-            const float* sb_blk = p.sb + (nblk < p.nb_n ? nblk : 0) * p.kb_n;
-            const bool valid = row < p.M && nblk < p.nb_n;
-            float acc[TN / 2];
+            const bool row_ok = row < p.M;
+            const bool valid = row_ok && (BROW || nblk < p.nb_n);
+            const float* sb_blk = p.sb + (!BROW && nblk < p.nb_n ? nblk : 0) * p.kb_n;
+            // per-row B: lane l stages the scales of columns col0 + l + 32 c (c < TN/64); zero past N
+            constexpr int SBC = TN / 64;
+            const int32_t kb_n32 = (int32_t)p.kb_n;
+            const float* sb_lane = p.sb + (BROW ? (col0 + lane) * p.kb_n : 0);
+            uint32_t sb_okm = 0;                                        // bit c: column c of this lane exists
 #pragma unroll
-            for (int i = 0; i < TN / 2; ++i) acc[i] = 0.0f;
+            for (int c = 0; c < SBC; ++c) sb_okm |= (BROW && col0 + lane + 32 * c < p.N) ? (1u << c) : 0u;
+            float sb_next[SBC * 4];
+#pragma unroll
+            for (int c = 0; c < SBC; ++c)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    sb_next[c * 4 + j] = ((sb_okm >> c) & 1u) && j < kb_n32 ? __ldg(sb_lane + (int64_t)32 * c * kb_n32 + j) : 0.0f;
+            uint64_t acc[TN / 4];
+#pragma unroll
+            for (int i = 0; i < TN / 4; ++i) acc[i] = 0ull;
             for (int64_t kb = 0; kb < p.kb_n; ++kb, ++g) {
                 const uint32_t pb = (uint32_t)(g % NP), use = (uint32_t)(g / NP);
-                const float scale = valid ? __fmul_rn(__ldg(sa_row + kb), __ldg(sb_blk + kb)) : 0.0f;
+                if (BROW && (kb & 3) == 0) {
+                    // publish this group of four K blocks' column scales; fetch the next group's
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < SBC; ++c)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) sb_slot[j * (TN / 2) + 32 * c + lane] = sb_next[c * 4 + j];
+                    __syncwarp();
+                    const int32_t k4 = (int32_t)kb + 4;
+#pragma unroll
+                    for (int c = 0; c < SBC; ++c)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            sb_next[c * 4 + j] = ((sb_okm >> c) & 1u) && k4 + j < kb_n32
+                                                     ? __ldg(sb_lane + (int64_t)32 * c * kb_n32 + k4 + j) : 0.0f;
+                }
+                const float sa_k = row_ok ? __ldg(sa_row + kb) : 0.0f;
+                const float scale = BROW ? sa_k : (valid ? __fmul_rn(sa_k, __ldg(sb_blk + kb)) : 0.0f);
+                const uint64_t scale2 = f2_pack(scale, scale);
                 if (!mbar_wait(bar_pfull + 8 * pb, use & 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
                 tc_fence_after();
+                const uint32_t tbuf = tmem + pb * TN + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * (TN / 2));
+                if (BROW) {
+                    // 32 columns at a time: the partial product and the column scales of a chunk in registers
+                    const float4* srow = reinterpret_cast<const float4*>(sb_slot + (kb & 3) * (TN / 2));
 #pragma unroll
-                for (int c = 0; c < TN / 2 / 32; ++c) {
-                    float v[32];
-                    tmem_ld32(tmem + pb * TN + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * (TN / 2) + c * 32), v);
+                    for (int c = 0; c < TN / 2 / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32_nowait(tbuf + c * 32, v);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                        if (c == TN / 2 / 32 - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) {
+                                if (leader && warp == 2) mbar_arrive_expect_tx(my_pempty + 8 * pb, 16);
+                                else mbar_arrive(my_pempty + 8 * pb);
+                            }
+                        }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[c * 32 + i] = __fmaf_rn(v[i], scale, acc[c * 32 + i]);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if (leader && warp == 2) mbar_arrive_expect_tx(my_pempty + 8 * pb, 16);
-                    else mbar_arrive(my_pempty + 8 * pb);
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 sb4 = srow[c * 8 + i];           // columns 4i..4i+3 of the chunk (broadcast)
+                            const uint64_t p0 = f2_mul(f2_pack(sb4.x, sb4.y), scale2);
+                            const uint64_t p1 = f2_mul(f2_pack(sb4.z, sb4.w), scale2);
+                            uint64_t& a0 = acc[c * 16 + 2 * i];
+                            uint64_t& a1 = acc[c * 16 + 2 * i + 1];
+                            a0 = f2_fma(f2_pack(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])), p0, a0);
+                            a1 = f2_fma(f2_pack(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])), p1, a1);
+                        }
+                    }
+                } else {
+                    uint32_t v[TN / 2];
+#pragma unroll
+                    for (int c = 0; c < TN / 2 / 32; ++c) tmem_ld32_nowait(tbuf + c * 32, v + 32 * c);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        // the partial product is in registers: hand the buffer back before promoting it
+                        if (leader && warp == 2) mbar_arrive_expect_tx(my_pempty + 8 * pb, 16);
+                        else mbar_arrive(my_pempty + 8 * pb);
+                    }
+#pragma unroll
+                    for (int i = 0; i < TN / 4; ++i)
+                        acc[i] = f2_fma(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), scale2, acc[i]);
                 }
             }
             if (!ok) break;
             uint32_t packed[TN / 4];
 #pragma unroll
-            for (int i = 0; i < TN / 4; ++i) packed[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+            for (int i = 0; i < TN / 4; ++i) {
+                float lo, hi;
+                f2_unpack(acc[i], lo, hi);
+                packed[i] = pack_bf16x2(lo, hi);
+            }
             epilogue_store<TN, false>(tp, &tmD, q, h, lane, tile.row0, tile.row_end, tile.n0, ebase, epi_chunk, packed);
         }
         if (lane == 0) bulk_wait_group_all();
@@ -1552,13 +1661,13 @@ cudaError_t launch_dq_impl(const DqGemmArgs& a, int num_sms, cudaStream_t stream
 }
 
 
-template <int TN>
+template <int TN, bool BROW>
 cudaError_t launch_bw_impl(const BwGemmArgs& a, int num_sms, cudaStream_t stream) {
-    using C = BwCfg<TN>;
+    using C = BwCfg<TN, BROW>;
     static PerDevice setup;                 // attributes, and the CTA pairs that fit on the GPU at once
     int resident_pairs = 0;
     const cudaError_t attr_err = per_device_once(setup, resident_pairs, [num_sms](int& rp) -> cudaError_t {
-        const cudaError_t e = cudaFuncSetAttribute(fp8bw_gemm_pair_kernel<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        const cudaError_t e = cudaFuncSetAttribute(fp8bw_gemm_pair_kernel<TN, BROW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(num_sms & ~1));
@@ -1569,7 +1678,7 @@ cudaError_t launch_bw_impl(const BwGemmArgs& a, int num_sms, cudaStream_t stream
         attr[0].val.clusterDim.x = 2; attr[0].val.clusterDim.y = 1; attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr; cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, fp8bw_gemm_pair_kernel<TN>, &cfg) != cudaSuccess || n <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&n, fp8bw_gemm_pair_kernel<TN, BROW>, &cfg) != cudaSuccess || n <= 0) {
             cudaGetLastError();
             n = num_sms / 2;
         }
@@ -1589,7 +1698,7 @@ cudaError_t launch_bw_impl(const BwGemmArgs& a, int num_sms, cudaStream_t stream
     p.n_tiles = (a.N + TN - 1) / TN;
     p.total_tiles = p.m_tiles * p.n_tiles;
     const int64_t pairs = max64(1, min64(p.total_tiles, (int64_t)min(resident_pairs, num_sms / 2)));
-    fp8bw_gemm_pair_kernel<TN><<<(unsigned)(2 * pairs), NUM_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmB, tmD, p);
+    fp8bw_gemm_pair_kernel<TN, BROW><<<(unsigned)(2 * pairs), NUM_THREADS, C::SMEM_ALLOC, stream>>>(tmA, tmB, tmD, p);
     return cudaGetLastError();
 }
 
@@ -1644,7 +1753,8 @@ cudaError_t launch_dq_gemm(const DqGemmArgs& args, int num_sms, cudaStream_t str
 }
 
 cudaError_t launch_fp8_blockwise_gemm(const BwGemmArgs& args, int num_sms, cudaStream_t stream) {
-    return launch_bw_impl<128>(args, num_sms, stream);
+    return args.b_row_scales ? launch_bw_impl<128, true>(args, num_sms, stream)
+                             : launch_bw_impl<128, false>(args, num_sms, stream);
 }
 
 uint32_t read_and_clear_device_status() {

@@ -120,6 +120,7 @@ struct BwGemmArgs {
     const uint8_t* a; const float* sa; const uint8_t* b; const float* sb;
     int64_t M, N, K;
     uint16_t* d; int64_t ldd;
+    bool b_row_scales;        // sb [N, K/128] (one scale per B row) instead of [ceil(N/128), K/128]
 };
 cudaError_t launch_fp8_blockwise_gemm(const BwGemmArgs& args, int num_sms, cudaStream_t stream);
 cudaError_t launch_nvfp4_weight_2d_given_amax(const uint16_t* w, int64_t G, int64_t O, int64_t H, uint8_t* q_row,

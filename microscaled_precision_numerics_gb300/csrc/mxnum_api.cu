@@ -375,6 +375,21 @@ mx_status mx_fp8_blockwise_gemm(const uint8_t* a, const float* sa, const uint8_t
     mxk::BwGemmArgs g{};
     g.a = a; g.sa = sa; g.b = b; g.sb = sb; g.M = M; g.N = N; g.K = K;
     g.d = static_cast<uint16_t*>(d); g.ldd = ldd;
+    g.b_row_scales = false;
+    return from_cuda(mxk::launch_fp8_blockwise_gemm(g, mxk::device_sm_count(), stream));
+}
+
+mx_status mx_fp8_blockwise_gemm_wgrad(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb, int64_t M,
+                                      int64_t N, int64_t K, void* d, int64_t ldd, cudaStream_t stream) {
+    if (!a || !sa || !b || !sb || !d || M <= 0 || N <= 0 || K <= 0 || ldd < N) return MX_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(d) || (reinterpret_cast<uintptr_t>(sa) & 3) ||
+        (reinterpret_cast<uintptr_t>(sb) & 3) || (N % 8) != 0 || (ldd % 8) != 0)
+        return MX_ERR_ALIGNMENT;
+    if ((K % 128) != 0 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
+    mxk::BwGemmArgs g{};
+    g.a = a; g.sa = sa; g.b = b; g.sb = sb; g.M = M; g.N = N; g.K = K;
+    g.d = static_cast<uint16_t*>(d); g.ldd = ldd;
+    g.b_row_scales = true;
     return from_cuda(mxk::launch_fp8_blockwise_gemm(g, mxk::device_sm_count(), stream));
 }
 

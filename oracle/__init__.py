@@ -524,6 +524,14 @@ def gemm_ref_fp8_blockwise(qa, sa, qb, sb) -> np.ndarray:
     return fp8_blockwise_decode_f64(qa, sa, 1, 128) @ fp8_blockwise_decode_f64(qb, sb, 128, 128).T
 
 
+def gemm_ref_fp8_blockwise_wgrad(qa, sa, qb, sb) -> np.ndarray:
+    """The blockwise FP8 weight-gradient GEMM (NeMo RL FP8 page, "FP8 nas camadas lineares": activations and
+    output gradients in [1, 128] tiles with FP32 scales; the weight gradient contracts both over tokens, so
+    both operands are [1, 128]-tiled along K): ref = DQ(A) @ DQ(B)^T in FP64, DQ the exact decoded values,
+    sa [M, K/128] and sb [N, K/128]."""
+    return fp8_blockwise_decode_f64(qa, sa, 1, 128) @ fp8_blockwise_decode_f64(qb, sb, 1, 128).T
+
+
 def rel_fro_error(d: np.ndarray, ref: np.ndarray) -> float:
     """||D - ref||_F / ||ref||_F."""
     d = np.asarray(d, dtype=np.float64)

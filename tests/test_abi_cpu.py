@@ -273,3 +273,12 @@ def test_watchdog_selftest_validation(lib):
     assert f(0, 1_000_000_001, NUL) == 1       # limit above 1 s
     assert f(2, 1_000_000, NUL) == 1           # unknown unit
     assert f(-1, 1_000_000, NUL) == 1
+
+
+def test_fp8_blockwise_wgrad_validation(lib):
+    f = lib.mx_fp8_blockwise_gemm_wgrad
+    assert f(NUL, A16, A16, A16, 128, 128, 128, A16, 128, NUL) == 1     # null A
+    assert f(A16, A16, A16, A16, 128, 128, 128, A16, 64, NUL) == 1      # ldd < N
+    assert f(A8, A16, A16, A16, 128, 128, 128, A16, 128, NUL) == 2      # misaligned A
+    assert f(A16, A16, A16, A16, 128, 132, 128, A16, 136, NUL) == 2     # N % 8
+    assert f(A16, A16, A16, A16, 128, 128, 192, A16, 128, NUL) == 3     # K % 128

@@ -238,3 +238,70 @@ def test_fp32_scale_gemm_dgrad_with_gpu_quantizers(mx, orc):
     _, wc, ws, _ = orc.fp8_blockwise_128x128(w, False)
     ref = orc.gemm_ref_fp8_blockwise(rq, rs, wc, np.ascontiguousarray(ws.T))
     assert orc.rel_fro_error(d.float().cpu().numpy().astype(np.float64), ref) <= TOL
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (384, 640, 1024), (200, 296, 384), (1, 8, 128),
+                                   (1024, 1280, 4096), (512, 384, 640)])
+def test_fp32_scale_gemm_wgrad(mx, orc, M, N, K):
+    """WGRAD dW = dY^T X with both operands the column-wise [1, 128] copies (tiles along tokens = K) and one
+    FP32 scale per row and 128-token block; operands from the oracle quantizer (column-wise = row-wise of the
+    transpose)."""
+    dyT = synthetic.random_bf16(M + N + 7 * K, (M, K), "normal", 1e-3)
+    xT = synthetic.random_bf16(M + 3 * N + K, (N, K), "student_t")
+    qa, sa, _ = orc.fp8_blockwise_1x128(dyT, False)
+    qb, sb, _ = orc.fp8_blockwise_1x128(xT, False)
+    d = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mx.mx_fp8_blockwise_gemm_wgrad(torch.from_numpy(qa).to(DEV), torch.from_numpy(sa).to(DEV),
+                                   torch.from_numpy(qb).to(DEV), torch.from_numpy(sb).to(DEV), M, N, K, d)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    ref = orc.gemm_ref_fp8_blockwise_wgrad(qa, sa, qb, sb)
+    got = d.float().cpu().numpy().astype(np.float64)
+    assert orc.rel_fro_error(got, ref) <= TOL
+    A = orc.fp8_blockwise_decode_f64(qa, sa, 1, 128)
+    B = orc.fp8_blockwise_decode_f64(qb, sb, 1, 128)
+    bound = 2.0 ** -7 * np.abs(ref) + 2.0 ** -15 * (np.abs(A) @ np.abs(B).T) + 1e-30
+    assert not (np.abs(got - ref) > bound).any()
+
+
+def test_fp32_scale_gemm_wgrad_integer_exact(mx, orc):
+    """Small-integer codes with power-of-two FP32 scales: every partial sum and every promoted product is
+    exact in FP32, so the GEMM must equal the reference bit for bit after BF16 rounding."""
+    rng = np.random.default_rng(21)
+    M, N, K = 256, 384, 512
+    ints = np.array([0x00, 0x30, 0x38, 0x3C, 0x40, 0x44, 0xB8, 0xC0], dtype=np.uint8)   # 0, +-0.5..3
+    qa = ints[rng.integers(0, ints.size, size=(M, K))]
+    qb = ints[rng.integers(0, ints.size, size=(N, K))]
+    sa = (2.0 ** rng.integers(-2, 3, size=(M, K // 128))).astype(np.float32)
+    sb = (2.0 ** rng.integers(-2, 3, size=(N, K // 128))).astype(np.float32)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    mx.mx_fp8_blockwise_gemm_wgrad(torch.from_numpy(qa).to(DEV), torch.from_numpy(sa).to(DEV),
+                                   torch.from_numpy(qb).to(DEV), torch.from_numpy(sb).to(DEV), M, N, K, d)
+    torch.cuda.synchronize()
+    ref = orc.gemm_ref_fp8_blockwise_wgrad(qa, sa, qb, sb)
+    want = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    got = d.view(torch.int16).cpu().numpy()
+    assert np.array_equal(got, want), first_mismatch(got, want)
+
+
+def test_fp32_scale_gemm_wgrad_with_gpu_quantizers(mx, orc):
+    """The weight gradient of a linear layer from the GPU quantizers' column-wise outputs: dY [T, O] and X [T, H]
+    quantized in [1, 128] tiles along tokens, dW [O, H] = dY^T X, against the oracle's quantization of the same
+    tensors (codes and scales compared bit-exact first)."""
+    T, O, H = 1024, 768, 512
+    dy = synthetic.random_bf16(61, (T, O), "normal", 1e-3)
+    x = synthetic.random_bf16(62, (T, H), "student_t")
+    qdy, sdy = u8((O, T)), f32((O, T // 128))
+    qx, sx = u8((H, T)), f32((H, T // 128))
+    mx.mx_fp8_blockwise_quantize_1x128(bf16_dev(dy), False, q_col=qdy, s_col=sdy)
+    mx.mx_fp8_blockwise_quantize_1x128(bf16_dev(x), False, q_col=qx, s_col=sx)
+    d = torch.full((O, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mx.mx_fp8_blockwise_gemm_wgrad(qdy, sdy, qx, sx, O, H, T, d)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    rq_dy, rs_dy, _ = orc.fp8_blockwise_1x128(np.ascontiguousarray(dy.T), False)
+    rq_x, rs_x, _ = orc.fp8_blockwise_1x128(np.ascontiguousarray(x.T), False)
+    assert np.array_equal(to_np(qdy), rq_dy) and np.array_equal(to_np(sdy), rs_dy)
+    assert np.array_equal(to_np(qx), rq_x) and np.array_equal(to_np(sx), rs_x)
+    ref = orc.gemm_ref_fp8_blockwise_wgrad(rq_dy, rs_dy, rq_x, rs_x)
+    assert orc.rel_fro_error(d.float().cpu().numpy().astype(np.float64), ref) <= TOL

@@ -224,3 +224,25 @@ def test_blockwise_gemm_reference(orc):
     mx_a = orc.fp8_blockwise_e8m0_rowwise(e_a.astype(np.uint8))
     mx_b = np.repeat(np.repeat(e_b.astype(np.uint8), 128, 0)[:N], 4, 1)
     assert np.array_equal(p2, orc.gemm_ref_mxfp8(qa, mx_a, qb, mx_b))
+
+
+def test_blockwise_wgrad_reference(orc):
+    """The weight-gradient form (per-row FP32 scales on both operands): a triple loop over hand-decoded
+    values; the forward form on the same codes whenever B's row scales are equal within each 128-row block;
+    and the transpose relation ref(A, B) = ref(B, A)^T (both operands are tiled the same way)."""
+    rng = np.random.default_rng(4)
+    M, N, K = 6, 131, 384
+    qa = rng.integers(0, 0x7F, size=(M, K), dtype=np.uint8) | (rng.integers(0, 2, size=(M, K), dtype=np.uint8) << 7)
+    qb = rng.integers(0, 0x7F, size=(N, K), dtype=np.uint8) | (rng.integers(0, 2, size=(N, K), dtype=np.uint8) << 7)
+    sa = rng.random((M, K // 128)).astype(np.float32) + np.float32(0.25)
+    sb = rng.random((N, K // 128)).astype(np.float32) + np.float32(0.25)
+    ref = orc.gemm_ref_fp8_blockwise_wgrad(qa, sa, qb, sb)
+    val = lambda c: (-1.0 if c & 0x80 else 1.0) * E4M3[c & 0x7F]
+    for (m, n) in [(0, 0), (5, 130), (3, 64), (1, 127)]:
+        want = sum(val(qa[m, k]) * float(sa[m, k // 128]) * val(qb[n, k]) * float(sb[n, k // 128]) for k in range(K))
+        assert ref[m, n] == pytest.approx(want, rel=1e-12, abs=1e-300)
+    blocks = rng.random(((N + 127) // 128, K // 128)).astype(np.float32)
+    sb_rows = np.repeat(blocks, 128, 0)[:N]
+    assert np.array_equal(orc.gemm_ref_fp8_blockwise_wgrad(qa, sa, qb, sb_rows),
+                          orc.gemm_ref_fp8_blockwise(qa, sa, qb, blocks))
+    assert np.allclose(orc.gemm_ref_fp8_blockwise_wgrad(qb, sb, qa, sa), ref.T, rtol=1e-13, atol=0)
