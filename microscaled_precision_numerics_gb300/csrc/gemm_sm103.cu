@@ -1160,15 +1160,22 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
     return d;
 }
 
-__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t r[32]) {
+// Issue a load of 16 TMEM columns of this warp's 32 lanes; the registers are valid only after
+// tmem_wait_ld on them.
+__device__ __forceinline__ void tmem_ld_issue(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr) : "memory");
+}
+// Wait for this thread's TMEM loads.  The registers pass through the statement, so no use of them
+// can be scheduled above the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+        : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+          "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+        :: "memory");
 }
 
 template <int TN, bool BROW>
@@ -1185,7 +1192,7 @@ struct BwCfg {
     static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 3 * NP + 1);
     static constexpr int SMEM_SIGNAL = (SMEM_MISC + 16 + 15) / 16 * 16;
     // per-row B scales: one slot per epilogue warp of 4 K blocks x TN/2 columns (FP32)
-    static constexpr int SB_SLOT_FLOATS = 4 * (TN / 2);
+    static constexpr int SB_SLOT_FLOATS = 2 * 4 * (TN / 2);   // two groups of four K blocks
     static constexpr int SMEM_SB = SMEM_SIGNAL + 16;
     static constexpr int SMEM_ALLOC = SMEM_SB + (BROW ? EPI_WARPS * SB_SLOT_FLOATS * 4 : 0) + 1024;
     static_assert(SMEM_B % 1024 == 0 && SMEM_EPI % 1024 == 0 && SMEM_SB % 16 == 0, "alignment");
@@ -1202,6 +1209,36 @@ __device__ __forceinline__ void tc2_mma_e4m3(uint32_t d, uint64_t adesc, uint64_
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
                  :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
+}
+
+// 4-byte asynchronous global -> shared copy; src_bytes = 0 stores a zero instead (the source is not read).
+__device__ __forceinline__ void cp_async_f32(uint32_t dst, const float* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Promotion of one CW-column chunk of a K block's partial product into the FP32 accumulators:
+//   acc[c] += P[c] * scale                 (forward forms: one factor per row and K block)
+//   acc[c] += P[c] * (scale * sb[c])       (per-row B: the column's scale from the warp's slot at srow)
+// as packed two-lane FP32 operations (IEEE round-to-nearest per lane).
+template <bool BROW, int CW>
+__device__ __forceinline__ void promote_chunk(uint64_t* acc, const uint32_t (&v)[CW], uint64_t scale2, uint32_t srow) {
+#pragma unroll
+    for (int i = 0; i < CW / 4; ++i) {
+        const uint64_t p0 = f2_pack(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]));
+        const uint64_t p1 = f2_pack(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+        if (BROW) {
+            uint64_t s01, s23;                                  // column scales 4i..4i+3 (broadcast)
+            asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(s01), "=l"(s23) : "r"(srow + (uint32_t)(16 * i)));
+            acc[2 * i] = f2_fma(p0, f2_mul(s01, scale2), acc[2 * i]);
+            acc[2 * i + 1] = f2_fma(p1, f2_mul(s23, scale2), acc[2 * i + 1]);
+        } else {
+            acc[2 * i] = f2_fma(p0, scale2, acc[2 * i]);
+            acc[2 * i + 1] = f2_fma(p1, scale2, acc[2 * i + 1]);
+        }
+    }
 }
 
 template <int TN, bool BROW>
@@ -1347,67 +1384,106 @@ fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         const uint32_t my_pempty = leader ? bar_pempty : bar_pempty_odd;
         // per-row B scales: this warp's slot, [4 K blocks][TN/2 columns]
         float* sb_slot = reinterpret_cast<float*>(smem + C::SMEM_SB) + (warp - 2) * C::SB_SLOT_FLOATS;
+        const uint32_t sb_slot_s = smem_u32(sb_slot);
         uint32_t epi_chunk = 0;
         int64_t g = 0;
         bool ok = true;
+        const int32_t kb_n32 = (int32_t)p.kb_n;
         for (int64_t t = pair_id; t < total_tiles && ok; t += n_pairs) {
             const PairTile tile = pair_dense_tile<TN>(tp, t, rank);
             const int64_t row = tile.row0 + q * 32 + lane;
             const int64_t col0 = tile.n0 + h * (TN / 2);            // first output column of this warp
             const int64_t nblk = col0 / 128;
-            const float* sa_row = p.sa + (row < p.M ? row : 0) * p.kb_n;
             const bool row_ok = row < p.M;
-            const bool valid = row_ok && (BROW || nblk < p.nb_n);
-            const float* sb_blk = p.sb + (!BROW && nblk < p.nb_n ? nblk : 0) * p.kb_n;
-            // per-row B: lane l stages the scales of columns col0 + l + 32 c (c < TN/64); zero past N
+            const bool blk_ok = BROW || nblk < p.nb_n;
+            const float* sa_row = p.sa + (row_ok ? row : 0) * p.kb_n;
+            const float* sb_blk = p.sb + (!BROW && blk_ok ? nblk : 0) * p.kb_n;
+            // the scales of four K blocks at a time, loaded a group ahead: this thread's row scales sa and,
+            // for the forward forms, the tile's block scales.  Per-row B: lane l copies the scales of its
+            // columns col0 + l + 32 c (zero past N or past K) straight into the warp's slot, transposed, two
+            // groups ahead by asynchronous copies (slot buffer = group parity).
             constexpr int SBC = TN / 64;
-            const int32_t kb_n32 = (int32_t)p.kb_n;
             const float* sb_lane = p.sb + (BROW ? (col0 + lane) * p.kb_n : 0);
             uint32_t sb_okm = 0;                                        // bit c: column c of this lane exists
 #pragma unroll
             for (int c = 0; c < SBC; ++c) sb_okm |= (BROW && col0 + lane + 32 * c < p.N) ? (1u << c) : 0u;
-            float sb_next[SBC * 4];
+            auto stage_group = [&](int32_t grp) {
+                const uint32_t dst = sb_slot_s + (uint32_t)((grp & 1) * 4 * (TN / 2) * 4);
 #pragma unroll
-            for (int c = 0; c < SBC; ++c)
+                for (int j = 0; j < 4; ++j) {
+                    const int32_t k = 4 * grp + j;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    sb_next[c * 4 + j] = ((sb_okm >> c) & 1u) && j < kb_n32 ? __ldg(sb_lane + (int64_t)32 * c * kb_n32 + j) : 0.0f;
+                    for (int c = 0; c < SBC; ++c) {
+                        const bool in = ((sb_okm >> c) & 1u) && k < kb_n32;
+                        cp_async_f32(dst + (uint32_t)((j * (TN / 2) + 32 * c + lane) * 4),
+                                     in ? sb_lane + (int64_t)32 * c * kb_n32 + k : p.sb, in ? 4u : 0u);
+                    }
+                }
+                cp_async_commit();
+            };
+            if (BROW) {
+                cp_async_wait0();                      // the previous tile's copies have landed
+                __syncwarp();
+                stage_group(0);
+                stage_group(1);
+            }
+            float sa_next[4], sk_next[4];
+            float sc_cur[4];                                    // this group's promotion factor per K block
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                sa_next[j] = row_ok && j < kb_n32 ? __ldg(sa_row + j) : 0.0f;
+                sk_next[j] = !BROW && blk_ok && j < kb_n32 ? __ldg(sb_blk + j) : 0.0f;
+            }
+            uint32_t packed[TN / 4];                       // the tile's BF16 results, this warp's slice
+            if constexpr (BROW) {
+            // Per-row B: software pipeline over 16-column chunks of each K block: one TMEM load is in flight
+            // while the previous chunk is promoted (two packed operations per column pair), the first chunk
+            // of kb + 1 behind the last of kb.
+            constexpr int CW = 16;
+            constexpr int NCH = (TN / 2) / CW;
+            static_assert(NCH % 2 == 0, "chunk parity alternates the two register sets");
             uint64_t acc[TN / 4];
 #pragma unroll
             for (int i = 0; i < TN / 4; ++i) acc[i] = 0ull;
-            for (int64_t kb = 0; kb < p.kb_n; ++kb, ++g) {
-                const uint32_t pb = (uint32_t)(g % NP), use = (uint32_t)(g / NP);
-                if (BROW && (kb & 3) == 0) {
-                    // publish this group of four K blocks' column scales; fetch the next group's
-                    __syncwarp();
-#pragma unroll
-                    for (int c = 0; c < SBC; ++c)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) sb_slot[j * (TN / 2) + 32 * c + lane] = sb_next[c * 4 + j];
-                    __syncwarp();
-                    const int32_t k4 = (int32_t)kb + 4;
-#pragma unroll
-                    for (int c = 0; c < SBC; ++c)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            sb_next[c * 4 + j] = ((sb_okm >> c) & 1u) && k4 + j < kb_n32
-                                                     ? __ldg(sb_lane + (int64_t)32 * c * kb_n32 + k4 + j) : 0.0f;
-                }
-                const float sa_k = row_ok ? __ldg(sa_row + kb) : 0.0f;
-                const float scale = BROW ? sa_k : (valid ? __fmul_rn(sa_k, __ldg(sb_blk + kb)) : 0.0f);
-                const uint64_t scale2 = f2_pack(scale, scale);
-                if (!mbar_wait(bar_pfull + 8 * pb, use & 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
+            const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * (TN / 2));
+            uint32_t va[CW], vb[CW];
+            if (kb_n32 > 0) {
+                const uint32_t pb0 = (uint32_t)(g % NP), use0 = (uint32_t)(g / NP);
+                if (!mbar_wait(bar_pfull + 8 * pb0, use0 & 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t tbuf = tmem + pb * TN + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * (TN / 2));
-                if (BROW) {
-                    // 32 columns at a time: the partial product and the column scales of a chunk in registers
-                    const float4* srow = reinterpret_cast<const float4*>(sb_slot + (kb & 3) * (TN / 2));
+                tmem_ld_issue(lane_base + pb0 * TN, va);
+                tmem_wait_ld(va);
+            }
+            for (int32_t kb = 0; kb < kb_n32 && ok; ++kb, ++g) {
+                const uint32_t pb = (uint32_t)(g % NP);
+                const int32_t j4 = kb & 3;
+                if (j4 == 0) {
+                    // this group's scales become current; per-row B waits for its column scales' copies
 #pragma unroll
-                    for (int c = 0; c < TN / 2 / 32; ++c) {
-                        uint32_t v[32];
-                        tmem_ld32_nowait(tbuf + c * 32, v);
-                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                        if (c == TN / 2 / 32 - 1) {
+                    for (int j = 0; j < 4; ++j) sc_cur[j] = sa_next[j];
+                    cp_async_wait1();                      // all but the newest group: this one has landed
+                    __syncwarp();
+                    const int32_t k4 = kb + 4;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const bool in = k4 + j < kb_n32;
+                        sa_next[j] = row_ok && in ? __ldg(sa_row + k4 + j) : 0.0f;
+                    }
+                }
+                const float scale = j4 == 0 ? sc_cur[0] : j4 == 1 ? sc_cur[1] : j4 == 2 ? sc_cur[2] : sc_cur[3];
+                const uint64_t scale2 = f2_pack(scale, scale);
+                const uint32_t srow = sb_slot_s + (uint32_t)((((kb >> 2) & 1) * 4 + j4) * (TN / 2) * 4);
+                const bool more = kb + 1 < kb_n32;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    uint32_t (&cur)[CW] = (c & 1) ? vb : va;
+                    uint32_t (&nxt)[CW] = (c & 1) ? va : vb;
+                    if (c + 1 < NCH) {
+                        tmem_ld_issue(lane_base + pb * TN + (uint32_t)((c + 1) * CW), nxt);
+                        promote_chunk<true, CW>(acc + c * (CW / 2), cur, scale2, srow + (uint32_t)(c * CW * 4));
+                        tmem_wait_ld(nxt);
+                        if (c + 2 == NCH) {
+                            // the whole K block is in registers: hand the buffer back
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) {
@@ -1415,44 +1491,74 @@ fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                                 else mbar_arrive(my_pempty + 8 * pb);
                             }
                         }
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 sb4 = srow[c * 8 + i];           // columns 4i..4i+3 of the chunk (broadcast)
-                            const uint64_t p0 = f2_mul(f2_pack(sb4.x, sb4.y), scale2);
-                            const uint64_t p1 = f2_mul(f2_pack(sb4.z, sb4.w), scale2);
-                            uint64_t& a0 = acc[c * 16 + 2 * i];
-                            uint64_t& a1 = acc[c * 16 + 2 * i + 1];
-                            a0 = f2_fma(f2_pack(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])), p0, a0);
-                            a1 = f2_fma(f2_pack(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])), p1, a1);
+                    } else {
+                        if (more) {
+                            const uint32_t pn = (uint32_t)((g + 1) % NP), usen = (uint32_t)((g + 1) / NP);
+                            if (!mbar_wait(bar_pfull + 8 * pn, usen & 1u, abort_flag, &g_mx_device_status)) ok = false;
+                            tc_fence_after();
+                            if (ok) tmem_ld_issue(lane_base + pn * TN, nxt);          // chunk 0 of kb + 1
                         }
+                        promote_chunk<true, CW>(acc + c * (CW / 2), cur, scale2, srow + (uint32_t)(c * CW * 4));
+                        if (more && ok) tmem_wait_ld(nxt);
                     }
-                } else {
-                    uint32_t v[TN / 2];
-#pragma unroll
-                    for (int c = 0; c < TN / 2 / 32; ++c) tmem_ld32_nowait(tbuf + c * 32, v + 32 * c);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                    tc_fence_before();
+                }
+                if (j4 == 3) {
+                    // the group's slot buffer is read: refill it with the group after next
                     __syncwarp();
-                    if (lane == 0) {
-                        // the partial product is in registers: hand the buffer back before promoting it
-                        if (leader && warp == 2) mbar_arrive_expect_tx(my_pempty + 8 * pb, 16);
-                        else mbar_arrive(my_pempty + 8 * pb);
-                    }
-#pragma unroll
-                    for (int i = 0; i < TN / 4; ++i)
-                        acc[i] = f2_fma(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), scale2, acc[i]);
+                    stage_group((kb >> 2) + 2);
                 }
             }
-            if (!ok) break;
-            uint32_t packed[TN / 4];
 #pragma unroll
             for (int i = 0; i < TN / 4; ++i) {
                 float lo, hi;
                 f2_unpack(acc[i], lo, hi);
                 packed[i] = pack_bf16x2(lo, hi);
             }
+            } else {
+            // Forward forms: promotion one K block at a time, the partial product's 32-column chunks loaded
+            // from TMEM and accumulated with the block's factor (scalar FP32 multiply-adds: measured faster
+            // here than the packed form), then the buffer handed back.
+            float accf[TN / 2];
+#pragma unroll
+            for (int i = 0; i < TN / 2; ++i) accf[i] = 0.0f;
+            for (int32_t kb = 0; kb < kb_n32; ++kb, ++g) {
+                const uint32_t pb = (uint32_t)(g % NP), use = (uint32_t)(g / NP);
+                const int32_t j4 = kb & 3;
+                if (j4 == 0) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) sc_cur[j] = __fmul_rn(sa_next[j], sk_next[j]);
+                    const int32_t k4 = kb + 4;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const bool in = k4 + j < kb_n32;
+                        sa_next[j] = row_ok && in ? __ldg(sa_row + k4 + j) : 0.0f;
+                        sk_next[j] = blk_ok && in ? __ldg(sb_blk + k4 + j) : 0.0f;
+                    }
+                }
+                const float scale = j4 == 0 ? sc_cur[0] : j4 == 1 ? sc_cur[1] : j4 == 2 ? sc_cur[2] : sc_cur[3];
+                if (!mbar_wait(bar_pfull + 8 * pb, use & 1u, abort_flag, &g_mx_device_status)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < TN / 2 / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(tmem + pb * TN + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * (TN / 2) + c * 32), v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) accf[c * 32 + i] = __fmaf_rn(v[i], scale, accf[c * 32 + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader && warp == 2) mbar_arrive_expect_tx(my_pempty + 8 * pb, 16);
+                    else mbar_arrive(my_pempty + 8 * pb);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < TN / 4; ++i) packed[i] = pack_bf16x2(accf[2 * i], accf[2 * i + 1]);
+            }
+            if (!ok) break;
             epilogue_store<TN, false>(tp, &tmD, q, h, lane, tile.row0, tile.row_end, tile.n0, ebase, epi_chunk, packed);
         }
+        if (BROW) cp_async_wait0();                   // no copy into this warp's slot outlives the CTA
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
     }
