@@ -463,10 +463,10 @@ class WGrad:
     name = "wgrad"
     unit = "TFLOP/s"
 
-    def __init__(self, mx, torch, dev, data=None):
+    def __init__(self, mx, torch, dev, data=None, tokens=32768):
         import synthetic
         self.mx, self.torch, self.dev = mx, torch, dev
-        d = data or synthetic.wgrad()
+        d = data or synthetic.wgrad(tokens=tokens)
         bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
         self.x, self.dy = bf(d["x"]), bf(d["dy"])
         self.rht_seed, self.sr_seed = d["rht_seed"], d["sr_seed"]
@@ -614,10 +614,10 @@ class DenseNVFP4:
     name = "dense_nvfp4"
     unit = "TFLOP/s"
 
-    def __init__(self, mx, torch, dev):
+    def __init__(self, mx, torch, dev, tokens=32768):
         import synthetic
         self.mx, self.torch, self.dev = mx, torch, dev
-        d = synthetic.dense_nvfp4()
+        d = synthetic.dense_nvfp4(tokens=tokens)
         bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
         self.x, self.dy, self.w = bf(d["x"]), bf(d["dy"]), bf(d["w"])
         self.rht_seed, self.sr_seed = d["rht_seed"], d["sr_seed"]
@@ -1033,9 +1033,9 @@ def make_workload(name, mx, torch, dev, args, data=None):
     if name == "dense_fp8_blockwise":
         return DenseBlockwise(mx, torch, dev)
     if name == "dense_nvfp4":
-        return DenseNVFP4(mx, torch, dev)
+        return DenseNVFP4(mx, torch, dev, tokens=args.tokens)
     if name == "wgrad":
-        return WGrad(mx, torch, dev, data=data)
+        return WGrad(mx, torch, dev, data=data, tokens=args.tokens)
     if name == "weight_sync":
         return WeightSync(mx, torch, dev, layers=args.layers, experts=args.experts)
     raise ValueError(name)
@@ -1406,6 +1406,7 @@ def main():
     ap.add_argument("--workload", choices=["dense_mlp", "moe", "moe_mxfp8", "dense_fp8_blockwise", "dense_nvfp4", "wgrad", "weight_sync"], default="dense_mlp")
     ap.add_argument("--layers", type=int, default=48, help="weight_sync: layers swept")
     ap.add_argument("--experts", type=int, default=128, help="moe / weight_sync: experts (fewer only for profiling)")
+    ap.add_argument("--tokens", type=int, default=32768, help="wgrad / dense_nvfp4: tokens (fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="dense_mlp only, without the other four configurations")

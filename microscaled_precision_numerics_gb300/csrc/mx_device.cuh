@@ -68,14 +68,7 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float v[8]) {
     return r;
 }
 
-// Two packed E2M1 codes (one byte) -> two FP16 values (exact); element 0 from the low nibble.
-// Value of a 4-bit E2M1 code (s ee m, bias 1; e = 0 subnormal m * 0.5) from its field definition.
-__device__ __forceinline__ float e2m1_value(uint32_t c) {
-    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
-    const uint32_t mag = e ? (((e + 126u) << 23) | (m << 22)) : (m ? 0x3F000000u : 0u);
-    return __uint_as_float(mag | ((c & 8u) << 28));
-}
-
+// Two packed E2M1 codes (the low byte) -> two FP16 values (exact); element 0 from the low nibble.
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
     uint32_t r;
     asm("{\n\t.reg .b8 c;\n\tcvt.u8.u32 c, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, c;\n\t}" : "=r"(r) : "r"(byte & 0xFFu));

@@ -55,15 +55,23 @@ __device__ __forceinline__ uint2 quant_block16(const uint4& a, const uint4& b, f
     return make_uint2(cvt_e2m1x8(v), cvt_e2m1x8(v + 8));
 }
 
-// Largest |fp32(fp32(value(q_i) * value(bs)) * S) - x_i| over n values whose codes are packed 8 per
-// word (even index in the low nibble).
+// Largest |fp32(fp32(value(q_i) * value(bs)) * S) - x_i| over n values (n a multiple of 8) whose codes are
+// packed 8 per word (even index in the low nibble).  value(q) * value(bs) has at most 6 significant bits
+// and lies in [2^-10, 2688], so the product of the two FP16 decodes (two elements per instruction: the
+// hardware E2M1 and E4M3 conversions, and a packed FP16 multiply) is exact and equals the FP32 product.
 __device__ __forceinline__ float nvfp4_max_dq_error(const float* x, const uint32_t* codes, int n, uint32_t bs, float S) {
-    const float bsv = e4m3_to_f32(bs);
+    uint32_t bs2;                                       // value(bs) in both FP16 halves
+    asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(bs2) : "r"((bs & 0xFFu) * 0x101u));
     float err = 0.0f;
 #pragma unroll
-    for (int i = 0; i < n; ++i) {
-        const float deq = __fmul_rn(__fmul_rn(e2m1_value((codes[i >> 3] >> (4 * (i & 7))) & 0xFu), bsv), S);
-        err = fmaxf(err, fabsf(__fsub_rn(deq, x[i])));
+    for (int i = 0; i < n; i += 2) {
+        const uint32_t q2 = e2m1x2_to_f16x2(codes[i >> 3] >> (4 * (i & 7)));
+        uint32_t p2;
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(p2) : "r"(q2), "r"(bs2));
+        const float p0 = __half2float(__ushort_as_half((unsigned short)(p2 & 0xFFFFu)));
+        const float p1 = __half2float(__ushort_as_half((unsigned short)(p2 >> 16)));
+        err = fmaxf(err, fabsf(__fsub_rn(__fmul_rn(p0, S), x[i])));
+        err = fmaxf(err, fabsf(__fsub_rn(__fmul_rn(p1, S), x[i + 1])));
     }
     return err;
 }
@@ -534,8 +542,22 @@ matrix_amax_kernel(const uint16_t* __restrict__ w, int64_t per_matrix, uint32_t*
     const uint16_t* base = w + g * per_matrix;
     uint32_t m2 = 0;
     const int64_t nvec = per_matrix / 8;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(base) + i);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const uint4* vb = reinterpret_cast<const uint4*>(base);
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // four independent 16-byte loads in flight per thread
+    for (; i + 3 * stride < nvec; i += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ldg(vb + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            m2 = absmax_bf16x2(m2, v[u].x); m2 = absmax_bf16x2(m2, v[u].y);
+            m2 = absmax_bf16x2(m2, v[u].z); m2 = absmax_bf16x2(m2, v[u].w);
+        }
+    }
+    for (; i < nvec; i += stride) {
+        const uint4 v = __ldg(vb + i);
         m2 = absmax_bf16x2(m2, v.x); m2 = absmax_bf16x2(m2, v.y);
         m2 = absmax_bf16x2(m2, v.z); m2 = absmax_bf16x2(m2, v.w);
     }
