@@ -1842,8 +1842,10 @@ bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const voi
 cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream) {
     if (args.G > MAX_GROUPS) return cudaErrorInvalidValue;
     const bool col_alpha = args.G == 0 && args.alpha_b_scope == 2;   // per-output-column factor (dense only)
-    // dense: 256-column tiles, one accumulator; grouped (a few K stages per tile): 128-column tiles
-    // with two accumulators so that each tile's epilogue overlaps the next tile's MMAs
+    // 256-column tiles with one accumulator, dense and grouped alike: for the grouped MoE shapes (K = 2048
+    // and 768) they measured faster than 128-column tiles with two accumulators (whose epilogue overlaps
+    // the next tile's MMAs but which read A twice as often): gate_up 0.118 against 0.146 ms, down 0.110
+    // against 0.132 ms (NVFP4; MXFP8 likewise)
     if (args.fmt == 0) {
         if (args.G > 0) return launch_pair_impl<0, true, false, 256>(args, num_sms, stream);
         return col_alpha ? launch_pair_impl<0, false, true, 256>(args, num_sms, stream)
