@@ -5,7 +5,8 @@ a host framework that owns all device memory, or a loop that must not call cudaM
 synchronizes the device): its per-matrix scratch is a fixed array inside the library rather than a
 caller workspace.  Through the C ABI, two calls in a row -- the second with a smaller weight
 magnitude and fewer matrices, so stale scratch from the first call would change its scales -- must
-match mx_nvfp4_quantize_weight_2d byte for byte (the quantizer tolerance is bit-exactness).
+match mx_nvfp4_quantize_weight_2d byte for byte (the quantizer tolerance is bit-exactness), and the CPU
+oracle's codes, tile scales and matrix scales for every matrix.
 This file is collected last so that a run stopping at the first failure has run every other test.
 """
 import ctypes
@@ -24,7 +25,7 @@ def _outputs(mx, G, O, H):
     return mx.alloc_nvfp4_weight_2d(G, O, H, DEV)
 
 
-def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
+def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(orc):
     import microscaled_precision_numerics_gb300 as mx
     L = mx.lib()
     f = L.mx_nvfp4_quantize_weight_2d_noalloc
@@ -50,6 +51,18 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         for k in ("q_row", "s_row", "q_col", "s_col", "s_w"):
             a, b = got[k].cpu().numpy(), ref[k].cpu().numpy()
             assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), f"call {call}: {k} differs"
+        # and the oracle, matrix by matrix
+        w_np = w.view(torch.int16).cpu().numpy().view(np.uint16)
+        srb, scb = orc.scale_layout_bytes(O, H // 16), orc.scale_layout_bytes(H, O // 16)
+        for g in range(G):
+            qr, qc, st, sw = orc.nvfp4_quantize_weight_2d(np.ascontiguousarray(w_np[g]))
+            assert np.array_equal(got["q_row"][g].cpu().numpy(), qr), f"call {call}: q_row of matrix {g}"
+            assert np.array_equal(got["q_col"][g].cpu().numpy(), qc), f"call {call}: q_col of matrix {g}"
+            assert np.array_equal(got["s_row"][g * srb:(g + 1) * srb].cpu().numpy(),
+                                  orc.scales_to_gemm_layout(orc.weight_2d_operand_scales(st, "row")))
+            assert np.array_equal(got["s_col"][g * scb:(g + 1) * scb].cpu().numpy(),
+                                  orc.scales_to_gemm_layout(orc.weight_2d_operand_scales(st, "col")))
+            assert got["s_w"][g].item() == float(sw), f"call {call}: s_w of matrix {g}"
 
 
 def test_noalloc_rejects_more_matrices_than_its_scratch():
