@@ -102,6 +102,50 @@ def test_dense_mlp_gemms_sampled(orc, dense):
     check_block(orc, dense["dw"].float().cpu().numpy()[np.ix_(o, h)], A @ B.T, np.abs(A) @ np.abs(B).T)
 
 
+def test_dense_mlp_fp32_scale_blockwise_sampled(mx, orc, dense):
+    """The dense MLP shapes in blockwise FP8 with FP32 scales (NeMo RL FP8 page, the DeepSeek-V3 recipe), in the
+    launch configuration `bench.py --workload dense_fp8_blockwise` times: X row-wise [1, 128] and W [128, 128]
+    for FPROP; dY and X column-wise [1, 128] (tiles along tokens) for WGRAD.  Sampled codes and scales are
+    compared bit-exact with the oracle, sampled 64 x 64 output blocks within the GEMM tolerance of the FP64
+    product of the oracle's own quantization."""
+    d, T, H, F = dense["data"], dense["T"], dense["H"], dense["F"]
+    u8 = lambda *sh: torch.empty(sh, dtype=torch.uint8, device=DEV)
+    f32 = lambda *sh: torch.empty(sh, dtype=torch.float32, device=DEV)
+    x, w, dy = bf16_dev(d["x"]), bf16_dev(d["w"]), bf16_dev(d["dy"])
+    qx, sx, qxc, sxc = u8(T, H), f32(T, H // 128), u8(H, T), f32(H, T // 128)
+    mx.mx_fp8_blockwise_quantize_1x128(x, False, q_row=qx, s_row=sx, q_col=qxc, s_col=sxc)
+    qdyc, sdyc = u8(F, T), f32(F, T // 128)
+    mx.mx_fp8_blockwise_quantize_1x128(dy, False, q_col=qdyc, s_col=sdyc)
+    qw, qwc, sw = u8(1, F, H), u8(1, H, F), f32(1, F // 128, H // 128)
+    mx.mx_fp8_blockwise_quantize_128x128(w[None], False, qw, qwc, sw)
+    y = torch.empty((T, F), dtype=torch.bfloat16, device=DEV)
+    dw = torch.empty((F, H), dtype=torch.bfloat16, device=DEV)
+    mx.mx_fp8_blockwise_gemm(qx, sx, qw[0], sw[0], T, F, H, y)
+    mx.mx_fp8_blockwise_gemm_wgrad(qdyc, sdyc, qxc, sxc, F, H, T, dw)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    rng = np.random.default_rng(104)
+    dec = orc.fp8_blockwise_decode_f64
+    # FPROP: 64 rows of X and a 64-row slab of W inside one 128 x 128 block row
+    m = np.sort(rng.choice(T, 64, replace=False))
+    rq, rs, _ = orc.fp8_blockwise_1x128(np.ascontiguousarray(d["x"][m]), False)
+    assert np.array_equal(to_np(qx)[m], rq) and np.array_equal(to_np(sx)[m], rs)
+    fb = int(rng.integers(0, F // 128)) * 128
+    wq, _, ws, _ = orc.fp8_blockwise_128x128(np.ascontiguousarray(d["w"][fb:fb + 128]), False)
+    assert np.array_equal(to_np(qw[0, fb:fb + 128]), wq) and np.array_equal(to_np(sw[0, fb // 128]), ws[0])
+    A, B = dec(rq, rs, 1, 128), dec(wq[:64], ws, 128, 128)
+    check_block(orc, y.float().cpu().numpy()[m][:, fb:fb + 64], A @ B.T, np.abs(A) @ np.abs(B).T)
+    # WGRAD: 64 columns of dY and of X over all tokens, each column's tiles along the tokens
+    o0 = int(rng.integers(0, F // 64)) * 64
+    h0 = int(rng.integers(0, H // 64)) * 64
+    aq, as_, _ = orc.fp8_blockwise_1x128(np.ascontiguousarray(d["dy"][:, o0:o0 + 64].T), False)
+    bq, bs, _ = orc.fp8_blockwise_1x128(np.ascontiguousarray(d["x"][:, h0:h0 + 64].T), False)
+    assert np.array_equal(to_np(qdyc[o0:o0 + 64]), aq) and np.array_equal(to_np(sdyc[o0:o0 + 64]), as_)
+    assert np.array_equal(to_np(qxc[h0:h0 + 64]), bq) and np.array_equal(to_np(sxc[h0:h0 + 64]), bs)
+    A, B = dec(aq, as_, 1, 128), dec(bq, bs, 1, 128)
+    check_block(orc, dw.float().cpu().numpy()[o0:o0 + 64, h0:h0 + 64], A @ B.T, np.abs(A) @ np.abs(B).T)
+
+
 # ------------------------------------------------------------------------------------------------
 # moe: Qwen3-30B-A3B expert layer, NVFP4
 # ------------------------------------------------------------------------------------------------
