@@ -142,6 +142,7 @@ class Tiny:
     name = "tiny"
     unit = "TFLOP/s"
     dtype = "e4m3 (f32 accumulate, bf16 out)"
+    graph = True          # launch-bound: also timed as one CUDA graph per step
 
     def __init__(self, mx, torch, dev, data=None):
         import synthetic
@@ -964,6 +965,34 @@ def e2e_generic(work, torch, steps, ops=None, units_per_step=None, warmup=2):
     return out
 
 
+def graph_step(work, torch, ops, steps, warmup):
+    """Capture one step's calls into a CUDA graph and time `steps` replays with CUDA events; returns the
+    replay value and ms per step (the eager ones kept under eager_*)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for op in ops:
+            op[4]()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for op in ops:
+            op[4]()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    return {"graph_ms_per_step": round(ms, 4), "graph_value": round(step_value(work, ops, ms), 2),
+            "graph_note": "the step's calls captured once into a CUDA graph and replayed (the value and ms_per_step "
+                          "above are the eager calls through the Python binding)"}
+
+
 def measure(work, torch, mx, peaks, steps, warmup, e2e=True, gpu_index=0):
     """Device-timed steps of a workload (CUDA events per op), its roofline, clocks and end-to-end run."""
     ops = work.ops()
@@ -979,6 +1008,10 @@ def measure(work, torch, mx, peaks, steps, warmup, e2e=True, gpu_index=0):
            "config": work.config(), "per_op": rep, "roofline": dominant_roofline(ops, per_op, peaks),
            "clocks": clocks, "gpu_launches": work.launches_per_step * steps,
            "watchdog": "ok" if status == 0 else f"status {status}"}
+    if getattr(work, "graph", False):
+        # a launch-bound step: the same calls captured once into a CUDA graph and replayed, so the host's
+        # per-call work (argument checks, tensor-map encoding, launch) leaves the step time
+        out.update(graph_step(work, torch, ops, steps, warmup))
     if hasattr(work, "aux_ops"):
         aops = work.aux_ops()
         if aops:
@@ -1403,7 +1436,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mxnum", "reference"], default="mxnum")
-    ap.add_argument("--workload", choices=["dense_mlp", "moe", "moe_mxfp8", "dense_fp8_blockwise", "dense_nvfp4", "wgrad", "weight_sync"], default="dense_mlp")
+    ap.add_argument("--workload", choices=["dense_mlp", "tiny", "moe", "moe_mxfp8", "dense_fp8_blockwise", "dense_nvfp4", "wgrad",
+                                           "weight_sync"], default="dense_mlp")
     ap.add_argument("--layers", type=int, default=48, help="weight_sync: layers swept")
     ap.add_argument("--experts", type=int, default=128, help="moe / weight_sync: experts (fewer only for profiling)")
     ap.add_argument("--tokens", type=int, default=32768, help="wgrad / dense_nvfp4: tokens (fewer only for profiling)")
