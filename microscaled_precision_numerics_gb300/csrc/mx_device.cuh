@@ -135,28 +135,55 @@ __device__ __forceinline__ uint32_t rht_sign_mask(uint64_t seed) {
     return philox4x32_10(0u, 0u, 1u, 0u, (uint32_t)seed, (uint32_t)(seed >> 32)).x & 0xFFFFu;
 }
 
-// In-register 16-point Walsh-Hadamard butterflies with strides 1, 2, 4, 8 (no signs, no 1/4).
-__device__ __forceinline__ void fwht16_unscaled(float v[16]) {
+// Packed two-lane FP32 arithmetic (IEEE round-to-nearest per lane, as the scalar forms): one instruction
+// for two lanes' operations, the same lane throughput on the FP32 pipe as the scalar forms.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// In-register 16-point Walsh-Hadamard butterflies with strides 1, 2, 4, 8 (no signs, no 1/4) on packed
+// pairs: two independent columns transformed together.
+__device__ __forceinline__ void fwht16_unscaled_x2(uint64_t v[16]) {
 #pragma unroll
     for (int h = 1; h < 16; h *= 2) {
 #pragma unroll
         for (int i = 0; i < 16; i += 2 * h) {
 #pragma unroll
             for (int j = i; j < i + h; ++j) {
-                const float a = v[j], b = v[j + h];
-                v[j] = __fadd_rn(a, b);
-                v[j + h] = __fsub_rn(a, b);
+                const uint64_t a = v[j], b = v[j + h];
+                v[j] = f2_add(a, b);
+                v[j + h] = f2_sub(a, b);
             }
         }
     }
 }
 
-// In-register 16-point transform without the final 1/4: signs, then butterflies with strides 1, 2, 4, 8.
-__device__ __forceinline__ void rht16_unscaled(float v[16], uint32_t signmask) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = ((signmask >> j) & 1u) ? -v[j] : v[j];
-    fwht16_unscaled(v);
-}
+
 
 // ---------------------------------------------------------------------------------------------
 // NVFP4 block-scale arithmetic (FP32, round to nearest, in the documented order).

@@ -334,17 +334,21 @@ __device__ __forceinline__ void load_16(const uint16_t* __restrict__ x, int64_t 
 // pair packed back to BF16 (RNE), so each word again holds the two columns' values of one token.
 template <int NW>
 __device__ __forceinline__ void rht16_pair_inplace(uint32_t (&xw)[16][NW], int w, uint32_t signmask) {
-    float a[16], b[16];
+    // the two columns as packed FP32 pairs: one instruction per butterfly for both
+    uint64_t p[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const uint32_t v = xw[i][w] ^ (((signmask >> i) & 1u) ? 0x80008000u : 0u);
-        a[i] = bf16_lo(v);
-        b[i] = bf16_hi(v);
+        p[i] = f2_pack(bf16_lo(v), bf16_hi(v));
     }
-    fwht16_unscaled(a);
-    fwht16_unscaled(b);
+    fwht16_unscaled_x2(p);
+    const uint64_t q = f2_pack(0.25f, 0.25f);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) xw[i][w] = pack_bf16x2(__fmul_rn(a[i], 0.25f), __fmul_rn(b[i], 0.25f));
+    for (int i = 0; i < 16; ++i) {
+        float lo, hi;
+        f2_unpack(f2_mul(p[i], q), lo, hi);
+        xw[i][w] = pack_bf16x2(lo, hi);
+    }
 }
 
 // Tensor amax of the (transformed) input.  With the transform, the maximum is taken over the FP32
@@ -365,13 +369,21 @@ colwise_amax_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint32
     if (RHT) {
         float mf = 0.0f;
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-            float v[16];
+        for (int jp = 0; jp < CPT / 2; ++jp) {
+            // the two columns of a word transformed together as packed FP32 pairs
+            uint64_t v[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = (j & 1) ? bf16_hi(xw[i][j >> 1]) : bf16_lo(xw[i][j >> 1]);
-            rht16_unscaled(v, signmask);
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t w = xw[i][jp] ^ (((signmask >> i) & 1u) ? 0x80008000u : 0u);
+                v[i] = f2_pack(bf16_lo(w), bf16_hi(w));
+            }
+            fwht16_unscaled_x2(v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) mf = fmaxf(mf, fabsf(v[i]));
+            for (int i = 0; i < 16; ++i) {
+                float lo, hi;
+                f2_unpack(v[i], lo, hi);
+                mf = fmaxf(mf, fmaxf(fabsf(lo), fabsf(hi)));
+            }
         }
         m = (pack_bf16x2(__fmul_rn(mf, 0.25f), 0.0f) & 0xFFFFu) << 16;
     } else {
