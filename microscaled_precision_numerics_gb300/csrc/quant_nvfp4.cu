@@ -584,48 +584,34 @@ matrix_amax_kernel(const uint16_t* __restrict__ w, int64_t per_matrix, uint32_t*
     }
 }
 
+// The work of one lane on its quarter of a 16x16 tile: rows 2 i + rpar (i = 0..7) x the 8 columns of
+// xr, the tile's other quarters in lanes l ^ 1, l ^ 16, l ^ 17; rS = nvfp4_fast_rs(S).  Writes this
+// lane's row-wise codes (rows o0 + 2 i + rpar at column h) and its half of the transposed codes, and
+// returns the tile's scale code.  All 32 lanes of the warp take part (shuffles); `store` gates the
+// global writes only.
 template <bool FOUR_SIX>
-__global__ void __launch_bounds__(128)
-weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, const uint32_t* __restrict__ amax,
-                      uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
-                      uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, float* __restrict__ s_w) {
-    __shared__ uint8_t st[W2_ROWS / 16][W2_COLS / 16];                 // tile scales
-    // matrices in the reverse of the amax pass's order: the first CTAs find the matrices that pass
-    // read last still in L2
-    const int64_t g = gridDim.z - 1 - blockIdx.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t o0 = (int64_t)blockIdx.y * W2_ROWS + warp * 16;
-    const int64_t h0 = (int64_t)blockIdx.x * W2_COLS;
-    const uint16_t* wg = w + g * O * H;
-    const float S = nvfp4_second_scale(__uint_as_float(amax[g]));
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) s_w[g] = S;
-
-    const int chunk = lane & 15, rpar = lane >> 4;
-    const int64_t h = h0 + chunk * 8;
-    const bool colv = h < H;
-    const bool rowv = o0 < O;
-    uint4 xr[8];
+__device__ __forceinline__ uint32_t w2d_lane_tile(const uint4 (&xr)[8], float S, float rS, int rpar, bool store,
+                                                  uint8_t* __restrict__ qrow_g, uint8_t* __restrict__ qcol_g,
+                                                  int64_t O, int64_t H, int64_t o0, int64_t h) {
     uint32_t m2 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int64_t o = o0 + 2 * i + rpar;
-        xr[i] = (rowv && colv) ? __ldcs(reinterpret_cast<const uint4*>(wg + o * H + h)) : make_uint4(0u, 0u, 0u, 0u);
         m2 = absmax_bf16x2(m2, xr[i].x); m2 = absmax_bf16x2(m2, xr[i].y);
         m2 = absmax_bf16x2(m2, xr[i].z); m2 = absmax_bf16x2(m2, xr[i].w);
     }
     uint32_t a16 = fold_halves(m2);
     a16 = max(a16, __shfl_xor_sync(0xFFFFFFFFu, a16, 1));
     a16 = max(a16, __shfl_xor_sync(0xFFFFFFFFu, a16, 16));
-    uint8_t* qrow_g = q_row + g * O * (H / 2);
     // codes of this lane's 8 rows x 8 columns with the tile's scale; with Four-over-Six both candidates
     // (the tile maximum mapped to 6 and to 4) and their largest dequantization errors, combined over the
-    // tile's four lanes (l, l^1, l^16, l^17), decide the scale
+    // tile's four lanes, decide the scale
     uint32_t codes[8];
     uint32_t bs = 0;
     float err_keep = 0.0f;
 #pragma unroll
     for (int k = 0; k < (FOUR_SIX ? 2 : 1); ++k) {
-        const uint32_t bsk = nvfp4_block_scale_m(__uint_as_float(a16 << 16), S, k == 0 ? 6.0f : 4.0f);
+        const uint32_t bsk = nvfp4_block_scale_fast(__uint_as_float(a16 << 16), S, rS, k == 0 ? 6.0f : 4.0f,
+                                                    k == 0 ? 1.0f / 6.0f : 0.25f);
         const float r = nvfp4_block_recip(bsk, S);
         uint32_t ck[8];
         float x[64];
@@ -660,49 +646,94 @@ weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, cons
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int rr = 2 * i + rpar;                     // row within the warp's 16
-        if (rowv && colv) __stcs(reinterpret_cast<uint32_t*>(qrow_g + (o0 + rr) * (H / 2) + h / 2), codes[i]);
+        if (store) __stcs(reinterpret_cast<uint32_t*>(qrow_g + (o0 + rr) * (H / 2) + h / 2), codes[i]);
     }
     // transposed copy: lanes l (even rows) and l ^ 16 (odd rows) swap code words; the even-row lane
     // then emits columns 0..3 of its chunk and the odd-row lane columns 4..7, each as the 8 bytes
-    // (16 rows, two per byte, even row in the low nibble) of that column's slice
-    uint32_t other[8];
+    // (16 rows, two per byte, even row in the low nibble) of that column's slice.  Per row pair i,
+    // byte b of ev[i] holds column 2b (even row's nibble low, odd row's high) and byte b of od[i]
+    // column 2b + 1; this lane's columns come from bytes p0 = 2 rpar and p0 + 1, gathered over the 8
+    // row pairs by byte permutes.
+    uint32_t ev[8], od[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) other[i] = __shfl_xor_sync(0xFFFFFFFFu, codes[i], 16);
-    uint8_t* qcol_g = q_col + g * H * (O / 2);
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, codes[i], 16);
+        const uint32_t e = rpar ? other : codes[i];
+        const uint32_t o = rpar ? codes[i] : other;
+        ev[i] = (e & 0x0F0F0F0Fu) | ((o << 4) & 0xF0F0F0F0u);
+        od[i] = ((e >> 4) & 0x0F0F0F0Fu) | (o & 0xF0F0F0F0u);
+    }
+    const uint32_t sel = rpar ? 0x7362u : 0x5140u;      // bytes p0 of a, p0 of b, p0 + 1 of a, p0 + 1 of b
+    uint32_t col[4][2];                                 // [column - 4 rpar][8-byte half]
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int i0 = 4 * half;
+        const uint32_t e01 = __byte_perm(ev[i0], ev[i0 + 1], sel), e23 = __byte_perm(ev[i0 + 2], ev[i0 + 3], sel);
+        const uint32_t o01 = __byte_perm(od[i0], od[i0 + 1], sel), o23 = __byte_perm(od[i0 + 2], od[i0 + 3], sel);
+        col[0][half] = __byte_perm(e01, e23, 0x5410u);
+        col[2][half] = __byte_perm(e01, e23, 0x7632u);
+        col[1][half] = __byte_perm(o01, o23, 0x5410u);
+        col[3][half] = __byte_perm(o01, o23, 0x7632u);
+    }
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-        const int j = jj + 4 * rpar;
-        uint32_t lo = 0u, hi = 0u;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t even = ((rpar ? other[i] : codes[i]) >> (4 * j)) & 0xFu;
-            const uint32_t odd = ((rpar ? codes[i] : other[i]) >> (4 * j)) & 0xFu;
-            const uint32_t byte = even | (odd << 4);
-            if (i < 4) lo |= byte << (8 * i); else hi |= byte << (8 * (i - 4));
-        }
-        const int64_t hc = h + j;
-        if (rowv && colv) __stcs(reinterpret_cast<uint2*>(qcol_g + hc * (O / 2) + o0 / 2), make_uint2(lo, hi));
+        const int64_t hc = h + jj + 4 * rpar;
+        if (store) __stcs(reinterpret_cast<uint2*>(qcol_g + hc * (O / 2) + o0 / 2), make_uint2(col[jj][0], col[jj][1]));
     }
+    return bs;
+}
+
+// Row-wise scales of the 16 rows o0 .. o0 + 15 of one warp: 8 tile scales each (tile columns from
+// h0 / 16), two words per row; lane l writes word (l & 1) of row o0 + (l >> 1).
+__device__ __forceinline__ void w2d_row_scales(const uint8_t (&stw)[W2_COLS / 16], uint8_t* __restrict__ s_row_g,
+                                               int64_t O, int64_t H, int64_t o0, int64_t h0, int lane) {
+    const int64_t nct = sf_col_tiles(H, 16);
+    const int rr = lane >> 1, half = lane & 1;
+    const int64_t kb = h0 / 16 + half * 4;
+    const int nb = (int)min64(4, H / 16 - kb);
+    if (o0 < O && nb > 0) {
+        uint8_t* p = s_row_g + sf_offset(o0 + rr, kb, nct);
+        if (nb == 4) {
+            *reinterpret_cast<uint32_t*>(p) = (uint32_t)stw[half * 4] | ((uint32_t)stw[half * 4 + 1] << 8) |
+                                              ((uint32_t)stw[half * 4 + 2] << 16) | ((uint32_t)stw[half * 4 + 3] << 24);
+        } else {
+            for (int i = 0; i < nb; ++i) p[i] = stw[half * 4 + i];
+        }
+    }
+}
+
+// Quantize pass: one 64 x 128 tile per CTA, each lane loading its own 16-byte chunks.
+template <bool FOUR_SIX>
+__global__ void __launch_bounds__(128)
+weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, const uint32_t* __restrict__ amax,
+                      uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
+                      uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, float* __restrict__ s_w) {
+    __shared__ uint8_t st[W2_ROWS / 16][W2_COLS / 16];                 // tile scales
+    // matrices in the reverse of the amax pass's order: the first CTAs find the matrices that pass
+    // read last still in L2
+    const int64_t g = gridDim.z - 1 - blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t o0 = (int64_t)blockIdx.y * W2_ROWS + warp * 16;
+    const int64_t h0 = (int64_t)blockIdx.x * W2_COLS;
+    const uint16_t* wg = w + g * O * H;
+    const float S = nvfp4_second_scale(__uint_as_float(amax[g]));
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) s_w[g] = S;
+
+    const int chunk = lane & 15, rpar = lane >> 4;
+    const int64_t h = h0 + chunk * 8;
+    const bool valid = (o0 < O) && (h < H);
+    uint4 xr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t o = o0 + 2 * i + rpar;
+        xr[i] = valid ? __ldcs(reinterpret_cast<const uint4*>(wg + o * H + h)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const uint32_t bs = w2d_lane_tile<FOUR_SIX>(xr, S, nvfp4_fast_rs(S), rpar, valid, q_row + g * O * (H / 2), q_col + g * H * (O / 2),
+                                                O, H, o0, h);
     if (lane < 16 && (lane & 1) == 0) st[warp][lane >> 1] = (uint8_t)bs;
     __syncthreads();
 
-    // row-wise scales: rows o0 .. o0 + 15 of this warp, 8 tile scales each (2 words per row)
-    {
-        const int64_t nct = sf_col_tiles(H, 16);
-        const int rr = lane >> 1, half = lane & 1;
-        const int64_t o = o0 + rr;
-        const int64_t kb = h0 / 16 + half * 4;
-        const int nb = (int)min64(4, H / 16 - kb);
-        if (rowv && nb > 0) {
-            uint8_t* p = s_row + g * host_scale_bytes_dev(O, H, 16) + sf_offset(o, kb, nct);
-            if (nb == 4) {
-                *reinterpret_cast<uint32_t*>(p) = (uint32_t)st[warp][half * 4] | ((uint32_t)st[warp][half * 4 + 1] << 8) |
-                                                  ((uint32_t)st[warp][half * 4 + 2] << 16) | ((uint32_t)st[warp][half * 4 + 3] << 24);
-            } else {
-                for (int i = 0; i < nb; ++i) p[i] = st[warp][half * 4 + i];
-            }
-        }
-    }
+    w2d_row_scales(st[warp], s_row + g * host_scale_bytes_dev(O, H, 16), O, H, o0, h0, lane);
     const int64_t ob = (int64_t)blockIdx.y * W2_ROWS;
     const int64_t nrows = min64(W2_ROWS, O - ob);      // multiple of 16
     // column-wise scales: row hc, scale columns ob/16 .. +3 (one word when all 4 row tiles exist)
@@ -723,6 +754,15 @@ weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, cons
             }
         }
     }
+}
+
+// The quantize pass of the plain (not Four-over-Six) 2D quantizer.
+cudaError_t launch_weight2d_quant_pass(const uint16_t* w, int64_t G, int64_t O, int64_t H, const uint32_t* amax,
+                                       uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, float* s_w,
+                                       cudaStream_t stream) {
+    dim3 grid((unsigned)((H + W2_COLS - 1) / W2_COLS), (unsigned)((O + W2_ROWS - 1) / W2_ROWS), (unsigned)G);
+    weight2d_quant_kernel<false><<<grid, 128, 0, stream>>>(w, O, H, amax, q_row, s_row, q_col, s_col, s_w);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -807,9 +847,7 @@ cudaError_t launch_nvfp4_weight_2d_given_amax(const uint16_t* w, int64_t G, int6
         cudaError_t e = cudaMemsetAsync(s_col, 0, (size_t)(host_scale_bytes(H, O, 16) * G), stream);
         if (e != cudaSuccess) return e;
     }
-    dim3 grid((unsigned)((H + W2_COLS - 1) / W2_COLS), (unsigned)((O + W2_ROWS - 1) / W2_ROWS), (unsigned)G);
-    weight2d_quant_kernel<false><<<grid, 128, 0, stream>>>(w, O, H, amax, q_row, s_row, q_col, s_col, s_w);
-    return cudaGetLastError();
+    return launch_weight2d_quant_pass(w, G, O, H, amax, q_row, s_row, q_col, s_col, s_w, stream);
 }
 
 cudaError_t launch_nvfp4_weight_2d(const uint16_t* w, int64_t G, int64_t O, int64_t H, uint8_t* q_row, uint8_t* s_row,
@@ -831,9 +869,9 @@ cudaError_t launch_nvfp4_weight_2d(const uint16_t* w, int64_t G, int64_t O, int6
     if (bx > cap) bx = cap;
     matrix_amax_kernel<<<dim3((unsigned)bx, (unsigned)G), 256, 0, stream>>>(w, per, ws);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!four_six) return launch_weight2d_quant_pass(w, G, O, H, ws, q_row, s_row, q_col, s_col, s_w, stream);
     dim3 grid((unsigned)((H + W2_COLS - 1) / W2_COLS), (unsigned)((O + W2_ROWS - 1) / W2_ROWS), (unsigned)G);
-    if (four_six) weight2d_quant_kernel<true><<<grid, 128, 0, stream>>>(w, O, H, ws, q_row, s_row, q_col, s_col, s_w);
-    else weight2d_quant_kernel<false><<<grid, 128, 0, stream>>>(w, O, H, ws, q_row, s_row, q_col, s_col, s_w);
+    weight2d_quant_kernel<true><<<grid, 128, 0, stream>>>(w, O, H, ws, q_row, s_row, q_col, s_col, s_w);
     return cudaGetLastError();
 }
 
