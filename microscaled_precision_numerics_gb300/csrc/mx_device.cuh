@@ -91,16 +91,44 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
 // (8 << 22) - 1 gives code 7 for every a >= 6 (and for infinities and NaN).
 // ---------------------------------------------------------------------------------------------
 
-// 2^22 - 1 - 64k for the k held in the low (high = false) or high half of a random word; 64k is a
-// sub-mask of 2^22 - 1, so the difference is an XOR.
-__device__ __forceinline__ uint32_t sr_kterm(uint32_t word, bool high) {
-    return (high ? ((word >> 10) & 0x3FFFC0u) : ((word << 6) & 0x3FFFC0u)) ^ 0x3FFFFFu;
+// Integer multiply-adds written out, so that they stay on the multiply-add pipe.
+__device__ __forceinline__ uint32_t mulhi_u32(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
-
-__device__ __forceinline__ uint32_t e2m1_sr_kterm(float v, uint32_t kterm) {
-    const uint32_t z = __float_as_uint(__fmul_ru(fabsf(v), __uint_as_float(0x00800000u)));   // a * 2^-126, rounded up
-    const uint32_t u = min(z + kterm, 0x01FFFFFFu);       // a >= 6: code 7
-    return (u >> 22) | ((__float_as_uint(v) >> 28) & 8u);
+__device__ __forceinline__ uint32_t mad_u32(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// The rounding above for the two values t0, t1 whose random k are the low and high halves of one Philox
+// output word: u = bits(z) + 2^22 - 1 - 64k (64k is a sub-mask of 2^22 - 1), clamped, gives the
+// magnitude code u >> 22; bit 3 is the sign of t.  The codes are added to acc0 at nibble n0 and to
+// acc1 at nibble n1 (acc0 and acc1 may be the same word).  The integer work runs as multiply-adds
+// where it can (the halves of the word, 64k, the shift by 22, the sign bit and the nibble placement),
+// leaving the logic pipe only the sum and the clamp.
+__device__ __forceinline__ void e2m1_sr_pair(float t0, float t1, uint32_t word, uint32_t& acc0, int n0, uint32_t& acc1,
+                                             int n1) {
+    const uint32_t r1 = mulhi_u32(word, 0x10000u);                 // high half
+    const uint32_t r0 = mad_u32(r1, 0xFFFF0000u, word);             // low half: word - 2^16 r1
+    const float t[2] = {t0, t1};
+    const uint32_t k[2] = {mad_u32(r0, 64u, 0u), mad_u32(r1, 64u, 0u)};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const uint32_t z = __float_as_uint(__fmul_ru(fabsf(t[e]), __uint_as_float(0x00800000u)));
+        const uint32_t u = min((z + 0x3FFFFFu) - k[e], 0x01FFFFFFu);
+        const uint32_t mag = mulhi_u32(u, 1024u);                    // u >> 22
+        const uint32_t sgn = mulhi_u32(__float_as_uint(t[e]), 2u);   // sign bit
+        const int n = e ? n1 : n0;
+        if (e) {
+            acc1 = mad_u32(mag, 1u << (4 * n), acc1);
+            acc1 = mad_u32(sgn, 8u << (4 * n), acc1);
+        } else {
+            acc0 = mad_u32(mag, 1u << (4 * n), acc0);
+            acc0 = mad_u32(sgn, 8u << (4 * n), acc0);
+        }
+    }
 }
 
 // acc + code * 2^(4 j) as one integer multiply-add (keeps the nibble packing off the logic pipe).

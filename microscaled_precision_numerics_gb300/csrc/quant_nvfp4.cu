@@ -46,9 +46,8 @@ __device__ __forceinline__ uint2 quant_block16(const uint4& a, const uint4& b, f
             const U4 rnd = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, k0, k1);
             const uint32_t rw[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                c[h] = pack_nibble(c[h], e2m1_sr_kterm(v[8 * h + j], sr_kterm(rw[j >> 1], j & 1)), j);
-            }
+            for (int jp = 0; jp < 4; ++jp)
+                e2m1_sr_pair(v[8 * h + 2 * jp], v[8 * h + 2 * jp + 1], rw[jp], c[h], 2 * jp, c[h], 2 * jp + 1);
         }
         return make_uint2(c[0], c[1]);
     }
@@ -467,10 +466,10 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
             const U4 r4 = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, k0, k1);
             const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) {
-                const uint32_t w = xw[i][j >> 1];
-                const float v = (j & 1) ? bf16_hi(w) : bf16_lo(w);
-                code[j][i >> 3] = pack_nibble(code[j][i >> 3], e2m1_sr_kterm(__fmul_rn(v, rcp[j]), sr_kterm(rw[j >> 1], j & 1)), i & 7);
+            for (int jp = 0; jp < CPT / 2; ++jp) {
+                const uint32_t w = xw[i][jp];
+                e2m1_sr_pair(__fmul_rn(bf16_lo(w), rcp[2 * jp]), __fmul_rn(bf16_hi(w), rcp[2 * jp + 1]), rw[jp],
+                             code[2 * jp][i >> 3], i & 7, code[2 * jp + 1][i >> 3], i & 7);
             }
         }
         if (valid) {
