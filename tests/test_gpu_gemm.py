@@ -54,8 +54,11 @@ def run_mxfp8(mx, orc, a, b, M, N, K):
     return d, A @ B.T, np.abs(A) @ np.abs(B).T
 
 
+# the last two give every CTA pair several tiles (more than the 76 pairs of the GPU run at once), so the
+# accumulator slots rotate and their barriers wrap; one with K beyond the 6-stage ring and a ragged N,
+# one with a single K stage
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (128, 256, 512), (256, 512, 1024), (200, 296, 384),
-                                   (1, 8, 128), (640, 1280, 2048)])
+                                   (1, 8, 128), (640, 1280, 2048), (4096, 4000, 1024), (2304, 4096, 128)])
 def test_mxfp8_gemm(mx, orc, M, N, K):
     a = synthetic.random_bf16(M + K, (M, K), "student_t")
     b = synthetic.random_bf16(N + K + 1, (N, K), "normal", 0.02)
