@@ -143,6 +143,7 @@ class Tiny:
     unit = "TFLOP/s"
     dtype = "e4m3 (f32 accumulate, bf16 out)"
     graph = True          # launch-bound: also timed as one CUDA graph per step
+    e2e_pipelined = False  # and its end-to-end copies run serially (staging copies would only add launches)
 
     def __init__(self, mx, torch, dev, data=None):
         import synthetic
@@ -929,39 +930,94 @@ def dominant_roofline(ops, per_op, peaks):
     return kind_roofline(kind, kms, kunits, is_bytes, kmem, peaks)
 
 
-def e2e_generic(work, torch, steps, ops=None, units_per_step=None, warmup=2):
+def e2e_generic(work, torch, steps, ops=None, units_per_step=None, warmup=2, pipelined=True):
     """End to end through the same calls: every step copies the step's inputs in from pinned host
-    memory, runs the ops and copies the results out to pinned host memory, one after the other on the
-    current stream (no overlap); CUDA events around all steps."""
+    memory, runs the ops and copies the results out to pinned host memory; CUDA events around all steps.
+    Reported two ways.  `value`: pipelined -- the host-to-device copies land in one of two device
+    staging sets on their own stream while the previous step computes, the step moves them into place
+    device-to-device, and its results leave through a second pair of staging sets on a third stream while
+    the next step computes.  `serial_value`: the same copies and calls one after the other on one stream
+    (the reported value as well when `pipelined` is false: a latency-bound step, where the staging copies
+    would only add launches)."""
     ins, outs = work.e2e_inputs(), work.e2e_outputs()
     ops = ops if ops is not None else work.ops()
     h_in = [t.cpu().pin_memory() for t in ins]
     h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    units = units_per_step if units_per_step is not None else step_units(work, ops)
+    to_value = lambda ms: round(units / (ms / 1e3) / unit_scale(work.unit), 2)
 
-    def step():
+    def serial_step():
         for d, h in zip(ins, h_in):
             d.copy_(h, non_blocking=True)
         for op in ops:
             op[4]()
         for d, h in zip(outs, h_out):
             h.copy_(d, non_blocking=True)
+
+    def timed(run, first_stream, last_stream):
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(first_stream)
+        run()
+        end.record(last_stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / steps
+
+    cur = torch.cuda.current_stream()
     for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps):
-        step()
-    end.record()
-    torch.cuda.synchronize()
-    ms = start.elapsed_time(end) / steps
-    units = units_per_step if units_per_step is not None else step_units(work, ops)
-    value = units / (ms / 1e3) / unit_scale(work.unit)
-    out = {"value": round(value, 2), "unit": work.unit, "ms_per_step": round(ms, 4), "steps": steps,
-           "h2d_bytes_per_step": int(sum(h.numel() * h.element_size() for h in h_in)),
-           "d2h_bytes_per_step": int(sum(h.numel() * h.element_size() for h in h_out)),
-           "note": "inputs copied in from pinned host memory, kernels, results copied out, every step, serially"}
-    del h_in, h_out
+        serial_step()
+    serial_ms = timed(lambda: [serial_step() for _ in range(steps)], cur, cur)
+    common = {"unit": work.unit, "steps": steps,
+              "h2d_bytes_per_step": int(sum(h.numel() * h.element_size() for h in h_in)),
+              "d2h_bytes_per_step": int(sum(h.numel() * h.element_size() for h in h_out))}
+    if not pipelined:
+        return {"value": to_value(serial_ms), "ms_per_step": round(serial_ms, 4), **common,
+                "serial_value": to_value(serial_ms), "serial_ms_per_step": round(serial_ms, 4),
+                "note": "inputs copied in from pinned host memory, kernels, results copied out, every step, serially "
+                        "(a latency-bound step: no staging pipeline)"}
+
+    st_in = [[torch.empty_like(t) for t in ins] for _ in range(2)]
+    st_out = [[torch.empty_like(t) for t in outs] for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]
+    ev_in, ev_used, ev_done, ev_out = ev(), ev(), ev(), ev()
+
+    def piped(n):
+        for i in range(n):
+            k = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_used[k])            # step i - 2 has moved staging set k into place
+                for st, h in zip(st_in[k], h_in):
+                    st.copy_(h, non_blocking=True)
+                ev_in[k].record(s_in)
+            cur.wait_event(ev_in[k])
+            for d, st in zip(ins, st_in[k]):
+                d.copy_(st)
+            ev_used[k].record(cur)
+            for op in ops:
+                op[4]()
+            if i >= 2:
+                cur.wait_event(ev_out[k])                   # step i - 2's results have left staging set k
+            for st, d in zip(st_out[k], outs):
+                st.copy_(d)
+            ev_done[k].record(cur)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[k])
+                for h, st in zip(h_out, st_out[k]):
+                    h.copy_(st, non_blocking=True)
+                ev_out[k].record(s_out)
+
+    piped(warmup)
+    s_in.wait_stream(s_out)                                 # the timed steps start after the warm-up's copies
+    ms = timed(lambda: piped(steps), s_in, s_out)
+    out = {"value": to_value(ms), "ms_per_step": round(ms, 4), **common,
+           "serial_value": to_value(serial_ms), "serial_ms_per_step": round(serial_ms, 4),
+           "note": "inputs copied in from pinned host memory and results copied out to pinned host memory every "
+                   "step; value: the copies of neighbouring steps overlap the kernels through two device staging "
+                   "sets (moved into place device-to-device inside the step); serial_value: copies and kernels "
+                   "one after the other on one stream"}
+    del h_in, h_out, st_in, st_out
     return out
 
 
@@ -1018,7 +1074,7 @@ def measure(work, torch, mx, peaks, steps, warmup, e2e=True, gpu_index=0):
             _, aper = time_ops(aops, torch, steps, warmup)
             out["aux"], _ = op_report(aops, aper, peaks)
     if e2e and hasattr(work, "e2e_inputs"):
-        out["e2e"] = e2e_generic(work, torch, steps, ops)
+        out["e2e"] = e2e_generic(work, torch, steps, ops, pipelined=getattr(work, "e2e_pipelined", True))
     return out
 
 
