@@ -105,29 +105,25 @@ __device__ __forceinline__ uint32_t mad_u32(uint32_t a, uint32_t b, uint32_t c) 
 // The rounding above for the two values t0, t1 whose random k are the low and high halves of one Philox
 // output word: u = bits(z) + 2^22 - 1 - 64k (64k is a sub-mask of 2^22 - 1), clamped, gives the
 // magnitude code u >> 22; bit 3 is the sign of t.  The codes are added to acc0 at nibble n0 and to
-// acc1 at nibble n1 (acc0 and acc1 may be the same word).  The integer work runs as multiply-adds
-// where it can (the halves of the word, 64k, the shift by 22, the sign bit and the nibble placement),
-// leaving the logic pipe only the sum and the clamp.
+// acc1 at nibble n1 (acc0 and acc1 may be the same word).  The integer work is split between the two
+// integer pipes: the halves of the word, 64k and the nibble placement as multiply-adds, the sum, the
+// clamp, the shift and the sign on the logic pipe (the split measured fastest; Philox's multiplies
+// already load the multiply-add pipe).
 __device__ __forceinline__ void e2m1_sr_pair(float t0, float t1, uint32_t word, uint32_t& acc0, int n0, uint32_t& acc1,
                                              int n1) {
     const uint32_t r1 = mulhi_u32(word, 0x10000u);                 // high half
     const uint32_t r0 = mad_u32(r1, 0xFFFF0000u, word);             // low half: word - 2^16 r1
-    const float t[2] = {t0, t1};
     const uint32_t k[2] = {mad_u32(r0, 64u, 0u), mad_u32(r1, 64u, 0u)};
+    const float t[2] = {t0, t1};
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const uint32_t z = __float_as_uint(__fmul_ru(fabsf(t[e]), __uint_as_float(0x00800000u)));
         const uint32_t u = min((z + 0x3FFFFFu) - k[e], 0x01FFFFFFu);
-        const uint32_t mag = mulhi_u32(u, 1024u);                    // u >> 22
-        const uint32_t sgn = mulhi_u32(__float_as_uint(t[e]), 2u);   // sign bit
         const int n = e ? n1 : n0;
-        if (e) {
-            acc1 = mad_u32(mag, 1u << (4 * n), acc1);
-            acc1 = mad_u32(sgn, 8u << (4 * n), acc1);
-        } else {
-            acc0 = mad_u32(mag, 1u << (4 * n), acc0);
-            acc0 = mad_u32(sgn, 8u << (4 * n), acc0);
-        }
+        // sign on the logic pipe: code = (u >> 22) | (bit 31 of t >> 28), placed by one multiply-add
+        const uint32_t code = (u >> 22) | ((__float_as_uint(t[e]) >> 28) & 8u);
+        if (e) acc1 = mad_u32(code, 1u << (4 * n), acc1);
+        else acc0 = mad_u32(code, 1u << (4 * n), acc0);
     }
 }
 
