@@ -127,13 +127,6 @@ __device__ __forceinline__ void e2m1_sr_pair(float t0, float t1, uint32_t word, 
     }
 }
 
-// acc + code * 2^(4 j) as one integer multiply-add (keeps the nibble packing off the logic pipe).
-__device__ __forceinline__ uint32_t pack_nibble(uint32_t acc, uint32_t code, int j) {
-    uint32_t r;
-    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(code), "r"(1u << (4 * j)), "r"(acc));
-    return r;
-}
-
 // ---------------------------------------------------------------------------------------------
 // Philox4x32-10 (Salmon et al., SC'11): counter (c0..c3), key (k0, k1).
 // ---------------------------------------------------------------------------------------------
@@ -152,11 +145,6 @@ __device__ __forceinline__ U4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c
         k0 += 0x9E3779B9u; k1 += 0xBB67AE85u;
     }
     return U4{c0, c1, c2, c3};
-}
-
-// RHT sign mask: bit j set means d_j = -1.
-__device__ __forceinline__ uint32_t rht_sign_mask(uint64_t seed) {
-    return philox4x32_10(0u, 0u, 1u, 0u, (uint32_t)seed, (uint32_t)(seed >> 32)).x & 0xFFFFu;
 }
 
 // Packed two-lane FP32 arithmetic (IEEE round-to-nearest per lane, as the scalar forms): one instruction
