@@ -282,3 +282,60 @@ def test_fp8_blockwise_wgrad_validation(lib):
     assert f(A8, A16, A16, A16, 128, 128, 128, A16, 128, NUL) == 2      # misaligned A
     assert f(A16, A16, A16, A16, 128, 132, 128, A16, 136, NUL) == 2     # N % 8
     assert f(A16, A16, A16, A16, 128, 128, 192, A16, 128, NUL) == 3     # K % 128
+
+
+# Every entry point with a size argument, as (function, a call that would pass its size checks, the
+# positions of its size arguments).  Each size set to 0, then to -1, must come back MX_ERR_INVALID_ARG from
+# the host-side checks (the addresses are never dereferenced: nothing is launched).
+def _sized_calls(lib):
+    A20 = ctypes.c_void_p(0x20000)
+    return [
+        ("mx_quantize_mxfp8", (A16, 32, 32, 32, A16, A16, A16, A16, NUL), [1, 2]),
+        ("mx_quantize_mxfp8_grouped", (A16, 32, 32, 32, 2, A16, A16, A16, NUL), [1, 2, 4]),
+        ("mx_quantize_mxfp8_amax", (A16, 256, 64, 64, A16, A16, NUL, NUL, 128, A16, NUL), [1, 2, 8]),
+        ("mx_nvfp4_quantize_per_token", (A16, 32, 32, 32, A16, A16, A16, NUL), [1, 2]),
+        ("mx_nvfp4_quantize_per_token_46", (A16, 32, 32, 32, A16, A16, A16, NUL), [1, 2]),
+        ("mx_nvfp4_quantize_per_token_grouped", (A16, 32, 32, 32, 2, A16, A16, A16, A16, NUL), [1, 2, 4]),
+        ("mx_nvfp4_quantize_weight_2d", (A16, 2, 32, 32, A16, A16, A16, A16, A16, A16, 4096, NUL), [1, 2, 3]),
+        ("mx_nvfp4_quantize_weight_2d_46", (A16, 2, 32, 32, A16, A16, A16, A16, A16, A16, 4096, NUL), [1, 2, 3]),
+        ("mx_nvfp4_quantize_weight_2d_noalloc", (A16, 2, 32, 32, A16, A16, A16, A16, A16, NUL), [1, 2, 3]),
+        ("mx_nvfp4_quantize_weight_2d_given_amax", (A16, 2, 32, 32, A16, A16, A16, A16, A16, A16, NUL), [1, 2, 3]),
+        ("mx_fp8_blockwise_quantize_1x128", (A16, 128, 128, 128, 0, A16, A16, NUL, A16, A16, NUL, NUL), [1, 2]),
+        ("mx_fp8_blockwise_quantize_128x128", (A16, 1, 128, 128, 0, A16, A16, A16, NUL, NUL, NUL), [1, 2, 3]),
+        ("mx_rht16", (A16, 32, 16, 0, A20, NUL), [1, 2]),
+        ("mx_nvfp4_quantize_1x16", (A16, 32, 32, 1, 0, 0, 0, 0, A16, A16, A16, A16, 16, NUL), [1, 2]),
+        ("mx_dequantize_bf16", (0, A16, A16, NUL, 0, 0, 32, 32, A16, NUL), [6, 7]),
+        ("mx_dequantize_nvfp4_amax", (A16, A16, A16, 128, 256, 64, A16, A16, NUL), [3, 4, 5]),
+        ("mx_scaled_gemm", (0, A16, A16, NUL, 0, A16, A16, NUL, 0, 128, 128, 128, A16, 128, NUL), [9, 10, 11]),
+        ("mx_grouped_scaled_gemm", (0, 2, A16, 256, A16, A16, NUL, A16, A16, NUL, 128, 128, A16, NUL), [1, 3, 10, 11]),
+        ("mx_gemm_bf16_dq_nvfp4", (A16, NUL, 0, A16, A16, A16, 1, 128, 128, 256, A16, 128, NUL), [7, 8, 9]),
+        ("mx_wgrad_bf16_dq_nvfp4", (A16, A16, A16, A16, 1, 128, 128, 128, A16, 128, NUL), [5, 6, 7]),
+        ("mx_fp8_blockwise_gemm", (A16, A16, A16, A16, 128, 128, 128, A16, 128, NUL), [4, 5, 6]),
+        ("mx_fp8_blockwise_gemm_wgrad", (A16, A16, A16, A16, 128, 128, 128, A16, 128, NUL), [4, 5, 6]),
+    ]
+
+
+def test_zero_and_negative_sizes_are_rejected_before_any_launch(lib):
+    covered = set()
+    for name, args, sizes in _sized_calls(lib):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        covered.add(name)
+        for i in sizes:
+            for bad in (0, -1):
+                call = list(args)
+                call[i] = bad
+                assert f(*[ctypes.c_int64(a) if isinstance(a, int) and j in sizes else a
+                           for j, a in enumerate(call)]) == 1, f"{name}: argument {i} = {bad}"
+    # every declared entry point that takes a size is in the table
+    sized = {n for n in declared_functions() if n not in (
+        "mx_status_string", "mx_scale_bytes", "mx_grouped_scale_bytes", "mx_workspace_bytes", "mx_check_device_status",
+        "mx_check_stream_status", "mx_watchdog_selftest", "mx_quantize_mxfp8_batched", "mx_count_mismatch")}
+    assert sized <= covered, sorted(sized - covered)
+
+
+def test_empty_comparison_is_a_no_op(lib):
+    """Comparing zero bytes counts nothing and launches nothing (the one zero-size call that succeeds)."""
+    f = lib.mx_count_mismatch
+    assert f(A16, A16, 0, A16, NUL) == 0
+    assert f(A16, A16, -1, A16, NUL) == 1
