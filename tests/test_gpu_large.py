@@ -1,0 +1,104 @@
+"""Parity past 2^31 elements: a 65600 x 32768 BF16 tensor (2 149 580 800 elements), so that element, code
+and scale offsets of the sampled outputs lie beyond the 32-bit range.
+
+The tensor is built on the device from a host-drawn 64-row block: row r is block row r % 64 times
+2^(((r // 64) % 7) - 3), an exact scaling of BF16 values.  Every oracle input is rebuilt on the host from the
+same block (sampled rows, full-height column slabs, and one 448-row period, which holds every 16-row group of
+the tensor and so its per-tensor maximum); nothing the device computes feeds the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from gpu_util import DEV, bf16_dev, first_mismatch, to_np, to_np_u16
+
+pytestmark = pytest.mark.gpu
+
+T, N = 65600, 32768
+RHT_SEED, SR_SEED = 81, 82
+BLOCK = synthetic.random_bf16(5150, (64, N), "normal", 1.0)
+
+
+def exponents(rows):
+    return ((np.asarray(rows, dtype=np.int64) // 64) % 7) - 3
+
+
+def host_rows(rows, c0=0, c1=N):
+    """Rows of the tensor (columns [c0, c1)) as BF16 bit patterns, built on the host."""
+    rows = np.asarray(rows, dtype=np.int64)
+    f = (BLOCK[rows % 64, c0:c1].astype(np.uint32) << 16).view(np.float32)
+    f = f * np.float32(2.0) ** exponents(rows).astype(np.float32)[:, None]
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.fixture(scope="module")
+def big():
+    import microscaled_precision_numerics_gb300 as mx
+    mx.lib()
+    blk = bf16_dev(BLOCK)
+    scale = torch.from_numpy((2.0 ** exponents(np.arange(T))).astype(np.float32)).to(DEV).to(torch.bfloat16)
+    x = blk.view(1, 64, N).expand(T // 64 + 1, 64, N).reshape(-1, N)[:T] * scale[:, None]
+    del blk
+    torch.cuda.synchronize()
+    assert x.numel() > 2 ** 31
+    # the device construction equals the host one (rows across the 2^31-element boundary)
+    for r in (0, 65535, 65536, T - 1):
+        assert np.array_equal(to_np_u16(x[r]), host_rows([r])[0])
+    yield mx, x
+    del x
+    torch.cuda.empty_cache()
+
+
+SAMPLE_ROWS = [0, 1, 4097, 65535, 65536, 65537, T - 1]
+
+
+def test_mxfp8_row_and_column_past_2g(big, orc):
+    mx, x = big
+    out = mx.alloc_mxfp8(T, N, DEV)
+    mx.mx_quantize_mxfp8(x, **out)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    rows = np.array(SAMPLE_ROWS)
+    qr, sr = orc.mxfp8_quantize_rowwise(host_rows(rows))
+    got_q = to_np(out["q_row"][torch.from_numpy(rows).to(DEV)])
+    assert np.array_equal(got_q, qr), first_mismatch(got_q, qr)
+    assert np.array_equal(orc.scales_from_gemm_layout(to_np(out["s_row"]), T, N // 32)[rows], sr)
+    for c0 in (0, N - 64):
+        qc, sc = orc.mxfp8_quantize_colwise(host_rows(np.arange(T), c0, c0 + 64))
+        got = to_np(out["q_col"][c0:c0 + 64])
+        assert np.array_equal(got, qc), first_mismatch(got, qc)
+        assert np.array_equal(orc.scales_from_gemm_layout(to_np(out["s_col"]), N, T // 32)[c0:c0 + 64], sc)
+    # the dequantize of the whole row-wise copy, sampled rows against the oracle's decode
+    y = torch.empty((T, N), dtype=torch.bfloat16, device=DEV)
+    mx.mx_dequantize_bf16(mx.MX_FMT_MXFP8, out["q_row"], out["s_row"], None, 0, T, N, y)
+    torch.cuda.synchronize()
+    got_y = to_np_u16(y[torch.from_numpy(rows).to(DEV)])
+    want_y = orc.dequant_mxfp8(qr, sr)
+    assert np.array_equal(got_y, want_y), first_mismatch(got_y, want_y)
+    del out, y
+
+
+def test_nvfp4_colwise_rht_sr_past_2g(big, orc):
+    mx, x = big
+    q = torch.empty((N, T // 2), dtype=torch.uint8, device=DEV)
+    s = torch.empty(mx.scale_bytes(N, T, 16), dtype=torch.uint8, device=DEV)
+    S = torch.empty(1, dtype=torch.float32, device=DEV)
+    ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+    mx.mx_nvfp4_quantize_1x16(x, True, True, RHT_SEED, True, SR_SEED, q, s, S, ws)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    # per-tensor scale from one 448-row period (every 16-row group of the tensor occurs in it), slab by slab
+    period = host_rows(np.arange(448))
+    amax = max(orc.nvfp4_1x16_amax(np.ascontiguousarray(period[:, c:c + 4096]), rht=True, rht_seed=RHT_SEED)
+               for c in range(0, N, 4096))
+    S_ref = orc.nvfp4_second_scale(amax)
+    assert to_np(S).view(np.uint32)[0] == np.float32(S_ref).view(np.uint32)
+    laid = orc.scales_from_gemm_layout(to_np(s), N, T // 16)
+    for c0 in (0, N - 64):
+        qo, so = orc.nvfp4_1x16_pass2(host_rows(np.arange(T), c0, c0 + 64), c0, N, S_ref, True, True, RHT_SEED,
+                                      True, SR_SEED)
+        got = to_np(q[c0:c0 + 64])
+        assert np.array_equal(got, qo), first_mismatch(got, qo)
+        assert np.array_equal(laid[c0:c0 + 64], so)
+    del q, s
