@@ -1,5 +1,6 @@
 """Parity past 2^31 elements: a 65600 x 32768 BF16 tensor (2 149 580 800 elements), so that element, code
-and scale offsets of the sampled outputs lie beyond the 32-bit range.
+and scale offsets of the sampled outputs lie beyond the 32-bit range: MXFP8 row and column quantize, the
+MXFP8 GEMM with that tensor as A, the MXFP8 dequantize, and the NVFP4 column-wise quantizer with RHT and SR.
 
 The tensor is built on the device from a host-drawn 64-row block: row r is block row r % 64 times
 2^(((r // 64) % 7) - 3), an exact scaling of BF16 values.  Every oracle input is rebuilt on the host from the
@@ -69,6 +70,23 @@ def test_mxfp8_row_and_column_past_2g(big, orc):
         got = to_np(out["q_col"][c0:c0 + 64])
         assert np.array_equal(got, qc), first_mismatch(got, qc)
         assert np.array_equal(orc.scales_from_gemm_layout(to_np(out["s_col"]), N, T // 32)[c0:c0 + 64], sc)
+    # FPROP-shaped GEMM with this tensor as A (2^31+ codes) and a 256-row B: sampled output rows against the
+    # FP64 product of the oracle's quantization of the same rows
+    b = synthetic.random_bf16(5151, (256, N), "normal", 0.02)
+    ob = mx.alloc_mxfp8(256, N, DEV, colwise=False)
+    mx.mx_quantize_mxfp8(bf16_dev(b), **ob)
+    d = torch.empty((T, 256), dtype=torch.bfloat16, device=DEV)
+    mx.mx_scaled_gemm(mx.MX_FMT_MXFP8, out["q_row"], out["s_row"], None, 0, ob["q_row"], ob["s_row"], None, 0,
+                      T, 256, N, d)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    A = orc.decode_mxfp8_f64(qr, sr)
+    B = orc.decode_mxfp8_f64(*orc.mxfp8_quantize_rowwise(b))
+    got_d = d[torch.from_numpy(rows).to(DEV)].float().cpu().numpy().astype(np.float64)
+    ref = A @ B.T
+    assert orc.rel_fro_error(got_d, ref) <= 1e-2
+    assert not (np.abs(got_d - ref) > 2.0 ** -7 * np.abs(ref) + 2.0 ** -15 * (np.abs(A) @ np.abs(B).T) + 1e-30).any()
+    del d
     # the dequantize of the whole row-wise copy, sampled rows against the oracle's decode
     y = torch.empty((T, N), dtype=torch.bfloat16, device=DEV)
     mx.mx_dequantize_bf16(mx.MX_FMT_MXFP8, out["q_row"], out["s_row"], None, 0, T, N, y)
