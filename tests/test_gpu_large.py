@@ -1,6 +1,7 @@
 """Parity past 2^31 elements: a 65600 x 32768 BF16 tensor (2 149 580 800 elements), so that element, code
 and scale offsets of the sampled outputs lie beyond the 32-bit range: MXFP8 row and column quantize, the
-MXFP8 GEMM with that tensor as A, the MXFP8 dequantize, and the NVFP4 column-wise quantizer with RHT and SR.
+MXFP8 GEMM with that tensor as A, the MXFP8 dequantize, the NVFP4 column-wise quantizer with RHT and SR,
+the per-token NVFP4 quantizer and the 16x16 weight quantizer (the tensor as 41 stacked matrices).
 
 The tensor is built on the device from a host-drawn 64-row block: row r is block row r % 64 times
 2^(((r // 64) % 7) - 3), an exact scaling of BF16 values.  Every oracle input is rebuilt on the host from the
@@ -120,3 +121,44 @@ def test_nvfp4_colwise_rht_sr_past_2g(big, orc):
         assert np.array_equal(got, qo), first_mismatch(got, qo)
         assert np.array_equal(laid[c0:c0 + 64], so)
     del q, s
+
+
+def test_nvfp4_per_token_past_2g(big, orc):
+    """Rows of 2048 blocks (the kernel's streaming path, rows re-read between the passes)."""
+    mx, x = big
+    out = mx.alloc_nvfp4_rows(T, N, DEV)
+    mx.mx_nvfp4_quantize_per_token(x, out["q"], out["s"], out["s2"])
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    rows = np.array(SAMPLE_ROWS)
+    q, s, st = orc.nvfp4_quantize_per_token(host_rows(rows))
+    sel = torch.from_numpy(rows).to(DEV)
+    got = to_np(out["q"][sel])
+    assert np.array_equal(got, q), first_mismatch(got, q)
+    assert np.array_equal(orc.scales_from_gemm_layout(to_np(out["s"]), T, N // 16)[rows], s)
+    assert np.array_equal(to_np(out["s2"][sel]).view(np.uint32), st.view(np.uint32))
+    del out
+
+
+def test_nvfp4_weight_2d_past_2g(big, orc):
+    """The tensor as 41 stacked 1600 x 32768 matrices; the last one lies past element 2^31."""
+    mx, x = big
+    G, O = 41, T // 41
+    w = x.view(G, O, N)
+    out = mx.alloc_nvfp4_weight_2d(G, O, N, DEV)
+    mx.mx_nvfp4_quantize_weight_2d(w, out["q_row"], out["s_row"], out["q_col"], out["s_col"], out["s_w"], out["ws"])
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    g = G - 1
+    qr, qc, st, sw = orc.nvfp4_quantize_weight_2d(host_rows(np.arange(g * O, (g + 1) * O)))
+    assert out["s_w"][g].item() == float(sw)
+    got = to_np(out["q_row"][g])
+    assert np.array_equal(got, qr), first_mismatch(got, qr)
+    got = to_np(out["q_col"][g])
+    assert np.array_equal(got, qc), first_mismatch(got, qc)
+    srb, scb = orc.scale_layout_bytes(O, N // 16), orc.scale_layout_bytes(N, O // 16)
+    assert np.array_equal(to_np(out["s_row"][g * srb:(g + 1) * srb]),
+                          orc.scales_to_gemm_layout(orc.weight_2d_operand_scales(st, "row")))
+    assert np.array_equal(to_np(out["s_col"][g * scb:(g + 1) * scb]),
+                          orc.scales_to_gemm_layout(orc.weight_2d_operand_scales(st, "col")))
+    del out
