@@ -41,6 +41,7 @@ FP8_OVER_BF16 = 2.0
 FP4_OVER_BF16 = 6.0
 # Published dense peaks of one GB300 (the GB300 NVL72 specification: FP4 1,080 PFLOP/s dense, FP8/FP6
 # 720 and FP16/BF16 360 PFLOP/s with 2:4 sparsity, per 72 GPUs), the denominators of the >= 60 % bar.
+HEAD_START_CYCLES = 2_000_000     # about 1 ms of SM clock: longer than the host needs to queue the first calls
 DATASHEET = {"bf16": 2500.0, "fp8": 5000.0, "fp4": 15000.0,
              "source": "GB300 NVL72 specification / 72 GPUs, dense (FP4 1080 PF dense; FP8 720 and BF16 360 PF "
                        "sparse, halved)"}
@@ -803,6 +804,7 @@ def time_device(work, torch, steps, warmup, dist=None):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    head_start(torch)
     start.record()
     for s in range(steps):
         e = evs[s]
@@ -819,6 +821,13 @@ def time_device(work, torch, steps, warmup, dist=None):
     return total_ms, per_op
 
 
+def head_start(torch):
+    """Just before a timed region (after its synchronize): a short device-side spin on the current stream,
+    so that the host queues the timed calls behind it and the first call's time does not include the host's
+    submission of that call to an idle GPU.  The spin ends before the start event is recorded."""
+    torch.cuda._sleep(HEAD_START_CYCLES)
+
+
 def time_ops(ops, torch, steps, warmup):
     """Per-op CUDA-event times (ms, averaged over `steps`) for a list of 5-tuples."""
     for _ in range(warmup):
@@ -828,6 +837,7 @@ def time_ops(ops, torch, steps, warmup):
     n = len(ops)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    head_start(torch)
     start.record()
     for st in range(steps):
         evs[st][0].record()
@@ -1038,6 +1048,7 @@ def graph_step(work, torch, ops, steps, warmup):
         g.replay()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    head_start(torch)
     start.record()
     for _ in range(steps):
         g.replay()
