@@ -568,3 +568,102 @@ def test_nvfp4_weight_2d_four_over_six(mx, orc, G, O, H):
         assert np.array_equal(to_np(out["s_col"][g * scb:(g + 1) * scb]),
                               orc.scales_to_gemm_layout(orc.weight_2d_operand_scales(st, "col")))
         assert to_np(out["s_w"])[g] == sw
+
+
+# ------------------------------------------------------------------------------------------------
+# Non-finite inputs.  The pages quantize finite training values; a block that holds an infinity or a NaN
+# gets unspecified codes and scale.  Every other block must be exact as before: the damage stays in the
+# blocks (MXFP8), tokens (per-token NVFP4) or matrices (2D NVFP4) that hold the value.
+# ------------------------------------------------------------------------------------------------
+NONFINITE = (0x7FC0, 0x7F80, 0xFF80)          # BF16 NaN, +Inf, -Inf
+
+
+def test_mxfp8_non_finite_values_stay_in_their_blocks(mx, orc):
+    R, K = 256, 512
+    x = synthetic.random_bf16(4040, (R, K), "normal", 1.0)
+    spots = [(3, 40), (100, 300), (200, 7)]
+    for (r, c), v in zip(spots, NONFINITE):
+        x[r, c] = v
+    out = mx.alloc_mxfp8(R, K, DEV)
+    mx.mx_quantize_mxfp8(bf16_dev(x), **out)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    qr, sr = orc.mxfp8_quantize_rowwise(x)
+    qc, sc = orc.mxfp8_quantize_colwise(x)
+    row_ok = np.ones((R, K // 32), dtype=bool)
+    col_ok = np.ones((K, R // 32), dtype=bool)
+    for r, c in spots:
+        row_ok[r, c // 32] = False
+        col_ok[c, r // 32] = False
+    got_sr = orc.scales_from_gemm_layout(to_np(out["s_row"]), R, K // 32)
+    got_sc = orc.scales_from_gemm_layout(to_np(out["s_col"]), K, R // 32)
+    assert np.array_equal(got_sr[row_ok], sr[row_ok])
+    assert np.array_equal(to_np(out["q_row"]).reshape(R, K // 32, 32)[row_ok], qr.reshape(R, K // 32, 32)[row_ok])
+    assert np.array_equal(got_sc[col_ok], sc[col_ok])
+    assert np.array_equal(to_np(out["q_col"]).reshape(K, R // 32, 32)[col_ok], qc.reshape(K, R // 32, 32)[col_ok])
+
+
+def test_nvfp4_per_token_non_finite_values_stay_in_their_tokens(mx, orc):
+    T, H = 64, 512
+    x = synthetic.random_bf16(4041, (T, H), "student_t")
+    rows = [5, 20, 41]
+    for r, v in zip(rows, NONFINITE):
+        x[r, 100 + r] = v
+    out = mx.alloc_nvfp4_rows(T, H, DEV)
+    mx.mx_nvfp4_quantize_per_token(bf16_dev(x), out["q"], out["s"], out["s2"])
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    q, s, st = orc.nvfp4_quantize_per_token(x)
+    ok = np.setdiff1d(np.arange(T), rows)
+    assert np.array_equal(to_np(out["q"])[ok], q[ok])
+    assert np.array_equal(orc.scales_from_gemm_layout(to_np(out["s"]), T, H // 16)[ok], s[ok])
+    assert np.array_equal(to_np(out["s2"]).view(np.uint32)[ok], st.view(np.uint32)[ok])
+
+
+def test_nvfp4_weight_2d_non_finite_values_stay_in_their_matrix(mx, orc):
+    G, O, H = 3, 64, 128
+    w = synthetic.random_bf16(4042, (G, O, H), "normal", 0.02)
+    w[1, 10, 20], w[1, 63, 127] = NONFINITE[0], NONFINITE[1]
+    out = mx.alloc_nvfp4_weight_2d(G, O, H, DEV)
+    mx.mx_nvfp4_quantize_weight_2d(bf16_dev(w), out["q_row"], out["s_row"], out["q_col"], out["s_col"], out["s_w"],
+                                   out["ws"])
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    srb, scb = orc.scale_layout_bytes(O, H // 16), orc.scale_layout_bytes(H, O // 16)
+    for g in (0, 2):
+        qr, qc, st, sw = orc.nvfp4_quantize_weight_2d(np.ascontiguousarray(w[g]))
+        assert np.array_equal(to_np(out["q_row"][g]), qr)
+        assert np.array_equal(to_np(out["q_col"][g]), qc)
+        assert np.array_equal(to_np(out["s_row"][g * srb:(g + 1) * srb]),
+                              orc.scales_to_gemm_layout(orc.weight_2d_operand_scales(st, "row")))
+        assert np.array_equal(to_np(out["s_col"][g * scb:(g + 1) * scb]),
+                              orc.scales_to_gemm_layout(orc.weight_2d_operand_scales(st, "col")))
+        assert out["s_w"][g].item() == float(sw)
+
+
+@pytest.mark.parametrize("v", NONFINITE)
+def test_nvfp4_per_tensor_non_finite(mx, orc, v):
+    """One scale for the whole tensor (RHT + SR column-wise here).  The tensor maximum skips a NaN, as the
+    oracle's does, so only the NaN's own block (its 16 tokens of one column, across which the transform
+    spreads it) is unspecified and every other block is exact; an infinity makes the scale infinite on both
+    sides.  Either way both passes run to the end with no device error."""
+    T, N = 64, 256
+    x = synthetic.random_bf16(4043, (T, N), "normal", 1.0)
+    x[17, 33] = v
+    q = torch.empty((N, T // 2), dtype=torch.uint8, device=DEV)
+    s = torch.empty(mx.scale_bytes(N, T, 16), dtype=torch.uint8, device=DEV)
+    S = torch.empty(1, dtype=torch.float32, device=DEV)
+    ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+    mx.mx_nvfp4_quantize_1x16(bf16_dev(x), True, True, 7, True, 8, q, s, S, ws)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    S_ref = orc.nvfp4_second_scale(orc.nvfp4_1x16_amax(x, rht=True, rht_seed=7))
+    assert to_np(S).view(np.uint32)[0] == np.float32(S_ref).view(np.uint32)
+    if v == NONFINITE[0]:
+        qo, so = orc.nvfp4_1x16_pass2(x, 0, N, S_ref, True, True, 7, True, 8)
+        ok = np.ones((N, T // 16), dtype=bool)
+        ok[33, 17 // 16] = False
+        assert np.array_equal(to_np(q).reshape(N, T // 16, 8)[ok], qo.reshape(N, T // 16, 8)[ok])
+        assert np.array_equal(orc.scales_from_gemm_layout(to_np(s), N, T // 16)[ok], so[ok])
+    else:
+        assert np.isinf(to_np(S)[0])
