@@ -667,3 +667,60 @@ def test_nvfp4_per_tensor_non_finite(mx, orc, v):
         assert np.array_equal(orc.scales_from_gemm_layout(to_np(s), N, T // 16)[ok], so[ok])
     else:
         assert np.isinf(to_np(S)[0])
+
+
+def test_nvfp4_all_zero_tensors(mx, orc):
+    """All-zero inputs put the second-level scale at 0 (S = 0, block scales 0, reciprocals 0): every NVFP4
+    quantizer gives the oracle's bytes (all-zero codes and scales, S = 0), and the GEMM and the dequantize
+    of those codes give zeros."""
+    T, H = 64, 256
+    x = np.zeros((T, H), dtype=np.uint16)
+    xd = bf16_dev(x)
+    out = mx.alloc_nvfp4_rows(T, H, DEV)
+    for fn, ref in ((mx.mx_nvfp4_quantize_per_token, orc.nvfp4_quantize_per_token),
+                    (mx.mx_nvfp4_quantize_per_token_46, orc.nvfp4_quantize_per_token_46)):
+        out["q"].fill_(0xA5)
+        out["s"].fill_(0xA5)
+        fn(xd, out["q"], out["s"], out["s2"])
+        q, s, st = ref(x)
+        assert np.array_equal(to_np(out["q"]), q)
+        assert np.array_equal(orc.scales_from_gemm_layout(to_np(out["s"]), T, H // 16), s)
+        assert np.array_equal(to_np(out["s2"]).view(np.uint32), st.view(np.uint32))
+    for colwise in (False, True):
+        for rht, sr in ((False, False), (True, False), (False, True), (True, True)):
+            if rht and not colwise:
+                continue                                  # the transform runs along tokens (column-wise) only
+            qd = torch.full((H, T // 2) if colwise else (T, H // 2), 0xA5, dtype=torch.uint8, device=DEV)
+            sd = torch.full((mx.scale_bytes(H, T, 16) if colwise else mx.scale_bytes(T, H, 16),), 0xA5,
+                            dtype=torch.uint8, device=DEV)
+            S = torch.full((1,), -1.0, dtype=torch.float32, device=DEV)
+            mx.mx_nvfp4_quantize_1x16(xd, colwise, rht, 5, sr, 6, qd, sd, S,
+                                      torch.empty(16, dtype=torch.uint8, device=DEV))
+            qo, so, So = orc.nvfp4_quantize_1x16(x, colwise=colwise, rht=rht, rht_seed=5, sr=sr, sr_seed=6)
+            assert to_np(S)[0] == np.float32(So) == 0.0
+            assert np.array_equal(to_np(qd), qo), (colwise, rht, sr)
+            rows, k = (H, T) if colwise else (T, H)
+            assert np.array_equal(orc.scales_from_gemm_layout(to_np(sd), rows, k // 16), so), (colwise, rht, sr)
+    G, O = 2, 64
+    w = np.zeros((G, O, H), dtype=np.uint16)
+    wo = mx.alloc_nvfp4_weight_2d(G, O, H, DEV)
+    for fn in (mx.mx_nvfp4_quantize_weight_2d, mx.mx_nvfp4_quantize_weight_2d_46):
+        for k in ("q_row", "s_row", "q_col", "s_col"):
+            wo[k].fill_(0xA5)
+        fn(bf16_dev(w), wo["q_row"], wo["s_row"], wo["q_col"], wo["s_col"], wo["s_w"], wo["ws"])
+        qr, qc, st, sw = orc.nvfp4_quantize_weight_2d(np.ascontiguousarray(w[0]))
+        for g in range(G):
+            assert np.array_equal(to_np(wo["q_row"][g]), qr) and np.array_equal(to_np(wo["q_col"][g]), qc)
+            assert wo["s_w"][g].item() == float(sw) == 0.0
+        assert int(wo["s_row"].sum()) == 0 and int(wo["s_col"].sum()) == 0
+    # the codes of zeros through the GEMM (per-token S = 0 on A) and the dequantize
+    mx.mx_nvfp4_quantize_per_token(xd, out["q"], out["s"], out["s2"])
+    d = torch.full((T, O), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mx.mx_scaled_gemm(mx.MX_FMT_NVFP4, out["q"], out["s"], out["s2"], mx.MX_SCOPE_ROW, wo["q_row"][0],
+                      wo["s_row"][:mx.scale_bytes(O, H, 16)], wo["s_w"][0:1], mx.MX_SCOPE_TENSOR, T, O, H, d)
+    y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mx.mx_dequantize_bf16(mx.MX_FMT_NVFP4, out["q"], out["s"], out["s2"], mx.MX_SCOPE_ROW, T, H, y)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    assert int(torch.count_nonzero(d.float())) == 0 and not torch.isnan(d.float()).any()
+    assert int(torch.count_nonzero(y.float())) == 0 and not torch.isnan(y.float()).any()
