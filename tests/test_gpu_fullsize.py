@@ -102,6 +102,28 @@ def test_dense_mlp_gemms_sampled(orc, dense):
     check_block(orc, dense["dw"].float().cpu().numpy()[np.ix_(o, h)], A @ B.T, np.abs(A) @ np.abs(B).T)
 
 
+def test_dense_mlp_gemms_full(orc, dense):
+    """Every output element of the three dense-MLP GEMMs (2.47 TFLOP) against the FP64 products of the
+    oracle's own MXFP8 quantization of the whole operands: the relative Frobenius error of each output
+    within 1e-2.  The element-wise bound is checked on the sampled blocks above."""
+    d, T, H, F = dense["data"], dense["T"], dense["H"], dense["F"]
+    dec = orc.decode_mxfp8_f64
+    X_r = dec(*orc.mxfp8_quantize_rowwise(d["x"]))
+    W_r = dec(*orc.mxfp8_quantize_rowwise(d["w"]))
+    err = orc.rel_fro_error(dense["y"].float().cpu().numpy().astype(np.float64), X_r @ W_r.T)     # FPROP
+    assert err <= TOL, f"FPROP {err}"
+    del W_r
+    dY_r = dec(*orc.mxfp8_quantize_rowwise(d["dy"]))
+    W_c = dec(*orc.mxfp8_quantize_colwise(d["w"]))
+    err = orc.rel_fro_error(dense["dx"].float().cpu().numpy().astype(np.float64), dY_r @ W_c.T)   # DGRAD
+    assert err <= TOL, f"DGRAD {err}"
+    del dY_r, W_c, X_r
+    dY_c = dec(*orc.mxfp8_quantize_colwise(d["dy"]))
+    X_c = dec(*orc.mxfp8_quantize_colwise(d["x"]))
+    err = orc.rel_fro_error(dense["dw"].float().cpu().numpy().astype(np.float64), dY_c @ X_c.T)   # WGRAD
+    assert err <= TOL, f"WGRAD {err}"
+
+
 def test_dense_mlp_fp32_scale_blockwise_sampled(mx, orc, dense):
     """The dense MLP shapes in blockwise FP8 with FP32 scales (NeMo RL FP8 page, the DeepSeek-V3 recipe), in the
     launch configuration `bench.py --workload dense_fp8_blockwise` times: X row-wise [1, 128] and W [128, 128]
