@@ -8,10 +8,10 @@
 // with one E4M3 scale per 16 (scale_vec::4X); the FP32 second-level scales are applied in the
 // epilogue.
 //
-// Structure: persistent clusters of two CTAs (one per SM) over 256 x 256 output tiles.  The even
-// CTA issues the pair MMA (tcgen05.mma.cta_group::2, M = 256): each CTA holds 128 rows of A and 128
-// of the 256 B rows in its shared memory and 128 accumulator rows in its TMEM, so each SM loads half
-// of the B tile.
+// Structure: persistent clusters of two CTAs (one per SM) over 256 x 256 output tiles (256 x 384 for
+// large dense MXFP8 GEMMs).  The even CTA issues the pair MMA (tcgen05.mma.cta_group::2, M = 256):
+// each CTA holds 128 rows of A and half of the B rows in its shared memory and 128 accumulator rows
+// in its TMEM, so each SM loads half of the B tile.
 //   warp 0        (both CTAs) TMA producer: A rows, B half and scale atoms (128-byte swizzle for the
 //                 operands) into a 6-stage (MXFP8) / 5-stage (NVFP4) ring; the loads of both CTAs
 //                 signal the stage barrier in the even CTA
@@ -110,6 +110,7 @@ __device__ __forceinline__ void bulk_signal_copy(uint32_t dst_cluster, uint32_t 
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -239,7 +240,7 @@ __device__ __forceinline__ void epilogue_drain(const Params& p, uint32_t tacc, i
 // Stores of one drained tile slice: rows [row0 + 32 q, +32) that belong to the tile, columns of the
 // warp's half.  TMA stores from the warp's two staging buffers at ebase, or plain 16-byte stores for
 // a slice that straddles the end of an expert group.
-template <int TN, bool GROUPED>
+template <int TN, bool GROUPED, int NBUF>
 __device__ __forceinline__ void epilogue_store(const Params& p, const CUtensorMap* tmD, int q, int h, int lane,
                                                int64_t row0, int64_t row_end, int64_t n0, uint32_t ebase,
                                                uint32_t& epi_chunk, const uint32_t (&packed)[TN / 4]) {
@@ -256,10 +257,13 @@ __device__ __forceinline__ void epilogue_store(const Params& p, const CUtensorMa
         for (int c = 0; c < EPI_HALF / EPI_COLS; ++c) {
             const int64_t col0 = nh + c * EPI_COLS;
             if (col0 < p.N) {
-                const uint32_t buf = ebase + (epi_chunk & 1u) * (uint32_t)EPI_BUF_BYTES;
+                const uint32_t buf = ebase + (NBUF == 2 ? (epi_chunk & 1u) * (uint32_t)EPI_BUF_BYTES : 0u);
                 ++epi_chunk;
-                // the store issued from this buffer two chunks ago must have read it
-                if (lane == 0) bulk_wait_group_read1();
+                // the store issued from this buffer NBUF chunks ago must have read it
+                if (lane == 0) {
+                    if (NBUF == 2) bulk_wait_group_read1();
+                    else bulk_wait_group_read0();
+                }
                 __syncwarp();
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
@@ -298,6 +302,11 @@ __device__ __forceinline__ void epilogue_store(const Params& p, const CUtensorMa
 //             drain is a small share of a tile
 //   TN = 128: two accumulators (2 x 128 columns): the epilogue of tile i overlaps the MMAs of tile
 //             i + 1; short-K grouped GEMMs, where a tile is only a few stages long
+//   TN = 384: one accumulator of 384 columns filled by two MMAs per K step (N = 256 into columns
+//             [0, 256), N = 128 into [256, 384)); dense MXFP8 only (the NVFP4 scale columns of a
+//             stage would not fit next to it in TMEM).  Each CTA holds B rows [128 r, +128) and
+//             [256 + 64 r, +64) of the tile, so both MMAs find their B halves and their B scale
+//             bands (128-row atoms 0-1 and 2) whole
 //   both CTAs  warp 0: TMA loads of this CTA's A rows, B half and scale atoms (the B scales of all
 //              TN columns, which each CTA's tensor core reads from its own TMEM); every load
 //              signals the stage barrier in the even (leader) CTA
@@ -307,11 +316,18 @@ __device__ __forceinline__ void epilogue_store(const Params& p, const CUtensorMa
 // ---------------------------------------------------------------------------------------------
 template <int FMT, bool GROUPED, int TN>
 struct PairCfg {
-    static_assert(TN == 128 || TN == 256, "tile width");
+    static_assert(TN == 128 || TN == 256 || TN == 384, "tile width");
+    static_assert(TN != 384 || (FMT == 0 && !GROUPED), "384-column tiles: dense MXFP8 only");
     static constexpr int ACC = TN == 128 ? 2 : 1;          // accumulator buffers
     // ring depth within the shared-memory budget (the grouped tables take 16.5 KB)
-    static constexpr int NST = FMT == 0 ? (TN == 256 ? (GROUPED ? 5 : 6) : (GROUPED ? 6 : 8))
+    static constexpr int NST = TN == 384 ? 5
+                             : FMT == 0 ? (TN == 256 ? (GROUPED ? 5 : 6) : (GROUPED ? 6 : 8))
                                         : (TN == 256 ? 5 : (GROUPED ? 6 : 7));
+    // rows per B load: 384-column tiles load each CTA's 192 rows as three 64-row boxes (128 rows for
+    // the N = 256 MMA, 64 for the N = 128 MMA), the other widths one box of TN / 2 rows
+    static constexpr int B_BOX = TN == 384 ? 64 : TN / 2;
+    // epilogue staging buffers per warp (one for 384-column tiles, so that a fifth stage fits)
+    static constexpr int EPI_NBUF = TN == 384 ? 1 : 2;
     static constexpr int SF_ATOMS_A = FMT == 0 ? 1 : 4;
     static constexpr int SFB_BANDS = TN / 128;
     static constexpr int SFA_BYTES = 512 * SF_ATOMS_A;     // this CTA's 128 rows
@@ -327,7 +343,7 @@ struct PairCfg {
     static constexpr int SMEM_SFA = SMEM_B + NST * B_BYTES;
     static constexpr int SMEM_SFB = SMEM_SFA + NST * SFA_BYTES;
     static constexpr int SMEM_EPI = (SMEM_SFB + NST * SFB_BYTES + 1023) / 1024 * 1024;
-    static constexpr int SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
+    static constexpr int SMEM_BAR = SMEM_EPI + EPI_WARPS * EPI_NBUF * EPI_BUF_BYTES;
     static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 7);
     static constexpr int SMEM_SIGNAL = (SMEM_MISC + 16 + 15) / 16 * 16;   // 16-byte signal source / target
     static constexpr int SMEM_TABLES = SMEM_SIGNAL + 16;   // grouped: row offsets, pair-tile and band prefixes
@@ -471,7 +487,16 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const int64_t ct0 = ks * C::SF_ATOMS_A;
                     const int32_t kb = (int32_t)(ks * BKB);
                     tma_load_2d_pair(sA, &tmA, kb, (int32_t)tile.row0, fb);
-                    tma_load_2d_pair(sB, &tmB, kb, (int32_t)brow, fb);
+                    if (TN == 384) {
+                        // the N = 256 MMA takes columns [128 rank, +128) of the tile from this CTA,
+                        // the N = 128 MMA columns [256 + 64 rank, +64)
+                        const int64_t b0 = tile.n0 + 128 * (int64_t)rank;
+                        tma_load_2d_pair(sB, &tmB, kb, (int32_t)b0, fb);
+                        tma_load_2d_pair(sB + 64 * BKB, &tmB, kb, (int32_t)(b0 + 64), fb);
+                        tma_load_2d_pair(sB + 128 * BKB, &tmB, kb, (int32_t)(tile.n0 + 256 + 64 * (int64_t)rank), fb);
+                    } else {
+                        tma_load_2d_pair(sB, &tmB, kb, (int32_t)brow, fb);
+                    }
                     // scale atoms: 512 bytes = two 256-byte rows of the scale maps; bands past the
                     // end of a tensor read as zeros
                     tma_load_2d_pair(sSFA, &tmSA, 0, (int32_t)((tile.band_a * p.nct + ct0) * 2), fb);
@@ -522,9 +547,21 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             // NVFP4: each MMA (K = 64) consumes a whole atom word
                             const uint32_t sf_id = FMT == 0 ? (uint32_t)j : 0u;
                             const uint32_t col = FMT == 0 ? 0u : (uint32_t)j;
-                            tc2_mma<FMT>(tacc, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j),
-                                         make_idesc<FMT, 2 * BM, TN>(sf_id), tSFA + 4 * col,
-                                         tSFB + C::SFB_BANDS * 4 * col, (ks > 0 || j > 0) ? 1u : 0u);
+                            const uint32_t accum = (ks > 0 || j > 0) ? 1u : 0u;
+                            if (TN == 384) {
+                                // columns [0, 256) from the first 128 B rows of each CTA (scale bands 0
+                                // and 1), columns [256, 384) from the next 64 (band 2)
+                                tc2_mma<FMT>(tacc, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j),
+                                             make_idesc<FMT, 2 * BM, 256>(sf_id), tSFA + 4 * col,
+                                             tSFB + C::SFB_BANDS * 4 * col, accum);
+                                tc2_mma<FMT>(tacc + 256, desc_sw128(sA + 32 * j), desc_sw128(sB + 128 * BKB + 32 * j),
+                                             make_idesc<FMT, 2 * BM, 128>(sf_id), tSFA + 4 * col,
+                                             tSFB + C::SFB_BANDS * 4 * col + 8, accum);
+                            } else {
+                                tc2_mma<FMT>(tacc, desc_sw128(sA + 32 * j), desc_sw128(sB + 32 * j),
+                                             make_idesc<FMT, 2 * BM, TN>(sf_id), tSFA + 4 * col,
+                                             tSFB + C::SFB_BANDS * 4 * col, accum);
+                            }
                         }
                         tc2_commit_mc(bar_empty + 8 * stage, (uint16_t)3);
                     }
@@ -575,7 +612,7 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int q = warp & 3;                     // TMEM lane quadrant this warp may access
         const int h = (warp - 2) >> 2;              // column half
         const uint32_t tempty_mine = leader ? bar_tempty : bar_tempty_odd;
-        const uint32_t ebase = sbase + C::SMEM_EPI + (uint32_t)((warp - 2) * 2 * EPI_BUF_BYTES);
+        const uint32_t ebase = sbase + C::SMEM_EPI + (uint32_t)((warp - 2) * C::EPI_NBUF * EPI_BUF_BYTES);
         uint32_t epi_chunk = 0;
         // tile coordinates and row scales of the next tile are fetched while this tile's stores run
         PairTile tile{};
@@ -601,7 +638,7 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int64_t row = tile.row0 + q * 32 + lane;
                 epilogue_alphas<GROUPED>(p, row, row < tile.row_end, tile.g, aa, ab_g);
             }
-            epilogue_store<TN, GROUPED>(p, &tmD, q, h, lane, cur.row0, cur.row_end, cur.n0, ebase, epi_chunk, packed);
+            epilogue_store<TN, GROUPED, C::EPI_NBUF>(p, &tmD, q, h, lane, cur.row0, cur.row_end, cur.n0, ebase, epi_chunk, packed);
         }
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
@@ -1517,7 +1554,7 @@ fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             for (int i = 0; i < TN / 4; ++i) packed[i] = pack_bf16x2(accf[2 * i], accf[2 * i + 1]);
             }
             if (!ok) break;
-            epilogue_store<TN, false>(tp, &tmD, q, h, lane, tile.row0, tile.row_end, tile.n0, ebase, epi_chunk, packed);
+            epilogue_store<TN, false, 2>(tp, &tmD, q, h, lane, tile.row0, tile.row_end, tile.n0, ebase, epi_chunk, packed);
         }
         if (BROW) cp_async_wait0();                   // no copy into this warp's slot outlives the CTA
         if (lane == 0) bulk_wait_group_all();
@@ -1643,7 +1680,7 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
     const int64_t sb_bytes = (GROUPED ? a.G : 1) * sb_group_bytes;
     CUtensorMap tmA, tmB, tmSA, tmSB, tmD;
     if (!make_map(&tmA, a.a, k_bytes, a.M, 128)) return cudaErrorInvalidValue;
-    if (!make_map(&tmB, a.b, k_bytes, GROUPED ? a.G * a.N : a.N, TN / 2)) return cudaErrorInvalidValue;
+    if (!make_map(&tmB, a.b, k_bytes, GROUPED ? a.G * a.N : a.N, (uint32_t)C::B_BOX)) return cudaErrorInvalidValue;
     if (!make_sf_map(&tmSA, a.sa, sa_bytes, (uint32_t)C::SF_ATOMS_A)) return cudaErrorInvalidValue;
     if (!make_sf_map(&tmSB, a.sb, sb_bytes, (uint32_t)C::SF_ATOMS_A)) return cudaErrorInvalidValue;   // one band per load
     if (!make_out_map(&tmD, a.d, a.M, a.N, a.ldd, (uint32_t)EPI_COLS)) return cudaErrorInvalidValue;
@@ -1800,6 +1837,19 @@ bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const voi
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Dense MXFP8 tile width.  A 256 x 384 tile loads 16 % fewer operand bytes per MMA than a 256 x 256
+// one (each A row serves 384 columns instead of 256) and measured 3-5 % faster per tile column on the
+// Qwen3-8B MLP shapes, but it wastes the padding of a ragged last column tile and fills the CTA pairs
+// in coarser waves.  Estimate each width's time as (waves of tiles over the pairs) x (tile width),
+// with the wide tile's rate 4 % better, and take the smaller: FPROP 8192 x 12288 x 4096 and WGRAD
+// 12288 x 4096 x 8192 take 384 columns, DGRAD 8192 x 4096 x 12288 and small GEMMs 256.
+static bool wide_mxfp8_tiles(const GemmArgs& a, int num_sms) {
+    const int64_t pairs = max64(1, num_sms / 2);
+    const int64_t m_tiles = (a.M + 2 * BM - 1) / (2 * BM);
+    auto waves = [&](int64_t tn) { return (m_tiles * ((a.N + tn - 1) / tn) + pairs - 1) / pairs; };
+    return waves(384) * 384 * 96 < waves(256) * 256 * 100;
+}
+
 cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream) {
     if (args.G > MAX_GROUPS) return cudaErrorInvalidValue;
     const bool col_alpha = args.G == 0 && args.alpha_b_scope == 2;   // per-output-column factor (dense only)
@@ -1809,6 +1859,7 @@ cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t s
     // against 0.132 ms (NVFP4; MXFP8 likewise)
     if (args.fmt == 0) {
         if (args.G > 0) return launch_pair_impl<0, true, false, 256>(args, num_sms, stream);
+        if (!col_alpha && wide_mxfp8_tiles(args, num_sms)) return launch_pair_impl<0, false, false, 384>(args, num_sms, stream);
         return col_alpha ? launch_pair_impl<0, false, true, 256>(args, num_sms, stream)
                          : launch_pair_impl<0, false, false, 256>(args, num_sms, stream);
     }

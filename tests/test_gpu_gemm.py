@@ -54,11 +54,14 @@ def run_mxfp8(mx, orc, a, b, M, N, K):
     return d, A @ B.T, np.abs(A) @ np.abs(B).T
 
 
-# the last two give every CTA pair several tiles (more than the 76 pairs of the GPU run at once), so the
-# accumulator slots rotate and their barriers wrap; one with K beyond the 6-stage ring and a ragged N,
-# one with a single K stage
+# (4096, 4000, 1024) and (2304, 4096, 128) give every CTA pair several tiles (more than the 76 pairs of
+# the GPU run at once), so the accumulator slots rotate and their barriers wrap; one with K beyond the
+# 6-stage ring and a ragged N, one with a single K stage.  The last two are wide enough for the
+# 256 x 384 tiles (two MMAs per K step, B rows in three 64-row boxes): several tiles per pair, K beyond
+# that ring's 5 stages, and a ragged M with a ragged last column tile (12280 = 31 x 384 + 376)
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (128, 256, 512), (256, 512, 1024), (200, 296, 384),
-                                   (1, 8, 128), (640, 1280, 2048), (4096, 4000, 1024), (2304, 4096, 128)])
+                                   (1, 8, 128), (640, 1280, 2048), (4096, 4000, 1024), (2304, 4096, 128),
+                                   (2304, 12288, 1024), (2000, 12280, 384)])
 def test_mxfp8_gemm(mx, orc, M, N, K):
     a = synthetic.random_bf16(M + K, (M, K), "student_t")
     b = synthetic.random_bf16(N + K + 1, (N, K), "normal", 0.02)
@@ -73,9 +76,10 @@ def test_mxfp8_gemm_tiny_config(mx, orc):
     check_close(orc, d, ref, absprod)
 
 
-def test_mxfp8_gemm_integer_exact(mx, orc):
+# the second shape runs on the 256 x 384 tiles
+@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (2304, 12288, 256)])
+def test_mxfp8_gemm_integer_exact(mx, orc, M, N, K):
     rng = np.random.default_rng(0)
-    M, N, K = 256, 512, 256
     ia = rng.integers(-8, 9, size=(M, K))
     ib = rng.integers(-8, 9, size=(N, K))
     enc = np.array([orc.e4m3_encode(float(v)) for v in range(-8, 9)], dtype=np.uint8)
@@ -85,7 +89,8 @@ def test_mxfp8_gemm_integer_exact(mx, orc):
     d = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
     mx.mx_scaled_gemm(mx.MX_FMT_MXFP8, dev_u8(qa), dev_u8(orc.scales_to_gemm_layout(sa)), None, 0,
                       dev_u8(qb), dev_u8(orc.scales_to_gemm_layout(sb)), None, 0, M, N, K, d)
-    ref = torch.from_numpy((ia @ ib.T).astype(np.float32)).to(torch.bfloat16)
+    # integer products summed exactly (|sum| <= 64 K < 2^24) in FP64, then rounded once to BF16
+    ref = torch.from_numpy((ia.astype(np.float64) @ ib.T.astype(np.float64)).astype(np.float32)).to(torch.bfloat16)
     got = d.cpu()
     assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), first_mismatch(got.float().numpy(), ref.float().numpy())
 
