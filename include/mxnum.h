@@ -281,7 +281,7 @@ mx_status mx_dequantize_bf16(mx_format fmt, const uint8_t* q, const uint8_t* s, 
  * TMA tensor stores, whose row pitch is a multiple of 16 bytes), ldd >= N; a, b, sa, sb, d 16-byte
  * aligned.  Runs as persistent clusters of two CTAs (one per SM) on 256 x 256 output tiles; large
  * dense MXFP8 GEMMs without a per-column alpha_b take 256 x 384 tiles where the tile count fills the
- * GPU's CTA pairs at least as evenly (the result does not depend on the tile width). */
+ * GPU's CTA pairs at least as evenly. */
 mx_status mx_scaled_gemm(mx_format fmt,
                          const uint8_t* a, const uint8_t* sa, const float* alpha_a, mx_scope alpha_a_scope,
                          const uint8_t* b, const uint8_t* sb, const float* alpha_b, mx_scope alpha_b_scope,
