@@ -111,6 +111,8 @@ __device__ __forceinline__ void bulk_signal_copy(uint32_t dst_cluster, uint32_t 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read_n() { asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory"); }
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -184,7 +186,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
 // ---------------------------------------------------------------------------------------------
 // Epilogue geometry: 8 warps, two per TMEM lane quadrant; warp (q, h) owns rows [32 q, 32 q + 32) of
 // the CTA's 128 and columns [TN/2 h, TN/2 (h + 1)) of the tile.  Stores go out in 32-row x 16-column
-// chunks (32-byte rows, 32-byte swizzle) through two 1 KB staging buffers per warp.
+// chunks (32-byte rows, 32-byte swizzle) through two 1 KB staging buffers per warp, or for short-K
+// NVFP4 GEMMs in 32 x 64 chunks (128-byte rows, 128-byte swizzle) through one 4 KB buffer per warp.
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_COLS = 16;
 constexpr int EPI_BUF_BYTES = 32 * 2 * EPI_COLS;
@@ -240,7 +243,7 @@ __device__ __forceinline__ void epilogue_drain(const Params& p, uint32_t tacc, i
 // Stores of one drained tile slice: rows [row0 + 32 q, +32) that belong to the tile, columns of the
 // warp's half.  TMA stores from the warp's two staging buffers at ebase, or plain 16-byte stores for
 // a slice that straddles the end of an expert group.
-template <int TN, bool GROUPED, int NBUF>
+template <int TN, bool GROUPED, int NBUF, int ECOLS>
 __device__ __forceinline__ void epilogue_store(const Params& p, const CUtensorMap* tmD, int q, int h, int lane,
                                                int64_t row0, int64_t row_end, int64_t n0, uint32_t ebase,
                                                uint32_t& epi_chunk, const uint32_t (&packed)[TN / 4]) {
@@ -252,24 +255,25 @@ __device__ __forceinline__ void epilogue_store(const Params& p, const CUtensorMa
     if (wrow0 >= row_end) return;
     if (!GROUPED || wrow0 + 32 <= row_end) {
         // TMA stores; the tensor map clips rows >= M and columns >= N
-        const uint32_t rbase_off = (uint32_t)(lane * 2 * EPI_COLS);
+        constexpr uint32_t BUF_BYTES = 32u * 2u * ECOLS;
+        const uint32_t rbase_off = (uint32_t)(lane * 2 * ECOLS);
 #pragma unroll
-        for (int c = 0; c < EPI_HALF / EPI_COLS; ++c) {
-            const int64_t col0 = nh + c * EPI_COLS;
+        for (int c = 0; c < EPI_HALF / ECOLS; ++c) {
+            const int64_t col0 = nh + c * ECOLS;
             if (col0 < p.N) {
-                const uint32_t buf = ebase + (NBUF == 2 ? (epi_chunk & 1u) * (uint32_t)EPI_BUF_BYTES : 0u);
+                const uint32_t buf = ebase + (epi_chunk % (uint32_t)NBUF) * BUF_BYTES;
                 ++epi_chunk;
                 // the store issued from this buffer NBUF chunks ago must have read it
-                if (lane == 0) {
-                    if (NBUF == 2) bulk_wait_group_read1();
-                    else bulk_wait_group_read0();
-                }
+                if (lane == 0) bulk_wait_group_read_n<NBUF - 1>();
                 __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    // 16-byte piece j of this row at its position under the 32-byte swizzle
-                    const uint32_t phys = (uint32_t)j ^ ((uint32_t)(lane >> 2) & 1u);
-                    const int pk = c * (EPI_COLS / 2) + 4 * j;
+                for (int j = 0; j < ECOLS / 8; ++j) {
+                    // 16-byte piece j of this row at its position under the 32- or 64-byte swizzle
+                    // (the piece index XORed with address bit 7, or bits 7-8)
+                    const uint32_t phys = ECOLS == 16 ? (uint32_t)j ^ ((uint32_t)(lane >> 2) & 1u)
+                                        : ECOLS == 32 ? (uint32_t)j ^ ((uint32_t)(lane >> 1) & 3u)
+                                                      : (uint32_t)j ^ ((uint32_t)lane & 7u);
+                    const int pk = c * (ECOLS / 2) + 4 * j;
                     st_shared_v4(buf + rbase_off + 16u * phys, packed[pk], packed[pk + 1], packed[pk + 2], packed[pk + 3]);
                 }
                 fence_proxy_async_smem();
@@ -314,7 +318,7 @@ __device__ __forceinline__ void epilogue_store(const Params& p, const CUtensorMa
 //              commits arrive on the barriers of both CTAs
 //   both CTAs  warps 2..9: epilogue of this CTA's 128 rows; TMEM release arrives in the leader
 // ---------------------------------------------------------------------------------------------
-template <int FMT, bool GROUPED, int TN>
+template <int FMT, bool GROUPED, int TN, int EV = 0>
 struct PairCfg {
     static_assert(TN == 128 || TN == 256 || TN == 384, "tile width");
     static_assert(TN != 384 || (FMT == 0 && !GROUPED), "384-column tiles: dense MXFP8 only");
@@ -327,7 +331,11 @@ struct PairCfg {
     // the N = 256 MMA, 64 for the N = 128 MMA), the other widths one box of TN / 2 rows
     static constexpr int B_BOX = TN == 384 ? 64 : TN / 2;
     // epilogue staging buffers per warp (one for 384-column tiles, so that a fifth stage fits)
-    static constexpr int EPI_NBUF = TN == 384 ? 1 : 2;
+    // epilogue stores: EV = 0, 32-row x 16-column chunks through two 1 KB buffers per warp; EV = 3,
+    // 32 x 64 chunks (128-byte rows, 128-byte swizzle) through one 4 KB buffer per warp
+    static constexpr int EPI_NBUF = TN == 384 ? 1 : (EV == 3 ? 1 : 2);
+    static constexpr int EPI_C = EV == 3 ? 64 : EPI_COLS;   // columns per staged store
+    static constexpr int EPI_BUF = 32 * 2 * EPI_C;
     static constexpr int SF_ATOMS_A = FMT == 0 ? 1 : 4;
     static constexpr int SFB_BANDS = TN / 128;
     static constexpr int SFA_BYTES = 512 * SF_ATOMS_A;     // this CTA's 128 rows
@@ -343,12 +351,17 @@ struct PairCfg {
     static constexpr int SMEM_SFA = SMEM_B + NST * B_BYTES;
     static constexpr int SMEM_SFB = SMEM_SFA + NST * SFA_BYTES;
     static constexpr int SMEM_EPI = (SMEM_SFB + NST * SFB_BYTES + 1023) / 1024 * 1024;
-    static constexpr int SMEM_BAR = SMEM_EPI + EPI_WARPS * EPI_NBUF * EPI_BUF_BYTES;
+    static constexpr int SMEM_BAR = SMEM_EPI + EPI_WARPS * EPI_NBUF * EPI_BUF;
     static constexpr int SMEM_MISC = SMEM_BAR + 8 * (2 * NST + 7);
     static constexpr int SMEM_SIGNAL = (SMEM_MISC + 16 + 15) / 16 * 16;   // 16-byte signal source / target
     static constexpr int SMEM_TABLES = SMEM_SIGNAL + 16;   // grouped: row offsets, pair-tile and band prefixes
-    static constexpr int SMEM_TOTAL = SMEM_TABLES + (GROUPED ? 8 * (MAX_GROUPS + 1) + 4 * (2 * (MAX_GROUPS + 1) + 32) : 0);
-    static constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;
+    // grouped: the tables hold G + 1 entries each, so the launch sizes them by G (table_bytes)
+    static constexpr int table_bytes(int64_t G) { return GROUPED ? (int)(8 * (G + 1) + 4 * (2 * (G + 1) + 32)) : 0; }
+    static constexpr int smem_alloc(int64_t G) { return SMEM_TABLES + table_bytes(G) + 1024; }
+    static constexpr int SMEM_LIMIT = 227 * 1024;
+    // the most groups whose tables fit (all of MX_MAX_GROUPS with the narrow staging)
+    static constexpr int64_t MAX_G = GROUPED ? (SMEM_LIMIT - 1024 - SMEM_TABLES - 4 * 32 - 8 - 8) / 16 : 0;
+    static constexpr int SMEM_ALLOC = smem_alloc(GROUPED ? 1 : 0);
     static_assert(SMEM_B % 1024 == 0 && SMEM_EPI % 1024 == 0, "operand and staging alignment");
     static_assert(TMEM_SF + NST * (SFA_COLS + SFB_COLS) <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
@@ -397,12 +410,12 @@ __device__ __forceinline__ PairTile pair_grouped_tile(const Params& p, const int
     return r;
 }
 
-template <int FMT, bool GROUPED, bool COL_ALPHA, int TN>
+template <int FMT, bool GROUPED, bool COL_ALPHA, int TN, int EV>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                     const __grid_constant__ CUtensorMap tmD, const Params p) {
-    using C = PairCfg<FMT, GROUPED, TN>;
+    using C = PairCfg<FMT, GROUPED, TN, EV>;
     constexpr int NST = C::NST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -416,9 +429,9 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
     int64_t* s_off = reinterpret_cast<int64_t*>(smem + C::SMEM_TABLES);
-    int* ptile2 = reinterpret_cast<int*>(s_off + (MAX_GROUPS + 1));
-    int* pband = ptile2 + (MAX_GROUPS + 1);
-    int* s_warp = pband + (MAX_GROUPS + 1);
+    int* ptile2 = reinterpret_cast<int*>(s_off + (p.G + 1));
+    int* pband = ptile2 + (p.G + 1);
+    int* s_warp = pband + (p.G + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -612,7 +625,7 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int q = warp & 3;                     // TMEM lane quadrant this warp may access
         const int h = (warp - 2) >> 2;              // column half
         const uint32_t tempty_mine = leader ? bar_tempty : bar_tempty_odd;
-        const uint32_t ebase = sbase + C::SMEM_EPI + (uint32_t)((warp - 2) * C::EPI_NBUF * EPI_BUF_BYTES);
+        const uint32_t ebase = sbase + C::SMEM_EPI + (uint32_t)((warp - 2) * C::EPI_NBUF * C::EPI_BUF);
         uint32_t epi_chunk = 0;
         // tile coordinates and row scales of the next tile are fetched while this tile's stores run
         PairTile tile{};
@@ -638,7 +651,7 @@ bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int64_t row = tile.row0 + q * 32 + lane;
                 epilogue_alphas<GROUPED>(p, row, row < tile.row_end, tile.g, aa, ab_g);
             }
-            epilogue_store<TN, GROUPED, C::EPI_NBUF>(p, &tmD, q, h, lane, cur.row0, cur.row_end, cur.n0, ebase, epi_chunk, packed);
+            epilogue_store<TN, GROUPED, C::EPI_NBUF, C::EPI_C>(p, &tmD, q, h, lane, cur.row0, cur.row_end, cur.n0, ebase, epi_chunk, packed);
         }
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
@@ -1554,7 +1567,7 @@ fp8bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             for (int i = 0; i < TN / 4; ++i) packed[i] = pack_bf16x2(accf[2 * i], accf[2 * i + 1]);
             }
             if (!ok) break;
-            epilogue_store<TN, false, 2>(tp, &tmD, q, h, lane, tile.row0, tile.row_end, tile.n0, ebase, epi_chunk, packed);
+            epilogue_store<TN, false, 2, EPI_COLS>(tp, &tmD, q, h, lane, tile.row0, tile.row_end, tile.n0, ebase, epi_chunk, packed);
         }
         if (BROW) cp_async_wait0();                   // no copy into this warp's slot outlives the CTA
         if (lane == 0) bulk_wait_group_all();
@@ -1634,7 +1647,8 @@ bool make_map(CUtensorMap* map, const uint8_t* base, int64_t k_bytes, int64_t ro
 // Output map: BF16 [rows, N] with row pitch ldd, box of `box_cols` x 32 rows, swizzled to match the
 // epilogue's staging layout.
 bool make_out_map(CUtensorMap* map, uint16_t* d, int64_t rows, int64_t N, int64_t ldd, uint32_t box_cols) {
-    const CUtensorMapSwizzle sw = box_cols * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    const CUtensorMapSwizzle sw = box_cols * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : box_cols * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
     return encode_tensor_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, d, (uint64_t)N, (uint64_t)rows, (uint64_t)(ldd * 2),
                                 box_cols, 32, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
@@ -1645,19 +1659,21 @@ bool make_sf_map(CUtensorMap* map, const uint8_t* base, int64_t bytes, uint32_t 
                                 2 * atoms, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
-template <int FMT, bool GROUPED, bool COL_ALPHA, int TN>
+template <int FMT, bool GROUPED, bool COL_ALPHA, int TN, int EV = 0>
 cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream) {
-    using C = PairCfg<FMT, GROUPED, TN>;
+    using C = PairCfg<FMT, GROUPED, TN, EV>;
     static PerDevice setup;                 // attributes, and the CTA pairs that fit on the GPU at once
     int resident_pairs = 0;
     const cudaError_t attr_err = per_device_once(setup, resident_pairs, [num_sms](int& rp) -> cudaError_t {
-        auto kern = bs_gemm_pair_kernel<FMT, GROUPED, COL_ALPHA, TN>;
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        auto kern = bs_gemm_pair_kernel<FMT, GROUPED, COL_ALPHA, TN, EV>;
+        // grouped launches size their tables by G: allow up to the per-block limit
+        const int max_alloc = GROUPED ? C::SMEM_LIMIT : C::SMEM_ALLOC;
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_alloc);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(num_sms & ~1));
         cfg.blockDim = dim3(NUM_THREADS);
-        cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+        cfg.dynamicSmemBytes = max_alloc;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2; attr[0].val.clusterDim.y = 1; attr[0].val.clusterDim.z = 1;
@@ -1683,7 +1699,7 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
     if (!make_map(&tmB, a.b, k_bytes, GROUPED ? a.G * a.N : a.N, (uint32_t)C::B_BOX)) return cudaErrorInvalidValue;
     if (!make_sf_map(&tmSA, a.sa, sa_bytes, (uint32_t)C::SF_ATOMS_A)) return cudaErrorInvalidValue;
     if (!make_sf_map(&tmSB, a.sb, sb_bytes, (uint32_t)C::SF_ATOMS_A)) return cudaErrorInvalidValue;   // one band per load
-    if (!make_out_map(&tmD, a.d, a.M, a.N, a.ldd, (uint32_t)EPI_COLS)) return cudaErrorInvalidValue;
+    if (!make_out_map(&tmD, a.d, a.M, a.N, a.ldd, (uint32_t)C::EPI_C)) return cudaErrorInvalidValue;
 
     Params p{};
     p.sa = a.sa; p.sb = a.sb;
@@ -1701,7 +1717,8 @@ cudaError_t launch_pair_impl(const GemmArgs& a, int num_sms, cudaStream_t stream
     // a persistent grid: only as many pairs as can be resident together (an odd SM left in a GPC
     // cannot host half a cluster)
     const int64_t pairs = max64(1, min64(tiles_bound, (int64_t)min(resident_pairs, num_sms / 2)));
-    bs_gemm_pair_kernel<FMT, GROUPED, COL_ALPHA, TN><<<(unsigned)(2 * pairs), NUM_THREADS, C::SMEM_ALLOC, stream>>>(
+    if (GROUPED && a.G > C::MAX_G) return cudaErrorInvalidValue;
+    bs_gemm_pair_kernel<FMT, GROUPED, COL_ALPHA, TN, EV><<<(unsigned)(2 * pairs), NUM_THREADS, C::smem_alloc(a.G), stream>>>(
         tmA, tmB, tmSA, tmSB, tmD, p);
     return cudaGetLastError();
 }
@@ -1863,7 +1880,17 @@ cudaError_t launch_scaled_gemm(const GemmArgs& args, int num_sms, cudaStream_t s
         return col_alpha ? launch_pair_impl<0, false, true, 256>(args, num_sms, stream)
                          : launch_pair_impl<0, false, false, 256>(args, num_sms, stream);
     }
-    if (args.G > 0) return launch_pair_impl<1, true, false, 256>(args, num_sms, stream);
+    // NVFP4 with at most three K stages per tile: the output write dominates, and 64-column staged stores
+    // (whole 128-byte lines) beat 16-column ones (K = 768 grouped down 108.6 -> 93.4 us; K = 256 / 768
+    // dense 72.5 / 78.0 -> 55.7 / 66.6 us for 65536 x 2048 outputs).  With longer K their single staging
+    // buffer per warp makes the drain the slower side (K = 2048 grouped 115 -> 122 us), so those keep
+    // the 16-column double-buffered stores
+    const bool short_k = args.K / 2 / BKB <= 3;
+    if (args.G > 0) {
+        if (short_k && args.G <= PairCfg<1, true, 256, 3>::MAX_G) return launch_pair_impl<1, true, false, 256, 3>(args, num_sms, stream);
+        return launch_pair_impl<1, true, false, 256>(args, num_sms, stream);
+    }
+    if (short_k && !col_alpha) return launch_pair_impl<1, false, false, 256, 3>(args, num_sms, stream);
     return col_alpha ? launch_pair_impl<1, false, true, 256>(args, num_sms, stream)
                      : launch_pair_impl<1, false, false, 256>(args, num_sms, stream);
 }

@@ -115,7 +115,11 @@ def test_mxfp8_gemm_rejects_wrong_scale_layout(mx, orc):
 # ------------------------------------------------------------------------------------------------
 # NVFP4
 # ------------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 1024), (200, 296, 512), (640, 768, 2048)])
+# K <= 768 (at most three K stages) writes through 32 x 64-column staged stores, longer K through
+# 32 x 16-column ones; the last shape gives every CTA pair several tiles with a ragged M and a ragged
+# last 64-column store (4040 = 63 x 64 + 8)
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 1024), (200, 296, 512), (640, 768, 2048),
+                                   (2000, 4040, 768)])
 def test_nvfp4_gemm_per_token_times_per_tensor(mx, orc, M, N, K):
     a = synthetic.random_bf16(M * 3 + K, (M, K), "student_t")
     b = synthetic.random_bf16(N * 3 + K, (N, K), "normal", 0.02)
