@@ -305,9 +305,9 @@ nvfp4_1x16_flat_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, con
 // Column-wise 1x16 along tokens with a per-tensor scale.  CTA tile: 128 tokens x (32 CPT) columns;
 // warp w owns tokens [16w, 16w + 16), lane l owns columns [CPT l, CPT l + CPT) (CPT = 8 with
 // stochastic rounding, whose Philox block spans 8 columns; 4 otherwise, which halves the registers
-// a thread holds and doubles the resident warps).  Each column's 16 codes (8 bytes) are stored
-// straight from registers into the transposed output (the 8 warps fill 64 contiguous bytes per
-// column, merged in L2); block scales are staged in shared memory and written as words.
+// a thread holds and doubles the resident warps).  Each column's 16 codes per warp (8 bytes) are
+// staged in shared memory, so that the CTA writes each column's 64 bytes (128 tokens) as whole
+// 32-byte sectors; the block scales of a full tile go out as whole 16-byte lines of the scale atoms.
 // ------------------------------------------------------------------------------------------------
 constexpr int CW_TOK = CW_TILE_TOKENS;
 constexpr int CW_THREADS = 256;
@@ -412,6 +412,9 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
     static_assert(!SR || CPT == 8, "one Philox block covers 8 columns");
     constexpr int COLS = 32 * CPT;
     __shared__ uint8_t ss[CW_TOK / 16][COLS];                         // block scales: [token block][column]
+    // transposed codes: 64 bytes per column, warp w's 8-byte slice in slot w ^ ((column / CPT) & 7), so
+    // that the 32 slices one warp stores at a time spread over 8 bank groups
+    __shared__ __align__(16) uint8_t qs[COLS * 64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tb0 = (int64_t)blockIdx.y * CW_TOK;
     const int64_t cb0 = (int64_t)blockIdx.x * COLS;
@@ -448,9 +451,9 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
                 float p[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) p[i] = __fmul_rn(h ? bf16_hi(xw[i][jp]) : bf16_lo(xw[i][jp]), rcp[j]);
-                // the 16 tokens of column n0 + j: 8 bytes, stored straight to the transposed output
-                if (valid) __stcs(reinterpret_cast<uint2*>(q + (n0 + j) * (T / 2) + t0 / 2),
-                                  make_uint2(cvt_e2m1x8(p), cvt_e2m1x8(p + 8)));
+                // the 16 tokens of column n0 + j: 8 bytes of the transposed output
+                *reinterpret_cast<uint2*>(qs + (lane * CPT + j) * 64 + 8 * (warp ^ (lane & 7))) =
+                    make_uint2(cvt_e2m1x8(p), cvt_e2m1x8(p + 8));
             }
         }
     }
@@ -472,17 +475,53 @@ colwise_quant_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t N, uint3
                              code[2 * jp][i >> 3], i & 7, code[2 * jp + 1][i >> 3], i & 7);
             }
         }
-        if (valid) {
 #pragma unroll
-            for (int j = 0; j < CPT; ++j)
-                __stcs(reinterpret_cast<uint2*>(q + (n0 + j) * (T / 2) + t0 / 2), make_uint2(code[j][0], code[j][1]));
-        }
+        for (int j = 0; j < CPT; ++j)
+            *reinterpret_cast<uint2*>(qs + (lane * CPT + j) * 64 + 8 * (warp ^ (lane & 7))) = make_uint2(code[j][0], code[j][1]);
     }
     __syncthreads();
 
-    // scales: column col gets the 8 block scales of this CTA's 128 tokens (two words of the layout)
     const int64_t ntok = min64(CW_TOK, T - tb0);      // multiple of 16
+    const int nslot = (int)(ntok / 16);               // 8-byte slices (warps) holding tokens
+    // codes: lane 4 c + k writes the 16 bytes of chunk k (tokens tb0 + 32 k .. + 31) of column c
+    {
+        const bool vec16 = (T / 2) % 16 == 0;
+        for (int idx = threadIdx.x; idx < COLS * 4; idx += CW_THREADS) {
+            const int c = idx >> 2, k = idx & 3;
+            const int64_t n = cb0 + c;
+            if (n >= N || 2 * k >= nslot) continue;
+            // logical slices 2k, 2k + 1 sit in 16-byte chunk k ^ (m >> 1), swapped when m is odd
+            const int m = (c / CPT) & 7;
+            uint4 v = *reinterpret_cast<const uint4*>(qs + c * 64 + 16 * (k ^ (m >> 1)));
+            if (m & 1) v = make_uint4(v.z, v.w, v.x, v.y);
+            uint8_t* dst = q + n * (T / 2) + tb0 / 2 + 16 * k;
+            if (vec16 && 2 * k + 1 < nslot) {
+                __stcs(reinterpret_cast<uint4*>(dst), v);
+            } else {
+                __stcs(reinterpret_cast<uint2*>(dst), make_uint2(v.x, v.y));
+                if (2 * k + 1 < nslot) __stcs(reinterpret_cast<uint2*>(dst + 8), make_uint2(v.z, v.w));
+            }
+        }
+    }
     const int64_t nct = sf_col_tiles(T, 16);
+    if (ntok == CW_TOK && cb0 + COLS <= N) {
+        // a full tile's scales are whole 512-byte atoms (128 columns x 4 token blocks): thread i writes
+        // line l = i & 31 (columns l, l + 32, l + 64, l + 96 of the atom) of token group (i >> 5) & 1
+        for (int idx = threadIdx.x; idx < COLS / 2; idx += CW_THREADS) {
+            const int l = idx & 31, grp = (idx >> 5) & 1, an = idx >> 6;
+            uint32_t wq[4];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const int col = 128 * an + l + 32 * qq;
+                wq[qq] = (uint32_t)ss[4 * grp][col] | ((uint32_t)ss[4 * grp + 1][col] << 8) |
+                         ((uint32_t)ss[4 * grp + 2][col] << 16) | ((uint32_t)ss[4 * grp + 3][col] << 24);
+            }
+            uint8_t* p = s + sf_offset(cb0 + 128 * an, tb0 / 16 + 4 * grp, nct) + 16 * l;
+            *reinterpret_cast<uint4*>(p) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        }
+        return;
+    }
+    // scales: column col gets the 8 block scales of this CTA's 128 tokens (two words of the layout)
     for (int idx = threadIdx.x; idx < COLS * 2; idx += CW_THREADS) {
         const int col = idx >> 1, half = idx & 1;
         const int64_t n = cb0 + col;
@@ -585,13 +624,14 @@ matrix_amax_kernel(const uint16_t* __restrict__ w, int64_t per_matrix, uint32_t*
 
 // The work of one lane on its quarter of a 16x16 tile: rows 2 i + rpar (i = 0..7) x the 8 columns of
 // xr, the tile's other quarters in lanes l ^ 1, l ^ 16, l ^ 17; rS = nvfp4_fast_rs(S).  Writes this
-// lane's row-wise codes (rows o0 + 2 i + rpar at column h) and its half of the transposed codes, and
-// returns the tile's scale code.  All 32 lanes of the warp take part (shuffles); `store` gates the
-// global writes only.
+// lane's row-wise codes (rows o0 + 2 i + rpar at column h), stages its half of the transposed codes
+// (8 bytes = the warp's 16 rows of each of 4 columns) at scol_w + 32 c for tile column c, and returns
+// the tile's scale code.  All 32 lanes of the warp take part (shuffles); `store` gates the global
+// writes only.
 template <bool FOUR_SIX>
 __device__ __forceinline__ uint32_t w2d_lane_tile(const uint4 (&xr)[8], float S, float rS, int rpar, bool store,
-                                                  uint8_t* __restrict__ qrow_g, uint8_t* __restrict__ qcol_g,
-                                                  int64_t O, int64_t H, int64_t o0, int64_t h) {
+                                                  uint8_t* __restrict__ qrow_g, uint8_t* scol_w,
+                                                  int64_t O, int64_t H, int64_t o0, int64_t h, int chunk) {
     uint32_t m2 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -675,10 +715,8 @@ __device__ __forceinline__ uint32_t w2d_lane_tile(const uint4 (&xr)[8], float S,
         col[3][half] = __byte_perm(o01, o23, 0x7632u);
     }
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-        const int64_t hc = h + jj + 4 * rpar;
-        if (store) __stcs(reinterpret_cast<uint2*>(qcol_g + hc * (O / 2) + o0 / 2), make_uint2(col[jj][0], col[jj][1]));
-    }
+    for (int jj = 0; jj < 4; ++jj)
+        *reinterpret_cast<uint2*>(scol_w + 32 * (chunk * 8 + jj + 4 * rpar)) = make_uint2(col[jj][0], col[jj][1]);
     return bs;
 }
 
@@ -708,6 +746,9 @@ weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, cons
                       uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
                       uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, float* __restrict__ s_w) {
     __shared__ uint8_t st[W2_ROWS / 16][W2_COLS / 16];                 // tile scales
+    // transposed codes of the CTA's 64 rows for each of its 128 columns (32 bytes per column, the
+    // 8-byte slice of warp w at byte 8 w), written out as whole 32-byte runs
+    __shared__ __align__(16) uint8_t scol[W2_COLS * 32];
     // matrices in the reverse of the amax pass's order: the first CTAs find the matrices that pass
     // read last still in L2
     const int64_t g = gridDim.z - 1 - blockIdx.z;
@@ -727,19 +768,71 @@ weight2d_quant_kernel(const uint16_t* __restrict__ w, int64_t O, int64_t H, cons
         const int64_t o = o0 + 2 * i + rpar;
         xr[i] = valid ? __ldcs(reinterpret_cast<const uint4*>(wg + o * H + h)) : make_uint4(0u, 0u, 0u, 0u);
     }
-    const uint32_t bs = w2d_lane_tile<FOUR_SIX>(xr, S, nvfp4_fast_rs(S), rpar, valid, q_row + g * O * (H / 2), q_col + g * H * (O / 2),
-                                                O, H, o0, h);
+    const uint32_t bs = w2d_lane_tile<FOUR_SIX>(xr, S, nvfp4_fast_rs(S), rpar, valid, q_row + g * O * (H / 2),
+                                                scol + 8 * warp, O, H, o0, h, chunk);
     if (lane < 16 && (lane & 1) == 0) st[warp][lane >> 1] = (uint8_t)bs;
     __syncthreads();
 
-    w2d_row_scales(st[warp], s_row + g * host_scale_bytes_dev(O, H, 16), O, H, o0, h0, lane);
     const int64_t ob = (int64_t)blockIdx.y * W2_ROWS;
     const int64_t nrows = min64(W2_ROWS, O - ob);      // multiple of 16
+    const bool full = nrows == W2_ROWS && h0 + W2_COLS <= H;
+    // transposed codes: thread t writes 16 bytes (rows ob + 32 half .. + 31) of column (t >> 1) + 64 k;
+    // lanes 2c and 2c + 1 fill one 32-byte sector
+    {
+        uint8_t* qc = q_col + g * H * (O / 2);
+        const int half = threadIdx.x & 1;
+        const int nslot = (int)(nrows / 16);            // 8-byte slices present
+        const bool vec16 = (O / 2) % 16 == 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int c = (threadIdx.x >> 1) + 64 * k;
+            const int64_t hc = h0 + c;
+            if (hc >= H) continue;
+            uint8_t* dst = qc + hc * (O / 2) + ob / 2 + 16 * half;
+            const uint2 lo = *reinterpret_cast<const uint2*>(scol + 32 * c + 16 * half);
+            const uint2 hi = *reinterpret_cast<const uint2*>(scol + 32 * c + 16 * half + 8);
+            if (vec16 && 2 * half + 1 < nslot) {
+                __stcs(reinterpret_cast<uint4*>(dst), make_uint4(lo.x, lo.y, hi.x, hi.y));
+            } else {
+                if (2 * half < nslot) __stcs(reinterpret_cast<uint2*>(dst), lo);
+                if (2 * half + 1 < nslot) __stcs(reinterpret_cast<uint2*>(dst + 8), hi);
+            }
+        }
+    }
+    const int64_t nct_col = sf_col_tiles(O, 16);
+    uint8_t* sbase = s_col + g * host_scale_bytes_dev(H, O, 16);
+    if (full) {
+        // row-wise scales: thread t < 64 writes rows ob + l and ob + l + 32 (l = t & 31) of scale columns
+        // h0 / 16 + 4 (t >> 5) .. + 3, 8 adjacent bytes of the scale atom
+        if (threadIdx.x < 64) {
+            const int l = threadIdx.x & 31, grp = threadIdx.x >> 5;
+            const int64_t nct = sf_col_tiles(H, 16);
+            auto word = [&](int r) {
+                const uint8_t* t4 = &st[r >> 4][4 * grp];
+                return (uint32_t)t4[0] | ((uint32_t)t4[1] << 8) | ((uint32_t)t4[2] << 16) | ((uint32_t)t4[3] << 24);
+            };
+            uint8_t* p = s_row + g * host_scale_bytes_dev(O, H, 16) + sf_offset(ob + l, h0 / 16 + 4 * grp, nct);
+            *reinterpret_cast<uint2*>(p) = make_uint2(word(l), word(l + 32));
+        } else if (threadIdx.x >= 96) {
+            // column-wise scales: the CTA's 128 columns x 4 row tiles are one whole 512-byte scale atom;
+            // lane t writes its 16-byte line (columns t, t + 32, t + 64, t + 96)
+            const int t = threadIdx.x - 96;
+            uint32_t wq[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int jt = (t + 32 * q) >> 4;
+                wq[q] = (uint32_t)st[0][jt] | ((uint32_t)st[1][jt] << 8) | ((uint32_t)st[2][jt] << 16) | ((uint32_t)st[3][jt] << 24);
+            }
+            uint8_t* p = sbase + sf_offset(h0, ob / 16, nct_col) + 16 * t;
+            *reinterpret_cast<uint4*>(p) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        }
+        return;
+    }
+    w2d_row_scales(st[warp], s_row + g * host_scale_bytes_dev(O, H, 16), O, H, o0, h0, lane);
     // column-wise scales: row hc, scale columns ob/16 .. +3 (one word when all 4 row tiles exist)
     {
-        const int64_t nct = sf_col_tiles(O, 16);
+        const int64_t nct = nct_col;
         const int nb = (int)(nrows / 16);
-        uint8_t* sbase = s_col + g * host_scale_bytes_dev(H, O, 16);
         for (int c = threadIdx.x; c < W2_COLS; c += 128) {
             const int64_t hc = h0 + c;
             if (hc >= H) continue;

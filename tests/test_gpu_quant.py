@@ -384,7 +384,10 @@ def test_rht16(mx, orc, shape):
 # ------------------------------------------------------------------------------------------------
 # NVFP4 2D weights
 # ------------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("G,O,H", [(3, 48, 80), (2, 256, 512), (1, 1536, 2048), (2, 2048, 768), (1, 16, 16)])
+# (208, 384): full 64 x 128 tiles whose 32-byte transposed-code runs start 8 bytes off a 16-byte boundary
+# (O / 2 = 104), plus a 16-row remainder tile; (48, 80) and (16, 16): partial tiles only
+@pytest.mark.parametrize("G,O,H", [(3, 48, 80), (2, 256, 512), (1, 1536, 2048), (2, 2048, 768), (1, 16, 16),
+                                   (2, 208, 384)])
 def test_nvfp4_weight_2d(mx, orc, G, O, H):
     w = synthetic.random_bf16(G * O + H, (G, O, H), "normal", 0.02)
     w[0, 0, :16] = 0x7F7F if O * H < 10000 else w[0, 0, :16]
