@@ -12,6 +12,21 @@ namespace mxk {
 
 namespace {
 
+// A thread's 16 BF16 outputs (32 bytes): one 256-bit store when the address is 32-byte aligned (every
+// output row starts on a 32-byte boundary when K % 16 == 0 and y is), so that a warp's store fills
+// 1 KB of whole lines in one instruction; two 16-byte stores otherwise.
+__device__ __forceinline__ void store_bf16x16(uint16_t* dst, const uint32_t (&out)[8]) {
+    if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+        asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                     :: "l"(dst), "r"(out[0]), "r"(out[1]), "r"(out[2]), "r"(out[3]), "r"(out[4]), "r"(out[5]),
+                        "r"(out[6]), "r"(out[7]) : "memory");
+    } else {
+        uint4* d = reinterpret_cast<uint4*>(dst);
+        __stcs(d, make_uint4(out[0], out[1], out[2], out[3]));
+        __stcs(d + 1, make_uint4(out[4], out[5], out[6], out[7]));
+    }
+}
+
 // MXFP8: thread = 16 codes (one uint4) -> 16 BF16 (two uint4).  Idx is the type of the thread index and
 // of its split into (row, column): 32-bit whenever the tensor has fewer than 2^32 such threads, since a
 // 64-bit division costs several times the rest of the thread's work.
@@ -38,9 +53,7 @@ dequant_mxfp8_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ 
         out[2 * i] = pack_bf16x2(a0, a1);
         out[2 * i + 1] = pack_bf16x2(a2, a3);
     }
-    uint4* dst = reinterpret_cast<uint4*>(y + r * K + k0);
-    __stcs(dst, make_uint4(out[0], out[1], out[2], out[3]));
-    __stcs(dst + 1, make_uint4(out[4], out[5], out[6], out[7]));
+    store_bf16x16(y + r * K + k0, out);
 }
 
 // NVFP4: thread = one 16-block (8 code bytes) -> 16 BF16 (Idx as above).
@@ -68,9 +81,7 @@ dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ 
             out[4 * i + j] = pack_bf16x2(__fmul_rn(__fmul_rn(v0, bs), S), __fmul_rn(__fmul_rn(v1, bs), S));
         }
     }
-    uint4* dst = reinterpret_cast<uint4*>(y + r * K + b * 16);
-    __stcs(dst, make_uint4(out[0], out[1], out[2], out[3]));
-    __stcs(dst + 1, make_uint4(out[4], out[5], out[6], out[7]));
+    store_bf16x16(y + r * K + b * 16, out);
 }
 
 // The same for groups of `group_rows` rows sharing one second-level scale, also writing each group's
@@ -111,9 +122,7 @@ dequant_nvfp4_amax_kernel(const uint8_t* __restrict__ q, const uint8_t* __restri
             }
         }
         m = fold_halves(m2);
-        uint4* dst = reinterpret_cast<uint4*>(y + r * K + b * 16);
-        __stcs(dst, make_uint4(out[0], out[1], out[2], out[3]));
-        __stcs(dst + 1, make_uint4(out[4], out[5], out[6], out[7]));
+        store_bf16x16(y + r * K + b * 16, out);
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t g0 = __shfl_sync(0xFFFFFFFFu, g, 0);

@@ -412,27 +412,37 @@ def test_nvfp4_weight_2d(mx, orc, G, O, H):
 # ------------------------------------------------------------------------------------------------
 # Dequantize (fed the oracle's codes, so it is checked independently of the GPU quantizers)
 # ------------------------------------------------------------------------------------------------
+def output_at(shape, offset_elems):
+    """A BF16 output whose first element sits offset_elems past a fresh (256-byte aligned) allocation."""
+    n = shape[0] * shape[1]
+    return torch.empty(n + 16, dtype=torch.bfloat16, device=DEV)[offset_elems:offset_elems + n].view(shape)
+
+
+# offset 8 elements: a 16-byte but not 32-byte aligned output, written with two 16-byte stores per
+# block instead of one 32-byte store
+@pytest.mark.parametrize("offset", [0, 8])
 @pytest.mark.parametrize("shape", [(256, 1024), (130, 96)])
-def test_dequant_mxfp8(mx, orc, shape):
+def test_dequant_mxfp8(mx, orc, shape, offset):
     R, K = shape
     x = edge_tensor(R + K, shape)
     q, s = orc.mxfp8_quantize_rowwise(x)
-    y = torch.empty(shape, dtype=torch.bfloat16, device=DEV)
+    y = output_at(shape, offset)
     mx.mx_dequantize_bf16(mx.MX_FMT_MXFP8, torch.from_numpy(q).to(DEV),
                           torch.from_numpy(orc.scales_to_gemm_layout(s)).to(DEV), None, 0, R, K, y)
     ref = orc.dequant_mxfp8(q, s)
     assert np.array_equal(to_np_u16(y), ref), first_mismatch(to_np_u16(y), ref)
 
 
+@pytest.mark.parametrize("offset", [0, 8])
 @pytest.mark.parametrize("per_row", [True, False])
-def test_dequant_nvfp4(mx, orc, per_row):
+def test_dequant_nvfp4(mx, orc, per_row, offset):
     x = edge_tensor(99, (200, 320))
     if per_row:
         q, s, s2 = orc.nvfp4_quantize_per_token(x)
     else:
         q, s, s2 = orc.nvfp4_quantize_1x16(x, colwise=False)
         s2 = np.array([s2], dtype=np.float32)
-    y = torch.empty((200, 320), dtype=torch.bfloat16, device=DEV)
+    y = output_at((200, 320), offset)
     mx.mx_dequantize_bf16(mx.MX_FMT_NVFP4, torch.from_numpy(q).to(DEV),
                           torch.from_numpy(orc.scales_to_gemm_layout(s)).to(DEV), torch.from_numpy(s2).to(DEV),
                           mx.MX_SCOPE_ROW if per_row else mx.MX_SCOPE_TENSOR, 200, 320, y)
