@@ -19,6 +19,20 @@ __host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return
 // ---------------------------------------------------------------------------------------------
 // BF16 / format conversions
 // ---------------------------------------------------------------------------------------------
+// 32 contiguous bytes written with one 256-bit streaming store when p is 32-byte aligned (a warp's
+// store then covers whole lines in one instruction), two 16-byte stores otherwise.  (The matching
+// 256-bit load made the per-token quantizer slower: 0.081 -> 0.101 ms on 65536 x 2048.)
+__device__ __forceinline__ void stcs_32b(void* p, const uint4& a, const uint4& b) {
+    if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
+        asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                     :: "l"(p), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                     : "memory");
+    } else {
+        __stcs(reinterpret_cast<uint4*>(p), a);
+        __stcs(reinterpret_cast<uint4*>(p) + 1, b);
+    }
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

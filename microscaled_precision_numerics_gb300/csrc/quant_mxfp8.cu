@@ -195,9 +195,8 @@ mxfp8_quantize_kernel(const __grid_constant__ Mx8Params p, int G, const int64_t*
                 am = max(am, a16);
                 const int64_t c = c0 + half * 64 + b * 32;
                 if (r < R && c < K) {
-                    uint4* dst = reinterpret_cast<uint4*>(q_row + r * K + c);
-                    __stcs(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-                    __stcs(dst + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+                    stcs_32b(q_row + r * K + c, make_uint4(codes[0], codes[1], codes[2], codes[3]),
+                             make_uint4(codes[4], codes[5], codes[6], codes[7]));
                 }
             }
             if (p.amax != nullptr) {
