@@ -27,6 +27,23 @@ __device__ __forceinline__ void store_bf16x16(uint16_t* dst, const uint32_t (&ou
     }
 }
 
+// The E4M3 block scale in both halves of an FP16 pair (exact: E4M3 values are FP16 values).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_pair(uint32_t code) {
+    uint32_t h2;
+    asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "r"((code & 0xFFu) * 0x101u));
+    return h2;
+}
+
+// value(q) * value(bs) for two codes: the product has at most 6 significant bits and lies in
+// [2^-10, 2688] (or is zero), so one packed FP16 multiply gives it exactly, and widening to FP32 gives
+// the same two FP32 values as the product taken in FP32.
+__device__ __forceinline__ void nvfp4_pair_value(uint32_t q2, uint32_t bs2, float& v0, float& v1) {
+    uint32_t p2;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(p2) : "r"(q2), "r"(bs2));
+    v0 = __half2float(__ushort_as_half((unsigned short)(p2 & 0xFFFFu)));
+    v1 = __half2float(__ushort_as_half((unsigned short)(p2 >> 16)));
+}
+
 // MXFP8: thread = 16 codes (one uint4) -> 16 BF16 (two uint4).  Idx is the type of the thread index and
 // of its split into (row, column): 32-bit whenever the tensor has fewer than 2^32 such threads, since a
 // 64-bit division costs several times the rest of the thread's work.
@@ -67,7 +84,7 @@ dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ 
     const Idx r_ = gid / per_row_blk;
     const int64_t r = (int64_t)r_, b = (int64_t)(gid - r_ * per_row_blk);
     const float S = rows_per_scale > 0 ? __ldg(s2 + (int64_t)(r_ / (Idx)rows_per_scale)) : __ldg(s2);
-    const float bs = e4m3_to_f32(__ldg(s + sf_offset(r, b, sf_col_tiles(K, 16))));
+    const uint32_t bs2 = e4m3_to_f16x2_pair(__ldg(s + sf_offset(r, b, sf_col_tiles(K, 16))));
     const uint2 c = __ldcs(reinterpret_cast<const uint2*>(q + r * (K / 2) + b * 8));
     const uint32_t cw[2] = {c.x, c.y};
     uint32_t out[8];
@@ -75,10 +92,9 @@ dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ 
     for (int i = 0; i < 2; ++i) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t h2 = e2m1x2_to_f16x2((cw[i] >> (8 * j)) & 0xFFu);
-            const float v0 = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
-            const float v1 = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
-            out[4 * i + j] = pack_bf16x2(__fmul_rn(__fmul_rn(v0, bs), S), __fmul_rn(__fmul_rn(v1, bs), S));
+            float v0, v1;
+            nvfp4_pair_value(e2m1x2_to_f16x2((cw[i] >> (8 * j)) & 0xFFu), bs2, v0, v1);
+            out[4 * i + j] = pack_bf16x2(__fmul_rn(v0, S), __fmul_rn(v1, S));
         }
     }
     store_bf16x16(y + r * K + b * 16, out);
@@ -106,7 +122,7 @@ dequant_nvfp4_amax_kernel(const uint8_t* __restrict__ q, const uint8_t* __restri
         const int64_t r = (int64_t)r_, b = (int64_t)(gid - r_ * per_row_blk);
         g = (int64_t)(r_ / (Idx)group_rows);
         const float S = __ldg(s2 + g);
-        const float bs = e4m3_to_f32(__ldg(s + sf_offset(r, b, sf_col_tiles(K, 16))));
+        const uint32_t bs2 = e4m3_to_f16x2_pair(__ldg(s + sf_offset(r, b, sf_col_tiles(K, 16))));
         const uint2 c = __ldcs(reinterpret_cast<const uint2*>(q + r * (K / 2) + b * 8));
         const uint32_t cw[2] = {c.x, c.y};
         uint32_t out[8], m2 = 0;
@@ -114,10 +130,9 @@ dequant_nvfp4_amax_kernel(const uint8_t* __restrict__ q, const uint8_t* __restri
         for (int i = 0; i < 2; ++i) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint32_t h2 = e2m1x2_to_f16x2((cw[i] >> (8 * j)) & 0xFFu);
-                const float v0 = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
-                const float v1 = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
-                out[4 * i + j] = pack_bf16x2(__fmul_rn(__fmul_rn(v0, bs), S), __fmul_rn(__fmul_rn(v1, bs), S));
+                float v0, v1;
+                nvfp4_pair_value(e2m1x2_to_f16x2((cw[i] >> (8 * j)) & 0xFFu), bs2, v0, v1);
+                out[4 * i + j] = pack_bf16x2(__fmul_rn(v0, S), __fmul_rn(v1, S));
                 m2 = absmax_bf16x2(m2, out[4 * i + j]);
             }
         }

@@ -60,6 +60,23 @@ def test_mxfp8_row_and_col(mx, orc, shape):
     assert np.array_equal(to_np(out["s_col"]), orc.scales_to_gemm_layout(sc))
 
 
+def test_mxfp8_row_codes_16_byte_aligned_output(mx, orc):
+    """Row-wise codes into a buffer that is 16-byte but not 32-byte aligned: the row pass then writes
+    each thread's 32 code bytes as two 16-byte stores instead of one 32-byte store."""
+    R, K = 384, 416
+    x = edge_tensor(R * 5 + K, (R, K))
+    out = mx.alloc_mxfp8(R, K, DEV)
+    q_row = torch.full((R * K + 32,), 0xAB, dtype=torch.uint8, device=DEV)[16:16 + R * K].view(R, K)
+    assert q_row.data_ptr() % 32 == 16
+    mx.mx_quantize_mxfp8(bf16_dev(x), q_row=q_row, s_row=out["s_row"], q_col=out["q_col"], s_col=out["s_col"])
+    torch.cuda.synchronize()
+    qr, sr = orc.mxfp8_quantize_rowwise(x)
+    qc, _ = orc.mxfp8_quantize_colwise(x)
+    assert np.array_equal(to_np(q_row), qr), first_mismatch(to_np(q_row), qr)
+    assert np.array_equal(to_np(out["s_row"]), orc.scales_to_gemm_layout(sr))
+    assert np.array_equal(to_np(out["q_col"]), qc)
+
+
 @pytest.mark.parametrize("which", ["both", "row", "col"])
 def test_mxfp8_batched(mx, orc, which):
     """One launch over tensors of different shapes (ragged tiles, one strided) gives each tensor exactly the
