@@ -44,17 +44,27 @@ __device__ __forceinline__ void nvfp4_pair_value(uint32_t q2, uint32_t bs2, floa
     v1 = __half2float(__ushort_as_half((unsigned short)(p2 >> 16)));
 }
 
+// n / d for the thread-index splits: with 32-bit indices by multiply-high (dv = make_divu32(d); a
+// division instruction sequence costs as much as a third of a dequantize thread's work), with 64-bit
+// ones plainly.
+template <typename Idx>
+__device__ __forceinline__ Idx idx_div(Idx n, Idx d, DivU32 dv) {
+    if constexpr (sizeof(Idx) == 4) return (Idx)divu32((uint32_t)n, dv);
+    else return n / d;
+}
+
 // MXFP8: thread = 16 codes (one uint4) -> 16 BF16 (two uint4).  Idx is the type of the thread index and
 // of its split into (row, column): 32-bit whenever the tensor has fewer than 2^32 such threads, since a
 // 64-bit division costs several times the rest of the thread's work.
 template <typename Idx>
 __global__ void __launch_bounds__(256)
 dequant_mxfp8_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t R, int64_t K,
-                     uint16_t* __restrict__ y) {
+                     uint16_t* __restrict__ y, DivU32 dv_row) {
     const Idx per_row = (Idx)(K / 16);
     const Idx gid = (Idx)blockIdx.x * (Idx)blockDim.x + (Idx)threadIdx.x;
     if ((int64_t)gid >= R * (int64_t)per_row) return;
-    const int64_t r = (int64_t)(gid / per_row), k0 = (int64_t)(gid % per_row) * 16;
+    const Idx r_ = idx_div<Idx>(gid, per_row, dv_row);
+    const int64_t r = (int64_t)r_, k0 = (int64_t)(gid - r_ * per_row) * 16;
     const uint32_t sc = __ldg(s + sf_offset(r, k0 / 32, sf_col_tiles(K, 32)));
     // 2^(sc - 127) as FP32; sc = 0 gives the subnormal 2^-127
     const float f = sc == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(sc << 23);
@@ -77,13 +87,14 @@ dequant_mxfp8_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ 
 template <typename Idx>
 __global__ void __launch_bounds__(256)
 dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, const float* __restrict__ s2,
-                     int64_t rows_per_scale, int64_t R, int64_t K, uint16_t* __restrict__ y) {
+                     int64_t rows_per_scale, int64_t R, int64_t K, uint16_t* __restrict__ y, DivU32 dv_row,
+                     DivU32 dv_scale) {
     const Idx per_row_blk = (Idx)(K / 16);
     const Idx gid = (Idx)blockIdx.x * (Idx)blockDim.x + (Idx)threadIdx.x;
     if ((int64_t)gid >= R * (int64_t)per_row_blk) return;
-    const Idx r_ = gid / per_row_blk;
+    const Idx r_ = idx_div<Idx>(gid, per_row_blk, dv_row);
     const int64_t r = (int64_t)r_, b = (int64_t)(gid - r_ * per_row_blk);
-    const float S = rows_per_scale > 0 ? __ldg(s2 + (int64_t)(r_ / (Idx)rows_per_scale)) : __ldg(s2);
+    const float S = rows_per_scale > 0 ? __ldg(s2 + (int64_t)idx_div<Idx>(r_, (Idx)rows_per_scale, dv_scale)) : __ldg(s2);
     const uint32_t bs2 = e4m3_to_f16x2_pair(__ldg(s + sf_offset(r, b, sf_col_tiles(K, 16))));
     const uint2 c = __ldcs(reinterpret_cast<const uint2*>(q + r * (K / 2) + b * 8));
     const uint32_t cw[2] = {c.x, c.y};
@@ -108,7 +119,7 @@ template <typename Idx>
 __global__ void __launch_bounds__(256)
 dequant_nvfp4_amax_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, const float* __restrict__ s2,
                           int64_t group_rows, int64_t R, int64_t K, uint16_t* __restrict__ y,
-                          uint32_t* __restrict__ amax) {
+                          uint32_t* __restrict__ amax, DivU32 dv_row, DivU32 dv_group) {
     __shared__ uint32_t w_max[8];
     __shared__ int64_t w_grp[8];                                     // -1: nothing left for the CTA to add
     const Idx per_row_blk = (Idx)(K / 16);
@@ -118,9 +129,9 @@ dequant_nvfp4_amax_kernel(const uint8_t* __restrict__ q, const uint8_t* __restri
     uint32_t m = 0;
     int64_t g = 0;
     if (valid) {
-        const Idx r_ = gid / per_row_blk;
+        const Idx r_ = idx_div<Idx>(gid, per_row_blk, dv_row);
         const int64_t r = (int64_t)r_, b = (int64_t)(gid - r_ * per_row_blk);
-        g = (int64_t)(r_ / (Idx)group_rows);
+        g = (int64_t)idx_div<Idx>(r_, (Idx)group_rows, dv_group);
         const float S = __ldg(s2 + g);
         const uint32_t bs2 = e4m3_to_f16x2_pair(__ldg(s + sf_offset(r, b, sf_col_tiles(K, 16))));
         const uint2 c = __ldcs(reinterpret_cast<const uint2*>(q + r * (K / 2) + b * 8));
@@ -213,12 +224,14 @@ cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const fl
     const int64_t threads = R * (K / 16);
     const unsigned blocks = (unsigned)((threads + 255) / 256);
     const bool idx32 = threads + 256 <= (int64_t)UINT32_MAX;       // every thread index fits 32 bits
+    const DivU32 dv_row = make_divu32((uint64_t)(K / 16));
+    const DivU32 dv_scale = make_divu32(rows_per_scale > 0 ? (uint64_t)rows_per_scale : 1u);
     if (fmt == 0) {
-        if (idx32) dequant_mxfp8_kernel<uint32_t><<<blocks, 256, 0, stream>>>(q, s, R, K, y);
-        else dequant_mxfp8_kernel<int64_t><<<blocks, 256, 0, stream>>>(q, s, R, K, y);
+        if (idx32) dequant_mxfp8_kernel<uint32_t><<<blocks, 256, 0, stream>>>(q, s, R, K, y, dv_row);
+        else dequant_mxfp8_kernel<int64_t><<<blocks, 256, 0, stream>>>(q, s, R, K, y, dv_row);
     } else {
-        if (idx32) dequant_nvfp4_kernel<uint32_t><<<blocks, 256, 0, stream>>>(q, s, s2, rows_per_scale, R, K, y);
-        else dequant_nvfp4_kernel<int64_t><<<blocks, 256, 0, stream>>>(q, s, s2, rows_per_scale, R, K, y);
+        if (idx32) dequant_nvfp4_kernel<uint32_t><<<blocks, 256, 0, stream>>>(q, s, s2, rows_per_scale, R, K, y, dv_row, dv_scale);
+        else dequant_nvfp4_kernel<int64_t><<<blocks, 256, 0, stream>>>(q, s, s2, rows_per_scale, R, K, y, dv_row, dv_scale);
     }
     return cudaGetLastError();
 }
@@ -229,10 +242,11 @@ cudaError_t launch_dequant_nvfp4_amax(const uint8_t* q, const uint8_t* s, const 
     if (e != cudaSuccess) return e;
     const int64_t threads = R * (K / 16);
     const unsigned blocks = (unsigned)((threads + 255) / 256);
+    const DivU32 dv_row = make_divu32((uint64_t)(K / 16)), dv_group = make_divu32((uint64_t)group_rows);
     if (threads + 256 <= (int64_t)UINT32_MAX)
-        dequant_nvfp4_amax_kernel<uint32_t><<<blocks, 256, 0, stream>>>(q, s, s2, group_rows, R, K, y, amax);
+        dequant_nvfp4_amax_kernel<uint32_t><<<blocks, 256, 0, stream>>>(q, s, s2, group_rows, R, K, y, amax, dv_row, dv_group);
     else
-        dequant_nvfp4_amax_kernel<int64_t><<<blocks, 256, 0, stream>>>(q, s, s2, group_rows, R, K, y, amax);
+        dequant_nvfp4_amax_kernel<int64_t><<<blocks, 256, 0, stream>>>(q, s, s2, group_rows, R, K, y, amax, dv_row, dv_group);
     return cudaGetLastError();
 }
 

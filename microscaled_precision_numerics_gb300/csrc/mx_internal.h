@@ -9,6 +9,24 @@
 
 namespace mxk {
 
+// Division of an unsigned 32-bit n by an invariant d >= 1 with one multiply-high, after Granlund and
+// Montgomery, "Division by invariant integers using multiplication" (PLDI 1994), section 4:
+// l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1, and q = (t + ((n - t) >> s1)) >> s2 with
+// t = mulhi(m, n), s1 = min(l, 1), s2 = max(l - 1, 0); exact for every n < 2^32.
+struct DivU32 {
+    uint32_t m, s1, s2;
+};
+inline DivU32 make_divu32(uint64_t d) {
+    uint32_t l = 0;
+    while (l < 32 && (1ull << l) < d) ++l;
+    const uint64_t m = (((1ull << l) - d) << 32) / d + 1;
+    return DivU32{(uint32_t)m, l > 0 ? 1u : 0u, l > 0 ? l - 1 : 0u};
+}
+__device__ __forceinline__ uint32_t divu32(uint32_t n, DivU32 d) {
+    const uint32_t t = __umulhi(n, d.m);
+    return (t + ((n - t) >> d.s1)) >> d.s2;
+}
+
 // One-time setup per device: kernel attributes (and the occupancy read after them) belong to each
 // device's context, so a process that drives several GPUs sets them once on every device.  The first
 // call with a device current runs f(value), which returns a CUDA status and may store one integer.
